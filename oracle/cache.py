@@ -1,0 +1,220 @@
+"""Whole-cache assembly on top of the C oracle -- TEST INFRASTRUCTURE ONLY.
+
+Builds, for a workload and raw K/V, the bytes every cache buffer must hold
+(packed records, scale/offset, key channel mean, 16-bit sink and recent
+regions) and the fp64 decode-attention output.  The per-token arithmetic is
+the C code in ``affine.c``/``format.c``; this module only loops over units and
+tokens and places results at the addresses the format specifies.
+
+Token regions ("KVQuant-NUQ" page, Attention Sink-Aware quantization; "D-Quant"
+page, Sec. 5.1 implementation details: the most recent 128 tokens in BF16):
+  * tokens t < n_sink are kept exact in 16-bit (raw slot t);
+  * every token t >= n_sink is quantized into quantized slot t - n_sink;
+  * the latest n_recent tokens are also kept exact in 16-bit, in raw slot
+    n_sink + (t mod n_recent); attention at length S reads them raw and reads
+    the quantized slots only for tokens in [n_sink, S - n_recent).
+  * the key channel mean is taken at prefill over [n_sink, S - n_recent).
+"""
+from __future__ import annotations
+
+import ctypes as C
+from dataclasses import dataclass
+
+import numpy as np
+
+import workloads as W
+
+from . import lib, pack_k_row, pack_v_token
+
+_ROT = {"none": 0, "hadamard": 1, "dense": 2}
+
+
+def _f32_input(bits: np.ndarray, dtype: str) -> np.ndarray:
+    return np.ascontiguousarray(W.bits_to_f32(bits, dtype), dtype=np.float32)
+
+
+def raw16_bits(bits: np.ndarray, dtype: str) -> np.ndarray:
+    """What a raw region stores: the 16-bit input as is; fp32 input as binary16."""
+    if dtype in ("f16", "bf16"):
+        return np.asarray(bits, dtype=np.uint16)
+    from . import f32_to_f16_bits
+    return f32_to_f16_bits(np.asarray(bits, dtype=np.float32)).reshape(np.shape(bits))
+
+
+def raw16_to_f64(bits16: np.ndarray, dtype: str) -> np.ndarray:
+    if dtype == "bf16":
+        return W.bf16_bits_to_f32(bits16).astype(np.float64)
+    return np.asarray(bits16, dtype=np.uint16).view(np.float16).astype(np.float64)
+
+
+def raw_dtype(dtype: str) -> str:
+    return "bf16" if dtype == "bf16" else "f16"
+
+
+@dataclass
+class QuantTensor:
+    """Oracle result for one tensor (K or V) of the whole cache."""
+    codes: np.ndarray     # [B, H, Sq, d] uint8, natural channel order
+    s: np.ndarray         # [B, H, Sq] float32 stored scale (after fp16 rounding if any)
+    o: np.ndarray         # [B, H, Sq] float32 stored offset
+    mu: np.ndarray        # [B, H, d] float32 (zeros when no mean)
+    xhat: np.ndarray      # [B, H, Sq, d] float32 dequantized, rotated space (+mu)
+
+
+def quantize_tensor(w: W.Workload, x_bits: np.ndarray, is_key: bool, S: int,
+                    T: np.ndarray | None = None, mu_frozen: np.ndarray | None = None,
+                    pos0: int = 0) -> QuantTensor:
+    """Quantize tokens [max(pos0, n_sink), pos0 + n) of x_bits [B,H,n,d].
+
+    pos0 == 0 is a prefill: the key mean is computed over [n_sink, S - n_recent).
+    pos0 > 0 appends with the frozen mean ``mu_frozen``.
+    """
+    L = lib()
+    B, H, n, d = x_bits.shape
+    x = _f32_input(x_bits, w.kv_dtype)
+    bits = w.bits
+    rot = _ROT[w.rot_k if is_key else w.rot_v]
+    mean = bool(w.mean_k) and is_key
+    meta_f16 = 1 if w.meta_dtype == "f16" else 0
+    q_t0 = max(0, w.n_sink - pos0)
+    nq = n - q_t0
+    codes = np.zeros((B, H, nq, d), dtype=np.uint8)
+    s = np.zeros((B, H, nq), dtype=np.float32)
+    o = np.zeros((B, H, nq), dtype=np.float32)
+    xhat = np.zeros((B, H, nq, d), dtype=np.float32)
+    mu = np.zeros((B, H, d), dtype=np.float32)
+    for b in range(B):
+        for h in range(H):
+            xu = np.ascontiguousarray(x[b, h])
+            Tp = None
+            if rot == 2:
+                Tu = np.ascontiguousarray(T[h], dtype=np.float32)
+                Tp = Tu.ctypes.data_as(C.c_void_p)
+            mode = 0
+            mu_u = np.zeros(d, dtype=np.float32)
+            if mean:
+                if pos0 == 0:
+                    mode = 1
+                else:
+                    mode = 2
+                    mu_u[:] = mu_frozen[b, h]
+            m_t0 = w.n_sink - pos0
+            m_t1 = S - w.n_recent - pos0
+            m_t0, m_t1 = max(0, m_t0), max(0, m_t1)
+            if m_t1 < m_t0:
+                m_t1 = m_t0
+            cu = np.zeros((nq, d), dtype=np.uint8)
+            su = np.zeros(nq, dtype=np.float32)
+            ou = np.zeros(nq, dtype=np.float32)
+            xh = np.zeros((nq, d), dtype=np.float32)
+            L.or_quantize_unit(xu, n, d, rot, Tp, mode, m_t0, m_t1, mu_u, bits, meta_f16,
+                               float(w.clip), q_t0, cu, su, ou, xh.ctypes.data_as(C.c_void_p))
+            codes[b, h], s[b, h], o[b, h], xhat[b, h], mu[b, h] = cu, su, ou, xh, mu_u
+    return QuantTensor(codes, s, o, mu, xhat)
+
+
+def pack_k(codes: np.ndarray, bits: int) -> np.ndarray:
+    """[..., n, d] codes -> [..., n, row_bytes] key records."""
+    lead = codes.shape[:-1]
+    flat = codes.reshape(-1, codes.shape[-1])
+    rows = np.stack([pack_k_row(c, bits) for c in flat]) if len(flat) else np.zeros((0, 1), np.uint8)
+    return rows.reshape(*lead, -1)
+
+
+def pack_v(codes: np.ndarray, bits: int) -> np.ndarray:
+    """[B, H, n, d] codes -> [B, H, ceil(n/2), pair_bytes] value pair records.
+    The second half of a trailing odd pair is left zero."""
+    B, H, n, d = codes.shape
+    pb = lib().or_v_pair_bytes(d, bits)
+    out = np.zeros((B, H, (n + 1) // 2, pb), dtype=np.uint8)
+    for b in range(B):
+        for h in range(H):
+            for t in range(n):
+                rec = out[b, h, t // 2]
+                pack_v_token(codes[b, h, t], bits, t & 1, rec)
+    return out
+
+
+def meta_f16_bits(s: np.ndarray, o: np.ndarray) -> np.ndarray:
+    """[..., n] scale/offset (already binary16 values) -> [..., n, 2] uint16 bits."""
+    return np.stack([s.astype(np.float16).view(np.uint16), o.astype(np.float16).view(np.uint16)], -1)
+
+
+def raw_regions(w: W.Workload, x_bits: np.ndarray, S: int, pos0: int = 0):
+    """Raw slots written by tokens [pos0, pos0+n): returns {slot: bits16[B,H,d]}.
+    Only tokens that are sinks or among the last n_recent of length S are kept."""
+    B, H, n, d = x_bits.shape
+    r16 = raw16_bits(x_bits, w.kv_dtype)
+    out = {}
+    for i in range(n):
+        t = pos0 + i
+        if t < w.n_sink:
+            out[t] = r16[:, :, i]
+        elif w.n_recent > 0 and t >= S - w.n_recent:
+            out[w.n_sink + (t % w.n_recent)] = r16[:, :, i]
+    return out
+
+
+def attention(w: W.Workload, q: np.ndarray, k_bits: np.ndarray, v_bits: np.ndarray, S: int,
+              qk: QuantTensor, qv: QuantTensor, sm_scale: float | None = None,
+              q_comp: np.ndarray | None = None, units=None) -> np.ndarray:
+    """fp64 decode attention over a cache of length S.
+
+    q [B,Hq,d] fp32.  k_bits/v_bits [B,Hkv,S,d] are the raw tokens (used as stored
+    in the 16-bit regions).  qk/qv hold the quantized tokens [n_sink, S).  Quantized
+    tokens are dequantized in fp64 from codes and metadata and mapped back to the raw
+    space.  Returns out [B,Hq,d] fp64 (entries of units not listed stay zero).
+    """
+    L = lib()
+    B, Hkv, _, d = k_bits.shape
+    G = w.n_q_heads // w.n_kv_heads
+    if sm_scale is None:
+        sm_scale = 1.0 / np.sqrt(d)
+    ns, nr = w.n_sink, w.n_recent
+    n_s = min(S, ns)
+    q_hi = max(n_s, S - nr)           # quantized tokens [n_s, q_hi)
+    rdt = raw_dtype(w.kv_dtype)
+    out = np.zeros((B, w.n_q_heads, d), dtype=np.float64)
+    if units is None:
+        units = [(b, h) for b in range(B) for h in range(Hkv)]
+    for (b, h) in units:
+        K = np.zeros((S, d), dtype=np.float64)
+        V = np.zeros((S, d), dtype=np.float64)
+        # 16-bit regions, as stored
+        kr = raw16_to_f64(raw16_bits(k_bits[b, h, :S], w.kv_dtype), rdt)
+        vr = raw16_to_f64(raw16_bits(v_bits[b, h, :S], w.kv_dtype), rdt)
+        K[:n_s], V[:n_s] = kr[:n_s], vr[:n_s]
+        K[q_hi:S], V[q_hi:S] = kr[q_hi:S], vr[q_hi:S]
+        nq = q_hi - n_s
+        if nq > 0:
+            for X, qt, key in ((K, qk, True), (V, qv, False)):
+                rot = _ROT[w.rot_k if key else w.rot_v]
+                cu = np.ascontiguousarray(qt.codes[b, h, :nq])
+                su = np.ascontiguousarray(qt.s[b, h, :nq])
+                ou = np.ascontiguousarray(qt.o[b, h, :nq])
+                mu_p = None
+                if key and w.mean_k:
+                    mu_u = np.ascontiguousarray(qt.mu[b, h])
+                    mu_p = mu_u.ctypes.data_as(C.c_void_p)
+                deq = np.zeros((nq, d), dtype=np.float64)
+                L.or_dequant_f64(cu, su, ou, mu_p, nq, d, 1 if rot == 1 else 0, deq)
+                if rot == 2:
+                    # keys live in the transformed space: q~ = Tinv^T q, so map k back
+                    # with k_raw[j] = sum_i Tinv^T[i][j] k~[i] (fp64 on the fp32 matrix).
+                    deq = deq @ q_comp[h].astype(np.float64)
+                X[n_s:q_hi] = deq
+        qg = q[b, h * G:(h + 1) * G].astype(np.float64)
+        out[b, h * G:(h + 1) * G] = _attn(L, qg, K, V, sm_scale)
+    return out
+
+
+def _attn(L, q, K, V, sm_scale):
+    G, d = q.shape
+    o = np.zeros((G, d), dtype=np.float64)
+    L.or_attention_f64(np.ascontiguousarray(q), np.ascontiguousarray(K), np.ascontiguousarray(V),
+                       G, K.shape[0], d, float(sm_scale), o)
+    return o
+
+
+__all__ = ["QuantTensor", "quantize_tensor", "pack_k", "pack_v", "meta_f16_bits", "raw_regions",
+           "attention", "raw16_bits", "raw16_to_f64", "raw_dtype"]
