@@ -1,0 +1,389 @@
+"""Decode-step benchmark: quantize the new token + GQA decode attention.
+
+One step = dq_quantize_kv of one new token per sequence (rotation, mean,
+grid, codes, packing, 16-bit recent slot) followed by dq_decode_attention over
+the whole cache.  The workload is the Llama-3-8B-shaped decode layer: batch 16,
+32 query / 8 KV heads, head_dim 128, 8192 cached tokens (4 sink + 128 recent
+in bf16, the rest packed), bf16 inputs, seeded synthetic K/V/q.  Each step
+re-appends the token at position 8191, so the cache length stays fixed.
+
+Inputs are larger than L2 in aggregate: steps rotate over several copies of
+the cache (their total exceeds the L2 size), so no step reads the previous
+step's bytes from L2.
+
+Prints ONE JSON line (rank 0).  ``--impl reference`` times the CPU oracle
+instead (the reference arm for this build).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads as W  # noqa: E402
+
+METRIC = "quantized decode-attn tokens/s & achieved HBM GB/s (% of roofline), 2/3/4-bit"
+ATTN_SRC = os.path.join(ROOT, "quantized_decode_attention_gb300", "csrc", "attn.cu")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "attn_traffic.json")
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=400)
+    p.add_argument("--warmup", type=int, default=20)
+    p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--bits", type=int, default=2)
+    p.add_argument("--variants", default="3,4", help="other code widths measured in the same run")
+    p.add_argument("--copies", type=int, default=0, help="cache copies rotated per step (0 = auto)")
+    p.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU baseline sample budget")
+    p.add_argument("--no-cpu", action="store_true")
+    return p.parse_args()
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def algorithmic_bytes(w: W.Workload, bits: int, S: int) -> dict:
+    """Bytes one decode-attention call must move: packed codes, scale/offset,
+    key mean, 16-bit sink/recent slots, q and out."""
+    U, d = w.batch * w.n_kv_heads, w.head_dim
+    n_raw = min(S, w.n_sink) + min(max(S - w.n_sink, 0), w.n_recent)
+    n_q = S - n_raw
+    meta = 2 if w.meta_dtype == "f16" else 4
+    codes = U * n_q * d * bits // 8 * 2
+    metab = U * n_q * 2 * meta * 2
+    mean = U * d * 4 if w.mean_k else 0
+    raw = U * n_raw * d * 2 * 2
+    q = w.batch * w.n_q_heads * d * 4
+    out = w.batch * w.n_q_heads * d * 2
+    total = codes + metab + mean + raw + q + out
+    return {"codes": codes, "meta": metab, "mean": mean, "raw": raw, "q": q, "out": out, "total": total}
+
+
+class Clocks:
+    """Samples SM clocks and throttle reasons with nvidia-smi during the timed region."""
+
+    def __init__(self, index: int):
+        self.index = index
+        self.samples = []
+        self.proc = None
+
+    def __enter__(self):
+        q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+             "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+             "clocks_event_reasons.sw_power_cap")
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={q}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) >= 7:
+                self.samples.append(parts)
+
+    def __exit__(self, *a):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=2)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        sm = [float(s[0]) for s in self.samples if s[0].replace(".", "").isdigit()]
+        mx = [float(s[1]) for s in self.samples if s[1].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for s in self.samples for i in range(4) if s[3 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(self.samples)}
+
+
+def traffic_for(kernel_sha: str, bits: int):
+    try:
+        with open(TRAFFIC_FILE) as f:
+            d = json.load(f)
+        ent = d.get(f"{bits}bit")
+        if ent and ent.get("attn_src_sha") == kernel_sha:
+            return ent.get("bytes_per_launch")
+    except Exception:
+        pass
+    return None
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+
+def setup_caches(w, bits, S, k_dev, v_dev, copies):
+    import torch
+    from quantized_decode_attention_gb300 import KVCache, make_config
+    cfg = make_config(batch=w.batch, n_kv_heads=w.n_kv_heads, n_q_heads=w.n_q_heads, head_dim=w.head_dim,
+                      max_seq=S, kv_dtype=w.kv_dtype, meta_dtype=w.meta_dtype, out_dtype=w.out_dtype, bits=bits,
+                      rot_k=w.rot_k, rot_v=w.rot_v, mean_k=w.mean_k, n_sink=w.n_sink, n_recent=w.n_recent)
+    base = KVCache.allocate(cfg, zero=False)
+    base.quantize(k_dev, v_dev, pos0=0)
+    base.check()
+    caches = [base]
+    for _ in range(copies - 1):
+        caches.append(base.clone_shared())
+    torch.cuda.synchronize()
+    return caches
+
+
+def run_gpu(args, w, bits, S, k_dev, v_dev, q_dev, knew_dev, vnew_dev, rank):
+    import torch
+    from quantized_decode_attention_gb300 import load
+    L2 = torch.cuda.get_device_properties(0).L2_cache_size
+    ab = algorithmic_bytes(w, bits, S)
+    per_copy = ab["total"]
+    copies = args.copies or max(3, int(np.ceil(3 * L2 / per_copy)) + 1)
+    caches = setup_caches(w, bits, S, k_dev, v_dev, copies)
+    td = {"bf16": torch.bfloat16, "f16": torch.float16, "f32": torch.float32}[w.out_dtype]
+    out = torch.empty((w.batch, w.n_q_heads, w.head_dim), dtype=td, device="cuda")
+    stream = torch.cuda.Stream()
+    sm_scale = w.head_dim ** -0.5
+    pos = S - 1
+
+    def step(c, s):
+        c.quantize(knew_dev, vnew_dev, pos0=pos, stream=s.cuda_stream)
+        c.attention(q_dev, out, S, sm_scale, stream=s.cuda_stream)
+
+    # CUDA graphs: one per cache copy holding [quantize new token, attention],
+    # and one holding a step on every copy in turn (replayed for the bulk).
+    singles = []
+    with torch.cuda.stream(stream):
+        for c in caches:
+            step(c, stream)  # warm up outside capture
+        stream.synchronize()
+        for c in caches:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                step(c, stream)
+            singles.append(g)
+        macro = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(macro, stream=stream):
+            for c in caches:
+                step(c, stream)
+    nc = len(caches)
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            singles[i % nc].replay()
+        stream.synchronize()
+        if torch.distributed.is_initialized():
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with Clocks(torch.cuda.current_device()) as clk:
+            t0.record(stream)
+            for _ in range(args.steps // nc):
+                macro.replay()
+            for i in range(args.steps % nc):
+                singles[i].replay()
+            t1.record(stream)
+            stream.synchronize()
+        total_ms = t0.elapsed_time(t1)
+        # duration of the attention kernel alone: the stream first sleeps so the
+        # host can enqueue [event, attention, event] triples ahead of the GPU,
+        # which then runs them back to back.
+        n_attn = min(args.steps, 200)
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_attn)]
+        torch.cuda._sleep(int(2e8))
+        for i in range(n_attn):
+            evs[i][0].record(stream)
+            caches[i % nc].attention(q_dev, out, S, sm_scale, stream=stream.cuda_stream)
+            evs[i][1].record(stream)
+        stream.synchronize()
+        attn_ms = [a.elapsed_time(b) for a, b in evs]
+    torch.cuda.synchronize()
+    # e2e: through the public API, host buffers: H2D of q and the new token,
+    # both calls, D2H of the output, every step.
+    q_h = q_dev.cpu().pin_memory()
+    k_h = knew_dev.cpu().pin_memory()
+    v_h = vnew_dev.cpu().pin_memory()
+    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    q_b, k_b, v_b = torch.empty_like(q_dev), torch.empty_like(knew_dev), torch.empty_like(vnew_dev)
+    n_e2e = min(args.steps, 200)
+    with torch.cuda.stream(stream):
+        for i in range(3):
+            caches[i % nc].quantize(k_b, v_b, pos0=pos, stream=stream.cuda_stream)
+        stream.synchronize()
+        e_t0, e_t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        wall0 = time.perf_counter()
+        e_t0.record(stream)
+        for i in range(n_e2e):
+            c = caches[i % nc]
+            q_b.copy_(q_h, non_blocking=True)
+            k_b.copy_(k_h, non_blocking=True)
+            v_b.copy_(v_h, non_blocking=True)
+            c.quantize(k_b, v_b, pos0=pos, stream=stream.cuda_stream)
+            c.attention(q_b, out, S, sm_scale, stream=stream.cuda_stream)
+            out_h.copy_(out, non_blocking=True)
+        e_t1.record(stream)
+        stream.synchronize()
+        wall = time.perf_counter() - wall0
+    e2e_ms = max(e_t0.elapsed_time(e_t1), wall * 1e3)
+    for c in caches:
+        c.check()
+    bytes_h2d = q_h.numel() * q_h.element_size() + k_h.numel() * k_h.element_size() * 2
+    bytes_d2h = out_h.numel() * out_h.element_size()
+    res = {
+        "total_ms": total_ms, "attn_ms": statistics.mean(attn_ms), "attn_ms_median": statistics.median(attn_ms),
+        "clocks": clk.summary(), "copies": nc, "algo": ab,
+        "e2e_tok_s": w.batch * n_e2e / (e2e_ms / 1e3), "h2d": bytes_h2d, "d2h": bytes_d2h,
+    }
+    for c in caches[1:]:
+        c.detach()
+    caches[0].close()
+    return res
+
+
+def cpu_baseline(w, bits, S, budget_s, k, v, q):
+    """The oracle as it stands, timed on this host: quantize one unit's cache and
+    run its fp64 decode attention, for as many units as fit the budget."""
+    import oracle
+    wb = w.with_(bits=bits)
+    oracle.build()
+    units = [(b, h) for b in range(w.batch) for h in range(w.n_kv_heads)]
+    done = 0
+    t0 = time.perf_counter()
+    for (b, h) in units:
+        ku, vu = k[b:b + 1, h:h + 1], v[b:b + 1, h:h + 1]
+        w1 = wb.with_(batch=1, n_kv_heads=1, n_q_heads=w.group)
+        qk = oracle.quantize_tensor(w1, ku, True, S)
+        qv = oracle.quantize_tensor(w1, vu, False, S)
+        oracle.attention(w1, q[b:b + 1, h * w.group:(h + 1) * w.group], ku, vu, S, qk, qv)
+        done += 1
+        if time.perf_counter() - t0 > budget_s:
+            break
+    el = time.perf_counter() - t0
+    per_call = el / done * len(units)
+    return {"value": w.batch / per_call, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": f"{done} of {len(units)} (batch, kv-head) units: oracle quantize of {S} tokens + fp64 "
+                      f"attention for {w.group} heads each, extrapolated to one full call"}
+
+
+def main():
+    args = parse()
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    w = W.LLAMA.with_(bits=args.bits)
+    S = w.seq
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        k, v = W.make_kv(w)
+        q = W.make_q(w)
+        steps = []
+        for i in range(args.warmup + args.steps):
+            r = cpu_baseline(w, args.bits, S, args.cpu_seconds / max(1, args.steps + args.warmup), k, v, q)
+            if i >= args.warmup:
+                steps.append(r["value"])
+        val = statistics.mean(steps)
+        line = {"impl": "reference", "metric": METRIC, "value": val, "unit": "tokens/s", "n_gpus": args.gpus,
+                "steps": args.steps, "warmup": args.warmup, "higher_is_better": True, "dtype": "f64",
+                "data": "synthetic", "config": {"workload": w.name, "batch": w.batch, "seq_len": S, "bits": args.bits},
+                "cpu_baseline": {"value": val, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                                 "sample": "each step: as many (batch, kv-head) units as fit its time share, "
+                                           "extrapolated to a full decode call"},
+                "e2e": {"value": val, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+                "vs_baseline": None}
+        print(json.dumps(line))
+        return
+
+    import torch
+    if world > 1:
+        import torch.distributed as dist
+        local = int(os.environ.get("LOCAL_RANK", "0"))
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    import __graft_entry__
+    __graft_entry__.build()
+    # inputs (seeded), uploaded once; bf16 bit patterns
+    k, v = W.make_kv(w)
+    q = W.make_q(w)
+    kn, vn = W.make_new_token(w)
+    dev16 = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).cuda().view(torch.bfloat16)
+    k_dev, v_dev, q_dev = dev16(k), dev16(v), torch.from_numpy(q).cuda()
+    kn_dev, vn_dev = dev16(kn), dev16(vn)
+    res = run_gpu(args, w, args.bits, S, k_dev, v_dev, q_dev, kn_dev, vn_dev, rank)
+    variants = {}
+    for vb in [int(x) for x in args.variants.split(",") if x.strip()]:
+        if vb == args.bits:
+            continue
+        r = run_gpu(args, w.with_(bits=vb), vb, S, k_dev, v_dev, q_dev, kn_dev, vn_dev, rank)
+        variants[f"{vb}bit"] = r
+    del k_dev, v_dev
+    total_ms = res["total_ms"]
+    if world > 1:
+        t = torch.tensor([total_ms], device="cuda")
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_step = total_ms / args.steps
+    value = w.batch * world / (ms_step / 1e3)
+    peak, peak_kind = peaks()
+    sha = hashlib.sha256(open(ATTN_SRC, "rb").read()).hexdigest()[:16]
+
+    def roof(r, bits):
+        achieved = r["algo"]["total"] / (r["attn_ms"] / 1e3) / 1e9
+        return {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
+                "traffic": traffic_for(sha, bits), "algorithmic_bytes": r["algo"]["total"],
+                "attn_us": round(r["attn_ms"] * 1e3, 2), "attn_us_median": round(r["attn_ms_median"] * 1e3, 2)}
+
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_step, 5), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f16-mma/f32-acc (bf16 in/out)", "data": "synthetic",
+        "config": {"workload": w.name, "batch": w.batch, "q_heads": w.n_q_heads, "kv_heads": w.n_kv_heads,
+                   "head_dim": w.head_dim, "seq_len": S, "bits": args.bits, "n_sink": w.n_sink,
+                   "n_recent": w.n_recent, "parallelism": f"replicas{world}",
+                   "l2": f"{res['copies']} cache copies rotated per step (> L2)",
+                   "step": "quantize 1 new token/seq + decode attention, CUDA graph per step"},
+        "roofline": roof(res, args.bits),
+        "clocks": res["clocks"],
+        "e2e": {"value": round(res["e2e_tok_s"], 1), "unit": "tokens/s", "h2d_bytes_per_step": res["h2d"],
+                "d2h_bytes_per_step": res["d2h"],
+                "how": "eager C-ABI calls per step with pinned-host q/new-token H2D and output D2H"},
+        "gpu_launches": 3 * args.steps,
+        "variants": {k2: {"value": round(w.batch / (r["total_ms"] / args.steps / 1e3), 1),
+                          "ms_per_step": round(r["total_ms"] / args.steps, 5), "roofline": roof(r, int(k2[0])),
+                          "e2e_tok_s": round(r["e2e_tok_s"], 1)} for k2, r in variants.items()},
+    }
+    if rank == 0 and not args.no_cpu:
+        line["cpu_baseline"] = cpu_baseline(w, args.bits, S, args.cpu_seconds, k, v, q)
+    if rank == 0:
+        print(json.dumps(line))
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,204 @@
+/*
+ * dq.h -- C ABI of libdq: quantized KV cache + GQA decode attention on GB300.
+ *
+ * What it computes
+ * ----------------
+ * dq_quantize_kv turns each token's key and value (one vector of head_dim
+ * values per KV head) into a fixed-size record of low-bit codes:
+ *   - an optional normalized Hadamard rotation per head (keys rotated online,
+ *     "D-Quant: Driftable Entropy Coding for KV Cache Quantization", Sec. 4.2),
+ *     or a dense d x d key transform applied after RoPE ("WUSH-KV: KV Cache
+ *     Quantization with Data-Adaptive Transforms", Key Contributions 2);
+ *   - removal of the key channel mean (D-Quant Sec. 4.2), frozen at prefill;
+ *   - a per-token affine grid x^ = o + s*m (D-Quant Sec. 3.1 Eq. (1) and
+ *     Sec. 4.2 Eq. (4)), from min/max or from a two-sided percentile clip
+ *     (WUSH-KV, Methodology: OSCAR-style percentile-clipped affine), with s
+ *     and o rounded to fp16 before the codes are assigned (D-Quant App. A);
+ *   - the first n_sink tokens and the latest n_recent tokens also kept exact
+ *     in 16-bit ("KVQuant-NUQ", Attention Sink-Aware quantization; D-Quant
+ *     Sec. 5.1: the most recent 128 tokens in BF16).
+ * dq_decode_attention computes, for every query head h of every sequence,
+ *   out_h = sum_t softmax_t(sm_scale * q_h . k^_t) v^_t
+ * over the cache of length seq_len, reading the packed codes and applying the
+ * affine terms after the contraction (D-Quant App. A Eq. (7)-(9)).  Query head
+ * h reads KV head floor(h * n_kv_heads / n_q_heads) (grouped-query attention).
+ *
+ * Conventions
+ * -----------
+ * - Every pointer named "device" is CUDA global memory of the current device;
+ *   the caller allocates and owns it.  Nothing here frees caller memory.
+ * - Every buffer must be 16-byte aligned (DQ_EALIGN otherwise).
+ * - Calls enqueue work on `stream` (a cudaStream_t; NULL = legacy default
+ *   stream) and return without synchronizing.  Argument errors are found on
+ *   the host before anything is enqueued and leave all buffers untouched.
+ *   Conditions found on the device (non-finite input) are latched in the
+ *   context and returned by dq_check().
+ * - A context (dq_ctx) is created by the first call that receives a pointer
+ *   to a NULL context; it holds the library's workspace on the device that
+ *   was current then and is bound to that config.  One context must not be
+ *   used from two host threads at once.  Release it with dq_free().
+ * - No function throws, aborts, exits or prints.  dq_last_error() gives a
+ *   thread-local message for the last failing call.
+ */
+#ifndef DQ_H
+#define DQ_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    DQ_OK = 0,
+    DQ_EINVAL = 1,        /* bad argument, size or config */
+    DQ_EALIGN = 2,        /* a buffer is not 16-byte aligned */
+    DQ_EUNSUPPORTED = 3,  /* valid but not implemented combination */
+    DQ_EINFEASIBLE = 4,   /* rANS container cannot hold the cheapest stream */
+    DQ_ENOMEM = 5,        /* workspace allocation failed */
+    DQ_ECUDA = 6,         /* a CUDA runtime call failed */
+    DQ_ENONFINITE = 7,    /* a quantized input value was NaN or infinite */
+    DQ_ETIMEOUT = 8       /* a bounded device wait ran out */
+} dq_status;
+
+typedef enum { DQ_F32 = 0, DQ_F16 = 1, DQ_BF16 = 2 } dq_dtype;
+typedef enum { DQ_AFFINE = 0, DQ_NUQ = 1, DQ_RANS = 2 } dq_scheme;
+typedef enum { DQ_ROT_NONE = 0, DQ_ROT_HADAMARD = 1, DQ_ROT_DENSE = 2 } dq_rot;
+
+/* Quantizer settings of one tensor (keys or values). */
+typedef struct {
+    int scheme;          /* dq_scheme */
+    int bits;            /* affine/NUQ code width: 2, 3 or 4 (3 needs head_dim 128) */
+    int levels;          /* DQ_RANS: alphabet size M */
+    int container_bytes; /* DQ_RANS: record size C */
+    int rot;             /* dq_rot; DQ_ROT_DENSE is keys only */
+    int mean;            /* keys only: 1 = remove the channel mean frozen at prefill */
+    float clip;          /* 0 = min/max grid; kappa in (0.5, 1) = clip to the
+                            (1-kappa, kappa) linear-interpolated quantiles */
+    int lloyd_iters;     /* DQ_NUQ */
+    float outlier_frac;  /* DQ_NUQ */
+} dq_tensor_cfg;
+
+typedef struct {
+    int batch, n_kv_heads, n_q_heads, head_dim, max_seq;
+    int kv_dtype;        /* dq_dtype of the K/V handed to dq_quantize_kv */
+    int meta_dtype;      /* DQ_F16 or DQ_F32: storage of s and o */
+    int out_dtype;       /* dq_dtype of the attention output */
+    dq_tensor_cfg k, v;
+    int n_sink, n_recent;
+    float rans_alpha;    /* DQ_RANS: sharpening exponent */
+    int rans_prob_bits;  /* DQ_RANS: frequency precision p */
+} dq_config;
+
+/*
+ * Cache buffers (device, caller-owned).  dq_kv_sizes() gives the byte size
+ * of each, in field order; a field whose size is 0 is unused and may be NULL.
+ *
+ * U = batch * n_kv_heads units, unit u = b * n_kv_heads + kv_head.
+ * Qcap = round_up(max_seq - n_sink, 16) quantized slots per unit; token
+ * t >= n_sink lives in quantized slot t - n_sink.
+ * Rcap = round_up(n_sink + n_recent, 16) raw slots per unit; token t < n_sink
+ * in raw slot t, the latest n_recent tokens in raw slot n_sink + t % n_recent.
+ *
+ * codes_k  [U][Qcap][Rk]      key records, Rk = head_dim*bits_k/8 bytes
+ * codes_v  [U][Qcap/2][2*Rv]  value records, one per token pair
+ * meta_k   [U][Qcap][2]       (s, o) per token, meta_dtype
+ * meta_v   [U][Qcap][2]
+ * mean_k   [U][head_dim]      fp32 key channel mean (rotated space)
+ * raw_k    [U][Rcap][head_dim]           16-bit keys (kv dtype; fp16 for fp32 input)
+ * raw_v    [U][Rcap/2][head_dim][2]      16-bit values, token pairs interleaved
+ * k_transform [n_kv_heads][head_dim][head_dim] fp32 T (DQ_ROT_DENSE keys)
+ * q_comp      [n_kv_heads][head_dim][head_dim] fp32 T^{-T} (query compensation)
+ *
+ * Bit layout of a record: little-endian 32-bit words; with b = 2 or 4 each
+ * 16-bit half holds 16/b fields of b bits, field f at bits [b*f, b*f+b); with
+ * b = 3 a 2-bit plane (low code bits, laid out as b = 2) is followed by a
+ * 1-bit plane (16 fields per half).  Key channel c of a token goes to
+ *   idx = ((c>>1)&3)*(d/8) + 2*(c>>4) + ((c>>3)&1), half = c&1;
+ * value channel c of token t goes to
+ *   idx = (c&7)*(d/8) + 2*(c>>4) + ((c>>3)&1), half = t&1,
+ * in both cases word idx/F, field idx%F with F = 16/b.
+ */
+typedef struct {
+    void *codes_k, *codes_v, *meta_k, *meta_v, *mean_k;
+    void *lut_k, *lut_v;
+    void *raw_k, *raw_v;
+    void *ol_rowptr_k, *ol_col_k, *ol_val_k, *ol_rowptr_v, *ol_col_v, *ol_val_v;
+    void *k_transform, *q_comp;
+} dq_kv_buffers;
+
+#define DQ_NUM_BUFFERS 17
+
+typedef struct dq_ctx dq_ctx;
+
+/*
+ * Byte size of every dq_kv_buffers field for `cfg`, in field order, into
+ * bytes[DQ_NUM_BUFFERS].  Host only; enqueues nothing.
+ * Errors: DQ_EINVAL (NULL argument or invalid config), DQ_EUNSUPPORTED.
+ */
+dq_status dq_kv_sizes(const dq_config *cfg, size_t bytes[DQ_NUM_BUFFERS]);
+
+/*
+ * Quantize tokens [pos0, pos0 + n_tok) of every sequence into the cache.
+ *   k, v : device, [batch][n_kv_heads][n_tok][head_dim] contiguous, kv_dtype.
+ * pos0 == 0 is a prefill of n_tok tokens: the key channel mean is computed over
+ * tokens [n_sink, n_tok - n_recent) and frozen.  pos0 > 0 appends with the
+ * frozen mean.  Every token t >= n_sink is written to its quantized slot;
+ * sinks and the latest n_recent tokens (of length pos0 + n_tok) also to their
+ * raw slots.  Requires pos0 + n_tok <= max_seq.
+ * The dense key transform reads bufs->k_transform.
+ * Errors: DQ_EINVAL, DQ_EALIGN, DQ_EUNSUPPORTED, DQ_ENOMEM, DQ_ECUDA (launch).
+ */
+dq_status dq_quantize_kv(dq_ctx **ctx, const dq_config *cfg, const dq_kv_buffers *bufs,
+                         const void *k, const void *v, long long pos0, long long n_tok,
+                         void *stream);
+
+/*
+ * Decode attention over the first seq_len tokens of every sequence.
+ *   q   : device, [batch][n_q_heads][head_dim] fp32
+ *   out : device, [batch][n_q_heads][head_dim] out_dtype
+ * Requires 1 <= seq_len <= max_seq and that every token < seq_len was
+ * quantized; with n_recent > 0, seq_len must be the length after the last
+ * dq_quantize_kv call (the recent slots hold that call's latest tokens).  sm_scale multiplies q.k (1/sqrt(head_dim) is usual).  Dense key
+ * transforms read bufs->q_comp to form T^{-T} q.
+ * Uses the context's workspace for split partials; concurrent calls on one
+ * context must be ordered on a stream.
+ * Errors: DQ_EINVAL, DQ_EALIGN, DQ_EUNSUPPORTED, DQ_ENOMEM, DQ_ECUDA.
+ */
+dq_status dq_decode_attention(dq_ctx **ctx, const dq_config *cfg, const dq_kv_buffers *bufs,
+                              const void *q, void *out, long long seq_len, float sm_scale,
+                              void *stream);
+
+/*
+ * Test export: write the dequantized fp32 values of quantized slots
+ * [slot0, slot0 + n) of K (which = 0) or V (which = 1) into
+ *   out : device, [batch][n_kv_heads][n][head_dim] fp32
+ * in the quantizer's space (rotated; keys with the channel mean added back):
+ * x^ = fp32(o + fp32(s*m)) (+ mu).
+ * Errors: DQ_EINVAL, DQ_EALIGN, DQ_EUNSUPPORTED, DQ_ENOMEM, DQ_ECUDA.
+ */
+dq_status dq_dequantize_kv(dq_ctx **ctx, const dq_config *cfg, const dq_kv_buffers *bufs,
+                           int which, long long slot0, long long n, float *out, void *stream);
+
+/*
+ * Synchronize `stream`, then return and clear the device-side status latched
+ * by earlier calls on this context (DQ_OK, DQ_ENONFINITE, DQ_ETIMEOUT), or
+ * DQ_ECUDA if the stream reports an error.  ctx may be NULL (returns DQ_OK).
+ */
+dq_status dq_check(dq_ctx *ctx, void *stream);
+
+/* Release a context and its workspace.  NULL-safe.  The caller must make sure
+ * no enqueued work still uses it. */
+void dq_free(dq_ctx *ctx);
+
+/* Thread-local message of the last error returned on this thread ("" if none). */
+const char *dq_last_error(void);
+
+/* Static name of a status code. */
+const char *dq_status_name(dq_status s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DQ_H */

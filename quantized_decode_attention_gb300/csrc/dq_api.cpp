@@ -1,0 +1,360 @@
+// Host side of libdq: validation, buffer sizes, the context, and launches.
+// No exceptions cross the C ABI; errors are returned as dq_status with a
+// thread-local message.
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <new>
+
+#include "dq.h"
+#include "dq_internal.h"
+
+namespace {
+
+thread_local char g_err[512] = "";
+
+dq_status fail(dq_status s, const char *fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    std::vsnprintf(g_err, sizeof g_err, fmt, ap);
+    va_end(ap);
+    return s;
+}
+
+dq_status ok() {
+    g_err[0] = '\0';
+    return DQ_OK;
+}
+
+long long round_up(long long x, long long m) { return (x + m - 1) / m * m; }
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+dq_status validate_tensor(const dq_tensor_cfg &t, int d, bool key, const char *name) {
+    if (t.scheme != DQ_AFFINE) return fail(DQ_EUNSUPPORTED, "%s: only the affine scheme is built", name);
+    if (t.bits < 2 || t.bits > 4) return fail(DQ_EINVAL, "%s: bits must be 2, 3 or 4 (got %d)", name, t.bits);
+    if (t.bits == 3 && d != 128) return fail(DQ_EUNSUPPORTED, "%s: 3-bit records need head_dim 128", name);
+    if (t.rot < DQ_ROT_NONE || t.rot > DQ_ROT_DENSE) return fail(DQ_EINVAL, "%s: bad rotation %d", name, t.rot);
+    if (!key && t.rot == DQ_ROT_DENSE) return fail(DQ_EUNSUPPORTED, "%s: dense transform is for keys", name);
+    if (!key && t.mean) return fail(DQ_EINVAL, "%s: channel mean removal is for keys", name);
+    if (!(t.clip == 0.0f || (t.clip > 0.5f && t.clip < 1.0f)))
+        return fail(DQ_EINVAL, "%s: clip must be 0 or in (0.5, 1)", name);
+    return DQ_OK;
+}
+
+}  // namespace
+
+namespace dq {
+
+dq_status make_layout(const dq_config *cfg, Layout *L) {
+    if (!cfg || !L) return fail(DQ_EINVAL, "NULL argument");
+    const dq_config &c = *cfg;
+    if (c.batch < 1 || c.n_kv_heads < 1 || c.n_q_heads < 1 || c.max_seq < 1)
+        return fail(DQ_EINVAL, "batch, heads and max_seq must be positive");
+    if (c.n_q_heads % c.n_kv_heads) return fail(DQ_EINVAL, "n_q_heads must be a multiple of n_kv_heads");
+    const int G = c.n_q_heads / c.n_kv_heads;
+    if (G > 4) return fail(DQ_EUNSUPPORTED, "at most 4 query heads per KV head (got %d)", G);
+    if (c.head_dim != 64 && c.head_dim != 128) return fail(DQ_EUNSUPPORTED, "head_dim must be 64 or 128");
+    if (c.kv_dtype < DQ_F32 || c.kv_dtype > DQ_BF16 || c.out_dtype < DQ_F32 || c.out_dtype > DQ_BF16)
+        return fail(DQ_EINVAL, "bad dtype");
+    if (c.meta_dtype != DQ_F16 && c.meta_dtype != DQ_F32) return fail(DQ_EINVAL, "meta_dtype must be F16 or F32");
+    if (c.n_sink < 0 || c.n_recent < 0 || c.n_sink > c.max_seq) return fail(DQ_EINVAL, "bad n_sink / n_recent");
+    dq_status s;
+    if ((s = validate_tensor(c.k, c.head_dim, true, "k")) != DQ_OK) return s;
+    if ((s = validate_tensor(c.v, c.head_dim, false, "v")) != DQ_OK) return s;
+    if (c.k.bits != c.v.bits) return fail(DQ_EUNSUPPORTED, "keys and values must use the same code width");
+
+    Layout &l = *L;
+    std::memset(&l, 0, sizeof l);
+    l.B = c.batch;
+    l.Hkv = c.n_kv_heads;
+    l.Hq = c.n_q_heads;
+    l.G = G;
+    l.d = c.head_dim;
+    l.U = c.batch * c.n_kv_heads;
+    l.bits_k = c.k.bits;
+    l.bits_v = c.v.bits;
+    l.rowK = c.head_dim * c.k.bits / 8;
+    l.pairV = 2 * c.head_dim * c.v.bits / 8;
+    l.qcap = round_up(c.max_seq - c.n_sink, 16);
+    l.rcap = static_cast<int>(round_up(c.n_sink + c.n_recent, 16));
+    l.meta_bytes = c.meta_dtype == DQ_F16 ? 2 : 4;
+    l.n_sink = c.n_sink;
+    l.n_recent = c.n_recent;
+    const size_t U = static_cast<size_t>(l.U), d = static_cast<size_t>(l.d);
+    l.sz[0] = U * l.qcap * l.rowK;                          // codes_k
+    l.sz[1] = U * (l.qcap / 2) * l.pairV;                   // codes_v
+    l.sz[2] = U * l.qcap * 2 * l.meta_bytes;                // meta_k
+    l.sz[3] = U * l.qcap * 2 * l.meta_bytes;                // meta_v
+    l.sz[4] = c.k.mean ? U * d * 4 : 0;                     // mean_k
+    l.sz[5] = 0;                                            // lut_k
+    l.sz[6] = 0;                                            // lut_v
+    l.sz[7] = U * l.rcap * d * 2;                           // raw_k
+    l.sz[8] = U * l.rcap * d * 2;                           // raw_v
+    for (int i = 9; i < 15; i++) l.sz[i] = 0;               // outlier side-channels
+    l.sz[15] = c.k.rot == DQ_ROT_DENSE ? static_cast<size_t>(c.n_kv_heads) * d * d * 4 : 0;  // k_transform
+    l.sz[16] = l.sz[15];                                    // q_comp
+    return DQ_OK;
+}
+
+}  // namespace dq
+
+using dq::Layout;
+
+static dq_status check_bufs(const Layout &L, const dq_kv_buffers *b) {
+    const void *const *p = reinterpret_cast<const void *const *>(b);
+    static const char *names[DQ_NUM_BUFFERS] = {"codes_k", "codes_v", "meta_k", "meta_v", "mean_k", "lut_k",
+                                                "lut_v", "raw_k", "raw_v", "ol_rowptr_k", "ol_col_k", "ol_val_k",
+                                                "ol_rowptr_v", "ol_col_v", "ol_val_v", "k_transform", "q_comp"};
+    for (int i = 0; i < DQ_NUM_BUFFERS; i++) {
+        if (L.sz[i] == 0) continue;
+        if (!p[i]) return fail(DQ_EINVAL, "buffer %s is NULL", names[i]);
+        if (!aligned16(p[i])) return fail(DQ_EALIGN, "buffer %s is not 16-byte aligned", names[i]);
+    }
+    return DQ_OK;
+}
+
+static bool same_cfg(const dq_config &a, const dq_config &b) { return std::memcmp(&a, &b, sizeof a) == 0; }
+
+static dq_status get_ctx(dq_ctx **pctx, const dq_config *cfg, const Layout &L) {
+    if (!pctx) return fail(DQ_EINVAL, "ctx pointer is NULL");
+    if (*pctx) {
+        if (!same_cfg((*pctx)->cfg, *cfg)) return fail(DQ_EINVAL, "context was created for a different config");
+        int dev = -1;
+        if (cudaGetDevice(&dev) != cudaSuccess || dev != (*pctx)->device)
+            return fail(DQ_EINVAL, "context belongs to device %d", (*pctx)->device);
+        return DQ_OK;
+    }
+    dq_ctx *c = new (std::nothrow) dq_ctx();
+    if (!c) return fail(DQ_ENOMEM, "host allocation failed");
+    std::memset(c, 0, sizeof *c);
+    c->cfg = *cfg;
+    c->L = L;
+    if (cudaGetDevice(&c->device) != cudaSuccess ||
+        cudaDeviceGetAttribute(&c->num_sms, cudaDevAttrMultiProcessorCount, c->device) != cudaSuccess) {
+        delete c;
+        return fail(DQ_ECUDA, "cannot query the current device");
+    }
+    // split partials: at most (1 + max split) items per unit
+    const long long max_tiles = (L.qcap + 15) / 16;
+    long long max_split = max_tiles < 1 ? 1 : max_tiles;
+    const long long cap_split = 64;
+    if (max_split > cap_split) max_split = cap_split;
+    c->partials_cap = static_cast<size_t>(L.U) * (1 + max_split) * 4 * (L.d + 2);
+    cudaError_t e1 = cudaMalloc(&c->status, sizeof(unsigned));
+    cudaError_t e2 = cudaMalloc(&c->partials, c->partials_cap * sizeof(float));
+    cudaError_t e3 = cudaMalloc(&c->counters, sizeof(int) * L.U);
+    if (e1 != cudaSuccess || e2 != cudaSuccess || e3 != cudaSuccess) {
+        cudaFree(c->status);
+        cudaFree(c->partials);
+        cudaFree(c->counters);
+        delete c;
+        cudaGetLastError();
+        return fail(DQ_ENOMEM, "workspace allocation failed");
+    }
+    if (cudaMemset(c->status, 0, sizeof(unsigned)) != cudaSuccess ||
+        cudaMemset(c->counters, 0, sizeof(int) * L.U) != cudaSuccess) {
+        dq_free(c);
+        return fail(DQ_ECUDA, "workspace initialization failed");
+    }
+    *pctx = c;
+    return DQ_OK;
+}
+
+extern "C" {
+
+const char *dq_last_error(void) { return g_err; }
+
+const char *dq_status_name(dq_status s) {
+    switch (s) {
+        case DQ_OK: return "DQ_OK";
+        case DQ_EINVAL: return "DQ_EINVAL";
+        case DQ_EALIGN: return "DQ_EALIGN";
+        case DQ_EUNSUPPORTED: return "DQ_EUNSUPPORTED";
+        case DQ_EINFEASIBLE: return "DQ_EINFEASIBLE";
+        case DQ_ENOMEM: return "DQ_ENOMEM";
+        case DQ_ECUDA: return "DQ_ECUDA";
+        case DQ_ENONFINITE: return "DQ_ENONFINITE";
+        case DQ_ETIMEOUT: return "DQ_ETIMEOUT";
+    }
+    return "DQ_UNKNOWN";
+}
+
+dq_status dq_kv_sizes(const dq_config *cfg, size_t bytes[DQ_NUM_BUFFERS]) {
+    if (!cfg || !bytes) return fail(DQ_EINVAL, "NULL argument");
+    Layout L;
+    dq_status s = dq::make_layout(cfg, &L);
+    if (s != DQ_OK) return s;
+    for (int i = 0; i < DQ_NUM_BUFFERS; i++) bytes[i] = L.sz[i];
+    return ok();
+}
+
+dq_status dq_quantize_kv(dq_ctx **ctx, const dq_config *cfg, const dq_kv_buffers *bufs, const void *k,
+                         const void *v, long long pos0, long long n_tok, void *stream) {
+    if (!cfg || !bufs || !k || !v) return fail(DQ_EINVAL, "NULL argument");
+    Layout L;
+    dq_status s = dq::make_layout(cfg, &L);
+    if (s != DQ_OK) return s;
+    if (pos0 < 0 || n_tok < 1 || pos0 + n_tok > cfg->max_seq)
+        return fail(DQ_EINVAL, "tokens [%lld, %lld) outside [0, max_seq=%d)", pos0, pos0 + n_tok, cfg->max_seq);
+    if ((s = check_bufs(L, bufs)) != DQ_OK) return s;
+    if (!aligned16(k) || !aligned16(v)) return fail(DQ_EALIGN, "k / v input not 16-byte aligned");
+    if ((s = get_ctx(ctx, cfg, L)) != DQ_OK) return s;
+
+    for (int which = 0; which < 2; which++) {
+        const dq_tensor_cfg &t = which == 0 ? cfg->k : cfg->v;
+        dq::QuantArgs a{};
+        a.x = which == 0 ? k : v;
+        a.in_dtype = cfg->kv_dtype;
+        a.pos0 = pos0;
+        a.n_tok = n_tok;
+        a.seq_after = pos0 + n_tok;
+        a.is_key = which == 0;
+        a.bits = t.bits;
+        a.rot = t.rot;
+        a.use_mean = which == 0 && t.mean;
+        a.meta_f16 = cfg->meta_dtype == DQ_F16;
+        a.clip = t.clip;
+        if (t.clip > 0.0f) {
+            const double plo = (1.0 - static_cast<double>(t.clip)) * (L.d - 1);
+            const double phi = static_cast<double>(t.clip) * (L.d - 1);
+            a.clip_ilo = static_cast<int>(std::floor(plo));
+            a.clip_flo = static_cast<float>(plo - std::floor(plo));
+            a.clip_ihi = static_cast<int>(std::floor(phi));
+            a.clip_fhi = static_cast<float>(phi - std::floor(phi));
+        }
+        a.hscale = static_cast<float>(1.0 / std::sqrt(static_cast<double>(L.d)));
+        a.codes = static_cast<uint8_t *>(which == 0 ? bufs->codes_k : bufs->codes_v);
+        a.meta = which == 0 ? bufs->meta_k : bufs->meta_v;
+        a.mean = which == 0 && t.mean ? static_cast<float *>(bufs->mean_k) : nullptr;
+        a.T = which == 0 && t.rot == DQ_ROT_DENSE ? static_cast<const float *>(bufs->k_transform) : nullptr;
+        a.raw = static_cast<uint16_t *>(which == 0 ? bufs->raw_k : bufs->raw_v);
+        a.status = (*ctx)->status;
+        int e;
+        if (a.use_mean && pos0 == 0) {
+            if ((e = dq::launch_key_mean(L, a, stream)) != 0)
+                return fail(DQ_ECUDA, "key mean launch: %s", cudaGetErrorString(static_cast<cudaError_t>(e)));
+        }
+        if ((e = dq::launch_quantize(L, a, stream)) != 0)
+            return fail(DQ_ECUDA, "quantize launch: %s", cudaGetErrorString(static_cast<cudaError_t>(e)));
+    }
+    return ok();
+}
+
+dq_status dq_decode_attention(dq_ctx **ctx, const dq_config *cfg, const dq_kv_buffers *bufs, const void *q,
+                              void *out, long long seq_len, float sm_scale, void *stream) {
+    if (!cfg || !bufs || !q || !out) return fail(DQ_EINVAL, "NULL argument");
+    Layout L;
+    dq_status s = dq::make_layout(cfg, &L);
+    if (s != DQ_OK) return s;
+    if (seq_len < 1 || seq_len > cfg->max_seq) return fail(DQ_EINVAL, "seq_len %lld outside [1, max_seq]", seq_len);
+    if (!std::isfinite(sm_scale)) return fail(DQ_EINVAL, "sm_scale is not finite");
+    if ((s = check_bufs(L, bufs)) != DQ_OK) return s;
+    if (!aligned16(q) || !aligned16(out)) return fail(DQ_EALIGN, "q / out not 16-byte aligned");
+    if ((s = get_ctx(ctx, cfg, L)) != DQ_OK) return s;
+    dq_ctx *c = *ctx;
+
+    dq::AttnArgs a{};
+    a.q = static_cast<const float *>(q);
+    a.out = out;
+    a.out_dtype = cfg->out_dtype;
+    a.codes_k = static_cast<const uint8_t *>(bufs->codes_k);
+    a.codes_v = static_cast<const uint8_t *>(bufs->codes_v);
+    a.meta_k = bufs->meta_k;
+    a.meta_v = bufs->meta_v;
+    a.mean_k = cfg->k.mean ? static_cast<const float *>(bufs->mean_k) : nullptr;
+    a.raw_k = static_cast<const uint16_t *>(bufs->raw_k);
+    a.raw_v = static_cast<const uint16_t *>(bufs->raw_v);
+    a.q_comp = cfg->k.rot == DQ_ROT_DENSE ? static_cast<const float *>(bufs->q_comp) : nullptr;
+    a.rot_k = cfg->k.rot;
+    a.rot_v = cfg->v.rot;
+    a.raw_bf16 = cfg->kv_dtype == DQ_BF16;
+    a.seq_len = seq_len;
+    const long long n_s = seq_len < cfg->n_sink ? seq_len : cfg->n_sink;
+    long long q_hi = seq_len - cfg->n_recent;
+    if (q_hi < n_s) q_hi = n_s;
+    a.n_q = q_hi - n_s;
+    a.n_sink_eff = static_cast<int>(n_s);
+    a.n_sink_cfg = cfg->n_sink;
+    a.n_recent_cfg = cfg->n_recent;
+    a.n_raw_slots = cfg->n_sink + cfg->n_recent;
+    a.has_raw = a.n_raw_slots > 0 ? 1 : 0;
+    a.tiles_q = (a.n_q + 15) / 16;
+    // split the quantized tiles so that about 4 CTAs per SM are resident
+    long long n_split = 0;
+    if (a.tiles_q > 0) {
+        const long long target = 4LL * c->num_sms;
+        n_split = target / L.U - a.has_raw;
+        if (const char *env = std::getenv("DQ_NSPLIT")) n_split = std::atoll(env);
+        const long long max_by_tiles = a.tiles_q / 8 > 0 ? a.tiles_q / 8 : 1;
+        if (n_split > max_by_tiles) n_split = max_by_tiles;
+        if (n_split > 64) n_split = 64;
+        if (n_split < 1) n_split = 1;
+    }
+    a.n_split = static_cast<int>(n_split);
+    a.items = a.has_raw + a.n_split;
+    if (a.items == 0) return fail(DQ_EINVAL, "nothing to attend to");
+    a.sm_log2 = sm_scale * 1.4426950408889634f;
+    a.hscale = static_cast<float>(1.0 / std::sqrt(static_cast<double>(L.d)));
+    a.partials = c->partials;
+    a.counters = c->counters;
+    a.status = c->status;
+    if (static_cast<size_t>(L.U) * a.items * 4 * (L.d + 2) > c->partials_cap)
+        return fail(DQ_EINVAL, "split workspace too small");
+    const int e = dq::launch_attention(L, a, c->num_sms, stream);
+    if (e != 0) return fail(DQ_ECUDA, "attention launch: %s", cudaGetErrorString(static_cast<cudaError_t>(e)));
+    return ok();
+}
+
+dq_status dq_dequantize_kv(dq_ctx **ctx, const dq_config *cfg, const dq_kv_buffers *bufs, int which,
+                           long long slot0, long long n, float *out, void *stream) {
+    if (!cfg || !bufs || !out) return fail(DQ_EINVAL, "NULL argument");
+    Layout L;
+    dq_status s = dq::make_layout(cfg, &L);
+    if (s != DQ_OK) return s;
+    if (which != 0 && which != 1) return fail(DQ_EINVAL, "which must be 0 (K) or 1 (V)");
+    if (slot0 < 0 || n < 1 || slot0 + n > L.qcap) return fail(DQ_EINVAL, "slots outside the cache");
+    if ((s = check_bufs(L, bufs)) != DQ_OK) return s;
+    if (!aligned16(out)) return fail(DQ_EALIGN, "out not 16-byte aligned");
+    if ((s = get_ctx(ctx, cfg, L)) != DQ_OK) return s;
+    dq::DequantArgs a{};
+    a.codes = static_cast<const uint8_t *>(which == 0 ? bufs->codes_k : bufs->codes_v);
+    a.meta = which == 0 ? bufs->meta_k : bufs->meta_v;
+    a.mean = which == 0 && cfg->k.mean ? static_cast<const float *>(bufs->mean_k) : nullptr;
+    a.is_key = which == 0;
+    a.bits = which == 0 ? cfg->k.bits : cfg->v.bits;
+    a.meta_f16 = cfg->meta_dtype == DQ_F16;
+    a.slot0 = slot0;
+    a.n = n;
+    a.out = out;
+    const int e = dq::launch_dequant(L, a, stream);
+    if (e != 0) return fail(DQ_ECUDA, "dequantize launch: %s", cudaGetErrorString(static_cast<cudaError_t>(e)));
+    return ok();
+}
+
+dq_status dq_check(dq_ctx *ctx, void *stream) {
+    if (!ctx) return ok();
+    cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return fail(DQ_ECUDA, "stream: %s", cudaGetErrorString(e));
+    unsigned st = 0;
+    if (cudaMemcpy(&st, ctx->status, sizeof st, cudaMemcpyDeviceToHost) != cudaSuccess)
+        return fail(DQ_ECUDA, "status read failed");
+    if (st && cudaMemset(ctx->status, 0, sizeof st) != cudaSuccess) return fail(DQ_ECUDA, "status clear failed");
+    if (st & dq::ST_TIMEOUT) return fail(DQ_ETIMEOUT, "a bounded device wait ran out");
+    if (st & dq::ST_NONFINITE) return fail(DQ_ENONFINITE, "non-finite K/V input");
+    return ok();
+}
+
+void dq_free(dq_ctx *ctx) {
+    if (!ctx) return;
+    cudaFree(ctx->status);
+    cudaFree(ctx->partials);
+    cudaFree(ctx->counters);
+    delete ctx;
+}
+
+}  // extern "C"

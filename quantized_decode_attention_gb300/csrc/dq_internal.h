@@ -1,0 +1,104 @@
+// Internal declarations shared by the host API and the CUDA kernels of libdq.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include "dq.h"
+
+namespace dq {
+
+// Status bits latched on the device (ctx->status word).
+enum : unsigned { ST_NONFINITE = 1u, ST_TIMEOUT = 2u, ST_BOUNDS = 4u };
+
+// Sizes and strides derived from a config (all in bytes unless noted).
+struct Layout {
+    int B, Hkv, Hq, G, d;
+    int U;               // units = B * Hkv
+    int bits_k, bits_v;
+    int rowK;            // bytes per key record
+    int pairV;           // bytes per value pair record
+    long long qcap;      // quantized slots per unit (multiple of 16)
+    int rcap;            // raw slots per unit (multiple of 16)
+    int meta_bytes;      // 2 (fp16) or 4 (fp32) per scale/offset value
+    int n_sink, n_recent;
+    size_t sz[DQ_NUM_BUFFERS];
+};
+
+dq_status make_layout(const dq_config *cfg, Layout *L);
+
+// Per-launch arguments of the quantize kernels.
+struct QuantArgs {
+    const void *x;          // [B][Hkv][n_tok][d] input
+    int in_dtype;           // dq_dtype
+    long long pos0, n_tok;  // tokens [pos0, pos0+n_tok)
+    long long seq_after;    // pos0 + n_tok
+    int is_key;
+    int bits, rot, use_mean, meta_f16;
+    float clip;             // 0 or kappa
+    int clip_ilo, clip_ihi; // quantile order-statistic indices
+    float clip_flo, clip_fhi;
+    float hscale;           // fp32(1/sqrt(d))
+    uint8_t *codes;         // codes_k or codes_v
+    void *meta;
+    float *mean;            // [U][d] (keys with mean) or nullptr
+    const float *T;         // dense transform [Hkv][d][d] or nullptr
+    uint16_t *raw;          // raw_k or raw_v
+    unsigned *status;
+};
+
+struct AttnArgs {
+    const float *q;         // [B][Hq][d]
+    void *out;              // [B][Hq][d]
+    int out_dtype;
+    const uint8_t *codes_k, *codes_v;
+    const void *meta_k, *meta_v;
+    const float *mean_k;    // nullptr if no mean
+    const uint16_t *raw_k, *raw_v;
+    const float *q_comp;    // [Hkv][d][d] T^{-T} or nullptr
+    int rot_k, rot_v;
+    int raw_bf16;           // raw region dtype: 1 bf16, 0 fp16
+    long long seq_len;
+    long long n_q;          // quantized tokens read: [n_sink, n_sink + n_q)
+    int n_sink_eff;         // valid sink slots
+    int n_raw_slots;        // raw slots scanned (n_sink + n_recent)
+    int n_sink_cfg, n_recent_cfg;
+    int has_raw;            // 1 if a raw item exists per unit
+    int n_split;            // quantized chunks per unit
+    int items;              // has_raw + n_split
+    long long tiles_q;      // ceil(n_q / 16)
+    float sm_log2;          // sm_scale * log2(e)
+    float hscale;
+    float *partials;        // [U][items][4][d + 2]
+    int *counters;          // [U], zero between calls
+    unsigned *status;
+};
+
+struct DequantArgs {
+    const uint8_t *codes;
+    const void *meta;
+    const float *mean;
+    int is_key, bits, meta_f16;
+    long long slot0, n;
+    float *out;
+};
+
+// launchers (return cudaError_t as int)
+int launch_key_mean(const Layout &L, const QuantArgs &a, void *stream);
+int launch_quantize(const Layout &L, const QuantArgs &a, void *stream);
+int launch_dequant(const Layout &L, const DequantArgs &a, void *stream);
+int launch_attention(const Layout &L, const AttnArgs &a, int num_sms, void *stream);
+size_t attention_smem_bytes(const Layout &L);
+
+}  // namespace dq
+
+struct dq_ctx {
+    dq_config cfg;
+    dq::Layout L;
+    int device;
+    int num_sms;
+    unsigned *status;    // device word
+    float *partials;     // split partials
+    size_t partials_cap; // floats
+    int *counters;       // [U]
+};

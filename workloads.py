@@ -170,3 +170,36 @@ def make_q(w: Workload, batch: Optional[int] = None, salt: int = 0) -> np.ndarra
 def make_new_token(w: Workload, batch: Optional[int] = None, salt: int = 0):
     """One new decode token's K and V, [B, Hkv, 1, d], same distributions as the cache."""
     return make_kv(w, seq=1, batch=batch, salt=10_000 + salt)
+
+
+def _sylvester(d: int) -> np.ndarray:
+    H = np.ones((1, 1))
+    while H.shape[0] < d:
+        H = np.block([[H, H], [H, -H]])
+    return H
+
+
+def dense_transform(w: Workload, gamma: float = 1e-2):
+    """Synthetic dense key transform T and its query compensation T^{-T}, per KV head.
+
+    Stands in for a calibrated transform: built from the synthetic key and query
+    covariances as c * (Hn) * Lambda^(-1/4) * U^T * L^T, with L the Cholesky factor of
+    the damped query covariance, U Lambda U^T = L^T (damped key covariance) L, and c
+    chosen so that ||T||_F = sqrt(d).  Returns float32 arrays [Hkv, d, d].
+    """
+    d = w.head_dim
+    Lk = cov_factor(w, TID_SIGMA_K)
+    Lq = cov_factor(w, TID_SIGMA_Q)
+    Hn = _sylvester(d) / np.sqrt(d)
+    Ts, Qs = [], []
+    for h in range(w.n_kv_heads):
+        SK = Lk[h] @ Lk[h].T
+        SQ = Lq[h] @ Lq[h].T
+        L = np.linalg.cholesky(SQ + gamma * np.trace(SQ) / d * np.eye(d))
+        M = SK + gamma * np.trace(SK) / d * np.eye(d)
+        lam, U = np.linalg.eigh(L.T @ M @ L)
+        T = Hn @ np.diag(lam ** -0.25) @ U.T @ L.T
+        T *= np.sqrt(d) / np.linalg.norm(T)
+        Ts.append(T)
+        Qs.append(np.linalg.inv(T).T)
+    return np.stack(Ts).astype(np.float32), np.stack(Qs).astype(np.float32)
