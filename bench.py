@@ -228,7 +228,7 @@ def run_gpu(args, w, bits, S, k_dev, v_dev, q_dev, knew_dev, vnew_dev, rank):
     k_h = knew_dev.cpu().pin_memory()
     v_h = vnew_dev.cpu().pin_memory()
     out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-    q_b, k_b, v_b = torch.empty_like(q_dev), torch.empty_like(knew_dev), torch.empty_like(vnew_dev)
+    q_b, k_b, v_b = q_dev.clone(), knew_dev.clone(), vnew_dev.clone()
     n_e2e = min(args.steps, 200)
     with torch.cuda.stream(stream):
         for i in range(3):

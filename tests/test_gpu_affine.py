@@ -4,7 +4,7 @@ Bit-exact: packed key/value records, fp16/fp32 scale-offset, the fp32 key
 channel mean, the 16-bit sink/recent slots and the dequantized fp32 values.
 Attention: max-abs error <= 2e-3 against the fp64 oracle on the same
 quantized cache (fp32 output); a bf16 output may add its own rounding, at
-most half a bf16 ulp of the result.
+most half a bf16 ulp of the result (<= 2^-8 |y|).
 """
 import numpy as np
 import pytest
@@ -119,7 +119,7 @@ def test_attention_parity(name, out_dtype):
         ref = oracle.attention(w, q, k, v, seq_len, qk, qv, q_comp=Qc)
         got = out_to_np(out)
         err = np.abs(got - ref)
-        bound = TOL + (2.0 ** -9 * np.abs(ref) if out_dtype == "bf16" else 0.0)
+        bound = TOL + (2.0 ** -8 * np.abs(ref) if out_dtype == "bf16" else 0.0)
         assert np.all(err <= bound), (seq_len, float(err.max()))
     cache.close()
 
