@@ -187,6 +187,38 @@ dq_status dq_dequantize_kv(dq_ctx **ctx, const dq_config *cfg, const dq_kv_buffe
  */
 dq_status dq_check(dq_ctx *ctx, void *stream);
 
+/*
+ * Allocation-free decode attention (this library's own addition; the pages
+ * have no counterpart).  Computes exactly what dq_decode_attention computes,
+ * with the same arguments minus the context, but never calls cudaMalloc,
+ * cudaFree or any allocating routine.  It is meant for callers that may not
+ * allocate device memory behind their own back: serving engines that hand out
+ * all device memory from one pre-reserved pool, decode loops that cannot
+ * afford the device-wide synchronization cudaMalloc/cudaFree can cause, and
+ * embedders with a fixed device-memory budget.
+ *
+ * Scratch: the split partials and tickets live in one statically sized device
+ * array of DQ_NOALLOC_SCRATCH_BYTES inside this library; every GPU that loads
+ * the library holds it until the process exits.
+ *   - The first call on a device looks up that array's device address (with
+ *     that device current) and caches it; make this first call before any
+ *     stream capture.
+ *   - All calls share the array and it keeps the last call's contents; each
+ *     call clears the part that must start at zero on `stream` first.  Calls
+ *     whose work overlaps on the GPU (different streams, or different host
+ *     threads without ordering) race on it and give wrong results: order them.
+ *   - Limits: batch * n_kv_heads <= 16384, and the split partials
+ *     (batch * n_kv_heads * items * 4 * (head_dim + 2) floats) must fit the
+ *     array; the split is narrowed to fit, and a config that cannot fit even
+ *     unsplit is refused with DQ_EINVAL and a message naming the limit.
+ *   - Device-side conditions (a bounded wait running out) are not reported by
+ *     this entry point; use the context-based one with dq_check to see them.
+ * Errors: DQ_EINVAL, DQ_EALIGN, DQ_EUNSUPPORTED, DQ_ECUDA.
+ */
+#define DQ_NOALLOC_SCRATCH_BYTES (4u << 20)
+dq_status dq_decode_attention_noalloc(const dq_config *cfg, const dq_kv_buffers *bufs, const void *q,
+                                      void *out, long long seq_len, float sm_scale, void *stream);
+
 /* Release a context and its workspace.  NULL-safe.  The caller must make sure
  * no enqueued work still uses it. */
 void dq_free(dq_ctx *ctx);

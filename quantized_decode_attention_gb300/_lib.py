@@ -73,6 +73,9 @@ def load() -> C.CDLL:
                                       C.c_longlong, C.c_float, P]
     L.dq_dequantize_kv.argtypes = [C.POINTER(P), C.POINTER(Config), C.POINTER(Buffers), C.c_int,
                                    C.c_longlong, C.c_longlong, P, P]
+    L.dq_decode_attention_noalloc.argtypes = [C.POINTER(Config), C.POINTER(Buffers), P, P, C.c_longlong,
+                                              C.c_float, P]
+    L.dq_decode_attention_noalloc.restype = C.c_int
     L.dq_check.argtypes = [P, P]
     L.dq_free.argtypes = [P]
     L.dq_free.restype = None
@@ -162,6 +165,15 @@ class KVCache:
         b = self.buffers()
         _raise(load().dq_decode_attention(C.byref(self.ctx), C.byref(self.cfg), C.byref(b), _ptr(q), _ptr(out),
                                           seq_len, sm_scale, _stream(stream)))
+
+    def attention_noalloc(self, q, out, seq_len: int, sm_scale: float | None = None, stream=None):
+        """Same result as attention(), through the entry point that allocates nothing
+        (its split workspace is a static device array inside the library)."""
+        if sm_scale is None:
+            sm_scale = self.cfg.head_dim ** -0.5
+        b = self.buffers()
+        _raise(load().dq_decode_attention_noalloc(C.byref(self.cfg), C.byref(b), _ptr(q), _ptr(out), seq_len,
+                                                  sm_scale, _stream(stream)))
 
     def dequantize(self, which: int, slot0: int, n: int, out, stream=None):
         b = self.buffers()

@@ -50,6 +50,11 @@ dq_status validate_tensor(const dq_tensor_cfg &t, int d, bool key, const char *n
 
 namespace dq {
 
+dq_status set_last_error(dq_status s, const char *msg) {
+    if (s == DQ_OK) return ok();
+    return fail(s, "%s", msg);
+}
+
 dq_status make_layout(const dq_config *cfg, Layout *L) {
     if (!cfg || !L) return fail(DQ_EINVAL, "NULL argument");
     const dq_config &c = *cfg;

@@ -27,6 +27,9 @@ struct Layout {
 
 dq_status make_layout(const dq_config *cfg, Layout *L);
 
+// Record `msg` as this thread's last error (empty for DQ_OK) and return `s`.
+dq_status set_last_error(dq_status s, const char *msg);
+
 // Per-launch arguments of the quantize kernels.
 struct QuantArgs {
     const void *x;          // [B][Hkv][n_tok][d] input
