@@ -95,7 +95,7 @@ typedef struct {
  * of each, in field order; a field whose size is 0 is unused and may be NULL.
  *
  * U = batch * n_kv_heads units, unit u = b * n_kv_heads + kv_head.
- * Qcap = round_up(max_seq - n_sink, 16) quantized slots per unit; token
+ * Qcap = round_up(max_seq - n_sink, 64) quantized slots per unit; token
  * t >= n_sink lives in quantized slot t - n_sink.
  * Rcap = round_up(n_sink + n_recent, 16) raw slots per unit; token t < n_sink
  * in raw slot t, the latest n_recent tokens in raw slot n_sink + t % n_recent.
@@ -207,10 +207,11 @@ dq_status dq_check(dq_ctx *ctx, void *stream);
  *     call clears the part that must start at zero on `stream` first.  Calls
  *     whose work overlaps on the GPU (different streams, or different host
  *     threads without ordering) race on it and give wrong results: order them.
- *   - Limits: batch * n_kv_heads <= 16384, and the split partials
- *     (batch * n_kv_heads * items * 4 * (head_dim + 2) floats) must fit the
- *     array; the split is narrowed to fit, and a config that cannot fit even
- *     unsplit is refused with DQ_EINVAL and a message naming the limit.
+ *   - Limits: batch * n_kv_heads <= 16384, and the split partials (two
+ *     records of 4 x (head_dim + 2) floats per KV head and CTA touching it)
+ *     must fit the array; the grid is narrowed until they do, and a config
+ *     that cannot fit even with one CTA is refused with DQ_EINVAL and a
+ *     message naming the limit.
  *   - Device-side conditions (a bounded wait running out) are not reported by
  *     this entry point; use the context-based one with dq_check to see them.
  * Errors: DQ_EINVAL, DQ_EALIGN, DQ_EUNSUPPORTED, DQ_ECUDA.

@@ -85,7 +85,7 @@ dq_status make_layout(const dq_config *cfg, Layout *L) {
     l.bits_v = c.v.bits;
     l.rowK = c.head_dim * c.k.bits / 8;
     l.pairV = 2 * c.head_dim * c.v.bits / 8;
-    l.qcap = round_up(c.max_seq - c.n_sink, 16);
+    l.qcap = round_up(c.max_seq - c.n_sink, 64);
     l.rcap = static_cast<int>(round_up(c.n_sink + c.n_recent, 16));
     l.meta_bytes = c.meta_dtype == DQ_F16 ? 2 : 4;
     l.n_sink = c.n_sink;
@@ -144,12 +144,11 @@ static dq_status get_ctx(dq_ctx **pctx, const dq_config *cfg, const Layout &L) {
         delete c;
         return fail(DQ_ECUDA, "cannot query the current device");
     }
-    // split partials: at most (1 + max split) items per unit
-    const long long max_tiles = (L.qcap + 15) / 16;
-    long long max_split = max_tiles < 1 ? 1 : max_tiles;
-    const long long cap_split = 64;
-    if (max_split > cap_split) max_split = cap_split;
-    c->partials_cap = static_cast<size_t>(L.U) * (1 + max_split) * 4 * (L.d + 2);
+    // split partials for the largest persistent grid the attention kernel can
+    // use (at most 8 CTAs per SM): a unit is touched by at most 2G/U + 2 CTAs,
+    // each writing two records of 4 heads x (head_dim + 2) floats
+    const long long G = 8LL * c->num_sms;
+    c->partials_cap = static_cast<size_t>((2 * G + 2LL * L.U) * 2 * 4 * (L.d + 2));
     cudaError_t e1 = cudaMalloc(&c->status, sizeof(unsigned));
     cudaError_t e2 = cudaMalloc(&c->partials, c->partials_cap * sizeof(float));
     cudaError_t e3 = cudaMalloc(&c->counters, sizeof(int) * L.U);
@@ -288,29 +287,14 @@ dq_status dq_decode_attention(dq_ctx **ctx, const dq_config *cfg, const dq_kv_bu
     a.n_recent_cfg = cfg->n_recent;
     a.n_raw_slots = cfg->n_sink + cfg->n_recent;
     a.has_raw = a.n_raw_slots > 0 ? 1 : 0;
-    a.tiles_q = (a.n_q + 15) / 16;
-    // split the quantized tiles so that about 4 CTAs per SM are resident
-    long long n_split = 0;
-    if (a.tiles_q > 0) {
-        const long long target = 4LL * c->num_sms;
-        n_split = target / L.U - a.has_raw;
-        if (const char *env = std::getenv("DQ_NSPLIT")) n_split = std::atoll(env);
-        const long long max_by_tiles = a.tiles_q / 8 > 0 ? a.tiles_q / 8 : 1;
-        if (n_split > max_by_tiles) n_split = max_by_tiles;
-        if (n_split > 64) n_split = 64;
-        if (n_split < 1) n_split = 1;
-    }
-    a.n_split = static_cast<int>(n_split);
-    a.items = a.has_raw + a.n_split;
-    if (a.items == 0) return fail(DQ_EINVAL, "nothing to attend to");
     a.sm_log2 = sm_scale * 1.4426950408889634f;
     a.hscale = static_cast<float>(1.0 / std::sqrt(static_cast<double>(L.d)));
     a.partials = c->partials;
     a.counters = c->counters;
     a.status = c->status;
-    if (static_cast<size_t>(L.U) * a.items * 4 * (L.d + 2) > c->partials_cap)
-        return fail(DQ_EINVAL, "split workspace too small");
-    const int e = dq::launch_attention(L, a, c->num_sms, stream);
+    int e = dq::plan_attention(L, a, c->num_sms, static_cast<long long>(c->partials_cap));
+    if (e != 0) return fail(DQ_ECUDA, "attention planning: %s", cudaGetErrorString(static_cast<cudaError_t>(e)));
+    e = dq::launch_attention(L, a, c->num_sms, stream);
     if (e != 0) return fail(DQ_ECUDA, "attention launch: %s", cudaGetErrorString(static_cast<cudaError_t>(e)));
     return ok();
 }

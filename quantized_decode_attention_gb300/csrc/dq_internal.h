@@ -66,13 +66,15 @@ struct AttnArgs {
     int n_sink_eff;         // valid sink slots
     int n_raw_slots;        // raw slots scanned (n_sink + n_recent)
     int n_sink_cfg, n_recent_cfg;
-    int has_raw;            // 1 if a raw item exists per unit
-    int n_split;            // quantized chunks per unit
-    int items;              // has_raw + n_split
-    long long tiles_q;      // ceil(n_q / 16)
+    int has_raw;            // 1 if the unit has 16-bit slots
+    int n_rt;               // 16-slot tiles of 16-bit tokens per unit
+    long long n_qc;         // 64-token chunks of packed tokens per unit
+    long long items_per_unit, total_items;
+    int grid;               // persistent CTAs (one wave)
+    int max_slots;          // partial-record slots per unit
     float sm_log2;          // sm_scale * log2(e)
     float hscale;
-    float *partials;        // [U][items][4][d + 2]
+    float *partials;        // [U][max_slots][2 kinds][4 heads][d + 2]
     int *counters;          // [U], zero between calls
     unsigned *status;
 };
@@ -91,6 +93,10 @@ int launch_key_mean(const Layout &L, const QuantArgs &a, void *stream);
 int launch_quantize(const Layout &L, const QuantArgs &a, void *stream);
 int launch_dequant(const Layout &L, const DequantArgs &a, void *stream);
 int launch_attention(const Layout &L, const AttnArgs &a, int num_sms, void *stream);
+// Fill the work schedule of `a` (items, grid, partial slots) for a launch on a
+// device with num_sms SMs whose partial workspace holds cap_floats floats.
+int plan_attention(const Layout &L, AttnArgs &a, int num_sms, long long cap_floats);
+long long attention_partial_floats(const Layout &L, const AttnArgs &a);
 size_t attention_smem_bytes(const Layout &L);
 
 }  // namespace dq

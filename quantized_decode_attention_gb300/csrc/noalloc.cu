@@ -117,34 +117,23 @@ extern "C" dq_status dq_decode_attention_noalloc(const dq_config *cfg, const dq_
     a.n_recent_cfg = cfg->n_recent;
     a.n_raw_slots = cfg->n_sink + cfg->n_recent;
     a.has_raw = a.n_raw_slots > 0 ? 1 : 0;
-    a.tiles_q = (a.n_q + 15) / 16;
-    long long n_split = 0;
-    if (a.tiles_q > 0) {
-        n_split = 4LL * num_sms / L.U - a.has_raw;
-        const long long max_by_tiles = a.tiles_q / 8 > 0 ? a.tiles_q / 8 : 1;
-        if (n_split > max_by_tiles) n_split = max_by_tiles;
-        if (n_split > 64) n_split = 64;
-        if (n_split < 1) n_split = 1;
-    }
-    // the partials must fit the static scratch: shrink the split first, then refuse
-    const size_t per_item = static_cast<size_t>(L.U) * 4 * (L.d + 2) * sizeof(float);
-    while (n_split > 1 && per_item * static_cast<size_t>(a.has_raw + n_split) > kPartialsBytes) n_split--;
-    a.n_split = static_cast<int>(n_split);
-    a.items = a.has_raw + a.n_split;
-    if (a.items == 0) return dq::set_last_error(DQ_EINVAL, "nothing to attend to");
-    const size_t need = per_item * static_cast<size_t>(a.items);
-    if (need > kPartialsBytes) {
-        char msg[200];
-        std::snprintf(msg, sizeof msg,
-                      "split partials need %zu bytes; the allocation-free scratch holds %zu (limit %zu bytes total)",
-                      need, kPartialsBytes, kScratchBytes);
-        return dq::set_last_error(DQ_EINVAL, msg);
-    }
     a.sm_log2 = sm_scale * 1.4426950408889634f;
     a.hscale = static_cast<float>(1.0 / std::sqrt(static_cast<double>(L.d)));
     a.counters = reinterpret_cast<int *>(scratch);
     a.status = reinterpret_cast<unsigned *>(scratch + kStatusOffset);
     a.partials = reinterpret_cast<float *>(scratch + kPartialsOffset);
+    // the partials must fit the static scratch: the plan narrows the grid
+    // until they do, and refuses the config if even one CTA's would not
+    const long long cap = static_cast<long long>(kPartialsBytes / sizeof(float));
+    int pe = dq::plan_attention(L, a, num_sms, cap);
+    if (pe == static_cast<int>(cudaErrorMemoryAllocation)) {
+        char msg[200];
+        std::snprintf(msg, sizeof msg,
+                      "split partials need %lld bytes; the allocation-free scratch holds %zu (limit %zu bytes total)",
+                      dq::attention_partial_floats(L, a) * 4, kPartialsBytes, kScratchBytes);
+        return dq::set_last_error(DQ_EINVAL, msg);
+    }
+    if (pe != 0) return dq::set_last_error(DQ_ECUDA, cudaGetErrorString(static_cast<cudaError_t>(pe)));
 
     // the tickets must start at zero; an earlier call leaves them at zero, but
     // clear them anyway so that one aborted call cannot poison the next

@@ -58,7 +58,7 @@ def expected_buffers(w: W.Workload, qk, qv, nq: int):
 def lib_views(w: W.Workload, cache, max_seq: int):
     """Reshape the library's byte buffers into [U-major] numpy views."""
     B, H, d = w.batch, w.n_kv_heads, w.head_dim
-    qcap = -(-(max_seq - w.n_sink) // 16) * 16
+    qcap = -(-(max_seq - w.n_sink) // 64) * 64
     rcap = -(-(w.n_sink + w.n_recent) // 16) * 16
     rowk = d * w.bits // 8
     t = {n: (x.cpu().numpy() if x is not None else None) for n, x in cache.tensors.items()}
