@@ -208,7 +208,7 @@ dq_status dq_check(dq_ctx *ctx, void *stream);
  *     whose work overlaps on the GPU (different streams, or different host
  *     threads without ordering) race on it and give wrong results: order them.
  *   - Limits: batch * n_kv_heads <= 16384, and the split partials (two
- *     records of 4 x (head_dim + 2) floats per KV head and CTA touching it)
+ *     records of 4 x (head_dim + 4) floats per KV head and CTA touching it)
  *     must fit the array; the grid is narrowed until they do, and a config
  *     that cannot fit even with one CTA is refused with DQ_EINVAL and a
  *     message naming the limit.

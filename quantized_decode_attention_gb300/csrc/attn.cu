@@ -11,12 +11,14 @@
 // rotated back with Hn (its own inverse) at the end.
 //
 // Design for GB300:
-//  * Work items: per KV head ("unit"), its 16-slot tiles of 16-bit sink/recent
-//    tokens followed by its 64-token chunks of packed tokens.  A persistent
-//    grid of one wave splits the list of all items into equal contiguous
-//    ranges (stream-K); a CTA walks its range unit by unit.
-//  * Packed chunks stream HBM -> shared memory with bulk asynchronous copies
-//    (cp.async.bulk, completion on an mbarrier), a 2-deep ring per warp.
+//  * Work items: per KV head ("unit"), its chunks of 64 packed tokens (32 at
+//    4 bits); the unit's 16-slot tiles of 16-bit sink/recent tokens ride along
+//    with its chunks.  A persistent grid of one wave splits the list of all
+//    chunks into equal contiguous ranges (stream-K); a CTA walks its range
+//    unit by unit, handing chunks to its warps one at a time.
+//  * Packed chunks and 16-bit tiles stream HBM -> shared memory with bulk
+//    asynchronous copies (cp.async.bulk, completion on an mbarrier), a 2-deep
+//    ring per warp.
 //  * Codes become mma operands with one AND per code pair: a code m held in a
 //    binary16 bit pattern below 2048 is exactly m * 2^-24 (scaled by a
 //    per-field power of two, folded into q and into the output rows).
@@ -24,7 +26,8 @@
 //    columns are 4 query heads x (hi, lo) binary16 halves of an fp32 operand,
 //    adjacent, so each lane owns one head and adds its halves in registers.
 //    P' is transposed into the B operand with movmatrix (no shared memory).
-//  * Softmax bookkeeping (max, rescale) once per 64 tokens.
+//  * Softmax bookkeeping once per chunk; the running max may lag by 2^8, so
+//    the accumulators are rescaled only when it grows by more than that.
 //  * Each CTA merges its 4 warps and writes one partial per (unit, kind);
 //    the last CTA to finish a unit (atomic ticket, no waiting) merges them,
 //    rotates the value accumulator back and writes the output.
@@ -37,9 +40,9 @@
 
 namespace dq {
 
-constexpr int CHUNK = 64;                           // tokens per packed work item
 constexpr int RTILE = 16;                           // slots per 16-bit work item
 constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;   // 2 s; a healthy copy takes microseconds
+constexpr float RESCALE_SLACK = 8.0f;               // log2 units the running max may lag
 
 struct AttnShape {
     int Hkv, G, D;
@@ -49,19 +52,24 @@ struct AttnShape {
 
 template <int D, int BK, int BV, bool M16>
 struct Cfg {
+    static constexpr int CK = 32;  // tokens per packed work item (chunk)
+    static constexpr int TILES = CK / 16;
     static constexpr int ROWK = D * BK / 8;
     static constexpr int PAIRV = 2 * D * BV / 8;
     static constexpr int MB = M16 ? 2 : 4;
-    static constexpr int KBYTES = CHUNK * ROWK;
-    static constexpr int VBYTES = CHUNK / 2 * PAIRV;
-    static constexpr int MBYTES = CHUNK * 2 * MB;
+    static constexpr int KBYTES = CK * ROWK;
+    static constexpr int VBYTES = CK / 2 * PAIRV;
+    static constexpr int MBYTES = CK * 2 * MB;
     static constexpr int STAGE = KBYTES + VBYTES + 2 * MBYTES;
-    static constexpr int NST = 2;
+    static constexpr int NST = 2;                 // bulk-copy ring depth per warp
+    static constexpr int RAWBYTES = 64 * D;       // one 16-slot tile of 16-bit keys + values
+    // bytes of one warp's ring: NST stages, or one 16-bit tile if that is larger
+    static constexpr int RING = NST * STAGE > RAWBYTES ? NST * STAGE : RAWBYTES;
     static constexpr int NKS = D / 16;
     static constexpr int NMT = D / 16;
-    static constexpr int PR = D + 2;  // floats per head in a partial record
+    static constexpr int PR = D + 4;  // floats per head in a partial record: acc[D], m, l, 0, 0
     // resident CTAs per SM the kernel is register-limited to (smem allows it)
-    static constexpr int MINB = STAGE <= 5120 ? 4 : (STAGE <= 7168 ? 3 : 2);
+    static constexpr int MINB = RING <= 10240 ? 4 : (RING <= 14336 ? 3 : 2);
 };
 
 // ---- code extraction --------------------------------------------------------
@@ -162,6 +170,9 @@ __device__ __forceinline__ uint32_t hilo_bf16(float x) {
 }
 
 // ---- online softmax of one warp; lane (g, tig) owns query head tig --------------
+// The running max m may lag the true maximum by up to RESCALE_SLACK (log2
+// units): probabilities are exp2(logit - m) <= 2^RESCALE_SLACK, and the
+// accumulators are rescaled only when a logit exceeds m by more than that.
 template <int NMT>
 struct WarpState {
     float m, l, ao;
@@ -180,19 +191,13 @@ struct WarpState {
         for (int k = 1; k < NT; k++) mx = fmaxf(mx, lg[k]);
 #pragma unroll
         for (int o = 4; o < 32; o <<= 1) mx = fmaxf(mx, __shfl_xor_sync(FULL, mx, o));
-        const float mn = fmaxf(m, mx);
-        const float mu = mn == -INFINITY ? 0.f : mn;
-        const float al = exp2f(m - mu);
-        m = mn;
-        float sum = 0.f;
-#pragma unroll
-        for (int k = 0; k < NT; k++) {
-            p[k] = exp2f(lg[k] - mu);
-            sum += p[k];
-        }
-        l = l * al + sum;
-        ao *= al;
-        if (__any_sync(FULL, al != 1.f)) {
+        const bool grow = mx > m + RESCALE_SLACK;  // also true for the first finite logit
+        if (__any_sync(FULL, grow)) {
+            const float mn = grow ? mx : m;
+            const float al = grow ? exp2f(m - mn) : 1.f;  // 0 when m was -inf
+            m = mn;
+            l *= al;
+            ao *= al;
 #pragma unroll
             for (int mi = 0; mi < NMT; mi++) {
                 acc[mi][0] *= al;
@@ -201,6 +206,14 @@ struct WarpState {
                 acc[mi][3] *= al;
             }
         }
+        const float mu = m == -INFINITY ? 0.f : m;
+        float sum = 0.f;
+#pragma unroll
+        for (int k = 0; k < NT; k++) {
+            p[k] = exp2f(lg[k] - mu);
+            sum += p[k];
+        }
+        l += sum;
     }
 };
 
@@ -211,18 +224,19 @@ struct Smem {
     float q_raw[4][D];
     float q_rot[4][D];
     float qsum[4], qmu[4];
-    float merge[4][4][C::PR];  // [warp][head][m, l, acc[D]]
+    float merge[4][4][C::PR];  // [warp][head][acc[D], m, l, -, -]
     uint64_t bars[4][C::NST];
+    int next_chunk;            // chunks of the current segment handed out so far
     int last;
-    alignas(128) uint8_t ring[4][C::NST][C::STAGE];
+    alignas(128) uint8_t ring[4][C::RING];  // per warp: stage s at s * STAGE
 };
 
-// Bulk-copy one 64-token chunk of unit u into a stage.
+// Bulk-copy packed chunk c (of CK tokens) of unit u into a stage.
 template <int D, int BK, int BV, bool M16>
 __device__ __forceinline__ void issue_chunk(const AttnArgs &a, const AttnShape &sh, int u, long long c,
                                             uint8_t *stage, uint64_t *bar) {
     using C = Cfg<D, BK, BV, M16>;
-    const long long t0 = c * CHUNK;
+    const long long t0 = c * C::CK;
     const uint8_t *ck = a.codes_k + (static_cast<long long>(u) * sh.qcap + t0) * C::ROWK;
     const uint8_t *cv = a.codes_v + (static_cast<long long>(u) * (sh.qcap / 2) + t0 / 2) * C::PAIRV;
     const uint8_t *mk = static_cast<const uint8_t *>(a.meta_k) + (static_cast<long long>(u) * sh.qcap + t0) * 2 * C::MB;
@@ -234,18 +248,29 @@ __device__ __forceinline__ void issue_chunk(const AttnArgs &a, const AttnShape &
     bulk_g2s(stage + C::KBYTES + C::VBYTES + C::MBYTES, mv, C::MBYTES, bar);
 }
 
+// Bulk-copy 16-bit tile r (16 slots: keys then value pairs) of unit u.
+template <int D>
+__device__ __forceinline__ void issue_raw(const AttnArgs &a, const AttnShape &sh, int u, long long r,
+                                          uint8_t *dst, uint64_t *bar) {
+    const uint16_t *rk = a.raw_k + (static_cast<long long>(u) * sh.rcap + r * RTILE) * D;
+    const uint16_t *rv = a.raw_v + (static_cast<long long>(u) * sh.rcap + r * RTILE) * D;
+    mbar_expect_tx(bar, 64 * D);
+    bulk_g2s(dst, rk, 32 * D, bar);
+    bulk_g2s(dst + 32 * D, rv, 32 * D, bar);
+}
+
 // B operand of q.K^T for this lane: column g = head g>>1, half g&1 of the
-// (scaled) query; channels 16i + 2tig + {0,1} and +8.
-template <int D, int BK, bool QUANT, bool BF16>
-__device__ __forceinline__ void build_qb(const float (*q)[D], uint32_t (&qb)[D / 16][2]) {
+// (scaled) query.  Lane slot (k-step i, sub, e) holds logical channel
+// 16i + 2tig + 8sub + e; `perm` maps it to the channel of q it multiplies.
+template <int D, int BK, bool QUANT, bool BF16, typename Perm>
+__device__ __forceinline__ void build_qb(const float (*q)[D], uint32_t (&qb)[D / 16][2], Perm perm) {
     const int lane = threadIdx.x & 31, g = lane >> 2, tig = lane & 3;
     const int h = g >> 1, part = g & 1;
 #pragma unroll
     for (int i = 0; i < D / 16; i++) {
 #pragma unroll
         for (int sub = 0; sub < 2; sub++) {
-            const int c = 16 * i + 2 * tig + 8 * sub;
-            float v0 = q[h][c], v1 = q[h][c + 1];
+            float v0 = q[h][perm(i, tig, sub, 0)], v1 = q[h][perm(i, tig, sub, 1)];
             if (QUANT) {
                 const float sc = exp2f(static_cast<float>(-field_exp(2 * i + sub, BK)));
                 v0 *= sc;
@@ -260,113 +285,112 @@ __device__ __forceinline__ void build_qb(const float (*q)[D], uint32_t (&qb)[D /
     }
 }
 
-// ---- packed chunks of one unit: this warp takes chunks c0 + warp, + 4, ... -----
-template <int D, int BK, int BV, bool M16>
-__device__ __forceinline__ void quant_part(const AttnArgs &a, const AttnShape &sh, Smem<D, BK, BV, M16> &S, int u,
-                                           long long c0, long long c1, WarpState<D / 16> &st) {
-    using C = Cfg<D, BK, BV, M16>;
-    constexpr int NKS = C::NKS, NMT = C::NMT;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int g = lane >> 2, tig = lane & 3;
-    uint32_t qb[NKS][2];
-    build_qb<D, BK, true, false>(S.q_rot, qb);
-    const float qs_l2 = a.sm_log2 * S.qsum[tig], qm_l2 = a.sm_log2 * S.qmu[tig];
-    const float sk_l2 = a.sm_log2 * 16777216.0f;  // 2^24 undoes the operand scaling
-    const long long first = c0 + warp;
-    const long long n = first < c1 ? (c1 - first + 3) / 4 : 0;
-    uint64_t *bars = S.bars[warp];
-    if (lane == 0)
-        for (long long j = 0; j < n && j < C::NST; j++)
-            issue_chunk<D, BK, BV, M16>(a, sh, u, first + 4 * j, S.ring[warp][j], &bars[j]);
-    __syncwarp();
-    bool timed_out = false;
-    for (long long j = 0; j < n; j++) {
-        const long long c = first + 4 * j;
-        const int s = static_cast<int>(j % C::NST);
-        const uint8_t *stg = S.ring[warp][s];
-        if (!mbar_wait(&bars[s], static_cast<unsigned>((j / C::NST) & 1), WAIT_LIMIT_NS)) timed_out = true;
-        // q . K^T for the 4 tiles of the chunk
-        float sc[4][4];
-#pragma unroll
-        for (int t = 0; t < 4; t++) {
-            constexpr int NW = Slice<D, BK>::NW;
-            uint32_t k0[NW], k1[NW];
-            load_k_slice<D, BK>(stg + (16 * t + g) * C::ROWK, tig, k0);
-            load_k_slice<D, BK>(stg + (16 * t + g + 8) * C::ROWK, tig, k1);
-            sc[t][0] = sc[t][1] = sc[t][2] = sc[t][3] = 0.f;
-#pragma unroll
-            for (int i = 0; i < NKS; i++)
-                mma_f16(sc[t], extract<BK>(k0, 2 * i), extract<BK>(k1, 2 * i), extract<BK>(k0, 2 * i + 1),
-                        extract<BK>(k1, 2 * i + 1), qb[i][0], qb[i][1]);
-        }
-        // logits of tokens 16t+g (k = 2t) and 16t+g+8 (k = 2t+1) for head tig
-        const uint8_t *smk = stg + C::KBYTES + C::VBYTES;
-        const uint8_t *smv = smk + C::MBYTES;
-        float lg[8];
-#pragma unroll
-        for (int t = 0; t < 4; t++)
-#pragma unroll
-            for (int hf = 0; hf < 2; hf++) {
-                const float2 km = ld_meta(smk, 16 * t + g + 8 * hf, M16);
-                const float dot = sc[t][2 * hf] + sc[t][2 * hf + 1];
-                lg[2 * t + hf] = (km.x * sk_l2) * dot + (km.y * qs_l2 + qm_l2);
-            }
-        const long long tok0 = c * CHUNK;
-        const bool ragged = tok0 + CHUNK > a.n_q;  // last chunk of the unit
-        if (ragged) {
-#pragma unroll
-            for (int k = 0; k < 8; k++)
-                if (tok0 + 16 * (k >> 1) + g + 8 * (k & 1) >= a.n_q) lg[k] = -INFINITY;
-        }
-        float p[8];
-        st.template update<8>(lg, p);
-        // P . V per tile: A = V^T (channels x tokens), B = (P * s_v) transposed
-        // by movmatrix; the offsets o_v accumulate separately (Eq. 9)
-        float aos = 0.f;
-#pragma unroll
-        for (int t = 0; t < 4; t++) {
-            float2 vm0 = ld_meta(smv, 16 * t + g, M16), vm1 = ld_meta(smv, 16 * t + g + 8, M16);
-            if (ragged) {  // masked tokens have p = 0, but their metadata may be anything
-                if (tok0 + 16 * t + g >= a.n_q) vm0 = make_float2(0.f, 0.f);
-                if (tok0 + 16 * t + g + 8 >= a.n_q) vm1 = make_float2(0.f, 0.f);
-            }
-            aos += p[2 * t] * vm0.y + p[2 * t + 1] * vm1.y;
-            const uint32_t b0 = movmatrix_t(hilo_f16(p[2 * t] * vm0.x));
-            const uint32_t b1 = movmatrix_t(hilo_f16(p[2 * t + 1] * vm1.x));
-            constexpr int NW = Slice<D, BV>::NW;
-            uint32_t v0[NW], v1[NW];
-            load_v_slice<D, BV>(stg + C::KBYTES + (8 * t + tig) * C::PAIRV, g, v0);
-            load_v_slice<D, BV>(stg + C::KBYTES + (8 * t + tig + 4) * C::PAIRV, g, v1);
-#pragma unroll
-            for (int mi = 0; mi < NMT; mi++)
-                mma_f16(st.acc[mi], extract<BV>(v0, 2 * mi), extract<BV>(v0, 2 * mi + 1), extract<BV>(v1, 2 * mi),
-                        extract<BV>(v1, 2 * mi + 1), b0, b1);
-        }
-        st.ao += aos;
-        __syncwarp();
-        if (lane == 0 && j + C::NST < n) {
-            fence_proxy_async();
-            issue_chunk<D, BK, BV, M16>(a, sh, u, first + 4 * (j + C::NST), S.ring[warp][s], &bars[s]);
-        }
+// Channel of a key record / of q that lane slot (i, tig, sub, e) stands for.
+struct PermIdentity {
+    __device__ __forceinline__ int operator()(int i, int tig, int sub, int e) const {
+        return 16 * i + 2 * tig + 8 * sub + e;
     }
-    if (timed_out && lane == 0) atomicOr(a.status, ST_TIMEOUT);
+};
+// 16-bit key rows are read with 16-byte vectors: lane tig takes channels
+// 32j + 8tig .. +7 of each row, j = i/2; register 2(i&1)+sub of vector j holds
+// channels 32j + 8tig + 4(i&1) + 2sub + {0, 1}.
+struct PermRawK {
+    __device__ __forceinline__ int operator()(int i, int tig, int sub, int e) const {
+        return 32 * (i >> 1) + 8 * tig + 4 * (i & 1) + 2 * sub + e;
+    }
+};
+// 16-bit value pairs are read with 16-byte vectors: lane g takes channels
+// (D/8)g .. (D/8)g + D/8 - 1; P.V row 16mi + 8h + g (m-tile mi, half h) is
+// the channel (D/8)g + 2mi + h.
+template <int D>
+__device__ __forceinline__ int raw_v_channel(int row) {
+    const int g = row & 7, h = (row >> 3) & 1, mi = row >> 4;
+    return (D / 8) * g + 2 * mi + h;
 }
 
-// ---- 16-bit sink/recent slots of one unit: this warp takes tiles t0 + warp, + 4 --
+__device__ __forceinline__ uint32_t vec_word(const uint4 &v, int r) {
+    return r == 0 ? v.x : (r == 1 ? v.y : (r == 2 ? v.z : v.w));
+}
+
+// One packed chunk already in shared memory (stage stg) -> warp state.
+template <int D, int BK, int BV, bool M16>
+__device__ __forceinline__ void process_chunk(const uint8_t *stg, long long tok0, long long n_q,
+                                              const uint32_t (&qb)[D / 16][2], float sk_l2, float qs_l2, float qm_l2,
+                                              WarpState<D / 16> &st) {
+    using C = Cfg<D, BK, BV, M16>;
+    constexpr int NKS = C::NKS, NMT = C::NMT, T = C::TILES;
+    const int lane = threadIdx.x & 31, g = lane >> 2, tig = lane & 3;
+    // q . K^T for the tiles of the chunk
+    float sc[T][4];
+#pragma unroll
+    for (int t = 0; t < T; t++) {
+        constexpr int NW = Slice<D, BK>::NW;
+        uint32_t k0[NW], k1[NW];
+        load_k_slice<D, BK>(stg + (16 * t + g) * C::ROWK, tig, k0);
+        load_k_slice<D, BK>(stg + (16 * t + g + 8) * C::ROWK, tig, k1);
+        sc[t][0] = sc[t][1] = sc[t][2] = sc[t][3] = 0.f;
+#pragma unroll
+        for (int i = 0; i < NKS; i++)
+            mma_f16(sc[t], extract<BK>(k0, 2 * i), extract<BK>(k1, 2 * i), extract<BK>(k0, 2 * i + 1),
+                    extract<BK>(k1, 2 * i + 1), qb[i][0], qb[i][1]);
+    }
+    // logits of tokens 16t+g (k = 2t) and 16t+g+8 (k = 2t+1) for head tig
+    const uint8_t *smk = stg + C::KBYTES + C::VBYTES;
+    const uint8_t *smv = smk + C::MBYTES;
+    float lg[2 * T];
+#pragma unroll
+    for (int t = 0; t < T; t++)
+#pragma unroll
+        for (int hf = 0; hf < 2; hf++) {
+            const float2 km = ld_meta(smk, 16 * t + g + 8 * hf, M16);
+            const float dot = sc[t][2 * hf] + sc[t][2 * hf + 1];
+            lg[2 * t + hf] = (km.x * sk_l2) * dot + (km.y * qs_l2 + qm_l2);
+        }
+    const bool ragged = tok0 + C::CK > n_q;  // last chunk of the unit
+    if (ragged) {
+#pragma unroll
+        for (int k = 0; k < 2 * T; k++)
+            if (tok0 + 16 * (k >> 1) + g + 8 * (k & 1) >= n_q) lg[k] = -INFINITY;
+    }
+    float p[2 * T];
+    st.template update<2 * T>(lg, p);
+    // P . V per tile: A = V^T (channels x tokens), B = (P * s_v) transposed by
+    // movmatrix; the offsets o_v accumulate separately (Eq. 9)
+    float aos = 0.f;
+#pragma unroll
+    for (int t = 0; t < T; t++) {
+        float2 vm0 = ld_meta(smv, 16 * t + g, M16), vm1 = ld_meta(smv, 16 * t + g + 8, M16);
+        if (ragged) {  // masked tokens have p = 0, but their metadata may be anything
+            if (tok0 + 16 * t + g >= n_q) vm0 = make_float2(0.f, 0.f);
+            if (tok0 + 16 * t + g + 8 >= n_q) vm1 = make_float2(0.f, 0.f);
+        }
+        aos += p[2 * t] * vm0.y + p[2 * t + 1] * vm1.y;
+        const uint32_t b0 = movmatrix_t(hilo_f16(p[2 * t] * vm0.x));
+        const uint32_t b1 = movmatrix_t(hilo_f16(p[2 * t + 1] * vm1.x));
+        constexpr int NW = Slice<D, BV>::NW;
+        uint32_t v0[NW], v1[NW];
+        load_v_slice<D, BV>(stg + C::KBYTES + (8 * t + tig) * C::PAIRV, g, v0);
+        load_v_slice<D, BV>(stg + C::KBYTES + (8 * t + tig + 4) * C::PAIRV, g, v1);
+#pragma unroll
+        for (int mi = 0; mi < NMT; mi++)
+            mma_f16(st.acc[mi], extract<BV>(v0, 2 * mi), extract<BV>(v0, 2 * mi + 1), extract<BV>(v1, 2 * mi),
+                    extract<BV>(v1, 2 * mi + 1), b0, b1);
+    }
+    st.ao += aos;
+}
+
+// One 16-bit tile (16 slots) already in shared memory -> warp state.  Rows are
+// read with 16-byte vectors; the resulting channel order is folded into the q
+// operand (PermRawK) and into the output rows (raw_v_channel).
 template <int D, bool BF16>
-__device__ __forceinline__ void raw_part(const AttnArgs &a, const AttnShape &sh, const float (*q_raw)[D], int u,
-                                         int t0, int t1, WarpState<D / 16> &st) {
-    constexpr int NKS = D / 16, NMT = D / 16;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int g = lane >> 2, tig = lane & 3;
-    uint32_t qb[NKS][2];
-    build_qb<D, 2, false, BF16>(q_raw, qb);
-    const uint16_t *rk = a.raw_k + static_cast<long long>(u) * sh.rcap * D;
-    const uint32_t *rv = reinterpret_cast<const uint32_t *>(a.raw_v + static_cast<long long>(u) * sh.rcap * D);
+__device__ __noinline__ void process_raw(const AttnArgs &a, const uint8_t *tile, long long s0,
+                                         const uint32_t (&qb)[D / 16][2], WarpState<D / 16> &st) {
+    constexpr int NKS = D / 16, NMT = D / 16, NV = D / 32;
+    const int lane = threadIdx.x & 31, g = lane >> 2, tig = lane & 3;
     // slot validity at length seq_len: sink slot s < min(seq_len, n_sink); ring
     // slot n_sink + r holds the latest token t < seq_len with t mod n_recent == r,
     // valid when that token is not itself a sink
-    auto valid = [&](int slot) -> bool {
+    auto valid = [&](long long slot) -> bool {
         if (slot >= a.n_raw_slots) return false;
         if (slot < a.n_sink_cfg) return slot < a.n_sink_eff;
         const long long r = slot - a.n_sink_cfg;
@@ -375,99 +399,76 @@ __device__ __forceinline__ void raw_part(const AttnArgs &a, const AttnShape &sh,
         const long long tr = a.seq_len - 1 - (back % a.n_recent_cfg);
         return tr >= a.n_sink_cfg;
     };
-    for (int tile = t0 + warp; tile < t1; tile += 4) {
-        const int s0 = tile * RTILE;
-        float sc[4] = {0.f, 0.f, 0.f, 0.f};
-        const uint16_t *k0 = rk + static_cast<long long>(s0 + g) * D;
-        const uint16_t *k1 = rk + static_cast<long long>(s0 + g + 8) * D;
+    const uint8_t *rowA = tile + g * D * 2, *rowB = tile + (g + 8) * D * 2;
+    float sc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int i = 0; i < NKS; i++) {
-            const int c = 16 * i + 2 * tig;
-            const uint32_t a0 = __ldg(reinterpret_cast<const unsigned *>(k0 + c));
-            const uint32_t a1 = __ldg(reinterpret_cast<const unsigned *>(k1 + c));
-            const uint32_t a2 = __ldg(reinterpret_cast<const unsigned *>(k0 + c + 8));
-            const uint32_t a3 = __ldg(reinterpret_cast<const unsigned *>(k1 + c + 8));
+    for (int j = 0; j < NV; j++) {
+        const uint4 kA = *reinterpret_cast<const uint4 *>(rowA + 64 * j + 16 * tig);
+        const uint4 kB = *reinterpret_cast<const uint4 *>(rowB + 64 * j + 16 * tig);
+#pragma unroll
+        for (int ii = 0; ii < 2; ii++) {
+            const int i = 2 * j + ii, r = 2 * ii;
+            if (i >= NKS) break;
+            const uint32_t a0 = vec_word(kA, r), a1 = vec_word(kB, r);
+            const uint32_t a2 = vec_word(kA, r + 1), a3 = vec_word(kB, r + 1);
             if (BF16) mma_bf16(sc, a0, a1, a2, a3, qb[i][0], qb[i][1]);
             else mma_f16(sc, a0, a1, a2, a3, qb[i][0], qb[i][1]);
         }
-        float lg[2];
-        lg[0] = valid(s0 + g) ? a.sm_log2 * (sc[0] + sc[1]) : -INFINITY;
-        lg[1] = valid(s0 + g + 8) ? a.sm_log2 * (sc[2] + sc[3]) : -INFINITY;
-        float p[2];
-        st.template update<2>(lg, p);
-        const uint32_t b0 = movmatrix_t(BF16 ? hilo_bf16(p[0]) : hilo_f16(p[0]));
-        const uint32_t b1 = movmatrix_t(BF16 ? hilo_bf16(p[1]) : hilo_f16(p[1]));
-        // values: pair-interleaved; zero the halves of invalid slots (their bits
-        // may be anything, and 0 * NaN would poison the accumulator)
-        const uint32_t m0 = (valid(s0 + 2 * tig) ? 0x0000ffffu : 0u) | (valid(s0 + 2 * tig + 1) ? 0xffff0000u : 0u);
-        const uint32_t m1 =
-            (valid(s0 + 2 * tig + 8) ? 0x0000ffffu : 0u) | (valid(s0 + 2 * tig + 9) ? 0xffff0000u : 0u);
-        const uint32_t *vp0 = rv + static_cast<long long>(s0 / 2 + tig) * D;
-        const uint32_t *vp1 = rv + static_cast<long long>(s0 / 2 + tig + 4) * D;
+    }
+    float lg[2];
+    lg[0] = valid(s0 + g) ? a.sm_log2 * (sc[0] + sc[1]) : -INFINITY;
+    lg[1] = valid(s0 + g + 8) ? a.sm_log2 * (sc[2] + sc[3]) : -INFINITY;
+    float p[2];
+    st.template update<2>(lg, p);
+    const uint32_t b0 = movmatrix_t(BF16 ? hilo_bf16(p[0]) : hilo_f16(p[0]));
+    const uint32_t b1 = movmatrix_t(BF16 ? hilo_bf16(p[1]) : hilo_f16(p[1]));
+    // zero the halves of invalid slots (their bits may be anything, and
+    // 0 * NaN would poison the accumulator)
+    const uint32_t m0 = (valid(s0 + 2 * tig) ? 0x0000ffffu : 0u) | (valid(s0 + 2 * tig + 1) ? 0xffff0000u : 0u);
+    const uint32_t m1 = (valid(s0 + 2 * tig + 8) ? 0x0000ffffu : 0u) | (valid(s0 + 2 * tig + 9) ? 0xffff0000u : 0u);
+    const uint8_t *pA = tile + 32 * D + tig * D * 4 + (D / 8) * g * 4;
+    const uint8_t *pB = tile + 32 * D + (tig + 4) * D * 4 + (D / 8) * g * 4;
+    uint4 vA[NV], vB[NV];
 #pragma unroll
-        for (int mi = 0; mi < NMT; mi++) {
-            const int c = 16 * mi + g;
-            const uint32_t a0 = __ldg(vp0 + c) & m0, a1 = __ldg(vp0 + c + 8) & m0;
-            const uint32_t a2 = __ldg(vp1 + c) & m1, a3 = __ldg(vp1 + c + 8) & m1;
-            if (BF16) mma_bf16(st.acc[mi], a0, a1, a2, a3, b0, b1);
-            else mma_f16(st.acc[mi], a0, a1, a2, a3, b0, b1);
-        }
+    for (int j = 0; j < NV; j++) {
+        vA[j] = *reinterpret_cast<const uint4 *>(pA + 16 * j);
+        vB[j] = *reinterpret_cast<const uint4 *>(pB + 16 * j);
+    }
+#pragma unroll
+    for (int mi = 0; mi < NMT; mi++) {
+        const int k0 = 2 * mi, k1 = 2 * mi + 1;  // channel (D/8)g + k of this lane's vectors
+        const uint32_t a0 = vec_word(vA[k0 >> 2], k0 & 3) & m0, a1 = vec_word(vA[k1 >> 2], k1 & 3) & m0;
+        const uint32_t a2 = vec_word(vB[k0 >> 2], k0 & 3) & m1, a3 = vec_word(vB[k1 >> 2], k1 & 3) & m1;
+        if (BF16) mma_bf16(st.acc[mi], a0, a1, a2, a3, b0, b1);
+        else mma_f16(st.acc[mi], a0, a1, a2, a3, b0, b1);
     }
 }
 
-// Warp state -> smem merge area (head tig), then CTA merge -> global record.
-template <int D, int BK, int BV, bool M16>
-__device__ __forceinline__ void write_record(Smem<D, BK, BV, M16> &S, WarpState<D / 16> &st, bool quant,
-                                             float *rec) {
-    using C = Cfg<D, BK, BV, M16>;
-    constexpr int NMT = C::NMT, PR = C::PR;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int g = lane >> 2, tig = lane & 3;
+// Warp state -> [acc[D], m, l] of head tig at `dst` (stride PR per head).
+// Packed tokens: undo the operand scaling and add the value offsets; 16-bit
+// tokens: put each row back at its channel.
+template <int D, int BV>
+__device__ __forceinline__ void store_state(WarpState<D / 16> &st, bool quant, float *dst, int PR) {
+    constexpr int NMT = D / 16;
+    const int lane = threadIdx.x & 31, g = lane >> 2, tig = lane & 3;
 #pragma unroll
     for (int o = 4; o < 32; o <<= 1) {
         st.l += __shfl_xor_sync(FULL, st.l, o);
         st.ao += __shfl_xor_sync(FULL, st.ao, o);
     }
-    float *wp = &S.merge[warp][tig][0];
+    float *wp = dst + tig * PR;
 #pragma unroll
     for (int mi = 0; mi < NMT; mi++)
 #pragma unroll
         for (int rr = 0; rr < 2; rr++) {
-            const int c = 16 * mi + 8 * rr + g;
-            float v = st.acc[mi][2 * rr] + st.acc[mi][2 * rr + 1];
-            if (quant) v = v * exp2f(static_cast<float>(24 - field_exp(2 * mi + rr, BV))) + st.ao;
-            wp[2 + c] = v;
+            const int row = 16 * mi + 8 * rr + g;
+            const float v = st.acc[mi][2 * rr] + st.acc[mi][2 * rr + 1];
+            if (quant) wp[row] = v * exp2f(static_cast<float>(24 - field_exp(2 * mi + rr, BV))) + st.ao;
+            else wp[raw_v_channel<D>(row)] = v;
         }
     if (g == 0) {
-        wp[0] = st.m;
-        wp[1] = st.l;
-    }
-    __syncthreads();
-    for (int idx = threadIdx.x; idx < 4 * PR; idx += blockDim.x) {
-        const int h = idx / PR, c = idx % PR;
-        float M = -INFINITY;
-#pragma unroll
-        for (int w = 0; w < 4; w++) M = fmaxf(M, S.merge[w][h][0]);
-        float v;
-        if (c == 0) {
-            v = M;
-        } else {
-            v = 0.f;
-#pragma unroll
-            for (int w = 0; w < 4; w++) {
-                const float mw = S.merge[w][h][0];
-                if (mw != -INFINITY) v += S.merge[w][h][c] * exp2f(mw - M);
-            }
-        }
-        rec[idx] = v;
-    }
-    __syncthreads();
-}
-
-__device__ __forceinline__ void write_empty(float *rec, int PR) {
-    if (threadIdx.x < 4) {
-        rec[threadIdx.x * PR] = -INFINITY;
-        rec[threadIdx.x * PR + 1] = 0.f;
+        wp[D] = st.m;
+        wp[D + 1] = st.l;
     }
 }
 
@@ -476,23 +477,97 @@ __device__ __forceinline__ int owner(long long x, long long N, int G) {
     return static_cast<int>(((x + 1) * G + N - 1) / N) - 1;
 }
 
+template <int V>
+struct VecT;
+template <>
+struct VecT<4> {
+    using T = float4;
+};
+template <>
+struct VecT<2> {
+    using T = float2;
+};
+__device__ __forceinline__ void vadd(float (&acc)[4], const float4 &v, float w) {
+    acc[0] += v.x * w; acc[1] += v.y * w; acc[2] += v.z * w; acc[3] += v.w * w;
+}
+__device__ __forceinline__ void vadd(float (&acc)[2], const float2 &v, float w) {
+    acc[0] += v.x * w; acc[1] += v.y * w;
+}
+
+// The last CTA of a unit: merge its split records, rotate the value
+// accumulator back, normalize and write the output; reset the ticket.
+template <int D, int PR>
+__device__ __noinline__ void combine_unit(const AttnArgs &a, const AttnShape &sh, int u, int n_ctas) {
+    constexpr int V = D / 32;
+    using VT = typename VecT<V>::T;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int b = u / sh.Hkv, kvh = u % sh.Hkv;
+    const int h = warp;
+    if (h < sh.G) {
+        const float *pu = a.partials + static_cast<long long>(u) * a.max_slots * 2 * 4 * PR + h * PR;
+        const int n_rec = 2 * n_ctas;  // record r: kind r & 1 (0: 16-bit, 1: packed)
+        float M = -INFINITY;
+#pragma unroll 4
+        for (int r = 0; r < n_rec; r++) M = fmaxf(M, __ldcg(pu + r * 4 * PR + D));
+        float Lsum = 0.f;
+        float accq[V], accr[V];
+#pragma unroll
+        for (int j = 0; j < V; j++) accq[j] = accr[j] = 0.f;
+#pragma unroll 4
+        for (int r = 0; r < n_rec; r++) {
+            const float *p = pu + r * 4 * PR;
+            const float mr = __ldcg(p + D), lr = __ldcg(p + D + 1);
+            const VT vv = __ldcg(reinterpret_cast<const VT *>(p) + lane);
+            const float wgt = mr == -INFINITY ? 0.f : exp2f(mr - M);
+            Lsum += lr * wgt;
+            if (r & 1) vadd(accq, vv, wgt);
+            else vadd(accr, vv, wgt);
+        }
+        if (a.rot_v == DQ_ROT_HADAMARD) {
+            fwht_warp<V>(accq);
+#pragma unroll
+            for (int j = 0; j < V; j++) accq[j] *= a.hscale;
+        }
+        const float inv = 1.f / Lsum;
+        const long long ob = (static_cast<long long>(b) * sh.Hkv * sh.G + kvh * sh.G + h) * D;
+#pragma unroll
+        for (int j = 0; j < V; j++) {
+            const float y = (accq[j] + accr[j]) * inv;
+            const long long oi = ob + lane * V + j;
+            if (a.out_dtype == DQ_F32) reinterpret_cast<float *>(a.out)[oi] = y;
+            else if (a.out_dtype == DQ_F16) reinterpret_cast<__half *>(a.out)[oi] = __float2half_rn(y);
+            else reinterpret_cast<__nv_bfloat16 *>(a.out)[oi] = __float2bfloat16_rn(y);
+        }
+    }
+    if (threadIdx.x == 0) a.counters[u] = 0;
+}
+
 // ---- the kernel ----------------------------------------------------------------
+// A CTA walks its item range unit by unit.  In each unit segment, warp 0 first
+// runs the segment's 16-bit tiles (if any) while warps 1-3 start on packed
+// chunks; chunks are handed out one at a time from a shared counter, so the
+// warps finish together.  Each warp streams its chunks through its own 2-deep
+// ring of bulk copies.
 template <int D, int BK, int BV, bool M16>
 __global__ void __launch_bounds__(128, Cfg<D, BK, BV, M16>::MINB) attn_kernel(AttnArgs a, AttnShape sh) {
     using C = Cfg<D, BK, BV, M16>;
-    constexpr int V = D / 32, PR = C::PR;
+    constexpr int V = D / 32, PR = C::PR, NKS = C::NKS;
     extern __shared__ __align__(128) uint8_t smem_raw[];
     Smem<D, BK, BV, M16> &S = *reinterpret_cast<Smem<D, BK, BV, M16> *>(smem_raw);
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tig = lane & 3;
     const int G = gridDim.x, i = blockIdx.x;
     const long long N = a.total_items, ipu = a.items_per_unit;
     const long long x0 = static_cast<long long>(i) * N / G, x1 = static_cast<long long>(i + 1) * N / G;
+    uint8_t *ring0 = S.ring[warp];
+    uint64_t *bars = S.bars[warp];
 
     if (lane == 0) {
-        for (int s = 0; s < C::NST; s++) mbar_init(&S.bars[warp][s], 1);
+        for (int s = 0; s < C::NST; s++) mbar_init(&bars[s], 1);
         fence_mbar_init();
     }
     __syncwarp();
+    uint32_t phase = 0;  // bit s: parity of the next completion of bars[s]
+    bool timed_out = false;
 
     for (long long x = x0; x < x1;) {
         const int u = static_cast<int>(x / ipu);
@@ -500,9 +575,45 @@ __global__ void __launch_bounds__(128, Cfg<D, BK, BV, M16>::MINB) attn_kernel(At
         const long long s0 = x - ub, s1 = (x1 < ub + ipu ? x1 : ub + ipu) - ub;
         x = ub + s1;
         const int b = u / sh.Hkv, kvh = u % sh.Hkv;
+        // items of a unit are its packed chunks; its 16-bit tiles ride along,
+        // tile r with chunk floor(r * n_qc / n_rt) (all tiles if it has no chunks)
+        long long q0 = 0, q1 = 0, r0, r1;
+        if (a.n_qc > 0) {
+            q0 = s0;
+            q1 = s1;
+            r0 = (s0 * a.n_rt + a.n_qc - 1) / a.n_qc;
+            r1 = (s1 * a.n_rt + a.n_qc - 1) / a.n_qc;
+        } else {
+            r0 = s0;
+            r1 = s1;
+        }
+        const int n_chunks = static_cast<int>(q1 - q0);
+        const bool raw_warp = warp == 0 && r0 < r1;
+
+        __syncthreads();  // the previous segment is done with the shared state
+        if (threadIdx.x == 0) S.next_chunk = 0;
+        __syncthreads();
+        // start the first copies before anything else
+        auto grab = [&]() -> int {
+            int v = 0;
+            if (lane == 0) v = atomicAdd(&S.next_chunk, 1);
+            v = __shfl_sync(FULL, v, 0);
+            return v < n_chunks ? v : -1;
+        };
+        int cq0 = -1, cq1 = -1;  // chunk (relative to q0) in flight in stage 0 / 1
+        auto start_chunks = [&]() {
+            cq0 = grab();
+            if (cq0 >= 0 && lane == 0) issue_chunk<D, BK, BV, M16>(a, sh, u, q0 + cq0, (S.ring[warp] + 0), &bars[0]);
+            cq1 = cq0 >= 0 ? grab() : -1;
+            if (cq1 >= 0 && lane == 0) issue_chunk<D, BK, BV, M16>(a, sh, u, q0 + cq1, (S.ring[warp] + C::STAGE), &bars[1]);
+        };
+        if (raw_warp) {
+            if (lane == 0) issue_raw<D>(a, sh, u, r0, ring0, &bars[0]);
+        } else {
+            start_chunks();
+        }
 
         // ---- query preparation: warp h handles query head h of this KV head ----
-        __syncthreads();
         {
             const int h = warp;
             float xq[V];
@@ -550,38 +661,82 @@ __global__ void __launch_bounds__(128, Cfg<D, BK, BV, M16>::MINB) attn_kernel(At
 
         const int first = owner(ub, N, G), last = owner(ub + ipu - 1, N, G);
         float *recs = a.partials + (static_cast<long long>(u) * a.max_slots + (i - first)) * 2 * 4 * PR;
-        // ---- 16-bit slots: items [0, n_rt) of the unit ----
-        const long long r0 = s0, r1 = s1 < a.n_rt ? s1 : a.n_rt;
-        if (r0 < r1) {
-            WarpState<D / 16> st;
+        WarpState<D / 16> st;
+
+        // ---- 16-bit tiles (warp 0): record kind 0 ----
+        if (raw_warp) {
+            uint32_t qb[NKS][2];
+            if (a.raw_bf16) build_qb<D, 2, false, true>(S.q_raw, qb, PermRawK());
+            else build_qb<D, 2, false, false>(S.q_raw, qb, PermRawK());
             st.init();
-            if (a.raw_bf16) raw_part<D, true>(a, sh, S.q_raw, u, static_cast<int>(r0), static_cast<int>(r1), st);
-            else raw_part<D, false>(a, sh, S.q_raw, u, static_cast<int>(r0), static_cast<int>(r1), st);
-            write_record<D, BK, BV, M16>(S, st, false, recs);
-        } else {
-            write_empty(recs, PR);
-        }
-        // ---- packed chunks: items [n_rt, ipu) ----
-        const long long q0 = (s0 > a.n_rt ? s0 : a.n_rt) - a.n_rt, q1 = s1 - a.n_rt;
-        if (q0 < q1) {
-            WarpState<D / 16> st;
-            st.init();
-            quant_part<D, BK, BV, M16>(a, sh, S, u, q0, q1, st);
-            write_record<D, BK, BV, M16>(S, st, true, recs + 4 * PR);
-            // the ring restarts at stage 0 for the next segment: re-arm the barriers
-            if (lane == 0) {
-                for (int s = 0; s < C::NST; s++) {
-                    asm volatile("mbarrier.inval.shared::cta.b64 [%0];\n" ::"r"(smem_u32(&S.bars[warp][s])));
-                    mbar_init(&S.bars[warp][s], 1);
+            for (long long r = r0; r < r1; r++) {
+                if (!mbar_wait(&bars[0], phase & 1u, WAIT_LIMIT_NS)) timed_out = true;
+                phase ^= 1u;
+                if (a.raw_bf16) process_raw<D, true>(a, ring0, r * RTILE, qb, st);
+                else process_raw<D, false>(a, ring0, r * RTILE, qb, st);
+                __syncwarp();
+                if (lane == 0 && r + 1 < r1) {
+                    fence_proxy_async();
+                    issue_raw<D>(a, sh, u, r + 1, ring0, &bars[0]);
                 }
-                fence_mbar_init();
             }
+            store_state<D, BV>(st, false, recs, PR);
             __syncwarp();
-        } else {
-            write_empty(recs + 4 * PR, PR);
+            start_chunks();  // warp 0 joins the packed chunks
+        } else if (warp == 0 && lane < 4) {
+            recs[lane * PR + D] = -INFINITY;  // no 16-bit tiles in this segment
+            recs[lane * PR + D + 1] = 0.f;
         }
 
-        // ---- ticket: the last CTA of the unit merges its records ----
+        // ---- packed chunks: all warps, handed out one at a time ----
+        st.init();
+        if (cq0 >= 0) {
+            uint32_t qb[NKS][2];
+            build_qb<D, BK, true, false>(S.q_rot, qb, PermIdentity());
+            const float qs_l2 = a.sm_log2 * S.qsum[tig], qm_l2 = a.sm_log2 * S.qmu[tig];
+            const float sk_l2 = a.sm_log2 * 16777216.0f;  // 2^24 undoes the operand scaling
+            const long long n_q = a.n_q;
+            int s = 0;
+            for (;;) {
+                const int cur = s ? cq1 : cq0;
+                if (cur < 0) break;
+                if (!mbar_wait(&bars[s], (phase >> s) & 1u, WAIT_LIMIT_NS)) timed_out = true;
+                phase ^= 1u << s;
+                const uint8_t *stg = S.ring[warp] + s * C::STAGE;
+                process_chunk<D, BK, BV, M16>(stg, (q0 + cur) * C::CK, n_q, qb, sk_l2, qs_l2, qm_l2, st);
+                __syncwarp();
+                const int nxt = grab();
+                if (nxt >= 0 && lane == 0) {
+                    fence_proxy_async();
+                    issue_chunk<D, BK, BV, M16>(a, sh, u, q0 + nxt, S.ring[warp] + s * C::STAGE, &bars[s]);
+                }
+                if (s) cq1 = nxt;
+                else cq0 = nxt;
+                s ^= 1;
+            }
+        }
+        store_state<D, BV>(st, true, &S.merge[warp][0][0], PR);
+        __syncthreads();
+        // CTA merge of the 4 warps -> record kind 1
+        for (int idx = threadIdx.x; idx < 4 * PR; idx += blockDim.x) {
+            const int h = idx / PR, c = idx % PR;
+            float M = -INFINITY;
+#pragma unroll
+            for (int w = 0; w < 4; w++) M = fmaxf(M, S.merge[w][h][D]);
+            float v = 0.f;
+            if (c == D) {
+                v = M;
+            } else if (c < D + 2) {
+#pragma unroll
+                for (int w = 0; w < 4; w++) {
+                    const float mw = S.merge[w][h][D];
+                    if (mw != -INFINITY) v += S.merge[w][h][c] * exp2f(mw - M);
+                }
+            }
+            recs[4 * PR + idx] = v;
+        }
+
+        // ---- ticket: the last CTA of the unit merges the records ----
         __threadfence();
         __syncthreads();
         if (threadIdx.x == 0) {
@@ -591,55 +746,15 @@ __global__ void __launch_bounds__(128, Cfg<D, BK, BV, M16>::MINB) attn_kernel(At
         __syncthreads();
         if (!S.last) continue;
         __threadfence();
-        {
-            const int h = warp;
-            if (h < sh.G) {
-                const float *pu = a.partials + static_cast<long long>(u) * a.max_slots * 2 * 4 * PR;
-                const int n_rec = 2 * (last - first + 1);
-                float M = -INFINITY;
-                for (int r = 0; r < n_rec; r++) M = fmaxf(M, __ldcg(pu + (r * 4 + h) * PR));
-                float Lsum = 0.f;
-                float accq[V], accr[V];
-#pragma unroll
-                for (int j = 0; j < V; j++) accq[j] = accr[j] = 0.f;
-                for (int r = 0; r < n_rec; r++) {
-                    const float *p = pu + (r * 4 + h) * PR;
-                    const float mr = __ldcg(p);
-                    if (mr == -INFINITY) continue;
-                    const float wgt = exp2f(mr - M);
-                    Lsum += __ldcg(p + 1) * wgt;
-                    const bool is_raw = (r & 1) == 0;
-#pragma unroll
-                    for (int j = 0; j < V; j++) {
-                        const float v = __ldcg(p + 2 + lane * V + j) * wgt;
-                        if (is_raw) accr[j] += v;
-                        else accq[j] += v;
-                    }
-                }
-                if (a.rot_v == DQ_ROT_HADAMARD) {
-                    fwht_warp<V>(accq);
-#pragma unroll
-                    for (int j = 0; j < V; j++) accq[j] *= a.hscale;
-                }
-                const float inv = 1.f / Lsum;
-                const long long ob = (static_cast<long long>(b) * sh.Hkv * sh.G + kvh * sh.G + h) * D;
-#pragma unroll
-                for (int j = 0; j < V; j++) {
-                    const float y = (accq[j] + accr[j]) * inv;
-                    const long long oi = ob + lane * V + j;
-                    if (a.out_dtype == DQ_F32) reinterpret_cast<float *>(a.out)[oi] = y;
-                    else if (a.out_dtype == DQ_F16) reinterpret_cast<__half *>(a.out)[oi] = __float2half_rn(y);
-                    else reinterpret_cast<__nv_bfloat16 *>(a.out)[oi] = __float2bfloat16_rn(y);
-                }
-            }
-            if (threadIdx.x == 0) a.counters[u] = 0;
-        }
+        combine_unit<D, PR>(a, sh, u, last - first + 1);
     }
+    if (timed_out && lane == 0) atomicOr(a.status, ST_TIMEOUT);
 }
 
 // ---- host side -------------------------------------------------------------
 template <int D, int BK, int BV, bool M16>
 struct Launcher {
+    static constexpr int CK = Cfg<D, BK, BV, M16>::CK;
     static int occupancy;  // resident CTAs per SM, set on first use
     static size_t smem() { return sizeof(Smem<D, BK, BV, M16>); }
     static int prepare() {
@@ -678,20 +793,23 @@ static int dispatch(const Layout &L, F &&f) {
 }
 
 long long attention_partial_floats(const Layout &L, const AttnArgs &a) {
-    return static_cast<long long>(L.U) * a.max_slots * 2 * 4 * (L.d + 2);
+    return static_cast<long long>(L.U) * a.max_slots * 2 * 4 * (L.d + 4);
 }
 
 int plan_attention(const Layout &L, AttnArgs &a, int num_sms, long long cap_floats) {
-    int occ = 0;
+    int occ = 0, ck = 0;
     const int e = dispatch(L, [&](auto l) {
         const int r = decltype(l)::prepare();
         occ = decltype(l)::occupancy;
+        ck = decltype(l)::CK;
         return r;
     });
     if (e != 0) return e;
     a.n_rt = a.has_raw ? (a.n_raw_slots + RTILE - 1) / RTILE : 0;
-    a.n_qc = (a.n_q + CHUNK - 1) / CHUNK;
-    a.items_per_unit = a.n_rt + a.n_qc;
+    a.n_qc = (a.n_q + ck - 1) / ck;
+    // a unit's items are its packed chunks (its 16-bit tiles ride along with
+    // them), or its 16-bit tiles when it has no packed tokens
+    a.items_per_unit = a.n_qc > 0 ? a.n_qc : a.n_rt;
     a.total_items = static_cast<long long>(L.U) * a.items_per_unit;
     long long G = static_cast<long long>(num_sms) * occ;
     if (const char *env = std::getenv("DQ_ATTN_GRID")) G = std::atoll(env);

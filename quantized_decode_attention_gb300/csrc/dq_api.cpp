@@ -146,9 +146,9 @@ static dq_status get_ctx(dq_ctx **pctx, const dq_config *cfg, const Layout &L) {
     }
     // split partials for the largest persistent grid the attention kernel can
     // use (at most 8 CTAs per SM): a unit is touched by at most 2G/U + 2 CTAs,
-    // each writing two records of 4 heads x (head_dim + 2) floats
+    // each writing two records of 4 heads x (head_dim + 4) floats
     const long long G = 8LL * c->num_sms;
-    c->partials_cap = static_cast<size_t>((2 * G + 2LL * L.U) * 2 * 4 * (L.d + 2));
+    c->partials_cap = static_cast<size_t>((2 * G + 2LL * L.U) * 2 * 4 * (L.d + 4));
     cudaError_t e1 = cudaMalloc(&c->status, sizeof(unsigned));
     cudaError_t e2 = cudaMalloc(&c->partials, c->partials_cap * sizeof(float));
     cudaError_t e3 = cudaMalloc(&c->counters, sizeof(int) * L.U);
