@@ -52,8 +52,9 @@ struct AttnShape {
 
 template <int D, int BK, int BV, bool M16>
 struct Cfg {
-    static constexpr int CK = 32;  // tokens per packed work item (chunk)
-    static constexpr int TILES = CK / 16;
+    static constexpr int CK = BK == 4 ? 32 : 64;  // tokens per packed work item (chunk)
+    static constexpr int SUB = 32;                // tokens per softmax step within a chunk
+    static constexpr int TILES = SUB / 16;
     static constexpr int ROWK = D * BK / 8;
     static constexpr int PAIRV = 2 * D * BV / 8;
     static constexpr int MB = M16 ? 2 : 4;
@@ -194,7 +195,7 @@ struct WarpState {
         const bool grow = mx > m + RESCALE_SLACK;  // also true for the first finite logit
         if (__any_sync(FULL, grow)) {
             const float mn = grow ? mx : m;
-            const float al = grow ? exp2f(m - mn) : 1.f;  // 0 when m was -inf
+            const float al = grow ? ex2(m - mn) : 1.f;  // 0 when m was -inf
             m = mn;
             l *= al;
             ao *= al;
@@ -210,7 +211,7 @@ struct WarpState {
         float sum = 0.f;
 #pragma unroll
         for (int k = 0; k < NT; k++) {
-            p[k] = exp2f(lg[k] - mu);
+            p[k] = ex2(lg[k] - mu);
             sum += p[k];
         }
         l += sum;
@@ -221,9 +222,9 @@ struct WarpState {
 template <int D, int BK, int BV, bool M16>
 struct Smem {
     using C = Cfg<D, BK, BV, M16>;
-    float q_raw[4][D];
-    float q_rot[4][D];
-    float qsum[4], qmu[4];
+    float q_raw[2][4][D];      // prepared queries of up to two units at a time
+    float q_rot[2][4][D];
+    float qsum[2][4], qmu[2][4];
     float merge[4][4][C::PR];  // [warp][head][acc[D], m, l, -, -]
     uint64_t bars[4][C::NST];
     int next_chunk;            // chunks of the current segment handed out so far
@@ -231,22 +232,37 @@ struct Smem {
     alignas(128) uint8_t ring[4][C::RING];  // per warp: stage s at s * STAGE
 };
 
-// Bulk-copy packed chunk c (of CK tokens) of unit u into a stage.
+// Global sources of one unit's packed records, and the bulk copy of chunk c
+// into a stage, issued by one elected lane without branching the warp.
 template <int D, int BK, int BV, bool M16>
-__device__ __forceinline__ void issue_chunk(const AttnArgs &a, const AttnShape &sh, int u, long long c,
-                                            uint8_t *stage, uint64_t *bar) {
-    using C = Cfg<D, BK, BV, M16>;
-    const long long t0 = c * C::CK;
-    const uint8_t *ck = a.codes_k + (static_cast<long long>(u) * sh.qcap + t0) * C::ROWK;
-    const uint8_t *cv = a.codes_v + (static_cast<long long>(u) * (sh.qcap / 2) + t0 / 2) * C::PAIRV;
-    const uint8_t *mk = static_cast<const uint8_t *>(a.meta_k) + (static_cast<long long>(u) * sh.qcap + t0) * 2 * C::MB;
-    const uint8_t *mv = static_cast<const uint8_t *>(a.meta_v) + (static_cast<long long>(u) * sh.qcap + t0) * 2 * C::MB;
-    mbar_expect_tx(bar, C::STAGE);
-    bulk_g2s(stage, ck, C::KBYTES, bar);
-    bulk_g2s(stage + C::KBYTES, cv, C::VBYTES, bar);
-    bulk_g2s(stage + C::KBYTES + C::VBYTES, mk, C::MBYTES, bar);
-    bulk_g2s(stage + C::KBYTES + C::VBYTES + C::MBYTES, mv, C::MBYTES, bar);
-}
+struct ChunkSrc {
+    const uint8_t *ck, *cv, *mk, *mv;
+    __device__ __forceinline__ ChunkSrc(const AttnArgs &a, const AttnShape &sh, int u) {
+        using C = Cfg<D, BK, BV, M16>;
+        ck = a.codes_k + static_cast<long long>(u) * sh.qcap * C::ROWK;
+        cv = a.codes_v + static_cast<long long>(u) * (sh.qcap / 2) * C::PAIRV;
+        mk = static_cast<const uint8_t *>(a.meta_k) + static_cast<long long>(u) * sh.qcap * 2 * C::MB;
+        mv = static_cast<const uint8_t *>(a.meta_v) + static_cast<long long>(u) * sh.qcap * 2 * C::MB;
+    }
+    __device__ __forceinline__ void issue(long long c, uint8_t *stage, uint64_t *bar) const {
+        using C = Cfg<D, BK, BV, M16>;
+        const uint32_t t0 = static_cast<uint32_t>(c) * C::CK;
+        const uint32_t sb = smem_u32(stage), br = smem_u32(bar);
+        asm volatile(
+            "{\n .reg .pred p;\n elect.sync _|p, 0xffffffff;\n"
+            "@p fence.proxy.async.shared::cta;\n"
+            "@p mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n"
+            "@p cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%2], [%3], %4, [%0];\n"
+            "@p cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%5], [%6], %7, [%0];\n"
+            "@p cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%8], [%9], %10, [%0];\n"
+            "@p cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%11], [%12], %10, [%0];\n}\n" ::"r"(br),
+            "r"(C::STAGE), "r"(sb), "l"(ck + static_cast<uint64_t>(t0) * C::ROWK), "r"(C::KBYTES),
+            "r"(sb + C::KBYTES), "l"(cv + static_cast<uint64_t>(t0 / 2) * C::PAIRV), "r"(C::VBYTES),
+            "r"(sb + C::KBYTES + C::VBYTES), "l"(mk + static_cast<uint64_t>(t0) * 2 * C::MB), "r"(C::MBYTES),
+            "r"(sb + C::KBYTES + C::VBYTES + C::MBYTES), "l"(mv + static_cast<uint64_t>(t0) * 2 * C::MB)
+            : "memory");
+    }
+};
 
 // Bulk-copy 16-bit tile r (16 slots: keys then value pairs) of unit u.
 template <int D>
@@ -312,22 +328,24 @@ __device__ __forceinline__ uint32_t vec_word(const uint4 &v, int r) {
     return r == 0 ? v.x : (r == 1 ? v.y : (r == 2 ? v.z : v.w));
 }
 
-// One packed chunk already in shared memory (stage stg) -> warp state.
+// SUB packed tokens already in shared memory -> warp state.  `stg` is the
+// stage, `o` the first token of the block within the chunk, `tok0` the token
+// index of the block within the unit.
 template <int D, int BK, int BV, bool M16>
-__device__ __forceinline__ void process_chunk(const uint8_t *stg, long long tok0, long long n_q,
+__device__ __forceinline__ void process_block(const uint8_t *stg, int o, long long tok0, long long n_q,
                                               const uint32_t (&qb)[D / 16][2], float sk_l2, float qs_l2, float qm_l2,
                                               WarpState<D / 16> &st) {
     using C = Cfg<D, BK, BV, M16>;
     constexpr int NKS = C::NKS, NMT = C::NMT, T = C::TILES;
     const int lane = threadIdx.x & 31, g = lane >> 2, tig = lane & 3;
-    // q . K^T for the tiles of the chunk
+    // q . K^T for the tiles of the block
     float sc[T][4];
 #pragma unroll
     for (int t = 0; t < T; t++) {
         constexpr int NW = Slice<D, BK>::NW;
         uint32_t k0[NW], k1[NW];
-        load_k_slice<D, BK>(stg + (16 * t + g) * C::ROWK, tig, k0);
-        load_k_slice<D, BK>(stg + (16 * t + g + 8) * C::ROWK, tig, k1);
+        load_k_slice<D, BK>(stg + (o + 16 * t + g) * C::ROWK, tig, k0);
+        load_k_slice<D, BK>(stg + (o + 16 * t + g + 8) * C::ROWK, tig, k1);
         sc[t][0] = sc[t][1] = sc[t][2] = sc[t][3] = 0.f;
 #pragma unroll
         for (int i = 0; i < NKS; i++)
@@ -342,11 +360,11 @@ __device__ __forceinline__ void process_chunk(const uint8_t *stg, long long tok0
     for (int t = 0; t < T; t++)
 #pragma unroll
         for (int hf = 0; hf < 2; hf++) {
-            const float2 km = ld_meta(smk, 16 * t + g + 8 * hf, M16);
+            const float2 km = ld_meta(smk, o + 16 * t + g + 8 * hf, M16);
             const float dot = sc[t][2 * hf] + sc[t][2 * hf + 1];
             lg[2 * t + hf] = (km.x * sk_l2) * dot + (km.y * qs_l2 + qm_l2);
         }
-    const bool ragged = tok0 + C::CK > n_q;  // last chunk of the unit
+    const bool ragged = tok0 + C::SUB > n_q;  // last block of the unit
     if (ragged) {
 #pragma unroll
         for (int k = 0; k < 2 * T; k++)
@@ -359,7 +377,7 @@ __device__ __forceinline__ void process_chunk(const uint8_t *stg, long long tok0
     float aos = 0.f;
 #pragma unroll
     for (int t = 0; t < T; t++) {
-        float2 vm0 = ld_meta(smv, 16 * t + g, M16), vm1 = ld_meta(smv, 16 * t + g + 8, M16);
+        float2 vm0 = ld_meta(smv, o + 16 * t + g, M16), vm1 = ld_meta(smv, o + 16 * t + g + 8, M16);
         if (ragged) {  // masked tokens have p = 0, but their metadata may be anything
             if (tok0 + 16 * t + g >= n_q) vm0 = make_float2(0.f, 0.f);
             if (tok0 + 16 * t + g + 8 >= n_q) vm1 = make_float2(0.f, 0.f);
@@ -369,8 +387,8 @@ __device__ __forceinline__ void process_chunk(const uint8_t *stg, long long tok0
         const uint32_t b1 = movmatrix_t(hilo_f16(p[2 * t + 1] * vm1.x));
         constexpr int NW = Slice<D, BV>::NW;
         uint32_t v0[NW], v1[NW];
-        load_v_slice<D, BV>(stg + C::KBYTES + (8 * t + tig) * C::PAIRV, g, v0);
-        load_v_slice<D, BV>(stg + C::KBYTES + (8 * t + tig + 4) * C::PAIRV, g, v1);
+        load_v_slice<D, BV>(stg + C::KBYTES + (o / 2 + 8 * t + tig) * C::PAIRV, g, v0);
+        load_v_slice<D, BV>(stg + C::KBYTES + (o / 2 + 8 * t + tig + 4) * C::PAIRV, g, v1);
 #pragma unroll
         for (int mi = 0; mi < NMT; mi++)
             mma_f16(st.acc[mi], extract<BV>(v0, 2 * mi), extract<BV>(v0, 2 * mi + 1), extract<BV>(v1, 2 * mi),
@@ -392,6 +410,7 @@ __device__ __noinline__ void process_raw(const AttnArgs &a, const uint8_t *tile,
     // valid when that token is not itself a sink
     auto valid = [&](long long slot) -> bool {
         if (slot >= a.n_raw_slots) return false;
+        if (a.raw_all_valid) return true;
         if (slot < a.n_sink_cfg) return slot < a.n_sink_eff;
         const long long r = slot - a.n_sink_cfg;
         const long long back = a.seq_len - 1 - r;
@@ -496,9 +515,11 @@ __device__ __forceinline__ void vadd(float (&acc)[2], const float2 &v, float w) 
 
 // The last CTA of a unit: merge its split records, rotate the value
 // accumulator back, normalize and write the output; reset the ticket.
+// Records are read in batches of 8 whose loads are all in flight together,
+// merged with a running maximum.
 template <int D, int PR>
 __device__ __noinline__ void combine_unit(const AttnArgs &a, const AttnShape &sh, int u, int n_ctas) {
-    constexpr int V = D / 32;
+    constexpr int V = D / 32, NB = 8;
     using VT = typename VecT<V>::T;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int b = u / sh.Hkv, kvh = u % sh.Hkv;
@@ -506,22 +527,40 @@ __device__ __noinline__ void combine_unit(const AttnArgs &a, const AttnShape &sh
     if (h < sh.G) {
         const float *pu = a.partials + static_cast<long long>(u) * a.max_slots * 2 * 4 * PR + h * PR;
         const int n_rec = 2 * n_ctas;  // record r: kind r & 1 (0: 16-bit, 1: packed)
-        float M = -INFINITY;
-#pragma unroll 4
-        for (int r = 0; r < n_rec; r++) M = fmaxf(M, __ldcg(pu + r * 4 * PR + D));
-        float Lsum = 0.f;
+        float M = -INFINITY, Lsum = 0.f;
         float accq[V], accr[V];
 #pragma unroll
         for (int j = 0; j < V; j++) accq[j] = accr[j] = 0.f;
-#pragma unroll 4
-        for (int r = 0; r < n_rec; r++) {
-            const float *p = pu + r * 4 * PR;
-            const float mr = __ldcg(p + D), lr = __ldcg(p + D + 1);
-            const VT vv = __ldcg(reinterpret_cast<const VT *>(p) + lane);
-            const float wgt = mr == -INFINITY ? 0.f : exp2f(mr - M);
-            Lsum += lr * wgt;
-            if (r & 1) vadd(accq, vv, wgt);
-            else vadd(accr, vv, wgt);
+        for (int r0 = 0; r0 < n_rec; r0 += NB) {
+            float mr[NB], lr[NB];
+            VT vv[NB];
+#pragma unroll
+            for (int k = 0; k < NB; k++) {
+                const float *p = pu + (r0 + k) * 4 * PR;
+                const bool in = r0 + k < n_rec;
+                mr[k] = in ? __ldcg(p + D) : -INFINITY;
+                lr[k] = in ? __ldcg(p + D + 1) : 0.f;
+                vv[k] = in ? __ldcg(reinterpret_cast<const VT *>(p) + lane) : VT{};
+            }
+            float mb = M;
+#pragma unroll
+            for (int k = 0; k < NB; k++) mb = fmaxf(mb, mr[k]);
+            if (mb == -INFINITY) continue;
+            const float al = M == -INFINITY ? 0.f : exp2f(M - mb);
+            M = mb;
+            Lsum *= al;
+#pragma unroll
+            for (int j = 0; j < V; j++) {
+                accq[j] *= al;
+                accr[j] *= al;
+            }
+#pragma unroll
+            for (int k = 0; k < NB; k++) {
+                const float w = mr[k] == -INFINITY ? 0.f : exp2f(mr[k] - M);
+                Lsum += lr[k] * w;
+                if ((r0 + k) & 1) vadd(accq, vv[k], w);
+                else vadd(accr, vv[k], w);
+            }
         }
         if (a.rot_v == DQ_ROT_HADAMARD) {
             fwht_warp<V>(accq);
@@ -542,16 +581,101 @@ __device__ __noinline__ void combine_unit(const AttnArgs &a, const AttnShape &sh
     if (threadIdx.x == 0) a.counters[u] = 0;
 }
 
+// Query preparation of unit u into slot qs: warp h takes query head h (raw q,
+// rotated or compensated q, sum q, q . mu).
+template <int D, int BK, int BV, bool M16>
+__device__ __forceinline__ void prep_query(const AttnArgs &a, const AttnShape &sh, Smem<D, BK, BV, M16> &S, int qs,
+                                           int u) {
+    constexpr int V = D / 32;
+    const int h = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int b = u / sh.Hkv, kvh = u % sh.Hkv;
+    float xq[V];
+    if (h < sh.G) {
+        const float *qp = a.q + (static_cast<long long>(b) * sh.Hkv * sh.G + kvh * sh.G + h) * D;
+#pragma unroll
+        for (int j = 0; j < V; j++) xq[j] = qp[lane * V + j];
+    } else {
+#pragma unroll
+        for (int j = 0; j < V; j++) xq[j] = 0.f;
+    }
+    float mu[V];
+#pragma unroll
+    for (int j = 0; j < V; j++) mu[j] = a.mean_k ? a.mean_k[static_cast<long long>(u) * D + lane * V + j] : 0.f;
+#pragma unroll
+    for (int j = 0; j < V; j++) S.q_raw[qs][h][lane * V + j] = xq[j];
+    if (a.rot_k == DQ_ROT_HADAMARD) {
+        fwht_warp<V>(xq);
+#pragma unroll
+        for (int j = 0; j < V; j++) xq[j] *= a.hscale;
+    } else if (a.rot_k == DQ_ROT_DENSE) {
+        // q~ = T^{-T} q with the caller's fp32 compensation matrix
+        __syncwarp();
+        const float *Qc = a.q_comp + static_cast<long long>(kvh) * D * D;
+#pragma unroll
+        for (int j = 0; j < V; j++) {
+            float acc = 0.f;
+            const float *row = Qc + static_cast<long long>(lane * V + j) * D;
+            for (int k = 0; k < D; k++) acc += row[k] * S.q_raw[qs][h][k];
+            xq[j] = acc;
+        }
+    }
+    float qsum = 0.f, qmu = 0.f;
+#pragma unroll
+    for (int j = 0; j < V; j++) {
+        S.q_rot[qs][h][lane * V + j] = xq[j];
+        qsum += xq[j];
+        qmu += xq[j] * mu[j];
+    }
+    qsum = warp_sum(qsum);
+    qmu = warp_sum(qmu);
+    if (lane == 0) {
+        S.qsum[qs][h] = qsum;
+        S.qmu[qs][h] = qmu;
+    }
+}
+
+// Next packed chunk (relative index) for this warp from the segment's shared
+// counter, or -1 when the segment's chunks are all handed out.
+__device__ __forceinline__ int grab_chunk(int *counter, int n_chunks) {
+    uint32_t v = 0;
+    asm volatile(
+        "{\n .reg .pred p;\n elect.sync _|p, 0xffffffff;\n @p atom.shared.add.u32 %0, [%1], 1;\n}\n"
+        : "+r"(v)
+        : "r"(smem_u32(counter))
+        : "memory");
+    v = __shfl_sync(FULL, v, 0);  // lane 0 is the elected lane of a full warp
+    return static_cast<int>(v) < n_chunks ? static_cast<int>(v) : -1;
+}
+
+// Items [s0, s1) of a unit -> packed chunks [q0, q1) and 16-bit tiles [r0, r1):
+// a unit's items are its chunks, tile r riding with chunk floor(r * n_qc / n_rt);
+// a unit without packed tokens has its tiles as items.
+__device__ __forceinline__ void segment_items(const AttnArgs &a, long long s0, long long s1, long long &q0,
+                                              long long &q1, long long &r0, long long &r1) {
+    if (a.n_qc > 0) {
+        q0 = s0;
+        q1 = s1;
+        r0 = (s0 * a.n_rt + a.n_qc - 1) / a.n_qc;
+        r1 = (s1 * a.n_rt + a.n_qc - 1) / a.n_qc;
+    } else {
+        q0 = q1 = 0;
+        r0 = s0;
+        r1 = s1;
+    }
+}
+
 // ---- the kernel ----------------------------------------------------------------
 // A CTA walks its item range unit by unit.  In each unit segment, warp 0 first
 // runs the segment's 16-bit tiles (if any) while warps 1-3 start on packed
 // chunks; chunks are handed out one at a time from a shared counter, so the
 // warps finish together.  Each warp streams its chunks through its own 2-deep
-// ring of bulk copies.
+// ring of bulk copies.  Loads that later work depends on go first: warp 0's
+// first 16-bit tile, then the queries of the CTA's first two units, and only
+// then the packed chunks.
 template <int D, int BK, int BV, bool M16>
 __global__ void __launch_bounds__(128, Cfg<D, BK, BV, M16>::MINB) attn_kernel(AttnArgs a, AttnShape sh) {
     using C = Cfg<D, BK, BV, M16>;
-    constexpr int V = D / 32, PR = C::PR, NKS = C::NKS;
+    constexpr int PR = C::PR, NKS = C::NKS;
     extern __shared__ __align__(128) uint8_t smem_raw[];
     Smem<D, BK, BV, M16> &S = *reinterpret_cast<Smem<D, BK, BV, M16> *>(smem_raw);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tig = lane & 3;
@@ -560,6 +684,7 @@ __global__ void __launch_bounds__(128, Cfg<D, BK, BV, M16>::MINB) attn_kernel(At
     const long long x0 = static_cast<long long>(i) * N / G, x1 = static_cast<long long>(i + 1) * N / G;
     uint8_t *ring0 = S.ring[warp];
     uint64_t *bars = S.bars[warp];
+    const int u_first = static_cast<int>(x0 / ipu), u_lastc = static_cast<int>((x1 - 1) / ipu);
 
     if (lane == 0) {
         for (int s = 0; s < C::NST; s++) mbar_init(&bars[s], 1);
@@ -568,96 +693,42 @@ __global__ void __launch_bounds__(128, Cfg<D, BK, BV, M16>::MINB) attn_kernel(At
     __syncwarp();
     uint32_t phase = 0;  // bit s: parity of the next completion of bars[s]
     bool timed_out = false;
+    {
+        // warp 0: the first segment's first 16-bit tile, before anything else
+        long long q0, q1, r0, r1;
+        const long long ub = static_cast<long long>(u_first) * ipu;
+        segment_items(a, x0 - ub, (x1 < ub + ipu ? x1 : ub + ipu) - ub, q0, q1, r0, r1);
+        if (warp == 0 && r0 < r1 && lane == 0) issue_raw<D>(a, sh, u_first, r0, ring0, &bars[0]);
+        prep_query<D, BK, BV, M16>(a, sh, S, 0, u_first);
+        if (u_lastc > u_first) prep_query<D, BK, BV, M16>(a, sh, S, 1, u_first + 1);
+    }
 
     for (long long x = x0; x < x1;) {
         const int u = static_cast<int>(x / ipu);
         const long long ub = static_cast<long long>(u) * ipu;
-        const long long s0 = x - ub, s1 = (x1 < ub + ipu ? x1 : ub + ipu) - ub;
-        x = ub + s1;
-        const int b = u / sh.Hkv, kvh = u % sh.Hkv;
-        // items of a unit are its packed chunks; its 16-bit tiles ride along,
-        // tile r with chunk floor(r * n_qc / n_rt) (all tiles if it has no chunks)
-        long long q0 = 0, q1 = 0, r0, r1;
-        if (a.n_qc > 0) {
-            q0 = s0;
-            q1 = s1;
-            r0 = (s0 * a.n_rt + a.n_qc - 1) / a.n_qc;
-            r1 = (s1 * a.n_rt + a.n_qc - 1) / a.n_qc;
-        } else {
-            r0 = s0;
-            r1 = s1;
-        }
+        const bool first_seg = x == x0;
+        long long q0, q1, r0, r1;
+        segment_items(a, x - ub, (x1 < ub + ipu ? x1 : ub + ipu) - ub, q0, q1, r0, r1);
+        x = x1 < ub + ipu ? x1 : ub + ipu;
         const int n_chunks = static_cast<int>(q1 - q0);
         const bool raw_warp = warp == 0 && r0 < r1;
+        const int qs = (u - u_first) & 1;
 
         __syncthreads();  // the previous segment is done with the shared state
         if (threadIdx.x == 0) S.next_chunk = 0;
+        if (!first_seg && raw_warp && lane == 0) issue_raw<D>(a, sh, u, r0, ring0, &bars[0]);
+        if (u - u_first >= 2) prep_query<D, BK, BV, M16>(a, sh, S, qs, u);  // units past the first two
         __syncthreads();
-        // start the first copies before anything else
-        auto grab = [&]() -> int {
-            int v = 0;
-            if (lane == 0) v = atomicAdd(&S.next_chunk, 1);
-            v = __shfl_sync(FULL, v, 0);
-            return v < n_chunks ? v : -1;
-        };
+
+        const ChunkSrc<D, BK, BV, M16> src(a, sh, u);
         int cq0 = -1, cq1 = -1;  // chunk (relative to q0) in flight in stage 0 / 1
         auto start_chunks = [&]() {
-            cq0 = grab();
-            if (cq0 >= 0 && lane == 0) issue_chunk<D, BK, BV, M16>(a, sh, u, q0 + cq0, (S.ring[warp] + 0), &bars[0]);
-            cq1 = cq0 >= 0 ? grab() : -1;
-            if (cq1 >= 0 && lane == 0) issue_chunk<D, BK, BV, M16>(a, sh, u, q0 + cq1, (S.ring[warp] + C::STAGE), &bars[1]);
+            cq0 = grab_chunk(&S.next_chunk, n_chunks);
+            if (cq0 >= 0) src.issue(q0 + cq0, S.ring[warp], &bars[0]);
+            cq1 = cq0 >= 0 ? grab_chunk(&S.next_chunk, n_chunks) : -1;
+            if (cq1 >= 0) src.issue(q0 + cq1, S.ring[warp] + C::STAGE, &bars[1]);
         };
-        if (raw_warp) {
-            if (lane == 0) issue_raw<D>(a, sh, u, r0, ring0, &bars[0]);
-        } else {
-            start_chunks();
-        }
-
-        // ---- query preparation: warp h handles query head h of this KV head ----
-        {
-            const int h = warp;
-            float xq[V];
-            if (h < sh.G) {
-                const float *qp = a.q + (static_cast<long long>(b) * sh.Hkv * sh.G + kvh * sh.G + h) * D;
-#pragma unroll
-                for (int j = 0; j < V; j++) xq[j] = qp[lane * V + j];
-            } else {
-#pragma unroll
-                for (int j = 0; j < V; j++) xq[j] = 0.f;
-            }
-#pragma unroll
-            for (int j = 0; j < V; j++) S.q_raw[h][lane * V + j] = xq[j];
-            if (a.rot_k == DQ_ROT_HADAMARD) {
-                fwht_warp<V>(xq);
-#pragma unroll
-                for (int j = 0; j < V; j++) xq[j] *= a.hscale;
-            } else if (a.rot_k == DQ_ROT_DENSE) {
-                // q~ = T^{-T} q with the caller's fp32 compensation matrix
-                __syncwarp();
-                const float *Qc = a.q_comp + static_cast<long long>(kvh) * D * D;
-#pragma unroll
-                for (int j = 0; j < V; j++) {
-                    float acc = 0.f;
-                    const float *row = Qc + static_cast<long long>(lane * V + j) * D;
-                    for (int k = 0; k < D; k++) acc += row[k] * S.q_raw[h][k];
-                    xq[j] = acc;
-                }
-            }
-            float qs = 0.f, qm = 0.f;
-#pragma unroll
-            for (int j = 0; j < V; j++) {
-                S.q_rot[h][lane * V + j] = xq[j];
-                qs += xq[j];
-                if (a.mean_k) qm += xq[j] * a.mean_k[static_cast<long long>(u) * D + lane * V + j];
-            }
-            qs = warp_sum(qs);
-            qm = warp_sum(qm);
-            if (lane == 0) {
-                S.qsum[h] = qs;
-                S.qmu[h] = qm;
-            }
-        }
-        __syncthreads();
+        if (!raw_warp) start_chunks();
 
         const int first = owner(ub, N, G), last = owner(ub + ipu - 1, N, G);
         float *recs = a.partials + (static_cast<long long>(u) * a.max_slots + (i - first)) * 2 * 4 * PR;
@@ -666,8 +737,8 @@ __global__ void __launch_bounds__(128, Cfg<D, BK, BV, M16>::MINB) attn_kernel(At
         // ---- 16-bit tiles (warp 0): record kind 0 ----
         if (raw_warp) {
             uint32_t qb[NKS][2];
-            if (a.raw_bf16) build_qb<D, 2, false, true>(S.q_raw, qb, PermRawK());
-            else build_qb<D, 2, false, false>(S.q_raw, qb, PermRawK());
+            if (a.raw_bf16) build_qb<D, 2, false, true>(S.q_raw[qs], qb, PermRawK());
+            else build_qb<D, 2, false, false>(S.q_raw[qs], qb, PermRawK());
             st.init();
             for (long long r = r0; r < r1; r++) {
                 if (!mbar_wait(&bars[0], phase & 1u, WAIT_LIMIT_NS)) timed_out = true;
@@ -692,8 +763,8 @@ __global__ void __launch_bounds__(128, Cfg<D, BK, BV, M16>::MINB) attn_kernel(At
         st.init();
         if (cq0 >= 0) {
             uint32_t qb[NKS][2];
-            build_qb<D, BK, true, false>(S.q_rot, qb, PermIdentity());
-            const float qs_l2 = a.sm_log2 * S.qsum[tig], qm_l2 = a.sm_log2 * S.qmu[tig];
+            build_qb<D, BK, true, false>(S.q_rot[qs], qb, PermIdentity());
+            const float qs_l2 = a.sm_log2 * S.qsum[qs][tig], qm_l2 = a.sm_log2 * S.qmu[qs][tig];
             const float sk_l2 = a.sm_log2 * 16777216.0f;  // 2^24 undoes the operand scaling
             const long long n_q = a.n_q;
             int s = 0;
@@ -703,13 +774,13 @@ __global__ void __launch_bounds__(128, Cfg<D, BK, BV, M16>::MINB) attn_kernel(At
                 if (!mbar_wait(&bars[s], (phase >> s) & 1u, WAIT_LIMIT_NS)) timed_out = true;
                 phase ^= 1u << s;
                 const uint8_t *stg = S.ring[warp] + s * C::STAGE;
-                process_chunk<D, BK, BV, M16>(stg, (q0 + cur) * C::CK, n_q, qb, sk_l2, qs_l2, qm_l2, st);
+                const long long tok0 = (q0 + cur) * C::CK;
+#pragma unroll 1
+                for (int o = 0; o < C::CK; o += C::SUB)
+                    process_block<D, BK, BV, M16>(stg, o, tok0 + o, n_q, qb, sk_l2, qs_l2, qm_l2, st);
                 __syncwarp();
-                const int nxt = grab();
-                if (nxt >= 0 && lane == 0) {
-                    fence_proxy_async();
-                    issue_chunk<D, BK, BV, M16>(a, sh, u, q0 + nxt, S.ring[warp] + s * C::STAGE, &bars[s]);
-                }
+                const int nxt = grab_chunk(&S.next_chunk, n_chunks);
+                if (nxt >= 0) src.issue(q0 + nxt, S.ring[warp] + s * C::STAGE, &bars[s]);
                 if (s) cq1 = nxt;
                 else cq0 = nxt;
                 s ^= 1;
@@ -806,6 +877,7 @@ int plan_attention(const Layout &L, AttnArgs &a, int num_sms, long long cap_floa
     });
     if (e != 0) return e;
     a.n_rt = a.has_raw ? (a.n_raw_slots + RTILE - 1) / RTILE : 0;
+    a.raw_all_valid = a.seq_len >= static_cast<long long>(a.n_sink_cfg) + a.n_recent_cfg;
     a.n_qc = (a.n_q + ck - 1) / ck;
     // a unit's items are its packed chunks (its 16-bit tiles ride along with
     // them), or its 16-bit tiles when it has no packed tokens

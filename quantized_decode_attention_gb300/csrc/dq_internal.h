@@ -67,6 +67,7 @@ struct AttnArgs {
     int n_raw_slots;        // raw slots scanned (n_sink + n_recent)
     int n_sink_cfg, n_recent_cfg;
     int has_raw;            // 1 if the unit has 16-bit slots
+    int raw_all_valid;      // seq_len >= n_sink + n_recent: every 16-bit slot is in use
     int n_rt;               // 16-slot tiles of 16-bit tokens per unit
     long long n_qc;         // 64-token chunks of packed tokens per unit
     long long items_per_unit, total_items;
