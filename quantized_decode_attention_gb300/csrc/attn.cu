@@ -52,25 +52,25 @@ struct AttnShape {
 
 template <int D, int BK, int BV, bool M16>
 struct Cfg {
-    static constexpr int CK = BK == 4 ? 32 : 64;  // tokens per packed work item (chunk)
-    static constexpr int SUB = 32;                // tokens per softmax step within a chunk
+    static constexpr int ST = 128;                // packed tokens per pipeline entry
+    static constexpr int SUB = 32;                // tokens of an entry per warp (one softmax step)
     static constexpr int TILES = SUB / 16;
     static constexpr int ROWK = D * BK / 8;
     static constexpr int PAIRV = 2 * D * BV / 8;
     static constexpr int MB = M16 ? 2 : 4;
-    static constexpr int KBYTES = CK * ROWK;
-    static constexpr int VBYTES = CK / 2 * PAIRV;
-    static constexpr int MBYTES = CK * 2 * MB;
-    static constexpr int STAGE = KBYTES + VBYTES + 2 * MBYTES;
-    static constexpr int NST = 2;                 // bulk-copy ring depth per warp
+    static constexpr int KBYTES = ST * ROWK;      // stage layout: keys, value pairs, key meta, value meta
+    static constexpr int VBYTES = ST / 2 * PAIRV;
+    static constexpr int MBYTES = ST * 2 * MB;
+    static constexpr int ENTRY = KBYTES + VBYTES + 2 * MBYTES;
     static constexpr int RAWBYTES = 64 * D;       // one 16-slot tile of 16-bit keys + values
-    // bytes of one warp's ring: NST stages, or one 16-bit tile if that is larger
-    static constexpr int RING = NST * STAGE > RAWBYTES ? NST * STAGE : RAWBYTES;
+    static constexpr int SLOT = ((ENTRY > RAWBYTES ? ENTRY : RAWBYTES) + 127) / 128 * 128;
+    // ring depth: four slots where four CTAs per SM still fit, else as many as
+    // fit three CTAs per SM (the 3-bit kernel is register-limited to three)
+    static constexpr int NST = SLOT <= 9216 ? 4 : (SLOT <= 13312 ? 4 : 3);
     static constexpr int NKS = D / 16;
     static constexpr int NMT = D / 16;
     static constexpr int PR = D + 4;  // floats per head in a partial record: acc[D], m, l, 0, 0
-    // resident CTAs per SM the kernel is register-limited to (smem allows it)
-    static constexpr int MINB = RING <= 10240 ? 4 : (RING <= 14336 ? 3 : 2);
+    static constexpr int MINB = (BK == 3 || SLOT > 9216) ? 3 : 4;  // resident CTAs per SM
 };
 
 // ---- code extraction --------------------------------------------------------
@@ -222,83 +222,80 @@ struct WarpState {
 template <int D, int BK, int BV, bool M16>
 struct Smem {
     using C = Cfg<D, BK, BV, M16>;
-    float q_raw[2][4][D];      // prepared queries of up to two units at a time
-    float q_rot[2][4][D];
+    // query operands of up to two units at a time: [unit slot][kind: 0 16-bit
+    // tiles, 1 packed][half: 0 hi, 1 lo][head][channel] 16-bit values, rows
+    // padded by 8 so that the 8 (half, head) rows of a warp's load hit
+    // different banks
+    uint16_t qh[2][2][2][4][D + 8];
     float qsum[2][4], qmu[2][4];
-    float merge[4][4][C::PR];  // [warp][head][acc[D], m, l, -, -]
-    uint64_t bars[4][C::NST];
-    int next_chunk;            // chunks of the current segment handed out so far
+    float msc[4][4], mM[4], mL[4];  // CTA merge: per-warp scale, max and sum per head
+    union {
+        float merge[4][4][C::PR];  // [warp][head][acc[D], m, l, -, -]
+        float qscr[4][D];          // query preparation (dense rotation): raw q per head
+    };
+    uint64_t full[C::NST];         // slot filled (transaction count of its copies)
+    unsigned rel[C::NST];          // releases of a slot so far (4 per entry)
     int last;
-    alignas(128) uint8_t ring[4][C::RING];  // per warp: stage s at s * STAGE
+    alignas(128) uint8_t ring[C::NST][C::SLOT];
 };
 
-// Global sources of one unit's packed records, and the bulk copy of chunk c
-// into a stage, issued by one elected lane without branching the warp.
-template <int D, int BK, int BV, bool M16>
-struct ChunkSrc {
-    const uint8_t *ck, *cv, *mk, *mv;
-    __device__ __forceinline__ ChunkSrc(const AttnArgs &a, const AttnShape &sh, int u) {
-        using C = Cfg<D, BK, BV, M16>;
-        ck = a.codes_k + static_cast<long long>(u) * sh.qcap * C::ROWK;
-        cv = a.codes_v + static_cast<long long>(u) * (sh.qcap / 2) * C::PAIRV;
-        mk = static_cast<const uint8_t *>(a.meta_k) + static_cast<long long>(u) * sh.qcap * 2 * C::MB;
-        mv = static_cast<const uint8_t *>(a.meta_v) + static_cast<long long>(u) * sh.qcap * 2 * C::MB;
-    }
-    __device__ __forceinline__ void issue(long long c, uint8_t *stage, uint64_t *bar) const {
-        using C = Cfg<D, BK, BV, M16>;
-        const uint32_t t0 = static_cast<uint32_t>(c) * C::CK;
-        const uint32_t sb = smem_u32(stage), br = smem_u32(bar);
-        asm volatile(
-            "{\n .reg .pred p;\n elect.sync _|p, 0xffffffff;\n"
-            "@p fence.proxy.async.shared::cta;\n"
-            "@p mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n"
-            "@p cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%2], [%3], %4, [%0];\n"
-            "@p cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%5], [%6], %7, [%0];\n"
-            "@p cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%8], [%9], %10, [%0];\n"
-            "@p cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%11], [%12], %10, [%0];\n}\n" ::"r"(br),
-            "r"(C::STAGE), "r"(sb), "l"(ck + static_cast<uint64_t>(t0) * C::ROWK), "r"(C::KBYTES),
-            "r"(sb + C::KBYTES), "l"(cv + static_cast<uint64_t>(t0 / 2) * C::PAIRV), "r"(C::VBYTES),
-            "r"(sb + C::KBYTES + C::VBYTES), "l"(mk + static_cast<uint64_t>(t0) * 2 * C::MB), "r"(C::MBYTES),
-            "r"(sb + C::KBYTES + C::VBYTES + C::MBYTES), "l"(mv + static_cast<uint64_t>(t0) * 2 * C::MB)
-            : "memory");
-    }
-};
-
-// Bulk-copy 16-bit tile r (16 slots: keys then value pairs) of unit u.
-template <int D>
-__device__ __forceinline__ void issue_raw(const AttnArgs &a, const AttnShape &sh, int u, long long r,
-                                          uint8_t *dst, uint64_t *bar) {
-    const uint16_t *rk = a.raw_k + (static_cast<long long>(u) * sh.rcap + r * RTILE) * D;
-    const uint16_t *rv = a.raw_v + (static_cast<long long>(u) * sh.rcap + r * RTILE) * D;
-    mbar_expect_tx(bar, 64 * D);
-    bulk_g2s(dst, rk, 32 * D, bar);
-    bulk_g2s(dst + 32 * D, rv, 32 * D, bar);
+// Shared-memory counter increment with acquire-release ordering at CTA scope;
+// returns the old value.
+__device__ __forceinline__ unsigned atom_add_acq_rel(unsigned *p) {
+    unsigned old;
+    asm volatile("atom.acq_rel.cta.shared::cta.add.u32 %0, [%1], 1;\n" : "=r"(old) : "r"(smem_u32(p)) : "memory");
+    return old;
 }
 
-// B operand of q.K^T for this lane: column g = head g>>1, half g&1 of the
-// (scaled) query.  Lane slot (k-step i, sub, e) holds logical channel
-// 16i + 2tig + 8sub + e; `perm` maps it to the channel of q it multiplies.
-template <int D, int BK, bool QUANT, bool BF16, typename Perm>
-__device__ __forceinline__ void build_qb(const float (*q)[D], uint32_t (&qb)[D / 16][2], Perm perm) {
-    const int lane = threadIdx.x & 31, g = lane >> 2, tig = lane & 3;
-    const int h = g >> 1, part = g & 1;
-#pragma unroll
-    for (int i = 0; i < D / 16; i++) {
-#pragma unroll
-        for (int sub = 0; sub < 2; sub++) {
-            float v0 = q[h][perm(i, tig, sub, 0)], v1 = q[h][perm(i, tig, sub, 1)];
-            if (QUANT) {
-                const float sc = exp2f(static_cast<float>(-field_exp(2 * i + sub, BK)));
-                v0 *= sc;
-                v1 *= sc;
-            }
-            const uint32_t w0 = BF16 ? hilo_bf16(v0) : hilo_f16(v0);
-            const uint32_t w1 = BF16 ? hilo_bf16(v1) : hilo_f16(v1);
-            const uint16_t e0 = static_cast<uint16_t>(part ? (w0 >> 16) : (w0 & 0xffffu));
-            const uint16_t e1 = static_cast<uint16_t>(part ? (w1 >> 16) : (w1 & 0xffffu));
-            qb[i][sub] = pack2(e0, e1);
-        }
+// Arrive on an mbarrier from one elected lane of the warp.
+__device__ __forceinline__ void mbar_arrive_elect(uint64_t *bar) {
+    asm volatile(
+        "{\n .reg .pred p;\n elect.sync _|p, 0xffffffff;\n"
+        "@p mbarrier.arrive.shared::cta.b64 _, [%0];\n}\n" ::"r"(smem_u32(bar))
+        : "memory");
+}
+
+// Pipeline entry e of unit u into a ring slot, issued by one elected lane of
+// the calling warp (all lanes call it with the same arguments).  Entries
+// [0, n_rt) are 16-slot tiles of 16-bit keys and values; entry n_rt + p holds
+// packed tokens [p*ST, p*ST + ST): keys, value pairs, key meta, value meta,
+// each at its fixed offset in the slot.  A last entry that would run past the
+// unit's capacity copies the 64 tokens that exist (capacity is a multiple of 64).
+template <int D, int BK, int BV, bool M16>
+__device__ __forceinline__ void issue_entry(const AttnArgs &a, const AttnShape &sh, int u, int e, uint8_t *slot,
+                                            uint64_t *bar) {
+    using C = Cfg<D, BK, BV, M16>;
+    const uint32_t sb = smem_u32(slot), br = smem_u32(bar);
+    if (e < a.n_rt) {
+        const long long r0 = static_cast<long long>(u) * sh.rcap + static_cast<long long>(e) * RTILE;
+        const uint16_t *rk = a.raw_k + r0 * D, *rv = a.raw_v + r0 * D;
+        asm volatile(
+            "{\n .reg .pred p;\n elect.sync _|p, 0xffffffff;\n"
+            "@p mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n"
+            "@p cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%2], [%3], %4, [%0];\n"
+            "@p cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%5], [%6], %4, [%0];\n}\n" ::"r"(br),
+            "n"(64 * D), "r"(sb), "l"(rk), "n"(32 * D), "r"(sb + 32 * D), "l"(rv)
+            : "memory");
+        return;
     }
+    const long long t0 = static_cast<long long>(e - a.n_rt) * C::ST;
+    const uint32_t nt = sh.qcap - t0 >= C::ST ? C::ST : static_cast<uint32_t>(sh.qcap - t0);
+    const long long g0 = static_cast<long long>(u) * sh.qcap + t0;
+    const uint8_t *ck = a.codes_k + g0 * C::ROWK;
+    const uint8_t *cv = a.codes_v + g0 / 2 * C::PAIRV;
+    const uint8_t *mk = static_cast<const uint8_t *>(a.meta_k) + g0 * 2 * C::MB;
+    const uint8_t *mv = static_cast<const uint8_t *>(a.meta_v) + g0 * 2 * C::MB;
+    const uint32_t kb = nt * C::ROWK, vb = nt / 2 * C::PAIRV, mb = nt * 2 * C::MB;
+    asm volatile(
+        "{\n .reg .pred p;\n elect.sync _|p, 0xffffffff;\n"
+        "@p mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n"
+        "@p cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%2], [%3], %4, [%0];\n"
+        "@p cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%5], [%6], %7, [%0];\n"
+        "@p cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%8], [%9], %10, [%0];\n"
+        "@p cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%11], [%12], %10, [%0];\n}\n" ::"r"(br),
+        "r"(kb + vb + 2 * mb), "r"(sb), "l"(ck), "r"(kb), "r"(sb + C::KBYTES), "l"(cv), "r"(vb),
+        "r"(sb + C::KBYTES + C::VBYTES), "l"(mk), "r"(mb), "r"(sb + C::KBYTES + C::VBYTES + C::MBYTES), "l"(mv)
+        : "memory");
 }
 
 // Channel of a key record / of q that lane slot (i, tig, sub, e) stands for.
@@ -328,13 +325,13 @@ __device__ __forceinline__ uint32_t vec_word(const uint4 &v, int r) {
     return r == 0 ? v.x : (r == 1 ? v.y : (r == 2 ? v.z : v.w));
 }
 
-// SUB packed tokens already in shared memory -> warp state.  `stg` is the
-// stage, `o` the first token of the block within the chunk, `tok0` the token
-// index of the block within the unit.
+// This warp's SUB packed tokens of an entry -> warp state.  `kp`, `vp`, `mkp`,
+// `mvp` point at the warp's first key record, value pair record, key meta and
+// value meta in the slot; tokens at or past `valid` (0 < valid) are masked.
 template <int D, int BK, int BV, bool M16>
-__device__ __forceinline__ void process_block(const uint8_t *stg, int o, long long tok0, long long n_q,
-                                              const uint32_t (&qb)[D / 16][2], float sk_l2, float qs_l2, float qm_l2,
-                                              WarpState<D / 16> &st) {
+__device__ __forceinline__ void process_block(const uint8_t *kp, const uint8_t *vp, const uint8_t *mkp,
+                                              const uint8_t *mvp, int valid, const uint32_t (&qb)[D / 16][2],
+                                              float sk_l2, float qs_l2, float qm_l2, WarpState<D / 16> &st) {
     using C = Cfg<D, BK, BV, M16>;
     constexpr int NKS = C::NKS, NMT = C::NMT, T = C::TILES;
     const int lane = threadIdx.x & 31, g = lane >> 2, tig = lane & 3;
@@ -344,8 +341,8 @@ __device__ __forceinline__ void process_block(const uint8_t *stg, int o, long lo
     for (int t = 0; t < T; t++) {
         constexpr int NW = Slice<D, BK>::NW;
         uint32_t k0[NW], k1[NW];
-        load_k_slice<D, BK>(stg + (o + 16 * t + g) * C::ROWK, tig, k0);
-        load_k_slice<D, BK>(stg + (o + 16 * t + g + 8) * C::ROWK, tig, k1);
+        load_k_slice<D, BK>(kp + (16 * t + g) * C::ROWK, tig, k0);
+        load_k_slice<D, BK>(kp + (16 * t + g + 8) * C::ROWK, tig, k1);
         sc[t][0] = sc[t][1] = sc[t][2] = sc[t][3] = 0.f;
 #pragma unroll
         for (int i = 0; i < NKS; i++)
@@ -353,22 +350,20 @@ __device__ __forceinline__ void process_block(const uint8_t *stg, int o, long lo
                     extract<BK>(k1, 2 * i + 1), qb[i][0], qb[i][1]);
     }
     // logits of tokens 16t+g (k = 2t) and 16t+g+8 (k = 2t+1) for head tig
-    const uint8_t *smk = stg + C::KBYTES + C::VBYTES;
-    const uint8_t *smv = smk + C::MBYTES;
     float lg[2 * T];
 #pragma unroll
     for (int t = 0; t < T; t++)
 #pragma unroll
         for (int hf = 0; hf < 2; hf++) {
-            const float2 km = ld_meta(smk, o + 16 * t + g + 8 * hf, M16);
+            const float2 km = ld_meta(mkp, 16 * t + g + 8 * hf, M16);
             const float dot = sc[t][2 * hf] + sc[t][2 * hf + 1];
             lg[2 * t + hf] = (km.x * sk_l2) * dot + (km.y * qs_l2 + qm_l2);
         }
-    const bool ragged = tok0 + C::SUB > n_q;  // last block of the unit
+    const bool ragged = valid < C::SUB;  // warp-uniform: the unit's last entry
     if (ragged) {
 #pragma unroll
         for (int k = 0; k < 2 * T; k++)
-            if (tok0 + 16 * (k >> 1) + g + 8 * (k & 1) >= n_q) lg[k] = -INFINITY;
+            if (16 * (k >> 1) + g + 8 * (k & 1) >= valid) lg[k] = -INFINITY;
     }
     float p[2 * T];
     st.template update<2 * T>(lg, p);
@@ -377,18 +372,18 @@ __device__ __forceinline__ void process_block(const uint8_t *stg, int o, long lo
     float aos = 0.f;
 #pragma unroll
     for (int t = 0; t < T; t++) {
-        float2 vm0 = ld_meta(smv, o + 16 * t + g, M16), vm1 = ld_meta(smv, o + 16 * t + g + 8, M16);
+        float2 vm0 = ld_meta(mvp, 16 * t + g, M16), vm1 = ld_meta(mvp, 16 * t + g + 8, M16);
         if (ragged) {  // masked tokens have p = 0, but their metadata may be anything
-            if (tok0 + 16 * t + g >= n_q) vm0 = make_float2(0.f, 0.f);
-            if (tok0 + 16 * t + g + 8 >= n_q) vm1 = make_float2(0.f, 0.f);
+            if (16 * t + g >= valid) vm0 = make_float2(0.f, 0.f);
+            if (16 * t + g + 8 >= valid) vm1 = make_float2(0.f, 0.f);
         }
         aos += p[2 * t] * vm0.y + p[2 * t + 1] * vm1.y;
         const uint32_t b0 = movmatrix_t(hilo_f16(p[2 * t] * vm0.x));
         const uint32_t b1 = movmatrix_t(hilo_f16(p[2 * t + 1] * vm1.x));
         constexpr int NW = Slice<D, BV>::NW;
         uint32_t v0[NW], v1[NW];
-        load_v_slice<D, BV>(stg + C::KBYTES + (o / 2 + 8 * t + tig) * C::PAIRV, g, v0);
-        load_v_slice<D, BV>(stg + C::KBYTES + (o / 2 + 8 * t + tig + 4) * C::PAIRV, g, v1);
+        load_v_slice<D, BV>(vp + (8 * t + tig) * C::PAIRV, g, v0);
+        load_v_slice<D, BV>(vp + (8 * t + tig + 4) * C::PAIRV, g, v1);
 #pragma unroll
         for (int mi = 0; mi < NMT; mi++)
             mma_f16(st.acc[mi], extract<BV>(v0, 2 * mi), extract<BV>(v0, 2 * mi + 1), extract<BV>(v1, 2 * mi),
@@ -401,7 +396,7 @@ __device__ __forceinline__ void process_block(const uint8_t *stg, int o, long lo
 // read with 16-byte vectors; the resulting channel order is folded into the q
 // operand (PermRawK) and into the output rows (raw_v_channel).
 template <int D, bool BF16>
-__device__ __noinline__ void process_raw(const AttnArgs &a, const uint8_t *tile, long long s0,
+__device__ __forceinline__ void process_raw(const AttnArgs &a, const uint8_t *tile, long long s0,
                                          const uint32_t (&qb)[D / 16][2], WarpState<D / 16> &st) {
     constexpr int NKS = D / 16, NMT = D / 16, NV = D / 32;
     const int lane = threadIdx.x & 31, g = lane >> 2, tig = lane & 3;
@@ -581,28 +576,52 @@ __device__ __noinline__ void combine_unit(const AttnArgs &a, const AttnShape &sh
     if (threadIdx.x == 0) a.counters[u] = 0;
 }
 
-// Query preparation of unit u into slot qs: warp h takes query head h (raw q,
-// rotated or compensated q, sum q, q . mu).
-template <int D, int BK, int BV, bool M16>
-__device__ __forceinline__ void prep_query(const AttnArgs &a, const AttnShape &sh, Smem<D, BK, BV, M16> &S, int qs,
-                                           int u) {
+// One lane's share of a unit's query head (warp h takes head h; lane l holds
+// channels l*V .. l*V+V-1) and of the key channel mean.  Loaded first thing, so
+// that the loads are in flight before the cache copies.
+template <int V>
+struct QIn {
+    float xq[V], mu[V];
+};
+template <int D>
+__device__ __forceinline__ void load_query(const AttnArgs &a, const AttnShape &sh, int u, QIn<D / 32> &in) {
     constexpr int V = D / 32;
     const int h = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int b = u / sh.Hkv, kvh = u % sh.Hkv;
-    float xq[V];
-    if (h < sh.G) {
-        const float *qp = a.q + (static_cast<long long>(b) * sh.Hkv * sh.G + kvh * sh.G + h) * D;
+    const long long qo = (static_cast<long long>(b) * sh.Hkv * sh.G + kvh * sh.G + h) * D + lane * V;
+    const long long mo = static_cast<long long>(u) * D + lane * V;
 #pragma unroll
-        for (int j = 0; j < V; j++) xq[j] = qp[lane * V + j];
-    } else {
-#pragma unroll
-        for (int j = 0; j < V; j++) xq[j] = 0.f;
+    for (int j = 0; j < V; j++) {
+        in.xq[j] = h < sh.G ? __ldg(a.q + qo + j) : 0.f;
+        in.mu[j] = a.mean_k ? __ldg(a.mean_k + mo + j) : 0.f;
     }
-    float mu[V];
+}
+
+// The (hi, lo) 16-bit halves of v into S.qh[qs][kind][0 / 1][h][c].
+template <int D, int BK, int BV, bool M16>
+__device__ __forceinline__ void put_hilo(Smem<D, BK, BV, M16> &S, int qs, int kind, int h, int c, float v,
+                                         bool bf16) {
+    const uint32_t w = bf16 ? hilo_bf16(v) : hilo_f16(v);
+    S.qh[qs][kind][0][h][c] = static_cast<uint16_t>(w & 0xffffu);
+    S.qh[qs][kind][1][h][c] = static_cast<uint16_t>(w >> 16);
+}
+
+// Query preparation of unit u into slot qs (warp h: head h).  Kind 0 (16-bit
+// keys): raw q in the raw region's 16-bit type.  Kind 1 (packed keys): q
+// rotated (or compensated) and scaled by 2^-E for the code field E that
+// channel c meets in the key operand (register c>>3 of a lane's slice); also
+// sum q and q . mu for the fold of the affine code (Eq. 8).
+template <int D, int BK, int BV, bool M16>
+__device__ __forceinline__ void prep_query(const AttnArgs &a, const AttnShape &sh, Smem<D, BK, BV, M16> &S, int qs,
+                                           int u, const QIn<D / 32> &in) {
+    constexpr int V = D / 32;
+    const int h = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    float xq[V];
 #pragma unroll
-    for (int j = 0; j < V; j++) mu[j] = a.mean_k ? a.mean_k[static_cast<long long>(u) * D + lane * V + j] : 0.f;
-#pragma unroll
-    for (int j = 0; j < V; j++) S.q_raw[qs][h][lane * V + j] = xq[j];
+    for (int j = 0; j < V; j++) {
+        xq[j] = in.xq[j];
+        put_hilo(S, qs, 0, h, lane * V + j, xq[j], a.raw_bf16 != 0);
+    }
     if (a.rot_k == DQ_ROT_HADAMARD) {
         fwht_warp<V>(xq);
 #pragma unroll
@@ -610,21 +629,27 @@ __device__ __forceinline__ void prep_query(const AttnArgs &a, const AttnShape &s
     } else if (a.rot_k == DQ_ROT_DENSE) {
         // q~ = T^{-T} q with the caller's fp32 compensation matrix
         __syncwarp();
-        const float *Qc = a.q_comp + static_cast<long long>(kvh) * D * D;
+#pragma unroll
+        for (int j = 0; j < V; j++) S.qscr[h][lane * V + j] = xq[j];
+        __syncwarp();
+        const float *Qc = a.q_comp + static_cast<long long>(u % sh.Hkv) * D * D;
 #pragma unroll
         for (int j = 0; j < V; j++) {
             float acc = 0.f;
             const float *row = Qc + static_cast<long long>(lane * V + j) * D;
-            for (int k = 0; k < D; k++) acc += row[k] * S.q_raw[qs][h][k];
+            for (int k = 0; k < D; k++) acc += row[k] * S.qscr[h][k];
             xq[j] = acc;
         }
+        __syncwarp();
     }
     float qsum = 0.f, qmu = 0.f;
 #pragma unroll
     for (int j = 0; j < V; j++) {
-        S.q_rot[qs][h][lane * V + j] = xq[j];
+        const int c = lane * V + j;
         qsum += xq[j];
-        qmu += xq[j] * mu[j];
+        qmu += xq[j] * in.mu[j];
+        const float sc = __int_as_float((127 - field_exp(c >> 3, BK)) << 23);  // 2^-E, exact
+        put_hilo(S, qs, 1, h, c, xq[j] * sc, false);
     }
     qsum = warp_sum(qsum);
     qmu = warp_sum(qmu);
@@ -634,178 +659,201 @@ __device__ __forceinline__ void prep_query(const AttnArgs &a, const AttnShape &s
     }
 }
 
-// Next packed chunk (relative index) for this warp from the segment's shared
-// counter, or -1 when the segment's chunks are all handed out.
-__device__ __forceinline__ int grab_chunk(int *counter, int n_chunks) {
-    uint32_t v = 0;
-    asm volatile(
-        "{\n .reg .pred p;\n elect.sync _|p, 0xffffffff;\n @p atom.shared.add.u32 %0, [%1], 1;\n}\n"
-        : "+r"(v)
-        : "r"(smem_u32(counter))
-        : "memory");
-    v = __shfl_sync(FULL, v, 0);  // lane 0 is the elected lane of a full warp
-    return static_cast<int>(v) < n_chunks ? static_cast<int>(v) : -1;
-}
-
-// Items [s0, s1) of a unit -> packed chunks [q0, q1) and 16-bit tiles [r0, r1):
-// a unit's items are its chunks, tile r riding with chunk floor(r * n_qc / n_rt);
-// a unit without packed tokens has its tiles as items.
-__device__ __forceinline__ void segment_items(const AttnArgs &a, long long s0, long long s1, long long &q0,
-                                              long long &q1, long long &r0, long long &r1) {
-    if (a.n_qc > 0) {
-        q0 = s0;
-        q1 = s1;
-        r0 = (s0 * a.n_rt + a.n_qc - 1) / a.n_qc;
-        r1 = (s1 * a.n_rt + a.n_qc - 1) / a.n_qc;
-    } else {
-        q0 = q1 = 0;
-        r0 = s0;
-        r1 = s1;
-    }
+// This lane's mma B operand of q.K^T from the prepared halves: column g of the
+// operand is head g>>1, half g&1; lane slot (k-step i, sub, e) holds channel
+// perm(i, tig, sub, e), and e = 0, 1 are adjacent channels (one 32-bit load).
+template <int D, int BK, int BV, bool M16, typename Perm>
+__device__ __forceinline__ void load_qb(const Smem<D, BK, BV, M16> &S, int qs, int kind, Perm perm,
+                                        uint32_t (&qb)[D / 16][2]) {
+    const int lane = threadIdx.x & 31, g = lane >> 2, tig = lane & 3;
+    const uint16_t *row = S.qh[qs][kind][g & 1][g >> 1];
+#pragma unroll
+    for (int i = 0; i < D / 16; i++)
+#pragma unroll
+        for (int sub = 0; sub < 2; sub++) qb[i][sub] = *reinterpret_cast<const uint32_t *>(row + perm(i, tig, sub, 0));
 }
 
 // ---- the kernel ----------------------------------------------------------------
-// A CTA walks its item range unit by unit.  In each unit segment, warp 0 first
-// runs the segment's 16-bit tiles (if any) while warps 1-3 start on packed
-// chunks; chunks are handed out one at a time from a shared counter, so the
-// warps finish together.  Each warp streams its chunks through its own 2-deep
-// ring of bulk copies.  Loads that later work depends on go first: warp 0's
-// first 16-bit tile, then the queries of the CTA's first two units, and only
-// then the packed chunks.
+// A CTA walks its range [x0, x1) of pipeline entries unit by unit; a unit's
+// entries are its 16-slot tiles of 16-bit tokens, then its packed entries of
+// ST tokens.  NST entries are in flight in a CTA-wide ring of bulk copies
+// (completion on full[s]); the last of the four warps to be done with a slot
+// refills it.  Every warp takes SUB tokens of each packed entry; a 16-bit tile
+// goes to warp (tile index mod 4).  The query loads go out first, then the
+// first NST copies, then the queries are prepared.  Every warp waits on full[]
+// for every entry (also the 16-bit tiles it leaves to another warp): a warp is
+// then never more than one phase ahead of a slot, which the parity test of the
+// wait requires.
 template <int D, int BK, int BV, bool M16>
 __global__ void __launch_bounds__(128, Cfg<D, BK, BV, M16>::MINB) attn_kernel(AttnArgs a, AttnShape sh) {
     using C = Cfg<D, BK, BV, M16>;
-    constexpr int PR = C::PR, NKS = C::NKS;
+    constexpr int PR = C::PR, NKS = C::NKS, NST = C::NST;
     extern __shared__ __align__(128) uint8_t smem_raw[];
     Smem<D, BK, BV, M16> &S = *reinterpret_cast<Smem<D, BK, BV, M16> *>(smem_raw);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tig = lane & 3;
     const int G = gridDim.x, i = blockIdx.x;
-    const long long N = a.total_items, ipu = a.items_per_unit;
+    const long long N = a.total_items;
+    const int ipu = static_cast<int>(a.items_per_unit), n_rt = a.n_rt;
     const long long x0 = static_cast<long long>(i) * N / G, x1 = static_cast<long long>(i + 1) * N / G;
-    uint8_t *ring0 = S.ring[warp];
-    uint64_t *bars = S.bars[warp];
+    const int n_ent = static_cast<int>(x1 - x0);
+    if (n_ent <= 0 || ipu <= 0) return;
     const int u_first = static_cast<int>(x0 / ipu), u_lastc = static_cast<int>((x1 - 1) / ipu);
-
-    if (lane == 0) {
-        for (int s = 0; s < C::NST; s++) mbar_init(&bars[s], 1);
-        fence_mbar_init();
-    }
-    __syncwarp();
-    uint32_t phase = 0;  // bit s: parity of the next completion of bars[s]
     bool timed_out = false;
-    {
-        // warp 0: the first segment's first 16-bit tile, before anything else
-        long long q0, q1, r0, r1;
-        const long long ub = static_cast<long long>(u_first) * ipu;
-        segment_items(a, x0 - ub, (x1 < ub + ipu ? x1 : ub + ipu) - ub, q0, q1, r0, r1);
-        if (warp == 0 && r0 < r1 && lane == 0) issue_raw<D>(a, sh, u_first, r0, ring0, &bars[0]);
-        prep_query<D, BK, BV, M16>(a, sh, S, 0, u_first);
-        if (u_lastc > u_first) prep_query<D, BK, BV, M16>(a, sh, S, 1, u_first + 1);
+
+    // the queries of the CTA's first two units: their loads go out before the copies
+    QIn<D / 32> qin0, qin1;
+    load_query<D>(a, sh, u_first, qin0);
+    if (u_lastc > u_first) load_query<D>(a, sh, u_first + 1, qin1);
+
+    // the CTA's entry k -> (unit, entry of the unit), copied into slot k % NST
+    // (all lanes of a warp call it; one elected lane issues)
+    auto issue_k = [&](int k) {
+        const unsigned x = static_cast<unsigned>(x0) + static_cast<unsigned>(k);
+        const unsigned u = x / static_cast<unsigned>(ipu);
+        issue_entry<D, BK, BV, M16>(a, sh, static_cast<int>(u), static_cast<int>(x - u * ipu), S.ring[k % NST],
+                                    &S.full[k % NST]);
+    };
+    if (warp == 0) {
+        if (lane == 0) {
+            for (int s = 0; s < NST; s++) {
+                mbar_init(&S.full[s], 1);
+                S.rel[s] = 0;
+            }
+            fence_mbar_init();
+        }
+        __syncwarp();
+        for (int k = 0; k < NST && k < n_ent; k++) issue_k(k);
     }
+    prep_query<D, BK, BV, M16>(a, sh, S, 0, u_first, qin0);
+    if (u_lastc > u_first) prep_query<D, BK, BV, M16>(a, sh, S, 1, u_first + 1, qin1);
+
+    int j = 0;  // the CTA's entry being consumed
+    auto acquire = [&]() -> const uint8_t * {
+        if (!mbar_wait(&S.full[j % NST], (j / NST) & 1, WAIT_LIMIT_NS)) timed_out = true;
+        return S.ring[j % NST];
+    };
+    // done with slot j % NST: the last of the four warps to release it (an
+    // acquire-release count of releases) loads entry j + NST into it
+    auto release = [&]() {
+        __syncwarp();
+        unsigned old = 0;
+        if (lane == 0) old = atom_add_acq_rel(&S.rel[j % NST]);
+        old = __shfl_sync(FULL, old, 0);
+        if ((old & 3u) == 3u && j + NST < n_ent) issue_k(j + NST);
+        ++j;
+    };
+    // CTA merge of the 4 warps' states in S.merge -> one record of 4 heads at
+    // dst (called after a __syncthreads that follows the warps' stores)
+    auto cta_merge = [&](float *dst) {
+        if (threadIdx.x < 4) {
+            const int h = threadIdx.x;
+            float M = -INFINITY;
+#pragma unroll
+            for (int w = 0; w < 4; w++) M = fmaxf(M, S.merge[w][h][D]);
+            float L = 0.f;
+#pragma unroll
+            for (int w = 0; w < 4; w++) {
+                const float mw = S.merge[w][h][D];
+                const float sw = mw == -INFINITY ? 0.f : exp2f(mw - M);
+                S.msc[w][h] = sw;
+                L += sw * S.merge[w][h][D + 1];
+            }
+            S.mM[h] = M;
+            S.mL[h] = L;
+        }
+        __syncthreads();
+        constexpr int P4 = PR / 4;
+        for (int idx = threadIdx.x; idx < 4 * P4; idx += blockDim.x) {
+            const int h = idx / P4, c4 = idx - h * P4;
+            float4 r;
+            if (c4 < D / 4) {
+                r = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                for (int w = 0; w < 4; w++) {
+                    const float sw = S.msc[w][h];
+                    const float4 v = reinterpret_cast<const float4 *>(S.merge[w][h])[c4];
+                    r.x += sw * v.x;
+                    r.y += sw * v.y;
+                    r.z += sw * v.z;
+                    r.w += sw * v.w;
+                }
+            } else {
+                r = make_float4(S.mM[h], S.mL[h], 0.f, 0.f);
+            }
+            reinterpret_cast<float4 *>(dst)[idx] = r;
+        }
+    };
 
     for (long long x = x0; x < x1;) {
         const int u = static_cast<int>(x / ipu);
         const long long ub = static_cast<long long>(u) * ipu;
-        const bool first_seg = x == x0;
-        long long q0, q1, r0, r1;
-        segment_items(a, x - ub, (x1 < ub + ipu ? x1 : ub + ipu) - ub, q0, q1, r0, r1);
-        x = x1 < ub + ipu ? x1 : ub + ipu;
-        const int n_chunks = static_cast<int>(q1 - q0);
-        const bool raw_warp = warp == 0 && r0 < r1;
+        const long long xe = x1 < ub + ipu ? x1 : ub + ipu;
+        const int e0 = static_cast<int>(x - ub), e1 = static_cast<int>(xe - ub);
+        x = xe;
         const int qs = (u - u_first) & 1;
-
-        __syncthreads();  // the previous segment is done with the shared state
-        if (threadIdx.x == 0) S.next_chunk = 0;
-        if (!first_seg && raw_warp && lane == 0) issue_raw<D>(a, sh, u, r0, ring0, &bars[0]);
-        if (u - u_first >= 2) prep_query<D, BK, BV, M16>(a, sh, S, qs, u);  // units past the first two
-        __syncthreads();
-
-        const ChunkSrc<D, BK, BV, M16> src(a, sh, u);
-        int cq0 = -1, cq1 = -1;  // chunk (relative to q0) in flight in stage 0 / 1
-        auto start_chunks = [&]() {
-            cq0 = grab_chunk(&S.next_chunk, n_chunks);
-            if (cq0 >= 0) src.issue(q0 + cq0, S.ring[warp], &bars[0]);
-            cq1 = cq0 >= 0 ? grab_chunk(&S.next_chunk, n_chunks) : -1;
-            if (cq1 >= 0) src.issue(q0 + cq1, S.ring[warp] + C::STAGE, &bars[1]);
-        };
-        if (!raw_warp) start_chunks();
-
+        __syncthreads();  // barriers and queries published; the last segment is done with S
+        if (u - u_first >= 2) {
+            QIn<D / 32> qin;
+            load_query<D>(a, sh, u, qin);
+            prep_query<D, BK, BV, M16>(a, sh, S, qs, u, qin);
+            __syncthreads();
+        }
         const int first = owner(ub, N, G), last = owner(ub + ipu - 1, N, G);
         float *recs = a.partials + (static_cast<long long>(u) * a.max_slots + (i - first)) * 2 * 4 * PR;
         WarpState<D / 16> st;
 
-        // ---- 16-bit tiles (warp 0): record kind 0 ----
-        if (raw_warp) {
+        // ---- 16-bit tiles: record kind 0 ----
+        const int r1 = e1 < n_rt ? e1 : n_rt;
+        if (e0 < r1) {
             uint32_t qb[NKS][2];
-            if (a.raw_bf16) build_qb<D, 2, false, true>(S.q_raw[qs], qb, PermRawK());
-            else build_qb<D, 2, false, false>(S.q_raw[qs], qb, PermRawK());
+            load_qb(S, qs, 0, PermRawK(), qb);
             st.init();
-            for (long long r = r0; r < r1; r++) {
-                if (!mbar_wait(&bars[0], phase & 1u, WAIT_LIMIT_NS)) timed_out = true;
-                phase ^= 1u;
-                if (a.raw_bf16) process_raw<D, true>(a, ring0, r * RTILE, qb, st);
-                else process_raw<D, false>(a, ring0, r * RTILE, qb, st);
-                __syncwarp();
-                if (lane == 0 && r + 1 < r1) {
-                    fence_proxy_async();
-                    issue_raw<D>(a, sh, u, r + 1, ring0, &bars[0]);
+            for (int e = e0; e < r1; e++) {
+                // every warp waits for every entry, so that no warp runs a full
+                // ring ahead and tests a slot's barrier two phases early
+                const uint8_t *slot = acquire();
+                if ((e & 3) == warp) {
+                    if (a.raw_bf16) process_raw<D, true>(a, slot, static_cast<long long>(e) * RTILE, qb, st);
+                    else process_raw<D, false>(a, slot, static_cast<long long>(e) * RTILE, qb, st);
                 }
+                release();
             }
-            store_state<D, BV>(st, false, recs, PR);
-            __syncwarp();
-            start_chunks();  // warp 0 joins the packed chunks
+            store_state<D, BV>(st, false, &S.merge[warp][0][0], PR);
+            __syncthreads();
+            cta_merge(recs);
+            __syncthreads();  // S.merge is free again
         } else if (warp == 0 && lane < 4) {
             recs[lane * PR + D] = -INFINITY;  // no 16-bit tiles in this segment
             recs[lane * PR + D + 1] = 0.f;
         }
 
-        // ---- packed chunks: all warps, handed out one at a time ----
+        // ---- packed entries: SUB tokens per warp; record kind 1 ----
         st.init();
-        if (cq0 >= 0) {
+        const int p0 = (e0 > n_rt ? e0 : n_rt) - n_rt, p1 = e1 - n_rt;
+        if (p0 < p1) {
             uint32_t qb[NKS][2];
-            build_qb<D, BK, true, false>(S.q_rot[qs], qb, PermIdentity());
+            load_qb(S, qs, 1, PermIdentity(), qb);
             const float qs_l2 = a.sm_log2 * S.qsum[qs][tig], qm_l2 = a.sm_log2 * S.qmu[qs][tig];
             const float sk_l2 = a.sm_log2 * 16777216.0f;  // 2^24 undoes the operand scaling
-            const long long n_q = a.n_q;
-            int s = 0;
-            for (;;) {
-                const int cur = s ? cq1 : cq0;
-                if (cur < 0) break;
-                if (!mbar_wait(&bars[s], (phase >> s) & 1u, WAIT_LIMIT_NS)) timed_out = true;
-                phase ^= 1u << s;
-                const uint8_t *stg = S.ring[warp] + s * C::STAGE;
-                const long long tok0 = (q0 + cur) * C::CK;
+            const int wv = static_cast<int>(a.n_q) - warp * C::SUB;  // valid tokens of entry 0 for this warp
+            // this warp's records in a slot: keys, value pairs, key meta, value meta
+            const int ok = warp * C::SUB * C::ROWK;
+            const int ov = C::KBYTES + warp * (C::SUB / 2) * C::PAIRV;
+            const int omk = C::KBYTES + C::VBYTES + warp * C::SUB * 2 * C::MB;
+            const int omv = omk + C::MBYTES;
 #pragma unroll 1
-                for (int o = 0; o < C::CK; o += C::SUB)
-                    process_block<D, BK, BV, M16>(stg, o, tok0 + o, n_q, qb, sk_l2, qs_l2, qm_l2, st);
-                __syncwarp();
-                const int nxt = grab_chunk(&S.next_chunk, n_chunks);
-                if (nxt >= 0) src.issue(q0 + nxt, S.ring[warp] + s * C::STAGE, &bars[s]);
-                if (s) cq1 = nxt;
-                else cq0 = nxt;
-                s ^= 1;
+            for (int q = p0; q < p1; q++) {
+                const uint8_t *slot = acquire();
+                const int valid = wv - q * C::ST;
+                if (valid > 0)
+                    process_block<D, BK, BV, M16>(slot + ok, slot + ov, slot + omk, slot + omv, valid, qb, sk_l2,
+                                                  qs_l2, qm_l2, st);
+                release();
             }
         }
         store_state<D, BV>(st, true, &S.merge[warp][0][0], PR);
         __syncthreads();
-        // CTA merge of the 4 warps -> record kind 1
-        for (int idx = threadIdx.x; idx < 4 * PR; idx += blockDim.x) {
-            const int h = idx / PR, c = idx % PR;
-            float M = -INFINITY;
-#pragma unroll
-            for (int w = 0; w < 4; w++) M = fmaxf(M, S.merge[w][h][D]);
-            float v = 0.f;
-            if (c == D) {
-                v = M;
-            } else if (c < D + 2) {
-#pragma unroll
-                for (int w = 0; w < 4; w++) {
-                    const float mw = S.merge[w][h][D];
-                    if (mw != -INFINITY) v += S.merge[w][h][c] * exp2f(mw - M);
-                }
-            }
-            recs[4 * PR + idx] = v;
-        }
+        cta_merge(recs + 4 * PR);
 
         // ---- ticket: the last CTA of the unit merges the records ----
         __threadfence();
@@ -825,7 +873,7 @@ __global__ void __launch_bounds__(128, Cfg<D, BK, BV, M16>::MINB) attn_kernel(At
 // ---- host side -------------------------------------------------------------
 template <int D, int BK, int BV, bool M16>
 struct Launcher {
-    static constexpr int CK = Cfg<D, BK, BV, M16>::CK;
+    static constexpr int ST = Cfg<D, BK, BV, M16>::ST;
     static int occupancy;  // resident CTAs per SM, set on first use
     static size_t smem() { return sizeof(Smem<D, BK, BV, M16>); }
     static int prepare() {
@@ -868,21 +916,22 @@ long long attention_partial_floats(const Layout &L, const AttnArgs &a) {
 }
 
 int plan_attention(const Layout &L, AttnArgs &a, int num_sms, long long cap_floats) {
-    int occ = 0, ck = 0;
+    int occ = 0, st = 0;
     const int e = dispatch(L, [&](auto l) {
         const int r = decltype(l)::prepare();
         occ = decltype(l)::occupancy;
-        ck = decltype(l)::CK;
+        st = decltype(l)::ST;
         return r;
     });
     if (e != 0) return e;
     a.n_rt = a.has_raw ? (a.n_raw_slots + RTILE - 1) / RTILE : 0;
     a.raw_all_valid = a.seq_len >= static_cast<long long>(a.n_sink_cfg) + a.n_recent_cfg;
-    a.n_qc = (a.n_q + ck - 1) / ck;
-    // a unit's items are its packed chunks (its 16-bit tiles ride along with
-    // them), or its 16-bit tiles when it has no packed tokens
-    a.items_per_unit = a.n_qc > 0 ? a.n_qc : a.n_rt;
+    a.n_qc = (a.n_q + st - 1) / st;
+    // a unit's pipeline entries: its 16-slot tiles of 16-bit tokens, then its
+    // packed entries of st tokens
+    a.items_per_unit = a.n_rt + a.n_qc;
     a.total_items = static_cast<long long>(L.U) * a.items_per_unit;
+    if (a.total_items >= (1LL << 31)) return static_cast<int>(cudaErrorInvalidValue);  // entries are indexed in 32 bits
     long long G = static_cast<long long>(num_sms) * occ;
     if (const char *env = std::getenv("DQ_ATTN_GRID")) G = std::atoll(env);
     if (G > a.total_items) G = a.total_items;

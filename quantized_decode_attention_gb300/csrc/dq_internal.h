@@ -69,8 +69,8 @@ struct AttnArgs {
     int has_raw;            // 1 if the unit has 16-bit slots
     int raw_all_valid;      // seq_len >= n_sink + n_recent: every 16-bit slot is in use
     int n_rt;               // 16-slot tiles of 16-bit tokens per unit
-    long long n_qc;         // 64-token chunks of packed tokens per unit
-    long long items_per_unit, total_items;
+    long long n_qc;         // packed pipeline entries per unit (128 tokens each, the last ragged)
+    long long items_per_unit, total_items;  // pipeline entries: n_rt + n_qc per unit
     int grid;               // persistent CTAs (one wave)
     int max_slots;          // partial-record slots per unit
     float sm_log2;          // sm_scale * log2(e)
