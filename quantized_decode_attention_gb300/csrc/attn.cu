@@ -26,11 +26,12 @@
 //    columns are 4 query heads x (hi, lo) binary16 halves of an fp32 operand,
 //    adjacent, so each lane owns one head and adds its halves in registers.
 //    P' is transposed into the B operand with movmatrix (no shared memory).
-//  * Softmax bookkeeping once per chunk; the running max may lag by 2^8, so
-//    the accumulators are rescaled only when it grows by more than that.
-//  * Each CTA merges its 4 warps and writes one partial per (unit, kind);
-//    the last CTA to finish a unit (atomic ticket, no waiting) merges them,
-//    rotates the value accumulator back and writes the output.
+//  * Softmax bookkeeping once per 32 tokens; the running max may lag by 2^8,
+//    so the accumulators are rescaled only when it grows by more than that.
+//  * Each CTA merges its 4 warps and writes one partial per (unit, kind); a
+//    second grid, launched as a programmatic dependent of the first, waits for
+//    it to finish, merges each unit's partials, rotates the value accumulator
+//    back and writes the output.
 #include <cuda_runtime.h>
 
 #include <cstdlib>
@@ -45,7 +46,7 @@ constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;   // 2 s; a healthy copy takes
 constexpr float RESCALE_SLACK = 8.0f;               // log2 units the running max may lag
 
 struct AttnShape {
-    int Hkv, G, D;
+    int U, Hkv, G, D;
     long long qcap;
     int rcap;
 };
@@ -235,7 +236,6 @@ struct Smem {
     };
     uint64_t full[C::NST];         // slot filled (transaction count of its copies)
     unsigned rel[C::NST];          // releases of a slot so far (4 per entry)
-    int last;
     alignas(128) uint8_t ring[C::NST][C::SLOT];
 };
 
@@ -508,13 +508,13 @@ __device__ __forceinline__ void vadd(float (&acc)[2], const float2 &v, float w) 
     acc[0] += v.x * w; acc[1] += v.y * w;
 }
 
-// The last CTA of a unit: merge its split records, rotate the value
-// accumulator back, normalize and write the output; reset the ticket.
-// Records are read in batches of 8 whose loads are all in flight together,
-// merged with a running maximum.
+// Merge the split records of unit u, rotate the value accumulator back,
+// normalize and write the output.
+// Records are read in batches of 16 whose loads are all in flight together
+// (one batch for up to 8 CTAs per unit), merged with a running maximum.
 template <int D, int PR>
-__device__ __noinline__ void combine_unit(const AttnArgs &a, const AttnShape &sh, int u, int n_ctas) {
-    constexpr int V = D / 32, NB = 8;
+__device__ __forceinline__ void combine_unit(const AttnArgs &a, const AttnShape &sh, int u, int n_ctas) {
+    constexpr int V = D / 32, NB = 16;
     using VT = typename VecT<V>::T;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int b = u / sh.Hkv, kvh = u % sh.Hkv;
@@ -551,7 +551,8 @@ __device__ __noinline__ void combine_unit(const AttnArgs &a, const AttnShape &sh
             }
 #pragma unroll
             for (int k = 0; k < NB; k++) {
-                const float w = mr[k] == -INFINITY ? 0.f : exp2f(mr[k] - M);
+                if (mr[k] == -INFINITY) continue;  // empty record: its value row was never written
+                const float w = exp2f(mr[k] - M);
                 Lsum += lr[k] * w;
                 if ((r0 + k) & 1) vadd(accq, vv[k], w);
                 else vadd(accr, vv[k], w);
@@ -573,7 +574,6 @@ __device__ __noinline__ void combine_unit(const AttnArgs &a, const AttnShape &sh
             else reinterpret_cast<__nv_bfloat16 *>(a.out)[oi] = __float2bfloat16_rn(y);
         }
     }
-    if (threadIdx.x == 0) a.counters[u] = 0;
 }
 
 // One lane's share of a unit's query head (warp h takes head h; lane l holds
@@ -696,6 +696,8 @@ __global__ void __launch_bounds__(128, Cfg<D, BK, BV, M16>::MINB) attn_kernel(At
     const int ipu = static_cast<int>(a.items_per_unit), n_rt = a.n_rt;
     const long long x0 = static_cast<long long>(i) * N / G, x1 = static_cast<long long>(i + 1) * N / G;
     const int n_ent = static_cast<int>(x1 - x0);
+    // the combine grid may be scheduled now; it waits for this whole grid
+    asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
     if (n_ent <= 0 || ipu <= 0) return;
     const int u_first = static_cast<int>(x0 / ipu), u_lastc = static_cast<int>((x1 - 1) / ipu);
     bool timed_out = false;
@@ -798,7 +800,7 @@ __global__ void __launch_bounds__(128, Cfg<D, BK, BV, M16>::MINB) attn_kernel(At
             prep_query<D, BK, BV, M16>(a, sh, S, qs, u, qin);
             __syncthreads();
         }
-        const int first = owner(ub, N, G), last = owner(ub + ipu - 1, N, G);
+        const int first = owner(ub, N, G);
         float *recs = a.partials + (static_cast<long long>(u) * a.max_slots + (i - first)) * 2 * 4 * PR;
         WarpState<D / 16> st;
 
@@ -854,20 +856,43 @@ __global__ void __launch_bounds__(128, Cfg<D, BK, BV, M16>::MINB) attn_kernel(At
         store_state<D, BV>(st, true, &S.merge[warp][0][0], PR);
         __syncthreads();
         cta_merge(recs + 4 * PR);
-
-        // ---- ticket: the last CTA of the unit merges the records ----
+        // publish: the records are visible GPU-wide before the unit's count moves
         __threadfence();
         __syncthreads();
-        if (threadIdx.x == 0) {
-            const int t = atomicAdd(a.counters + u, 1);
-            S.last = (t == last - first);
-        }
-        __syncthreads();
-        if (!S.last) continue;
-        __threadfence();
-        combine_unit<D, PR>(a, sh, u, last - first + 1);
+        if (threadIdx.x == 0) atomicAdd(a.counters + u, 1);
     }
     if (timed_out && lane == 0) atomicOr(a.status, ST_TIMEOUT);
+}
+
+// The split records of unit u -> output.  This grid is a programmatic
+// dependent of the attention grid, so its CTAs can start as SMs free up; CTA u
+// waits (bounded) until all CTAs that touch unit u have published their
+// records, merges them and clears the unit's count for the next call.  The
+// attention grid never waits on this one, so the wait always ends.
+template <int D>
+__global__ void __launch_bounds__(128) combine_kernel(AttnArgs a, AttnShape sh) {
+    __shared__ int ok;
+    const int u = blockIdx.x;
+    const long long N = a.total_items, ipu = a.items_per_unit;
+    const int first = owner(static_cast<long long>(u) * ipu, N, a.grid);
+    const int last = owner(static_cast<long long>(u) * ipu + ipu - 1, N, a.grid);
+    if (threadIdx.x == 0) {
+        const int need = last - first + 1;
+        const uint64_t t0 = global_ns();
+        int got;
+        for (;;) {
+            asm volatile("ld.acquire.gpu.global.b32 %0, [%1];\n" : "=r"(got) : "l"(a.counters + u) : "memory");
+            if (got >= need || global_ns() - t0 > WAIT_LIMIT_NS) break;
+            __nanosleep(256);
+        }
+        ok = got >= need;
+        if (!ok) atomicOr(a.status, ST_TIMEOUT);
+    }
+    __syncthreads();
+    if (!ok) return;
+    combine_unit<D, D + 4>(a, sh, u, last - first + 1);
+    __syncthreads();
+    if (threadIdx.x == 0) a.counters[u] = 0;
 }
 
 // ---- host side -------------------------------------------------------------
@@ -889,8 +914,20 @@ struct Launcher {
         return 0;
     }
     static int launch(const AttnArgs &a, const AttnShape &sh, void *stream) {
-        attn_kernel<D, BK, BV, M16><<<a.grid, 128, smem(), static_cast<cudaStream_t>(stream)>>>(a, sh);
-        return static_cast<int>(cudaGetLastError());
+        const cudaStream_t st = static_cast<cudaStream_t>(stream);
+        attn_kernel<D, BK, BV, M16><<<a.grid, 128, smem(), st>>>(a, sh);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return static_cast<int>(e);
+        cudaLaunchConfig_t lc = {};
+        lc.gridDim = dim3(static_cast<unsigned>(sh.U));
+        lc.blockDim = dim3(128);
+        lc.stream = st;
+        cudaLaunchAttribute at[1];
+        at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        at[0].val.programmaticStreamSerializationAllowed = 1;
+        lc.attrs = at;
+        lc.numAttrs = 1;
+        return static_cast<int>(cudaLaunchKernelEx(&lc, combine_kernel<D>, a, sh));
     }
 };
 template <int D, int BK, int BV, bool M16>
@@ -949,7 +986,7 @@ int plan_attention(const Layout &L, AttnArgs &a, int num_sms, long long cap_floa
 }
 
 int launch_attention(const Layout &L, const AttnArgs &a, int, void *stream) {
-    AttnShape sh{L.Hkv, L.G, L.d, L.qcap, L.rcap};
+    AttnShape sh{L.U, L.Hkv, L.G, L.d, L.qcap, L.rcap};
     return dispatch(L, [&](auto l) { return decltype(l)::launch(a, sh, stream); });
 }
 

@@ -161,6 +161,11 @@ __device__ __forceinline__ uint64_t global_ns() {
     return t;
 }
 
+// Longest a single try_wait may suspend the thread before it reports "not yet"
+// (it returns as soon as the phase completes): waiting warps then sleep instead
+// of spinning and leave the issue slots to the warps doing arithmetic.
+constexpr unsigned WAIT_SUSPEND_NS = 1000000;
+
 // Wait for phase `parity` of an mbarrier for at most `limit_ns` nanoseconds of
 // wall time (try_wait may itself suspend for a while, so the bound is taken
 // on the global timer, not on the number of polls).  Returns false on timeout.
@@ -170,10 +175,10 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, unsigned parity, uint64
     for (unsigned it = 0;; ++it) {
         uint32_t done;
         asm volatile(
-            "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+            "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
             " selp.u32 %0, 1, 0, p;\n}\n"
             : "=r"(done)
-            : "r"(addr), "r"(parity)
+            : "r"(addr), "r"(parity), "n"(WAIT_SUSPEND_NS)
             : "memory");
         if (done) return true;
         if (it == 0) t0 = global_ns();

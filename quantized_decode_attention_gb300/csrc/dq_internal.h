@@ -75,8 +75,8 @@ struct AttnArgs {
     int max_slots;          // partial-record slots per unit
     float sm_log2;          // sm_scale * log2(e)
     float hscale;
-    float *partials;        // [U][max_slots][2 kinds][4 heads][d + 2]
-    int *counters;          // [U], zero between calls
+    float *partials;        // [U][max_slots][2 kinds][4 heads][d + 4]
+    int *counters;          // [U] CTAs done with the unit; zero between calls
     unsigned *status;
 };
 
