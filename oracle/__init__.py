@@ -5,7 +5,7 @@ arm of ``bench.py`` may import this package.  The CUDA library never does, and
 this package never imports the CUDA library: the two share nothing but the
 seeded input generators in ``workloads.py``.
 
-The arithmetic lives in plain C (``affine.c``, ``format.c``), compiled with
+The arithmetic lives in plain C (``affine.c``, ``format.c``, ``nuq.c``), compiled with
 ``-O2 -ffp-contract=off`` into ``liboracle.so``; this module only marshals
 arguments and assembles whole-cache buffers from per-token C results.
 """
@@ -82,6 +82,17 @@ def lib():
             L.or_raw_v_index.argtypes = [C.c_int, C.c_int, C.c_int]
             L.or_raw_slot.restype = C.c_int
             L.or_raw_slot.argtypes = [C.c_long, C.c_int, C.c_int]
+            _u16 = _P(dtype=np.uint16, flags="C_CONTIGUOUS")
+            L.or_topk_abs.argtypes = [_f32, C.c_int, C.c_int, _u8]
+            L.or_outlier_count.restype = C.c_int
+            L.or_outlier_count.argtypes = [C.c_float, C.c_int]
+            L.or_r32_sum.restype = C.c_float
+            L.or_r32_sum.argtypes = [_f32, C.c_int]
+            L.or_nuq_fit.restype = C.c_int
+            L.or_nuq_fit.argtypes = [_f32, C.c_void_p, C.c_int, C.c_int, C.c_int, _f32, C.c_void_p]
+            L.or_nuq_assign.argtypes = [_f32, C.c_int, _u16, C.c_int, _u8]
+            L.or_nuq_vector.restype = C.c_int
+            L.or_nuq_vector.argtypes = [_f32, C.c_int, C.c_int, C.c_int, C.c_float, _u8, _u16, _u8]
             _lib = L
         return _lib
 
@@ -184,6 +195,54 @@ def unpack_v_token(rec, d: int, bits: int, e: int) -> np.ndarray:
 
 def raw_slot(t: int, n_sink: int, n_recent: int) -> int:
     return lib().or_raw_slot(t, n_sink, n_recent)
+
+
+def topk_abs(x, k: int) -> np.ndarray:
+    """Rank-based top-k by |x| (ties to the lower index) -> bool mask."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    flag = np.zeros(x.size, dtype=np.uint8)
+    lib().or_topk_abs(x, x.size, int(k), flag)
+    return flag.astype(bool)
+
+
+def outlier_count(f: float, n: int) -> int:
+    return int(lib().or_outlier_count(float(f), int(n)))
+
+
+def r32_sum(x) -> float:
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    return float(lib().or_r32_sum(x, x.size))
+
+
+def nuq_fit(x, levels: int, iters: int, exclude=None):
+    """Lloyd-Max levels of the non-excluded values: (fp32 levels, fp16 bits, n_fit)."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    lev = np.zeros(levels, dtype=np.float32)
+    lut = np.zeros(levels, dtype=np.uint16)
+    ex = None
+    if exclude is not None:
+        ex = np.ascontiguousarray(exclude, dtype=np.uint8)
+    nf = lib().or_nuq_fit(x, None if ex is None else ex.ctypes.data_as(C.c_void_p), x.size, levels, iters, lev,
+                          lut.ctypes.data_as(C.c_void_p))
+    return lev, lut, nf
+
+
+def nuq_assign(x, lut16) -> np.ndarray:
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    lut16 = np.ascontiguousarray(lut16, dtype=np.uint16)
+    codes = np.zeros(x.size, dtype=np.uint8)
+    lib().or_nuq_assign(x, x.size, lut16, lut16.size, codes)
+    return codes
+
+
+def nuq_vector(x, bits: int, iters: int, frac: float):
+    """One vector: (outlier mask, fp16 table, codes)."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    flag = np.zeros(x.size, dtype=np.uint8)
+    lut = np.zeros(1 << bits, dtype=np.uint16)
+    codes = np.zeros(x.size, dtype=np.uint8)
+    lib().or_nuq_vector(x, x.size, bits, iters, float(frac), flag, lut, codes)
+    return flag.astype(bool), lut, codes
 
 
 def attention_f64(q: np.ndarray, K: np.ndarray, V: np.ndarray, sm_scale: float) -> np.ndarray:
