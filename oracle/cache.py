@@ -113,6 +113,85 @@ def quantize_tensor(w: W.Workload, x_bits: np.ndarray, is_key: bool, S: int,
     return QuantTensor(codes, s, o, mu, xhat)
 
 
+@dataclass
+class NuqTensor:
+    """Oracle result for one tensor under the non-uniform (Lloyd-Max) scheme.
+
+    "KVQuant-NUQ" page, Quantization axes: keys get one table per channel over
+    the quantized tokens, values one table per token over its channels; the
+    outliers of each vector (exactly k by rank) keep their fp16 value."""
+    codes: np.ndarray     # [B, H, Sq, d] uint8 nearest-level codes (outliers included)
+    lut: np.ndarray       # keys [B, H, d, L], values [B, H, Sq, L]: fp16 bits
+    outlier: np.ndarray   # [B, H, Sq, d] bool
+    val16: np.ndarray     # [B, H, Sq, d] uint16: fp16 bits of the input (outlier values)
+    xhat: np.ndarray      # [B, H, Sq, d] float32: table value, or the outlier's fp16 value
+
+
+def quantize_nuq(w: W.Workload, x_bits: np.ndarray, is_key: bool, S: int) -> NuqTensor:
+    """Prefill of tokens [n_sink, S) of x_bits [B,H,S,d] under the NUQ scheme."""
+    from . import nuq_vector
+    B, H, n, d = x_bits.shape
+    x = _f32_input(x_bits, w.kv_dtype)[:, :, w.n_sink:S]
+    nq = x.shape[2]
+    L = 1 << w.bits
+    iters, frac = w.extra.get("lloyd_iters", 8), w.extra.get("outlier_frac", 0.01)
+    codes = np.zeros((B, H, nq, d), dtype=np.uint8)
+    out = np.zeros((B, H, nq, d), dtype=bool)
+    lut = np.zeros((B, H, d if is_key else nq, L), dtype=np.uint16)
+    for b in range(B):
+        for h in range(H):
+            if is_key:
+                for c in range(d):
+                    fl, lu, co = nuq_vector(np.ascontiguousarray(x[b, h, :, c]), w.bits, iters, frac)
+                    codes[b, h, :, c], out[b, h, :, c], lut[b, h, c] = co, fl, lu
+            else:
+                for t in range(nq):
+                    fl, lu, co = nuq_vector(np.ascontiguousarray(x[b, h, t]), w.bits, iters, frac)
+                    codes[b, h, t], out[b, h, t], lut[b, h, t] = co, fl, lu
+    # fp16 rounding (RNE) as a library primitive; the oracle's own binary16
+    # conversion is pinned against the same numpy cast
+    val16 = x.astype(np.float16).view(np.uint16)
+    levels = lut.view(np.float16).astype(np.float32)
+    if is_key:
+        tab = np.take_along_axis(levels[:, :, None, :, :], codes[..., None].astype(np.int64), axis=-1)[..., 0]
+    else:
+        tab = np.take_along_axis(levels[:, :, :, None, :], codes[..., None].astype(np.int64), axis=-1)[..., 0]
+    xhat = np.where(out, val16.view(np.float16).astype(np.float32), tab).astype(np.float32)
+    return NuqTensor(codes, lut, out, val16, xhat)
+
+
+def nuq_key_outliers_csr(nt: NuqTensor, qcap: int, nnz_cap: int):
+    """Key side channel by token: rowptr [B,H,qcap+1] int32, col/val [B,H,nnz_cap]
+    uint16 (channel, fp16 bits), a token's entries in channel order."""
+    B, H, nq, d = nt.outlier.shape
+    rowptr = np.zeros((B, H, qcap + 1), dtype=np.int32)
+    col = np.zeros((B, H, nnz_cap), dtype=np.uint16)
+    val = np.zeros((B, H, nnz_cap), dtype=np.uint16)
+    for b in range(B):
+        for h in range(H):
+            cnt = nt.outlier[b, h].sum(axis=1)
+            rowptr[b, h, 1:nq + 1] = np.cumsum(cnt)
+            rowptr[b, h, nq + 1:] = rowptr[b, h, nq]
+            tt, cc = np.nonzero(nt.outlier[b, h])          # row-major: tokens ascending, channels ascending
+            col[b, h, :len(cc)] = cc
+            val[b, h, :len(cc)] = nt.val16[b, h, tt, cc]
+    return rowptr, col, val
+
+
+def nuq_value_outliers(nt: NuqTensor, qcap: int, k: int):
+    """Value side channel, exactly k per token: col/val [B,H,qcap,k] in channel order."""
+    B, H, nq, d = nt.outlier.shape
+    col = np.zeros((B, H, qcap, k), dtype=np.uint16)
+    val = np.zeros((B, H, qcap, k), dtype=np.uint16)
+    for b in range(B):
+        for h in range(H):
+            for t in range(nq):
+                cc = np.flatnonzero(nt.outlier[b, h, t])
+                col[b, h, t, :len(cc)] = cc
+                val[b, h, t, :len(cc)] = nt.val16[b, h, t, cc]
+    return col, val
+
+
 def pack_k(codes: np.ndarray, bits: int) -> np.ndarray:
     """[..., n, d] codes -> [..., n, row_bytes] key records."""
     lead = codes.shape[:-1]
@@ -186,7 +265,10 @@ def attention(w: W.Workload, q: np.ndarray, k_bits: np.ndarray, v_bits: np.ndarr
         K[:n_s], V[:n_s] = kr[:n_s], vr[:n_s]
         K[q_hi:S], V[q_hi:S] = kr[q_hi:S], vr[q_hi:S]
         nq = q_hi - n_s
-        if nq > 0:
+        if nq > 0 and isinstance(qk, NuqTensor):
+            K[n_s:q_hi] = qk.xhat[b, h, :nq].astype(np.float64)
+            V[n_s:q_hi] = qv.xhat[b, h, :nq].astype(np.float64)
+        elif nq > 0:
             for X, qt, key in ((K, qk, True), (V, qv, False)):
                 rot = _ROT[w.rot_k if key else w.rot_v]
                 cu = np.ascontiguousarray(qt.codes[b, h, :nq])
@@ -216,5 +298,6 @@ def _attn(L, q, K, V, sm_scale):
     return o
 
 
-__all__ = ["QuantTensor", "quantize_tensor", "pack_k", "pack_v", "meta_f16_bits", "raw_regions",
+__all__ = ["QuantTensor", "quantize_tensor", "NuqTensor", "quantize_nuq", "nuq_key_outliers_csr",
+           "nuq_value_outliers", "pack_k", "pack_v", "meta_f16_bits", "raw_regions",
            "attention", "raw16_bits", "raw16_to_f64", "raw_dtype"]

@@ -21,7 +21,8 @@
  *    token (sample axis = channels).
  * Readings where the page is silent (all stated with the tests):
  *  - k = floor(f * n + 0.5); ties in |x| go to the lower index.
- *  - Quantile init: level i = sorted[floor((2i+1) * n / (2L))] of the n fit values.
+ *  - Quantile init: level i = sorted[floor((2i+1) * n / (2L))] of the n fit values
+ *    (a -0 among them counts as +0, so equal values have one bit pattern).
  *  - Assignment ties go to the lower level; an empty level keeps its value.
  *  - A level's new value is (sum of its values) / count in fp32, the sum taken
  *    in the canonical order R32 over the vector's positions: lane l = p mod 32
@@ -121,7 +122,7 @@ int or_nuq_fit(const float *x, const uint8_t *excl, int n, int L, int iters, flo
     uint8_t *asg = (uint8_t *)malloc((size_t)(n > 0 ? n : 1));
     int nf = 0;
     for (int p = 0; p < n; p++)
-        if (!excl || !excl[p]) fit[nf++] = x[p];
+        if (!excl || !excl[p]) fit[nf++] = x[p] + 0.0f;  /* -0 -> +0: equal values sort to equal bits */
     if (nf == 0) {
         for (int i = 0; i < L; i++) lev32[i] = 0.0f;
     } else {

@@ -95,7 +95,8 @@ def _raise(st: int):
 
 def make_config(*, batch, n_kv_heads, n_q_heads, head_dim, max_seq, kv_dtype="bf16", meta_dtype="f16",
                 out_dtype="bf16", bits=2, bits_v=None, rot_k="hadamard", rot_v="hadamard", mean_k=True,
-                clip_k=0.0, clip_v=None, n_sink=0, n_recent=0, scheme="affine") -> Config:
+                clip_k=0.0, clip_v=None, n_sink=0, n_recent=0, scheme="affine", lloyd_iters=8,
+                outlier_frac=0.01) -> Config:
     c = Config()
     c.batch, c.n_kv_heads, c.n_q_heads, c.head_dim, c.max_seq = batch, n_kv_heads, n_q_heads, head_dim, max_seq
     c.kv_dtype, c.meta_dtype, c.out_dtype = DTYPES[kv_dtype], DTYPES[meta_dtype], DTYPES[out_dtype]
@@ -106,6 +107,9 @@ def make_config(*, batch, n_kv_heads, n_q_heads, head_dim, max_seq, kv_dtype="bf
     c.k.clip = clip_k
     c.v.clip = clip_k if clip_v is None else clip_v
     c.n_sink, c.n_recent = n_sink, n_recent
+    if scheme == "nuq":
+        c.k.lloyd_iters = c.v.lloyd_iters = lloyd_iters
+        c.k.outlier_frac = c.v.outlier_frac = outlier_frac
     c.rans_alpha, c.rans_prob_bits = 1.4, 8
     return c
 

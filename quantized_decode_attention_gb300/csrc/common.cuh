@@ -90,6 +90,28 @@ __host__ __device__ __forceinline__ int field_exp(int r, int bits) {
     return f <= 4 ? 2 * f : 2 * (f - 5);
 }
 
+// ---- record packing (writers) -----------------------------------------------
+// Number of 32-bit words in a key row / a value pair record.
+template <int D, int BITS>
+struct Rec {
+    static constexpr int K_WORDS = D * BITS / 32;
+    static constexpr int V_WORDS = 2 * D * BITS / 32;
+};
+
+// OR-contribution of one code to word w of a key row (BITS 2/4: one plane;
+// BITS 3: 2-bit plane words first, then the 1-bit plane).
+template <int D, int BITS>
+__device__ __forceinline__ uint32_t contrib(int w, int idx, int half, uint32_t m, int words_lo) {
+    if (BITS == 3) {
+        uint32_t v = 0;
+        if (w == idx / 8) v |= (m & 3u) << (16 * half + 2 * (idx % 8));
+        if (w == words_lo + idx / 16) v |= ((m >> 2) & 1u) << (16 * half + (idx % 16));
+        return v;
+    }
+    constexpr int F = 16 / BITS;
+    return (w == idx / F) ? (m << (16 * half + BITS * (idx % F))) : 0u;
+}
+
 // ---- mma.sync m16n8k16, fp32 accumulate -----------------------------------
 __device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
                                         uint32_t a3, uint32_t b0, uint32_t b1) {

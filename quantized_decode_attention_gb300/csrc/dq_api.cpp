@@ -35,8 +35,16 @@ long long round_up(long long x, long long m) { return (x + m - 1) / m * m; }
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 dq_status validate_tensor(const dq_tensor_cfg &t, int d, bool key, const char *name) {
-    if (t.scheme != DQ_AFFINE) return fail(DQ_EUNSUPPORTED, "%s: only the affine scheme is built", name);
+    if (t.scheme != DQ_AFFINE && t.scheme != DQ_NUQ)
+        return fail(DQ_EUNSUPPORTED, "%s: only the affine and non-uniform schemes are built", name);
     if (t.bits < 2 || t.bits > 4) return fail(DQ_EINVAL, "%s: bits must be 2, 3 or 4 (got %d)", name, t.bits);
+    if (t.scheme == DQ_NUQ) {
+        if (t.rot != DQ_ROT_NONE || t.mean || t.clip != 0.0f)
+            return fail(DQ_EUNSUPPORTED, "%s: the non-uniform scheme takes no rotation, mean or clip", name);
+        if (t.lloyd_iters < 0 || t.lloyd_iters > 64) return fail(DQ_EINVAL, "%s: lloyd_iters outside [0, 64]", name);
+        if (!(t.outlier_frac >= 0.0f && t.outlier_frac < 0.5f))
+            return fail(DQ_EINVAL, "%s: outlier_frac outside [0, 0.5)", name);
+    }
     if (t.bits == 3 && d != 128) return fail(DQ_EUNSUPPORTED, "%s: 3-bit records need head_dim 128", name);
     if (t.rot < DQ_ROT_NONE || t.rot > DQ_ROT_DENSE) return fail(DQ_EINVAL, "%s: bad rotation %d", name, t.rot);
     if (!key && t.rot == DQ_ROT_DENSE) return fail(DQ_EUNSUPPORTED, "%s: dense transform is for keys", name);
@@ -72,6 +80,10 @@ dq_status make_layout(const dq_config *cfg, Layout *L) {
     if ((s = validate_tensor(c.k, c.head_dim, true, "k")) != DQ_OK) return s;
     if ((s = validate_tensor(c.v, c.head_dim, false, "v")) != DQ_OK) return s;
     if (c.k.bits != c.v.bits) return fail(DQ_EUNSUPPORTED, "keys and values must use the same code width");
+    if (c.k.scheme != c.v.scheme) return fail(DQ_EUNSUPPORTED, "keys and values must use the same scheme");
+    if (c.k.scheme == DQ_NUQ && c.max_seq - c.n_sink > 8192)
+        return fail(DQ_EUNSUPPORTED, "non-uniform key fit: at most 8192 quantized tokens (got %d)",
+                    c.max_seq - c.n_sink);
 
     Layout &l = *L;
     std::memset(&l, 0, sizeof l);
@@ -91,16 +103,34 @@ dq_status make_layout(const dq_config *cfg, Layout *L) {
     l.n_sink = c.n_sink;
     l.n_recent = c.n_recent;
     const size_t U = static_cast<size_t>(l.U), d = static_cast<size_t>(l.d);
+    l.scheme = c.k.scheme;
+    l.levels = 1 << c.k.bits;
+    const bool nuq = l.scheme == DQ_NUQ;
+    if (nuq) {
+        l.k_out_cap = dq::nuq_outlier_count(c.k.outlier_frac, c.max_seq - c.n_sink);
+        l.nnzk_cap = round_up(static_cast<long long>(d) * l.k_out_cap, 8);
+        l.k_out_v = dq::nuq_outlier_count(c.v.outlier_frac, c.head_dim);
+        l.rp_stride = l.qcap + 4;
+    }
     l.sz[0] = U * l.qcap * l.rowK;                          // codes_k
     l.sz[1] = U * (l.qcap / 2) * l.pairV;                   // codes_v
-    l.sz[2] = U * l.qcap * 2 * l.meta_bytes;                // meta_k
-    l.sz[3] = U * l.qcap * 2 * l.meta_bytes;                // meta_v
+    l.sz[2] = nuq ? 0 : U * l.qcap * 2 * l.meta_bytes;      // meta_k
+    l.sz[3] = nuq ? 0 : U * l.qcap * 2 * l.meta_bytes;      // meta_v
     l.sz[4] = c.k.mean ? U * d * 4 : 0;                     // mean_k
-    l.sz[5] = 0;                                            // lut_k
-    l.sz[6] = 0;                                            // lut_v
+    l.sz[5] = nuq ? U * d * l.levels * 2 : 0;               // lut_k
+    l.sz[6] = nuq ? U * l.qcap * l.levels * 2 : 0;          // lut_v
     l.sz[7] = U * l.rcap * d * 2;                           // raw_k
     l.sz[8] = U * l.rcap * d * 2;                           // raw_v
     for (int i = 9; i < 15; i++) l.sz[i] = 0;               // outlier side-channels
+    if (nuq && l.k_out_cap > 0) {
+        l.sz[9] = U * l.rp_stride * 4;                      // ol_rowptr_k
+        l.sz[10] = U * l.nnzk_cap * 2;                      // ol_col_k
+        l.sz[11] = l.sz[10];                                // ol_val_k
+    }
+    if (nuq && l.k_out_v > 0) {
+        l.sz[13] = U * l.qcap * l.k_out_v * 2;              // ol_col_v
+        l.sz[14] = l.sz[13];                                // ol_val_v
+    }
     l.sz[15] = c.k.rot == DQ_ROT_DENSE ? static_cast<size_t>(c.n_kv_heads) * d * d * 4 : 0;  // k_transform
     l.sz[16] = l.sz[15];                                    // q_comp
     return DQ_OK;
@@ -152,10 +182,14 @@ static dq_status get_ctx(dq_ctx **pctx, const dq_config *cfg, const Layout &L) {
     cudaError_t e1 = cudaMalloc(&c->status, sizeof(unsigned));
     cudaError_t e2 = cudaMalloc(&c->partials, c->partials_cap * sizeof(float));
     cudaError_t e3 = cudaMalloc(&c->counters, sizeof(int) * L.U);
-    if (e1 != cudaSuccess || e2 != cudaSuccess || e3 != cudaSuccess) {
+    cudaError_t e4 = cudaSuccess;
+    if (L.scheme == DQ_NUQ)
+        e4 = cudaMalloc(&c->nuq_bits, static_cast<size_t>(L.U) * L.qcap * (L.d / 32) * sizeof(uint32_t));
+    if (e1 != cudaSuccess || e2 != cudaSuccess || e3 != cudaSuccess || e4 != cudaSuccess) {
         cudaFree(c->status);
         cudaFree(c->partials);
         cudaFree(c->counters);
+        cudaFree(c->nuq_bits);
         delete c;
         cudaGetLastError();
         return fail(DQ_ENOMEM, "workspace allocation failed");
@@ -167,6 +201,59 @@ static dq_status get_ctx(dq_ctx **pctx, const dq_config *cfg, const Layout &L) {
     }
     *pctx = c;
     return DQ_OK;
+}
+
+// Non-uniform scheme, prefill only ("KVQuant-NUQ" page, Quantization axes: key
+// tables are fit at prefill and frozen; appending decode tokens needs the
+// frozen per-channel outlier threshold, which is not built).
+static dq_status quantize_nuq(dq_ctx *c, const dq_config *cfg, const Layout &L, const dq_kv_buffers *bufs,
+                              const void *k, const void *v, long long pos0, long long n_tok, void *stream) {
+    if (pos0 != 0)
+        return fail(DQ_EUNSUPPORTED, "non-uniform scheme: only a prefill from position 0 is built (no appends)");
+    const cudaStream_t st = static_cast<cudaStream_t>(stream);
+    dq::QuantArgs a{};
+    a.in_dtype = cfg->kv_dtype;
+    a.pos0 = 0;
+    a.n_tok = n_tok;
+    a.seq_after = n_tok;
+    a.bits = cfg->k.bits;
+    a.status = c->status;
+    a.n_fit = static_cast<int>(n_tok > L.n_sink ? n_tok - L.n_sink : 0);
+    int e;
+    // values: per-token tables, codes and side channel; raw copies
+    a.x = v;
+    a.is_key = 0;
+    a.codes = static_cast<uint8_t *>(bufs->codes_v);
+    a.raw = static_cast<uint16_t *>(bufs->raw_v);
+    a.lut = static_cast<uint16_t *>(bufs->lut_v);
+    a.ol_col = static_cast<uint16_t *>(bufs->ol_col_v);
+    a.ol_val = static_cast<uint16_t *>(bufs->ol_val_v);
+    a.k_out = L.k_out_v;
+    a.iters = cfg->v.lloyd_iters;
+    if ((e = dq::launch_nuq_values(L, a, stream)) != 0)
+        return fail(DQ_ECUDA, "value quantize launch: %s", cudaGetErrorString(static_cast<cudaError_t>(e)));
+    // keys: per-channel tables and outlier bitmap, then codes, then side channel
+    a.x = k;
+    a.is_key = 1;
+    a.codes = static_cast<uint8_t *>(bufs->codes_k);
+    a.raw = static_cast<uint16_t *>(bufs->raw_k);
+    a.lut = static_cast<uint16_t *>(bufs->lut_k);
+    a.olbits = c->nuq_bits;
+    a.ol_rowptr = static_cast<int *>(bufs->ol_rowptr_k);
+    a.ol_col = static_cast<uint16_t *>(bufs->ol_col_k);
+    a.ol_val = static_cast<uint16_t *>(bufs->ol_val_k);
+    a.k_out = dq::nuq_outlier_count(cfg->k.outlier_frac, a.n_fit);
+    a.iters = cfg->k.lloyd_iters;
+    if (cudaMemsetAsync(c->nuq_bits, 0, static_cast<size_t>(L.U) * L.qcap * (L.d / 32) * sizeof(uint32_t), st) !=
+        cudaSuccess)
+        return fail(DQ_ECUDA, "clearing the key outlier bitmap failed");
+    if (a.n_fit > 0 && (e = dq::launch_nuq_key_fit(L, a, stream)) != 0)
+        return fail(DQ_ECUDA, "key fit launch: %s", cudaGetErrorString(static_cast<cudaError_t>(e)));
+    if ((e = dq::launch_nuq_key_codes(L, a, stream)) != 0)
+        return fail(DQ_ECUDA, "key quantize launch: %s", cudaGetErrorString(static_cast<cudaError_t>(e)));
+    if (L.k_out_cap > 0 && (e = dq::launch_nuq_key_csr(L, a, stream)) != 0)
+        return fail(DQ_ECUDA, "key side-channel launch: %s", cudaGetErrorString(static_cast<cudaError_t>(e)));
+    return ok();
 }
 
 extern "C" {
@@ -208,6 +295,7 @@ dq_status dq_quantize_kv(dq_ctx **ctx, const dq_config *cfg, const dq_kv_buffers
     if ((s = check_bufs(L, bufs)) != DQ_OK) return s;
     if (!aligned16(k) || !aligned16(v)) return fail(DQ_EALIGN, "k / v input not 16-byte aligned");
     if ((s = get_ctx(ctx, cfg, L)) != DQ_OK) return s;
+    if (L.scheme == DQ_NUQ) return quantize_nuq(*ctx, cfg, L, bufs, k, v, pos0, n_tok, stream);
 
     for (int which = 0; which < 2; which++) {
         const dq_tensor_cfg &t = which == 0 ? cfg->k : cfg->v;
@@ -261,6 +349,7 @@ dq_status dq_decode_attention(dq_ctx **ctx, const dq_config *cfg, const dq_kv_bu
     if (!aligned16(q) || !aligned16(out)) return fail(DQ_EALIGN, "q / out not 16-byte aligned");
     if ((s = get_ctx(ctx, cfg, L)) != DQ_OK) return s;
     dq_ctx *c = *ctx;
+    if (L.scheme == DQ_NUQ) return fail(DQ_EUNSUPPORTED, "non-uniform scheme: attention is not built yet");
 
     dq::AttnArgs a{};
     a.q = static_cast<const float *>(q);
@@ -310,6 +399,7 @@ dq_status dq_dequantize_kv(dq_ctx **ctx, const dq_config *cfg, const dq_kv_buffe
     if ((s = check_bufs(L, bufs)) != DQ_OK) return s;
     if (!aligned16(out)) return fail(DQ_EALIGN, "out not 16-byte aligned");
     if ((s = get_ctx(ctx, cfg, L)) != DQ_OK) return s;
+    if (L.scheme == DQ_NUQ) return fail(DQ_EUNSUPPORTED, "non-uniform scheme: use the tables and side channel");
     dq::DequantArgs a{};
     a.codes = static_cast<const uint8_t *>(which == 0 ? bufs->codes_k : bufs->codes_v);
     a.meta = which == 0 ? bufs->meta_k : bufs->meta_v;
@@ -343,6 +433,7 @@ void dq_free(dq_ctx *ctx) {
     cudaFree(ctx->status);
     cudaFree(ctx->partials);
     cudaFree(ctx->counters);
+    cudaFree(ctx->nuq_bits);
     delete ctx;
 }
 

@@ -22,6 +22,13 @@ struct Layout {
     int rcap;            // raw slots per unit (multiple of 16)
     int meta_bytes;      // 2 (fp16) or 4 (fp32) per scale/offset value
     int n_sink, n_recent;
+    // non-uniform scheme (scheme == DQ_NUQ)
+    int scheme;          // dq_scheme of both tensors
+    int levels;          // 2^bits table entries
+    int k_out_cap;       // key outliers per channel at the longest prefill
+    long long nnzk_cap;  // key side-channel entries per unit (multiple of 8)
+    int k_out_v;         // value outliers per token
+    long long rp_stride; // ints per unit of the key row pointers (qcap + 4)
     size_t sz[DQ_NUM_BUFFERS];
 };
 
@@ -48,6 +55,14 @@ struct QuantArgs {
     const float *T;         // dense transform [Hkv][d][d] or nullptr
     uint16_t *raw;          // raw_k or raw_v
     unsigned *status;
+    // non-uniform scheme
+    uint16_t *lut;          // keys [U][d][L], values [U][Qcap][L] fp16 tables
+    uint32_t *olbits;       // keys: [U][Qcap][d/32] outlier bitmap (scratch, zeroed first)
+    int *ol_rowptr;         // keys: [U][rp_stride] row pointers by quantized slot
+    uint16_t *ol_col, *ol_val;  // keys: [U][nnzk_cap]; values: [U][Qcap][k_out_v]
+    int k_out;              // outliers per vector (keys: per channel at this prefill)
+    int iters;              // Lloyd sweeps
+    int n_fit;              // keys: quantized tokens in the prefill
 };
 
 struct AttnArgs {
@@ -92,6 +107,13 @@ struct DequantArgs {
 // launchers (return cudaError_t as int)
 int launch_key_mean(const Layout &L, const QuantArgs &a, void *stream);
 int launch_quantize(const Layout &L, const QuantArgs &a, void *stream);
+// non-uniform scheme, prefill: value tables/codes/outliers and raw copies;
+// key tables + outlier bitmap; key codes and raw copies; key side channel
+int launch_nuq_values(const Layout &L, const QuantArgs &a, void *stream);
+int launch_nuq_key_fit(const Layout &L, const QuantArgs &a, void *stream);
+int launch_nuq_key_codes(const Layout &L, const QuantArgs &a, void *stream);
+int launch_nuq_key_csr(const Layout &L, const QuantArgs &a, void *stream);
+int nuq_outlier_count(float f, int n);
 int launch_dequant(const Layout &L, const DequantArgs &a, void *stream);
 int launch_attention(const Layout &L, const AttnArgs &a, int num_sms, void *stream);
 // Fill the work schedule of `a` (items, grid, partial slots) for a launch on a
@@ -111,4 +133,5 @@ struct dq_ctx {
     float *partials;     // split partials
     size_t partials_cap; // floats
     int *counters;       // [U]
+    uint32_t *nuq_bits;  // non-uniform scheme: key outlier bitmap scratch [U][Qcap][d/32]
 };

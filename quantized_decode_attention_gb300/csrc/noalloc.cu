@@ -80,6 +80,8 @@ extern "C" dq_status dq_decode_attention_noalloc(const dq_config *cfg, const dq_
         if (!aligned16(p[i])) return dq::set_last_error(DQ_EALIGN, "a cache buffer is not 16-byte aligned");
     }
     if (!aligned16(q) || !aligned16(out)) return dq::set_last_error(DQ_EALIGN, "q / out not 16-byte aligned");
+    if (L.scheme == DQ_NUQ)
+        return dq::set_last_error(DQ_EUNSUPPORTED, "non-uniform scheme: attention is not built yet");
     if (static_cast<size_t>(L.U) > kMaxUnits) {
         char msg[200];
         std::snprintf(msg, sizeof msg, "batch * n_kv_heads = %d exceeds the allocation-free limit of %zu", L.U,

@@ -90,27 +90,6 @@ __global__ void key_mean_kernel(QuantArgs a, int Hkv, long long t0, long long t1
 // ---------------------------------------------------------------------------
 // Record packing helpers.
 // ---------------------------------------------------------------------------
-// Number of 32-bit words in a key row / a value pair record.
-template <int D, int BITS>
-struct Rec {
-    static constexpr int K_WORDS = D * BITS / 32;
-    static constexpr int V_WORDS = 2 * D * BITS / 32;
-};
-
-// OR-contribution of one code to word w of a key row (BITS 2/4: one plane;
-// BITS 3: 2-bit plane words first, then the 1-bit plane).
-template <int D, int BITS>
-__device__ __forceinline__ uint32_t contrib(int w, int idx, int half, uint32_t m, int words_lo) {
-    if (BITS == 3) {
-        uint32_t v = 0;
-        if (w == idx / 8) v |= (m & 3u) << (16 * half + 2 * (idx % 8));
-        if (w == words_lo + idx / 16) v |= ((m >> 2) & 1u) << (16 * half + (idx % 16));
-        return v;
-    }
-    constexpr int F = 16 / BITS;
-    return (w == idx / F) ? (m << (16 * half + BITS * (idx % F))) : 0u;
-}
-
 // ---------------------------------------------------------------------------
 // Quantize tokens [pos0, pos0 + n_tok): one warp per (unit, token).
 // ---------------------------------------------------------------------------

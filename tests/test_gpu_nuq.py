@@ -1,0 +1,119 @@
+"""GPU parity of the non-uniform (Lloyd-Max) scheme against the oracle.
+
+"KVQuant-NUQ" (VeloxQuant-MLX docs): per-channel key tables and per-token value
+tables fit at prefill, rank-based outliers in an fp16 side channel, sinks kept
+exact.  Tables, codes, side channel and 16-bit regions must match bit for bit.
+"""
+import numpy as np
+import pytest
+
+import workloads as W
+from oracle import cache as OC
+
+from helpers import cfg_for, to_device
+
+pytestmark = pytest.mark.gpu
+
+CASES = {
+    # a 3-bit cache of the KVQuant shape, Student-t data; several 64-token blocks and a ragged tail
+    "nuq3-d128": W.NUQ.with_(batch=1, n_kv_heads=2, n_q_heads=8, seq=300),
+    # 2-bit, d64, a recent window as well as the sink
+    "nuq2-d64-recent": W.NUQ.with_(batch=2, n_kv_heads=1, n_q_heads=4, head_dim=64, seq=200, bits=2, n_recent=16),
+    # 4-bit, no sink
+    "nuq4-d128-nosink": W.NUQ.with_(batch=1, n_kv_heads=1, n_q_heads=4, seq=130, bits=4, n_sink=0),
+    # plain NUQ (no outliers) and no Lloyd sweeps (quantile seeds only)
+    "nuq3-frac0-iters0": W.NUQ.with_(batch=1, n_kv_heads=1, n_q_heads=4, seq=97,
+                                     extra={"outlier_frac": 0.0, "lloyd_iters": 0}),
+    # bf16 input: side-channel values are rounded to fp16
+    "nuq3-bf16": W.NUQ.with_(batch=1, n_kv_heads=1, n_q_heads=4, seq=150, kv_dtype="bf16"),
+}
+
+
+def _views(w, cache, S):
+    from quantized_decode_attention_gb300 import kv_sizes
+    B, H, d, L = w.batch, w.n_kv_heads, w.head_dim, 1 << w.bits
+    qcap = -(-(S - w.n_sink) // 64) * 64
+    rcap = -(-(w.n_sink + w.n_recent) // 16) * 16
+    rowk = d * w.bits // 8
+    t = {n: (x.cpu().numpy() if x is not None else None) for n, x in cache.tensors.items()}
+    sizes = kv_sizes(cache.cfg)
+    v = {
+        "codes_k": t["codes_k"].reshape(B, H, qcap, rowk),
+        "codes_v": t["codes_v"].reshape(B, H, qcap // 2, 2 * rowk),
+        "lut_k": t["lut_k"].view(np.uint16).reshape(B, H, d, L),
+        "lut_v": t["lut_v"].view(np.uint16).reshape(B, H, qcap, L),
+    }
+    if t["ol_rowptr_k"] is not None:
+        v["rowptr"] = t["ol_rowptr_k"].view(np.int32).reshape(B, H, -1)
+        v["col_k"] = t["ol_col_k"].view(np.uint16).reshape(B, H, -1)
+        v["val_k"] = t["ol_val_k"].view(np.uint16).reshape(B, H, -1)
+    if t["ol_col_v"] is not None:
+        v["col_v"] = t["ol_col_v"].view(np.uint16).reshape(B, H, qcap, -1)
+        v["val_v"] = t["ol_val_v"].view(np.uint16).reshape(B, H, qcap, -1)
+    if rcap:
+        v["raw_k"] = t["raw_k"].view(np.uint16).reshape(B, H, rcap, d)
+        v["raw_v"] = t["raw_v"].view(np.uint16).reshape(B, H, rcap // 2, d, 2)
+    assert sizes["meta_k"] == 0 and sizes["mean_k"] == 0
+    return v, qcap
+
+
+@pytest.mark.parametrize("name", list(CASES))
+def test_nuq_prefill_is_bit_exact(name):
+    import torch
+    from quantized_decode_attention_gb300 import KVCache
+    w = CASES[name]
+    S = w.seq
+    k, v = W.make_kv(w)
+    cache = KVCache.allocate(cfg_for(w))
+    cache.quantize(to_device(k, w.kv_dtype), to_device(v, w.kv_dtype))
+    torch.cuda.synchronize()
+    cache.check()
+    got, qcap = _views(w, cache, S)
+    nk = OC.quantize_nuq(w, k, True, S)
+    nv = OC.quantize_nuq(w, v, False, S)
+    nq = S - w.n_sink
+    assert np.array_equal(got["lut_k"], nk.lut)
+    assert np.array_equal(got["lut_v"][:, :, :nq], nv.lut)
+    assert np.array_equal(got["codes_k"][:, :, :nq], OC.pack_k(nk.codes, w.bits))
+    pv = OC.pack_v(nv.codes, w.bits)
+    full = nq // 2
+    assert np.array_equal(got["codes_v"][:, :, :full], pv[:, :, :full])
+    if nq % 2:  # the last record holds one token: compare its half only
+        half = got["codes_v"][:, :, full].view(np.uint16).reshape(w.batch, w.n_kv_heads, -1, 2)[..., 0]
+        want = pv[:, :, full].view(np.uint16).reshape(w.batch, w.n_kv_heads, -1, 2)[..., 0]
+        assert np.array_equal(half, want)
+    kk = OC.nuq_key_outliers_csr(nk, qcap, got["col_k"].shape[-1]) if "rowptr" in got else None
+    if kk is not None:
+        rp, col, val = kk
+        assert np.array_equal(got["rowptr"][:, :, :qcap + 1], rp)
+        for b in range(w.batch):
+            for h in range(w.n_kv_heads):
+                n_nz = rp[b, h, -1]
+                assert np.array_equal(got["col_k"][b, h, :n_nz], col[b, h, :n_nz])
+                assert np.array_equal(got["val_k"][b, h, :n_nz], val[b, h, :n_nz])
+    else:
+        assert not nk.outlier.any()
+    if "col_v" in got:
+        col, val = OC.nuq_value_outliers(nv, qcap, got["col_v"].shape[-1])
+        assert np.array_equal(got["col_v"][:, :, :nq], col[:, :, :nq])
+        assert np.array_equal(got["val_v"][:, :, :nq], val[:, :, :nq])
+    else:
+        assert not nv.outlier.any()
+    regions_k = OC.raw_regions(w, k, S)
+    regions_v = OC.raw_regions(w, v, S)
+    for slot, bits in regions_k.items():
+        assert np.array_equal(got["raw_k"][:, :, slot], bits), slot
+    for slot, bits in regions_v.items():
+        assert np.array_equal(got["raw_v"][:, :, slot // 2, :, slot & 1], bits), slot
+
+
+def test_nuq_append_is_refused():
+    import torch
+    from quantized_decode_attention_gb300 import KVCache, DQError
+    w = CASES["nuq3-d128"]
+    k, v = W.make_kv(w)
+    cache = KVCache.allocate(cfg_for(w, max_seq=w.seq + 8))
+    cache.quantize(to_device(k, w.kv_dtype), to_device(v, w.kv_dtype))
+    with pytest.raises(DQError):
+        cache.quantize(to_device(k[:, :, :1], w.kv_dtype), to_device(v[:, :, :1], w.kv_dtype), pos0=w.seq)
+    torch.cuda.synchronize()
