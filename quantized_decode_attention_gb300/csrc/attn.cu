@@ -51,7 +51,9 @@ struct AttnShape {
     int rcap;
 };
 
-template <int D, int BK, int BV, bool M16>
+// NUQ: the non-uniform scheme (per-channel key tables, per-token value tables,
+// fp16 outlier side channel) instead of the affine one.
+template <int D, int BK, int BV, bool M16, bool NUQ = false>
 struct Cfg {
     static constexpr int ST = 128;                // packed tokens per pipeline entry
     static constexpr int SUB = 32;                // tokens of an entry per warp (one softmax step)
@@ -59,19 +61,23 @@ struct Cfg {
     static constexpr int ROWK = D * BK / 8;
     static constexpr int PAIRV = 2 * D * BV / 8;
     static constexpr int MB = M16 ? 2 : 4;
-    static constexpr int KBYTES = ST * ROWK;      // stage layout: keys, value pairs, key meta, value meta
+    static constexpr int LV = 1 << BV;            // table entries (non-uniform scheme)
+    // stage layout: keys, value pairs, then (affine) key meta, value meta or
+    // (non-uniform) the tokens' value tables
+    static constexpr int KBYTES = ST * ROWK;
     static constexpr int VBYTES = ST / 2 * PAIRV;
-    static constexpr int MBYTES = ST * 2 * MB;
-    static constexpr int ENTRY = KBYTES + VBYTES + 2 * MBYTES;
+    static constexpr int MBYTES = NUQ ? 0 : ST * 2 * MB;
+    static constexpr int LUTV = NUQ ? ST * LV * 2 : 0;
+    static constexpr int ENTRY = KBYTES + VBYTES + 2 * MBYTES + LUTV;
     static constexpr int RAWBYTES = 64 * D;       // one 16-slot tile of 16-bit keys + values
     static constexpr int SLOT = ((ENTRY > RAWBYTES ? ENTRY : RAWBYTES) + 127) / 128 * 128;
     // ring depth: four slots where four CTAs per SM still fit, else as many as
     // fit three CTAs per SM (the 3-bit kernel is register-limited to three)
-    static constexpr int NST = SLOT <= 9216 ? 4 : (SLOT <= 13312 ? 4 : 3);
+    static constexpr int NST = NUQ ? (SLOT <= 10240 ? 3 : 2) : (SLOT <= 13312 ? 4 : 3);
     static constexpr int NKS = D / 16;
     static constexpr int NMT = D / 16;
     static constexpr int PR = D + 4;  // floats per head in a partial record: acc[D], m, l, 0, 0
-    static constexpr int MINB = (BK == 3 || SLOT > 9216) ? 3 : 4;  // resident CTAs per SM
+    static constexpr int MINB = (NUQ || BK == 3 || SLOT > 9216) ? 3 : 4;  // resident CTAs per SM
 };
 
 // ---- code extraction --------------------------------------------------------
@@ -186,17 +192,19 @@ struct WarpState {
         for (int mi = 0; mi < NMT; mi++) acc[mi][0] = acc[mi][1] = acc[mi][2] = acc[mi][3] = 0.f;
     }
     // logits (log2 units) of NT tokens held by this lane -> probabilities
+    // returns the factor the accumulators were scaled by (1 if they were not)
     template <int NT>
-    __device__ __forceinline__ void update(const float (&lg)[NT], float (&p)[NT]) {
+    __device__ __forceinline__ float update(const float (&lg)[NT], float (&p)[NT]) {
         float mx = lg[0];
 #pragma unroll
         for (int k = 1; k < NT; k++) mx = fmaxf(mx, lg[k]);
 #pragma unroll
         for (int o = 4; o < 32; o <<= 1) mx = fmaxf(mx, __shfl_xor_sync(FULL, mx, o));
         const bool grow = mx > m + RESCALE_SLACK;  // also true for the first finite logit
+        float al = 1.f;
         if (__any_sync(FULL, grow)) {
             const float mn = grow ? mx : m;
-            const float al = grow ? ex2(m - mn) : 1.f;  // 0 when m was -inf
+            al = grow ? ex2(m - mn) : 1.f;  // 0 when m was -inf
             m = mn;
             l *= al;
             ao *= al;
@@ -216,13 +224,14 @@ struct WarpState {
             sum += p[k];
         }
         l += sum;
+        return al;
     }
 };
 
 // ---- shared memory -----------------------------------------------------------
-template <int D, int BK, int BV, bool M16>
+template <int D, int BK, int BV, bool M16, bool NUQ = false>
 struct Smem {
-    using C = Cfg<D, BK, BV, M16>;
+    using C = Cfg<D, BK, BV, M16, NUQ>;
     // query operands of up to two units at a time: [unit slot][kind: 0 16-bit
     // tiles, 1 packed][half: 0 hi, 1 lo][head][channel] 16-bit values, rows
     // padded by 8 so that the 8 (half, head) rows of a warp's load hit
@@ -236,6 +245,13 @@ struct Smem {
     };
     uint64_t full[C::NST];         // slot filled (transaction count of its copies)
     unsigned rel[C::NST];          // releases of a slot so far (4 per entry)
+    // non-uniform scheme only (one element otherwise): key tables [unit slot]
+    // [channel][level], fp32 queries, this block's probabilities per warp, and
+    // the value side channel's corrections per warp [warp][head][channel]
+    uint16_t lutk[NUQ ? 2 : 1][NUQ ? D * C::LV : 1];
+    float qf[NUQ ? 2 : 1][4][NUQ ? D : 1];
+    float pb[NUQ ? 4 : 1][4][NUQ ? C::SUB : 1];
+    float corr[NUQ ? 4 : 1][4][NUQ ? D : 1];
     alignas(128) uint8_t ring[C::NST][C::SLOT];
 };
 
@@ -261,10 +277,10 @@ __device__ __forceinline__ void mbar_arrive_elect(uint64_t *bar) {
 // packed tokens [p*ST, p*ST + ST): keys, value pairs, key meta, value meta,
 // each at its fixed offset in the slot.  A last entry that would run past the
 // unit's capacity copies the 64 tokens that exist (capacity is a multiple of 64).
-template <int D, int BK, int BV, bool M16>
+template <int D, int BK, int BV, bool M16, bool NUQ = false>
 __device__ __forceinline__ void issue_entry(const AttnArgs &a, const AttnShape &sh, int u, int e, uint8_t *slot,
                                             uint64_t *bar) {
-    using C = Cfg<D, BK, BV, M16>;
+    using C = Cfg<D, BK, BV, M16, NUQ>;
     const uint32_t sb = smem_u32(slot), br = smem_u32(bar);
     if (e < a.n_rt) {
         const long long r0 = static_cast<long long>(u) * sh.rcap + static_cast<long long>(e) * RTILE;
@@ -283,6 +299,20 @@ __device__ __forceinline__ void issue_entry(const AttnArgs &a, const AttnShape &
     const long long g0 = static_cast<long long>(u) * sh.qcap + t0;
     const uint8_t *ck = a.codes_k + g0 * C::ROWK;
     const uint8_t *cv = a.codes_v + g0 / 2 * C::PAIRV;
+    if constexpr (NUQ) {
+        const uint8_t *lv = reinterpret_cast<const uint8_t *>(a.lut_v) + g0 * C::LV * 2;
+        const uint32_t kb = nt * C::ROWK, vb = nt / 2 * C::PAIRV, lb = nt * C::LV * 2;
+        asm volatile(
+            "{\n .reg .pred p;\n elect.sync _|p, 0xffffffff;\n"
+            "@p mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n"
+            "@p cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%2], [%3], %4, [%0];\n"
+            "@p cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%5], [%6], %7, [%0];\n"
+            "@p cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%8], [%9], %10, [%0];\n}\n" ::"r"(br),
+            "r"(kb + vb + lb), "r"(sb), "l"(ck), "r"(kb), "r"(sb + C::KBYTES), "l"(cv), "r"(vb),
+            "r"(sb + C::KBYTES + C::VBYTES), "l"(lv), "r"(lb)
+            : "memory");
+        return;
+    }
     const uint8_t *mk = static_cast<const uint8_t *>(a.meta_k) + g0 * 2 * C::MB;
     const uint8_t *mv = static_cast<const uint8_t *>(a.meta_v) + g0 * 2 * C::MB;
     const uint32_t kb = nt * C::ROWK, vb = nt / 2 * C::PAIRV, mb = nt * 2 * C::MB;
@@ -323,6 +353,184 @@ __device__ __forceinline__ int raw_v_channel(int row) {
 
 __device__ __forceinline__ uint32_t vec_word(const uint4 &v, int r) {
     return r == 0 ? v.x : (r == 1 ? v.y : (r == 2 ? v.z : v.w));
+}
+
+// ---- non-uniform scheme ---------------------------------------------------------
+// Integer codes (half 0, half 1) of field r of a lane's record slice; the same
+// fields extract<BITS> turns into mma operands in the affine scheme.
+template <int BITS>
+__device__ __forceinline__ void field_codes(const uint32_t *w, int r, uint32_t &m0, uint32_t &m1) {
+    if (BITS == 4) {
+        const uint32_t x = w[r >> 2], sh = 4 * (r & 3);
+        m0 = (x >> sh) & 15u;
+        m1 = (x >> (16 + sh)) & 15u;
+        return;
+    }
+    const uint32_t x = w[r >> 3], sh = 2 * (r & 7);
+    m0 = (x >> sh) & 3u;
+    m1 = (x >> (16 + sh)) & 3u;
+    if (BITS == 3) {  // the 1-bit plane word holds register r at bits r and 16 + r
+        m0 |= ((w[2] >> r) & 1u) << 2;
+        m1 |= ((w[2] >> (16 + r)) & 1u) << 2;
+    }
+}
+
+// Code of field idx, half `half` of a whole record (words_lo: 2-bit plane
+// words of a 3-bit record).
+template <int BITS>
+__device__ __forceinline__ uint32_t code_in_rec(const uint8_t *rec, int idx, int half, int words_lo) {
+    const uint32_t *w = reinterpret_cast<const uint32_t *>(rec);
+    if (BITS == 3) {
+        const uint32_t lo = (w[idx >> 3] >> (16 * half + 2 * (idx & 7))) & 3u;
+        const uint32_t hi = (w[words_lo + (idx >> 4)] >> (16 * half + (idx & 15))) & 1u;
+        return lo | (hi << 2);
+    }
+    constexpr int F = 16 / BITS;
+    return (w[idx / F] >> (16 * half + BITS * (idx % F))) & ((1u << BITS) - 1u);
+}
+
+__device__ __forceinline__ float f16v(uint16_t h) { return __half2float(__ushort_as_half(h)); }
+
+// This warp's SUB tokens of a non-uniform entry -> warp state.  Operands are
+// table values: K^[r][c] = lut_k[c][code] from the unit's key tables in
+// shared memory, V^[t][c] = lut_v[t][code] from the tokens' tables in the
+// slot ("KVQuant-NUQ" page: dequantize = table lookup).  Outliers keep their
+// fp16 value: a key outlier adds q_c (x - table value) to its logit, a value
+// outlier adds p_t (x - table value) to corr[head][c] (this lane's channels
+// c = g mod 8, kept in the warp state's scale).
+template <int D, int BK, int BV>
+__device__ __forceinline__ void process_block_nuq(const uint8_t *kp, const uint8_t *vp, const uint16_t *lvp, int valid,
+                                                  const uint32_t (&qb)[D / 16][2], const uint16_t *lutk,
+                                                  const float (*qf)[D], float sm_l2, WarpState<D / 16> &st,
+                                                  float (*corr)[D], float (*pb)[32], const AttnArgs &a,
+                                                  const AttnShape &sh, int u, long long s0) {
+    constexpr int NKS = D / 16, NMT = D / 16, T = 2, LV = 1 << BV, ROWK = D * BK / 8, PAIRV = 2 * D * BV / 8;
+    constexpr int NWK = Slice<D, BK>::NW, NWV = Slice<D, BV>::NW;
+    const int lane = threadIdx.x & 31, g = lane >> 2, tig = lane & 3;
+    const uint16_t *lk = lutk + 2 * tig * LV;  // table rows of this lane's channels 16i + 2tig + 8sub + e
+    float sc[T][4];
+#pragma unroll
+    for (int t = 0; t < T; t++) {
+        uint32_t k0[NWK], k1[NWK];
+        load_k_slice<D, BK>(kp + (16 * t + g) * ROWK, tig, k0);
+        load_k_slice<D, BK>(kp + (16 * t + g + 8) * ROWK, tig, k1);
+        sc[t][0] = sc[t][1] = sc[t][2] = sc[t][3] = 0.f;
+#pragma unroll
+        for (int i = 0; i < NKS; i++) {
+            uint32_t m0, m1, r[4];
+#pragma unroll
+            for (int q = 0; q < 4; q++) {
+                const int f = 2 * i + (q >> 1);
+                field_codes<BK>((q & 1) ? k1 : k0, f, m0, m1);
+                const uint16_t *l0 = lk + (16 * i + 8 * (q >> 1)) * LV;
+                r[q] = pack2(l0[m0], l0[LV + m1]);
+            }
+            mma_f16(sc[t], r[0], r[1], r[2], r[3], qb[i][0], qb[i][1]);
+        }
+    }
+    float lg[2 * T];
+#pragma unroll
+    for (int k = 0; k < 2 * T; k++) {
+        const int t = k >> 1, hf = k & 1;
+        lg[k] = sm_l2 * (sc[t][2 * hf] + sc[t][2 * hf + 1]);
+    }
+    if (a.ol_rowptr_k) {  // key side channel of this lane's tokens, head tig
+        const int *rp = a.ol_rowptr_k + static_cast<long long>(u) * a.rp_stride;
+        const uint16_t *col = a.ol_col_k + static_cast<long long>(u) * a.nnzk_cap;
+        const uint16_t *val = a.ol_val_k + static_cast<long long>(u) * a.nnzk_cap;
+#pragma unroll
+        for (int k = 0; k < 2 * T; k++) {
+            const int row = 16 * (k >> 1) + g + 8 * (k & 1);
+            if (row >= valid) continue;
+            const int e1 = rp[s0 + row + 1];
+            float cr = 0.f;
+            for (int e = rp[s0 + row]; e < e1; e++) {
+                const int c = col[e];
+                const uint32_t m = code_in_rec<BK>(kp + row * ROWK, k_idx(c, D), c & 1, D / 16);
+                cr += qf[tig][c] * (f16v(val[e]) - f16v(lutk[c * LV + m]));
+            }
+            lg[k] += sm_l2 * cr;
+        }
+    }
+    const bool ragged = valid < 32;
+    if (ragged) {
+#pragma unroll
+        for (int k = 0; k < 2 * T; k++)
+            if (16 * (k >> 1) + g + 8 * (k & 1) >= valid) lg[k] = -INFINITY;
+    }
+    float p[2 * T];
+    const float al = st.template update<2 * T>(lg, p);
+    const int kv = a.k_out_v;
+    if (kv > 0) {
+        if (al != 1.f) {
+#pragma unroll
+            for (int j = 0; j < D / 8; j++) corr[tig][8 * j + g] *= al;
+        }
+#pragma unroll
+        for (int k = 0; k < 2 * T; k++) pb[tig][16 * (k >> 1) + g + 8 * (k & 1)] = p[k];
+        __syncwarp();
+    }
+    // P . V per tile: A = V^T (channels x tokens) from the tokens' tables
+#pragma unroll
+    for (int t = 0; t < T; t++) {
+        const uint32_t b0 = movmatrix_t(hilo_f16(p[2 * t]));
+        const uint32_t b1 = movmatrix_t(hilo_f16(p[2 * t + 1]));
+        uint32_t v0[NWV], v1[NWV];
+        load_v_slice<D, BV>(vp + (8 * t + tig) * PAIRV, g, v0);
+        load_v_slice<D, BV>(vp + (8 * t + tig + 4) * PAIRV, g, v1);
+        const uint16_t *la = lvp + (16 * t + 2 * tig) * LV, *lb = la + 8 * LV;
+#pragma unroll
+        for (int mi = 0; mi < NMT; mi++) {
+            uint32_t m0, m1, r[4];
+            field_codes<BV>(v0, 2 * mi, m0, m1);
+            r[0] = pack2(la[m0], la[LV + m1]);
+            field_codes<BV>(v0, 2 * mi + 1, m0, m1);
+            r[1] = pack2(la[m0], la[LV + m1]);
+            field_codes<BV>(v1, 2 * mi, m0, m1);
+            r[2] = pack2(lb[m0], lb[LV + m1]);
+            field_codes<BV>(v1, 2 * mi + 1, m0, m1);
+            r[3] = pack2(lb[m0], lb[LV + m1]);
+            mma_f16(st.acc[mi], r[0], r[1], r[2], r[3], b0, b1);
+        }
+    }
+    if (kv > 0) {  // value side channel: token tt's entries go to the lanes owning channel c
+        const long long tb = static_cast<long long>(u) * sh.qcap + s0;
+        for (int j = 0; j < kv; j++) {
+            const bool in = lane < valid;
+            const uint32_t cm = in ? a.ol_col_v[(tb + lane) * kv + j] : 0xffffu;
+            const uint32_t vm = in ? a.ol_val_v[(tb + lane) * kv + j] : 0u;
+            for (int tt = 0; tt < 32; tt++) {
+                const int c = static_cast<int>(__shfl_sync(FULL, cm, tt));
+                const uint16_t vv = static_cast<uint16_t>(__shfl_sync(FULL, vm, tt));
+                if (c == 0xffff || (c & 7) != g) continue;
+                const uint32_t m = code_in_rec<BV>(vp + (tt >> 1) * PAIRV, v_idx(c, D), tt & 1, D / 8);
+                corr[tig][c] += pb[tig][tt] * (f16v(vv) - f16v(lvp[tt * LV + m]));
+            }
+        }
+        __syncwarp();
+    }
+}
+
+// Warp state of a non-uniform segment -> [acc[D], m, l] of head tig at dst:
+// rows are channels, plus the value side channel's corrections.
+template <int D>
+__device__ __forceinline__ void store_state_nuq(WarpState<D / 16> &st, const float (*corr)[D], float *dst, int PR) {
+    constexpr int NMT = D / 16;
+    const int lane = threadIdx.x & 31, g = lane >> 2, tig = lane & 3;
+#pragma unroll
+    for (int o = 4; o < 32; o <<= 1) st.l += __shfl_xor_sync(FULL, st.l, o);
+    float *wp = dst + tig * PR;
+#pragma unroll
+    for (int mi = 0; mi < NMT; mi++)
+#pragma unroll
+        for (int rr = 0; rr < 2; rr++) {
+            const int row = 16 * mi + 8 * rr + g;
+            wp[row] = st.acc[mi][2 * rr] + st.acc[mi][2 * rr + 1] + corr[tig][row];
+        }
+    if (g == 0) {
+        wp[D] = st.m;
+        wp[D + 1] = st.l;
+    }
 }
 
 // This warp's SUB packed tokens of an entry -> warp state.  `kp`, `vp`, `mkp`,
@@ -598,8 +806,8 @@ __device__ __forceinline__ void load_query(const AttnArgs &a, const AttnShape &s
 }
 
 // The (hi, lo) 16-bit halves of v into S.qh[qs][kind][0 / 1][h][c].
-template <int D, int BK, int BV, bool M16>
-__device__ __forceinline__ void put_hilo(Smem<D, BK, BV, M16> &S, int qs, int kind, int h, int c, float v,
+template <int D, int BK, int BV, bool M16, bool NUQ>
+__device__ __forceinline__ void put_hilo(Smem<D, BK, BV, M16, NUQ> &S, int qs, int kind, int h, int c, float v,
                                          bool bf16) {
     const uint32_t w = bf16 ? hilo_bf16(v) : hilo_f16(v);
     S.qh[qs][kind][0][h][c] = static_cast<uint16_t>(w & 0xffffu);
@@ -611,9 +819,9 @@ __device__ __forceinline__ void put_hilo(Smem<D, BK, BV, M16> &S, int qs, int ki
 // rotated (or compensated) and scaled by 2^-E for the code field E that
 // channel c meets in the key operand (register c>>3 of a lane's slice); also
 // sum q and q . mu for the fold of the affine code (Eq. 8).
-template <int D, int BK, int BV, bool M16>
-__device__ __forceinline__ void prep_query(const AttnArgs &a, const AttnShape &sh, Smem<D, BK, BV, M16> &S, int qs,
-                                           int u, const QIn<D / 32> &in) {
+template <int D, int BK, int BV, bool M16, bool NUQ>
+__device__ __forceinline__ void prep_query(const AttnArgs &a, const AttnShape &sh, Smem<D, BK, BV, M16, NUQ> &S,
+                                           int qs, int u, const QIn<D / 32> &in) {
     constexpr int V = D / 32;
     const int h = threadIdx.x >> 5, lane = threadIdx.x & 31;
     float xq[V];
@@ -648,8 +856,10 @@ __device__ __forceinline__ void prep_query(const AttnArgs &a, const AttnShape &s
         const int c = lane * V + j;
         qsum += xq[j];
         qmu += xq[j] * in.mu[j];
-        const float sc = __int_as_float((127 - field_exp(c >> 3, BK)) << 23);  // 2^-E, exact
+        // packed keys: 2^-E of the code field (affine), or 1 (table values)
+        const float sc = NUQ ? 1.f : __int_as_float((127 - field_exp(c >> 3, BK)) << 23);
         put_hilo(S, qs, 1, h, c, xq[j] * sc, false);
+        if constexpr (NUQ) S.qf[qs][h][c] = xq[j];
     }
     qsum = warp_sum(qsum);
     qmu = warp_sum(qmu);
@@ -657,13 +867,19 @@ __device__ __forceinline__ void prep_query(const AttnArgs &a, const AttnShape &s
         S.qsum[qs][h] = qsum;
         S.qmu[qs][h] = qmu;
     }
+    if constexpr (NUQ) {  // the unit's key tables
+        constexpr int LV = Cfg<D, BK, BV, M16, NUQ>::LV;
+        const uint32_t *src = reinterpret_cast<const uint32_t *>(a.lut_k + static_cast<long long>(u) * D * LV);
+        uint32_t *dst = reinterpret_cast<uint32_t *>(S.lutk[qs]);
+        for (int i = threadIdx.x; i < D * LV / 2; i += blockDim.x) dst[i] = src[i];
+    }
 }
 
 // This lane's mma B operand of q.K^T from the prepared halves: column g of the
 // operand is head g>>1, half g&1; lane slot (k-step i, sub, e) holds channel
 // perm(i, tig, sub, e), and e = 0, 1 are adjacent channels (one 32-bit load).
-template <int D, int BK, int BV, bool M16, typename Perm>
-__device__ __forceinline__ void load_qb(const Smem<D, BK, BV, M16> &S, int qs, int kind, Perm perm,
+template <int D, int BK, int BV, bool M16, bool NUQ, typename Perm>
+__device__ __forceinline__ void load_qb(const Smem<D, BK, BV, M16, NUQ> &S, int qs, int kind, Perm perm,
                                         uint32_t (&qb)[D / 16][2]) {
     const int lane = threadIdx.x & 31, g = lane >> 2, tig = lane & 3;
     const uint16_t *row = S.qh[qs][kind][g & 1][g >> 1];
@@ -684,12 +900,12 @@ __device__ __forceinline__ void load_qb(const Smem<D, BK, BV, M16> &S, int qs, i
 // for every entry (also the 16-bit tiles it leaves to another warp): a warp is
 // then never more than one phase ahead of a slot, which the parity test of the
 // wait requires.
-template <int D, int BK, int BV, bool M16>
-__global__ void __launch_bounds__(128, Cfg<D, BK, BV, M16>::MINB) attn_kernel(AttnArgs a, AttnShape sh) {
-    using C = Cfg<D, BK, BV, M16>;
+template <int D, int BK, int BV, bool M16, bool NUQ = false>
+__global__ void __launch_bounds__(128, Cfg<D, BK, BV, M16, NUQ>::MINB) attn_kernel(AttnArgs a, AttnShape sh) {
+    using C = Cfg<D, BK, BV, M16, NUQ>;
     constexpr int PR = C::PR, NKS = C::NKS, NST = C::NST;
     extern __shared__ __align__(128) uint8_t smem_raw[];
-    Smem<D, BK, BV, M16> &S = *reinterpret_cast<Smem<D, BK, BV, M16> *>(smem_raw);
+    Smem<D, BK, BV, M16, NUQ> &S = *reinterpret_cast<Smem<D, BK, BV, M16, NUQ> *>(smem_raw);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tig = lane & 3;
     const int G = gridDim.x, i = blockIdx.x;
     const long long N = a.total_items;
@@ -712,7 +928,7 @@ __global__ void __launch_bounds__(128, Cfg<D, BK, BV, M16>::MINB) attn_kernel(At
     auto issue_k = [&](int k) {
         const unsigned x = static_cast<unsigned>(x0) + static_cast<unsigned>(k);
         const unsigned u = x / static_cast<unsigned>(ipu);
-        issue_entry<D, BK, BV, M16>(a, sh, static_cast<int>(u), static_cast<int>(x - u * ipu), S.ring[k % NST],
+        issue_entry<D, BK, BV, M16, NUQ>(a, sh, static_cast<int>(u), static_cast<int>(x - u * ipu), S.ring[k % NST],
                                     &S.full[k % NST]);
     };
     if (warp == 0) {
@@ -726,8 +942,8 @@ __global__ void __launch_bounds__(128, Cfg<D, BK, BV, M16>::MINB) attn_kernel(At
         __syncwarp();
         for (int k = 0; k < NST && k < n_ent; k++) issue_k(k);
     }
-    prep_query<D, BK, BV, M16>(a, sh, S, 0, u_first, qin0);
-    if (u_lastc > u_first) prep_query<D, BK, BV, M16>(a, sh, S, 1, u_first + 1, qin1);
+    prep_query<D, BK, BV, M16, NUQ>(a, sh, S, 0, u_first, qin0);
+    if (u_lastc > u_first) prep_query<D, BK, BV, M16, NUQ>(a, sh, S, 1, u_first + 1, qin1);
 
     int j = 0;  // the CTA's entry being consumed
     auto acquire = [&]() -> const uint8_t * {
@@ -797,7 +1013,7 @@ __global__ void __launch_bounds__(128, Cfg<D, BK, BV, M16>::MINB) attn_kernel(At
         if (u - u_first >= 2) {
             QIn<D / 32> qin;
             load_query<D>(a, sh, u, qin);
-            prep_query<D, BK, BV, M16>(a, sh, S, qs, u, qin);
+            prep_query<D, BK, BV, M16, NUQ>(a, sh, S, qs, u, qin);
             __syncthreads();
         }
         const int first = owner(ub, N, G);
@@ -832,6 +1048,31 @@ __global__ void __launch_bounds__(128, Cfg<D, BK, BV, M16>::MINB) attn_kernel(At
         // ---- packed entries: SUB tokens per warp; record kind 1 ----
         st.init();
         const int p0 = (e0 > n_rt ? e0 : n_rt) - n_rt, p1 = e1 - n_rt;
+        if constexpr (NUQ) {
+#pragma unroll
+            for (int j = 0; j < D / 8; j++) S.corr[warp][tig][8 * j + (lane >> 2)] = 0.f;  // this lane's channels
+            __syncwarp();
+            if (p0 < p1) {
+                uint32_t qb[NKS][2];
+                load_qb(S, qs, 1, PermIdentity(), qb);
+                const int wv = static_cast<int>(a.n_q) - warp * C::SUB;
+                const int ok = warp * C::SUB * C::ROWK;
+                const int ov = C::KBYTES + warp * (C::SUB / 2) * C::PAIRV;
+                const int ol = C::KBYTES + C::VBYTES + warp * C::SUB * C::LV * 2;
+#pragma unroll 1
+                for (int q = p0; q < p1; q++) {
+                    const uint8_t *slot = acquire();
+                    const int valid = wv - q * C::ST;
+                    if (valid > 0)
+                        process_block_nuq<D, BK, BV>(slot + ok, slot + ov, reinterpret_cast<const uint16_t *>(slot + ol),
+                                                     valid, qb, S.lutk[qs], S.qf[qs], a.sm_log2, st, S.corr[warp],
+                                                     S.pb[warp], a, sh, u,
+                                                     static_cast<long long>(q) * C::ST + warp * C::SUB);
+                    release();
+                }
+            }
+            store_state_nuq<D>(st, S.corr[warp], &S.merge[warp][0][0], PR);
+        } else {
         if (p0 < p1) {
             uint32_t qb[NKS][2];
             load_qb(S, qs, 1, PermIdentity(), qb);
@@ -854,6 +1095,7 @@ __global__ void __launch_bounds__(128, Cfg<D, BK, BV, M16>::MINB) attn_kernel(At
             }
         }
         store_state<D, BV>(st, true, &S.merge[warp][0][0], PR);
+        }
         __syncthreads();
         cta_merge(recs + 4 * PR);
         // publish: the records are visible GPU-wide before the unit's count moves
@@ -896,14 +1138,14 @@ __global__ void __launch_bounds__(128) combine_kernel(AttnArgs a, AttnShape sh) 
 }
 
 // ---- host side -------------------------------------------------------------
-template <int D, int BK, int BV, bool M16>
+template <int D, int BK, int BV, bool M16, bool NUQ = false>
 struct Launcher {
-    static constexpr int ST = Cfg<D, BK, BV, M16>::ST;
+    static constexpr int ST = Cfg<D, BK, BV, M16, NUQ>::ST;
     static int occupancy;  // resident CTAs per SM, set on first use
-    static size_t smem() { return sizeof(Smem<D, BK, BV, M16>); }
+    static size_t smem() { return sizeof(Smem<D, BK, BV, M16, NUQ>); }
     static int prepare() {
         if (occupancy > 0) return 0;
-        auto kern = attn_kernel<D, BK, BV, M16>;
+        auto kern = attn_kernel<D, BK, BV, M16, NUQ>;
         cudaError_t e =
             cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem()));
         if (e != cudaSuccess) return static_cast<int>(e);
@@ -915,7 +1157,7 @@ struct Launcher {
     }
     static int launch(const AttnArgs &a, const AttnShape &sh, void *stream) {
         const cudaStream_t st = static_cast<cudaStream_t>(stream);
-        attn_kernel<D, BK, BV, M16><<<a.grid, 128, smem(), st>>>(a, sh);
+        attn_kernel<D, BK, BV, M16, NUQ><<<a.grid, 128, smem(), st>>>(a, sh);
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return static_cast<int>(e);
         cudaLaunchConfig_t lc = {};
@@ -930,8 +1172,8 @@ struct Launcher {
         return static_cast<int>(cudaLaunchKernelEx(&lc, combine_kernel<D>, a, sh));
     }
 };
-template <int D, int BK, int BV, bool M16>
-int Launcher<D, BK, BV, M16>::occupancy = 0;
+template <int D, int BK, int BV, bool M16, bool NUQ>
+int Launcher<D, BK, BV, M16, NUQ>::occupancy = 0;
 
 template <int D, bool M16, typename F>
 static int dispatch_bits(const Layout &L, F &&f) {
@@ -943,6 +1185,15 @@ static int dispatch_bits(const Layout &L, F &&f) {
 
 template <typename F>
 static int dispatch(const Layout &L, F &&f) {
+    if (L.scheme == DQ_NUQ) {  // no meta: one instantiation per (d, bits)
+        if (L.d == 128) {
+            if (L.bits_k == 2) return f(Launcher<128, 2, 2, true, true>());
+            if (L.bits_k == 3) return f(Launcher<128, 3, 3, true, true>());
+            return f(Launcher<128, 4, 4, true, true>());
+        }
+        if (L.bits_k == 2) return f(Launcher<64, 2, 2, true, true>());
+        return f(Launcher<64, 4, 4, true, true>());
+    }
     const bool m16 = L.meta_bytes == 2;
     if (L.d == 128) return m16 ? dispatch_bits<128, true>(L, f) : dispatch_bits<128, false>(L, f);
     return m16 ? dispatch_bits<64, true>(L, f) : dispatch_bits<64, false>(L, f);

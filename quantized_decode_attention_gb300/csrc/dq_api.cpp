@@ -58,6 +58,24 @@ dq_status validate_tensor(const dq_tensor_cfg &t, int d, bool key, const char *n
 
 namespace dq {
 
+void set_nuq_args(const Layout &L, const dq_kv_buffers *b, AttnArgs &a) {
+    if (L.scheme != DQ_NUQ) return;
+    a.lut_k = static_cast<const uint16_t *>(b->lut_k);
+    a.lut_v = static_cast<const uint16_t *>(b->lut_v);
+    if (L.k_out_cap > 0) {
+        a.ol_rowptr_k = static_cast<const int *>(b->ol_rowptr_k);
+        a.ol_col_k = static_cast<const uint16_t *>(b->ol_col_k);
+        a.ol_val_k = static_cast<const uint16_t *>(b->ol_val_k);
+    }
+    if (L.k_out_v > 0) {
+        a.ol_col_v = static_cast<const uint16_t *>(b->ol_col_v);
+        a.ol_val_v = static_cast<const uint16_t *>(b->ol_val_v);
+        a.k_out_v = L.k_out_v;
+    }
+    a.rp_stride = L.rp_stride;
+    a.nnzk_cap = L.nnzk_cap;
+}
+
 dq_status set_last_error(dq_status s, const char *msg) {
     if (s == DQ_OK) return ok();
     return fail(s, "%s", msg);
@@ -349,7 +367,6 @@ dq_status dq_decode_attention(dq_ctx **ctx, const dq_config *cfg, const dq_kv_bu
     if (!aligned16(q) || !aligned16(out)) return fail(DQ_EALIGN, "q / out not 16-byte aligned");
     if ((s = get_ctx(ctx, cfg, L)) != DQ_OK) return s;
     dq_ctx *c = *ctx;
-    if (L.scheme == DQ_NUQ) return fail(DQ_EUNSUPPORTED, "non-uniform scheme: attention is not built yet");
 
     dq::AttnArgs a{};
     a.q = static_cast<const float *>(q);
@@ -381,6 +398,7 @@ dq_status dq_decode_attention(dq_ctx **ctx, const dq_config *cfg, const dq_kv_bu
     a.partials = c->partials;
     a.counters = c->counters;
     a.status = c->status;
+    dq::set_nuq_args(L, bufs, a);
     int e = dq::plan_attention(L, a, c->num_sms, static_cast<long long>(c->partials_cap));
     if (e != 0) return fail(DQ_ECUDA, "attention planning: %s", cudaGetErrorString(static_cast<cudaError_t>(e)));
     e = dq::launch_attention(L, a, c->num_sms, stream);

@@ -93,6 +93,13 @@ struct AttnArgs {
     float *partials;        // [U][max_slots][2 kinds][4 heads][d + 4]
     int *counters;          // [U] CTAs done with the unit; zero between calls
     unsigned *status;
+    // non-uniform scheme
+    const uint16_t *lut_k, *lut_v;        // [U][d][L] / [U][Qcap][L] fp16 tables
+    const int *ol_rowptr_k;               // [U][rp_stride] key side-channel rows by slot (or null)
+    const uint16_t *ol_col_k, *ol_val_k;  // [U][nnzk_cap]
+    const uint16_t *ol_col_v, *ol_val_v;  // [U][Qcap][k_out_v]
+    long long rp_stride, nnzk_cap;
+    int k_out_v;                          // value outliers per token (0: none)
 };
 
 struct DequantArgs {
@@ -103,6 +110,10 @@ struct DequantArgs {
     long long slot0, n;
     float *out;
 };
+
+struct AttnArgs;
+// Fill the non-uniform scheme's table and side-channel pointers (no-op otherwise).
+void set_nuq_args(const Layout &L, const dq_kv_buffers *b, AttnArgs &a);
 
 // launchers (return cudaError_t as int)
 int launch_key_mean(const Layout &L, const QuantArgs &a, void *stream);

@@ -80,8 +80,6 @@ extern "C" dq_status dq_decode_attention_noalloc(const dq_config *cfg, const dq_
         if (!aligned16(p[i])) return dq::set_last_error(DQ_EALIGN, "a cache buffer is not 16-byte aligned");
     }
     if (!aligned16(q) || !aligned16(out)) return dq::set_last_error(DQ_EALIGN, "q / out not 16-byte aligned");
-    if (L.scheme == DQ_NUQ)
-        return dq::set_last_error(DQ_EUNSUPPORTED, "non-uniform scheme: attention is not built yet");
     if (static_cast<size_t>(L.U) > kMaxUnits) {
         char msg[200];
         std::snprintf(msg, sizeof msg, "batch * n_kv_heads = %d exceeds the allocation-free limit of %zu", L.U,
@@ -123,6 +121,7 @@ extern "C" dq_status dq_decode_attention_noalloc(const dq_config *cfg, const dq_
     a.hscale = static_cast<float>(1.0 / std::sqrt(static_cast<double>(L.d)));
     a.counters = reinterpret_cast<int *>(scratch);
     a.status = reinterpret_cast<unsigned *>(scratch + kStatusOffset);
+    dq::set_nuq_args(L, bufs, a);
     a.partials = reinterpret_cast<float *>(scratch + kPartialsOffset);
     // the partials must fit the static scratch: the plan narrows the grid
     // until they do, and refuses the config if even one CTA's would not

@@ -117,3 +117,39 @@ def test_nuq_append_is_refused():
     with pytest.raises(DQError):
         cache.quantize(to_device(k[:, :, :1], w.kv_dtype), to_device(v[:, :, :1], w.kv_dtype), pos0=w.seq)
     torch.cuda.synchronize()
+
+
+def _out_tol(w, ref):
+    # 2e-3 for the arithmetic, plus rounding of the output to its 16-bit type
+    ulp = 2.0 ** -8 if w.out_dtype == "bf16" else (2.0 ** -11 if w.out_dtype == "f16" else 0.0)
+    return 2e-3 + ulp * np.abs(ref)
+
+
+@pytest.mark.parametrize("name", list(CASES))
+def test_nuq_attention_matches_oracle(name):
+    import torch
+    from quantized_decode_attention_gb300 import KVCache
+    from helpers import out_to_np
+    w = CASES[name]
+    S = w.seq
+    k, v = W.make_kv(w)
+    q = W.make_q(w)
+    cache = KVCache.allocate(cfg_for(w))
+    cache.quantize(to_device(k, w.kv_dtype), to_device(v, w.kv_dtype))
+    dt = {"f16": torch.float16, "bf16": torch.bfloat16, "f32": torch.float32}[w.out_dtype]
+    out = torch.empty((w.batch, w.n_q_heads, w.head_dim), dtype=dt, device="cuda")
+    qd = to_device(q, "f32")
+    cache.attention(qd, out, S)
+    torch.cuda.synchronize()
+    cache.check()
+    got = out_to_np(out)
+    nk = OC.quantize_nuq(w, k, True, S)
+    nv = OC.quantize_nuq(w, v, False, S)
+    ref = OC.attention(w, q, k, v, S, nk, nv)
+    assert np.all(np.isfinite(got))
+    assert np.all(np.abs(got - ref) <= _out_tol(w, ref)), float(np.max(np.abs(got - ref)))
+    # the allocation-free entry point computes the same
+    out2 = torch.empty_like(out)
+    cache.attention_noalloc(qd, out2, S)
+    torch.cuda.synchronize()
+    assert np.all(np.abs(out_to_np(out2) - ref) <= _out_tol(w, ref))
