@@ -118,6 +118,27 @@ typedef struct {
  * value channel c of token t goes to
  *   idx = (c&7)*(d/8) + 2*(c>>4) + ((c>>3)&1), half = t&1,
  * in both cases word idx/F, field idx%F with F = 16/b.
+ *
+ * Non-uniform scheme (DQ_NUQ on both tensors; "KVQuant-NUQ", How it works:
+ * Lloyd-Max levels, keys per channel, values per token, Dense-and-Sparse
+ * outliers).  Codes keep the record layout above but index fp16 tables of
+ * L = 2^bits levels; meta_k, meta_v, mean_k and ol_rowptr_v are unused:
+ * lut_k       [U][head_dim][L]    fp16 levels of each key channel
+ * lut_v       [U][Qcap][L]        fp16 levels of each value token (by slot)
+ * ol_rowptr_k [U][Qcap+4]         int32: key outliers of slot p are entries
+ *                                 [rowptr[p], rowptr[p+1]); rowptr[p] for p
+ *                                 >= the fitted token count holds the total
+ * ol_col_k    [U][NNZk]           uint16 channel of each key outlier, channel
+ *                                 order within a slot
+ * ol_val_k    [U][NNZk]           its exact fp16 value
+ * ol_col_v    [U][Qcap][kv]       uint16 channel of each value outlier of a
+ *                                 token, in channel order
+ * ol_val_v    [U][Qcap][kv]       its exact fp16 value
+ * with kk = floor(k.outlier_frac * (max_seq - n_sink) + 0.5) outliers per key
+ * channel, kv = floor(v.outlier_frac * head_dim + 0.5) per value token and
+ * NNZk = round_up(head_dim * kk, 8).  A code of an outlier element is its
+ * nearest level like any other; attention replaces the table value by the
+ * stored one.
  */
 typedef struct {
     void *codes_k, *codes_v, *meta_k, *meta_v, *mean_k;
@@ -147,6 +168,9 @@ dq_status dq_kv_sizes(const dq_config *cfg, size_t bytes[DQ_NUM_BUFFERS]);
  * sinks and the latest n_recent tokens (of length pos0 + n_tok) also to their
  * raw slots.  Requires pos0 + n_tok <= max_seq.
  * The dense key transform reads bufs->k_transform.
+ * DQ_NUQ is prefill only (pos0 == 0; appends give DQ_EUNSUPPORTED) and needs
+ * max_seq - n_sink <= 8192: the key tables are fitted over every quantized
+ * token of the prefill.
  * Errors: DQ_EINVAL, DQ_EALIGN, DQ_EUNSUPPORTED, DQ_ENOMEM, DQ_ECUDA (launch).
  */
 dq_status dq_quantize_kv(dq_ctx **ctx, const dq_config *cfg, const dq_kv_buffers *bufs,
@@ -174,7 +198,8 @@ dq_status dq_decode_attention(dq_ctx **ctx, const dq_config *cfg, const dq_kv_bu
  * [slot0, slot0 + n) of K (which = 0) or V (which = 1) into
  *   out : device, [batch][n_kv_heads][n][head_dim] fp32
  * in the quantizer's space (rotated; keys with the channel mean added back):
- * x^ = fp32(o + fp32(s*m)) (+ mu).
+ * x^ = fp32(o + fp32(s*m)) (+ mu).  DQ_NUQ caches give DQ_EUNSUPPORTED (their
+ * dequantized values are the table entries and the stored outliers).
  * Errors: DQ_EINVAL, DQ_EALIGN, DQ_EUNSUPPORTED, DQ_ENOMEM, DQ_ECUDA.
  */
 dq_status dq_dequantize_kv(dq_ctx **ctx, const dq_config *cfg, const dq_kv_buffers *bufs,
