@@ -49,6 +49,7 @@ def parse():
     p.add_argument("--copies", type=int, default=0, help="cache copies rotated per step (0 = auto)")
     p.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU baseline sample budget")
     p.add_argument("--no-cpu", action="store_true")
+    p.add_argument("--no-nuq", action="store_true", help="skip the KVQuant NUQ cache measurement")
     return p.parse_args()
 
 
@@ -76,6 +77,27 @@ def algorithmic_bytes(w: W.Workload, bits: int, S: int) -> dict:
     out = w.batch * w.n_q_heads * d * 2
     total = codes + metab + mean + raw + q + out
     return {"codes": codes, "meta": metab, "mean": mean, "raw": raw, "q": q, "out": out, "total": total}
+
+
+def nuq_algorithmic_bytes(w: W.Workload, S: int) -> dict:
+    """Bytes one non-uniform decode-attention call must move: key and value
+    codes, per-token value tables, per-channel key tables, the outlier side
+    channels (key CSR by token with its row pointers, value entries per token),
+    the 16-bit sinks, q and out."""
+    U, d, L = w.batch * w.n_kv_heads, w.head_dim, 1 << w.bits
+    n_raw = min(S, w.n_sink)
+    n_q = S - n_raw
+    frac = w.extra.get("outlier_frac", 0.01)
+    kk = int(np.floor(np.float64(np.float32(frac)) * n_q + 0.5))
+    kv = int(np.floor(np.float64(np.float32(frac)) * d + 0.5))
+    codes = U * n_q * d * w.bits // 8 * 2
+    lut = U * n_q * L * 2 + U * d * L * 2
+    side = U * (d * kk * 4 + (n_q + 1) * 4) + U * n_q * kv * 4
+    raw = U * n_raw * d * 2 * 2
+    q = w.batch * w.n_q_heads * d * 4
+    out = w.batch * w.n_q_heads * d * 2
+    total = codes + lut + side + raw + q + out
+    return {"codes": codes, "tables": lut, "outliers": side, "raw": raw, "q": q, "out": out, "total": total}
 
 
 class Clocks:
@@ -129,7 +151,7 @@ def traffic_for(kernel_sha: str, bits: int):
     try:
         with open(TRAFFIC_FILE) as f:
             d = json.load(f)
-        ent = d.get(f"{bits}bit")
+        ent = d.get(bits if isinstance(bits, str) else f"{bits}bit")
         if ent and ent.get("attn_src_sha") == kernel_sha:
             return ent.get("bytes_per_launch")
     except Exception:
@@ -264,6 +286,94 @@ def run_gpu(args, w, bits, S, k_dev, v_dev, q_dev, knew_dev, vnew_dev, rank):
     return res
 
 
+def run_gpu_nuq(args, w):
+    """KVQuant NUQ cache (prefill only: no append step): each step is one
+    decode-attention call, rotating over cache copies larger than L2."""
+    import torch
+    from quantized_decode_attention_gb300 import KVCache, make_config
+    S = w.seq
+    k, v = W.make_kv(w)
+    q = W.make_q(w)
+    f16 = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).cuda().view(torch.float16)
+    k_dev, v_dev, q_dev = f16(k), f16(v), torch.from_numpy(q).cuda()
+    cfg = make_config(batch=w.batch, n_kv_heads=w.n_kv_heads, n_q_heads=w.n_q_heads, head_dim=w.head_dim,
+                      max_seq=S, kv_dtype=w.kv_dtype, out_dtype=w.out_dtype, bits=w.bits, rot_k="none",
+                      rot_v="none", mean_k=False, n_sink=w.n_sink, n_recent=w.n_recent, scheme="nuq",
+                      lloyd_iters=w.extra.get("lloyd_iters", 8), outlier_frac=w.extra.get("outlier_frac", 0.01))
+    L2 = torch.cuda.get_device_properties(0).L2_cache_size
+    ab = nuq_algorithmic_bytes(w, S)
+    copies = args.copies or max(3, int(np.ceil(3 * L2 / ab["total"])) + 1)
+    stream = torch.cuda.Stream()
+    base = KVCache.allocate(cfg, zero=False)
+    with torch.cuda.stream(stream):
+        base.quantize(k_dev, v_dev, pos0=0, stream=stream.cuda_stream)  # context and workspace
+        stream.synchronize()
+        p0, p1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        p0.record(stream)
+        base.quantize(k_dev, v_dev, pos0=0, stream=stream.cuda_stream)
+        p1.record(stream)
+        stream.synchronize()
+    prefill_ms = p0.elapsed_time(p1)
+    base.check()
+    caches = [base] + [base.clone_shared() for _ in range(copies - 1)]
+    del k_dev, v_dev
+    out = torch.empty((w.batch, w.n_q_heads, w.head_dim), dtype=torch.float16, device="cuda")
+    sm_scale = w.head_dim ** -0.5
+    with torch.cuda.stream(stream):
+        for c in caches:
+            c.attention(q_dev, out, S, sm_scale, stream=stream.cuda_stream)
+        stream.synchronize()
+        macro = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(macro, stream=stream):
+            for c in caches:
+                c.attention(q_dev, out, S, sm_scale, stream=stream.cuda_stream)
+        nc = len(caches)
+        reps = max(1, args.steps // nc)
+        for _ in range(max(1, args.warmup // nc)):
+            macro.replay()
+        stream.synchronize()
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for _ in range(reps):
+            macro.replay()
+        t1.record(stream)
+        stream.synchronize()
+        total_ms = t0.elapsed_time(t1)
+        n_attn = min(args.steps, 200)
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_attn)]
+        torch.cuda._sleep(int(2e8))
+        for i in range(n_attn):
+            evs[i][0].record(stream)
+            caches[i % nc].attention(q_dev, out, S, sm_scale, stream=stream.cuda_stream)
+            evs[i][1].record(stream)
+        stream.synchronize()
+        attn_ms = [a.elapsed_time(b) for a, b in evs]
+        # e2e through the public API: q H2D from pinned memory, output D2H
+        q_h = q_dev.cpu().pin_memory()
+        out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        q_b = q_dev.clone()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        wall0 = time.perf_counter()
+        e0.record(stream)
+        for i in range(n_attn):
+            q_b.copy_(q_h, non_blocking=True)
+            caches[i % nc].attention(q_b, out, S, sm_scale, stream=stream.cuda_stream)
+            out_h.copy_(out, non_blocking=True)
+        e1.record(stream)
+        stream.synchronize()
+        e2e_ms = max(e0.elapsed_time(e1), (time.perf_counter() - wall0) * 1e3)
+    for c in caches:
+        c.check()
+    steps = reps * nc
+    res = {"total_ms": total_ms, "steps": steps, "attn_ms": statistics.mean(attn_ms),
+           "attn_ms_median": statistics.median(attn_ms), "algo": ab, "copies": nc, "prefill_ms": prefill_ms,
+           "e2e_tok_s": w.batch * n_attn / (e2e_ms / 1e3)}
+    for c in caches[1:]:
+        c.detach()
+    caches[0].close()
+    return res
+
+
 def cpu_baseline(w, bits, S, budget_s, k, v, q):
     """The oracle as it stands, timed on this host: quantize one unit's cache and
     run its fp64 decode attention, for as many units as fit the budget."""
@@ -341,6 +451,7 @@ def main():
         r = run_gpu(args, w.with_(bits=vb), vb, S, k_dev, v_dev, q_dev, kn_dev, vn_dev, rank)
         variants[f"{vb}bit"] = r
     del k_dev, v_dev
+    nuq = None if args.no_nuq else run_gpu_nuq(args, W.NUQ)
     total_ms = res["total_ms"]
     if world > 1:
         t = torch.tensor([total_ms], device="cuda")
@@ -377,6 +488,17 @@ def main():
                           "ms_per_step": round(r["total_ms"] / args.steps, 5), "roofline": roof(r, int(k2[0])),
                           "e2e_tok_s": round(r["e2e_tok_s"], 1)} for k2, r in variants.items()},
     }
+    if nuq is not None:
+        line["variants"][f"{W.NUQ.name}-{W.NUQ.bits}bit"] = {
+            "value": round(W.NUQ.batch / (nuq["total_ms"] / nuq["steps"] / 1e3), 1),
+            "ms_per_step": round(nuq["total_ms"] / nuq["steps"], 5),
+            "roofline": roof(nuq, "nuq"), "e2e_tok_s": round(nuq["e2e_tok_s"], 1),
+            "prefill_ms": round(nuq["prefill_ms"], 3),
+            "config": {"batch": W.NUQ.batch, "q_heads": W.NUQ.n_q_heads, "kv_heads": W.NUQ.n_kv_heads,
+                       "head_dim": W.NUQ.head_dim, "seq_len": W.NUQ.seq, "bits": W.NUQ.bits,
+                       "n_sink": W.NUQ.n_sink, "outlier_frac": 0.01, "lloyd_iters": 8,
+                       "l2": f"{nuq['copies']} cache copies rotated per step (> L2)",
+                       "step": "decode attention (prefill-only scheme), CUDA graph over the copies"}}
     if rank == 0 and not args.no_cpu:
         line["cpu_baseline"] = cpu_baseline(w, args.bits, S, args.cpu_seconds, k, v, q)
     if rank == 0:

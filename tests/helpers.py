@@ -76,3 +76,32 @@ def lib_views(w: W.Workload, cache, max_seq: int):
         out["raw_k"] = t["raw_k"].view(np.uint16).reshape(B, H, rcap, d)
         out["raw_v"] = t["raw_v"].view(np.uint16).reshape(B, H, rcap // 2, d, 2)
     return out
+
+
+def nuq_views(w: W.Workload, cache, S: int):
+    """Reshape a non-uniform cache's byte buffers into [B, H, ...] numpy views."""
+    from quantized_decode_attention_gb300 import kv_sizes
+    B, H, d, L = w.batch, w.n_kv_heads, w.head_dim, 1 << w.bits
+    qcap = -(-(S - w.n_sink) // 64) * 64
+    rcap = -(-(w.n_sink + w.n_recent) // 16) * 16
+    rowk = d * w.bits // 8
+    t = {n: (x.cpu().numpy() if x is not None else None) for n, x in cache.tensors.items()}
+    sizes = kv_sizes(cache.cfg)
+    v = {
+        "codes_k": t["codes_k"].reshape(B, H, qcap, rowk),
+        "codes_v": t["codes_v"].reshape(B, H, qcap // 2, 2 * rowk),
+        "lut_k": t["lut_k"].view(np.uint16).reshape(B, H, d, L),
+        "lut_v": t["lut_v"].view(np.uint16).reshape(B, H, qcap, L),
+    }
+    if t["ol_rowptr_k"] is not None:
+        v["rowptr"] = t["ol_rowptr_k"].view(np.int32).reshape(B, H, -1)
+        v["col_k"] = t["ol_col_k"].view(np.uint16).reshape(B, H, -1)
+        v["val_k"] = t["ol_val_k"].view(np.uint16).reshape(B, H, -1)
+    if t["ol_col_v"] is not None:
+        v["col_v"] = t["ol_col_v"].view(np.uint16).reshape(B, H, qcap, -1)
+        v["val_v"] = t["ol_val_v"].view(np.uint16).reshape(B, H, qcap, -1)
+    if rcap:
+        v["raw_k"] = t["raw_k"].view(np.uint16).reshape(B, H, rcap, d)
+        v["raw_v"] = t["raw_v"].view(np.uint16).reshape(B, H, rcap // 2, d, 2)
+    assert sizes["meta_k"] == 0 and sizes["mean_k"] == 0
+    return v, qcap

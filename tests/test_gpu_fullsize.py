@@ -1,0 +1,143 @@
+"""Parity at the benchmark's full sizes, on sampled (batch, KV head) units.
+
+The caches and calls are the ones the benchmark times:
+- the Llama-3-8B-shaped decode layer (batch 16, 32 query / 8 KV heads, d128,
+  8192 bf16 tokens, 4 sinks + 128 recent) at 2, 3 and 4 bits, prefilled, then
+  one token re-appended at position 8191 and attention over 8192 tokens, both
+  replayed from one CUDA graph;
+- the KVQuant NUQ cache (batch 8, 4096 fp16 Student-t tokens, 3 bits, 1 sink,
+  1 % outliers), prefilled, attention over 4096 tokens from a CUDA graph.
+The oracle recomputes a few units one by one.  Their records, metadata, tables
+and side channels must match bit for bit, and the outputs of their query heads
+must be within the attention tolerance (2e-3 plus the output's own rounding).
+"""
+import numpy as np
+import pytest
+
+import oracle
+import workloads as W
+from oracle import cache as OC
+
+from helpers import cfg_for, expected_buffers, lib_views, nuq_views, out_to_np, to_device
+
+pytestmark = pytest.mark.gpu
+
+LLAMA_UNITS = [(0, 0), (7, 3), (15, 7)]
+NUQ_UNITS = [(0, 0), (3, 5), (7, 7)]
+
+
+def _tol(ref, out_dtype):
+    ulp = {"bf16": 2.0 ** -8, "f16": 2.0 ** -11}.get(out_dtype, 0.0)
+    return 2e-3 + ulp * np.abs(ref)
+
+
+def _graph_replay(fn):
+    """Run fn(stream) once eagerly, then capture it in a CUDA graph and replay it."""
+    import torch
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        fn(s)
+        s.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            fn(s)
+        g.replay()
+        s.synchronize()
+    return g
+
+
+@pytest.fixture(scope="module")
+def llama_inputs():
+    w = W.LLAMA
+    k, v = W.make_kv(w)
+    kn, vn = W.make_new_token(w)
+    q = W.make_q(w)
+    return w, k, v, kn, vn, q
+
+
+@pytest.mark.parametrize("bits", [2, 3, 4])
+def test_llama_full_size_sampled_units(llama_inputs, bits):
+    import torch
+    from quantized_decode_attention_gb300 import KVCache
+    w0, k, v, kn, vn, q = llama_inputs
+    w = w0.with_(bits=bits)
+    S = w.seq
+    cache = KVCache.allocate(cfg_for(w), zero=False)
+    cache.quantize(to_device(k, "bf16"), to_device(v, "bf16"), pos0=0)
+    kn_d, vn_d, q_d = to_device(kn, "bf16"), to_device(vn, "bf16"), to_device(q, "f32")
+    out = torch.empty((w.batch, w.n_q_heads, w.head_dim), dtype=torch.bfloat16, device="cuda")
+
+    def step(s):
+        cache.quantize(kn_d, vn_d, pos0=S - 1, stream=s.cuda_stream)
+        cache.attention(q_d, out, S, stream=s.cuda_stream)
+
+    _graph_replay(step)
+    cache.check()
+    got_out = out_to_np(out)
+    got = lib_views(w, cache, S)
+    # the cache the calls describe: token S-1 replaced by the new one (it lies
+    # in the recent window at prefill, so the frozen key mean is unchanged)
+    kf, vf = k.copy(), v.copy()
+    kf[:, :, S - 1], vf[:, :, S - 1] = kn[:, :, 0], vn[:, :, 0]
+    nq = S - w.n_sink
+    w1 = w.with_(batch=1, n_kv_heads=1, n_q_heads=w.group)
+    for b, h in LLAMA_UNITS:
+        ku, vu = kf[b:b + 1, h:h + 1], vf[b:b + 1, h:h + 1]
+        qk = oracle.quantize_tensor(w1, ku, True, S)
+        qv = oracle.quantize_tensor(w1, vu, False, S)
+        exp = expected_buffers(w1, qk, qv, nq)
+        assert np.array_equal(got["codes_k"][b, h, :nq], exp["codes_k"][0, 0]), (b, h)
+        assert np.array_equal(got["codes_v"][b, h, :nq // 2], exp["codes_v"][0, 0, :nq // 2]), (b, h)
+        assert np.array_equal(got["meta_k"][b, h, :nq], exp["meta_k"][0, 0]), (b, h)
+        assert np.array_equal(got["meta_v"][b, h, :nq], exp["meta_v"][0, 0]), (b, h)
+        assert np.array_equal(got["mean_k"][b, h].view(np.uint32), qk.mu[0, 0].view(np.uint32)), (b, h)
+        assert np.array_equal(got["raw_k"][b, h, w.n_sink + (S - 1) % w.n_recent], kn[b, h, 0])
+        qu = q[b:b + 1, h * w.group:(h + 1) * w.group]
+        ref = oracle.attention(w1, qu, ku, vu, S, qk, qv)[0]
+        g = got_out[b, h * w.group:(h + 1) * w.group]
+        assert np.all(np.abs(g - ref) <= _tol(ref, w.out_dtype)), (b, h, float(np.max(np.abs(g - ref))))
+    assert np.all(np.isfinite(got_out))
+    cache.close()
+
+
+def test_nuq_full_size_sampled_units():
+    import torch
+    from quantized_decode_attention_gb300 import KVCache
+    w = W.NUQ
+    S = w.seq
+    k, v = W.make_kv(w)
+    q = W.make_q(w)
+    cache = KVCache.allocate(cfg_for(w), zero=False)
+    cache.quantize(to_device(k, w.kv_dtype), to_device(v, w.kv_dtype), pos0=0)
+    q_d = to_device(q, "f32")
+    out = torch.empty((w.batch, w.n_q_heads, w.head_dim), dtype=torch.float16, device="cuda")
+    _graph_replay(lambda s: cache.attention(q_d, out, S, stream=s.cuda_stream))
+    cache.check()
+    got_out = out_to_np(out)
+    got, qcap = nuq_views(w, cache, S)
+    nq = S - w.n_sink
+    w1 = w.with_(batch=1, n_kv_heads=1, n_q_heads=w.group)
+    for b, h in NUQ_UNITS:
+        ku, vu = k[b:b + 1, h:h + 1], v[b:b + 1, h:h + 1]
+        nk = OC.quantize_nuq(w1, ku, True, S)
+        nv = OC.quantize_nuq(w1, vu, False, S)
+        assert np.array_equal(got["lut_k"][b, h], nk.lut[0, 0]), (b, h)
+        assert np.array_equal(got["lut_v"][b, h, :nq], nv.lut[0, 0]), (b, h)
+        assert np.array_equal(got["codes_k"][b, h, :nq], OC.pack_k(nk.codes, w.bits)[0, 0]), (b, h)
+        pv = OC.pack_v(nv.codes, w.bits)[0, 0]
+        assert np.array_equal(got["codes_v"][b, h, :nq // 2], pv[:nq // 2]), (b, h)
+        rp, col, val = OC.nuq_key_outliers_csr(nk, qcap, got["col_k"].shape[-1])
+        assert np.array_equal(got["rowptr"][b, h, :qcap + 1], rp[0, 0]), (b, h)
+        n_nz = int(rp[0, 0, -1])
+        assert n_nz == w.head_dim * oracle.outlier_count(0.01, nq)
+        assert np.array_equal(got["col_k"][b, h, :n_nz], col[0, 0, :n_nz]), (b, h)
+        assert np.array_equal(got["val_k"][b, h, :n_nz], val[0, 0, :n_nz]), (b, h)
+        cv, vv = OC.nuq_value_outliers(nv, qcap, got["col_v"].shape[-1])
+        assert np.array_equal(got["col_v"][b, h, :nq], cv[0, 0, :nq]), (b, h)
+        assert np.array_equal(got["val_v"][b, h, :nq], vv[0, 0, :nq]), (b, h)
+        qu = q[b:b + 1, h * w.group:(h + 1) * w.group]
+        ref = OC.attention(w1, qu, ku, vu, S, nk, nv)[0]
+        g = got_out[b, h * w.group:(h + 1) * w.group]
+        assert np.all(np.abs(g - ref) <= _tol(ref, w.out_dtype)), (b, h, float(np.max(np.abs(g - ref))))
+    assert np.all(np.isfinite(got_out))
+    cache.close()

@@ -10,7 +10,7 @@ import pytest
 import workloads as W
 from oracle import cache as OC
 
-from helpers import cfg_for, to_device
+from helpers import cfg_for, nuq_views, to_device
 
 pytestmark = pytest.mark.gpu
 
@@ -29,34 +29,6 @@ CASES = {
 }
 
 
-def _views(w, cache, S):
-    from quantized_decode_attention_gb300 import kv_sizes
-    B, H, d, L = w.batch, w.n_kv_heads, w.head_dim, 1 << w.bits
-    qcap = -(-(S - w.n_sink) // 64) * 64
-    rcap = -(-(w.n_sink + w.n_recent) // 16) * 16
-    rowk = d * w.bits // 8
-    t = {n: (x.cpu().numpy() if x is not None else None) for n, x in cache.tensors.items()}
-    sizes = kv_sizes(cache.cfg)
-    v = {
-        "codes_k": t["codes_k"].reshape(B, H, qcap, rowk),
-        "codes_v": t["codes_v"].reshape(B, H, qcap // 2, 2 * rowk),
-        "lut_k": t["lut_k"].view(np.uint16).reshape(B, H, d, L),
-        "lut_v": t["lut_v"].view(np.uint16).reshape(B, H, qcap, L),
-    }
-    if t["ol_rowptr_k"] is not None:
-        v["rowptr"] = t["ol_rowptr_k"].view(np.int32).reshape(B, H, -1)
-        v["col_k"] = t["ol_col_k"].view(np.uint16).reshape(B, H, -1)
-        v["val_k"] = t["ol_val_k"].view(np.uint16).reshape(B, H, -1)
-    if t["ol_col_v"] is not None:
-        v["col_v"] = t["ol_col_v"].view(np.uint16).reshape(B, H, qcap, -1)
-        v["val_v"] = t["ol_val_v"].view(np.uint16).reshape(B, H, qcap, -1)
-    if rcap:
-        v["raw_k"] = t["raw_k"].view(np.uint16).reshape(B, H, rcap, d)
-        v["raw_v"] = t["raw_v"].view(np.uint16).reshape(B, H, rcap // 2, d, 2)
-    assert sizes["meta_k"] == 0 and sizes["mean_k"] == 0
-    return v, qcap
-
-
 @pytest.mark.parametrize("name", list(CASES))
 def test_nuq_prefill_is_bit_exact(name):
     import torch
@@ -68,7 +40,7 @@ def test_nuq_prefill_is_bit_exact(name):
     cache.quantize(to_device(k, w.kv_dtype), to_device(v, w.kv_dtype))
     torch.cuda.synchronize()
     cache.check()
-    got, qcap = _views(w, cache, S)
+    got, qcap = nuq_views(w, cache, S)
     nk = OC.quantize_nuq(w, k, True, S)
     nv = OC.quantize_nuq(w, v, False, S)
     nq = S - w.n_sink
