@@ -5,7 +5,7 @@ arm of ``bench.py`` may import this package.  The CUDA library never does, and
 this package never imports the CUDA library: the two share nothing but the
 seeded input generators in ``workloads.py``.
 
-The arithmetic lives in plain C (``affine.c``, ``format.c``, ``nuq.c``), compiled with
+The arithmetic lives in plain C (``affine.c``, ``format.c``, ``nuq.c``, ``rans.c``), compiled with
 ``-O2 -ffp-contract=off`` into ``liboracle.so``; this module only marshals
 arguments and assembles whole-cache buffers from per-token C results.
 """
@@ -93,6 +93,31 @@ def lib():
             L.or_nuq_assign.argtypes = [_f32, C.c_int, _u16, C.c_int, _u8]
             L.or_nuq_vector.restype = C.c_int
             L.or_nuq_vector.argtypes = [_f32, C.c_int, C.c_int, C.c_int, C.c_float, _u8, _u16, _u8]
+            _i32 = _P(dtype=np.int32, flags="C_CONTIGUOUS")
+            _i64 = _P(dtype=np.int64, flags="C_CONTIGUOUS")
+            L.or_dq_expected_max.restype = C.c_double
+            L.or_dq_expected_max.argtypes = [C.c_int]
+            L.or_dq_table.restype = C.c_int
+            L.or_dq_table.argtypes = [C.c_int, C.c_int, C.c_double, C.c_int, _i32, _i32, _f64]
+            L.or_dq_costs.argtypes = [_i32, C.c_int, C.c_int, _i64]
+            L.or_dq_pow2_table.argtypes = [_f32]
+            L.or_dq_drift.restype = C.c_int
+            L.or_dq_drift.argtypes = [_f32, C.c_int, C.c_float, C.c_float, _i64, C.c_int, C.c_longlong, _f32,
+                                      _u8, C.POINTER(C.c_longlong)]
+            L.or_dq_refit.argtypes = [_f32, _u8, C.c_int, C.POINTER(C.c_float), C.POINTER(C.c_float)]
+            L.or_rans_encode.restype = C.c_int
+            L.or_rans_encode.argtypes = [_u8, C.c_int, _i32, _i32, C.c_int, C.c_int, _u8]
+            L.or_rans_decode.restype = C.c_int
+            L.or_rans_decode.argtypes = [_u8, C.c_int, C.c_int, _i32, _i32, C.c_int, C.c_int, _u8,
+                                         C.POINTER(C.c_uint32), C.POINTER(C.c_int)]
+            L.or_dq_encode_stream.restype = C.c_int
+            L.or_dq_encode_stream.argtypes = [_f32, C.c_int, C.c_int, C.c_int, _i32, _i32, C.c_int, _i64, _f32,
+                                              _u8, C.POINTER(C.c_uint16), C.POINTER(C.c_uint16), _u8, C.c_void_p]
+            L.or_dq_window_mean.argtypes = [_f32, C.c_int, C.c_int, _P(dtype=np.int8, flags="C_CONTIGUOUS"),
+                                            C.POINTER(C.c_uint16), _f32]
+            L.or_dq_encode_streams.argtypes = [_f32, C.c_int, C.c_int, C.c_int, C.c_int, _i32, _i32, C.c_int, _i64,
+                                               _f32, _u8, _u16, _u16, _u8, _i32]
+            L.or_rotate_hadamard_rows.argtypes = [_f32, _f32, C.c_long, C.c_int]
             _lib = L
         return _lib
 
@@ -124,6 +149,15 @@ def rotate_hadamard(x: np.ndarray) -> np.ndarray:
     x = np.ascontiguousarray(x, dtype=np.float32)
     y = np.empty_like(x)
     lib().or_rotate_hadamard(x, y, x.shape[-1])
+    return y
+
+
+def rotate_hadamard_rows(x: np.ndarray) -> np.ndarray:
+    """The normalized Hadamard rotation of every row (last axis) of x."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    y = np.empty_like(x)
+    d = x.shape[-1]
+    lib().or_rotate_hadamard_rows(x, y, x.size // d, d)
     return y
 
 
@@ -243,6 +277,131 @@ def nuq_vector(x, bits: int, iters: int, frac: float):
     codes = np.zeros(x.size, dtype=np.uint8)
     lib().or_nuq_vector(x, x.size, bits, iters, float(frac), flag, lut, codes)
     return flag.astype(bool), lut, codes
+
+
+# ---- D-Quant container (rans.c) ---------------------------------------------
+
+class DqTable:
+    """Frequency table of one tensor: f, c (int32), fixed-point costs r (int64),
+    the unsharpened bin probabilities, and the prob precision p."""
+
+    def __init__(self, n: int, M: int, alpha: float = 1.4, p: int = 8):
+        self.n, self.M, self.alpha, self.p = n, M, alpha, p
+        self.f = np.zeros(M, dtype=np.int32)
+        self.c = np.zeros(M, dtype=np.int32)
+        self.prob = np.zeros(M, dtype=np.float64)
+        if lib().or_dq_table(n, M, float(alpha), p, self.f, self.c, self.prob) != 0:
+            raise ValueError("no valid frequency table")
+        self.r = np.zeros(M, dtype=np.int64)
+        lib().or_dq_costs(self.f, M, p, self.r)
+
+    @classmethod
+    def from_freqs(cls, f, p: int = 8) -> "DqTable":
+        """A table with given frequencies (summing to 2^p), for hand-worked cases."""
+        t = cls.__new__(cls)
+        t.n, t.M, t.alpha, t.p = 0, len(f), 1.0, p
+        t.f = np.ascontiguousarray(f, dtype=np.int32)
+        t.c = np.concatenate([[0], np.cumsum(t.f)[:-1]]).astype(np.int32)
+        t.prob = t.f / float(1 << p)
+        t.r = np.zeros(t.M, dtype=np.int64)
+        lib().or_dq_costs(t.f, t.M, p, t.r)
+        return t
+
+
+def dq_expected_max(n: int) -> float:
+    return float(lib().or_dq_expected_max(n))
+
+
+def dq_pow2_table() -> np.ndarray:
+    F = np.zeros(512, dtype=np.float32)
+    lib().or_dq_pow2_table(F)
+    return F
+
+
+def dq_budget_fx(C_bytes: int) -> int:
+    """B * 2^16 with B = 8C - 32 (sigma = a 32-bit state)."""
+    return (8 * C_bytes - 32) * 65536
+
+
+def dq_drift(x, s: float, o: float, tab: DqTable, C_bytes: int | None = None, F=None, budget_fx=None):
+    """Drift assignment: (symbols, integer cost, feasible).  The budget is that of a
+    C_bytes container, or budget_fx (bits * 2^16) directly."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    F = dq_pow2_table() if F is None else F
+    m = np.zeros(x.size, dtype=np.uint8)
+    cost = C.c_longlong(0)
+    bfx = dq_budget_fx(C_bytes) if budget_fx is None else int(budget_fx)
+    ok = lib().or_dq_drift(x, x.size, float(s), float(o), tab.r, tab.M, bfx, F, m, C.byref(cost))
+    return m, int(cost.value), bool(ok)
+
+
+def dq_refit(x, m, s: float, o: float):
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    m = np.ascontiguousarray(m, dtype=np.uint8)
+    sc, oc = C.c_float(s), C.c_float(o)
+    lib().or_dq_refit(x, m, x.size, C.byref(sc), C.byref(oc))
+    return float(sc.value), float(oc.value)
+
+
+def rans_encode(m, tab: DqTable, C_bytes: int):
+    """(container bytes, emitted byte count or -1 on overflow)."""
+    m = np.ascontiguousarray(m, dtype=np.uint8)
+    out = np.zeros(C_bytes, dtype=np.uint8)
+    pushed = lib().or_rans_encode(m, m.size, tab.f, tab.c, tab.p, C_bytes, out)
+    return out, int(pushed)
+
+
+def rans_decode(container, n: int, tab: DqTable):
+    """(symbols, final state, bytes consumed after the state); raises if the
+    decoder would read past the container."""
+    pay = np.ascontiguousarray(container, dtype=np.uint8)
+    m = np.zeros(n, dtype=np.uint8)
+    xf, used = C.c_uint32(0), C.c_int(0)
+    if lib().or_rans_decode(pay, pay.size, n, tab.f, tab.c, tab.M, tab.p, m, C.byref(xf), C.byref(used)) != 0:
+        raise ValueError("decoder ran past the container")
+    return m, int(xf.value), int(used.value)
+
+
+def dq_encode_stream(x, tab: DqTable, C_bytes: int, F=None):
+    """Algorithm 1 on one stream: dict(container, s16, o16, m, m_near, flags)."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    F = dq_pow2_table() if F is None else F
+    cont = np.zeros(C_bytes, dtype=np.uint8)
+    m = np.zeros(x.size, dtype=np.uint8)
+    mn = np.zeros(x.size, dtype=np.uint8)
+    s16, o16 = C.c_uint16(0), C.c_uint16(0)
+    flags = lib().or_dq_encode_stream(x, x.size, tab.M, C_bytes, tab.f, tab.c, tab.p, tab.r, F, cont,
+                                      C.byref(s16), C.byref(o16), m, mn.ctypes.data_as(C.c_void_p))
+    return {"container": cont, "s16": int(s16.value), "o16": int(o16.value), "m": m, "m_near": mn,
+            "flags": int(flags)}
+
+
+def dq_encode_streams(X, tab: DqTable, C_bytes: int, F=None):
+    """Algorithm 1 on each row of X [ns, n]: (containers [ns, C], s16 [ns], o16 [ns],
+    symbols [ns, n], flags [ns])."""
+    X = np.ascontiguousarray(X, dtype=np.float32)
+    ns, n = X.shape
+    F = dq_pow2_table() if F is None else F
+    cont = np.zeros((ns, C_bytes), dtype=np.uint8)
+    s16 = np.zeros(ns, dtype=np.uint16)
+    o16 = np.zeros(ns, dtype=np.uint16)
+    m = np.zeros((ns, n), dtype=np.uint8)
+    flags = np.zeros(ns, dtype=np.int32)
+    if ns:
+        lib().or_dq_encode_streams(X, ns, n, tab.M, C_bytes, tab.f, tab.c, tab.p, tab.r, F, cont, s16, o16, m,
+                                   flags)
+    return cont, s16, o16, m, flags
+
+
+def dq_window_mean(y):
+    """y [n_tok, n] fp32 -> (int8 q [n], fp16 scale bits, dequantized mean [n] fp32)."""
+    y = np.ascontiguousarray(y, dtype=np.float32)
+    n_tok, n = y.shape
+    q = np.zeros(n, dtype=np.int8)
+    mu = np.zeros(n, dtype=np.float32)
+    sc = C.c_uint16(0)
+    lib().or_dq_window_mean(y, n_tok, n, q, C.byref(sc), mu)
+    return q, int(sc.value), mu
 
 
 def attention_f64(q: np.ndarray, K: np.ndarray, V: np.ndarray, sm_scale: float) -> np.ndarray:

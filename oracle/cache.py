@@ -192,6 +192,88 @@ def nuq_value_outliers(nt: NuqTensor, qcap: int, k: int):
     return col, val
 
 
+@dataclass
+class DqTensor:
+    """D-Quant cache of one tensor (all KV heads of a token form one stream).
+
+    container [B, Sq, C] uint8; s16, o16 [B, Sq] uint16 fp16 bits; m [B, Sq, n]
+    symbols (n = Hkv * d, head-major); flags [B, Sq] (1 = over budget, 2 =
+    container overflow); keys also carry the windowed mean: mean_q [B, Wn, n]
+    int8, mean_sc [B, Wn] fp16 bits, mu_hat [B, Wn, n] fp32 (window = 128
+    quantized slots)."""
+    container: np.ndarray
+    s16: np.ndarray
+    o16: np.ndarray
+    m: np.ndarray
+    flags: np.ndarray
+    mean_q: np.ndarray | None = None
+    mean_sc: np.ndarray | None = None
+    mu_hat: np.ndarray | None = None
+
+
+def dq_tables(w: W.Workload):
+    """(key table, value table) of a D-Quant workload."""
+    from . import DqTable
+    n = w.n_kv_heads * w.head_dim
+    a = w.extra.get("alpha", 1.4)
+    return (DqTable(n, w.extra.get("levels_k", 8), alpha=a), DqTable(n, w.extra.get("levels_v", 6), alpha=a))
+
+
+def quantize_dquant(w: W.Workload, x_bits: np.ndarray, is_key: bool, S: int) -> DqTensor:
+    """Prefill of tokens [n_sink, S) of x_bits [B,Hkv,S,d] under D-Quant
+    (Algorithm 1 per stream; keys rotated and windowed-mean removed)."""
+    from . import dq_encode_streams, dq_window_mean, rotate_hadamard_rows
+    B, H, _, d = x_bits.shape
+    n = H * d
+    ns = w.n_sink
+    nq = S - ns
+    x = _f32_input(x_bits, w.kv_dtype)[:, :, ns:S]                 # [B,H,nq,d]
+    rot = w.rot_k if is_key else w.rot_v
+    if rot == "hadamard":
+        x = rotate_hadamard_rows(x)
+    streams = np.ascontiguousarray(x.transpose(0, 2, 1, 3).reshape(B, nq, n))
+    tk, tv = dq_tables(w)
+    tab = tk if is_key else tv
+    C_bytes = w.extra.get("container_k" if is_key else "container_v")
+    mean_q = mean_sc = mu_hat = None
+    if is_key and w.mean_k:
+        Wl = w.extra.get("mean_window", 128)
+        nw = -(-nq // Wl)
+        mean_q = np.zeros((B, nw, n), dtype=np.int8)
+        mean_sc = np.zeros((B, nw), dtype=np.uint16)
+        mu_hat = np.zeros((B, nw, n), dtype=np.float32)
+        for b in range(B):
+            for wi in range(nw):
+                q8, sc, mh = dq_window_mean(streams[b, wi * Wl:(wi + 1) * Wl])
+                mean_q[b, wi], mean_sc[b, wi], mu_hat[b, wi] = q8, sc, mh
+        widx = np.arange(nq) // Wl
+        streams = (streams - mu_hat[:, widx]).astype(np.float32)   # fp32 subtraction
+    cont, s16, o16, m, flags = dq_encode_streams(streams.reshape(B * nq, n), tab, C_bytes)
+    return DqTensor(cont.reshape(B, nq, C_bytes), s16.reshape(B, nq), o16.reshape(B, nq), m.reshape(B, nq, n),
+                    flags.reshape(B, nq), mean_q, mean_sc, mu_hat)
+
+
+def dquant_dequant_f64(w: W.Workload, dt: DqTensor, is_key: bool) -> np.ndarray:
+    """Dequantized quantized tokens in the raw space, fp64 [B, Hkv, Sq, d]:
+    x^ = s m + o (+ the dequantized window mean for keys), rotated back."""
+    B, nq, n = dt.m.shape
+    H, d = w.n_kv_heads, w.head_dim
+    s = dt.s16.view(np.float16).astype(np.float64)
+    o = dt.o16.view(np.float16).astype(np.float64)
+    x = s[..., None] * dt.m.astype(np.float64) + o[..., None]
+    if dt.mu_hat is not None:
+        Wl = w.extra.get("mean_window", 128)
+        x = x + dt.mu_hat[:, np.arange(nq) // Wl].astype(np.float64)
+    x = x.reshape(B, nq, H, d).transpose(0, 2, 1, 3)
+    if (w.rot_k if is_key else w.rot_v) == "hadamard":
+        # the normalized Hadamard transform is its own inverse (fp64, exact +-1 entries)
+        Hm = np.array([[1.0]])
+        while Hm.shape[0] < d:
+            Hm = np.block([[Hm, Hm], [Hm, -Hm]])
+        x = x @ (Hm / np.sqrt(d))
+    return np.ascontiguousarray(x)
+
+
 def pack_k(codes: np.ndarray, bits: int) -> np.ndarray:
     """[..., n, d] codes -> [..., n, row_bytes] key records."""
     lead = codes.shape[:-1]
@@ -265,7 +347,10 @@ def attention(w: W.Workload, q: np.ndarray, k_bits: np.ndarray, v_bits: np.ndarr
         K[:n_s], V[:n_s] = kr[:n_s], vr[:n_s]
         K[q_hi:S], V[q_hi:S] = kr[q_hi:S], vr[q_hi:S]
         nq = q_hi - n_s
-        if nq > 0 and isinstance(qk, NuqTensor):
+        if nq > 0 and isinstance(qk, DqTensor):
+            K[n_s:q_hi] = dquant_dequant_f64(w, qk, True)[b, h, :nq]
+            V[n_s:q_hi] = dquant_dequant_f64(w, qv, False)[b, h, :nq]
+        elif nq > 0 and isinstance(qk, NuqTensor):
             K[n_s:q_hi] = qk.xhat[b, h, :nq].astype(np.float64)
             V[n_s:q_hi] = qv.xhat[b, h, :nq].astype(np.float64)
         elif nq > 0:
@@ -299,5 +384,6 @@ def _attn(L, q, K, V, sm_scale):
 
 
 __all__ = ["QuantTensor", "quantize_tensor", "NuqTensor", "quantize_nuq", "nuq_key_outliers_csr",
+           "DqTensor", "dq_tables", "quantize_dquant", "dquant_dequant_f64",
            "nuq_value_outliers", "pack_k", "pack_v", "meta_f16_bits", "raw_regions",
            "attention", "raw16_bits", "raw16_to_f64", "raw_dtype"]

@@ -1,0 +1,298 @@
+"""Pins of the D-Quant oracle (fixed-size rANS container with Drift) against
+facts fixed outside the oracle.
+
+Source: "D-Quant: Driftable Entropy Coding for KV Cache Quantization" --
+Sec. 4.2 Eq. (3)-(4) (container budget, token-wise affine grid, Gaussian
+order-statistics model), Sec. 4.3 Eq. (5)-(6) (Drift), Sec. 4.4 (sharpening),
+App. A Algorithms 1-2 (encoder, decoder), App. C (drift moves symbols by at
+most one level).  The rANS coder is Duda (2013), cited on the page.
+"""
+import itertools
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+
+pytestmark = pytest.mark.filterwarnings("ignore")
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "rans_hand.json")
+L_STATE = 1 << 23
+
+
+# ---- probability model ------------------------------------------------------
+
+@pytest.mark.parametrize("n,want,tol", [
+    (1, 0.0, 1e-12),
+    (2, 1.0 / math.sqrt(math.pi), 1e-9),              # closed form
+    (3, 3.0 / (2.0 * math.sqrt(math.pi)), 1e-9),      # closed form
+    (5, 1.16296, 2e-5),                                # tabulated expected maxima of N(0,1) samples
+    (10, 1.53875, 2e-5),
+    (100, 2.50759, 2e-5),
+])
+def test_expected_max_of_normals(n, want, tol):
+    assert abs(oracle.dq_expected_max(n) - want) < tol
+
+
+def test_bin_probabilities_match_a_library_integration():
+    scipy = pytest.importorskip("scipy")
+    from scipy import integrate, stats
+    n, M = 1024, 8
+    dens = lambda x: x * n * stats.norm.pdf(x) * stats.norm.cdf(x) ** (n - 1)
+    a = integrate.quad(dens, -12, 12, limit=400, points=[2.0, 3.0, 4.0])[0]
+    assert abs(oracle.dq_expected_max(n) - a) < 1e-8
+    u = -a + 2 * a * np.arange(M) / (M - 1)
+    edges = np.concatenate([[-np.inf], (u[1:] + u[:-1]) / 2, [np.inf]])
+    p = np.diff(stats.norm.cdf(edges))
+    t = oracle.DqTable(n, M, alpha=1.4)
+    assert np.allclose(t.prob, p, atol=1e-10)
+
+
+@pytest.mark.parametrize("M", [2, 3, 4, 6, 8, 12, 16])
+@pytest.mark.parametrize("alpha", [1.0, 1.4])
+def test_frequency_table_is_a_valid_symmetric_model(M, alpha):
+    t = oracle.DqTable(1024, M, alpha=alpha)
+    assert t.f.sum() == 256 and t.f.min() >= 1
+    assert np.array_equal(t.c, np.concatenate([[0], np.cumsum(t.f)[:-1]]))
+    assert abs(t.prob.sum() - 1.0) < 1e-12
+    assert np.allclose(t.prob, t.prob[::-1], atol=1e-12)
+    # the model is symmetric; only the one frequency that absorbed the rounding
+    # shortfall may break the mirror
+    assert (t.f != t.f[::-1]).sum() <= 2
+    # sharpening never flattens: the central symbols are at least as likely
+    assert t.f[M // 2] >= t.f[0]
+    # fixed-point costs round -log2(f/256) up to 1/65536 of a bit
+    exact = (8.0 - np.log2(t.f)) * 65536.0
+    assert np.all(t.r >= exact - 1e-9) and np.all(t.r < exact + 1.0)
+
+
+def test_costs_of_power_of_two_frequencies_are_exact():
+    f = [128, 64, 32, 16, 8, 4, 2, 1, 1]
+    t = oracle.DqTable.from_freqs(f)
+    assert t.r.tolist() == [65536 * k for k in (1, 2, 3, 4, 5, 6, 7, 8, 8)]
+
+
+def test_paper_operating_point_bits_per_value():
+    # 331-byte keys (+ an INT8 mean of 1024 channels per 128 tokens) and 231-byte
+    # values, per 1024-value stream: 2.68 and 1.84 bits per value, 2.26 on average
+    n = 1024
+    # with fp16 (s, o) per stream: (331 + 4 + 8) * 8 / 1024 = 2.68, (231 + 4) * 8 / 1024 = 1.84
+    assert round((331 + 4 + n / 128) * 8 / n, 2) == 2.68
+    assert round((231 + 4) * 8 / n, 2) == 1.84
+    assert round(((331 + 4 + n / 128) + (231 + 4)) * 8 / (2 * n), 2) == 2.26
+
+
+def test_sixteen_levels_do_not_fit_2p26_bits():
+    # the cheapest 16-level symbol costs more than a 289-byte container allows
+    t = oracle.DqTable(1024, 16)
+    assert 1024 * t.r.min() > oracle.dq_budget_fx(289)
+    assert 1024 * t.r.min() <= oracle.dq_budget_fx(343)
+
+
+# ---- rANS container ---------------------------------------------------------
+
+def test_hand_worked_containers():
+    g = json.load(open(GOLDEN))
+    for case in g["cases"]:
+        t = oracle.DqTable.from_freqs(case["f"])
+        assert t.c.tolist() == case["c"]
+        m = np.array(case["symbols"], dtype=np.uint8)
+        cont, pushed = oracle.rans_encode(m, t, case["C"])
+        assert pushed == case["emitted"], case["name"]
+        assert cont.tolist() == case["container"], case["name"]
+        dm, xf, used = oracle.rans_decode(cont, m.size, t)
+        assert np.array_equal(dm, m) and xf == L_STATE and used == pushed
+
+
+def _random_table(g, M):
+    while True:
+        f = g.integers(1, 60, size=M)
+        f = np.maximum(1, np.round(f * 256 / f.sum())).astype(int)
+        f[np.argmax(f)] += 256 - f.sum()
+        if f.min() >= 1:
+            return oracle.DqTable.from_freqs(f)
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_round_trip_and_information_identity(seed):
+    g = np.random.default_rng(seed)
+    M = int(g.integers(2, 17))
+    t = _random_table(g, M)
+    n = int(g.integers(1, 700))
+    p = t.f / 256.0
+    m = g.choice(M, size=n, p=p).astype(np.uint8)
+    info = float(np.sum(-np.log2(t.f[m] / 256.0)))
+    C = 4 + int(info / 8) + 64
+    cont, pushed = oracle.rans_encode(m, t, C)
+    assert pushed >= 0
+    dm, xf, used = oracle.rans_decode(cont, n, t)
+    assert np.array_equal(dm, m)
+    assert xf == L_STATE and used == pushed          # the decoder ends where the encoder began
+    assert np.all(cont[4 + pushed:] == 0)
+    x_final = int(cont[0]) | int(cont[1]) << 8 | int(cont[2]) << 16 | int(cont[3]) << 24
+    bits = 8 * pushed + math.log2(x_final) - 23
+    # each step scales the state by 256/f within a factor (1 +- 2^-15)
+    assert abs(bits - info) <= n * math.log2(1 + 2.0 ** -15) + 1e-9
+
+
+def test_uniform_frequencies_cost_exactly_k_bits():
+    t = oracle.DqTable.from_freqs([64, 64, 64, 64])    # 2 bits per symbol
+    g = np.random.default_rng(3)
+    for n in (1, 3, 4, 13, 64):
+        m = g.integers(0, 4, size=n).astype(np.uint8)
+        cont, pushed = oracle.rans_encode(m, t, 64)
+        x_final = int.from_bytes(bytes(cont[:4]), "little")
+        assert 8 * pushed + math.log2(x_final) - 23 == pytest.approx(2 * n, abs=n * 1e-4)
+        # the state holds 23..31 bits, so 2n - 8 < 8 * bytes <= 2n
+        assert pushed == n // 4
+
+
+# ---- Drift ------------------------------------------------------------------
+
+def _grid(s, o, M):
+    return np.array([np.float32(o) + np.float32(s) * np.float32(m) for m in range(M)], dtype=np.float32)
+
+
+def _minmax(x, M):
+    lo, hi = np.float32(x.min()), np.float32(x.max())
+    return np.float32((hi - lo) / np.float32(M - 1)), lo
+
+
+@pytest.mark.parametrize("seed", range(5))
+def test_drift_is_optimal_for_its_own_rate_brute_force(seed):
+    g = np.random.default_rng(100 + seed)
+    n, M = 5, 4
+    t = oracle.DqTable(n, M, alpha=1.4)
+    x = g.standard_normal(n).astype(np.float32)
+    s, o = _minmax(x, M)
+    grid = _grid(s, o, M).astype(np.float64)
+    xs = x.astype(np.float64)
+    allm = np.array(list(itertools.product(range(M), repeat=n)))
+    dist = ((xs[None, :] - grid[allm]) ** 2).sum(1)
+    cost = t.r[allm].sum(1)
+    lo_b, hi_b = int(cost.min()), int(cost.max())
+    for budget in np.linspace(lo_b - 1000, hi_b + 1000, 25).astype(np.int64):
+        m, c, ok = oracle.dq_drift(x, s, o, t, budget_fx=int(budget))
+        assert c == int(t.r[m].sum())
+        if budget < lo_b:
+            assert not ok
+            continue
+        assert ok and c <= budget
+        d = float(((xs - grid[m]) ** 2).sum())
+        # no assignment that spends at most as many bits has lower distortion
+        better = dist[(cost <= c)].min()
+        assert d <= better + 1e-6 * max(1.0, better), (budget, d, better)
+
+
+def test_drift_distortion_falls_as_the_budget_grows():
+    g = np.random.default_rng(8)
+    t = oracle.DqTable(1024, 8)
+    x = g.standard_normal(1024).astype(np.float32)
+    s, o = _minmax(x, 8)
+    grid = _grid(s, o, 8).astype(np.float64)
+    prev = None
+    for C in range(200, 420, 10):
+        m, c, ok = oracle.dq_drift(x, s, o, t, C)
+        d = float(((x.astype(np.float64) - grid[m]) ** 2).sum())
+        if ok:
+            assert c <= oracle.dq_budget_fx(C)
+        if prev is not None:
+            assert d <= prev + 1e-9
+        prev = d
+
+
+def test_drift_is_nearest_rounding_when_that_fits():
+    g = np.random.default_rng(9)
+    t = oracle.DqTable(1024, 8)
+    x = g.standard_normal(1024).astype(np.float32)
+    s, o = _minmax(x, 8)
+    grid = _grid(s, o, 8)
+    near = np.argmin(np.abs(x[:, None] - grid[None, :]), axis=1)
+    assert int(t.r[near].sum()) <= oracle.dq_budget_fx(1000)
+    m, _, ok = oracle.dq_drift(x, s, o, t, 1000)
+    assert ok and np.array_equal(m, near)
+
+
+# ---- Refit ------------------------------------------------------------------
+
+def test_refit_recovers_an_exact_line():
+    g = np.random.default_rng(4)
+    m = g.integers(0, 8, size=1024).astype(np.uint8)
+    x = (np.float32(-1.5) + np.float32(0.25) * m.astype(np.float32)).astype(np.float32)
+    s, o = oracle.dq_refit(x, m, 9.0, 9.0)
+    assert s == 0.25 and o == -1.5
+
+
+def test_refit_is_least_squares():
+    g = np.random.default_rng(5)
+    x = g.standard_normal(1024).astype(np.float32)
+    m = np.clip(np.rint((x + 3) / 0.8), 0, 7).astype(np.uint8)
+    s, o = oracle.dq_refit(x, m, 0.0, 0.0)
+    A = np.stack([m.astype(np.float64), np.ones(1024)], 1)
+    ls, lo = np.linalg.lstsq(A, x.astype(np.float64), rcond=None)[0]
+    assert abs(s - ls) < 1e-5 and abs(o - lo) < 1e-5
+
+
+def test_refit_keeps_a_degenerate_fit():
+    x = np.random.default_rng(6).standard_normal(64).astype(np.float32)
+    m = np.full(64, 3, dtype=np.uint8)
+    assert oracle.dq_refit(x, m, 0.5, -0.25) == (0.5, -0.25)
+
+
+# ---- windowed INT8 key mean -------------------------------------------------
+
+def test_window_mean_exact_and_bounded():
+    g = np.random.default_rng(7)
+    n = 1024
+    mu = (g.integers(-64, 64, size=n) / 16.0).astype(np.float32)   # dyadic: sums are exact
+    y = np.repeat(mu[None, :], 128, 0)
+    q, sc16, mu_hat = oracle.dq_window_mean(y)
+    sc = float(np.array([sc16], dtype=np.uint16).view(np.float16)[0])
+    assert sc == float(np.float16(np.float32(np.abs(mu).max()) / np.float32(127)))
+    assert np.abs(q.astype(int)).max() == 127
+    assert np.all(np.abs(mu_hat.astype(np.float64) - mu) <= sc / 2 * (1 + 1e-3))
+    q0, s0, m0 = oracle.dq_window_mean(np.zeros((5, n), dtype=np.float32))
+    assert s0 == 0 and not q0.any() and not m0.any()
+
+
+# ---- Algorithm 1 end to end -------------------------------------------------
+
+@pytest.mark.parametrize("M,C", [(8, 331), (6, 231)])
+def test_streams_fill_their_containers_and_decode(M, C):
+    g = np.random.default_rng(M)
+    t = oracle.DqTable(1024, M)
+    F = oracle.dq_pow2_table()
+    changed = []
+    for _ in range(20):
+        x = g.standard_normal(1024).astype(np.float32)
+        r = oracle.dq_encode_stream(x, t, C, F)
+        assert r["flags"] == 0
+        m, xf, used = oracle.rans_decode(r["container"], 1024, t)
+        assert np.array_equal(m, r["m"]) and xf == L_STATE and 4 + used <= C
+        # drift only makes local corrections: no symbol moves more than one level
+        assert np.abs(r["m"].astype(int) - r["m_near"].astype(int)).max() <= 1
+        changed.append(np.mean(r["m"] != r["m_near"]))
+    assert np.mean(changed) < 0.2
+
+
+def test_key_streams_drift_less_than_value_streams():
+    g = np.random.default_rng(11)
+    F = oracle.dq_pow2_table()
+    fr = {}
+    for M, C in ((8, 331), (6, 231)):
+        t = oracle.DqTable(1024, M)
+        fr[M] = np.mean([np.mean((lambda r: r["m"] != r["m_near"])(
+            oracle.dq_encode_stream(g.standard_normal(1024).astype(np.float32), t, C, F))) for _ in range(20)])
+    assert fr[8] < fr[6]
+
+
+def test_constant_stream():
+    t = oracle.DqTable(1024, 8)
+    x = np.full(1024, 0.75, dtype=np.float32)
+    r = oracle.dq_encode_stream(x, t, 331)
+    assert r["flags"] == 0 and r["s16"] == 0
+    assert float(np.array([r["o16"]], dtype=np.uint16).view(np.float16)[0]) == 0.75
+    assert np.all(r["m"] == np.argmax(t.f))     # every value takes the cheapest symbol

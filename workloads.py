@@ -67,7 +67,9 @@ QWEN_LONG = Workload("qwen3-8b-long", 4, batch=4, n_kv_heads=8, n_q_heads=32, he
                      mean_k=False, clip=0.999, k_dist="cov")
 DQUANT = Workload("dquant-rans", 5, batch=32, n_kv_heads=8, n_q_heads=32, head_dim=128,
                   seq=16384, kv_dtype="bf16", scheme="rans", rot_k="hadamard", rot_v="none",
-                  n_recent=128)
+                  n_recent=128, meta_dtype="f16",
+                  extra={"levels_k": 8, "levels_v": 6, "container_k": 331, "container_v": 231,
+                         "alpha": 1.4, "mean_window": 128})
 
 WORKLOADS = {w.name: w for w in (TINY, LLAMA, NUQ, QWEN_LONG, DQUANT)}
 
