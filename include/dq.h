@@ -139,6 +139,24 @@ typedef struct {
  * NNZk = round_up(head_dim * kk, 8).  A code of an outlier element is its
  * nearest level like any other; attention replaces the table value by the
  * stored one.
+ *
+ * Entropy-coded scheme (DQ_RANS on both tensors; "D-Quant: Driftable Entropy
+ * Coding for KV Cache Quantization", Sec. 4.2-4.5 and App. A).  A stream is
+ * the n = n_kv_heads * head_dim values of one token's key (or value), KV heads
+ * in order; head_dim must be 128 and n_kv_heads 1, 2, 4 or 8.  Here
+ * Qcap = round_up(max_seq - n_sink, 128) and quantized slot p of sequence b:
+ * codes_k     [B][Qcap][Ck]    rANS containers of Ck = k.container_bytes:
+ *                              the final 32-bit state little endian, then the
+ *                              emitted bytes (last emitted first), then zeros
+ * codes_v     [B][Qcap][Cv]
+ * meta_k      [B][Qcap][2]     fp16 (s, o) of the stream's grid o + s m
+ * meta_v      [B][Qcap][2]
+ * mean_k      [B][Qcap/128][n + 16]  keys with mean = 1: per window of 128
+ *                              quantized slots, n INT8 channel means (stream
+ *                              order) and at byte n the fp16 scale; the mean
+ *                              is q * scale
+ * raw_k, raw_v as above; the other buffers are unused.  Symbols are coded with
+ * p = 8 bits of probability, state floor L = 2^23, one byte at a time.
  */
 typedef struct {
     void *codes_k, *codes_v, *meta_k, *meta_v, *mean_k;
@@ -170,7 +188,9 @@ dq_status dq_kv_sizes(const dq_config *cfg, size_t bytes[DQ_NUM_BUFFERS]);
  * The dense key transform reads bufs->k_transform.
  * DQ_NUQ is prefill only (pos0 == 0; appends give DQ_EUNSUPPORTED) and needs
  * max_seq - n_sink <= 8192: the key tables are fitted over every quantized
- * token of the prefill.
+ * token of the prefill.  DQ_RANS is prefill only as well (the windowed key
+ * mean is taken over each window's tokens); a stream whose cheapest coding
+ * still exceeds its container latches DQ_EINFEASIBLE (see dq_check).
  * Errors: DQ_EINVAL, DQ_EALIGN, DQ_EUNSUPPORTED, DQ_ENOMEM, DQ_ECUDA (launch).
  */
 dq_status dq_quantize_kv(dq_ctx **ctx, const dq_config *cfg, const dq_kv_buffers *bufs,
@@ -204,6 +224,19 @@ dq_status dq_decode_attention(dq_ctx **ctx, const dq_config *cfg, const dq_kv_bu
  */
 dq_status dq_dequantize_kv(dq_ctx **ctx, const dq_config *cfg, const dq_kv_buffers *bufs,
                            int which, long long slot0, long long n, float *out, void *stream);
+
+/*
+ * The symbol model of an entropy-coded (DQ_RANS) tensor: which = 0 keys,
+ * 1 values.  Writes its number of levels M and the frequencies f[0..M) and
+ * cumulative starts c[0..M) (f sums to 2^8; entries past M are 0).  Host only.
+ * D-Quant Sec. 4.2 (the model comes from Gaussian order statistics: levels on
+ * -a + 2a m/(M-1) with a the expected maximum of n standard normals, each
+ * with the normal mass of its bin) and Sec. 4.4 (sharpening p' ~ p^alpha);
+ * f_m = max(1, round(256 p'_m)) with the rounding shortfall given to the
+ * largest frequency.
+ * Errors: DQ_EINVAL, DQ_EUNSUPPORTED, DQ_EINFEASIBLE (as dq_kv_sizes).
+ */
+dq_status dq_rans_model(const dq_config *cfg, int which, int *levels, int f[16], int c[16]);
 
 /*
  * Synchronize `stream`, then return and clear the device-side status latched

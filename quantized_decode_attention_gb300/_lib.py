@@ -82,10 +82,22 @@ def load() -> C.CDLL:
     L.dq_last_error.restype = C.c_char_p
     L.dq_status_name.restype = C.c_char_p
     L.dq_status_name.argtypes = [C.c_int]
-    for f in ("dq_kv_sizes", "dq_quantize_kv", "dq_decode_attention", "dq_dequantize_kv", "dq_check"):
+    L.dq_rans_model.argtypes = [C.POINTER(Config), C.c_int, C.POINTER(C.c_int), C.POINTER(C.c_int),
+                                C.POINTER(C.c_int)]
+    for f in ("dq_kv_sizes", "dq_quantize_kv", "dq_decode_attention", "dq_dequantize_kv", "dq_check",
+              "dq_rans_model"):
         getattr(L, f).restype = C.c_int
     _lib = L
     return L
+
+
+def rans_model(cfg: Config, which: int):
+    """(f, c) of the symbol model of keys (which=0) or values (which=1)."""
+    M = C.c_int(0)
+    f = (C.c_int * 16)()
+    c = (C.c_int * 16)()
+    _raise(load().dq_rans_model(C.byref(cfg), which, C.byref(M), f, c))
+    return list(f[:M.value]), list(c[:M.value])
 
 
 def _raise(st: int):
@@ -96,7 +108,8 @@ def _raise(st: int):
 def make_config(*, batch, n_kv_heads, n_q_heads, head_dim, max_seq, kv_dtype="bf16", meta_dtype="f16",
                 out_dtype="bf16", bits=2, bits_v=None, rot_k="hadamard", rot_v="hadamard", mean_k=True,
                 clip_k=0.0, clip_v=None, n_sink=0, n_recent=0, scheme="affine", lloyd_iters=8,
-                outlier_frac=0.01) -> Config:
+                outlier_frac=0.01, levels_k=8, levels_v=6, container_k=331, container_v=231,
+                rans_alpha=1.4) -> Config:
     c = Config()
     c.batch, c.n_kv_heads, c.n_q_heads, c.head_dim, c.max_seq = batch, n_kv_heads, n_q_heads, head_dim, max_seq
     c.kv_dtype, c.meta_dtype, c.out_dtype = DTYPES[kv_dtype], DTYPES[meta_dtype], DTYPES[out_dtype]
@@ -110,7 +123,10 @@ def make_config(*, batch, n_kv_heads, n_q_heads, head_dim, max_seq, kv_dtype="bf
     if scheme == "nuq":
         c.k.lloyd_iters = c.v.lloyd_iters = lloyd_iters
         c.k.outlier_frac = c.v.outlier_frac = outlier_frac
-    c.rans_alpha, c.rans_prob_bits = 1.4, 8
+    c.rans_alpha, c.rans_prob_bits = rans_alpha, 8
+    if scheme == "rans":
+        c.k.levels, c.v.levels = levels_k, levels_v
+        c.k.container_bytes, c.v.container_bytes = container_k, container_v
     return c
 
 

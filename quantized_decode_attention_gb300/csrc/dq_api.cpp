@@ -8,6 +8,7 @@
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
+#include <mutex>
 #include <new>
 
 #include "dq.h"
@@ -35,8 +36,19 @@ long long round_up(long long x, long long m) { return (x + m - 1) / m * m; }
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 dq_status validate_tensor(const dq_tensor_cfg &t, int d, bool key, const char *name) {
-    if (t.scheme != DQ_AFFINE && t.scheme != DQ_NUQ)
-        return fail(DQ_EUNSUPPORTED, "%s: only the affine and non-uniform schemes are built", name);
+    if (t.scheme != DQ_AFFINE && t.scheme != DQ_NUQ && t.scheme != DQ_RANS)
+        return fail(DQ_EINVAL, "%s: unknown scheme %d", name, t.scheme);
+    if (t.scheme == DQ_RANS) {
+        if (t.levels < 2 || t.levels > dq::RANS_MAX_LEVELS)
+            return fail(DQ_EINVAL, "%s: levels must be in [2, %d] (got %d)", name, dq::RANS_MAX_LEVELS, t.levels);
+        if (t.container_bytes < 8 || t.container_bytes > 4096)
+            return fail(DQ_EINVAL, "%s: container_bytes must be in [8, 4096]", name);
+        if (t.rot != DQ_ROT_NONE && t.rot != DQ_ROT_HADAMARD)
+            return fail(DQ_EUNSUPPORTED, "%s: the entropy-coded scheme takes no rotation or a Hadamard one", name);
+        if (t.clip != 0.0f) return fail(DQ_EUNSUPPORTED, "%s: the entropy-coded scheme takes no clip", name);
+        if (!key && t.mean) return fail(DQ_EINVAL, "%s: channel mean removal is for keys", name);
+        return DQ_OK;
+    }
     if (t.bits < 2 || t.bits > 4) return fail(DQ_EINVAL, "%s: bits must be 2, 3 or 4 (got %d)", name, t.bits);
     if (t.scheme == DQ_NUQ) {
         if (t.rot != DQ_ROT_NONE || t.mean || t.clip != 0.0f)
@@ -52,6 +64,39 @@ dq_status validate_tensor(const dq_tensor_cfg &t, int d, bool key, const char *n
     if (!(t.clip == 0.0f || (t.clip > 0.5f && t.clip < 1.0f)))
         return fail(DQ_EINVAL, "%s: clip must be 0 or in (0.5, 1)", name);
     return DQ_OK;
+}
+
+// Symbol models are a few milliseconds of host arithmetic; keep the last few.
+struct TableCacheEntry {
+    int n, M, C, p;
+    float alpha;
+    int rc;
+    dq::RansTable t;
+};
+std::mutex g_table_mu;
+TableCacheEntry g_tables[8];
+int g_tables_n = 0, g_tables_next = 0;
+
+int cached_table(int n, int M, float alpha, int p, int C, dq::RansTable *out) {
+    std::lock_guard<std::mutex> lk(g_table_mu);
+    for (int i = 0; i < g_tables_n; i++) {
+        const TableCacheEntry &e = g_tables[i];
+        if (e.n == n && e.M == M && e.C == C && e.p == p && e.alpha == alpha) {
+            *out = e.t;
+            return e.rc;
+        }
+    }
+    TableCacheEntry &e = g_tables[g_tables_next];
+    g_tables_next = (g_tables_next + 1) % 8;
+    if (g_tables_n < 8) g_tables_n++;
+    e.n = n;
+    e.M = M;
+    e.C = C;
+    e.p = p;
+    e.alpha = alpha;
+    e.rc = dq::rans_build_table(n, M, alpha, p, C, &e.t);
+    *out = e.t;
+    return e.rc;
 }
 
 }  // namespace
@@ -97,8 +142,17 @@ dq_status make_layout(const dq_config *cfg, Layout *L) {
     dq_status s;
     if ((s = validate_tensor(c.k, c.head_dim, true, "k")) != DQ_OK) return s;
     if ((s = validate_tensor(c.v, c.head_dim, false, "v")) != DQ_OK) return s;
-    if (c.k.bits != c.v.bits) return fail(DQ_EUNSUPPORTED, "keys and values must use the same code width");
     if (c.k.scheme != c.v.scheme) return fail(DQ_EUNSUPPORTED, "keys and values must use the same scheme");
+    if (c.k.scheme != DQ_RANS && c.k.bits != c.v.bits)
+        return fail(DQ_EUNSUPPORTED, "keys and values must use the same code width");
+    if (c.k.scheme == DQ_RANS) {
+        if (c.head_dim != 128) return fail(DQ_EUNSUPPORTED, "entropy-coded scheme: head_dim must be 128");
+        if (c.n_kv_heads != 1 && c.n_kv_heads != 2 && c.n_kv_heads != 4 && c.n_kv_heads != 8)
+            return fail(DQ_EUNSUPPORTED, "entropy-coded scheme: 1, 2, 4 or 8 KV heads per stream");
+        if (c.meta_dtype != DQ_F16) return fail(DQ_EINVAL, "entropy-coded scheme: metadata is fp16");
+        if (c.rans_prob_bits != 8) return fail(DQ_EUNSUPPORTED, "entropy-coded scheme: prob_bits must be 8");
+        if (!(c.rans_alpha > 0.0f && c.rans_alpha <= 8.0f)) return fail(DQ_EINVAL, "rans_alpha outside (0, 8]");
+    }
     if (c.k.scheme == DQ_NUQ && c.max_seq - c.n_sink > 8192)
         return fail(DQ_EUNSUPPORTED, "non-uniform key fit: at most 8192 quantized tokens (got %d)",
                     c.max_seq - c.n_sink);
@@ -115,7 +169,7 @@ dq_status make_layout(const dq_config *cfg, Layout *L) {
     l.bits_v = c.v.bits;
     l.rowK = c.head_dim * c.k.bits / 8;
     l.pairV = 2 * c.head_dim * c.v.bits / 8;
-    l.qcap = round_up(c.max_seq - c.n_sink, 64);
+    l.qcap = round_up(c.max_seq - c.n_sink, c.k.scheme == DQ_RANS ? 128 : 64);
     l.rcap = static_cast<int>(round_up(c.n_sink + c.n_recent, 16));
     l.meta_bytes = c.meta_dtype == DQ_F16 ? 2 : 4;
     l.n_sink = c.n_sink;
@@ -151,6 +205,34 @@ dq_status make_layout(const dq_config *cfg, Layout *L) {
     }
     l.sz[15] = c.k.rot == DQ_ROT_DENSE ? static_cast<size_t>(c.n_kv_heads) * d * d * 4 : 0;  // k_transform
     l.sz[16] = l.sz[15];                                    // q_comp
+    if (c.k.scheme == DQ_RANS) {
+        l.n_stream = c.n_kv_heads * c.head_dim;
+        l.ck = c.k.container_bytes;
+        l.cv = c.v.container_bytes;
+        l.mk = c.k.levels;
+        l.mv = c.v.levels;
+        l.wcap = l.qcap / 128;
+        l.mean_rec = l.n_stream + 16;
+        const size_t B = static_cast<size_t>(c.batch);
+        for (int i = 0; i < DQ_NUM_BUFFERS; i++) l.sz[i] = 0;
+        l.sz[0] = B * l.qcap * l.ck;                        // codes_k: containers
+        l.sz[1] = B * l.qcap * l.cv;                        // codes_v
+        l.sz[2] = B * l.qcap * 4;                           // meta_k: (s, o) fp16
+        l.sz[3] = B * l.qcap * 4;                           // meta_v
+        l.sz[4] = c.k.mean ? B * l.wcap * l.mean_rec : 0;   // mean_k: INT8 window means + scale
+        l.sz[7] = U * l.rcap * d * 2;                       // raw_k
+        l.sz[8] = U * l.rcap * d * 2;                       // raw_v
+        RansTable tk, tv;
+        if (cached_table(l.n_stream, l.mk, c.rans_alpha, c.rans_prob_bits, l.ck, &tk) != 0 ||
+            cached_table(l.n_stream, l.mv, c.rans_alpha, c.rans_prob_bits, l.cv, &tv) != 0)
+            return fail(DQ_EINVAL, "entropy-coded scheme: no valid symbol model for these levels");
+        if (tk.min_stream_cost > tk.budget_fx)
+            return fail(DQ_EINFEASIBLE, "k: %d levels cannot fit a %d-byte container (cheapest stream %.1f bits)",
+                        l.mk, l.ck, tk.min_stream_cost / 65536.0);
+        if (tv.min_stream_cost > tv.budget_fx)
+            return fail(DQ_EINFEASIBLE, "v: %d levels cannot fit a %d-byte container (cheapest stream %.1f bits)",
+                        l.mv, l.cv, tv.min_stream_cost / 65536.0);
+    }
     return DQ_OK;
 }
 
@@ -203,14 +285,30 @@ static dq_status get_ctx(dq_ctx **pctx, const dq_config *cfg, const Layout &L) {
     cudaError_t e4 = cudaSuccess;
     if (L.scheme == DQ_NUQ)
         e4 = cudaMalloc(&c->nuq_bits, static_cast<size_t>(L.U) * L.qcap * (L.d / 32) * sizeof(uint32_t));
+    if (L.scheme == DQ_RANS) e4 = cudaMalloc(&c->rans, sizeof(dq::RansDevTables));
     if (e1 != cudaSuccess || e2 != cudaSuccess || e3 != cudaSuccess || e4 != cudaSuccess) {
         cudaFree(c->status);
         cudaFree(c->partials);
         cudaFree(c->counters);
         cudaFree(c->nuq_bits);
+        cudaFree(c->rans);
         delete c;
         cudaGetLastError();
         return fail(DQ_ENOMEM, "workspace allocation failed");
+    }
+    if (L.scheme == DQ_RANS) {
+        dq::RansDevTables h;
+        std::memset(&h, 0, sizeof h);
+        if (cached_table(L.n_stream, L.mk, cfg->rans_alpha, cfg->rans_prob_bits, L.ck, &h.k) != 0 ||
+            cached_table(L.n_stream, L.mv, cfg->rans_alpha, cfg->rans_prob_bits, L.cv, &h.v) != 0) {
+            dq_free(c);
+            return fail(DQ_EINVAL, "entropy-coded scheme: no valid symbol model");
+        }
+        dq::rans_pow2_table(h.F);
+        if (cudaMemcpy(c->rans, &h, sizeof h, cudaMemcpyHostToDevice) != cudaSuccess) {
+            dq_free(c);
+            return fail(DQ_ECUDA, "symbol model upload failed");
+        }
     }
     if (cudaMemset(c->status, 0, sizeof(unsigned)) != cudaSuccess ||
         cudaMemset(c->counters, 0, sizeof(int) * L.U) != cudaSuccess) {
@@ -274,9 +372,85 @@ static dq_status quantize_nuq(dq_ctx *c, const dq_config *cfg, const Layout &L, 
     return ok();
 }
 
+// Entropy-coded scheme, prefill only ("D-Quant" page, Sec. 4.2: the keys'
+// windowed mean needs its window's tokens; decode-time block flushes from the
+// recent window are not built).
+static dq_status quantize_rans(dq_ctx *c, const dq_config *cfg, const Layout &L, const dq_kv_buffers *bufs,
+                               const void *k, const void *v, long long pos0, long long n_tok, void *stream) {
+    if (pos0 != 0)
+        return fail(DQ_EUNSUPPORTED, "entropy-coded scheme: only a prefill from position 0 is built (no appends)");
+    dq::RansQuantArgs a{};
+    a.in_dtype = cfg->kv_dtype;
+    a.B = L.B;
+    a.Hkv = L.Hkv;
+    a.n = L.n_stream;
+    a.n_tok = n_tok;
+    a.n_sink = L.n_sink;
+    a.n_recent = L.n_recent;
+    a.n_fit = static_cast<int>(n_tok > L.n_sink ? n_tok - L.n_sink : 0);
+    a.hscale = static_cast<float>(1.0 / std::sqrt(128.0));
+    a.n_win = (a.n_fit + 127) / 128;
+    a.qcap = L.qcap;
+    a.wcap = L.wcap;
+    a.rcap = L.rcap;
+    a.mean_rec = L.mean_rec;
+    a.status = c->status;
+    const size_t need = static_cast<size_t>(L.B) * a.n_fit * L.n_stream;
+    if (need > c->rans_sym_cap) {
+        cudaFree(c->rans_sym);
+        c->rans_sym = nullptr;
+        c->rans_sym_cap = 0;
+        if (cudaMalloc(&c->rans_sym, need) != cudaSuccess) {
+            cudaGetLastError();
+            return fail(DQ_ENOMEM, "symbol scratch of %zu bytes", need);
+        }
+        c->rans_sym_cap = need;
+    }
+    a.sym = c->rans_sym;
+    int e;
+    for (int which = 0; which < 2; which++) {
+        const dq_tensor_cfg &t = which == 0 ? cfg->k : cfg->v;
+        a.x = which == 0 ? k : v;
+        a.is_key = which == 0;
+        a.rot = t.rot == DQ_ROT_HADAMARD;
+        a.raw = static_cast<uint16_t *>(which == 0 ? bufs->raw_k : bufs->raw_v);
+        a.codes = static_cast<uint8_t *>(which == 0 ? bufs->codes_k : bufs->codes_v);
+        a.meta = which == 0 ? bufs->meta_k : bufs->meta_v;
+        a.mean = which == 0 && t.mean ? static_cast<uint8_t *>(bufs->mean_k) : nullptr;
+        const dq::RansTable *tb = which == 0 ? &c->rans->k : &c->rans->v;
+        if ((e = dq::launch_rans_raw(a, stream)) != 0)
+            return fail(DQ_ECUDA, "raw copy launch: %s", cudaGetErrorString(static_cast<cudaError_t>(e)));
+        if (a.mean && (e = dq::launch_rans_mean(a, stream)) != 0)
+            return fail(DQ_ECUDA, "window mean launch: %s", cudaGetErrorString(static_cast<cudaError_t>(e)));
+        if ((e = dq::launch_rans_drift(a, tb, c->rans->F, t.levels, stream)) != 0)
+            return fail(DQ_ECUDA, "drift launch: %s", cudaGetErrorString(static_cast<cudaError_t>(e)));
+        if ((e = dq::launch_rans_encode(a, tb, t.container_bytes, stream)) != 0)
+            return fail(DQ_ECUDA, "rANS encode launch: %s", cudaGetErrorString(static_cast<cudaError_t>(e)));
+    }
+    return ok();
+}
+
 extern "C" {
 
 const char *dq_last_error(void) { return g_err; }
+
+dq_status dq_rans_model(const dq_config *cfg, int which, int *levels, int f[16], int c[16]) {
+    if (!cfg || !levels || !f || !c || (which != 0 && which != 1)) return fail(DQ_EINVAL, "bad argument");
+    Layout L;
+    dq_status s = dq::make_layout(cfg, &L);
+    if (s != DQ_OK) return s;
+    if (L.scheme != DQ_RANS) return fail(DQ_EINVAL, "not an entropy-coded config");
+    dq::RansTable t;
+    if (cached_table(L.n_stream, which == 0 ? L.mk : L.mv, cfg->rans_alpha, cfg->rans_prob_bits,
+                     which == 0 ? L.ck : L.cv, &t) != 0)
+        return fail(DQ_EINVAL, "no valid symbol model");
+    *levels = t.M;
+    for (int m = 0; m < 16; m++) {
+        f[m] = m < t.M ? t.f[m] : 0;
+        c[m] = m < t.M ? t.c[m] : 0;
+    }
+    return ok();
+}
 
 const char *dq_status_name(dq_status s) {
     switch (s) {
@@ -314,6 +488,7 @@ dq_status dq_quantize_kv(dq_ctx **ctx, const dq_config *cfg, const dq_kv_buffers
     if (!aligned16(k) || !aligned16(v)) return fail(DQ_EALIGN, "k / v input not 16-byte aligned");
     if ((s = get_ctx(ctx, cfg, L)) != DQ_OK) return s;
     if (L.scheme == DQ_NUQ) return quantize_nuq(*ctx, cfg, L, bufs, k, v, pos0, n_tok, stream);
+    if (L.scheme == DQ_RANS) return quantize_rans(*ctx, cfg, L, bufs, k, v, pos0, n_tok, stream);
 
     for (int which = 0; which < 2; which++) {
         const dq_tensor_cfg &t = which == 0 ? cfg->k : cfg->v;
@@ -367,6 +542,7 @@ dq_status dq_decode_attention(dq_ctx **ctx, const dq_config *cfg, const dq_kv_bu
     if (!aligned16(q) || !aligned16(out)) return fail(DQ_EALIGN, "q / out not 16-byte aligned");
     if ((s = get_ctx(ctx, cfg, L)) != DQ_OK) return s;
     dq_ctx *c = *ctx;
+    if (L.scheme == DQ_RANS) return fail(DQ_EUNSUPPORTED, "entropy-coded attention is not built yet");
 
     dq::AttnArgs a{};
     a.q = static_cast<const float *>(q);
@@ -418,6 +594,7 @@ dq_status dq_dequantize_kv(dq_ctx **ctx, const dq_config *cfg, const dq_kv_buffe
     if (!aligned16(out)) return fail(DQ_EALIGN, "out not 16-byte aligned");
     if ((s = get_ctx(ctx, cfg, L)) != DQ_OK) return s;
     if (L.scheme == DQ_NUQ) return fail(DQ_EUNSUPPORTED, "non-uniform scheme: use the tables and side channel");
+    if (L.scheme == DQ_RANS) return fail(DQ_EUNSUPPORTED, "entropy-coded scheme: decode the containers");
     dq::DequantArgs a{};
     a.codes = static_cast<const uint8_t *>(which == 0 ? bufs->codes_k : bufs->codes_v);
     a.meta = which == 0 ? bufs->meta_k : bufs->meta_v;
@@ -442,6 +619,7 @@ dq_status dq_check(dq_ctx *ctx, void *stream) {
         return fail(DQ_ECUDA, "status read failed");
     if (st && cudaMemset(ctx->status, 0, sizeof st) != cudaSuccess) return fail(DQ_ECUDA, "status clear failed");
     if (st & dq::ST_TIMEOUT) return fail(DQ_ETIMEOUT, "a bounded device wait ran out");
+    if (st & dq::ST_INFEASIBLE) return fail(DQ_EINFEASIBLE, "a stream did not fit its container");
     if (st & dq::ST_NONFINITE) return fail(DQ_ENONFINITE, "non-finite K/V input");
     return ok();
 }
@@ -452,6 +630,8 @@ void dq_free(dq_ctx *ctx) {
     cudaFree(ctx->partials);
     cudaFree(ctx->counters);
     cudaFree(ctx->nuq_bits);
+    cudaFree(ctx->rans);
+    cudaFree(ctx->rans_sym);
     delete ctx;
 }
 

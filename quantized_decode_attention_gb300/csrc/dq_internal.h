@@ -9,7 +9,7 @@
 namespace dq {
 
 // Status bits latched on the device (ctx->status word).
-enum : unsigned { ST_NONFINITE = 1u, ST_TIMEOUT = 2u, ST_BOUNDS = 4u };
+enum : unsigned { ST_NONFINITE = 1u, ST_TIMEOUT = 2u, ST_BOUNDS = 4u, ST_INFEASIBLE = 8u };
 
 // Sizes and strides derived from a config (all in bytes unless noted).
 struct Layout {
@@ -29,8 +29,60 @@ struct Layout {
     long long nnzk_cap;  // key side-channel entries per unit (multiple of 8)
     int k_out_v;         // value outliers per token
     long long rp_stride; // ints per unit of the key row pointers (qcap + 4)
+    // entropy-coded scheme (scheme == DQ_RANS): one stream per token and tensor
+    int n_stream;        // values per stream = Hkv * d
+    int ck, cv;          // container bytes of a key / value stream
+    int mk, mv;          // levels of the key / value grid
+    long long wcap;      // mean windows per sequence (qcap / 128)
+    int mean_rec;        // bytes per window record: n_stream INT8 + fp16 scale, padded to 16
     size_t sz[DQ_NUM_BUFFERS];
 };
+
+// Entropy-coded scheme: the symbol model of one tensor (host-built, copied to
+// the device context).  dec[z] = m | f_m << 4 | (z - c_m) << 16 for the 2^8
+// slots z of the decoder.
+constexpr int RANS_MAX_LEVELS = 16;
+struct RansTable {
+    int M, C;
+    int f[RANS_MAX_LEVELS], c[RANS_MAX_LEVELS];
+    long long r[RANS_MAX_LEVELS];            // costs, 16 fractional bits, rounded up
+    float rf[RANS_MAX_LEVELS];               // r / 2^16 (exact)
+    unsigned long long rcp[RANS_MAX_LEVELS]; // ceil(2^40 / f): x / f = (x * rcp) >> 40 for x < 2^31
+    uint32_t dec[256];
+    long long budget_fx;                     // (8C - 32) * 2^16
+    long long min_stream_cost;               // n * min r
+};
+struct RansDevTables {
+    RansTable k, v;
+    float F[512];                            // fp32(2^(k/512))
+};
+int rans_build_table(int n, int M, double alpha, int prob_bits, int C, RansTable *t);
+void rans_pow2_table(float *F);
+
+// Per-launch arguments of the entropy-coded prefill kernels.
+struct RansQuantArgs {
+    const void *x;          // [B][Hkv][n_tok][128] input
+    int in_dtype;
+    int B, Hkv, n;          // n = Hkv * 128
+    long long n_tok;        // prefill length
+    int n_sink, n_recent;
+    int n_fit;              // quantized tokens n_tok - n_sink
+    int is_key, rot;
+    float hscale;
+    int n_win;              // mean windows covering the quantized tokens
+    long long qcap, wcap;
+    int rcap, mean_rec;
+    uint8_t *mean;          // [B][wcap][mean_rec] or nullptr
+    uint8_t *sym;           // scratch [B][n_fit][n] symbols
+    uint8_t *codes;         // [B][qcap][C] containers
+    void *meta;             // [B][qcap] (s, o) fp16
+    uint16_t *raw;          // [U][rcap][128] or [U][rcap/2][128][2]
+    unsigned *status;
+};
+int launch_rans_mean(const RansQuantArgs &a, void *stream);
+int launch_rans_drift(const RansQuantArgs &a, const RansTable *tb, const float *F, int M, void *stream);
+int launch_rans_encode(const RansQuantArgs &a, const RansTable *tb, int C, void *stream);
+int launch_rans_raw(const RansQuantArgs &a, void *stream);
 
 dq_status make_layout(const dq_config *cfg, Layout *L);
 
@@ -145,4 +197,7 @@ struct dq_ctx {
     size_t partials_cap; // floats
     int *counters;       // [U]
     uint32_t *nuq_bits;  // non-uniform scheme: key outlier bitmap scratch [U][Qcap][d/32]
+    dq::RansDevTables *rans;  // entropy-coded scheme: symbol models (device)
+    uint8_t *rans_sym;   // entropy-coded scheme: symbol scratch of a prefill
+    size_t rans_sym_cap; // bytes
 };

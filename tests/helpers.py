@@ -14,7 +14,10 @@ def cfg_for(w: W.Workload, max_seq: int | None = None, out_dtype: str | None = N
                        out_dtype=out_dtype or w.out_dtype, bits=w.bits, rot_k=w.rot_k, rot_v=w.rot_v,
                        mean_k=w.mean_k, clip_k=w.clip, clip_v=w.clip, n_sink=w.n_sink, n_recent=w.n_recent,
                        scheme=w.scheme, lloyd_iters=w.extra.get("lloyd_iters", 8),
-                       outlier_frac=w.extra.get("outlier_frac", 0.01))
+                       outlier_frac=w.extra.get("outlier_frac", 0.01),
+                       levels_k=w.extra.get("levels_k", 8), levels_v=w.extra.get("levels_v", 6),
+                       container_k=w.extra.get("container_k", 331), container_v=w.extra.get("container_v", 231),
+                       rans_alpha=w.extra.get("alpha", 1.4))
 
 
 def to_device(arr: np.ndarray, dtype: str):
@@ -104,4 +107,27 @@ def nuq_views(w: W.Workload, cache, S: int):
         v["raw_k"] = t["raw_k"].view(np.uint16).reshape(B, H, rcap, d)
         v["raw_v"] = t["raw_v"].view(np.uint16).reshape(B, H, rcap // 2, d, 2)
     assert sizes["meta_k"] == 0 and sizes["mean_k"] == 0
+    return v, qcap
+
+
+def dquant_views(w: W.Workload, cache, S: int):
+    """Reshape an entropy-coded cache's byte buffers into [B, ...] numpy views."""
+    B, H, d = w.batch, w.n_kv_heads, w.head_dim
+    n = H * d
+    qcap = -(-(S - w.n_sink) // 128) * 128
+    rcap = -(-(w.n_sink + w.n_recent) // 16) * 16
+    t = {nm: (x.cpu().numpy() if x is not None else None) for nm, x in cache.tensors.items()}
+    v = {
+        "codes_k": t["codes_k"].reshape(B, qcap, w.extra["container_k"]),
+        "codes_v": t["codes_v"].reshape(B, qcap, w.extra["container_v"]),
+        "meta_k": t["meta_k"].view(np.uint16).reshape(B, qcap, 2),
+        "meta_v": t["meta_v"].view(np.uint16).reshape(B, qcap, 2),
+    }
+    if t["mean_k"] is not None:
+        rec = t["mean_k"].reshape(B, qcap // 128, n + 16)
+        v["mean_q"] = rec[:, :, :n].view(np.int8)
+        v["mean_sc"] = np.ascontiguousarray(rec[:, :, n:n + 2]).view(np.uint16)[..., 0]
+    if rcap:
+        v["raw_k"] = t["raw_k"].view(np.uint16).reshape(B, H, rcap, d)
+        v["raw_v"] = t["raw_v"].view(np.uint16).reshape(B, H, rcap // 2, d, 2)
     return v, qcap

@@ -87,3 +87,54 @@ def test_validation_errors_without_gpu(lib):
     lib.dq_free(None)
     assert lib.dq_check(None, None) == 0
     assert lib.dq_status_name(7) == b"DQ_ENONFINITE"
+
+
+def _dquant(**kw):
+    from quantized_decode_attention_gb300 import make_config
+    args = dict(batch=32, n_kv_heads=8, n_q_heads=32, head_dim=128, max_seq=16384, scheme="rans",
+                rot_k="hadamard", rot_v="none", mean_k=True, n_recent=128, levels_k=8, levels_v=6,
+                container_k=331, container_v=231)
+    args.update(kw)
+    return make_config(**args)
+
+
+def test_sizes_dquant_layout(lib):
+    """D-Quant Sec. 5.1: 331- and 231-byte containers per 1024-value stream with fp16
+    (s, o) and an INT8 window mean are 2.68 + 1.84 = 2.26 bits per value on average."""
+    from quantized_decode_attention_gb300 import kv_sizes
+    s = kv_sizes(_dquant())
+    B, qcap, n = 32, 16384, 1024
+    assert s["codes_k"] == B * qcap * 331 and s["codes_v"] == B * qcap * 231
+    assert s["meta_k"] == s["meta_v"] == B * qcap * 4
+    assert s["mean_k"] == B * (qcap // 128) * (n + 16)
+    assert s["lut_k"] == 0 and s["ol_col_k"] == 0
+    bpv = (s["codes_k"] + s["codes_v"] + s["meta_k"] + s["meta_v"] + s["mean_k"]) * 8 / (2 * B * qcap * n)
+    assert bpv == pytest.approx(2.26, abs=0.005)
+
+
+def test_dquant_model_matches_the_oracle(lib):
+    import oracle
+    from quantized_decode_attention_gb300._lib import rans_model
+    for H, Mk, Mv, Ck, Cv in ((8, 8, 6, 331, 231), (2, 16, 4, 172, 100), (1, 3, 2, 60, 40)):
+        cfg = _dquant(n_kv_heads=H, n_q_heads=4 * H, levels_k=Mk, levels_v=Mv, container_k=Ck, container_v=Cv)
+        for which, M in ((0, Mk), (1, Mv)):
+            f, c = rans_model(cfg, which)
+            t = oracle.DqTable(H * 128, M, alpha=1.4)
+            assert f == t.f.tolist() and c == t.c.tolist(), (H, M)
+
+
+def test_dquant_infeasible_container_is_refused(lib):
+    """16 levels at 2.26 bits per value cannot fit: the cheapest symbol costs more."""
+    from quantized_decode_attention_gb300 import DQError, kv_sizes
+    with pytest.raises(DQError) as e:
+        kv_sizes(_dquant(levels_k=16, container_k=289))
+    assert e.value.status == 4   # DQ_EINFEASIBLE
+    kv_sizes(_dquant(levels_k=16, container_k=343))
+
+
+def test_dquant_validation(lib):
+    from quantized_decode_attention_gb300 import DQError, kv_sizes
+    for bad in (dict(head_dim=64), dict(n_kv_heads=3, n_q_heads=12), dict(levels_k=17), dict(container_v=4),
+                dict(meta_dtype="f32"), dict(rot_k="dense")):
+        with pytest.raises(DQError):
+            kv_sizes(_dquant(**bad))

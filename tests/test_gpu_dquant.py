@@ -1,0 +1,87 @@
+"""GPU parity of the D-Quant entropy-coded scheme against the oracle.
+
+"D-Quant: Driftable Entropy Coding for KV Cache Quantization": one stream per
+token and tensor over all KV heads, Hadamard-rotated keys with a windowed INT8
+channel mean, Drift under the container budget, fp16 (s, o), rANS containers
+of fixed size (Sec. 4.2-4.5, App. A).  Containers, metadata, window means and
+16-bit regions must match the oracle bit for bit.
+"""
+import numpy as np
+import pytest
+
+import workloads as W
+from oracle import cache as OC
+
+from helpers import cfg_for, dquant_views, to_device
+
+pytestmark = pytest.mark.gpu
+
+
+def dq(**kw):
+    extra = dict(W.DQUANT.extra)
+    extra.update(kw.pop("extra", {}))
+    return W.DQUANT.with_(extra=extra, **kw)
+
+
+CASES = {
+    # 2 KV heads (256-value streams), containers scaled from the paper's 331/231 bytes per 1024 values
+    "dq-h2": dq(batch=2, n_kv_heads=2, n_q_heads=8, seq=300, n_recent=16,
+                extra={"container_k": 83, "container_v": 58}),
+    # the paper's operating point: 8 KV heads, 8/6 levels in 331/231-byte containers
+    "dq-h8-paper": dq(batch=1, n_kv_heads=8, n_q_heads=32, seq=200, n_recent=16),
+    # 16 key levels, 4 value levels, sinks and a short recent window, ragged last window
+    "dq-h4-m16-sinks": dq(batch=1, n_kv_heads=4, n_q_heads=16, seq=260, n_sink=2, n_recent=8,
+                          extra={"levels_k": 16, "container_k": 172, "levels_v": 4, "container_v": 100}),
+    # one KV head, no key mean, rotated values, fp16 input
+    "dq-h1-nomean": dq(batch=2, n_kv_heads=1, n_q_heads=4, seq=150, n_recent=0, mean_k=False, rot_v="hadamard",
+                       kv_dtype="f16", extra={"container_k": 42, "container_v": 30}),
+}
+
+
+def _quantize(w):
+    import torch
+    from quantized_decode_attention_gb300 import KVCache
+    k, v = W.make_kv(w)
+    cache = KVCache.allocate(cfg_for(w))
+    cache.quantize(to_device(k, w.kv_dtype), to_device(v, w.kv_dtype))
+    torch.cuda.synchronize()
+    cache.check()
+    return cache, k, v
+
+
+@pytest.mark.parametrize("name", list(CASES))
+def test_dquant_prefill_is_bit_exact(name):
+    w = CASES[name]
+    S = w.seq
+    cache, k, v = _quantize(w)
+    got, qcap = dquant_views(w, cache, S)
+    dk = OC.quantize_dquant(w, k, True, S)
+    dv = OC.quantize_dquant(w, v, False, S)
+    assert not dk.flags.any() and not dv.flags.any()
+    nq = S - w.n_sink
+    assert np.array_equal(got["codes_k"][:, :nq], dk.container)
+    assert np.array_equal(got["codes_v"][:, :nq], dv.container)
+    assert np.array_equal(got["meta_k"][:, :nq, 0], dk.s16) and np.array_equal(got["meta_k"][:, :nq, 1], dk.o16)
+    assert np.array_equal(got["meta_v"][:, :nq, 0], dv.s16) and np.array_equal(got["meta_v"][:, :nq, 1], dv.o16)
+    if w.mean_k:
+        nw = dk.mean_q.shape[1]
+        assert np.array_equal(got["mean_q"][:, :nw], dk.mean_q)
+        assert np.array_equal(got["mean_sc"][:, :nw], dk.mean_sc)
+    for slot, bits in OC.raw_regions(w, k, S).items():
+        assert np.array_equal(got["raw_k"][:, :, slot], bits), slot
+    for slot, bits in OC.raw_regions(w, v, S).items():
+        assert np.array_equal(got["raw_v"][:, :, slot // 2, :, slot & 1], bits), slot
+    cache.close()
+
+
+def test_dquant_append_is_refused():
+    import torch
+    from quantized_decode_attention_gb300 import DQError, KVCache
+    w = CASES["dq-h2"]
+    k, v = W.make_kv(w)
+    cache = KVCache.allocate(cfg_for(w, max_seq=w.seq + 8))
+    cache.quantize(to_device(k, w.kv_dtype), to_device(v, w.kv_dtype))
+    with pytest.raises(DQError):
+        cache.quantize(to_device(k[:, :, :1], w.kv_dtype), to_device(v[:, :, :1], w.kv_dtype), pos0=w.seq)
+    torch.cuda.synchronize()
+    cache.close()
