@@ -206,7 +206,11 @@ dq_status dq_quantize_kv(dq_ctx **ctx, const dq_config *cfg, const dq_kv_buffers
  * dq_quantize_kv call (the recent slots hold that call's latest tokens).  sm_scale multiplies q.k (1/sqrt(head_dim) is usual).  Dense key
  * transforms read bufs->q_comp to form T^{-T} q.
  * Uses the context's workspace for split partials; concurrent calls on one
- * context must be ordered on a stream.
+ * context must be ordered on a stream.  DQ_RANS caches are decoded in place
+ * (D-Quant Sec. 4.5: token-centric, each container decoded once, App. A
+ * Eq. (8)-(9) for the affine terms); a container that asks for more bytes than
+ * it holds (a corrupt cache) stops reading there and latches DQ_EINVAL for
+ * dq_check.
  * Errors: DQ_EINVAL, DQ_EALIGN, DQ_EUNSUPPORTED, DQ_ENOMEM, DQ_ECUDA.
  */
 dq_status dq_decode_attention(dq_ctx **ctx, const dq_config *cfg, const dq_kv_buffers *bufs,
@@ -240,7 +244,9 @@ dq_status dq_rans_model(const dq_config *cfg, int which, int *levels, int f[16],
 
 /*
  * Synchronize `stream`, then return and clear the device-side status latched
- * by earlier calls on this context (DQ_OK, DQ_ENONFINITE, DQ_ETIMEOUT), or
+ * by earlier calls on this context (DQ_OK, DQ_ENONFINITE, DQ_ETIMEOUT,
+ * DQ_EINFEASIBLE for a stream over its container, DQ_EINVAL for a container
+ * that asked for more bytes than it holds), or
  * DQ_ECUDA if the stream reports an error.  ctx may be NULL (returns DQ_OK).
  */
 dq_status dq_check(dq_ctx *ctx, void *stream);
@@ -272,6 +278,8 @@ dq_status dq_check(dq_ctx *ctx, void *stream);
  *     message naming the limit.
  *   - Device-side conditions (a bounded wait running out) are not reported by
  *     this entry point; use the context-based one with dq_check to see them.
+ * DQ_RANS caches are refused (DQ_EUNSUPPORTED): their symbol model lives in a
+ * context.
  * Errors: DQ_EINVAL, DQ_EALIGN, DQ_EUNSUPPORTED, DQ_ECUDA.
  */
 #define DQ_NOALLOC_SCRATCH_BYTES (4u << 20)

@@ -1,0 +1,479 @@
+// Decode attention over D-Quant entropy-coded containers (sm_103a).
+//
+// "D-Quant: Driftable Entropy Coding for KV Cache Quantization", Sec. 4.5
+// Decoding and App. A:
+//  * a stream spans all KV heads of a token, so decoding is organised around
+//    tokens: every stream is decoded once, one lane per token, head after
+//    head (the stream's order), and the decoded levels feed that head's
+//    query heads directly;
+//  * Algorithm 2: state from the first 4 bytes, z = x mod 2^8 selects the
+//    table entry (level, f, c), x <- f floor(x / 2^8) + z - c, one byte shifted
+//    in while x < 2^23; one lookup serves decoding and reconstruction;
+//  * Eq. (8): q . k^_t = s_t sum_j q_j m_tj + o_t sum_j q_j + sum_j q_j mu_j, so
+//    keys contract decoded levels and apply the affine terms afterwards;
+//  * Eq. (9): sum_t a_t v^_tj = sum_t (a_t s_t) m_tj + sum_t a_t o_t, so the
+//    value scale folds into the attention weight and the offset is summed
+//    apart.
+// Work: an item is 512 quantized tokens of one sequence (4 warps x 4 chunks of
+// 32 tokens) or the 16-bit tokens (sinks + recent window) of one sequence.
+// Per KV head h a warp, for each of its chunks, decodes 128 key and 128 value
+// symbols per lane, takes the key dot products with the rotated query rows
+// (scalar FMAs, the query broadcast from shared memory), updates the online
+// softmax of the G query heads, stages the value levels in shared memory and
+// runs P.V on the tensor cores (mma m16n8k16, 8 columns = 4 query heads x hi/lo
+// halves of P' = p s).  The decoder states of a lane's 4 tokens stay in
+// registers between heads.  The 4 warps merge their states per head and write
+// one record per query head; a second grid merges the items of a sequence,
+// rotates the value space back and normalises.
+#include <cuda_runtime.h>
+
+#include <cmath>
+
+#include "common.cuh"
+#include "dq_internal.h"
+
+namespace dq {
+namespace {
+
+constexpr int RW = 4;                  // warps per CTA
+constexpr int RCH = 4;                 // 32-token chunks per warp
+constexpr int ITEM = 32 * RW * RCH;    // quantized tokens per item
+constexpr int REC = 132;               // floats per record: acc[128], m, l, 2 pad
+constexpr uint32_t RANS_L = 1u << 23;
+constexpr float SLACK = 8.0f;          // running max may lag by this much (log2 units)
+constexpr int VST = 40;                // u16 per staged value row (32 tokens + pad)
+
+__device__ __forceinline__ uint32_t pack_h2(uint16_t lo, uint16_t hi) {
+    return static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
+}
+
+__device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};\n"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// One rANS stream being decoded by a lane: state, a 32-bit buffer of the next
+// container bytes, and a guard on the bytes a well-formed container can hold.
+struct Dec {
+    uint32_t x, wbuf;
+    const uint32_t *wp;  // next aligned word
+    int nb;              // bytes left in wbuf
+    int left;            // container bytes after the state not yet read
+    __device__ __forceinline__ void open(const uint8_t *base, int C, bool valid) {
+        if (!valid) {  // an idle lane: decodes zeros, reads nothing, reports nothing
+            x = RANS_L;
+            wbuf = 0;
+            wp = nullptr;
+            nb = 0;
+            left = -(1 << 30);
+            return;
+        }
+        x = static_cast<uint32_t>(base[0]) | (static_cast<uint32_t>(base[1]) << 8) |
+            (static_cast<uint32_t>(base[2]) << 16) | (static_cast<uint32_t>(base[3]) << 24);
+        const uintptr_t p = reinterpret_cast<uintptr_t>(base + 4);
+        const int off = static_cast<int>(p & 3u);
+        wp = reinterpret_cast<const uint32_t *>(p - off);
+        wbuf = __ldg(wp) >> (8 * off);
+        wp++;
+        nb = 4 - off;
+        left = C - 4;
+    }
+    // one symbol: returns the 64-bit table entry
+    __device__ __forceinline__ uint2 step(const uint2 *dec, bool &bad) {
+        const uint2 e = dec[x & 255u];
+        x = (e.x & 0x1ffu) * (x >> 8) + (e.x >> 16);
+        if (x < RANS_L) {
+            if (nb == 0) {
+                // never past the container: a well-formed one holds every byte read
+                wbuf = left > 0 ? __ldg(wp) : 0u;
+                wp++;
+                nb = 4;
+            }
+            if (left == 0) bad = true;
+            x = (x << 8) | (wbuf & 255u);
+            wbuf >>= 8;
+            nb--;
+            left--;
+        }
+        return e;
+    }
+};
+
+struct RecMerge {
+    float m[RW][4], l[RW][4];
+    float acc[RW][4][128];
+};
+
+template <int H>
+struct RansSmem {
+    uint2 dec_k[256], dec_v[256];
+    float4 qk[H][128];            // rotated query rows of head h's 4 query heads, by channel
+    float qsum[4 * H];            // sum_c q_rot[qh][c]
+    float qmu[4][4 * H];          // sum_c q_rot[qh][c] mu^_w[c] for the item's 4 windows
+    uint16_t vst[RW][128][VST];   // staged value levels (fp16), [channel][token]
+    uint16_t pst[RW][8][VST];     // staged P' (fp16 hi/lo), [column][token]
+    RecMerge mg;
+};
+
+// ---------------------------------------------------------------------------
+// Quantized item: 512 tokens of one sequence.
+// ---------------------------------------------------------------------------
+template <int H>
+__device__ void rans_quant_item(RansSmem<H> &S, const RansAttnArgs &a, int b, long long s0) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, tig = lane & 3;
+    constexpr int N = 128 * H, HQ = 4 * H;
+    // rotated queries of this sequence (normalized Hadamard per head when keys are rotated)
+    for (int qh = warp; qh < HQ; qh += RW) {
+        float q4[4];
+        const float *qp = a.q + (static_cast<long long>(b) * HQ + qh) * 128 + 4 * lane;
+#pragma unroll
+        for (int j = 0; j < 4; j++) q4[j] = qp[j];
+        if (a.rot_k) {
+            fwht_warp<4>(q4);
+#pragma unroll
+            for (int j = 0; j < 4; j++) q4[j] = __fmul_rn(q4[j], a.hscale);
+        }
+        const int h = qh >> 2, gq = qh & 3;
+#pragma unroll
+        for (int j = 0; j < 4; j++) reinterpret_cast<float *>(&S.qk[h][4 * lane + j])[gq] = q4[j];
+        const float sum = warp_sum(q4[0] + q4[1] + q4[2] + q4[3]);
+        if (lane == 0) S.qsum[qh] = sum;
+        // window means: INT8 q times the fp16 scale
+        for (int w = 0; w < 4; w++) {
+            const long long win = s0 / 128 + w;
+            float dmu = 0.f;
+            if (a.mean && win < a.wcap) {
+                const uint8_t *rec = a.mean + (static_cast<long long>(b) * a.wcap + win) * a.mean_rec;
+                const float sc = __half2float(*reinterpret_cast<const __half *>(rec + N));
+                const uint32_t qw = reinterpret_cast<const uint32_t *>(rec)[32 * h + lane];
+#pragma unroll
+                for (int j = 0; j < 4; j++)
+                    dmu += q4[j] * (static_cast<float>(static_cast<int8_t>((qw >> (8 * j)) & 0xffu)) * sc);
+            }
+            dmu = warp_sum(dmu);
+            if (lane == 0) S.qmu[w][qh] = dmu;
+        }
+    }
+    __syncthreads();
+    // this lane's 4 tokens (one per chunk) and their decoders
+    Dec dk[RCH], dv[RCH];
+    bool bad = false;
+#pragma unroll
+    for (int ch = 0; ch < RCH; ch++) {
+        const long long slot = s0 + 32 * (RCH * warp + ch) + lane;
+        const bool valid = slot < a.n_q;
+        dk[ch].open(a.codes_k + (static_cast<long long>(b) * a.qcap + (valid ? slot : 0)) * a.ck, a.ck, valid);
+        dv[ch].open(a.codes_v + (static_cast<long long>(b) * a.qcap + (valid ? slot : 0)) * a.cv, a.cv, valid);
+    }
+    uint16_t(*vst)[VST] = S.vst[warp];
+    uint16_t(*pst)[VST] = S.pst[warp];
+#pragma unroll 1
+    for (int h = 0; h < H; h++) {
+        float acc[8][4];
+#pragma unroll
+        for (int mi = 0; mi < 8; mi++) acc[mi][0] = acc[mi][1] = acc[mi][2] = acc[mi][3] = 0.f;
+        float mrun[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+        float lsum[4] = {0.f, 0.f, 0.f, 0.f}, osum[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int ch = 0; ch < RCH; ch++) {
+            const long long slot = s0 + 32 * (RCH * warp + ch) + lane;
+            const bool valid = slot < a.n_q;
+            float dot[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 4
+            for (int c = 0; c < 128; c++) {
+                const uint2 ek = dk[ch].step(S.dec_k, bad);
+                const uint2 ev = dv[ch].step(S.dec_v, bad);
+                const float lev = __uint_as_float(ek.y);
+                const float4 q4 = S.qk[h][c];
+                dot[0] = fmaf(q4.x, lev, dot[0]);
+                dot[1] = fmaf(q4.y, lev, dot[1]);
+                dot[2] = fmaf(q4.z, lev, dot[2]);
+                dot[3] = fmaf(q4.w, lev, dot[3]);
+                vst[c][lane] = static_cast<uint16_t>(ev.y);
+            }
+            // Eq. (8) affine terms, log2 units
+            float sk = 0.f, ok = 0.f, sv = 0.f, ov = 0.f;
+            if (valid) {
+                const __half2 mk = reinterpret_cast<const __half2 *>(a.meta_k)[static_cast<long long>(b) * a.qcap + slot];
+                const __half2 mv = reinterpret_cast<const __half2 *>(a.meta_v)[static_cast<long long>(b) * a.qcap + slot];
+                sk = __low2float(mk);
+                ok = __high2float(mk);
+                sv = __low2float(mv);
+                ov = __high2float(mv);
+            }
+            const int wi = static_cast<int>((slot - s0) >> 7);
+            float lg[4], mx[4];
+#pragma unroll
+            for (int gq = 0; gq < 4; gq++) {
+                const int qh = 4 * h + gq;
+                lg[gq] = valid ? a.sm_log2 * (sk * dot[gq] + ok * S.qsum[qh] + S.qmu[wi][qh]) : -INFINITY;
+                mx[gq] = warp_max(lg[gq]);
+            }
+            // online softmax per query head (warp-uniform running max)
+            float al[4];
+#pragma unroll
+            for (int gq = 0; gq < 4; gq++) {
+                al[gq] = 1.f;
+                if (mx[gq] > mrun[gq] + SLACK || (mrun[gq] == -INFINITY && mx[gq] > -INFINITY)) {
+                    al[gq] = mrun[gq] == -INFINITY ? 0.f : ex2(mrun[gq] - mx[gq]);
+                    mrun[gq] = mx[gq];
+                    lsum[gq] *= al[gq];
+                    osum[gq] *= al[gq];
+                }
+            }
+            const float my_al = tig == 0 ? al[0] : (tig == 1 ? al[1] : (tig == 2 ? al[2] : al[3]));
+            if (my_al != 1.f) {
+#pragma unroll
+                for (int mi = 0; mi < 8; mi++)
+#pragma unroll
+                    for (int r = 0; r < 4; r++) acc[mi][r] *= my_al;
+            }
+#pragma unroll
+            for (int gq = 0; gq < 4; gq++) {
+                const float p = valid ? ex2(lg[gq] - mrun[gq]) : 0.f;
+                lsum[gq] += p;
+                osum[gq] = fmaf(p, ov, osum[gq]);
+                const __half hi = __float2half_rn(p * sv);
+                const __half lo = __float2half_rn(p * sv - __half2float(hi));
+                pst[2 * gq][lane] = __half_as_ushort(hi);
+                pst[2 * gq + 1][lane] = __half_as_ushort(lo);
+            }
+            __syncwarp();
+            // P . V: A = V^T (channels x tokens), B = P' (tokens x 8 columns)
+#pragma unroll
+            for (int kt = 0; kt < 2; kt++) {
+                const uint32_t b0 = *reinterpret_cast<const uint32_t *>(&pst[g][16 * kt + 2 * tig]);
+                const uint32_t b1 = *reinterpret_cast<const uint32_t *>(&pst[g][16 * kt + 2 * tig + 8]);
+#pragma unroll
+                for (int mi = 0; mi < 8; mi++) {
+                    const uint32_t a0 = *reinterpret_cast<const uint32_t *>(&vst[16 * mi + g][16 * kt + 2 * tig]);
+                    const uint32_t a1 = *reinterpret_cast<const uint32_t *>(&vst[16 * mi + g + 8][16 * kt + 2 * tig]);
+                    const uint32_t a2 = *reinterpret_cast<const uint32_t *>(&vst[16 * mi + g][16 * kt + 2 * tig + 8]);
+                    const uint32_t a3 =
+                        *reinterpret_cast<const uint32_t *>(&vst[16 * mi + g + 8][16 * kt + 2 * tig + 8]);
+                    mma16816(acc[mi], a0, a1, a2, a3, b0, b1);
+                }
+            }
+            __syncwarp();
+        }
+        // warp totals of l and the offset sums; this warp's record per query head
+#pragma unroll
+        for (int gq = 0; gq < 4; gq++) {
+            lsum[gq] = warp_sum(lsum[gq]);
+            osum[gq] = warp_sum(osum[gq]);
+        }
+        const float my_o = tig == 0 ? osum[0] : (tig == 1 ? osum[1] : (tig == 2 ? osum[2] : osum[3]));
+#pragma unroll
+        for (int mi = 0; mi < 8; mi++) {
+            S.mg.acc[warp][tig][16 * mi + g] = acc[mi][0] + acc[mi][1] + my_o;
+            S.mg.acc[warp][tig][16 * mi + g + 8] = acc[mi][2] + acc[mi][3] + my_o;
+        }
+        if (lane < 4) {
+            S.mg.m[warp][lane] = lane == 0 ? mrun[0] : (lane == 1 ? mrun[1] : (lane == 2 ? mrun[2] : mrun[3]));
+            S.mg.l[warp][lane] = lane == 0 ? lsum[0] : (lane == 1 ? lsum[1] : (lane == 2 ? lsum[2] : lsum[3]));
+        }
+        __syncthreads();
+        // merge the 4 warps: warp gq writes the record of query head 4h + gq
+        {
+            const int gq = warp;
+            float M = -INFINITY;
+#pragma unroll
+            for (int w = 0; w < RW; w++) M = fmaxf(M, S.mg.m[w][gq]);
+            float sc[RW], L = 0.f;
+#pragma unroll
+            for (int w = 0; w < RW; w++) {
+                sc[w] = S.mg.m[w][gq] == -INFINITY ? 0.f : ex2(S.mg.m[w][gq] - M);
+                L += S.mg.l[w][gq] * sc[w];
+            }
+            float *rec = a.partials + ((static_cast<long long>(b) * a.items_per_b + s0 / ITEM) * HQ + 4 * h + gq) * REC;
+#pragma unroll
+            for (int j = 0; j < 4; j++) {
+                const int c = lane + 32 * j;
+                float v = 0.f;
+#pragma unroll
+                for (int w = 0; w < RW; w++) v += S.mg.acc[w][gq][c] * sc[w];
+                rec[c] = v;
+            }
+            if (lane == 0) {
+                rec[128] = M;
+                rec[129] = L;
+            }
+        }
+        __syncthreads();
+    }
+    if (bad) atomicOr(a.status, ST_BOUNDS);
+}
+
+// ---------------------------------------------------------------------------
+// 16-bit item: the sinks and the recent window of one sequence, every head.
+// Warp gq handles query head 4h + gq of KV head h; lanes own 4 channels.
+// ---------------------------------------------------------------------------
+template <int H>
+__device__ void rans_raw_item(RansSmem<H> &S, const RansAttnArgs &a, int b) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    constexpr int HQ = 4 * H;
+    for (int h = 0; h < H; h++) {
+        const int qh = 4 * h + warp;
+        const long long u = static_cast<long long>(b) * H + h;
+        float q4[4];
+        const float *qp = a.q + (static_cast<long long>(b) * HQ + qh) * 128 + 4 * lane;
+#pragma unroll
+        for (int j = 0; j < 4; j++) q4[j] = qp[j];
+        float M = -INFINITY, L = 0.f, acc[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int i = 0; i < a.n_raw; i++) {
+            const int slot = i < a.n_sink_eff ? i : a.n_sink_cfg + static_cast<int>((a.recent_t0 + (i - a.n_sink_eff)) % a.n_recent_cfg);
+            const uint16_t *kr = a.raw_k + (u * a.rcap + slot) * 128 + 4 * lane;
+            float s = 0.f;
+#pragma unroll
+            for (int j = 0; j < 4; j++) {
+                const uint16_t bits = kr[j];
+                const float kv = a.raw_bf16 ? __uint_as_float(static_cast<uint32_t>(bits) << 16)
+                                            : __half2float(__ushort_as_half(bits));
+                s = fmaf(q4[j], kv, s);
+            }
+            const float lg = a.sm_log2 * warp_sum(s);
+            const float Mn = fmaxf(M, lg);
+            const float al = M == -INFINITY ? 0.f : ex2(M - Mn);
+            const float p = ex2(lg - Mn);
+            L = L * al + p;
+            const uint16_t *vr = a.raw_v + ((u * (a.rcap / 2) + slot / 2) * 128 + 4 * lane) * 2 + (slot & 1);
+#pragma unroll
+            for (int j = 0; j < 4; j++) {
+                const uint16_t bits = vr[2 * j];
+                const float vv = a.raw_bf16 ? __uint_as_float(static_cast<uint32_t>(bits) << 16)
+                                            : __half2float(__ushort_as_half(bits));
+                acc[j] = fmaf(p, vv, acc[j] * al);
+            }
+            M = Mn;
+        }
+        float *rec = a.partials + ((static_cast<long long>(b) * a.items_per_b + a.items_per_b - 1) * HQ + qh) * REC;
+#pragma unroll
+        for (int j = 0; j < 4; j++) rec[4 * lane + j] = acc[j];
+        if (lane == 0) {
+            rec[128] = M;
+            rec[129] = L;
+        }
+    }
+}
+
+template <int H>
+__global__ void __launch_bounds__(128) attn_rans_kernel(RansAttnArgs a, const RansDevTables *tabs) {
+    extern __shared__ __align__(16) unsigned char smraw[];
+    RansSmem<H> &S = *reinterpret_cast<RansSmem<H> *>(smraw);
+    const int b = blockIdx.x / a.items_per_b, it = blockIdx.x % a.items_per_b;
+    if (it == a.items_per_b - 1) {
+        rans_raw_item<H>(S, a, b);
+        return;
+    }
+    // decoder tables: entry = (f | (z - c) << 16, level as fp32 bits) for keys,
+    // (f | (z - c) << 16, level as fp16 bits) for values
+    for (int z = threadIdx.x; z < 256; z += blockDim.x) {
+        const uint32_t ek = tabs->k.dec[z], ev = tabs->v.dec[z];
+        const uint32_t mk = ek & 15u, mv = ev & 15u;
+        S.dec_k[z] = make_uint2(((ek >> 4) & 0x1ffu) | ((ek >> 16) << 16), __float_as_uint(static_cast<float>(mk)));
+        S.dec_v[z] = make_uint2(((ev >> 4) & 0x1ffu) | ((ev >> 16) << 16),
+                                static_cast<uint32_t>(__half_as_ushort(__uint2half_rn(mv))));
+    }
+    __syncthreads();
+    rans_quant_item<H>(S, a, b, static_cast<long long>(it) * ITEM);
+}
+
+// ---------------------------------------------------------------------------
+// Merge the records of a sequence: one CTA per (sequence, KV head), warp gq
+// for query head 4h + gq.  Quantized records live in the value space the
+// encoder saw (rotated back here when values were rotated); the 16-bit record
+// is in the original space.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(128) rans_combine_kernel(RansAttnArgs a) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int b = blockIdx.x / a.Hkv, h = blockIdx.x % a.Hkv;
+    const int HQ = 4 * a.Hkv, qh = 4 * h + warp;
+    const int nqi = a.items_per_b - 1;
+    float M = -INFINITY;
+    for (int i = 0; i < a.items_per_b; i++) {
+        const float *rec = a.partials + ((static_cast<long long>(b) * a.items_per_b + i) * HQ + qh) * REC;
+        if (i < nqi ? i < a.n_qitems : a.n_raw > 0) M = fmaxf(M, rec[128]);
+    }
+    float L = 0.f, aq[4] = {0.f, 0.f, 0.f, 0.f}, ar[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int i = 0; i < a.items_per_b; i++) {
+        const bool used = i < nqi ? i < a.n_qitems : a.n_raw > 0;
+        if (!used) continue;
+        const float *rec = a.partials + ((static_cast<long long>(b) * a.items_per_b + i) * HQ + qh) * REC;
+        const float m = rec[128];
+        if (m == -INFINITY) continue;
+        const float sc = ex2(m - M);
+        L += rec[129] * sc;
+        float *dst = i < nqi ? aq : ar;
+#pragma unroll
+        for (int j = 0; j < 4; j++) dst[j] += rec[4 * lane + j] * sc;
+    }
+    if (a.rot_v) {
+        fwht_warp<4>(aq);
+#pragma unroll
+        for (int j = 0; j < 4; j++) aq[j] *= a.hscale;
+    }
+    const float inv = L > 0.f ? 1.f / L : 0.f;
+    const long long o = (static_cast<long long>(b) * HQ + qh) * 128 + 4 * lane;
+#pragma unroll
+    for (int j = 0; j < 4; j++) {
+        const float y = (aq[j] + ar[j]) * inv;
+        if (a.out_dtype == DQ_F32) reinterpret_cast<float *>(a.out)[o + j] = y;
+        else if (a.out_dtype == DQ_F16) reinterpret_cast<__half *>(a.out)[o + j] = __float2half_rn(y);
+        else reinterpret_cast<__nv_bfloat16 *>(a.out)[o + j] = __float2bfloat16_rn(y);
+    }
+}
+
+}  // namespace
+
+size_t rans_attention_smem(int H) {
+    switch (H) {
+        case 1: return sizeof(RansSmem<1>);
+        case 2: return sizeof(RansSmem<2>);
+        case 4: return sizeof(RansSmem<4>);
+        default: return sizeof(RansSmem<8>);
+    }
+}
+
+long long rans_partial_floats(int B, int Hq, long long qcap) {
+    const long long items = (qcap + ITEM - 1) / ITEM + 1;
+    return static_cast<long long>(B) * items * Hq * REC;
+}
+
+int launch_attention_rans(const RansAttnArgs &a0, const RansDevTables *tabs, void *stream) {
+    RansAttnArgs a = a0;
+    a.n_qitems = static_cast<int>((a.n_q + ITEM - 1) / ITEM);
+    a.items_per_b = a.n_qitems + 1;
+    const cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const size_t smem = rans_attention_smem(a.Hkv);
+    const unsigned grid = static_cast<unsigned>(a.B * a.items_per_b);
+    cudaError_t e = cudaSuccess;
+    switch (a.Hkv) {
+        case 1:
+            e = cudaFuncSetAttribute(attn_rans_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+            if (e == cudaSuccess) attn_rans_kernel<1><<<grid, 32 * RW, smem, st>>>(a, tabs);
+            break;
+        case 2:
+            e = cudaFuncSetAttribute(attn_rans_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+            if (e == cudaSuccess) attn_rans_kernel<2><<<grid, 32 * RW, smem, st>>>(a, tabs);
+            break;
+        case 4:
+            e = cudaFuncSetAttribute(attn_rans_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+            if (e == cudaSuccess) attn_rans_kernel<4><<<grid, 32 * RW, smem, st>>>(a, tabs);
+            break;
+        case 8:
+            e = cudaFuncSetAttribute(attn_rans_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+            if (e == cudaSuccess) attn_rans_kernel<8><<<grid, 32 * RW, smem, st>>>(a, tabs);
+            break;
+        default: return static_cast<int>(cudaErrorInvalidValue);
+    }
+    if (e != cudaSuccess) return static_cast<int>(e);
+    if ((e = cudaGetLastError()) != cudaSuccess) return static_cast<int>(e);
+    rans_combine_kernel<<<static_cast<unsigned>(a.B * a.Hkv), 128, 0, st>>>(a);
+    return static_cast<int>(cudaGetLastError());
+}
+
+}  // namespace dq

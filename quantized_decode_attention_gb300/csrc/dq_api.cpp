@@ -149,6 +149,8 @@ dq_status make_layout(const dq_config *cfg, Layout *L) {
         if (c.head_dim != 128) return fail(DQ_EUNSUPPORTED, "entropy-coded scheme: head_dim must be 128");
         if (c.n_kv_heads != 1 && c.n_kv_heads != 2 && c.n_kv_heads != 4 && c.n_kv_heads != 8)
             return fail(DQ_EUNSUPPORTED, "entropy-coded scheme: 1, 2, 4 or 8 KV heads per stream");
+        if (c.n_q_heads != 4 * c.n_kv_heads)
+            return fail(DQ_EUNSUPPORTED, "entropy-coded scheme: 4 query heads per KV head");
         if (c.meta_dtype != DQ_F16) return fail(DQ_EINVAL, "entropy-coded scheme: metadata is fp16");
         if (c.rans_prob_bits != 8) return fail(DQ_EUNSUPPORTED, "entropy-coded scheme: prob_bits must be 8");
         if (!(c.rans_alpha > 0.0f && c.rans_alpha <= 8.0f)) return fail(DQ_EINVAL, "rans_alpha outside (0, 8]");
@@ -285,13 +287,19 @@ static dq_status get_ctx(dq_ctx **pctx, const dq_config *cfg, const Layout &L) {
     cudaError_t e4 = cudaSuccess;
     if (L.scheme == DQ_NUQ)
         e4 = cudaMalloc(&c->nuq_bits, static_cast<size_t>(L.U) * L.qcap * (L.d / 32) * sizeof(uint32_t));
-    if (L.scheme == DQ_RANS) e4 = cudaMalloc(&c->rans, sizeof(dq::RansDevTables));
+    if (L.scheme == DQ_RANS) {
+        e4 = cudaMalloc(&c->rans, sizeof(dq::RansDevTables));
+        if (e4 == cudaSuccess)
+            e4 = cudaMalloc(&c->rans_partials,
+                            sizeof(float) * static_cast<size_t>(dq::rans_partial_floats(L.B, L.Hq, L.qcap)));
+    }
     if (e1 != cudaSuccess || e2 != cudaSuccess || e3 != cudaSuccess || e4 != cudaSuccess) {
         cudaFree(c->status);
         cudaFree(c->partials);
         cudaFree(c->counters);
         cudaFree(c->nuq_bits);
         cudaFree(c->rans);
+        cudaFree(c->rans_partials);
         delete c;
         cudaGetLastError();
         return fail(DQ_ENOMEM, "workspace allocation failed");
@@ -542,7 +550,46 @@ dq_status dq_decode_attention(dq_ctx **ctx, const dq_config *cfg, const dq_kv_bu
     if (!aligned16(q) || !aligned16(out)) return fail(DQ_EALIGN, "q / out not 16-byte aligned");
     if ((s = get_ctx(ctx, cfg, L)) != DQ_OK) return s;
     dq_ctx *c = *ctx;
-    if (L.scheme == DQ_RANS) return fail(DQ_EUNSUPPORTED, "entropy-coded attention is not built yet");
+    if (L.scheme == DQ_RANS) {
+        dq::RansAttnArgs r{};
+        r.q = static_cast<const float *>(q);
+        r.out = out;
+        r.out_dtype = cfg->out_dtype;
+        r.codes_k = static_cast<const uint8_t *>(bufs->codes_k);
+        r.codes_v = static_cast<const uint8_t *>(bufs->codes_v);
+        r.meta_k = bufs->meta_k;
+        r.meta_v = bufs->meta_v;
+        r.mean = cfg->k.mean ? static_cast<const uint8_t *>(bufs->mean_k) : nullptr;
+        r.raw_k = static_cast<const uint16_t *>(bufs->raw_k);
+        r.raw_v = static_cast<const uint16_t *>(bufs->raw_v);
+        r.B = L.B;
+        r.Hkv = L.Hkv;
+        r.ck = L.ck;
+        r.cv = L.cv;
+        r.qcap = L.qcap;
+        r.wcap = L.wcap;
+        r.mean_rec = L.mean_rec;
+        r.rcap = L.rcap;
+        const long long n_s = seq_len < cfg->n_sink ? seq_len : cfg->n_sink;
+        long long q_hi = seq_len - cfg->n_recent;
+        if (q_hi < n_s) q_hi = n_s;
+        r.n_q = q_hi - n_s;
+        r.n_sink_eff = static_cast<int>(n_s);
+        r.n_sink_cfg = cfg->n_sink;
+        r.n_recent_cfg = cfg->n_recent;
+        r.recent_t0 = q_hi;
+        r.n_raw = static_cast<int>(n_s + (seq_len - q_hi));
+        r.rot_k = cfg->k.rot == DQ_ROT_HADAMARD;
+        r.rot_v = cfg->v.rot == DQ_ROT_HADAMARD;
+        r.raw_bf16 = cfg->kv_dtype == DQ_BF16;
+        r.hscale = static_cast<float>(1.0 / std::sqrt(128.0));
+        r.sm_log2 = sm_scale * 1.4426950408889634f;
+        r.partials = c->rans_partials;
+        r.status = c->status;
+        const int e = dq::launch_attention_rans(r, c->rans, stream);
+        if (e != 0) return fail(DQ_ECUDA, "attention launch: %s", cudaGetErrorString(static_cast<cudaError_t>(e)));
+        return ok();
+    }
 
     dq::AttnArgs a{};
     a.q = static_cast<const float *>(q);
@@ -620,6 +667,7 @@ dq_status dq_check(dq_ctx *ctx, void *stream) {
     if (st && cudaMemset(ctx->status, 0, sizeof st) != cudaSuccess) return fail(DQ_ECUDA, "status clear failed");
     if (st & dq::ST_TIMEOUT) return fail(DQ_ETIMEOUT, "a bounded device wait ran out");
     if (st & dq::ST_INFEASIBLE) return fail(DQ_EINFEASIBLE, "a stream did not fit its container");
+    if (st & dq::ST_BOUNDS) return fail(DQ_EINVAL, "a container asked for more bytes than it holds (corrupt cache)");
     if (st & dq::ST_NONFINITE) return fail(DQ_ENONFINITE, "non-finite K/V input");
     return ok();
 }
@@ -632,6 +680,7 @@ void dq_free(dq_ctx *ctx) {
     cudaFree(ctx->nuq_bits);
     cudaFree(ctx->rans);
     cudaFree(ctx->rans_sym);
+    cudaFree(ctx->rans_partials);
     delete ctx;
 }
 

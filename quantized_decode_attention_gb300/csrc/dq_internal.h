@@ -84,6 +84,31 @@ int launch_rans_drift(const RansQuantArgs &a, const RansTable *tb, const float *
 int launch_rans_encode(const RansQuantArgs &a, const RansTable *tb, int C, void *stream);
 int launch_rans_raw(const RansQuantArgs &a, void *stream);
 
+// Per-call arguments of the entropy-coded decode attention.
+struct RansAttnArgs {
+    const float *q;          // [B][4 Hkv][128]
+    void *out;               // [B][4 Hkv][128]
+    int out_dtype;
+    const uint8_t *codes_k, *codes_v;  // [B][qcap][ck] / [B][qcap][cv]
+    const void *meta_k, *meta_v;       // [B][qcap] (s, o) fp16
+    const uint8_t *mean;     // [B][wcap][mean_rec] or nullptr
+    const uint16_t *raw_k, *raw_v;
+    int B, Hkv, ck, cv;
+    long long qcap, wcap;
+    int mean_rec, rcap;
+    long long n_q;           // quantized slots read: [0, n_q)
+    int n_sink_eff, n_sink_cfg, n_recent_cfg;
+    long long recent_t0;     // first token of the recent window read
+    int n_raw;               // 16-bit tokens read
+    int rot_k, rot_v, raw_bf16;
+    float hscale, sm_log2;
+    float *partials;         // [B][items_per_b][4 Hkv][132]
+    unsigned *status;
+    int n_qitems, items_per_b;  // set by the launcher
+};
+int launch_attention_rans(const RansAttnArgs &a, const RansDevTables *tabs, void *stream);
+long long rans_partial_floats(int B, int Hq, long long qcap);
+
 dq_status make_layout(const dq_config *cfg, Layout *L);
 
 // Record `msg` as this thread's last error (empty for DQ_OK) and return `s`.
@@ -199,5 +224,6 @@ struct dq_ctx {
     uint32_t *nuq_bits;  // non-uniform scheme: key outlier bitmap scratch [U][Qcap][d/32]
     dq::RansDevTables *rans;  // entropy-coded scheme: symbol models (device)
     uint8_t *rans_sym;   // entropy-coded scheme: symbol scratch of a prefill
+    float *rans_partials;  // entropy-coded scheme: attention item records
     size_t rans_sym_cap; // bytes
 };

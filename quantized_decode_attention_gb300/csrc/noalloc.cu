@@ -71,6 +71,8 @@ extern "C" dq_status dq_decode_attention_noalloc(const dq_config *cfg, const dq_
     dq::Layout L;
     dq_status s = dq::make_layout(cfg, &L);
     if (s != DQ_OK) return s;
+    if (L.scheme == DQ_RANS)
+        return dq::set_last_error(DQ_EUNSUPPORTED, "entropy-coded caches decode with the symbol model of a context");
     if (seq_len < 1 || seq_len > cfg->max_seq) return dq::set_last_error(DQ_EINVAL, "seq_len outside [1, max_seq]");
     if (!std::isfinite(sm_scale)) return dq::set_last_error(DQ_EINVAL, "sm_scale is not finite");
     const void *const *p = reinterpret_cast<const void *const *>(bufs);

@@ -85,3 +85,53 @@ def test_dquant_append_is_refused():
         cache.quantize(to_device(k[:, :, :1], w.kv_dtype), to_device(v[:, :, :1], w.kv_dtype), pos0=w.seq)
     torch.cuda.synchronize()
     cache.close()
+
+
+def _tol(ref, out_dtype):
+    ulp = {"bf16": 2.0 ** -8, "f16": 2.0 ** -11}.get(out_dtype, 0.0)
+    return 2e-3 + ulp * np.abs(ref)
+
+
+@pytest.mark.parametrize("name", list(CASES))
+@pytest.mark.parametrize("out_dtype", ["f32", "bf16"])
+def test_dquant_attention_matches_oracle(name, out_dtype):
+    import torch
+    from quantized_decode_attention_gb300 import KVCache
+    from helpers import out_to_np
+    w = CASES[name].with_(out_dtype=out_dtype)
+    S = w.seq
+    k, v = W.make_kv(w)
+    q = W.make_q(w)
+    cache = KVCache.allocate(cfg_for(w))
+    cache.quantize(to_device(k, w.kv_dtype), to_device(v, w.kv_dtype))
+    dk = OC.quantize_dquant(w, k, True, S)
+    dv = OC.quantize_dquant(w, v, False, S)
+    td = {"f32": torch.float32, "bf16": torch.bfloat16}[out_dtype]
+    out = torch.empty((w.batch, w.n_q_heads, w.head_dim), dtype=td, device="cuda")
+    qd = to_device(q, "f32")
+    # the recent ring holds the latest tokens of the prefill, so shorter lengths
+    # are only meaningful without a recent window
+    lens = [S] if w.n_recent else [S, S - 37, w.n_sink + 1, 1]
+    for L in lens:
+        cache.attention(qd, out, L)
+        torch.cuda.synchronize()
+        cache.check()
+        got = out_to_np(out)
+        ref = OC.attention(w, q, k, v, L, dk, dv)
+        assert np.all(np.isfinite(got))
+        err = np.abs(got - ref)
+        assert np.all(err <= _tol(ref, out_dtype)), (L, float(err.max()))
+    cache.close()
+
+
+def test_dquant_noalloc_is_refused():
+    import torch
+    from quantized_decode_attention_gb300 import DQError, KVCache
+    w = CASES["dq-h2"]
+    k, v = W.make_kv(w)
+    cache = KVCache.allocate(cfg_for(w))
+    cache.quantize(to_device(k, w.kv_dtype), to_device(v, w.kv_dtype))
+    out = torch.empty((w.batch, w.n_q_heads, w.head_dim), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(DQError):
+        cache.attention_noalloc(to_device(W.make_q(w), "f32"), out, w.seq)
+    cache.close()
