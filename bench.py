@@ -50,6 +50,7 @@ def parse():
     p.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU baseline sample budget")
     p.add_argument("--no-cpu", action="store_true")
     p.add_argument("--no-nuq", action="store_true", help="skip the KVQuant NUQ cache measurement")
+    p.add_argument("--no-dquant", action="store_true", help="skip the D-Quant cache measurement")
     return p.parse_args()
 
 
@@ -98,6 +99,24 @@ def nuq_algorithmic_bytes(w: W.Workload, S: int) -> dict:
     out = w.batch * w.n_q_heads * d * 2
     total = codes + lut + side + raw + q + out
     return {"codes": codes, "tables": lut, "outliers": side, "raw": raw, "q": q, "out": out, "total": total}
+
+
+def dquant_algorithmic_bytes(w: W.Workload, S: int) -> dict:
+    """Bytes one D-Quant decode-attention call must move: the key and value
+    containers and fp16 (s, o) of the quantized tokens, the INT8 window means
+    covering them, the 16-bit sinks and recent window, q and out."""
+    U, d = w.batch * w.n_kv_heads, w.head_dim
+    n = w.n_kv_heads * d
+    n_raw = min(S, w.n_sink) + min(max(S - w.n_sink, 0), w.n_recent)
+    n_q = S - n_raw
+    cont = w.batch * n_q * (w.extra["container_k"] + w.extra["container_v"])
+    meta = w.batch * n_q * 8
+    mean = w.batch * (-(-n_q // 128)) * (n + 16) if w.mean_k else 0
+    raw = U * n_raw * d * 2 * 2
+    q = w.batch * w.n_q_heads * d * 4
+    out = w.batch * w.n_q_heads * d * 2
+    total = cont + meta + mean + raw + q + out
+    return {"containers": cont, "meta": meta, "mean": mean, "raw": raw, "q": q, "out": out, "total": total}
 
 
 class Clocks:
@@ -374,6 +393,85 @@ def run_gpu_nuq(args, w):
     return res
 
 
+def run_gpu_dquant(args, w):
+    """D-Quant cache (prefill only): each step is one decode-attention call,
+    rotating over cache copies larger than L2."""
+    import torch
+    from quantized_decode_attention_gb300 import KVCache, make_config
+    S = w.seq
+    k, v = W.make_kv(w)
+    q = W.make_q(w)
+    b16 = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).cuda().view(torch.bfloat16)
+    k_dev, v_dev, q_dev = b16(k), b16(v), torch.from_numpy(q).cuda()
+    del k, v
+    e = w.extra
+    cfg = make_config(batch=w.batch, n_kv_heads=w.n_kv_heads, n_q_heads=w.n_q_heads, head_dim=w.head_dim,
+                      max_seq=S, kv_dtype=w.kv_dtype, out_dtype=w.out_dtype, rot_k=w.rot_k, rot_v=w.rot_v,
+                      mean_k=w.mean_k, n_sink=w.n_sink, n_recent=w.n_recent, scheme="rans",
+                      levels_k=e["levels_k"], levels_v=e["levels_v"], container_k=e["container_k"],
+                      container_v=e["container_v"], rans_alpha=e["alpha"])
+    L2 = torch.cuda.get_device_properties(0).L2_cache_size
+    ab = dquant_algorithmic_bytes(w, S)
+    copies = args.copies or max(3, int(np.ceil(3 * L2 / ab["total"])) + 1)
+    stream = torch.cuda.Stream()
+    base = KVCache.allocate(cfg, zero=False)
+    with torch.cuda.stream(stream):
+        base.quantize(k_dev, v_dev, pos0=0, stream=stream.cuda_stream)  # context, scratch
+        stream.synchronize()
+        p0, p1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        p0.record(stream)
+        base.quantize(k_dev, v_dev, pos0=0, stream=stream.cuda_stream)
+        p1.record(stream)
+        stream.synchronize()
+    prefill_ms = p0.elapsed_time(p1)
+    base.check()
+    del k_dev, v_dev
+    caches = [base] + [base.clone_shared() for _ in range(copies - 1)]
+    out = torch.empty((w.batch, w.n_q_heads, w.head_dim), dtype=torch.bfloat16, device="cuda")
+    sm_scale = w.head_dim ** -0.5
+    nc = len(caches)
+    steps = max(nc, min(args.steps, 60))
+    with torch.cuda.stream(stream):
+        for i in range(max(3, nc)):
+            caches[i % nc].attention(q_dev, out, S, sm_scale, stream=stream.cuda_stream)
+        stream.synchronize()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda._sleep(int(2e8))
+        t0.record(stream)
+        for i in range(steps):
+            evs[i][0].record(stream)
+            caches[i % nc].attention(q_dev, out, S, sm_scale, stream=stream.cuda_stream)
+            evs[i][1].record(stream)
+        t1.record(stream)
+        stream.synchronize()
+        total_ms = t0.elapsed_time(t1)
+        attn_ms = [a.elapsed_time(b) for a, b in evs]
+        q_h = q_dev.cpu().pin_memory()
+        out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        q_b = q_dev.clone()
+        n_e2e = min(steps, 20)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        wall0 = time.perf_counter()
+        e0.record(stream)
+        for i in range(n_e2e):
+            q_b.copy_(q_h, non_blocking=True)
+            caches[i % nc].attention(q_b, out, S, sm_scale, stream=stream.cuda_stream)
+            out_h.copy_(out, non_blocking=True)
+        e1.record(stream)
+        stream.synchronize()
+        e2e_ms = max(e0.elapsed_time(e1), (time.perf_counter() - wall0) * 1e3)
+    for c in caches:
+        c.check()
+    res = {"total_ms": total_ms, "steps": steps, "attn_ms": statistics.mean(attn_ms),
+           "attn_ms_median": statistics.median(attn_ms), "algo": ab, "copies": nc, "prefill_ms": prefill_ms,
+           "e2e_tok_s": w.batch * n_e2e / (e2e_ms / 1e3)}
+    for c in caches[1:]:
+        c.detach()
+    caches[0].close()
+    return res
+
+
 def cpu_baseline(w, bits, S, budget_s, k, v, q):
     """The oracle as it stands, timed on this host: quantize one unit's cache and
     run its fp64 decode attention, for as many units as fit the budget."""
@@ -452,6 +550,7 @@ def main():
         variants[f"{vb}bit"] = r
     del k_dev, v_dev
     nuq = None if args.no_nuq else run_gpu_nuq(args, W.NUQ)
+    dqr = None if args.no_dquant else run_gpu_dquant(args, W.DQUANT)
     total_ms = res["total_ms"]
     if world > 1:
         t = torch.tensor([total_ms], device="cuda")
@@ -499,6 +598,19 @@ def main():
                        "n_sink": W.NUQ.n_sink, "outlier_frac": 0.01, "lloyd_iters": 8,
                        "l2": f"{nuq['copies']} cache copies rotated per step (> L2)",
                        "step": "decode attention (prefill-only scheme), CUDA graph over the copies"}}
+    if dqr is not None:
+        D = W.DQUANT
+        line["variants"][f"{D.name}-k{D.extra['levels_k']}x{D.extra['container_k']}-v{D.extra['levels_v']}x{D.extra['container_v']}"] = {
+            "value": round(D.batch / (dqr["total_ms"] / dqr["steps"] / 1e3), 1),
+            "ms_per_step": round(dqr["total_ms"] / dqr["steps"], 5),
+            "roofline": roof(dqr, "dquant"), "e2e_tok_s": round(dqr["e2e_tok_s"], 1),
+            "prefill_ms": round(dqr["prefill_ms"], 3),
+            "config": {"batch": D.batch, "q_heads": D.n_q_heads, "kv_heads": D.n_kv_heads, "head_dim": D.head_dim,
+                       "seq_len": D.seq, "n_recent": D.n_recent, "levels_k": D.extra["levels_k"],
+                       "levels_v": D.extra["levels_v"], "container_k": D.extra["container_k"],
+                       "container_v": D.extra["container_v"], "bits_per_value": 2.26,
+                       "l2": f"{dqr['copies']} cache copies rotated per step (> L2)",
+                       "step": "decode attention (prefill-only scheme), one call per step"}}
     if rank == 0 and not args.no_cpu:
         line["cpu_baseline"] = cpu_baseline(w, args.bits, S, args.cpu_seconds, k, v, q)
     if rank == 0:

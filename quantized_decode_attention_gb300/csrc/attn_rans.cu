@@ -56,49 +56,70 @@ __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-// One rANS stream being decoded by a lane: state, a 32-bit buffer of the next
-// container bytes, and a guard on the bytes a well-formed container can hold.
+// Predicated 32-bit read-only load: returns *p when pred, else dflt (no branch).
+__device__ __forceinline__ uint32_t ldg_if(const uint32_t *p, bool pred, uint32_t dflt) {
+    uint32_t v = dflt;
+    asm("{\n .reg .pred q;\n setp.ne.b32 q, %2, 0;\n @q ld.global.nc.u32 %0, [%1];\n}\n"
+        : "+r"(v)
+        : "l"(p), "r"(static_cast<int>(pred)));
+    return v;
+}
+
+// One rANS stream being decoded by a lane.  The container bytes after the
+// state sit in a 64-bit reservoir (the next byte at bit `pos`); every 4
+// symbols, refill() moves in the word prefetched at the previous refill and
+// fetches the next one (a predicated load, so there is no branch and no wait),
+// which keeps at least 4 unread bytes in the reservoir - enough for 4 symbols,
+// each taking at most one byte.  Loads stay inside the aligned words that
+// overlap the container (wl counts those not yet loaded); an idle lane loads
+// nothing.  A well-formed stream ends in the state the encoder started from
+// (2^23), which the caller checks.
 struct Dec {
-    uint32_t x, wbuf;
-    const uint32_t *wp;  // next aligned word
-    int nb;              // bytes left in wbuf
-    int left;            // container bytes after the state not yet read
+    uint32_t x, nxt, pos;
+    uint64_t buf;
+    const uint32_t *wp;  // next word to load
+    int wl;              // words overlapping the container not yet loaded
     __device__ __forceinline__ void open(const uint8_t *base, int C, bool valid) {
-        if (!valid) {  // an idle lane: decodes zeros, reads nothing, reports nothing
+        if (!valid) {  // an idle lane: decodes zeros, reads nothing
             x = RANS_L;
-            wbuf = 0;
+            nxt = pos = 0;
+            buf = 0;
             wp = nullptr;
-            nb = 0;
-            left = -(1 << 30);
+            wl = 0;
             return;
         }
         x = static_cast<uint32_t>(base[0]) | (static_cast<uint32_t>(base[1]) << 8) |
             (static_cast<uint32_t>(base[2]) << 16) | (static_cast<uint32_t>(base[3]) << 24);
-        const uintptr_t p = reinterpret_cast<uintptr_t>(base + 4);
-        const int off = static_cast<int>(p & 3u);
-        wp = reinterpret_cast<const uint32_t *>(p - off);
-        wbuf = __ldg(wp) >> (8 * off);
-        wp++;
-        nb = 4 - off;
-        left = C - 4;
+        const uintptr_t p0 = reinterpret_cast<uintptr_t>(base + 4);
+        const uintptr_t pe = reinterpret_cast<uintptr_t>(base + C - 1);  // C >= 8: pe >= p0
+        const int off = static_cast<int>(p0 & 3u);
+        const uint32_t *w0 = reinterpret_cast<const uint32_t *>(p0 - off);
+        const int words = static_cast<int>(((pe & ~uintptr_t(3)) - (p0 - off)) / 4) + 1;
+        const uint32_t lo = __ldg(w0);
+        const uint32_t hi = words > 1 ? __ldg(w0 + 1) : 0u;
+        nxt = words > 2 ? __ldg(w0 + 2) : 0u;
+        buf = static_cast<uint64_t>(lo) | (static_cast<uint64_t>(hi) << 32);
+        pos = 8u * off;
+        wp = w0 + 3;
+        wl = words - 3;
     }
-    // one symbol: returns the 64-bit table entry
-    __device__ __forceinline__ uint2 step(const uint2 *dec, bool &bad) {
+    __device__ __forceinline__ void refill() {
+        const bool r = pos >= 32u;
+        const uint64_t nb = (buf >> 32) | (static_cast<uint64_t>(nxt) << 32);
+        buf = r ? nb : buf;
+        pos = r ? pos - 32u : pos;
+        nxt = r ? ldg_if(wp, wl > 0, 0u) : nxt;
+        wp += r ? 1 : 0;
+        wl -= r ? 1 : 0;
+    }
+    // one symbol (Algorithm 2): returns the 64-bit table entry
+    __device__ __forceinline__ uint2 step(const uint2 *dec) {
         const uint2 e = dec[x & 255u];
         x = (e.x & 0x1ffu) * (x >> 8) + (e.x >> 16);
-        if (x < RANS_L) {
-            if (nb == 0) {
-                // never past the container: a well-formed one holds every byte read
-                wbuf = left > 0 ? __ldg(wp) : 0u;
-                wp++;
-                nb = 4;
-            }
-            if (left == 0) bad = true;
-            x = (x << 8) | (wbuf & 255u);
-            wbuf >>= 8;
-            nb--;
-            left--;
-        }
+        const bool need = x < RANS_L;
+        const uint32_t byte = static_cast<uint32_t>(buf >> pos);
+        x = need ? __byte_perm(byte, x, 0x6540) : x;  // (x << 8) | (byte & 255)
+        pos += need ? 8u : 0u;
         return e;
     }
 };
@@ -111,11 +132,11 @@ struct RecMerge {
 template <int H>
 struct RansSmem {
     uint2 dec_k[256], dec_v[256];
-    float4 qk[H][128];            // rotated query rows of head h's 4 query heads, by channel
-    float qsum[4 * H];            // sum_c q_rot[qh][c]
-    float qmu[4][4 * H];          // sum_c q_rot[qh][c] mu^_w[c] for the item's 4 windows
-    uint16_t vst[RW][128][VST];   // staged value levels (fp16), [channel][token]
-    uint16_t pst[RW][8][VST];     // staged P' (fp16 hi/lo), [column][token]
+    float4 qk[H][128];               // rotated query rows of head h's 4 query heads, by channel
+    float qsum[4 * H];               // sum_c q_rot[qh][c]
+    float qmu[4][4 * H];             // sum_c q_rot[qh][c] mu^_w[c] for the item's 4 windows
+    uint16_t vst[RW][RCH][16][VST];  // staged value levels (fp16) of 16 channels, [chunk][channel][token]
+    uint16_t pst[RW][RCH][8][VST];   // staged P' (fp16 hi/lo), [chunk][column][token]
     RecMerge mg;
 };
 
@@ -160,112 +181,119 @@ __device__ void rans_quant_item(RansSmem<H> &S, const RansAttnArgs &a, int b, lo
     }
     __syncthreads();
     // this lane's 4 tokens (one per chunk) and their decoders
+    // this lane's 4 tokens (one per chunk), their decoders and metadata
     Dec dk[RCH], dv[RCH];
-    bool bad = false;
+    bool bad = false, valid[RCH];
+    float sk[RCH], ok[RCH], sv[RCH], ov[RCH];
+    int wi[RCH];
 #pragma unroll
     for (int ch = 0; ch < RCH; ch++) {
         const long long slot = s0 + 32 * (RCH * warp + ch) + lane;
-        const bool valid = slot < a.n_q;
-        dk[ch].open(a.codes_k + (static_cast<long long>(b) * a.qcap + (valid ? slot : 0)) * a.ck, a.ck, valid);
-        dv[ch].open(a.codes_v + (static_cast<long long>(b) * a.qcap + (valid ? slot : 0)) * a.cv, a.cv, valid);
+        valid[ch] = slot < a.n_q;
+        const long long rs = static_cast<long long>(b) * a.qcap + (valid[ch] ? slot : 0);
+        dk[ch].open(a.codes_k + rs * a.ck, a.ck, valid[ch]);
+        dv[ch].open(a.codes_v + rs * a.cv, a.cv, valid[ch]);
+        sk[ch] = ok[ch] = sv[ch] = ov[ch] = 0.f;
+        if (valid[ch]) {
+            const __half2 mk = reinterpret_cast<const __half2 *>(a.meta_k)[rs];
+            const __half2 mv = reinterpret_cast<const __half2 *>(a.meta_v)[rs];
+            sk[ch] = __low2float(mk);
+            ok[ch] = __high2float(mk);
+            sv[ch] = __low2float(mv);
+            ov[ch] = __high2float(mv);
+        }
+        wi[ch] = static_cast<int>((slot - s0) >> 7);
     }
-    uint16_t(*vst)[VST] = S.vst[warp];
-    uint16_t(*pst)[VST] = S.pst[warp];
+    uint16_t(*vst)[16][VST] = S.vst[warp];
+    uint16_t(*pst)[8][VST] = S.pst[warp];
 #pragma unroll 1
     for (int h = 0; h < H; h++) {
-        float acc[8][4];
+        // keys of head h: 128 symbols of each of the 4 streams, interleaved
+        float dot[RCH][4];
 #pragma unroll
-        for (int mi = 0; mi < 8; mi++) acc[mi][0] = acc[mi][1] = acc[mi][2] = acc[mi][3] = 0.f;
-        float mrun[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-        float lsum[4] = {0.f, 0.f, 0.f, 0.f}, osum[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int ch = 0; ch < RCH; ch++) {
-            const long long slot = s0 + 32 * (RCH * warp + ch) + lane;
-            const bool valid = slot < a.n_q;
-            float dot[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int ch = 0; ch < RCH; ch++) dot[ch][0] = dot[ch][1] = dot[ch][2] = dot[ch][3] = 0.f;
 #pragma unroll 4
-            for (int c = 0; c < 128; c++) {
-                const uint2 ek = dk[ch].step(S.dec_k, bad);
-                const uint2 ev = dv[ch].step(S.dec_v, bad);
-                const float lev = __uint_as_float(ek.y);
-                const float4 q4 = S.qk[h][c];
-                dot[0] = fmaf(q4.x, lev, dot[0]);
-                dot[1] = fmaf(q4.y, lev, dot[1]);
-                dot[2] = fmaf(q4.z, lev, dot[2]);
-                dot[3] = fmaf(q4.w, lev, dot[3]);
-                vst[c][lane] = static_cast<uint16_t>(ev.y);
-            }
-            // Eq. (8) affine terms, log2 units
-            float sk = 0.f, ok = 0.f, sv = 0.f, ov = 0.f;
-            if (valid) {
-                const __half2 mk = reinterpret_cast<const __half2 *>(a.meta_k)[static_cast<long long>(b) * a.qcap + slot];
-                const __half2 mv = reinterpret_cast<const __half2 *>(a.meta_v)[static_cast<long long>(b) * a.qcap + slot];
-                sk = __low2float(mk);
-                ok = __high2float(mk);
-                sv = __low2float(mv);
-                ov = __high2float(mv);
-            }
-            const int wi = static_cast<int>((slot - s0) >> 7);
-            float lg[4], mx[4];
+        for (int c = 0; c < 128; c++) {
+            if ((c & 3) == 0) {
 #pragma unroll
-            for (int gq = 0; gq < 4; gq++) {
-                const int qh = 4 * h + gq;
-                lg[gq] = valid ? a.sm_log2 * (sk * dot[gq] + ok * S.qsum[qh] + S.qmu[wi][qh]) : -INFINITY;
-                mx[gq] = warp_max(lg[gq]);
+                for (int ch = 0; ch < RCH; ch++) dk[ch].refill();
             }
-            // online softmax per query head (warp-uniform running max)
-            float al[4];
+            const float4 q4 = S.qk[h][c];
 #pragma unroll
-            for (int gq = 0; gq < 4; gq++) {
-                al[gq] = 1.f;
-                if (mx[gq] > mrun[gq] + SLACK || (mrun[gq] == -INFINITY && mx[gq] > -INFINITY)) {
-                    al[gq] = mrun[gq] == -INFINITY ? 0.f : ex2(mrun[gq] - mx[gq]);
-                    mrun[gq] = mx[gq];
-                    lsum[gq] *= al[gq];
-                    osum[gq] *= al[gq];
-                }
+            for (int ch = 0; ch < RCH; ch++) {
+                const float lev = __uint_as_float(dk[ch].step(S.dec_k).y);
+                dot[ch][0] = fmaf(q4.x, lev, dot[ch][0]);
+                dot[ch][1] = fmaf(q4.y, lev, dot[ch][1]);
+                dot[ch][2] = fmaf(q4.z, lev, dot[ch][2]);
+                dot[ch][3] = fmaf(q4.w, lev, dot[ch][3]);
             }
-            const float my_al = tig == 0 ? al[0] : (tig == 1 ? al[1] : (tig == 2 ? al[2] : al[3]));
-            if (my_al != 1.f) {
-#pragma unroll
-                for (int mi = 0; mi < 8; mi++)
-#pragma unroll
-                    for (int r = 0; r < 4; r++) acc[mi][r] *= my_al;
-            }
-#pragma unroll
-            for (int gq = 0; gq < 4; gq++) {
-                const float p = valid ? ex2(lg[gq] - mrun[gq]) : 0.f;
-                lsum[gq] += p;
-                osum[gq] = fmaf(p, ov, osum[gq]);
-                const __half hi = __float2half_rn(p * sv);
-                const __half lo = __float2half_rn(p * sv - __half2float(hi));
-                pst[2 * gq][lane] = __half_as_ushort(hi);
-                pst[2 * gq + 1][lane] = __half_as_ushort(lo);
-            }
-            __syncwarp();
-            // P . V: A = V^T (channels x tokens), B = P' (tokens x 8 columns)
-#pragma unroll
-            for (int kt = 0; kt < 2; kt++) {
-                const uint32_t b0 = *reinterpret_cast<const uint32_t *>(&pst[g][16 * kt + 2 * tig]);
-                const uint32_t b1 = *reinterpret_cast<const uint32_t *>(&pst[g][16 * kt + 2 * tig + 8]);
-#pragma unroll
-                for (int mi = 0; mi < 8; mi++) {
-                    const uint32_t a0 = *reinterpret_cast<const uint32_t *>(&vst[16 * mi + g][16 * kt + 2 * tig]);
-                    const uint32_t a1 = *reinterpret_cast<const uint32_t *>(&vst[16 * mi + g + 8][16 * kt + 2 * tig]);
-                    const uint32_t a2 = *reinterpret_cast<const uint32_t *>(&vst[16 * mi + g][16 * kt + 2 * tig + 8]);
-                    const uint32_t a3 =
-                        *reinterpret_cast<const uint32_t *>(&vst[16 * mi + g + 8][16 * kt + 2 * tig + 8]);
-                    mma16816(acc[mi], a0, a1, a2, a3, b0, b1);
-                }
-            }
-            __syncwarp();
         }
-        // warp totals of l and the offset sums; this warp's record per query head
+        // Eq. (8) affine terms (log2 units) and one softmax step over the warp's 128 tokens
+        float mrun[4], lsum[4], osum[4];
 #pragma unroll
         for (int gq = 0; gq < 4; gq++) {
-            lsum[gq] = warp_sum(lsum[gq]);
-            osum[gq] = warp_sum(osum[gq]);
+            const int qh = 4 * h + gq;
+            float lg[RCH], mx = -INFINITY;
+#pragma unroll
+            for (int ch = 0; ch < RCH; ch++) {
+                lg[ch] = valid[ch] ? a.sm_log2 * (sk[ch] * dot[ch][gq] + ok[ch] * S.qsum[qh] + S.qmu[wi[ch]][qh])
+                                   : -INFINITY;
+                mx = fmaxf(mx, lg[ch]);
+            }
+            mx = warp_max(mx);
+            mrun[gq] = mx;
+            float ls = 0.f, os = 0.f;
+#pragma unroll
+            for (int ch = 0; ch < RCH; ch++) {
+                const float p = valid[ch] ? ex2(lg[ch] - mx) : 0.f;
+                ls += p;
+                os = fmaf(p, ov[ch], os);
+                const __half hi = __float2half_rn(p * sv[ch]);
+                const __half lo = __float2half_rn(p * sv[ch] - __half2float(hi));
+                pst[ch][2 * gq][lane] = __half_as_ushort(hi);
+                pst[ch][2 * gq + 1][lane] = __half_as_ushort(lo);
+            }
+            lsum[gq] = warp_sum(ls);
+            osum[gq] = warp_sum(os);
         }
+        __syncwarp();
+        uint32_t bf[RCH][2][2];
+#pragma unroll
+        for (int ch = 0; ch < RCH; ch++)
+#pragma unroll
+            for (int kt = 0; kt < 2; kt++) {
+                bf[ch][kt][0] = *reinterpret_cast<const uint32_t *>(&pst[ch][g][16 * kt + 2 * tig]);
+                bf[ch][kt][1] = *reinterpret_cast<const uint32_t *>(&pst[ch][g][16 * kt + 2 * tig + 8]);
+            }
+        // values of head h, 16 channels at a time: stage the levels, then P . V
+        // (A = V^T: 16 channels x 16 tokens, B = P': 16 tokens x 8 columns)
+        float acc[8][4];
+#pragma unroll
+        for (int mi = 0; mi < 8; mi++) {
+            acc[mi][0] = acc[mi][1] = acc[mi][2] = acc[mi][3] = 0.f;
+#pragma unroll 4
+            for (int cc = 0; cc < 16; cc++) {
+                if ((cc & 3) == 0) {
+#pragma unroll
+                    for (int ch = 0; ch < RCH; ch++) dv[ch].refill();
+                }
+#pragma unroll
+                for (int ch = 0; ch < RCH; ch++) vst[ch][cc][lane] = static_cast<uint16_t>(dv[ch].step(S.dec_v).y);
+            }
+            __syncwarp();
+#pragma unroll
+            for (int ch = 0; ch < RCH; ch++)
+#pragma unroll
+                for (int kt = 0; kt < 2; kt++) {
+                    const uint32_t a0 = *reinterpret_cast<const uint32_t *>(&vst[ch][g][16 * kt + 2 * tig]);
+                    const uint32_t a1 = *reinterpret_cast<const uint32_t *>(&vst[ch][g + 8][16 * kt + 2 * tig]);
+                    const uint32_t a2 = *reinterpret_cast<const uint32_t *>(&vst[ch][g][16 * kt + 2 * tig + 8]);
+                    const uint32_t a3 = *reinterpret_cast<const uint32_t *>(&vst[ch][g + 8][16 * kt + 2 * tig + 8]);
+                    mma16816(acc[mi], a0, a1, a2, a3, bf[ch][kt][0], bf[ch][kt][1]);
+                }
+            __syncwarp();
+        }
+        // this warp's record per query head into the merge area
         const float my_o = tig == 0 ? osum[0] : (tig == 1 ? osum[1] : (tig == 2 ? osum[2] : osum[3]));
 #pragma unroll
         for (int mi = 0; mi < 8; mi++) {
@@ -305,6 +333,9 @@ __device__ void rans_quant_item(RansSmem<H> &S, const RansAttnArgs &a, int b, lo
         }
         __syncthreads();
     }
+    // a well-formed container decodes back to the encoder's initial state
+#pragma unroll
+    for (int ch = 0; ch < RCH; ch++) bad = bad || (valid[ch] && (dk[ch].x != RANS_L || dv[ch].x != RANS_L));
     if (bad) atomicOr(a.status, ST_BOUNDS);
 }
 

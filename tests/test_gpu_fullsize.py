@@ -141,3 +141,46 @@ def test_nuq_full_size_sampled_units():
         assert np.all(np.abs(g - ref) <= _tol(ref, w.out_dtype)), (b, h, float(np.max(np.abs(g - ref))))
     assert np.all(np.isfinite(got_out))
     cache.close()
+
+
+DQ_BATCHES = [0, 31]
+
+
+def test_dquant_full_size_sampled_sequences():
+    """The D-Quant cache of the benchmark (batch 32, 8 KV heads, 16384 bf16
+    tokens, 128 recent; keys 8 levels in 331 bytes, values 6 levels in 231
+    bytes): containers, metadata and window means of two sequences bit for bit,
+    and their 32 query heads' outputs within the attention tolerance."""
+    import torch
+    from quantized_decode_attention_gb300 import KVCache
+    w = W.DQUANT
+    S = w.seq
+    k, v = W.make_kv(w)
+    q = W.make_q(w)
+    cache = KVCache.allocate(cfg_for(w), zero=False)
+    cache.quantize(to_device(k, "bf16"), to_device(v, "bf16"), pos0=0)
+    q_d = to_device(q, "f32")
+    out = torch.empty((w.batch, w.n_q_heads, w.head_dim), dtype=torch.bfloat16, device="cuda")
+    _graph_replay(lambda s: cache.attention(q_d, out, S, stream=s.cuda_stream))
+    cache.check()
+    got_out = out_to_np(out)
+    from helpers import dquant_views
+    got, qcap = dquant_views(w, cache, S)
+    nq = S - w.n_sink
+    w1 = w.with_(batch=1)
+    for b in DQ_BATCHES:
+        kb, vb = k[b:b + 1], v[b:b + 1]
+        dk = OC.quantize_dquant(w1, kb, True, S)
+        dv = OC.quantize_dquant(w1, vb, False, S)
+        assert not dk.flags.any() and not dv.flags.any()
+        assert np.array_equal(got["codes_k"][b, :nq], dk.container[0]), b
+        assert np.array_equal(got["codes_v"][b, :nq], dv.container[0]), b
+        assert np.array_equal(got["meta_k"][b, :nq, 0], dk.s16[0]) and np.array_equal(got["meta_k"][b, :nq, 1], dk.o16[0])
+        assert np.array_equal(got["meta_v"][b, :nq, 0], dv.s16[0]) and np.array_equal(got["meta_v"][b, :nq, 1], dv.o16[0])
+        nw = dk.mean_q.shape[1]
+        assert np.array_equal(got["mean_q"][b, :nw], dk.mean_q[0])
+        assert np.array_equal(got["mean_sc"][b, :nw], dk.mean_sc[0])
+        ref = OC.attention(w1, q[b:b + 1], kb, vb, S, dk, dv)[0]
+        assert np.all(np.abs(got_out[b] - ref) <= _tol(ref, "bf16")), (b, float(np.max(np.abs(got_out[b] - ref))))
+    assert np.all(np.isfinite(got_out))
+    cache.close()
