@@ -56,13 +56,12 @@ __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-// Predicated 32-bit read-only load: returns *p when pred, else dflt (no branch).
-__device__ __forceinline__ uint32_t ldg_if(const uint32_t *p, bool pred, uint32_t dflt) {
-    uint32_t v = dflt;
+// Predicated 32-bit read-only load into v: v = *p when pred, else v is kept.
+// Nothing reads v here, so the load's latency is only paid where v is next used.
+__device__ __forceinline__ void ldg_into_if(uint32_t &v, const uint32_t *p, bool pred) {
     asm("{\n .reg .pred q;\n setp.ne.b32 q, %2, 0;\n @q ld.global.nc.u32 %0, [%1];\n}\n"
         : "+r"(v)
         : "l"(p), "r"(static_cast<int>(pred)));
-    return v;
 }
 
 // One rANS stream being decoded by a lane.  The container bytes after the
@@ -103,12 +102,14 @@ struct Dec {
         wp = w0 + 3;
         wl = words - 3;
     }
+    // Past the container's last word nxt keeps a stale word: a well-formed
+    // stream never consumes those bytes (the final-state check catches one that does).
     __device__ __forceinline__ void refill() {
         const bool r = pos >= 32u;
         const uint64_t nb = (buf >> 32) | (static_cast<uint64_t>(nxt) << 32);
         buf = r ? nb : buf;
         pos = r ? pos - 32u : pos;
-        nxt = r ? ldg_if(wp, wl > 0, 0u) : nxt;
+        ldg_into_if(nxt, wp, r && wl > 0);
         wp += r ? 1 : 0;
         wl -= r ? 1 : 0;
     }
