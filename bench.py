@@ -51,6 +51,7 @@ def parse():
     p.add_argument("--no-cpu", action="store_true")
     p.add_argument("--no-nuq", action="store_true", help="skip the KVQuant NUQ cache measurement")
     p.add_argument("--no-dquant", action="store_true", help="skip the D-Quant cache measurement")
+    p.add_argument("--qwen", default="32768,131072", help="Qwen3-8B-shaped long-context lengths measured")
     return p.parse_args()
 
 
@@ -76,8 +77,10 @@ def algorithmic_bytes(w: W.Workload, bits: int, S: int) -> dict:
     raw = U * n_raw * d * 2 * 2
     q = w.batch * w.n_q_heads * d * 4
     out = w.batch * w.n_q_heads * d * 2
-    total = codes + metab + mean + raw + q + out
-    return {"codes": codes, "meta": metab, "mean": mean, "raw": raw, "q": q, "out": out, "total": total}
+    qcomp = w.n_kv_heads * d * d * 4 if w.rot_k == "dense" else 0   # T^-T for the queries
+    total = codes + metab + mean + raw + q + out + qcomp
+    return {"codes": codes, "meta": metab, "mean": mean, "raw": raw, "q": q, "out": out, "q_comp": qcomp,
+            "total": total}
 
 
 def nuq_algorithmic_bytes(w: W.Workload, S: int) -> dict:
@@ -187,8 +190,13 @@ def setup_caches(w, bits, S, k_dev, v_dev, copies):
     from quantized_decode_attention_gb300 import KVCache, make_config
     cfg = make_config(batch=w.batch, n_kv_heads=w.n_kv_heads, n_q_heads=w.n_q_heads, head_dim=w.head_dim,
                       max_seq=S, kv_dtype=w.kv_dtype, meta_dtype=w.meta_dtype, out_dtype=w.out_dtype, bits=bits,
-                      rot_k=w.rot_k, rot_v=w.rot_v, mean_k=w.mean_k, n_sink=w.n_sink, n_recent=w.n_recent)
+                      rot_k=w.rot_k, rot_v=w.rot_v, mean_k=w.mean_k, clip_k=w.clip, clip_v=w.clip,
+                      n_sink=w.n_sink, n_recent=w.n_recent)
     base = KVCache.allocate(cfg, zero=False)
+    if w.rot_k == "dense":
+        T, Qc = W.dense_transform(w)
+        base.tensors["k_transform"].view(torch.float32).copy_(torch.from_numpy(T).reshape(-1))
+        base.tensors["q_comp"].view(torch.float32).copy_(torch.from_numpy(Qc).reshape(-1))
     base.quantize(k_dev, v_dev, pos0=0)
     base.check()
     caches = [base]
@@ -303,6 +311,23 @@ def run_gpu(args, w, bits, S, k_dev, v_dev, q_dev, knew_dev, vnew_dev, rank):
         c.detach()
     caches[0].close()
     return res
+
+
+def run_qwen_long(args, S, rank):
+    """Qwen3-8B-shaped long-context decode step at S tokens: dense key transform,
+    99.9-percentile clipped 2-bit grid, no 16-bit regions."""
+    import torch
+    w = W.QWEN_LONG.with_(seq=S)
+    k, v = W.make_kv(w)
+    q = W.make_q(w)
+    kn, vn = W.make_new_token(w)
+    dev16 = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).cuda().view(torch.bfloat16)
+    k_dev, v_dev = dev16(k), dev16(v)
+    del k, v
+    r = run_gpu(args, w, w.bits, S, k_dev, v_dev, torch.from_numpy(q).cuda(), dev16(kn), dev16(vn), rank)
+    del k_dev, v_dev
+    torch.cuda.empty_cache()
+    return w, r
 
 
 def run_gpu_nuq(args, w):
@@ -551,6 +576,7 @@ def main():
     del k_dev, v_dev
     nuq = None if args.no_nuq else run_gpu_nuq(args, W.NUQ)
     dqr = None if args.no_dquant else run_gpu_dquant(args, W.DQUANT)
+    qwen = [run_qwen_long(args, int(x), rank) for x in args.qwen.split(",") if x.strip()]
     total_ms = res["total_ms"]
     if world > 1:
         t = torch.tensor([total_ms], device="cuda")
@@ -598,6 +624,15 @@ def main():
                        "n_sink": W.NUQ.n_sink, "outlier_frac": 0.01, "lloyd_iters": 8,
                        "l2": f"{nuq['copies']} cache copies rotated per step (> L2)",
                        "step": "decode attention (prefill-only scheme), CUDA graph over the copies"}}
+    for wq, r in qwen:
+        line["variants"][f"{wq.name}-s{wq.seq}-{wq.bits}bit"] = {
+            "value": round(wq.batch / (r["total_ms"] / args.steps / 1e3), 1),
+            "ms_per_step": round(r["total_ms"] / args.steps, 5),
+            "roofline": roof(r, f"qwen{wq.seq}"), "e2e_tok_s": round(r["e2e_tok_s"], 1),
+            "config": {"batch": wq.batch, "q_heads": wq.n_q_heads, "kv_heads": wq.n_kv_heads,
+                       "head_dim": wq.head_dim, "seq_len": wq.seq, "bits": wq.bits, "clip": wq.clip,
+                       "key_transform": "dense", "l2": f"{r['copies']} cache copies rotated per step (> L2)",
+                       "step": "quantize 1 new token/seq + decode attention, CUDA graph per step"}}
     if dqr is not None:
         D = W.DQUANT
         line["variants"][f"{D.name}-k{D.extra['levels_k']}x{D.extra['container_k']}-v{D.extra['levels_v']}x{D.extra['container_v']}"] = {

@@ -108,7 +108,7 @@ def quantize_tensor(w: W.Workload, x_bits: np.ndarray, is_key: bool, S: int,
             ou = np.zeros(nq, dtype=np.float32)
             xh = np.zeros((nq, d), dtype=np.float32)
             L.or_quantize_unit(xu, n, d, rot, Tp, mode, m_t0, m_t1, mu_u, bits, meta_f16,
-                               float(w.clip), q_t0, cu, su, ou, xh.ctypes.data_as(C.c_void_p))
+                               float(np.float32(w.clip)), q_t0, cu, su, ou, xh.ctypes.data_as(C.c_void_p))
             codes[b, h], s[b, h], o[b, h], xhat[b, h], mu[b, h] = cu, su, ou, xh, mu_u
     return QuantTensor(codes, s, o, mu, xhat)
 

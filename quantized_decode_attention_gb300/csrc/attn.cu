@@ -789,7 +789,7 @@ __device__ __forceinline__ void combine_unit(const AttnArgs &a, const AttnShape 
 // that the loads are in flight before the cache copies.
 template <int V>
 struct QIn {
-    float xq[V], mu[V];
+    float xq[V], mu[V], xt[V];  // xt: the compensated query when it was computed beforehand
 };
 template <int D>
 __device__ __forceinline__ void load_query(const AttnArgs &a, const AttnShape &sh, int u, QIn<D / 32> &in) {
@@ -802,6 +802,7 @@ __device__ __forceinline__ void load_query(const AttnArgs &a, const AttnShape &s
     for (int j = 0; j < V; j++) {
         in.xq[j] = h < sh.G ? __ldg(a.q + qo + j) : 0.f;
         in.mu[j] = a.mean_k ? __ldg(a.mean_k + mo + j) : 0.f;
+        in.xt[j] = a.q_tilde && h < sh.G ? __ldg(a.q_tilde + qo + j) : 0.f;
     }
 }
 
@@ -834,8 +835,12 @@ __device__ __forceinline__ void prep_query(const AttnArgs &a, const AttnShape &s
         fwht_warp<V>(xq);
 #pragma unroll
         for (int j = 0; j < V; j++) xq[j] *= a.hscale;
+    } else if (a.rot_k == DQ_ROT_DENSE && a.q_tilde) {
+        // q~ = T^{-T} q, computed once per call by qcomp_kernel
+#pragma unroll
+        for (int j = 0; j < V; j++) xq[j] = in.xt[j];
     } else if (a.rot_k == DQ_ROT_DENSE) {
-        // q~ = T^{-T} q with the caller's fp32 compensation matrix
+        // q~ = T^{-T} q with the caller's fp32 compensation matrix (no workspace for it)
         __syncwarp();
 #pragma unroll
         for (int j = 0; j < V; j++) S.qscr[h][lane * V + j] = xq[j];
@@ -1234,6 +1239,36 @@ int plan_attention(const Layout &L, AttnArgs &a, int num_sms, long long cap_floa
         if (G < 1) G = 1;
     }
     return attention_partial_floats(L, a) <= cap_floats ? 0 : static_cast<int>(cudaErrorMemoryAllocation);
+}
+
+// q~ = T^{-T} q for every query head (WUSH-KV, Methodology: queries are
+// compensated with the inverse transform): one CTA per (sequence, KV head),
+// thread i computes output channel i of the G query heads from row i of the
+// fp32 compensation matrix.
+template <int D>
+__global__ void __launch_bounds__(D) qcomp_kernel(const float *q, const float *qc, float *qt, int Hkv, int G) {
+    __shared__ float qs[4][D];
+    const int b = blockIdx.x / Hkv, kvh = blockIdx.x % Hkv, i = threadIdx.x;
+    const long long q0 = (static_cast<long long>(b) * Hkv + kvh) * G * D;
+    for (int g = 0; g < G; g++) qs[g][i] = q[q0 + static_cast<long long>(g) * D + i];
+    __syncthreads();
+    const float4 *row = reinterpret_cast<const float4 *>(qc + (static_cast<long long>(kvh) * D + i) * D);
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int k4 = 0; k4 < D / 4; k4++) {
+        const float4 r = __ldg(row + k4);
+#pragma unroll
+        for (int g = 0; g < 4; g++)
+            if (g < G)
+                acc[g] += r.x * qs[g][4 * k4] + r.y * qs[g][4 * k4 + 1] + r.z * qs[g][4 * k4 + 2] + r.w * qs[g][4 * k4 + 3];
+    }
+    for (int g = 0; g < G; g++) qt[q0 + static_cast<long long>(g) * D + i] = acc[g];
+}
+
+int launch_qcomp(const Layout &L, const float *q, const float *qc, float *qt, void *stream) {
+    const unsigned grid = static_cast<unsigned>(L.U);
+    if (L.d == 128) qcomp_kernel<128><<<grid, 128, 0, static_cast<cudaStream_t>(stream)>>>(q, qc, qt, L.Hkv, L.G);
+    else qcomp_kernel<64><<<grid, 64, 0, static_cast<cudaStream_t>(stream)>>>(q, qc, qt, L.Hkv, L.G);
+    return static_cast<int>(cudaGetLastError());
 }
 
 int launch_attention(const Layout &L, const AttnArgs &a, int, void *stream) {

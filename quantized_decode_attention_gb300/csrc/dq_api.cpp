@@ -287,6 +287,8 @@ static dq_status get_ctx(dq_ctx **pctx, const dq_config *cfg, const Layout &L) {
     cudaError_t e4 = cudaSuccess;
     if (L.scheme == DQ_NUQ)
         e4 = cudaMalloc(&c->nuq_bits, static_cast<size_t>(L.U) * L.qcap * (L.d / 32) * sizeof(uint32_t));
+    if (e4 == cudaSuccess && cfg->k.rot == DQ_ROT_DENSE)
+        e4 = cudaMalloc(&c->q_tilde, sizeof(float) * static_cast<size_t>(L.B) * L.Hq * L.d);
     if (L.scheme == DQ_RANS) {
         e4 = cudaMalloc(&c->rans, sizeof(dq::RansDevTables));
         if (e4 == cudaSuccess)
@@ -300,6 +302,7 @@ static dq_status get_ctx(dq_ctx **pctx, const dq_config *cfg, const Layout &L) {
         cudaFree(c->nuq_bits);
         cudaFree(c->rans);
         cudaFree(c->rans_partials);
+        cudaFree(c->q_tilde);
         delete c;
         cudaGetLastError();
         return fail(DQ_ENOMEM, "workspace allocation failed");
@@ -603,6 +606,11 @@ dq_status dq_decode_attention(dq_ctx **ctx, const dq_config *cfg, const dq_kv_bu
     a.raw_k = static_cast<const uint16_t *>(bufs->raw_k);
     a.raw_v = static_cast<const uint16_t *>(bufs->raw_v);
     a.q_comp = cfg->k.rot == DQ_ROT_DENSE ? static_cast<const float *>(bufs->q_comp) : nullptr;
+    if (cfg->k.rot == DQ_ROT_DENSE) {
+        const int eq = dq::launch_qcomp(L, a.q, a.q_comp, c->q_tilde, stream);
+        if (eq != 0) return fail(DQ_ECUDA, "query compensation launch: %s", cudaGetErrorString(static_cast<cudaError_t>(eq)));
+        a.q_tilde = c->q_tilde;
+    }
     a.rot_k = cfg->k.rot;
     a.rot_v = cfg->v.rot;
     a.raw_bf16 = cfg->kv_dtype == DQ_BF16;
@@ -681,6 +689,7 @@ void dq_free(dq_ctx *ctx) {
     cudaFree(ctx->rans);
     cudaFree(ctx->rans_sym);
     cudaFree(ctx->rans_partials);
+    cudaFree(ctx->q_tilde);
     delete ctx;
 }
 

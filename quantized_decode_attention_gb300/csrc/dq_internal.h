@@ -151,6 +151,7 @@ struct AttnArgs {
     const float *mean_k;    // nullptr if no mean
     const uint16_t *raw_k, *raw_v;
     const float *q_comp;    // [Hkv][d][d] T^{-T} or nullptr
+    const float *q_tilde;   // [B][Hq][d] T^{-T} q computed beforehand, or nullptr
     int rot_k, rot_v;
     int raw_bf16;           // raw region dtype: 1 bf16, 0 fp16
     long long seq_len;
@@ -204,6 +205,8 @@ int launch_nuq_key_csr(const Layout &L, const QuantArgs &a, void *stream);
 int nuq_outlier_count(float f, int n);
 int launch_dequant(const Layout &L, const DequantArgs &a, void *stream);
 int launch_attention(const Layout &L, const AttnArgs &a, int num_sms, void *stream);
+// q~ = T^{-T} q of every query head into qt [B][Hq][d] (dense key transforms)
+int launch_qcomp(const Layout &L, const float *q, const float *qc, float *qt, void *stream);
 // Fill the work schedule of `a` (items, grid, partial slots) for a launch on a
 // device with num_sms SMs whose partial workspace holds cap_floats floats.
 int plan_attention(const Layout &L, AttnArgs &a, int num_sms, long long cap_floats);
@@ -225,5 +228,6 @@ struct dq_ctx {
     dq::RansDevTables *rans;  // entropy-coded scheme: symbol models (device)
     uint8_t *rans_sym;   // entropy-coded scheme: symbol scratch of a prefill
     float *rans_partials;  // entropy-coded scheme: attention item records
+    float *q_tilde;      // dense key transform: compensated queries [B][Hq][d]
     size_t rans_sym_cap; // bytes
 };

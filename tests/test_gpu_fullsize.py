@@ -184,3 +184,55 @@ def test_dquant_full_size_sampled_sequences():
         assert np.all(np.abs(got_out[b] - ref) <= _tol(ref, "bf16")), (b, float(np.max(np.abs(got_out[b] - ref))))
     assert np.all(np.isfinite(got_out))
     cache.close()
+
+
+QWEN_UNITS = [(0, 0), (3, 7)]
+
+
+def test_qwen_long_full_size_sampled_units():
+    """The Qwen3-8B-shaped long-context cache (batch 4, 32 query / 8 KV heads,
+    131072 bf16 tokens, dense key transform with compensated queries, 2-bit
+    grid clipped to the 0.1 / 99.9 % quantiles): the new token re-appended at
+    the last position and attention over 131072 tokens from one CUDA graph;
+    two units' records bit for bit and their heads' outputs within tolerance."""
+    import torch
+    from quantized_decode_attention_gb300 import KVCache
+    w = W.QWEN_LONG.with_(seq=131072)
+    S = w.seq
+    k, v = W.make_kv(w)
+    kn, vn = W.make_new_token(w)
+    q = W.make_q(w)
+    T, Qc = W.dense_transform(w)
+    cache = KVCache.allocate(cfg_for(w), zero=False)
+    cache.tensors["k_transform"].view(torch.float32).copy_(torch.from_numpy(T).reshape(-1))
+    cache.tensors["q_comp"].view(torch.float32).copy_(torch.from_numpy(Qc).reshape(-1))
+    cache.quantize(to_device(k, "bf16"), to_device(v, "bf16"), pos0=0)
+    kn_d, vn_d, q_d = to_device(kn, "bf16"), to_device(vn, "bf16"), to_device(q, "f32")
+    out = torch.empty((w.batch, w.n_q_heads, w.head_dim), dtype=torch.bfloat16, device="cuda")
+
+    def step(s):
+        cache.quantize(kn_d, vn_d, pos0=S - 1, stream=s.cuda_stream)
+        cache.attention(q_d, out, S, stream=s.cuda_stream)
+
+    _graph_replay(step)
+    cache.check()
+    got_out = out_to_np(out)
+    got = lib_views(w, cache, S)
+    w1 = w.with_(batch=1, n_kv_heads=1, n_q_heads=w.group)
+    for b, h in QWEN_UNITS:
+        ku = k[b:b + 1, h:h + 1].copy()
+        vu = v[b:b + 1, h:h + 1].copy()
+        ku[:, :, S - 1], vu[:, :, S - 1] = kn[b:b + 1, h:h + 1, 0], vn[b:b + 1, h:h + 1, 0]
+        qk = oracle.quantize_tensor(w1, ku, True, S, T=T[h:h + 1])
+        qv = oracle.quantize_tensor(w1, vu, False, S)
+        exp = expected_buffers(w1, qk, qv, S)
+        assert np.array_equal(got["codes_k"][b, h, :S], exp["codes_k"][0, 0]), (b, h)
+        assert np.array_equal(got["codes_v"][b, h, :S // 2], exp["codes_v"][0, 0, :S // 2]), (b, h)
+        assert np.array_equal(got["meta_k"][b, h, :S], exp["meta_k"][0, 0]), (b, h)
+        assert np.array_equal(got["meta_v"][b, h, :S], exp["meta_v"][0, 0]), (b, h)
+        qu = q[b:b + 1, h * w.group:(h + 1) * w.group]
+        ref = oracle.attention(w1, qu, ku, vu, S, qk, qv, q_comp=Qc[h:h + 1])[0]
+        g = got_out[b, h * w.group:(h + 1) * w.group]
+        assert np.all(np.abs(g - ref) <= _tol(ref, w.out_dtype)), (b, h, float(np.max(np.abs(g - ref))))
+    assert np.all(np.isfinite(got_out))
+    cache.close()

@@ -149,9 +149,11 @@ def make_kv(w: Workload, seq: Optional[int] = None, batch: Optional[int] = None,
         k += mu[None, :, None, :]
         k *= sc[None, :, None, :]
     elif w.k_dist == "cov":
-        L = cov_factor(w, TID_SIGMA_K)
+        L = cov_factor(w, TID_SIGMA_K).astype(np.float32)
         z = _draw(w, TID_K, "normal", shape, salt)
-        k = np.einsum("hij,bhsj->bhsi", L.astype(np.float32), z, optimize=True).astype(np.float32)
+        k = np.empty_like(z)
+        for h in range(w.n_kv_heads):          # k = L z per (sequence, token): a BLAS product per head
+            k[:, h] = z[:, h] @ L[h].T
     else:
         k = _draw(w, TID_K, w.k_dist, shape, salt)
     v = _draw(w, TID_V, w.v_dist, shape, salt)
