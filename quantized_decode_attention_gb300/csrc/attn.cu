@@ -396,8 +396,10 @@ __device__ __forceinline__ float f16v(uint16_t h) { return __half2float(__ushort
 // shared memory, V^[t][c] = lut_v[t][code] from the tokens' tables in the
 // slot ("KVQuant-NUQ" page: dequantize = table lookup).  Outliers keep their
 // fp16 value: a key outlier adds q_c (x - table value) to its logit, a value
-// outlier adds p_t (x - table value) to corr[head][c] (this lane's channels
-// c = g mod 8, kept in the warp state's scale).
+// outlier adds p_t (x - table value) to corr[head][c] (kept in the warp
+// state's scale).  Both side channels are read a whole warp at a time, their
+// loads issued before the key contraction; contributions meet in shared
+// memory (pb holds the logit corrections, then the probabilities).
 template <int D, int BK, int BV>
 __device__ __forceinline__ void process_block_nuq(const uint8_t *kp, const uint8_t *vp, const uint16_t *lvp, int valid,
                                                   const uint32_t (&qb)[D / 16][2], const uint16_t *lutk,
@@ -407,6 +409,21 @@ __device__ __forceinline__ void process_block_nuq(const uint8_t *kp, const uint8
     constexpr int NKS = D / 16, NMT = D / 16, T = 2, LV = 1 << BV, ROWK = D * BK / 8, PAIRV = 2 * D * BV / 8;
     constexpr int NWK = Slice<D, BK>::NW, NWV = Slice<D, BV>::NW;
     const int lane = threadIdx.x & 31, g = lane >> 2, tig = lane & 3;
+    // side-channel loads first: key row starts of this warp's tokens, value outliers of this lane's token
+    const int *rp = a.ol_rowptr_k ? a.ol_rowptr_k + static_cast<long long>(u) * a.rp_stride + s0 : nullptr;
+    int rpv = 0, e_end = 0;
+    if (rp) {  // valid counts every token to the end of the cache; this warp's rows are the first 32
+        const int vr = valid < 32 ? valid : 32;
+        rpv = rp[lane < vr ? lane : vr];
+        e_end = rp[vr];
+    }
+    const int kv = a.k_out_v;
+    const long long tv = static_cast<long long>(u) * sh.qcap + s0 + lane;
+    uint32_t cv0 = 0xffffu, xv0 = 0u;
+    if (kv > 0 && lane < valid) {
+        cv0 = a.ol_col_v[tv * kv];
+        xv0 = a.ol_val_v[tv * kv];
+    }
     const uint16_t *lk = lutk + 2 * tig * LV;  // table rows of this lane's channels 16i + 2tig + 8sub + e
     float sc[T][4];
 #pragma unroll
@@ -434,23 +451,32 @@ __device__ __forceinline__ void process_block_nuq(const uint8_t *kp, const uint8
         const int t = k >> 1, hf = k & 1;
         lg[k] = sm_l2 * (sc[t][2 * hf] + sc[t][2 * hf + 1]);
     }
-    if (a.ol_rowptr_k) {  // key side channel of this lane's tokens, head tig
-        const int *rp = a.ol_rowptr_k + static_cast<long long>(u) * a.rp_stride;
-        const uint16_t *col = a.ol_col_k + static_cast<long long>(u) * a.nnzk_cap;
-        const uint16_t *val = a.ol_val_k + static_cast<long long>(u) * a.nnzk_cap;
+    if (rp) {  // key side channel: one lane per entry of [row start of token 0, end of the last token)
+        pb[0][lane] = pb[1][lane] = pb[2][lane] = pb[3][lane] = 0.f;
+        __syncwarp();
+        const int e_beg = __shfl_sync(FULL, rpv, 0);
+        for (int eb = e_beg; eb < e_end; eb += 32) {
+            const int e = eb + lane;
+            int r = 0;  // the token of entry e: the last row starting at or before it
 #pragma unroll
-        for (int k = 0; k < 2 * T; k++) {
-            const int row = 16 * (k >> 1) + g + 8 * (k & 1);
-            if (row >= valid) continue;
-            const int e1 = rp[s0 + row + 1];
-            float cr = 0.f;
-            for (int e = rp[s0 + row]; e < e1; e++) {
-                const int c = col[e];
-                const uint32_t m = code_in_rec<BK>(kp + row * ROWK, k_idx(c, D), c & 1, D / 16);
-                cr += qf[tig][c] * (f16v(val[e]) - f16v(lutk[c * LV + m]));
+            for (int stp = 16; stp; stp >>= 1) {
+                const int s = __shfl_sync(FULL, rpv, r + stp);
+                if (r + stp < 32 && s <= e) r += stp;
             }
-            lg[k] += sm_l2 * cr;
+            if (e < e_end) {
+                const long long ei = static_cast<long long>(u) * a.nnzk_cap + e;
+                const int c = a.ol_col_k[ei];
+                const float x = f16v(a.ol_val_k[ei]);
+                const uint32_t m = code_in_rec<BK>(kp + r * ROWK, k_idx(c, D), c & 1, D / 16);
+                const float dlt = x - f16v(lutk[c * LV + m]);
+#pragma unroll
+                for (int h = 0; h < 4; h++) atomicAdd(&pb[h][r], qf[h][c] * dlt);
+            }
         }
+        __syncwarp();
+#pragma unroll
+        for (int k = 0; k < 2 * T; k++) lg[k] += sm_l2 * pb[tig][16 * (k >> 1) + g + 8 * (k & 1)];
+        __syncwarp();
     }
     const bool ragged = valid < 32;
     if (ragged) {
@@ -460,7 +486,6 @@ __device__ __forceinline__ void process_block_nuq(const uint8_t *kp, const uint8
     }
     float p[2 * T];
     const float al = st.template update<2 * T>(lg, p);
-    const int kv = a.k_out_v;
     if (kv > 0) {
         if (al != 1.f) {
 #pragma unroll
@@ -493,18 +518,18 @@ __device__ __forceinline__ void process_block_nuq(const uint8_t *kp, const uint8
             mma_f16(st.acc[mi], r[0], r[1], r[2], r[3], b0, b1);
         }
     }
-    if (kv > 0) {  // value side channel: token tt's entries go to the lanes owning channel c
-        const long long tb = static_cast<long long>(u) * sh.qcap + s0;
+    if (kv > 0) {  // value side channel: lane t adds p_t (x - table value) at its outlier channels
         for (int j = 0; j < kv; j++) {
-            const bool in = lane < valid;
-            const uint32_t cm = in ? a.ol_col_v[(tb + lane) * kv + j] : 0xffffu;
-            const uint32_t vm = in ? a.ol_val_v[(tb + lane) * kv + j] : 0u;
-            for (int tt = 0; tt < 32; tt++) {
-                const int c = static_cast<int>(__shfl_sync(FULL, cm, tt));
-                const uint16_t vv = static_cast<uint16_t>(__shfl_sync(FULL, vm, tt));
-                if (c == 0xffff || (c & 7) != g) continue;
-                const uint32_t m = code_in_rec<BV>(vp + (tt >> 1) * PAIRV, v_idx(c, D), tt & 1, D / 8);
-                corr[tig][c] += pb[tig][tt] * (f16v(vv) - f16v(lvp[tt * LV + m]));
+            uint32_t c = cv0, xb = xv0;
+            if (j > 0 && lane < valid) {
+                c = a.ol_col_v[tv * kv + j];
+                xb = a.ol_val_v[tv * kv + j];
+            }
+            if (lane < valid && c != 0xffffu) {
+                const uint32_t m = code_in_rec<BV>(vp + (lane >> 1) * PAIRV, v_idx(static_cast<int>(c), D), lane & 1, D / 8);
+                const float dlt = f16v(static_cast<uint16_t>(xb)) - f16v(lvp[lane * LV + m]);
+#pragma unroll
+                for (int h = 0; h < 4; h++) atomicAdd(&corr[h][c], pb[h][lane] * dlt);
             }
         }
         __syncwarp();
