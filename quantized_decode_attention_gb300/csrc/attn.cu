@@ -1267,32 +1267,38 @@ int plan_attention(const Layout &L, AttnArgs &a, int num_sms, long long cap_floa
 }
 
 // q~ = T^{-T} q for every query head (WUSH-KV, Methodology: queries are
-// compensated with the inverse transform): one CTA per (sequence, KV head),
-// thread i computes output channel i of the G query heads from row i of the
-// fp32 compensation matrix.
+// compensated with the inverse transform).  One warp per (sequence, KV head,
+// 32 output channels); lane i computes output channel 32 blk + i of the G
+// query heads from its row of the fp32 compensation matrix (loads unrolled,
+// so a lane has its whole row in flight at once).
 template <int D>
-__global__ void __launch_bounds__(D) qcomp_kernel(const float *q, const float *qc, float *qt, int Hkv, int G) {
+__global__ void __launch_bounds__(32) qcomp_kernel(const float *q, const float *qc, float *qt, int Hkv, int G) {
     __shared__ float qs[4][D];
-    const int b = blockIdx.x / Hkv, kvh = blockIdx.x % Hkv, i = threadIdx.x;
+    constexpr int NB = D / 32;
+    const int blk = blockIdx.x % NB, bk = blockIdx.x / NB;
+    const int b = bk / Hkv, kvh = bk % Hkv, lane = threadIdx.x, i = 32 * blk + lane;
     const long long q0 = (static_cast<long long>(b) * Hkv + kvh) * G * D;
-    for (int g = 0; g < G; g++) qs[g][i] = q[q0 + static_cast<long long>(g) * D + i];
-    __syncthreads();
+    for (int g = 0; g < G; g++)
+        for (int c = lane; c < D; c += 32) qs[g][c] = q[q0 + static_cast<long long>(g) * D + c];
+    __syncwarp();
     const float4 *row = reinterpret_cast<const float4 *>(qc + (static_cast<long long>(kvh) * D + i) * D);
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
-    for (int k4 = 0; k4 < D / 4; k4++) {
-        const float4 r = __ldg(row + k4);
+    float4 r[D / 4];
 #pragma unroll
-        for (int g = 0; g < 4; g++)
-            if (g < G)
-                acc[g] += r.x * qs[g][4 * k4] + r.y * qs[g][4 * k4 + 1] + r.z * qs[g][4 * k4 + 2] + r.w * qs[g][4 * k4 + 3];
+    for (int k4 = 0; k4 < D / 4; k4++) r[k4] = __ldg(row + k4);
+    for (int g = 0; g < G; g++) {
+        float acc = 0.f;
+#pragma unroll
+        for (int k4 = 0; k4 < D / 4; k4++)
+            acc += r[k4].x * qs[g][4 * k4] + r[k4].y * qs[g][4 * k4 + 1] + r[k4].z * qs[g][4 * k4 + 2] +
+                   r[k4].w * qs[g][4 * k4 + 3];
+        qt[q0 + static_cast<long long>(g) * D + i] = acc;
     }
-    for (int g = 0; g < G; g++) qt[q0 + static_cast<long long>(g) * D + i] = acc[g];
 }
 
 int launch_qcomp(const Layout &L, const float *q, const float *qc, float *qt, void *stream) {
-    const unsigned grid = static_cast<unsigned>(L.U);
-    if (L.d == 128) qcomp_kernel<128><<<grid, 128, 0, static_cast<cudaStream_t>(stream)>>>(q, qc, qt, L.Hkv, L.G);
-    else qcomp_kernel<64><<<grid, 64, 0, static_cast<cudaStream_t>(stream)>>>(q, qc, qt, L.Hkv, L.G);
+    const unsigned grid = static_cast<unsigned>(L.U) * static_cast<unsigned>(L.d / 32);
+    if (L.d == 128) qcomp_kernel<128><<<grid, 32, 0, static_cast<cudaStream_t>(stream)>>>(q, qc, qt, L.Hkv, L.G);
+    else qcomp_kernel<64><<<grid, 32, 0, static_cast<cudaStream_t>(stream)>>>(q, qc, qt, L.Hkv, L.G);
     return static_cast<int>(cudaGetLastError());
 }
 

@@ -425,12 +425,14 @@ __global__ void __launch_bounds__(128) rans_combine_kernel(RansAttnArgs a) {
     const int b = blockIdx.x / a.Hkv, h = blockIdx.x % a.Hkv;
     const int HQ = 4 * a.Hkv, qh = 4 * h + warp;
     const int nqi = a.items_per_b - 1;
-    float M = -INFINITY;
-    for (int i = 0; i < a.items_per_b; i++) {
+    float M = -INFINITY;  // lanes read the records' maxima in parallel
+    for (int i = lane; i < a.items_per_b; i += 32) {
         const float *rec = a.partials + ((static_cast<long long>(b) * a.items_per_b + i) * HQ + qh) * REC;
         if (i < nqi ? i < a.n_qitems : a.n_raw > 0) M = fmaxf(M, rec[128]);
     }
+    M = warp_max(M);
     float L = 0.f, aq[4] = {0.f, 0.f, 0.f, 0.f}, ar[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 4
     for (int i = 0; i < a.items_per_b; i++) {
         const bool used = i < nqi ? i < a.n_qitems : a.n_raw > 0;
         if (!used) continue;
