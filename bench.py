@@ -169,12 +169,24 @@ class Clocks:
                 "reasons": reasons, "samples": len(self.samples)}
 
 
-def traffic_for(kernel_sha: str, bits: int):
+RANS_SRC = os.path.join(ROOT, "quantized_decode_attention_gb300", "csrc", "attn_rans.cu")
+
+
+def src_sha(path: str) -> str:
+    return hashlib.sha256(open(path, "rb").read()).hexdigest()[:16]
+
+
+def traffic_for(kernel_sha: str, bits):
+    """DRAM bytes per attention launch from the committed ncu capture, or None
+    when the kernel source differs from the one captured."""
+    key = bits if isinstance(bits, str) else f"{bits}bit"
+    if key == "dquant":
+        kernel_sha = src_sha(RANS_SRC)
     try:
         with open(TRAFFIC_FILE) as f:
             d = json.load(f)
-        ent = d.get(bits if isinstance(bits, str) else f"{bits}bit")
-        if ent and ent.get("attn_src_sha") == kernel_sha:
+        ent = d.get(key)
+        if ent and ent.get("src_sha", ent.get("attn_src_sha")) == kernel_sha:
             return ent.get("bytes_per_launch")
     except Exception:
         pass
