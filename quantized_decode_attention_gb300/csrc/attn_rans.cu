@@ -125,6 +125,24 @@ struct Dec {
     }
 };
 
+// One symbol of each of N streams, written phase by phase across the streams
+// (table lookups, state updates, byte merges) so their dependent chains
+// interleave.  e[ch] receives stream ch's table entry.
+template <int N>
+__device__ __forceinline__ void step_all(Dec (&d)[N], const uint2 *dec, uint2 (&e)[N]) {
+#pragma unroll
+    for (int ch = 0; ch < N; ch++) e[ch] = dec[d[ch].x & 255u];
+#pragma unroll
+    for (int ch = 0; ch < N; ch++) d[ch].x = (e[ch].x & 0x1ffu) * (d[ch].x >> 8) + (e[ch].x >> 16);
+#pragma unroll
+    for (int ch = 0; ch < N; ch++) {
+        const bool need = d[ch].x < RANS_L;
+        const uint32_t byte = static_cast<uint32_t>(d[ch].buf >> d[ch].pos);
+        d[ch].x = need ? __byte_perm(byte, d[ch].x, 0x6540) : d[ch].x;
+        d[ch].pos += need ? 8u : 0u;
+    }
+}
+
 struct RecMerge {
     float m[RW][4], l[RW][4];
     float acc[RW][4][128];
@@ -220,9 +238,11 @@ __device__ void rans_quant_item(RansSmem<H> &S, const RansAttnArgs &a, int b, lo
                 for (int ch = 0; ch < RCH; ch++) dk[ch].refill();
             }
             const float4 q4 = S.qk[h][c];
+            uint2 ek[RCH];
+            step_all<RCH>(dk, S.dec_k, ek);
 #pragma unroll
             for (int ch = 0; ch < RCH; ch++) {
-                const float lev = __uint_as_float(dk[ch].step(S.dec_k).y);
+                const float lev = __uint_as_float(ek[ch].y);
                 dot[ch][0] = fmaf(q4.x, lev, dot[ch][0]);
                 dot[ch][1] = fmaf(q4.y, lev, dot[ch][1]);
                 dot[ch][2] = fmaf(q4.z, lev, dot[ch][2]);
@@ -278,8 +298,10 @@ __device__ void rans_quant_item(RansSmem<H> &S, const RansAttnArgs &a, int b, lo
 #pragma unroll
                     for (int ch = 0; ch < RCH; ch++) dv[ch].refill();
                 }
+                uint2 ev[RCH];
+                step_all<RCH>(dv, S.dec_v, ev);
 #pragma unroll
-                for (int ch = 0; ch < RCH; ch++) vst[ch][cc][lane] = static_cast<uint16_t>(dv[ch].step(S.dec_v).y);
+                for (int ch = 0; ch < RCH; ch++) vst[ch][cc][lane] = static_cast<uint16_t>(ev[ch].y);
             }
             __syncwarp();
 #pragma unroll
