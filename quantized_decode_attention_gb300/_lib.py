@@ -166,9 +166,14 @@ class KVCache:
         return cls(cfg, tensors, C.c_void_p())
 
     def buffers(self) -> Buffers:
-        b = Buffers()
-        for n in BUFFER_NAMES:
-            setattr(b, n, _ptr(self.tensors.get(n)))
+        """The C struct of buffer pointers, built once: the tensors never move
+        (their contents are written in place)."""
+        b = getattr(self, "_bufs", None)
+        if b is None:
+            b = Buffers()
+            for n in BUFFER_NAMES:
+                setattr(b, n, _ptr(self.tensors.get(n)))
+            self._bufs = b
         return b
 
     def quantize(self, k, v, pos0: int = 0, stream=None):
