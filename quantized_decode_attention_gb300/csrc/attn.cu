@@ -425,13 +425,14 @@ __device__ __forceinline__ void process_block_nuq(const uint8_t *kp, const uint8
         xv0 = a.ol_val_v[tv * kv];
     }
     const uint16_t *lk = lutk + 2 * tig * LV;  // table rows of this lane's channels 16i + 2tig + 8sub + e
-    float sc[T][4];
-#pragma unroll
+    // the two key tiles run through one copy of the (large, table-lookup) code
+    float lg[2 * T];
+#pragma unroll 1
     for (int t = 0; t < T; t++) {
         uint32_t k0[NWK], k1[NWK];
         load_k_slice<D, BK>(kp + (16 * t + g) * ROWK, tig, k0);
         load_k_slice<D, BK>(kp + (16 * t + g + 8) * ROWK, tig, k1);
-        sc[t][0] = sc[t][1] = sc[t][2] = sc[t][3] = 0.f;
+        float s4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int i = 0; i < NKS; i++) {
             uint32_t m0, m1, r[4];
@@ -442,14 +443,16 @@ __device__ __forceinline__ void process_block_nuq(const uint8_t *kp, const uint8
                 const uint16_t *l0 = lk + (16 * i + 8 * (q >> 1)) * LV;
                 r[q] = pack2(l0[m0], l0[LV + m1]);
             }
-            mma_f16(sc[t], r[0], r[1], r[2], r[3], qb[i][0], qb[i][1]);
+            mma_f16(s4, r[0], r[1], r[2], r[3], qb[i][0], qb[i][1]);
         }
-    }
-    float lg[2 * T];
-#pragma unroll
-    for (int k = 0; k < 2 * T; k++) {
-        const int t = k >> 1, hf = k & 1;
-        lg[k] = sm_l2 * (sc[t][2 * hf] + sc[t][2 * hf + 1]);
+        const float l0 = sm_l2 * (s4[0] + s4[1]), l1 = sm_l2 * (s4[2] + s4[3]);
+        if (t == 0) {
+            lg[0] = l0;
+            lg[1] = l1;
+        } else {
+            lg[2] = l0;
+            lg[3] = l1;
+        }
     }
     if (rp) {  // key side channel: one lane per entry of [row start of token 0, end of the last token)
         pb[0][lane] = pb[1][lane] = pb[2][lane] = pb[3][lane] = 0.f;
@@ -496,10 +499,10 @@ __device__ __forceinline__ void process_block_nuq(const uint8_t *kp, const uint8
         __syncwarp();
     }
     // P . V per tile: A = V^T (channels x tokens) from the tokens' tables
-#pragma unroll
+#pragma unroll 1
     for (int t = 0; t < T; t++) {
-        const uint32_t b0 = movmatrix_t(hilo_f16(p[2 * t]));
-        const uint32_t b1 = movmatrix_t(hilo_f16(p[2 * t + 1]));
+        const uint32_t b0 = movmatrix_t(hilo_f16(t == 0 ? p[0] : p[2]));
+        const uint32_t b1 = movmatrix_t(hilo_f16(t == 0 ? p[1] : p[3]));
         uint32_t v0[NWV], v1[NWV];
         load_v_slice<D, BV>(vp + (8 * t + tig) * PAIRV, g, v0);
         load_v_slice<D, BV>(vp + (8 * t + tig + 4) * PAIRV, g, v1);
