@@ -154,9 +154,11 @@ struct RansSmem {
     float4 qk[H][128];               // rotated query rows of head h's 4 query heads, by channel
     float qsum[4 * H];               // sum_c q_rot[qh][c]
     float qmu[4][4 * H];             // sum_c q_rot[qh][c] mu^_w[c] for the item's 4 windows
-    uint16_t vst[RW][RCH][16][VST];  // staged value levels (fp16) of 16 channels, [chunk][channel][token]
     uint16_t pst[RW][RCH][8][VST];   // staged P' (fp16 hi/lo), [chunk][column][token]
-    RecMerge mg;
+    union {                          // the merge follows the head's value pass
+        uint16_t vst[RW][RCH][16][VST];  // staged value levels (fp16) of 16 channels, [chunk][channel][token]
+        RecMerge mg;
+    };
 };
 
 // ---------------------------------------------------------------------------
@@ -316,7 +318,9 @@ __device__ void rans_quant_item(RansSmem<H> &S, const RansAttnArgs &a, int b, lo
                 }
             __syncwarp();
         }
-        // this warp's record per query head into the merge area
+        // this warp's record per query head into the merge area (which overlays
+        // the staging tiles: every warp must be done with its value pass)
+        __syncthreads();
         const float my_o = tig == 0 ? osum[0] : (tig == 1 ? osum[1] : (tig == 2 ? osum[2] : osum[3]));
 #pragma unroll
         for (int mi = 0; mi < 8; mi++) {
@@ -415,7 +419,7 @@ __device__ void rans_raw_item(RansSmem<H> &S, const RansAttnArgs &a, int b) {
 }
 
 template <int H>
-__global__ void __launch_bounds__(128) attn_rans_kernel(RansAttnArgs a, const RansDevTables *tabs) {
+__global__ void __launch_bounds__(128, 4) attn_rans_kernel(RansAttnArgs a, const RansDevTables *tabs) {
     extern __shared__ __align__(16) unsigned char smraw[];
     RansSmem<H> &S = *reinterpret_cast<RansSmem<H> *>(smraw);
     const int b = blockIdx.x / a.items_per_b, it = blockIdx.x % a.items_per_b;
