@@ -83,6 +83,30 @@ def algorithmic_bytes(w: W.Workload, bits: int, S: int) -> dict:
             "total": total}
 
 
+def reduce_max(x: float) -> float:
+    """The maximum of x over the ranks of the process group (x itself without one)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return x
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate(total_ms: float, steps: int, batch_per_rank: int, world: int):
+    """(ms per step, whole-job tokens/s): the slowest rank's time, every rank's tokens."""
+    ms_step = reduce_max(total_ms) / steps
+    return ms_step, batch_per_rank * world / (ms_step / 1e3)
+
+
+def barrier():
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
 def nuq_algorithmic_bytes(w: W.Workload, S: int) -> dict:
     """Bytes one non-uniform decode-attention call must move: key and value
     codes, per-token value tables, per-channel key tables, the outlier side
@@ -257,8 +281,7 @@ def run_gpu(args, w, bits, S, k_dev, v_dev, q_dev, knew_dev, vnew_dev, rank):
         for i in range(args.warmup):
             singles[i % nc].replay()
         stream.synchronize()
-        if torch.distributed.is_initialized():
-            torch.distributed.barrier()
+        barrier()
         torch.cuda.synchronize()
         t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         with Clocks(torch.cuda.current_device()) as clk:
@@ -269,6 +292,8 @@ def run_gpu(args, w, bits, S, k_dev, v_dev, q_dev, knew_dev, vnew_dev, rank):
                 singles[i].replay()
             t1.record(stream)
             stream.synchronize()
+        torch.cuda.synchronize()
+        barrier()
         total_ms = t0.elapsed_time(t1)
         # duration of the attention kernel alone: the stream first sleeps so the
         # host can enqueue [event, attention, event] triples ahead of the GPU,
@@ -594,13 +619,7 @@ def main():
     nuq = None if args.no_nuq else run_gpu_nuq(args, W.NUQ)
     dqr = None if args.no_dquant else run_gpu_dquant(args, W.DQUANT)
     qwen = [run_qwen_long(args, int(x), rank) for x in args.qwen.split(",") if x.strip()]
-    total_ms = res["total_ms"]
-    if world > 1:
-        t = torch.tensor([total_ms], device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
-    ms_step = total_ms / args.steps
-    value = w.batch * world / (ms_step / 1e3)
+    ms_step, value = aggregate(res["total_ms"], args.steps, w.batch, world)
     peak, peak_kind = peaks()
     sha = hashlib.sha256(open(ATTN_SRC, "rb").read()).hexdigest()[:16]
 
