@@ -52,6 +52,7 @@ def parse():
     p.add_argument("--no-nuq", action="store_true", help="skip the KVQuant NUQ cache measurement")
     p.add_argument("--no-dquant", action="store_true", help="skip the D-Quant cache measurement")
     p.add_argument("--qwen", default="32768,131072", help="Qwen3-8B-shaped long-context lengths measured")
+    p.add_argument("--no-bf16", action="store_true", help="skip the unquantized 16-bit cache context entry")
     return p.parse_args()
 
 
@@ -649,10 +650,18 @@ def main():
             continue
         r = run_gpu(args, w.with_(bits=vb), vb, S, k_dev, v_dev, q_dev, kn_dev, vn_dev, rank)
         variants[f"{vb}bit"] = r
+    # context: the same decode step over an unquantized bf16 cache (every token a
+    # 16-bit slot of the library's own 16-bit path), the pages' "vs BF16" point
+    bf16 = None
+    if not args.no_bf16:
+        wb = W.LLAMA.with_(n_sink=S, n_recent=0, mean_k=False, rot_k="none", rot_v="none")
+        bf16 = run_gpu(args, wb, wb.bits, S, k_dev, v_dev, q_dev, kn_dev, vn_dev, rank)
+        torch.cuda.empty_cache()
     del k_dev, v_dev
     nuq = None if args.no_nuq else run_gpu_nuq(args, W.NUQ)
     dqr = None if args.no_dquant else run_gpu_dquant(args, W.DQUANT)
     qwen = [run_qwen_long(args, int(x), rank) for x in args.qwen.split(",") if x.strip()]
+
     ms_step, value = aggregate(res["total_ms"], args.steps, w.batch, world)
     peak, peak_kind = peaks()
     sha = hashlib.sha256(open(ATTN_SRC, "rb").read()).hexdigest()[:16]
@@ -703,6 +712,13 @@ def main():
                        "head_dim": wq.head_dim, "seq_len": wq.seq, "bits": wq.bits, "clip": wq.clip,
                        "key_transform": "dense", "l2": f"{r['copies']} cache copies rotated per step (> L2)",
                        "step": "quantize 1 new token/seq + decode attention, CUDA graph per step"}}
+    if bf16 is not None:
+        line["variants"]["llama3-8b-decode-bf16-cache"] = {
+            "value": round(w.batch / (bf16["total_ms"] / args.steps / 1e3), 1),
+            "ms_per_step": round(bf16["total_ms"] / args.steps, 5),
+            "roofline": roof(bf16, "bf16"), "e2e_tok_s": round(bf16["e2e_tok_s"], 1),
+            "config": {"batch": w.batch, "seq_len": S, "cache": "bf16, unquantized (all tokens 16-bit slots)",
+                       "role": "context: the same step without quantization, through the library's 16-bit path"}}
     if dqr is not None:
         D = W.DQUANT
         line["variants"][f"{D.name}-k{D.extra['levels_k']}x{D.extra['container_k']}-v{D.extra['levels_v']}x{D.extra['container_v']}"] = {

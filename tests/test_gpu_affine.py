@@ -174,3 +174,26 @@ def test_nonfinite_input_is_reported():
     assert e.value.name == "DQ_ENONFINITE"
     cache.check()  # cleared
     cache.close()
+
+
+def test_unquantized_16bit_cache():
+    """Every token a 16-bit slot (n_sink = the whole sequence): the cache holds the
+    inputs as given and attention is exact to fp32 rounding."""
+    import torch
+    from quantized_decode_attention_gb300 import KVCache
+    w = small(W.LLAMA, batch=2, n_kv_heads=2, n_q_heads=8, seq=300, n_sink=300, n_recent=0)
+    k, v = W.make_kv(w)
+    q = W.make_q(w)
+    cache = KVCache.allocate(cfg_for(w, out_dtype="f32"))
+    cache.quantize(to_device(k, "bf16"), to_device(v, "bf16"))
+    rcap = -(-300 // 16) * 16
+    raw_k = cache.tensors["raw_k"].cpu().numpy().view(np.uint16).reshape(w.batch, w.n_kv_heads, rcap, w.head_dim)
+    assert np.array_equal(raw_k[:, :, :300], k)
+    out = torch.empty((w.batch, w.n_q_heads, w.head_dim), dtype=torch.float32, device="cuda")
+    cache.attention(to_device(q, "f32"), out, 300)
+    cache.check()
+    qk = oracle.quantize_tensor(w, k, True, 300)
+    qv = oracle.quantize_tensor(w, v, False, 300)
+    ref = oracle.attention(w, q, k, v, 300, qk, qv)
+    assert np.abs(out_to_np(out) - ref).max() <= TOL
+    cache.close()
