@@ -188,9 +188,15 @@ dq_status dq_kv_sizes(const dq_config *cfg, size_t bytes[DQ_NUM_BUFFERS]);
  * The dense key transform reads bufs->k_transform.
  * DQ_NUQ is prefill only (pos0 == 0; appends give DQ_EUNSUPPORTED) and needs
  * max_seq - n_sink <= 8192: the key tables are fitted over every quantized
- * token of the prefill.  DQ_RANS is prefill only as well (the windowed key
- * mean is taken over each window's tokens); a stream whose cheapest coding
- * still exceeds its container latches DQ_EINFEASIBLE (see dq_check).
+ * token of the prefill.  DQ_RANS (D-Quant Sec. 4.2, windowed key mean): a
+ * prefill encodes every token t >= n_sink, its last 128-slot window's mean
+ * taken over the tokens it has; an append (pos0 > 0) keeps its tokens in the
+ * 16-bit recent window only and, for each 128-slot window that it completes,
+ * re-encodes the whole window (mean, fit, containers), reading the window's
+ * older tokens from the recent window.  Appends therefore need n_recent >= 128
+ * and a 16-bit kv_dtype (else DQ_EUNSUPPORTED), and must follow one another
+ * without gaps.  A stream whose cheapest coding still exceeds its container
+ * latches DQ_EINFEASIBLE (see dq_check).
  * Errors: DQ_EINVAL, DQ_EALIGN, DQ_EUNSUPPORTED, DQ_ENOMEM, DQ_ECUDA (launch).
  */
 dq_status dq_quantize_kv(dq_ctx **ctx, const dq_config *cfg, const dq_kv_buffers *bufs,

@@ -383,13 +383,34 @@ static dq_status quantize_nuq(dq_ctx *c, const dq_config *cfg, const Layout &L, 
     return ok();
 }
 
-// Entropy-coded scheme, prefill only ("D-Quant" page, Sec. 4.2: the keys'
-// windowed mean needs its window's tokens; decode-time block flushes from the
-// recent window are not built).
+// Entropy-coded scheme ("D-Quant" page, Sec. 4.2).  A prefill from position 0
+// encodes every slot after the sinks, its last window's key mean taken over the
+// tokens it has.  An append keeps its tokens in the 16-bit recent window and
+// flushes each 128-slot window that it completes: the window's key mean, the
+// Drift fit and the rANS containers of all its slots, older tokens read from the
+// recent window.  That needs the window's oldest token still there (n_recent of
+// at least 128) and exact 16-bit copies (a 16-bit kv dtype).  The flush runs
+// before this call's tokens are copied into the recent window.
 static dq_status quantize_rans(dq_ctx *c, const dq_config *cfg, const Layout &L, const dq_kv_buffers *bufs,
                                const void *k, const void *v, long long pos0, long long n_tok, void *stream) {
-    if (pos0 != 0)
-        return fail(DQ_EUNSUPPORTED, "entropy-coded scheme: only a prefill from position 0 is built (no appends)");
+    const long long S = pos0 + n_tok, ns = L.n_sink;
+    long long slot0 = 0, n_fit = 0;
+    if (pos0 == 0) {
+        n_fit = n_tok > ns ? n_tok - ns : 0;
+    } else {
+        if (L.n_recent < 128)
+            return fail(DQ_EUNSUPPORTED, "entropy-coded appends need n_recent >= 128 (has %d)", L.n_recent);
+        if (cfg->kv_dtype == DQ_F32)
+            return fail(DQ_EUNSUPPORTED, "entropy-coded appends need a 16-bit kv dtype");
+        const long long s_lo = (pos0 > ns ? pos0 : ns) - ns, s_hi = S - ns - 1;  // this call's slots
+        if (s_hi >= s_lo) {
+            const long long wa = s_lo / 128, wb = s_hi >= 127 ? (s_hi - 127) / 128 : -1;
+            if (wb >= wa) {
+                slot0 = 128 * wa;
+                n_fit = 128 * (wb - wa + 1);
+            }
+        }
+    }
     dq::RansQuantArgs a{};
     a.in_dtype = cfg->kv_dtype;
     a.B = L.B;
@@ -398,14 +419,24 @@ static dq_status quantize_rans(dq_ctx *c, const dq_config *cfg, const Layout &L,
     a.n_tok = n_tok;
     a.n_sink = L.n_sink;
     a.n_recent = L.n_recent;
-    a.n_fit = static_cast<int>(n_tok > L.n_sink ? n_tok - L.n_sink : 0);
+    a.pos0 = pos0;
+    a.slot0 = slot0;
+    a.n_fit = static_cast<int>(n_fit);
     a.hscale = static_cast<float>(1.0 / std::sqrt(128.0));
     a.n_win = (a.n_fit + 127) / 128;
     a.qcap = L.qcap;
     a.wcap = L.wcap;
     a.rcap = L.rcap;
     a.mean_rec = L.mean_rec;
+    a.raw_bf16 = cfg->kv_dtype == DQ_BF16;
     a.status = c->status;
+    // this call's tokens that stay 16-bit: sinks, and those among the latest n_recent
+    const long long sink_end = S < ns ? S : ns;
+    a.raw_ns = static_cast<int>(sink_end > pos0 ? sink_end - pos0 : 0);
+    long long r0 = S - L.n_recent;
+    if (r0 < pos0) r0 = pos0;
+    if (r0 < ns) r0 = ns;
+    a.raw_nr = static_cast<int>(S > r0 ? S - r0 : 0);
     const size_t need = static_cast<size_t>(L.B) * a.n_fit * L.n_stream;
     if (need > c->rans_sym_cap) {
         cudaFree(c->rans_sym);
@@ -419,7 +450,7 @@ static dq_status quantize_rans(dq_ctx *c, const dq_config *cfg, const Layout &L,
     }
     a.sym = c->rans_sym;
     int e;
-    for (int which = 0; which < 2; which++) {
+    for (int which = 0; which < 2 && a.n_fit > 0; which++) {
         const dq_tensor_cfg &t = which == 0 ? cfg->k : cfg->v;
         a.x = which == 0 ? k : v;
         a.is_key = which == 0;
@@ -429,14 +460,19 @@ static dq_status quantize_rans(dq_ctx *c, const dq_config *cfg, const Layout &L,
         a.meta = which == 0 ? bufs->meta_k : bufs->meta_v;
         a.mean = which == 0 && t.mean ? static_cast<uint8_t *>(bufs->mean_k) : nullptr;
         const dq::RansTable *tb = which == 0 ? &c->rans->k : &c->rans->v;
-        if ((e = dq::launch_rans_raw(a, stream)) != 0)
-            return fail(DQ_ECUDA, "raw copy launch: %s", cudaGetErrorString(static_cast<cudaError_t>(e)));
         if (a.mean && (e = dq::launch_rans_mean(a, stream)) != 0)
             return fail(DQ_ECUDA, "window mean launch: %s", cudaGetErrorString(static_cast<cudaError_t>(e)));
         if ((e = dq::launch_rans_drift(a, tb, c->rans->F, t.levels, stream)) != 0)
             return fail(DQ_ECUDA, "drift launch: %s", cudaGetErrorString(static_cast<cudaError_t>(e)));
         if ((e = dq::launch_rans_encode(a, tb, t.container_bytes, stream)) != 0)
             return fail(DQ_ECUDA, "rANS encode launch: %s", cudaGetErrorString(static_cast<cudaError_t>(e)));
+    }
+    for (int which = 0; which < 2 && a.raw_ns + a.raw_nr > 0; which++) {
+        a.x = which == 0 ? k : v;
+        a.is_key = which == 0;
+        a.raw = static_cast<uint16_t *>(which == 0 ? bufs->raw_k : bufs->raw_v);
+        if ((e = dq::launch_rans_raw(a, stream)) != 0)
+            return fail(DQ_ECUDA, "raw copy launch: %s", cudaGetErrorString(static_cast<cudaError_t>(e)));
     }
     return ok();
 }

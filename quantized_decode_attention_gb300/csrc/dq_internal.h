@@ -78,6 +78,12 @@ struct RansQuantArgs {
     void *meta;             // [B][qcap] (s, o) fp16
     uint16_t *raw;          // [U][rcap][128] or [U][rcap/2][128][2]
     unsigned *status;
+    // appends (block flush): tokens [pos0, pos0 + n_tok) are this call's input; the
+    // quantized slots [slot0, slot0 + n_fit) are (re)encoded, their tokens read from
+    // the input or, when older, from the 16-bit recent ring (raw, kv dtype raw_bf16)
+    long long pos0, slot0;
+    int raw_bf16;
+    int raw_ns, raw_nr;     // this call's tokens copied as sinks / into the recent ring
 };
 int launch_rans_mean(const RansQuantArgs &a, void *stream);
 int launch_rans_drift(const RansQuantArgs &a, const RansTable *tb, const float *F, int M, void *stream);

@@ -114,6 +114,28 @@ namespace {
 
 constexpr uint32_t RANS_L = 1u << 23;
 
+// Channels 4 lane .. 4 lane + 3 of KV head h of the token in quantized slot
+// `slot` of sequence b: from this call's input when the token is one of its
+// tokens, else from the 16-bit recent ring (an older token of a block flush).
+__device__ __forceinline__ void load_tok4(const RansQuantArgs &a, int b, int h, long long slot, int lane,
+                                          float (&r)[4]) {
+    const long long t = a.n_sink + slot;
+    if (t >= a.pos0) {
+        const long long base = ((static_cast<long long>(b) * a.Hkv + h) * a.n_tok + (t - a.pos0)) * 128 + 4 * lane;
+#pragma unroll
+        for (int j = 0; j < 4; j++) r[j] = ld_in(a.x, base + j, a.in_dtype);
+        return;
+    }
+    const long long rs = a.n_sink + t % a.n_recent, u = static_cast<long long>(b) * a.Hkv + h;
+#pragma unroll
+    for (int j = 0; j < 4; j++) {
+        const int c = 4 * lane + j;
+        const long long off = a.is_key ? (u * a.rcap + rs) * 128 + c : ((u * (a.rcap / 2) + rs / 2) * 128 + c) * 2 + (rs & 1);
+        const uint16_t bits = a.raw[off];
+        r[j] = a.raw_bf16 ? __uint_as_float(static_cast<uint32_t>(bits) << 16) : __half2float(__ushort_as_half(bits));
+    }
+}
+
 // ---------------------------------------------------------------------------
 // Windowed key mean: one CTA per (sequence, window of 128 quantized slots),
 // one warp per KV head.  Lane l holds channels 4l..4l+3 of its head; every
@@ -123,14 +145,12 @@ __global__ void __launch_bounds__(256) rans_mean_kernel(RansQuantArgs a) {
     __shared__ float wmax[8];
     const int b = blockIdx.x / a.n_win, w = blockIdx.x % a.n_win;
     const int h = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const long long t0 = a.n_sink + 128LL * w;
-    const long long t1 = min(t0 + 128, a.n_sink + static_cast<long long>(a.n_fit));
+    const long long s0 = a.slot0 + 128LL * w;
+    const long long s1 = min(s0 + 128, a.slot0 + static_cast<long long>(a.n_fit));
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
-    for (long long t = t0; t < t1; t++) {
-        const long long base = ((static_cast<long long>(b) * a.Hkv + h) * a.n_tok + t) * 128 + 4 * lane;
+    for (long long sl = s0; sl < s1; sl++) {
         float x[4];
-#pragma unroll
-        for (int j = 0; j < 4; j++) x[j] = ld_in(a.x, base + j, a.in_dtype);
+        load_tok4(a, b, h, sl, lane, x);
         if (a.rot) {
             fwht_warp<4>(x);
 #pragma unroll
@@ -139,11 +159,11 @@ __global__ void __launch_bounds__(256) rans_mean_kernel(RansQuantArgs a) {
 #pragma unroll
         for (int j = 0; j < 4; j++) acc[j] = __fadd_rn(acc[j], x[j]);
     }
-    const float cnt = static_cast<float>(t1 - t0);
+    const float cnt = static_cast<float>(s1 - s0);
     float mu[4], am = 0.f;
 #pragma unroll
     for (int j = 0; j < 4; j++) {
-        mu[j] = t1 > t0 ? __fdiv_rn(acc[j], cnt) : 0.f;
+        mu[j] = s1 > s0 ? __fdiv_rn(acc[j], cnt) : 0.f;
         am = fmaxf(am, fabsf(mu[j]));
     }
     am = warp_max(am);
@@ -157,7 +177,7 @@ __global__ void __launch_bounds__(256) rans_mean_kernel(RansQuantArgs a) {
     __syncthreads();
     const __half sc16 = __float2half_rn(__fdiv_rn(wmax[0], 127.0f));
     const float sc = __half2float(sc16);
-    uint8_t *rec = a.mean + (static_cast<long long>(b) * a.wcap + w) * a.mean_rec;
+    uint8_t *rec = a.mean + (static_cast<long long>(b) * a.wcap + a.slot0 / 128 + w) * a.mean_rec;
     uint32_t packed = 0;
 #pragma unroll
     for (int j = 0; j < 4; j++) {
@@ -312,20 +332,17 @@ __global__ void __launch_bounds__(128) rans_drift_kernel(RansQuantArgs a, const 
     const long long gw = static_cast<long long>(blockIdx.x) * 4 + warp;
     if (gw >= static_cast<long long>(a.B) * a.n_fit) return;
     const int b = static_cast<int>(gw / a.n_fit);
-    const long long slot = gw % a.n_fit, t = a.n_sink + slot;
+    const long long slot = a.slot0 + gw % a.n_fit;
     const int M = tb.M;
     float *xs = stage[warp][0], *mx = stage[warp][1];
     bool finite = true;
     float lo = INFINITY, hi = -INFINITY;
 #pragma unroll 1
     for (int h = 0; h < H; h++) {
-        const long long base = ((static_cast<long long>(b) * H + h) * a.n_tok + t) * 128 + 4 * lane;
         float r[4];
+        load_tok4(a, b, h, slot, lane, r);
 #pragma unroll
-        for (int j = 0; j < 4; j++) {
-            r[j] = ld_in(a.x, base + j, a.in_dtype);
-            finite = finite && isfinite(r[j]);
-        }
+        for (int j = 0; j < 4; j++) finite = finite && isfinite(r[j]);
         if (a.rot) {
             fwht_warp<4>(r);
 #pragma unroll
@@ -393,11 +410,11 @@ __global__ void __launch_bounds__(32) rans_encode_kernel(RansQuantArgs a, const 
     __syncthreads();
     const int C = tb.C, N = a.n;
     const int b = blockIdx.y;
-    const long long slot0 = 32LL * blockIdx.x, slot = slot0 + threadIdx.x;
+    const long long rel0 = 32LL * blockIdx.x, rel = rel0 + threadIdx.x;  // within the flushed range
     uint8_t *mine = cont + threadIdx.x * C;
     for (int i = 0; i < C; i++) mine[i] = 0;
-    if (slot < a.n_fit) {
-        const uint8_t *sym = a.sym + (static_cast<long long>(b) * a.n_fit + slot) * N;
+    if (rel < a.n_fit) {
+        const uint8_t *sym = a.sym + (static_cast<long long>(b) * a.n_fit + rel) * N;
         uint32_t x = RANS_L;
         int pushed = 0;
         bool over = false;
@@ -431,13 +448,14 @@ __global__ void __launch_bounds__(32) rans_encode_kernel(RansQuantArgs a, const 
     }
     __syncthreads();
     // 32 containers are 32 * C bytes, a multiple of 16, at a 16-byte aligned offset
-    uint4 *dst = reinterpret_cast<uint4 *>(a.codes + (static_cast<long long>(b) * a.qcap + slot0) * C);
+    uint4 *dst = reinterpret_cast<uint4 *>(a.codes + (static_cast<long long>(b) * a.qcap + a.slot0 + rel0) * C);
     const uint4 *src = reinterpret_cast<const uint4 *>(cont);
     for (int i = threadIdx.x; i < 2 * C; i += 32) dst[i] = src[i];
 }
 
-// 16-bit regions: sinks and the latest n_recent tokens of the prefill.  One
-// warp per (unit, token) of those sets; lanes copy 4 channels each.
+// 16-bit regions: this call's sinks (raw_ns tokens from pos0) and its tokens
+// among the latest n_recent of the sequence (raw_nr tokens ending at pos0 +
+// n_tok).  One warp per (unit, token) of those sets; lanes copy 4 channels each.
 __global__ void __launch_bounds__(128) rans_raw_kernel(RansQuantArgs a, int n_sel) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const long long gw = static_cast<long long>(blockIdx.x) * 4 + warp;
@@ -445,17 +463,16 @@ __global__ void __launch_bounds__(128) rans_raw_kernel(RansQuantArgs a, int n_se
     if (gw >= U * n_sel) return;
     const long long u = gw / n_sel;
     const int i = static_cast<int>(gw % n_sel);
-    const int ns = min(a.n_sink, static_cast<int>(a.n_tok));
     long long t;
     int slot;
-    if (i < ns) {
-        t = i;
-        slot = i;
+    if (i < a.raw_ns) {
+        t = a.pos0 + i;
+        slot = static_cast<int>(t);
     } else {
-        t = a.n_tok - (n_sel - ns) + (i - ns);
+        t = a.pos0 + a.n_tok - a.raw_nr + (i - a.raw_ns);
         slot = a.n_sink + static_cast<int>(t % a.n_recent);
     }
-    const long long base = (u * a.n_tok + t) * 128;
+    const long long base = (u * a.n_tok + (t - a.pos0)) * 128;
     const long long ub = u * a.rcap * 128;
 #pragma unroll
     for (int j = 0; j < 4; j++) {
@@ -514,10 +531,7 @@ int launch_rans_encode(const RansQuantArgs &a, const RansTable *tb, int C, void 
 }
 
 int launch_rans_raw(const RansQuantArgs &a, void *stream) {
-    const int ns = static_cast<int>(a.n_tok < a.n_sink ? a.n_tok : a.n_sink);
-    long long nr = a.n_recent;
-    if (nr > a.n_tok - ns) nr = a.n_tok - ns;
-    const int n_sel = ns + static_cast<int>(nr);
+    const int n_sel = a.raw_ns + a.raw_nr;
     const long long warps = static_cast<long long>(a.B) * a.Hkv * n_sel;
     if (warps == 0) return 0;
     rans_raw_kernel<<<static_cast<unsigned>((warps + 3) / 4), 128, 0, static_cast<cudaStream_t>(stream)>>>(a, n_sel);

@@ -74,10 +74,75 @@ def test_dquant_prefill_is_bit_exact(name):
     cache.close()
 
 
-def test_dquant_append_is_refused():
+# Appends keep their tokens in the 16-bit recent window and flush each 128-slot
+# window that they complete.  The prefill leaves its last window partial; the
+# appends then complete windows one token at a time and several at once, one
+# batch starting inside a window whose older tokens sit in the recent window.
+APPEND = dq(batch=2, n_kv_heads=2, n_q_heads=8, seq=575, n_sink=4, n_recent=128, out_dtype="f32",
+            extra={"container_k": 83, "container_v": 58})
+APPEND_STEPS = [200] + [1] * 70 + [300, 5]
+
+
+def _check_windows(w, cache, k, v, S, S_cap):
+    """Every complete window up to length S equals the oracle's encoding of S tokens."""
+    got, _ = dquant_views(w, cache, S_cap)
+    dk = OC.quantize_dquant(w, k[:, :, :S], True, S)
+    dv = OC.quantize_dquant(w, v[:, :, :S], False, S)
+    assert not dk.flags.any() and not dv.flags.any()
+    nw = (S - w.n_sink) // 128
+    nq = 128 * nw
+    assert nw > 0
+    assert np.array_equal(got["codes_k"][:, :nq], dk.container[:, :nq])
+    assert np.array_equal(got["codes_v"][:, :nq], dv.container[:, :nq])
+    assert np.array_equal(got["meta_k"][:, :nq, 0], dk.s16[:, :nq])
+    assert np.array_equal(got["meta_k"][:, :nq, 1], dk.o16[:, :nq])
+    assert np.array_equal(got["meta_v"][:, :nq, 0], dv.s16[:, :nq])
+    assert np.array_equal(got["meta_v"][:, :nq, 1], dv.o16[:, :nq])
+    assert np.array_equal(got["mean_q"][:, :nw], dk.mean_q[:, :nw])
+    assert np.array_equal(got["mean_sc"][:, :nw], dk.mean_sc[:, :nw])
+    for slot, bits in OC.raw_regions(w, k[:, :, :S], S).items():
+        assert np.array_equal(got["raw_k"][:, :, slot], bits), slot
+    for slot, bits in OC.raw_regions(w, v[:, :, :S], S).items():
+        assert np.array_equal(got["raw_v"][:, :, slot // 2, :, slot & 1], bits), slot
+    return dk, dv
+
+
+def test_dquant_appends_flush_complete_windows():
+    import torch
+    from quantized_decode_attention_gb300 import KVCache
+    from helpers import out_to_np
+    w = APPEND
+    S_cap = w.seq
+    k, v = W.make_kv(w)
+    q = W.make_q(w)
+    cache = KVCache.allocate(cfg_for(w))
+    out = torch.empty((w.batch, w.n_q_heads, w.head_dim), dtype=torch.float32, device="cuda")
+    qd = to_device(q, "f32")
+    pos = 0
+    for n in APPEND_STEPS:
+        cache.quantize(to_device(k[:, :, pos:pos + n], w.kv_dtype), to_device(v[:, :, pos:pos + n], w.kv_dtype),
+                       pos0=pos)
+        pos += n
+        if pos in (270, 570, 575):
+            torch.cuda.synchronize()
+            cache.check()
+            dk, dv = _check_windows(w, cache, k, v, pos, S_cap)
+            cache.attention(qd, out, pos)
+            torch.cuda.synchronize()
+            cache.check()
+            got = out_to_np(out)
+            ref = OC.attention(w, q, k[:, :, :pos], v[:, :, :pos], pos, dk, dv)
+            err = np.abs(got - ref)
+            assert np.all(err <= _tol(ref, "f32")), (pos, float(err.max()))
+    assert pos == w.seq
+    cache.close()
+
+
+@pytest.mark.parametrize("why", ["short-recent", "f32-input"])
+def test_dquant_append_is_refused(why):
     import torch
     from quantized_decode_attention_gb300 import DQError, KVCache
-    w = CASES["dq-h2"]
+    w = CASES["dq-h2"] if why == "short-recent" else APPEND.with_(kv_dtype="f32", seq=300)
     k, v = W.make_kv(w)
     cache = KVCache.allocate(cfg_for(w, max_seq=w.seq + 8))
     cache.quantize(to_device(k, w.kv_dtype), to_device(v, w.kv_dtype))
