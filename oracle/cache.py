@@ -24,7 +24,7 @@ import numpy as np
 
 import workloads as W
 
-from . import lib, pack_k_row, pack_v_token
+from . import lib, nuq_assign, outlier_count, pack_k_row, pack_v_token
 
 _ROT = {"none": 0, "hadamard": 1, "dense": 2}
 
@@ -158,6 +158,64 @@ def quantize_nuq(w: W.Workload, x_bits: np.ndarray, is_key: bool, S: int) -> Nuq
         tab = np.take_along_axis(levels[:, :, :, None, :], codes[..., None].astype(np.int64), axis=-1)[..., 0]
     xhat = np.where(out, val16.view(np.float16).astype(np.float32), tab).astype(np.float32)
     return NuqTensor(codes, lut, out, val16, xhat)
+
+
+def nuq_key_thresholds(w: W.Workload, x_bits: np.ndarray, P: int) -> np.ndarray:
+    """Per-channel key outlier thresholds frozen at a prefill of P tokens, fp32 [B, H, d].
+
+    "KVQuant-NUQ" page, Dense-and-Sparse outlier isolation: a decode key column
+    has one sample, so it is screened against a threshold fixed at prefill.
+    Reading: the threshold of a channel is the magnitude of its k-th largest
+    |x| over the prefill's quantized tokens [n_sink, P), k the prefill's rank
+    count, i.e. the smallest magnitude the prefill sent to the side channel;
+    +inf when k = 0 (no decode outliers)."""
+    x = _f32_input(x_bits, w.kv_dtype)[:, :, w.n_sink:P]
+    k = outlier_count(w.extra.get("outlier_frac", 0.01), x.shape[2])
+    B, H, _, d = x.shape
+    if k == 0:
+        return np.full((B, H, d), np.inf, dtype=np.float32)
+    mags = -np.sort(-np.abs(x), axis=2)            # descending along tokens
+    return np.ascontiguousarray(mags[:, :, k - 1, :], dtype=np.float32)
+
+
+def quantize_nuq_stream(w: W.Workload, x_bits: np.ndarray, is_key: bool, P: int, S: int,
+                        nnz_cap: int | None = None) -> NuqTensor:
+    """Tokens [n_sink, S) of a cache filled by a prefill of P tokens (P > n_sink)
+    and then appends of tokens [P, S).
+
+    "KVQuant-NUQ" page, Quantization axes and Dense-and-Sparse outlier isolation:
+    values are fitted per token, so an appended value is quantized exactly as at
+    prefill.  Keys keep the per-channel tables of the prefill; an appended key
+    takes the nearest level of its channel's table and is an outlier when
+    |x| >= the channel's frozen threshold (nuq_key_thresholds).  The key side
+    channel holds nnz_cap entries per (sequence, head), filled in token order and
+    channel order; an outlier that finds it full is not stored and keeps its level."""
+    if not is_key:
+        return quantize_nuq(w, x_bits, False, S)
+    pre = quantize_nuq(w, x_bits, True, P)
+    B, H, _, d = x_bits.shape
+    thr = nuq_key_thresholds(w, x_bits, P)
+    x = _f32_input(x_bits, w.kv_dtype)[:, :, P:S]
+    nd = x.shape[2]
+    codes = np.zeros((B, H, nd, d), dtype=np.uint8)
+    for b in range(B):
+        for h in range(H):
+            for c in range(d):
+                codes[b, h, :, c] = nuq_assign(np.ascontiguousarray(x[b, h, :, c]), pre.lut[b, h, c])
+    out = np.abs(x) >= thr[:, :, None, :]
+    if nnz_cap is not None:
+        for b in range(B):
+            for h in range(H):
+                room = nnz_cap - int(pre.outlier[b, h].sum())
+                flat = out[b, h].reshape(-1)             # token-major, channels ascending
+                idx = np.flatnonzero(flat)
+                flat[idx[max(room, 0):]] = False
+    val16 = x.astype(np.float16).view(np.uint16)
+    levels = pre.lut.view(np.float16).astype(np.float32)
+    tab = np.take_along_axis(levels[:, :, None, :, :], codes[..., None].astype(np.int64), axis=-1)[..., 0]
+    xhat = np.where(out, val16.view(np.float16).astype(np.float32), tab).astype(np.float32)
+    return NuqTensor(np.concatenate([pre.codes, codes], 2), pre.lut, np.concatenate([pre.outlier, out], 2),
+                     np.concatenate([pre.val16, val16], 2), np.concatenate([pre.xhat, xhat], 2))
 
 
 def nuq_key_outliers_csr(nt: NuqTensor, qcap: int, nnz_cap: int):
@@ -384,6 +442,7 @@ def _attn(L, q, K, V, sm_scale):
 
 
 __all__ = ["QuantTensor", "quantize_tensor", "NuqTensor", "quantize_nuq", "nuq_key_outliers_csr",
+           "nuq_key_thresholds", "quantize_nuq_stream",
            "DqTensor", "dq_tables", "quantize_dquant", "dquant_dequant_f64",
            "nuq_value_outliers", "pack_k", "pack_v", "meta_f16_bits", "raw_regions",
            "attention", "raw16_bits", "raw16_to_f64", "raw_dtype"]

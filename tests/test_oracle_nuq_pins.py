@@ -141,3 +141,90 @@ def test_codes_are_the_nearest_fp16_level():
     dist = np.abs(x[:, None] - lev[None, :])           # fp32, as the definition
     want = np.argmin(dist, axis=1)                     # first minimum = lower index on ties
     assert np.array_equal(codes, want)
+
+
+# ---- decode-time keys ("KVQuant-NUQ" page, Dense-and-Sparse outlier isolation:
+# decode keys against the per-channel threshold frozen at prefill) ----------------
+
+def _nuq_w(S, d=64, n_sink=1, frac=0.05):
+    import workloads as W
+    return W.NUQ.with_(batch=1, n_kv_heads=2, n_q_heads=8, head_dim=d, seq=S, kv_dtype="f32", n_sink=n_sink,
+                       extra={"lloyd_iters": 8, "outlier_frac": frac})
+
+
+def test_frozen_threshold_is_the_kth_magnitude():
+    from oracle import cache as OC
+    rng = np.random.default_rng(7)
+    P, d = 101, 64
+    w = _nuq_w(P, d)
+    x = rng.standard_normal((1, 2, P, d)).astype(np.float32)
+    thr = OC.nuq_key_thresholds(w, x, P)
+    k = oracle.outlier_count(0.05, P - 1)
+    assert k == 5
+    for h in range(2):
+        for c in range(d):
+            col = [abs(float(v)) for v in x[0, h, 1:P, c]]
+            assert sum(1 for m in col if m >= thr[0, h, c]) == k
+            assert float(thr[0, h, c]) == sorted(col, reverse=True)[k - 1]
+    # no prefill outliers: nothing is an outlier at decode either
+    assert np.all(np.isinf(OC.nuq_key_thresholds(_nuq_w(P, d, frac=0.0), x, P)))
+
+
+def test_reappended_prefill_tokens_reproduce_the_prefill():
+    # a decode copy of a prefill key gets the prefill's code, and the threshold
+    # test picks exactly the prefill's rank outliers (distinct magnitudes)
+    from oracle import cache as OC
+    rng = np.random.default_rng(8)
+    P, d, ns = 90, 64, 1
+    S = P + (P - ns)
+    w = _nuq_w(S, d, n_sink=ns)
+    x = np.zeros((1, 2, S, d), dtype=np.float32)
+    x[:, :, :P] = rng.standard_normal((1, 2, P, d))
+    x[:, :, P:] = x[:, :, ns:P]
+    nt = OC.quantize_nuq_stream(w, x, True, P, S)
+    nq = P - ns
+    assert nt.outlier[:, :, :nq].sum() == 2 * d * oracle.outlier_count(0.05, nq)
+    assert np.array_equal(nt.codes[:, :, nq:], nt.codes[:, :, :nq])
+    assert np.array_equal(nt.outlier[:, :, nq:], nt.outlier[:, :, :nq])
+    assert np.array_equal(nt.xhat[:, :, nq:], nt.xhat[:, :, :nq])
+
+
+def test_key_side_channel_cap_drops_the_latest_entries():
+    from oracle import cache as OC
+    rng = np.random.default_rng(9)
+    P, d, S = 60, 64, 100
+    w = _nuq_w(S, d)
+    x = (rng.standard_normal((1, 2, S, d)) * 1.5).astype(np.float32)
+    free = OC.quantize_nuq_stream(w, x, True, P, S)
+    n_pre = int(free.outlier[0, 0, :P - 1].sum())
+    n_dec = int(free.outlier[0, 0, P - 1:].sum())
+    assert n_dec > 10
+    cap = n_pre + n_dec - 7
+    capped = OC.quantize_nuq_stream(w, x, True, P, S, nnz_cap=cap)
+    assert int(capped.outlier[0, 0].sum()) == cap
+    # the 7 dropped are the last 7 decode outliers in token-major, channel order
+    t, c = np.nonzero(free.outlier[0, 0, P - 1:])
+    dropped = set(zip(t[-7:].tolist(), c[-7:].tolist()))
+    t2, c2 = np.nonzero(free.outlier[0, 0, P - 1:] & ~capped.outlier[0, 0, P - 1:])
+    assert set(zip(t2.tolist(), c2.tolist())) == dropped
+    # a dropped outlier keeps the level of its code
+    lev = capped.lut[0, 0].view(np.float16).astype(np.float32)
+    for (ti, ci) in dropped:
+        assert capped.xhat[0, 0, P - 1 + ti, ci] == lev[ci, capped.codes[0, 0, P - 1 + ti, ci]]
+    # a cap below the prefill's own entries stores no decode outlier
+    none = OC.quantize_nuq_stream(w, x, True, P, S, nnz_cap=n_pre - 1)
+    assert not none.outlier[:, :, P - 1:].any()
+
+
+def test_value_tokens_are_fitted_independently():
+    # per-token value tables: a token's table and codes do not depend on the others
+    from oracle import cache as OC
+    rng = np.random.default_rng(10)
+    S, d = 12, 64
+    w = _nuq_w(S, d)
+    x = rng.standard_normal((1, 2, S, d)).astype(np.float32)
+    full = OC.quantize_nuq_stream(w, x, False, 5, S)
+    for t in (1, 6, 11):
+        one = OC.quantize_nuq(w, np.ascontiguousarray(x[:, :, [0, t]]), False, 2)
+        assert np.array_equal(one.lut[:, :, 0], full.lut[:, :, t - 1])
+        assert np.array_equal(one.codes[:, :, 0], full.codes[:, :, t - 1])
