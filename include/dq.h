@@ -122,12 +122,16 @@ typedef struct {
  * Non-uniform scheme (DQ_NUQ on both tensors; "KVQuant-NUQ", How it works:
  * Lloyd-Max levels, keys per channel, values per token, Dense-and-Sparse
  * outliers).  Codes keep the record layout above but index fp16 tables of
- * L = 2^bits levels; meta_k, meta_v, mean_k and ol_rowptr_v are unused:
+ * L = 2^bits levels; meta_v, mean_k and ol_rowptr_v are unused:
+ * meta_k      [U][head_dim]       fp32 key outlier threshold of each channel,
+ *                                 frozen at prefill (the magnitude of its kk-th
+ *                                 rank outlier, +inf when kk = 0); present when
+ *                                 kk > 0
  * lut_k       [U][head_dim][L]    fp16 levels of each key channel
  * lut_v       [U][Qcap][L]        fp16 levels of each value token (by slot)
  * ol_rowptr_k [U][Qcap+4]         int32: key outliers of slot p are entries
  *                                 [rowptr[p], rowptr[p+1]); rowptr[p] for p
- *                                 >= the fitted token count holds the total
+ *                                 >= the quantized token count holds the total
  * ol_col_k    [U][NNZk]           uint16 channel of each key outlier, channel
  *                                 order within a slot
  * ol_val_k    [U][NNZk]           its exact fp16 value
@@ -136,7 +140,8 @@ typedef struct {
  * ol_val_v    [U][Qcap][kv]       its exact fp16 value
  * with kk = floor(k.outlier_frac * (max_seq - n_sink) + 0.5) outliers per key
  * channel, kv = floor(v.outlier_frac * head_dim + 0.5) per value token and
- * NNZk = round_up(head_dim * kk, 8).  A code of an outlier element is its
+ * NNZk = round_up(2 * head_dim * kk, 8) (the prefill's bound twice: decode
+ * keys add entries too).  A code of an outlier element is its
  * nearest level like any other; attention replaces the table value by the
  * stored one.
  *
@@ -186,9 +191,14 @@ dq_status dq_kv_sizes(const dq_config *cfg, size_t bytes[DQ_NUM_BUFFERS]);
  * sinks and the latest n_recent tokens (of length pos0 + n_tok) also to their
  * raw slots.  Requires pos0 + n_tok <= max_seq.
  * The dense key transform reads bufs->k_transform.
- * DQ_NUQ is prefill only (pos0 == 0; appends give DQ_EUNSUPPORTED) and needs
- * max_seq - n_sink <= 8192: the key tables are fitted over every quantized
- * token of the prefill.  DQ_RANS (D-Quant Sec. 4.2, windowed key mean): a
+ * DQ_NUQ ("KVQuant-NUQ", Quantization axes) needs max_seq - n_sink <= 8192:
+ * a prefill fits the key tables over every quantized token it has and freezes
+ * them with each channel's outlier threshold.  An append (pos0 > n_sink, after
+ * such a prefill; else DQ_EUNSUPPORTED) codes its keys against the frozen
+ * tables, appends each element with |x| >= its channel's threshold to the key
+ * side channel, and fits each value token as a prefill does.  Entries that
+ * find the side channel full are not stored (the element keeps its level) and
+ * dq_check reports DQ_EINFEASIBLE.  DQ_RANS (D-Quant Sec. 4.2, windowed key mean): a
  * prefill encodes every token t >= n_sink, its last 128-slot window's mean
  * taken over the tokens it has; an append (pos0 > 0) keeps its tokens in the
  * 16-bit recent window only and, for each 128-slot window that it completes,
@@ -251,7 +261,8 @@ dq_status dq_rans_model(const dq_config *cfg, int which, int *levels, int f[16],
 /*
  * Synchronize `stream`, then return and clear the device-side status latched
  * by earlier calls on this context (DQ_OK, DQ_ENONFINITE, DQ_ETIMEOUT,
- * DQ_EINFEASIBLE for a stream over its container, DQ_EINVAL for a container
+ * DQ_EINFEASIBLE for a stream over its container or a full NUQ key side
+ * channel, DQ_EINVAL for a container
  * that asked for more bytes than it holds), or
  * DQ_ECUDA if the stream reports an error.  ctx may be NULL (returns DQ_OK).
  */

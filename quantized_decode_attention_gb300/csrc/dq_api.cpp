@@ -182,13 +182,14 @@ dq_status make_layout(const dq_config *cfg, Layout *L) {
     const bool nuq = l.scheme == DQ_NUQ;
     if (nuq) {
         l.k_out_cap = dq::nuq_outlier_count(c.k.outlier_frac, c.max_seq - c.n_sink);
-        l.nnzk_cap = round_up(static_cast<long long>(d) * l.k_out_cap, 8);
+        l.nnzk_cap = round_up(2LL * static_cast<long long>(d) * l.k_out_cap, 8);  // room for decode keys
         l.k_out_v = dq::nuq_outlier_count(c.v.outlier_frac, c.head_dim);
         l.rp_stride = l.qcap + 4;
     }
     l.sz[0] = U * l.qcap * l.rowK;                          // codes_k
     l.sz[1] = U * (l.qcap / 2) * l.pairV;                   // codes_v
-    l.sz[2] = nuq ? 0 : U * l.qcap * 2 * l.meta_bytes;      // meta_k
+    l.sz[2] = nuq ? (l.k_out_cap > 0 ? U * d * 4 : 0)      // meta_k; NUQ: frozen key outlier thresholds
+                  : U * l.qcap * 2 * l.meta_bytes;
     l.sz[3] = nuq ? 0 : U * l.qcap * 2 * l.meta_bytes;      // meta_v
     l.sz[4] = c.k.mean ? U * d * 4 : 0;                     // mean_k
     l.sz[5] = nuq ? U * d * l.levels * 2 : 0;               // lut_k
@@ -330,22 +331,28 @@ static dq_status get_ctx(dq_ctx **pctx, const dq_config *cfg, const Layout &L) {
     return DQ_OK;
 }
 
-// Non-uniform scheme, prefill only ("KVQuant-NUQ" page, Quantization axes: key
-// tables are fit at prefill and frozen; appending decode tokens needs the
-// frozen per-channel outlier threshold, which is not built).
+// Non-uniform scheme ("KVQuant-NUQ" page, Quantization axes; Dense-and-Sparse
+// outlier isolation).  A prefill (pos0 == 0) fits the key tables per channel
+// over its quantized tokens and freezes them with each channel's outlier
+// threshold; an append (pos0 > n_sink, after such a prefill) codes its keys
+// against the frozen tables, sends |x| >= threshold to the side channel while
+// it has room, and fits each value token as the prefill does.
 static dq_status quantize_nuq(dq_ctx *c, const dq_config *cfg, const Layout &L, const dq_kv_buffers *bufs,
                               const void *k, const void *v, long long pos0, long long n_tok, void *stream) {
-    if (pos0 != 0)
-        return fail(DQ_EUNSUPPORTED, "non-uniform scheme: only a prefill from position 0 is built (no appends)");
+    if (pos0 != 0 && pos0 <= L.n_sink)
+        return fail(DQ_EUNSUPPORTED, "non-uniform scheme: appends need a prefill that quantized a token (pos0 > n_sink)");
     const cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const bool append = pos0 > 0;
     dq::QuantArgs a{};
     a.in_dtype = cfg->kv_dtype;
-    a.pos0 = 0;
+    a.pos0 = pos0;
     a.n_tok = n_tok;
-    a.seq_after = n_tok;
+    a.seq_after = pos0 + n_tok;
     a.bits = cfg->k.bits;
     a.status = c->status;
-    a.n_fit = static_cast<int>(n_tok > L.n_sink ? n_tok - L.n_sink : 0);
+    a.n_fit = append ? 0 : static_cast<int>(n_tok > L.n_sink ? n_tok - L.n_sink : 0);
+    a.slot_lo = append ? pos0 - L.n_sink : 0;
+    a.n_slots = append ? static_cast<int>(n_tok) : a.n_fit;
     int e;
     // values: per-token tables, codes and side channel; raw copies
     a.x = v;
@@ -359,7 +366,8 @@ static dq_status quantize_nuq(dq_ctx *c, const dq_config *cfg, const Layout &L, 
     a.iters = cfg->v.lloyd_iters;
     if ((e = dq::launch_nuq_values(L, a, stream)) != 0)
         return fail(DQ_ECUDA, "value quantize launch: %s", cudaGetErrorString(static_cast<cudaError_t>(e)));
-    // keys: per-channel tables and outlier bitmap, then codes, then side channel
+    // keys: per-channel tables, thresholds and outlier bitmap (prefill), codes
+    // (and, for an append, the bitmap by threshold), then the side channel
     a.x = k;
     a.is_key = 1;
     a.codes = static_cast<uint8_t *>(bufs->codes_k);
@@ -369,13 +377,16 @@ static dq_status quantize_nuq(dq_ctx *c, const dq_config *cfg, const Layout &L, 
     a.ol_rowptr = static_cast<int *>(bufs->ol_rowptr_k);
     a.ol_col = static_cast<uint16_t *>(bufs->ol_col_k);
     a.ol_val = static_cast<uint16_t *>(bufs->ol_val_k);
+    a.thr = L.k_out_cap > 0 ? static_cast<float *>(bufs->meta_k) : nullptr;
     a.k_out = dq::nuq_outlier_count(cfg->k.outlier_frac, a.n_fit);
     a.iters = cfg->k.lloyd_iters;
-    if (cudaMemsetAsync(c->nuq_bits, 0, static_cast<size_t>(L.U) * L.qcap * (L.d / 32) * sizeof(uint32_t), st) !=
-        cudaSuccess)
-        return fail(DQ_ECUDA, "clearing the key outlier bitmap failed");
-    if (a.n_fit > 0 && (e = dq::launch_nuq_key_fit(L, a, stream)) != 0)
-        return fail(DQ_ECUDA, "key fit launch: %s", cudaGetErrorString(static_cast<cudaError_t>(e)));
+    if (!append) {
+        if (cudaMemsetAsync(c->nuq_bits, 0, static_cast<size_t>(L.U) * L.qcap * (L.d / 32) * sizeof(uint32_t), st) !=
+            cudaSuccess)
+            return fail(DQ_ECUDA, "clearing the key outlier bitmap failed");
+        if (a.n_fit > 0 && (e = dq::launch_nuq_key_fit(L, a, stream)) != 0)
+            return fail(DQ_ECUDA, "key fit launch: %s", cudaGetErrorString(static_cast<cudaError_t>(e)));
+    }
     if ((e = dq::launch_nuq_key_codes(L, a, stream)) != 0)
         return fail(DQ_ECUDA, "key quantize launch: %s", cudaGetErrorString(static_cast<cudaError_t>(e)));
     if (L.k_out_cap > 0 && (e = dq::launch_nuq_key_csr(L, a, stream)) != 0)
@@ -711,6 +722,8 @@ dq_status dq_check(dq_ctx *ctx, void *stream) {
     if (st && cudaMemset(ctx->status, 0, sizeof st) != cudaSuccess) return fail(DQ_ECUDA, "status clear failed");
     if (st & dq::ST_TIMEOUT) return fail(DQ_ETIMEOUT, "a bounded device wait ran out");
     if (st & dq::ST_INFEASIBLE) return fail(DQ_EINFEASIBLE, "a stream did not fit its container");
+    if (st & dq::ST_SIDE_FULL)
+        return fail(DQ_EINFEASIBLE, "the key outlier side channel is full: later decode-key outliers keep their level");
     if (st & dq::ST_BOUNDS) return fail(DQ_EINVAL, "a container asked for more bytes than it holds (corrupt cache)");
     if (st & dq::ST_NONFINITE) return fail(DQ_ENONFINITE, "non-finite K/V input");
     return ok();

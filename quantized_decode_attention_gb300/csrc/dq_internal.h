@@ -9,7 +9,7 @@
 namespace dq {
 
 // Status bits latched on the device (ctx->status word).
-enum : unsigned { ST_NONFINITE = 1u, ST_TIMEOUT = 2u, ST_BOUNDS = 4u, ST_INFEASIBLE = 8u };
+enum : unsigned { ST_NONFINITE = 1u, ST_TIMEOUT = 2u, ST_BOUNDS = 4u, ST_INFEASIBLE = 8u, ST_SIDE_FULL = 16u };
 
 // Sizes and strides derived from a config (all in bytes unless noted).
 struct Layout {
@@ -26,7 +26,7 @@ struct Layout {
     int scheme;          // dq_scheme of both tensors
     int levels;          // 2^bits table entries
     int k_out_cap;       // key outliers per channel at the longest prefill
-    long long nnzk_cap;  // key side-channel entries per unit (multiple of 8)
+    long long nnzk_cap;  // key side-channel entries per unit (multiple of 8): twice the longest prefill's
     int k_out_v;         // value outliers per token
     long long rp_stride; // ints per unit of the key row pointers (qcap + 4)
     // entropy-coded scheme (scheme == DQ_RANS): one stream per token and tensor
@@ -146,6 +146,9 @@ struct QuantArgs {
     int k_out;              // outliers per vector (keys: per channel at this prefill)
     int iters;              // Lloyd sweeps
     int n_fit;              // keys: quantized tokens in the prefill
+    float *thr;             // keys: [U][d] outlier thresholds frozen at prefill (fp32 magnitudes)
+    long long slot_lo;      // first quantized slot written by this call
+    int n_slots;            // quantized slots written by this call
 };
 
 struct AttnArgs {

@@ -1,4 +1,4 @@
-// Non-uniform (Lloyd-Max) KV-cache quantizer, prefill (sm_103a).
+// Non-uniform (Lloyd-Max) KV-cache quantizer: prefill and decode-time appends (sm_103a).
 //
 // "KVQuant-NUQ" (VeloxQuant-MLX docs), How it works:
 //  * Non-uniform levels (Lloyd-Max): 2^bits levels seeded at evenly spaced
@@ -10,6 +10,11 @@
 //    prefill, values per token over its channels.
 //  * Attention Sink-Aware quantization: the first n_sink tokens stay exact in
 //    16-bit and take no part in the fit.
+//  * Decode-time keys keep the prefill's per-channel tables and are screened
+//    against the per-channel threshold frozen at prefill (the magnitude of the
+//    channel's k-th rank outlier): |x| >= threshold goes to the side channel,
+//    appended in token order while it has room.  Decode values are fitted per
+//    token like prefill values.
 // The fit follows one fixed arithmetic order so that the tables are bit-exact:
 // level sums in the R32 order (lane l = position mod 32 adds its positions in
 // increasing order, then a xor butterfly), sum / count in fp32, fp16 table,
@@ -152,6 +157,9 @@ __global__ void __launch_bounds__(256) nuq_key_fit_kernel(QuantArgs a, Layout L,
         atomicOr(&outmask[p >> 5], 1u << (p & 31));
         atomicOr(&a.olbits[(static_cast<long long>(u) * L.qcap + p) * (D / 32) + c / 32], 1u << (c & 31));
     }
+    // the threshold decode keys are screened against: the k-th largest magnitude
+    if (threadIdx.x == 0 && a.thr)
+        a.thr[static_cast<long long>(u) * D + c] = k > 0 ? __uint_as_float(static_cast<uint32_t>(keys[k - 1] >> 32)) : INFINITY;
     __syncthreads();
     // quantile seeds: sort the fit values (outliers and padding sort last)
     uint32_t *k32 = reinterpret_cast<uint32_t *>(keys);
@@ -212,8 +220,8 @@ __global__ void __launch_bounds__(128) nuq_value_kernel(QuantArgs a, Layout L) {
     const long long gw = static_cast<long long>(blockIdx.x) * WPB + warp;
     if (gw >= static_cast<long long>(L.U) * a.n_tok) return;
     const int u = static_cast<int>(gw / a.n_tok);
-    const long long t = gw % a.n_tok;
-    const long long base = (static_cast<long long>(u) * a.n_tok + t) * D;
+    const long long ti = gw % a.n_tok, t = a.pos0 + ti;  // row of the input, position in the sequence
+    const long long base = (static_cast<long long>(u) * a.n_tok + ti) * D;
     float x[V];
     bool finite = true;
 #pragma unroll
@@ -368,12 +376,13 @@ __global__ void __launch_bounds__(128) nuq_key_code_kernel(QuantArgs a, Layout L
     const long long gw = static_cast<long long>(blockIdx.x) * WPB + warp;
     if (gw >= static_cast<long long>(L.U) * a.n_tok) return;
     const int u = static_cast<int>(gw / a.n_tok);
-    const long long t = gw % a.n_tok;
-    const long long base = (static_cast<long long>(u) * a.n_tok + t) * D;
+    const long long ti = gw % a.n_tok, t = a.pos0 + ti;  // row of the input, position in the sequence
+    const long long base = (static_cast<long long>(u) * a.n_tok + ti) * D;
     const int rs = raw_slot_of(t, a.seq_after, L);
     if (rs >= 0) copy_raw<V>(a, L, u, base, rs, true);
     if (t < L.n_sink) return;
     const long long slot = t - L.n_sink;
+    const bool screen = a.pos0 > 0 && a.thr != nullptr;  // decode keys: outliers by the frozen threshold
     uint32_t m[V];
 #pragma unroll
     for (int j = 0; j < V; j++) {
@@ -384,6 +393,10 @@ __global__ void __launch_bounds__(128) nuq_key_code_kernel(QuantArgs a, Layout L
         for (int i = 0; i < LV; i++)
             lev[i] = __half2float(__ushort_as_half(a.lut[(static_cast<long long>(u) * D + c) * LV + i]));
         m[j] = static_cast<uint32_t>(nearest<LV>(x, lev));
+        if (screen) {
+            const unsigned ob = __ballot_sync(FULL, fabsf(x) >= a.thr[static_cast<long long>(u) * D + c]);
+            if (lane == 0) a.olbits[(static_cast<long long>(u) * L.qcap + slot) * V + j] = ob;
+        }
     }
     constexpr int WK = Rec<D, BITS>::K_WORDS, WLO = D * 2 / 32;
     uint32_t *row = reinterpret_cast<uint32_t *>(a.codes + (static_cast<long long>(u) * L.qcap + slot) * L.rowK);
@@ -401,18 +414,22 @@ __global__ void __launch_bounds__(128) nuq_key_code_kernel(QuantArgs a, Layout L
 }
 
 // ---------------------------------------------------------------------------
-// Key side channel, rows by quantized slot: one CTA per unit.  Each thread
-// takes a contiguous run of slots; a block scan of the run counts gives the
-// row pointers; entries follow in channel order.
+// Key side channel, rows by quantized slot: one CTA per unit, over this
+// call's slots [slot_lo, slot_lo + n_slots).  Each thread takes a contiguous
+// run of slots; a block scan of the run counts gives the row pointers, which
+// continue from the row pointer already stored at slot_lo (0 for a prefill);
+// entries follow in channel order.  Entries past the capacity are not stored
+// (the row pointers count stored entries only) and latch ST_SIDE_FULL.
 // ---------------------------------------------------------------------------
 template <int D>
 __global__ void __launch_bounds__(256) nuq_key_csr_kernel(QuantArgs a, Layout L) {
     constexpr int W = D / 32;
     __shared__ int part[256];
-    const int u = blockIdx.x, n = a.n_fit;
+    const int u = blockIdx.x, n = a.n_slots;
+    const long long s0 = a.slot_lo, cap = L.nnzk_cap;
     const int chunk = (n + blockDim.x - 1) / blockDim.x;
     const int p0 = min(n, static_cast<int>(threadIdx.x) * chunk), p1 = min(n, p0 + chunk);
-    const uint32_t *bits = a.olbits + static_cast<long long>(u) * L.qcap * W;
+    const uint32_t *bits = a.olbits + (static_cast<long long>(u) * L.qcap + s0) * W;
     int local = 0;
     for (int p = p0; p < p1; p++)
 #pragma unroll
@@ -425,27 +442,32 @@ __global__ void __launch_bounds__(256) nuq_key_csr_kernel(QuantArgs a, Layout L)
         part[threadIdx.x] += v;
         __syncthreads();
     }
-    int run = part[threadIdx.x] - local;
-    const int total = part[blockDim.x - 1];
     int *rp = a.ol_rowptr + static_cast<long long>(u) * L.rp_stride;
+    const long long run0 = s0 > 0 ? rp[s0] : 0;
+    __syncthreads();  // every thread has read rp[s0] before it is rewritten
+    long long run = run0 + part[threadIdx.x] - local;
+    const long long total = run0 + part[blockDim.x - 1];
     uint16_t *col = a.ol_col + static_cast<long long>(u) * L.nnzk_cap;
     uint16_t *val = a.ol_val + static_cast<long long>(u) * L.nnzk_cap;
     for (int p = p0; p < p1; p++) {
-        rp[p] = run;
+        rp[s0 + p] = static_cast<int>(min(run, cap));
 #pragma unroll
         for (int w = 0; w < W; w++) {
             uint32_t b = bits[p * W + w];
             while (b) {
                 const int c = 32 * w + __ffs(b) - 1;
                 b &= b - 1;
-                const long long xi = (static_cast<long long>(u) * a.n_tok + L.n_sink + p) * D + c;
-                col[run] = static_cast<uint16_t>(c);
-                val[run] = __half_as_ushort(__float2half_rn(ld_in(a.x, xi, a.in_dtype)));
+                if (run < cap) {
+                    const long long xi = (static_cast<long long>(u) * a.n_tok + (s0 + p + L.n_sink - a.pos0)) * D + c;
+                    col[run] = static_cast<uint16_t>(c);
+                    val[run] = __half_as_ushort(__float2half_rn(ld_in(a.x, xi, a.in_dtype)));
+                }
                 run++;
             }
         }
     }
-    for (long long p = n + threadIdx.x; p <= L.qcap; p += blockDim.x) rp[p] = total;
+    for (long long p = s0 + n + threadIdx.x; p <= L.qcap; p += blockDim.x) rp[p] = static_cast<int>(min(total, cap));
+    if (threadIdx.x == 0 && total > cap) atomicOr(a.status, ST_SIDE_FULL);
 }
 
 // ---- launchers ----------------------------------------------------------------

@@ -106,7 +106,9 @@ def nuq_views(w: W.Workload, cache, S: int):
     if rcap:
         v["raw_k"] = t["raw_k"].view(np.uint16).reshape(B, H, rcap, d)
         v["raw_v"] = t["raw_v"].view(np.uint16).reshape(B, H, rcap // 2, d, 2)
-    assert sizes["meta_k"] == 0 and sizes["mean_k"] == 0
+    if t["meta_k"] is not None:  # frozen per-channel key outlier thresholds, fp32
+        v["thr_k"] = t["meta_k"].view(np.float32).reshape(B, H, d)
+    assert sizes["meta_v"] == 0 and sizes["mean_k"] == 0
     return v, qcap
 
 

@@ -29,20 +29,8 @@ CASES = {
 }
 
 
-@pytest.mark.parametrize("name", list(CASES))
-def test_nuq_prefill_is_bit_exact(name):
-    import torch
-    from quantized_decode_attention_gb300 import KVCache
-    w = CASES[name]
-    S = w.seq
-    k, v = W.make_kv(w)
-    cache = KVCache.allocate(cfg_for(w))
-    cache.quantize(to_device(k, w.kv_dtype), to_device(v, w.kv_dtype))
-    torch.cuda.synchronize()
-    cache.check()
-    got, qcap = nuq_views(w, cache, S)
-    nk = OC.quantize_nuq(w, k, True, S)
-    nv = OC.quantize_nuq(w, v, False, S)
+def _compare(w, got, qcap, k, v, nk, nv, S):
+    """Tables, codes, side channels and 16-bit regions of a cache of length S."""
     nq = S - w.n_sink
     assert np.array_equal(got["lut_k"], nk.lut)
     assert np.array_equal(got["lut_v"][:, :, :nq], nv.lut)
@@ -71,24 +59,126 @@ def test_nuq_prefill_is_bit_exact(name):
         assert np.array_equal(got["val_v"][:, :, :nq], val[:, :, :nq])
     else:
         assert not nv.outlier.any()
-    regions_k = OC.raw_regions(w, k, S)
-    regions_v = OC.raw_regions(w, v, S)
-    for slot, bits in regions_k.items():
+    for slot, bits in OC.raw_regions(w, k[:, :, :S], S).items():
         assert np.array_equal(got["raw_k"][:, :, slot], bits), slot
-    for slot, bits in regions_v.items():
+    for slot, bits in OC.raw_regions(w, v[:, :, :S], S).items():
         assert np.array_equal(got["raw_v"][:, :, slot // 2, :, slot & 1], bits), slot
 
 
-def test_nuq_append_is_refused():
+@pytest.mark.parametrize("name", list(CASES))
+def test_nuq_prefill_is_bit_exact(name):
+    import torch
+    from quantized_decode_attention_gb300 import KVCache
+    w = CASES[name]
+    S = w.seq
+    k, v = W.make_kv(w)
+    cache = KVCache.allocate(cfg_for(w))
+    cache.quantize(to_device(k, w.kv_dtype), to_device(v, w.kv_dtype))
+    torch.cuda.synchronize()
+    cache.check()
+    got, qcap = nuq_views(w, cache, S)
+    nk = OC.quantize_nuq(w, k, True, S)
+    nv = OC.quantize_nuq(w, v, False, S)
+    _compare(w, got, qcap, k, v, nk, nv, S)
+    if "thr_k" in got:
+        assert np.array_equal(got["thr_k"], OC.nuq_key_thresholds(w, k, S))
+
+
+# Decode-time appends: keys against the tables and thresholds frozen at the
+# prefill, values fitted per token; one token at a time and in batches.
+STREAM = {
+    "nuq3-d128": (W.NUQ.with_(batch=1, n_kv_heads=2, n_q_heads=8, seq=300), [200] + [1] * 40 + [60]),
+    "nuq2-d64-recent": (W.NUQ.with_(batch=2, n_kv_heads=1, n_q_heads=4, head_dim=64, seq=200, bits=2,
+                                    n_recent=16), [120, 1, 1, 1, 77]),
+    "nuq4-bf16-nosink": (W.NUQ.with_(batch=1, n_kv_heads=1, n_q_heads=4, seq=180, bits=4, kv_dtype="bf16",
+                                     n_sink=0), [100, 1, 79]),
+}
+
+
+def _stream_cache(w, steps, k, v, check_at):
+    """Fill a cache by the given calls; yields (cache, P, S) after each call whose end is in check_at."""
+    from quantized_decode_attention_gb300 import KVCache
+    cache = KVCache.allocate(cfg_for(w))
+    pos = 0
+    for n in steps:
+        cache.quantize(to_device(k[:, :, pos:pos + n], w.kv_dtype), to_device(v[:, :, pos:pos + n], w.kv_dtype),
+                       pos0=pos)
+        pos += n
+        if pos in check_at:
+            yield cache, steps[0], pos
+    cache.close()
+
+
+@pytest.mark.parametrize("name", list(STREAM))
+def test_nuq_appends_match_oracle(name):
+    import torch
+    from helpers import out_to_np
+    w, steps = STREAM[name]
+    k, v = W.make_kv(w)
+    q = W.make_q(w)
+    qd = to_device(q, "f32")
+    dt = {"f16": torch.float16, "bf16": torch.bfloat16, "f32": torch.float32}[w.out_dtype]
+    out = torch.empty((w.batch, w.n_q_heads, w.head_dim), dtype=dt, device="cuda")
+    mid = steps[0] + sum(steps[1:-1])
+    for cache, P, S in _stream_cache(w, steps, k, v, (mid, w.seq)):
+        torch.cuda.synchronize()
+        cache.check()
+        got, qcap = nuq_views(w, cache, w.seq)
+        nnz = got["col_k"].shape[-1] if "col_k" in got else None
+        nk = OC.quantize_nuq_stream(w, k[:, :, :S], True, P, S, nnz)
+        nv = OC.quantize_nuq_stream(w, v[:, :, :S], False, P, S)
+        if S == w.seq:
+            assert nk.outlier[:, :, P - w.n_sink:].any()  # decode keys did meet the threshold
+        _compare(w, got, qcap, k, v, nk, nv, S)
+        assert np.array_equal(got["thr_k"], OC.nuq_key_thresholds(w, k, P))
+        cache.attention(qd, out, S)
+        torch.cuda.synchronize()
+        cache.check()
+        ref = OC.attention(w, q, k[:, :, :S], v[:, :, :S], S, nk, nv)
+        assert np.all(np.abs(out_to_np(out) - ref) <= _out_tol(w, ref)), (S, float(np.max(np.abs(out_to_np(out) - ref))))
+
+
+def test_nuq_key_side_channel_overflow():
+    """Decode keys four times the prefill's scale overflow the side channel: the
+    cache reports it, and keeps exactly the first entries that fit."""
+    import torch
+    from quantized_decode_attention_gb300 import DQError
+    from helpers import out_to_np
+    w = W.NUQ.with_(batch=1, n_kv_heads=2, n_q_heads=8, seq=260, n_recent=0)
+    P = 60
+    k, v = W.make_kv(w)
+    kf = W.bits_to_f32(k, w.kv_dtype).copy()
+    kf[:, :, P:] *= 4.0
+    k = W.to_dtype_bits(kf, w.kv_dtype)
+    q = W.make_q(w)
+    for cache, P_, S in _stream_cache(w, [P, 100, 100], k, v, (w.seq,)):
+        torch.cuda.synchronize()
+        with pytest.raises(DQError):
+            cache.check()
+        got, qcap = nuq_views(w, cache, w.seq)
+        nnz = got["col_k"].shape[-1]
+        nk = OC.quantize_nuq_stream(w, k, True, P, S, nnz)
+        nv = OC.quantize_nuq_stream(w, v, False, P, S)
+        assert np.all(nk.outlier.sum(axis=(2, 3)) == nnz)   # the channel is full in every unit
+        _compare(w, got, qcap, k, v, nk, nv, S)
+        out = torch.empty((w.batch, w.n_q_heads, w.head_dim), dtype=torch.float16, device="cuda")
+        cache.attention(to_device(q, "f32"), out, S)
+        torch.cuda.synchronize()
+        ref = OC.attention(w, q, k, v, S, nk, nv)
+        assert np.all(np.abs(out_to_np(out) - ref) <= _out_tol(w, ref))
+
+
+def test_nuq_append_without_quantized_prefill_is_refused():
     import torch
     from quantized_decode_attention_gb300 import KVCache, DQError
-    w = CASES["nuq3-d128"]
+    w = CASES["nuq3-d128"]            # one sink
     k, v = W.make_kv(w)
-    cache = KVCache.allocate(cfg_for(w, max_seq=w.seq + 8))
-    cache.quantize(to_device(k, w.kv_dtype), to_device(v, w.kv_dtype))
+    cache = KVCache.allocate(cfg_for(w))
+    cache.quantize(to_device(k[:, :, :1], w.kv_dtype), to_device(v[:, :, :1], w.kv_dtype))
     with pytest.raises(DQError):
-        cache.quantize(to_device(k[:, :, :1], w.kv_dtype), to_device(v[:, :, :1], w.kv_dtype), pos0=w.seq)
+        cache.quantize(to_device(k[:, :, 1:2], w.kv_dtype), to_device(v[:, :, 1:2], w.kv_dtype), pos0=1)
     torch.cuda.synchronize()
+    cache.close()
 
 
 def _out_tol(w, ref):
