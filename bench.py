@@ -205,7 +205,7 @@ def traffic_for(kernel_sha: str, bits):
     """DRAM bytes per attention launch from the committed ncu capture, or None
     when the kernel source differs from the one captured."""
     key = bits if isinstance(bits, str) else f"{bits}bit"
-    if key == "dquant":
+    if key.startswith("dquant"):
         kernel_sha = src_sha(RANS_SRC)
     try:
         with open(TRAFFIC_FILE) as f:
@@ -659,7 +659,7 @@ def main():
         torch.cuda.empty_cache()
     del k_dev, v_dev
     nuq = None if args.no_nuq else run_gpu_nuq(args, W.NUQ)
-    dqr = None if args.no_dquant else run_gpu_dquant(args, W.DQUANT)
+    dqrs = [] if args.no_dquant else [(D, run_gpu_dquant(args, D)) for D in (W.DQUANT, W.DQUANT_196)]
     qwen = [run_qwen_long(args, int(x), rank) for x in args.qwen.split(",") if x.strip()]
 
     ms_step, value = aggregate(res["total_ms"], args.steps, w.batch, world)
@@ -702,7 +702,7 @@ def main():
                        "head_dim": W.NUQ.head_dim, "seq_len": W.NUQ.seq, "bits": W.NUQ.bits,
                        "n_sink": W.NUQ.n_sink, "outlier_frac": 0.01, "lloyd_iters": 8,
                        "l2": f"{nuq['copies']} cache copies rotated per step (> L2)",
-                       "step": "decode attention (prefill-only scheme), CUDA graph over the copies"}}
+                       "step": "decode attention over a prefilled cache, CUDA graph over the copies"}}
     for wq, r in qwen:
         line["variants"][f"{wq.name}-s{wq.seq}-{wq.bits}bit"] = {
             "value": round(wq.batch / (r["total_ms"] / args.steps / 1e3), 1),
@@ -719,19 +719,18 @@ def main():
             "roofline": roof(bf16, "bf16"), "e2e_tok_s": round(bf16["e2e_tok_s"], 1),
             "config": {"batch": w.batch, "seq_len": S, "cache": "bf16, unquantized (all tokens 16-bit slots)",
                        "role": "context: the same step without quantization, through the library's 16-bit path"}}
-    if dqr is not None:
-        D = W.DQUANT
+    for D, dqr in dqrs:
         line["variants"][f"{D.name}-k{D.extra['levels_k']}x{D.extra['container_k']}-v{D.extra['levels_v']}x{D.extra['container_v']}"] = {
             "value": round(D.batch / (dqr["total_ms"] / dqr["steps"] / 1e3), 1),
             "ms_per_step": round(dqr["total_ms"] / dqr["steps"], 5),
-            "roofline": roof(dqr, "dquant"), "e2e_tok_s": round(dqr["e2e_tok_s"], 1),
+            "roofline": roof(dqr, "dquant" if D is W.DQUANT else "dquant196"), "e2e_tok_s": round(dqr["e2e_tok_s"], 1),
             "prefill_ms": round(dqr["prefill_ms"], 3),
             "config": {"batch": D.batch, "q_heads": D.n_q_heads, "kv_heads": D.n_kv_heads, "head_dim": D.head_dim,
                        "seq_len": D.seq, "n_recent": D.n_recent, "levels_k": D.extra["levels_k"],
                        "levels_v": D.extra["levels_v"], "container_k": D.extra["container_k"],
-                       "container_v": D.extra["container_v"], "bits_per_value": 2.26,
+                       "container_v": D.extra["container_v"], "bits_per_value": round(W.dquant_bits_per_value(D), 3),
                        "l2": f"{dqr['copies']} cache copies rotated per step (> L2)",
-                       "step": "decode attention (prefill-only scheme), one call per step"}}
+                       "step": "decode attention over a prefilled cache, one call per step"}}
     if rank == 0 and not args.no_cpu:
         line["cpu_baseline"] = cpu_baseline(w, args.bits, S, args.cpu_seconds, k, v, q)
     if rank == 0:

@@ -4,6 +4,7 @@ import ctypes as C
 import os
 import re
 
+import numpy as np
 import pytest
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
@@ -110,6 +111,26 @@ def test_sizes_dquant_layout(lib):
     assert s["lut_k"] == 0 and s["ol_col_k"] == 0
     bpv = (s["codes_k"] + s["codes_v"] + s["meta_k"] + s["meta_v"] + s["mean_k"]) * 8 / (2 * B * qcap * n)
     assert bpv == pytest.approx(2.26, abs=0.005)
+
+
+def test_sizes_dquant_196(lib):
+    """D-Quant Sec. 5 ("lower storage budget"): the same 8 / 6 levels at 1.96 bits
+    per value.  The sizes the library reports give that budget, and both
+    containers hold the cheapest coding of a stream (the model's most probable
+    symbol in every position, plus the 32-bit state) with room to spare."""
+    import oracle
+    import workloads as W
+    from quantized_decode_attention_gb300 import kv_sizes
+    e = W.DQUANT_196.extra
+    s = kv_sizes(_dquant(container_k=e["container_k"], container_v=e["container_v"]))
+    B, qcap, n = 32, 16384, 1024
+    bpv = (s["codes_k"] + s["codes_v"] + s["meta_k"] + s["meta_v"] + s["mean_k"]) * 8 / (2 * B * qcap * n)
+    assert bpv == pytest.approx(1.96, abs=0.005)
+    assert bpv == pytest.approx(W.dquant_bits_per_value(W.DQUANT_196), abs=1e-3)
+    for M, C in ((8, e["container_k"]), (6, e["container_v"])):
+        t = oracle.DqTable(n, M, alpha=1.4)
+        cheapest = min(-np.log2(f / 256.0) for f in t.f) * n + 32
+        assert cheapest < 8 * C
 
 
 def test_dquant_model_matches_the_oracle(lib):

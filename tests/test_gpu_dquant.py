@@ -32,6 +32,9 @@ CASES = {
     # 16 key levels, 4 value levels, sinks and a short recent window, ragged last window
     "dq-h4-m16-sinks": dq(batch=1, n_kv_heads=4, n_q_heads=16, seq=260, n_sink=2, n_recent=8,
                           extra={"levels_k": 16, "container_k": 172, "levels_v": 4, "container_v": 100}),
+    # the 1.96-bit operating point: 8 / 6 levels in 286- / 200-byte containers
+    "dq-h8-196": dq(batch=1, n_kv_heads=8, n_q_heads=32, seq=200, n_recent=16,
+                    extra={"container_k": 286, "container_v": 200}),
     # one KV head, no key mean, rotated values, fp16 input
     "dq-h1-nomean": dq(batch=2, n_kv_heads=1, n_q_heads=4, seq=150, n_recent=0, mean_k=False, rot_v="hadamard",
                        kv_dtype="f16", extra={"container_k": 42, "container_v": 30}),

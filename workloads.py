@@ -71,7 +71,22 @@ DQUANT = Workload("dquant-rans", 5, batch=32, n_kv_heads=8, n_q_heads=32, head_d
                   extra={"levels_k": 8, "levels_v": 6, "container_k": 331, "container_v": 231,
                          "alpha": 1.4, "mean_window": 128})
 
-WORKLOADS = {w.name: w for w in (TINY, LLAMA, NUQ, QWEN_LONG, DQUANT)}
+# D-Quant at 1.96 bits per value with the same 8 / 6 levels (D-Quant Sec. 5,
+# "lower storage budget"; Fig. 4 middle): the 2.26-bit payloads scaled in
+# proportion, keys 8 levels in 286 bytes and values 6 levels in 200 bytes
+DQUANT_196 = DQUANT.with_(name="dquant-rans-1.96bpv",
+                          extra={**DQUANT.extra, "container_k": 286, "container_v": 200})
+
+WORKLOADS = {w.name: w for w in (TINY, LLAMA, NUQ, QWEN_LONG, DQUANT, DQUANT_196)}
+
+
+def dquant_bits_per_value(w: Workload) -> float:
+    """Storage of a D-Quant cache per quantized value: containers, fp16 (s, o)
+    per stream, and the keys' INT8 window mean with its fp16 scale per 128 tokens."""
+    n = w.n_kv_heads * w.head_dim
+    e = w.extra
+    mean = (n + 2) / e.get("mean_window", 128) if w.mean_k else 0.0
+    return ((e["container_k"] + 4 + mean) + (e["container_v"] + 4)) * 8 / (2 * n)
 
 
 def rng(index: int, tid: int, salt: int = 0) -> np.random.Generator:
