@@ -65,24 +65,22 @@ __device__ __forceinline__ void ldg_into_if(uint32_t &v, const uint32_t *p, bool
 }
 
 // One rANS stream being decoded by a lane.  The container bytes after the
-// state sit in a 64-bit reservoir (the next byte at bit `pos`); every 4
-// symbols, refill() moves in the word prefetched at the previous refill and
-// fetches the next one (a predicated load, so there is no branch and no wait),
-// which keeps at least 4 unread bytes in the reservoir - enough for 4 symbols,
-// each taking at most one byte.  Loads stay inside the aligned words that
-// overlap the container (wl counts those not yet loaded); an idle lane loads
-// nothing.  A well-formed stream ends in the state the encoder started from
-// (2^23), which the caller checks.
+// state sit in two words, lo then hi, the next byte being byte k of the pair
+// (one byte permute picks it); every 4 symbols refill() moves hi and the word
+// prefetched at the previous refill in and fetches the next one (a predicated
+// load, so there is no branch and no wait), which keeps at least 4 unread bytes
+// in the pair - enough for 4 symbols, each taking at most one byte.  Loads stay
+// inside the aligned words that overlap the container (wl counts those not yet
+// loaded); an idle lane loads nothing.  A well-formed stream ends in the state
+// the encoder started from (2^23), which the caller checks.
 struct Dec {
-    uint32_t x, nxt, pos;
-    uint64_t buf;
+    uint32_t x, lo, hi, nxt, k;
     const uint32_t *wp;  // next word to load
     int wl;              // words overlapping the container not yet loaded
     __device__ __forceinline__ void open(const uint8_t *base, int C, bool valid) {
         if (!valid) {  // an idle lane: decodes zeros, reads nothing
             x = RANS_L;
-            nxt = pos = 0;
-            buf = 0;
+            lo = hi = nxt = k = 0;
             wp = nullptr;
             wl = 0;
             return;
@@ -94,34 +92,23 @@ struct Dec {
         const int off = static_cast<int>(p0 & 3u);
         const uint32_t *w0 = reinterpret_cast<const uint32_t *>(p0 - off);
         const int words = static_cast<int>(((pe & ~uintptr_t(3)) - (p0 - off)) / 4) + 1;
-        const uint32_t lo = __ldg(w0);
-        const uint32_t hi = words > 1 ? __ldg(w0 + 1) : 0u;
+        lo = __ldg(w0);
+        hi = words > 1 ? __ldg(w0 + 1) : 0u;
         nxt = words > 2 ? __ldg(w0 + 2) : 0u;
-        buf = static_cast<uint64_t>(lo) | (static_cast<uint64_t>(hi) << 32);
-        pos = 8u * off;
+        k = static_cast<uint32_t>(off);
         wp = w0 + 3;
         wl = words - 3;
     }
     // Past the container's last word nxt keeps a stale word: a well-formed
     // stream never consumes those bytes (the final-state check catches one that does).
     __device__ __forceinline__ void refill() {
-        const bool r = pos >= 32u;
-        const uint64_t nb = (buf >> 32) | (static_cast<uint64_t>(nxt) << 32);
-        buf = r ? nb : buf;
-        pos = r ? pos - 32u : pos;
+        const bool r = k >= 4u;
+        lo = r ? hi : lo;
+        hi = r ? nxt : hi;
+        k = r ? k - 4u : k;
         ldg_into_if(nxt, wp, r && wl > 0);
         wp += r ? 1 : 0;
         wl -= r ? 1 : 0;
-    }
-    // one symbol (Algorithm 2): returns the 64-bit table entry
-    __device__ __forceinline__ uint2 step(const uint2 *dec) {
-        const uint2 e = dec[x & 255u];
-        x = (e.x & 0x1ffu) * (x >> 8) + (e.x >> 16);
-        const bool need = x < RANS_L;
-        const uint32_t byte = static_cast<uint32_t>(buf >> pos);
-        x = need ? __byte_perm(byte, x, 0x6540) : x;  // (x << 8) | (byte & 255)
-        pos += need ? 8u : 0u;
-        return e;
     }
 };
 
@@ -137,9 +124,9 @@ __device__ __forceinline__ void step_all(Dec (&d)[N], const uint2 *dec, uint2 (&
 #pragma unroll
     for (int ch = 0; ch < N; ch++) {
         const bool need = d[ch].x < RANS_L;
-        const uint32_t byte = static_cast<uint32_t>(d[ch].buf >> d[ch].pos);
-        d[ch].x = need ? __byte_perm(byte, d[ch].x, 0x6540) : d[ch].x;
-        d[ch].pos += need ? 8u : 0u;
+        const uint32_t byte = __byte_perm(d[ch].lo, d[ch].hi, d[ch].k);  // byte k of (hi, lo) in byte 0
+        d[ch].x = need ? __byte_perm(byte, d[ch].x, 0x6540) : d[ch].x;   // (x << 8) | byte
+        d[ch].k += need ? 1u : 0u;
     }
 }
 
