@@ -575,6 +575,35 @@ def oracle_pool():
     return _POOL
 
 
+FEASIBLE_BUDGETS = (1.0, 1.25, 1.5, 1.75, 2.0, 2.25, 2.5, 2.75, 3.0, 3.5, 4.0)
+
+
+def feasible_alphabet(n: int = 1024, budgets=FEASIBLE_BUDGETS) -> list:
+    """D-Quant App. C (Fig. 6 left): the largest number of levels (2..16) whose
+    cheapest stream still fits a container of b bits per value of payload plus the
+    32-bit state, by the library's own symbol model (dq_kv_sizes refuses an
+    infeasible one), against the 2^floor(b) levels of fixed-width coding at that
+    rate.  Host only: no kernel runs."""
+    from quantized_decode_attention_gb300 import DQError, kv_sizes, make_config
+    H = n // 128
+    out = []
+    for b in budgets:
+        C = int(np.ceil((b * n + 32) / 8))
+        best = None
+        for M in range(2, 17):
+            cfg = make_config(batch=1, n_kv_heads=H, n_q_heads=4 * H, head_dim=128, max_seq=256, scheme="rans",
+                              rot_k="hadamard", rot_v="none", mean_k=True, levels_k=M, levels_v=2,
+                              container_k=C, container_v=C)
+            try:
+                kv_sizes(cfg)
+                best = M
+            except DQError:
+                pass
+        out.append({"payload_bits_per_value": b, "container_bytes": C, "entropy_coded_levels": best,
+                    "fixed_width_levels": 2 ** int(b)})
+    return out
+
+
 def cpu_baseline(w, bits, S, budget_s, k, v, q):
     """The oracle as it stands, timed on this host's cores: each worker quantizes
     one unit's cache and runs its fp64 decode attention; as many units as fit
@@ -733,6 +762,10 @@ def main():
                        "step": "decode attention over a prefilled cache, one call per step"}}
     if rank == 0 and not args.no_cpu:
         line["cpu_baseline"] = cpu_baseline(w, args.bits, S, args.cpu_seconds, k, v, q)
+    if rank == 0:
+        line["diagnostics"] = {"dquant_feasible_alphabet": feasible_alphabet(),
+                               "note": "largest D-Quant alphabet whose cheapest 1024-value stream fits the "
+                                       "container, by the library's symbol model, vs fixed-width levels"}
     if rank == 0:
         print(json.dumps(line))
     if world > 1:

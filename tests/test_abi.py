@@ -159,3 +159,33 @@ def test_dquant_validation(lib):
                 dict(meta_dtype="f32"), dict(rot_k="dense")):
         with pytest.raises(DQError):
             kv_sizes(_dquant(**bad))
+
+
+def test_dquant_feasible_alphabet_matches_the_oracle(lib):
+    """D-Quant App. C (Fig. 6 left): the largest alphabet whose cheapest stream fits
+    a container, by the library (as the bench reports it) and by the oracle's own
+    symbol model (cheapest symbol cost times n against B = 8C - 32 bits).  The
+    entropy-coded container holds at least the levels of fixed-width coding at the
+    same rate, and the default 8 / 6 levels lie inside the region at the key and
+    value payloads of the 2.26-bit point (331 and 231 bytes)."""
+    import oracle
+    sys_path_bench()
+    import bench
+    n = 1024
+    got = bench.feasible_alphabet(n)
+    for row in got:
+        C = row["container_bytes"]
+        feas = [M for M in range(2, 17)
+                if int(oracle.DqTable(n, M, alpha=1.4).r.min()) * n <= oracle.dq_budget_fx(C)]
+        assert row["entropy_coded_levels"] == (max(feas) if feas else None), row
+        assert row["entropy_coded_levels"] >= row["fixed_width_levels"], row
+    for M, C in ((8, 331), (6, 231)):
+        assert int(oracle.DqTable(n, M, alpha=1.4).r.min()) * n <= oracle.dq_budget_fx(C)
+
+
+def sys_path_bench():
+    import os
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    if root not in sys.path:
+        sys.path.insert(0, root)
