@@ -40,12 +40,7 @@ constexpr int RCH = 4;                 // 32-token chunks per warp
 constexpr int ITEM = 32 * RW * RCH;    // quantized tokens per item
 constexpr int REC = 132;               // floats per record: acc[128], m, l, 2 pad
 constexpr uint32_t RANS_L = 1u << 23;
-constexpr float SLACK = 8.0f;          // running max may lag by this much (log2 units)
 constexpr int VST = 40;                // u16 per staged value row (32 tokens + pad)
-
-__device__ __forceinline__ uint32_t pack_h2(uint16_t lo, uint16_t hi) {
-    return static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
-}
 
 __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                          uint32_t b0, uint32_t b1) {
