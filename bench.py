@@ -374,8 +374,9 @@ def run_qwen_long(args, S, rank):
 
 
 def run_gpu_nuq(args, w):
-    """KVQuant NUQ cache (prefill only: no append step): each step is one
-    decode-attention call, rotating over cache copies larger than L2."""
+    """KVQuant NUQ cache, prefilled: each step is one decode-attention call,
+    rotating over cache copies larger than L2 (appends are checked by the tests;
+    re-appending at the last position would not change what a step reads)."""
     import torch
     from quantized_decode_attention_gb300 import KVCache, make_config
     S = w.seq
@@ -462,8 +463,10 @@ def run_gpu_nuq(args, w):
 
 
 def run_gpu_dquant(args, w):
-    """D-Quant cache (prefill only): each step is one decode-attention call,
-    rotating over cache copies larger than L2."""
+    """D-Quant cache, prefilled: each step is one decode-attention call,
+    rotating over cache copies larger than L2.  An append at the last position
+    would flush a whole 128-slot window on every step, which real decoding does
+    once every 128 tokens, so appends are checked by the tests, not timed here."""
     import torch
     from quantized_decode_attention_gb300 import KVCache, make_config
     S = w.seq
