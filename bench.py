@@ -12,7 +12,7 @@ the cache (their total exceeds the L2 size), so no step reads the previous
 step's bytes from L2.
 
 Prints ONE JSON line (rank 0).  ``--impl reference`` times the CPU oracle
-instead (the reference arm for this build).
+instead: the slow CPU implementation the GPU results are checked against.
 """
 from __future__ import annotations
 
@@ -607,6 +607,105 @@ def feasible_alphabet(n: int = 1024, budgets=FEASIBLE_BUDGETS) -> list:
     return out
 
 
+# D-Quant Sec. 5.4 (Fig. 4) varies one setting at a time around the 8 / 6-level,
+# 331 / 231-byte point: the alphabets at that storage, the storage at 8 / 6
+# levels, and the key/value split of the same total.  The pages score each
+# setting by long-context task accuracy of a trained model; on synthetic data the
+# measurable counterpart is how far the decode-attention output moves from exact
+# attention over the unquantized tokens.
+ABL_LEVELS = ((4, 6), (6, 6), (8, 6), (10, 6), (12, 6), (16, 6), (8, 3), (8, 4), (8, 8), (8, 10), (8, 16))
+# key / value containers in the 331 : 231 proportion: about 1.6, 1.96, 2.26, 2.6
+# and 3.0 bits per value with the fp16 (s, o) and the INT8 window means
+ABL_BUDGETS = ((232, 162), (286, 200), (331, 231), (383, 267), (443, 309))
+ABL_KEY_BYTES = (256, 281, 306, 331, 356, 381)  # key container; the value container gets 562 minus it
+ABL_PAIR_BYTES = 331 + 231
+
+
+def exact_attention(q: np.ndarray, k_bits: np.ndarray, v_bits: np.ndarray, kv_dtype: str) -> np.ndarray:
+    """softmax(q K^T / sqrt(d)) V in fp64 over the unquantized 16-bit tokens.
+    q [B, Hq, d] fp32; k_bits, v_bits [B, Hkv, S, d] bf16 / fp16 bit patterns;
+    query head h reads KV head floor(h Hkv / Hq).  Returns [B, Hq, d] fp64."""
+    def f64(bits):
+        u = np.ascontiguousarray(bits, dtype=np.uint16)
+        if kv_dtype == "bf16":
+            return (u.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+        return u.view(np.float16).astype(np.float64)
+    K, V = f64(k_bits), f64(v_bits)
+    B, Hq, d = q.shape
+    G = Hq // K.shape[1]
+    qg = q.astype(np.float64).reshape(B, K.shape[1], G, d)
+    s = np.einsum("bhgd,bhtd->bhgt", qg, K) / np.sqrt(d)
+    p = np.exp(s - s.max(axis=-1, keepdims=True))
+    p /= p.sum(axis=-1, keepdims=True)
+    return np.einsum("bhgt,bhtd->bhgd", p, V).reshape(B, Hq, d)
+
+
+def dquant_attention_output(w, k_dev, v_dev, q_dev, levels_k, levels_v, ck, cv):
+    """The library's fp32 decode-attention output over a D-Quant cache of w's shape,
+    prefilled with every token, at the given alphabets and containers; None when
+    the symbol model cannot fit a stream into its container."""
+    import torch
+    from quantized_decode_attention_gb300 import DQError, KVCache, kv_sizes, make_config
+    cfg = make_config(batch=w.batch, n_kv_heads=w.n_kv_heads, n_q_heads=w.n_q_heads, head_dim=w.head_dim,
+                      max_seq=w.seq, kv_dtype=w.kv_dtype, out_dtype="f32", rot_k=w.rot_k, rot_v=w.rot_v,
+                      mean_k=w.mean_k, n_sink=w.n_sink, n_recent=w.n_recent, scheme="rans",
+                      levels_k=levels_k, levels_v=levels_v, container_k=ck, container_v=cv,
+                      rans_alpha=w.extra["alpha"])
+    try:
+        kv_sizes(cfg)
+    except DQError as e:
+        if e.name == "DQ_EINFEASIBLE":
+            return None
+        raise
+    cache = KVCache.allocate(cfg)
+    try:
+        cache.quantize(k_dev, v_dev, pos0=0)
+        out = torch.empty((w.batch, w.n_q_heads, w.head_dim), dtype=torch.float32, device="cuda")
+        cache.attention(q_dev, out, w.seq)
+        torch.cuda.synchronize()
+        cache.check()
+        return out.cpu().numpy().astype(np.float64)
+    finally:
+        cache.close()
+
+
+def dquant_ablation(batch: int = 4, quantized: int = 2048, levels=ABL_LEVELS, budgets=ABL_BUDGETS,
+                    key_bytes=ABL_KEY_BYTES) -> dict:
+    """D-Quant Sec. 5.4 (Fig. 4) on the D-Quant workload's synthetic tokens (batch
+    `batch`, `quantized` quantized tokens plus the 128-token 16-bit window): for each
+    setting, the relative L2 distance and the largest absolute difference between
+    the library's decode-attention output and exact fp64 attention over the same
+    unquantized tokens.  Settings whose streams cannot fit are marked infeasible."""
+    import torch
+    base = W.DQUANT.with_(batch=batch, seq=quantized + W.DQUANT.n_recent)
+    k, v = W.make_kv(base)
+    q = W.make_q(base)
+    ref = exact_attention(q, k, v, base.kv_dtype)
+    dev16 = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).cuda().view(torch.bfloat16)
+    k_dev, v_dev, q_dev = dev16(k), dev16(v), torch.from_numpy(q).cuda()
+
+    def case(mk, mv, ck, cv):
+        e = {**base.extra, "levels_k": mk, "levels_v": mv, "container_k": ck, "container_v": cv}
+        row = {"levels_k": mk, "levels_v": mv, "container_k": ck, "container_v": cv,
+               "bits_per_value": round(W.dquant_bits_per_value(base.with_(extra=e)), 3)}
+        out = dquant_attention_output(base, k_dev, v_dev, q_dev, mk, mv, ck, cv)
+        if out is None:
+            row["infeasible"] = True
+        else:
+            row["rel_l2_err"] = float(np.linalg.norm(out - ref) / np.linalg.norm(ref))
+            row["max_abs_err"] = float(np.abs(out - ref).max())
+        return row
+
+    res = {"workload": f"{base.name}: batch {batch}, {quantized} quantized + {base.n_recent} 16-bit tokens, "
+                       f"{base.n_kv_heads} KV heads (1024-value streams)",
+           "levels": [case(mk, mv, 331, 231) for mk, mv in levels],
+           "budget": [case(8, 6, ck, cv) for ck, cv in budgets],
+           "kv_split": [case(8, 6, ck, ABL_PAIR_BYTES - ck) for ck in key_bytes]}
+    del k_dev, v_dev, q_dev
+    torch.cuda.empty_cache()
+    return res
+
+
 def cpu_baseline(w, bits, S, budget_s, k, v, q):
     """The oracle as it stands, timed on this host's cores: each worker quantizes
     one unit's cache and runs its fp64 decode attention; as many units as fit
@@ -769,6 +868,14 @@ def main():
         line["diagnostics"] = {"dquant_feasible_alphabet": feasible_alphabet(),
                                "note": "largest D-Quant alphabet whose cheapest 1024-value stream fits the "
                                        "container, by the library's symbol model, vs fixed-width levels"}
+        if not args.no_dquant:
+            try:
+                abl = dquant_ablation()
+            except Exception as e:  # a diagnostic never costs the measurement line
+                abl = {"error": f"{type(e).__name__}: {e}"}
+            abl["note"] = ("decode-attention output (fp32) against exact fp64 attention over the unquantized "
+                           "tokens, one D-Quant setting varied at a time around 8 / 6 levels in 331 / 231 bytes")
+            line["diagnostics"]["dquant_ablation"] = abl
     if rank == 0:
         print(json.dumps(line))
     if world > 1:

@@ -189,3 +189,44 @@ def sys_path_bench():
     root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
     if root not in sys.path:
         sys.path.insert(0, root)
+
+
+def test_ablation_reference_is_exact_attention():
+    """The D-Quant ablation (Sec. 5.4, Fig. 4) scores each setting against exact
+    attention over the unquantized tokens.  That reference, as the bench computes
+    it, equals the oracle's fp64 attention on the same bf16 / fp16 tokens, unit by
+    unit, with query head h reading KV head floor(h Hkv / Hq)."""
+    import oracle
+    import workloads as W
+    sys_path_bench()
+    import bench
+    for dt in ("bf16", "f16"):
+        w = W.DQUANT.with_(batch=2, n_kv_heads=2, n_q_heads=8, seq=70, kv_dtype=dt)
+        k, v = W.make_kv(w)
+        q = W.make_q(w)
+        got = bench.exact_attention(q, k, v, dt)
+        K = oracle.raw16_to_f64(k, dt)
+        V = oracle.raw16_to_f64(v, dt)
+        G = w.n_q_heads // w.n_kv_heads
+        for b in range(w.batch):
+            for h in range(w.n_kv_heads):
+                ref = oracle.attention_f64(q[b, h * G:(h + 1) * G], K[b, h], V[b, h], w.head_dim ** -0.5)
+                np.testing.assert_allclose(got[b, h * G:(h + 1) * G], ref, rtol=1e-12, atol=1e-13)
+
+
+def test_ablation_settings_feasibility(lib):
+    """Every setting of the three ablation axes fits its containers by the symbol
+    model, except 16 value levels in 231 bytes: the cheapest 16-level symbol costs
+    more than the 1.77 bits per value that container leaves (the dash of D-Quant
+    Table 2), which the bench reports as infeasible."""
+    import oracle
+    sys_path_bench()
+    import bench
+    n = 1024
+    fits = lambda M, C: int(oracle.DqTable(n, M, alpha=1.4).r.min()) * n <= oracle.dq_budget_fx(C)
+    for mk, mv in bench.ABL_LEVELS:
+        assert fits(mk, 331) and (fits(mv, 231) == (mv != 16)), (mk, mv)
+    for ck, cv in bench.ABL_BUDGETS:
+        assert fits(8, ck) and fits(6, cv), (ck, cv)
+    for ck in bench.ABL_KEY_BYTES:
+        assert fits(8, ck) and fits(6, bench.ABL_PAIR_BYTES - ck), ck

@@ -203,3 +203,50 @@ def test_dquant_noalloc_is_refused():
     with pytest.raises(DQError):
         cache.attention_noalloc(to_device(W.make_q(w), "f32"), out, w.seq)
     cache.close()
+
+
+def _bench():
+    import os
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    if root not in sys.path:
+        sys.path.insert(0, root)
+    import bench
+    return bench
+
+
+def test_dquant_ablation_diagnostic():
+    """The bench's D-Quant ablation (Sec. 5.4, Fig. 4) at a small size: each
+    feasible setting's attention output is the library's, within the attention
+    tolerance of the oracle's output over its own encoding of the same tokens, and
+    its reported distance to exact attention agrees with the oracle's within what
+    that tolerance allows; 16 value levels in 231 bytes are reported infeasible."""
+    import torch
+    bench = _bench()
+    nq = 256
+    w = W.DQUANT.with_(batch=1, seq=nq + W.DQUANT.n_recent)
+    k, v = W.make_kv(w)
+    q = W.make_q(w)
+    exact = bench.exact_attention(q, k, v, w.kv_dtype)
+    settings = [(8, 6, 331, 231), (12, 6, 331, 231), (8, 6, 286, 200), (8, 6, 381, 181)]
+    res = bench.dquant_ablation(batch=1, quantized=nq, levels=((8, 6), (12, 6), (8, 16)), budgets=((286, 200),),
+                                key_bytes=(381,))
+    rows = res["levels"] + res["budget"] + res["kv_split"]
+    assert rows[2]["infeasible"] and (rows[2]["levels_v"], rows[2]["container_v"]) == (16, 231)
+    feasible = [r for r in rows if not r.get("infeasible")]
+    assert [(r["levels_k"], r["levels_v"], r["container_k"], r["container_v"]) for r in feasible] == settings
+    dev16 = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).cuda().view(torch.bfloat16)
+    k_dev, v_dev, q_dev = dev16(k), dev16(v), torch.from_numpy(q).cuda()
+    norm = np.linalg.norm(exact)
+    for row, (mk, mv, ck, cv) in zip(feasible, settings):
+        e = {**w.extra, "levels_k": mk, "levels_v": mv, "container_k": ck, "container_v": cv}
+        wc = w.with_(extra=e, out_dtype="f32")
+        got = bench.dquant_attention_output(wc, k_dev, v_dev, q_dev, mk, mv, ck, cv)
+        ref = OC.attention(wc, q, k, v, wc.seq, OC.quantize_dquant(wc, k, True, wc.seq),
+                           OC.quantize_dquant(wc, v, False, wc.seq))
+        assert np.all(np.abs(got - ref) <= 2e-3), (row, float(np.abs(got - ref).max()))
+        # every output within 2e-3 of the oracle's moves the L2 distance by at most 2e-3 sqrt(N)
+        slack = 2e-3 * np.sqrt(exact.size) / norm + 1e-12
+        assert abs(row["rel_l2_err"] - np.linalg.norm(ref - exact) / norm) <= slack, row
+        assert abs(row["max_abs_err"] - np.abs(ref - exact).max()) <= 2e-3 + 1e-12, row
+        assert 0.0 < row["rel_l2_err"] < 1.0, row
