@@ -234,13 +234,19 @@ def setup_caches(w, bits, S, k_dev, v_dev, copies):
         T, Qc = W.dense_transform(w)
         base.tensors["k_transform"].view(torch.float32).copy_(torch.from_numpy(T).reshape(-1))
         base.tensors["q_comp"].view(torch.float32).copy_(torch.from_numpy(Qc).reshape(-1))
+    base.quantize(k_dev, v_dev, pos0=0)  # the first call also creates the context
+    base.check()
+    p0, p1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    p0.record()
     base.quantize(k_dev, v_dev, pos0=0)
+    p1.record()
+    torch.cuda.synchronize()
     base.check()
     caches = [base]
     for _ in range(copies - 1):
         caches.append(base.clone_shared())
     torch.cuda.synchronize()
-    return caches
+    return caches, p0.elapsed_time(p1)
 
 
 def run_gpu(args, w, bits, S, k_dev, v_dev, q_dev, knew_dev, vnew_dev, rank):
@@ -250,7 +256,7 @@ def run_gpu(args, w, bits, S, k_dev, v_dev, q_dev, knew_dev, vnew_dev, rank):
     ab = algorithmic_bytes(w, bits, S)
     per_copy = ab["total"]
     copies = args.copies or max(3, int(np.ceil(3 * L2 / per_copy)) + 1)
-    caches = setup_caches(w, bits, S, k_dev, v_dev, copies)
+    caches, prefill_ms = setup_caches(w, bits, S, k_dev, v_dev, copies)
     td = {"bf16": torch.bfloat16, "f16": torch.float16, "f32": torch.float32}[w.out_dtype]
     out = torch.empty((w.batch, w.n_q_heads, w.head_dim), dtype=td, device="cuda")
     stream = torch.cuda.Stream()
@@ -308,6 +314,15 @@ def run_gpu(args, w, bits, S, k_dev, v_dev, q_dev, knew_dev, vnew_dev, rank):
             evs[i][1].record(stream)
         stream.synchronize()
         attn_ms = [a.elapsed_time(b) for a, b in evs]
+        # the step's other call alone: quantizing the new token of every sequence
+        qevs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_attn)]
+        torch.cuda._sleep(int(2e8))
+        for i in range(n_attn):
+            qevs[i][0].record(stream)
+            caches[i % nc].quantize(knew_dev, vnew_dev, pos0=pos, stream=stream.cuda_stream)
+            qevs[i][1].record(stream)
+        stream.synchronize()
+        token_ms = [a.elapsed_time(b) for a, b in qevs]
     torch.cuda.synchronize()
     # e2e: through the public API, host buffers: H2D of q and the new token,
     # both calls, D2H of the output, every step.  The step's inputs sit in one
@@ -349,6 +364,9 @@ def run_gpu(args, w, bits, S, k_dev, v_dev, q_dev, knew_dev, vnew_dev, rank):
         "total_ms": total_ms, "attn_ms": statistics.mean(attn_ms), "attn_ms_median": statistics.median(attn_ms),
         "clocks": clk.summary(), "copies": nc, "algo": ab,
         "e2e_tok_s": w.batch * n_e2e / (e2e_ms / 1e3), "h2d": bytes_h2d, "d2h": bytes_d2h,
+        "prefill_ms": prefill_ms, "token_ms": statistics.mean(token_ms),
+        "prefill_bytes": 2 * k_dev.numel() * k_dev.element_size() + sum(
+            t.numel() * t.element_size() for t in caches[0].tensors.values() if t is not None),
     }
     for c in caches[1:]:
         c.detach()
@@ -819,6 +837,11 @@ def main():
                 "d2h_bytes_per_step": res["d2h"],
                 "how": "eager C-ABI calls per step: one pinned-host H2D copy of q and the new token, output D2H"},
         "gpu_launches": 3 * args.steps,
+        "quantize": {"token_us": round(res["token_ms"] * 1e3, 2), "prefill_us": round(res["prefill_ms"] * 1e3, 1),
+                     "prefill_gbs": round(res["prefill_bytes"] / (res["prefill_ms"] / 1e3) / 1e9, 1),
+                     "prefill_bytes": res["prefill_bytes"],
+                     "how": "token: dq_quantize_kv of one new token per sequence alone (CUDA events); prefill: "
+                            "the whole cache from 16-bit K and V, bytes = inputs read + cache buffers written"},
         "variants": {k2: {"value": round(w.batch / (r["total_ms"] / args.steps / 1e3), 1),
                           "ms_per_step": round(r["total_ms"] / args.steps, 5), "roofline": roof(r, int(k2[0])),
                           "e2e_tok_s": round(r["e2e_tok_s"], 1)} for k2, r in variants.items()},
