@@ -724,6 +724,111 @@ def dquant_ablation(batch: int = 4, quantized: int = 2048, levels=ABL_LEVELS, bu
     return res
 
 
+def codes_of_records(rec: np.ndarray, bits: int) -> np.ndarray:
+    """Every code held in fixed-stride records (uint8 [..., record bytes]; key
+    rows or value pair records), in no particular order.  Records are
+    little-endian 32-bit words.  At 2 and 4 bits each 16-bit half holds 16/b
+    fields.  At 3 bits, a 2-bit plane of R/16 words comes first (the 2-bit
+    layout), then a 1-bit plane: field i of half h keeps its low two bits at
+    bit 16h + 2(i mod 8) of plane word i/8, and its high bit at bit
+    16h + (i mod 16) of 1-bit-plane word i/16."""
+    w = np.ascontiguousarray(rec, dtype=np.uint8)
+    w = w.reshape(-1, w.shape[-1]).view("<u4").astype(np.int64)
+    if bits in (2, 4):
+        sh = np.array([16 * h + bits * f for h in (0, 1) for f in range(16 // bits)])
+        return ((w[:, :, None] >> sh) & ((1 << bits) - 1)).ravel()
+    R = w.shape[1] * 32 // 3                  # codes per record
+    i = np.arange(R // 2)
+    out = []
+    for h in (0, 1):
+        lo = (w[:, i >> 3] >> (16 * h + 2 * (i & 7))) & 3
+        hi = (w[:, R // 16 + (i >> 4)] >> (16 * h + (i & 15))) & 1
+        out.append(lo | (hi << 2))
+    return np.concatenate(out, axis=1).ravel()
+
+
+def coding_stats(hist: np.ndarray, p: np.ndarray) -> dict:
+    """D-Quant Sec. 3 (Table 1) for a symbol histogram over M levels against a model p:
+    the empirical entropy H (bits per value), Coding Gain = log2 M - H (what entropy
+    coding could save over fixed-width codes) and Normal Gap = CE - H (the extra
+    rate of coding with p instead of the empirical frequencies; CE the cross-entropy)."""
+    q = np.asarray(hist, dtype=np.float64)
+    q = q / q.sum()
+    nz = q > 0
+    H = float(-(q[nz] * np.log2(q[nz])).sum())
+    CE = float(-(q[nz] * np.log2(np.asarray(p, dtype=np.float64)[nz])).sum())
+    return {"entropy": H, "coding_gain": float(np.log2(len(q))) - H, "normal_gap": CE - H}
+
+
+def hadamard_rows(x: np.ndarray) -> np.ndarray:
+    """Rows of x times the normalized Sylvester Hadamard matrix, in fp64."""
+    d = x.shape[-1]
+    Hn = np.array([[1.0]])
+    while Hn.shape[0] < d:
+        Hn = np.block([[Hn, Hn], [Hn, -Hn]])
+    return np.asarray(x, dtype=np.float64) @ (Hn / np.sqrt(d))
+
+
+def preprocessing_row(tensor: str, name: str, x: np.ndarray, xhat: np.ndarray, codes_buf: np.ndarray,
+                      record_bytes: int, p: np.ndarray) -> dict:
+    """One row of the Table 1 analogue: x the tokens in the quantizer's space (fp64),
+    xhat their dequantized values, codes_buf a cache's whole code buffer (flat
+    uint8, records of record_bytes back to back), p the model of the 8 levels."""
+    err = x - xhat
+    codes = codes_of_records(np.asarray(codes_buf, dtype=np.uint8).reshape(-1, record_bytes), 3)
+    row = {"tensor": tensor, "preprocessing": name, "nmse": float((err * err).sum() / (x * x).sum())}
+    row.update(coding_stats(np.bincount(codes, minlength=8), p))
+    return row
+
+
+def preprocessing_effect(batch: int = 2, seq: int = 2048) -> dict:
+    """D-Quant Sec. 3 (Table 1) on the Llama-shaped synthetic keys (channel means
+    and outlier channels) and values: each token's head vector on an 8-level
+    min/max grid (the library's 3-bit affine quantizer, fp32 s and o), raw, after
+    the Hadamard rotation, and (keys) after also removing the channel mean.  Per
+    row: NMSE of the dequantized values (in the quantizer's space, against the
+    power of the rotated tokens), the codes' empirical entropy, Coding Gain and
+    Normal Gap against the library's analytic order-statistics model for d values."""
+    import torch
+    from quantized_decode_attention_gb300 import KVCache, make_config, symbol_probs
+    if seq % 2:
+        raise ValueError("seq must be even (value records hold token pairs)")
+    w = W.LLAMA.with_(batch=batch, seq=seq)
+    B, H, d = w.batch, w.n_kv_heads, w.head_dim
+    k, v = W.make_kv(w)
+    p = np.array(symbol_probs(d, 8))
+    dev16 = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).cuda().view(torch.bfloat16)
+    k_dev, v_dev = dev16(k), dev16(v)
+    xs = {0: W.bf16_bits_to_f32(k).astype(np.float64), 1: W.bf16_bits_to_f32(v).astype(np.float64)}
+    rows = []
+    for name, rot, mean, values in (("raw", "none", False, True), ("hadamard", "hadamard", False, True),
+                                    ("hadamard+mean", "hadamard", True, False)):
+        cfg = make_config(batch=B, n_kv_heads=H, n_q_heads=w.n_q_heads, head_dim=d, max_seq=seq, kv_dtype="bf16",
+                          meta_dtype="f32", out_dtype="f32", bits=3, rot_k=rot, rot_v=rot, mean_k=mean,
+                          n_sink=0, n_recent=0)
+        cache = KVCache.allocate(cfg)
+        try:
+            cache.quantize(k_dev, v_dev, pos0=0)
+            xh = torch.empty((B, H, seq, d), dtype=torch.float32, device="cuda")
+            for which in ((0, 1) if values else (0,)):
+                cache.dequantize(which, 0, seq, xh)
+                torch.cuda.synchronize()
+                cache.check()
+                x = hadamard_rows(xs[which]) if rot == "hadamard" else xs[which]
+                rec = 3 * d // 8 if which == 0 else 3 * d // 4   # key row / value pair record
+                n_rec = seq if which == 0 else seq // 2               # records written per unit
+                buf = cache.tensors["codes_k" if which == 0 else "codes_v"].cpu().numpy()
+                buf = buf.reshape(B * H, -1, rec)[:, :n_rec]          # [unit][slot capacity][record]
+                rows.append(preprocessing_row("k" if which == 0 else "v", name, x,
+                                              xh.cpu().numpy().astype(np.float64), buf, rec, p))
+        finally:
+            cache.close()
+    del k_dev, v_dev
+    torch.cuda.empty_cache()
+    return {"workload": f"{w.name}: batch {batch}, {seq} tokens, {H} KV heads, d {d}; 8 levels per token and head",
+            "model": [round(x, 6) for x in p.tolist()], "rows": rows}
+
+
 def cpu_baseline(w, bits, S, budget_s, k, v, q):
     """The oracle as it stands, timed on this host's cores: each worker quantizes
     one unit's cache and runs its fp64 decode attention; as many units as fit
@@ -899,6 +1004,14 @@ def main():
             abl["note"] = ("decode-attention output (fp32) against exact fp64 attention over the unquantized "
                            "tokens, one D-Quant setting varied at a time around 8 / 6 levels in 331 / 231 bytes")
             line["diagnostics"]["dquant_ablation"] = abl
+        try:
+            pre = preprocessing_effect()
+        except Exception as e:  # a diagnostic never costs the measurement line
+            pre = {"error": f"{type(e).__name__}: {e}"}
+        pre["note"] = ("8-level per-token grids of the Llama-shaped synthetic K and V through the library's "
+                       "3-bit quantizer: NMSE, entropy, Coding Gain = log2 M - H, Normal Gap = CE - H against "
+                       "the analytic order-statistics model")
+        line["diagnostics"]["preprocessing"] = pre
     if rank == 0:
         print(json.dumps(line))
     if world > 1:

@@ -259,6 +259,19 @@ dq_status dq_dequantize_kv(dq_ctx **ctx, const dq_config *cfg, const dq_kv_buffe
 dq_status dq_rans_model(const dq_config *cfg, int which, int *levels, int f[16], int c[16]);
 
 /*
+ * The analytic symbol probabilities before sharpening: for streams of n
+ * values on a per-token grid of `levels` levels, level m sits at normalized
+ * position -a + 2a m/(levels-1), a = E[max of n iid N(0,1)], and p[m] is the
+ * standard-normal mass of its bin (edges at the midpoints, outer bins open).
+ * D-Quant Sec. 4.2 ("Gaussian order statistics"); Sec. 3 Table 1 and App. C
+ * (Fig. 6 middle) compare this model with measured symbol frequencies (the
+ * "Normal Gap").  Writes p[0..levels) (summing to 1) and zeros up to 16.
+ * Host only: no device, stream or context is touched.
+ * Errors: DQ_EINVAL (p NULL, n < 1, levels outside [2, 16]).
+ */
+dq_status dq_symbol_probs(int n, int levels, double p[16]);
+
+/*
  * Synchronize `stream`, then return and clear the device-side status latched
  * by earlier calls on this context (DQ_OK, DQ_ENONFINITE, DQ_ETIMEOUT,
  * DQ_EINFEASIBLE for a stream over its container or a full NUQ key side

@@ -84,8 +84,9 @@ def load() -> C.CDLL:
     L.dq_status_name.argtypes = [C.c_int]
     L.dq_rans_model.argtypes = [C.POINTER(Config), C.c_int, C.POINTER(C.c_int), C.POINTER(C.c_int),
                                 C.POINTER(C.c_int)]
+    L.dq_symbol_probs.argtypes = [C.c_int, C.c_int, C.POINTER(C.c_double)]
     for f in ("dq_kv_sizes", "dq_quantize_kv", "dq_decode_attention", "dq_dequantize_kv", "dq_check",
-              "dq_rans_model"):
+              "dq_rans_model", "dq_symbol_probs"):
         getattr(L, f).restype = C.c_int
     _lib = L
     return L
@@ -98,6 +99,14 @@ def rans_model(cfg: Config, which: int):
     c = (C.c_int * 16)()
     _raise(load().dq_rans_model(C.byref(cfg), which, C.byref(M), f, c))
     return list(f[:M.value]), list(c[:M.value])
+
+
+def symbol_probs(n: int, levels: int):
+    """Unsharpened level probabilities of the Gaussian order-statistics model
+    for streams of n values on a per-token grid of `levels` levels."""
+    p = (C.c_double * 16)()
+    _raise(load().dq_symbol_probs(n, levels, p))
+    return list(p[:levels])
 
 
 def _raise(st: int):

@@ -510,6 +510,17 @@ dq_status dq_rans_model(const dq_config *cfg, int which, int *levels, int f[16],
     return ok();
 }
 
+dq_status dq_symbol_probs(int n, int levels, double p[16]) {
+    if (!p) return fail(DQ_EINVAL, "p is NULL");
+    if (n < 1) return fail(DQ_EINVAL, "n must be positive (got %d)", n);
+    if (levels < 2 || levels > dq::RANS_MAX_LEVELS)
+        return fail(DQ_EINVAL, "levels must be in [2, %d] (got %d)", dq::RANS_MAX_LEVELS, levels);
+    double q[dq::RANS_MAX_LEVELS];
+    if (dq::rans_model_probs(n, levels, q) != 0) return fail(DQ_EINVAL, "no symbol model");
+    for (int m = 0; m < 16; m++) p[m] = m < levels ? q[m] : 0.0;
+    return ok();
+}
+
 const char *dq_status_name(dq_status s) {
     switch (s) {
         case DQ_OK: return "DQ_OK";

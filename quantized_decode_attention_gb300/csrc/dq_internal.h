@@ -56,6 +56,9 @@ struct RansDevTables {
     RansTable k, v;
     float F[512];                            // fp32(2^(k/512))
 };
+// Unsharpened level probabilities p[0..M) of the Gaussian order-statistics model
+// for streams of n values (0, or -1 for n < 1 or M outside [2, 16]).
+int rans_model_probs(int n, int M, double *p);
 int rans_build_table(int n, int M, double alpha, int prob_bits, int C, RansTable *t);
 void rans_pow2_table(float *F);
 

@@ -53,17 +53,26 @@ double expected_max_normal(int n) {
 
 }  // namespace
 
-int rans_build_table(int n, int M, double alpha, int prob_bits, int C, RansTable *t) {
-    const int total = 1 << prob_bits;
-    if (M < 2 || M > RANS_MAX_LEVELS || prob_bits != 8) return -1;
+int rans_model_probs(int n, int M, double *p) {
+    if (n < 1 || M < 2 || M > RANS_MAX_LEVELS) return -1;
     const double a = expected_max_normal(n);
-    double p[RANS_MAX_LEVELS], z = 0.0;
     for (int m = 0; m < M; m++) {
         // bin of level m: midpoints to its neighbours on the grid -a + 2a m/(M-1)
         const double um = -a + 2.0 * a * m / (M - 1);
         const double lo = m == 0 ? 0.0 : normal_cdf(um - a / (M - 1));
         const double hi = m == M - 1 ? 1.0 : normal_cdf(um + a / (M - 1));
-        p[m] = std::pow(hi - lo, alpha);
+        p[m] = hi - lo;
+    }
+    return 0;
+}
+
+int rans_build_table(int n, int M, double alpha, int prob_bits, int C, RansTable *t) {
+    const int total = 1 << prob_bits;
+    if (M < 2 || M > RANS_MAX_LEVELS || prob_bits != 8) return -1;
+    double p[RANS_MAX_LEVELS], z = 0.0;
+    if (rans_model_probs(n, M, p) != 0) return -1;
+    for (int m = 0; m < M; m++) {
+        p[m] = std::pow(p[m], alpha);
         z += p[m];
     }
     int sum = 0;
