@@ -278,6 +278,9 @@ dq_status dq_symbol_probs(int n, int levels, double p[16]);
  * channel, DQ_EINVAL for a container
  * that asked for more bytes than it holds), or
  * DQ_ECUDA if the stream reports an error.  ctx may be NULL (returns DQ_OK).
+ * DQ_ETIMEOUT means a kernel stopped waiting after its time limit (2 s) so
+ * that it could not hang: that call's output is not valid, and the context
+ * may keep a stale per-unit count, so free it (dq_free) and start a new one.
  */
 dq_status dq_check(dq_ctx *ctx, void *stream);
 
