@@ -315,3 +315,185 @@ def test_drift_makes_sparse_local_corrections(M, C, frac_max):
         assert d.max() <= 1
         changed += int((d > 0).sum())
     assert changed / (200 * 1024) < frac_max
+
+
+# ---- Algorithm 1 as a sequence of steps -------------------------------------
+
+ALG1 = os.path.join(os.path.dirname(__file__), "golden", "alg1_hand.json")
+
+
+def _f16_bits(v: float) -> int:
+    return int(np.array([v], dtype=np.float16).view(np.uint16)[0])
+
+
+def _f16_val(bits: int) -> float:
+    return float(np.array([bits], dtype=np.uint16).view(np.float16)[0])
+
+
+def _lstsq(x, m):
+    A = np.stack([np.asarray(m, np.float64), np.ones(len(x))], 1)
+    return np.linalg.lstsq(A, np.asarray(x, np.float64), rcond=None)[0]
+
+
+def test_algorithm1_hand_worked_stream():
+    """App. A Algorithm 1 on a stream worked by hand (tests/golden/alg1_hand.json):
+    FitMinMax, Drift, Refit, fp16 s and o, Drift, then the coder.  The fixture's
+    own steps are checked with a library least-squares solve and numpy's fp16
+    rounding, and each plausible wrong order (no refit, no second Drift, fp16
+    before the first Drift) is shown to give a different stream."""
+    d = json.load(open(ALG1))
+    x = np.array(d["x"], dtype=np.float32)
+    M, C = d["M"], d["container"]
+    t = oracle.DqTable.from_freqs(d["freqs"])
+    r = oracle.dq_encode_stream(x, t, C)
+    want_s16, want_o16 = d["step4_fp16"]["s16_bits"], d["step4_fp16"]["o16_bits"]
+    assert r["flags"] == 0
+    assert (r["s16"], r["o16"]) == (want_s16, want_o16)
+    assert r["m"].tolist() == d["step5_drift_symbols"]
+    m, xf, _ = oracle.rans_decode(r["container"], x.size, t)
+    assert m.tolist() == d["step5_drift_symbols"] and xf == L_STATE
+
+    # the fixture is consistent with the page's steps
+    s0 = (np.float32(x.max()) - np.float32(x.min())) / np.float32(M - 1)
+    assert float(s0) == d["step1_fitminmax"]["s"] and float(x.min()) == d["step1_fitminmax"]["o"]
+    grid0 = np.float32(0.0) + s0 * np.arange(M, dtype=np.float32)
+    assert np.argmin(np.abs(x[:, None] - grid0[None, :]), 1).tolist() == d["step2_drift_symbols"]
+    ls, lo = _lstsq(x, d["step2_drift_symbols"])
+    assert abs(ls - d["step3_refit"]["s"]) < 1e-12 and abs(lo - d["step3_refit"]["o"]) < 1e-12
+    assert (_f16_bits(ls), _f16_bits(lo)) == (want_s16, want_o16)
+    g16 = np.float32(_f16_val(want_o16)) + np.float32(_f16_val(want_s16)) * np.arange(M, dtype=np.float32)
+    assert np.argmin(np.abs(x[:, None] - g16[None, :]), 1).tolist() == d["step5_drift_symbols"]
+
+    # each wrong order, run through the oracle's own (separately pinned) steps
+    m1, _, _ = oracle.dq_drift(x, float(s0), 0.0, t, C)
+    assert m1.tolist() == d["step2_drift_symbols"]
+    assert _f16_bits(float(s0)) != want_s16                                   # Refit dropped
+    assert m1.tolist() != d["step5_drift_symbols"]                            # second Drift dropped
+    mA, _, _ = oracle.dq_drift(x, _f16_val(_f16_bits(float(s0))), 0.0, t, C)  # fp16 before the first Drift
+    sA, oA = oracle.dq_refit(x, mA, 0.0, 0.0)
+    assert (_f16_bits(sA), _f16_bits(oA)) != (want_s16, want_o16)
+    w = d["wrong_orders"]
+    assert _f16_val(_f16_bits(float(s0))) == w["no_refit_s16"]
+    assert (_f16_val(_f16_bits(sA)), _f16_val(_f16_bits(oA))) == (w["fp16_before_first_drift"]["s16"],
+                                                                    w["fp16_before_first_drift"]["o16"])
+
+
+def test_algorithm1_final_symbols_are_drift_on_the_fp16_refit_grid():
+    """With a budget that binds (Drift moves symbols away from nearest rounding),
+    the stream's s and o are the fp16 least-squares fit to the first Drift's
+    symbols on the min/max grid, and its symbols are Drift on that fp16 grid
+    (App. A Algorithm 1, lines FitMinMax to the second Drift)."""
+    t = oracle.DqTable(64, 8)
+    F = oracle.dq_pow2_table()
+    rng = np.random.default_rng(21)
+    C, checked, bound = 22, 0, 0
+    for _ in range(20):
+        x = rng.standard_normal(64).astype(np.float32)
+        s0 = (np.float32(x.max()) - np.float32(x.min())) / np.float32(7)
+        o0 = np.float32(x.min())
+        grid = o0 + s0 * np.arange(8, dtype=np.float32)
+        near = np.argmin(np.abs(x[:, None] - grid[None, :]), 1)
+        m1, _, ok1 = oracle.dq_drift(x, float(s0), float(o0), t, C, F)
+        bound += not np.array_equal(m1, near)
+        ls, lo = _lstsq(x, m1)
+        # skip a sample whose fp64 fit sits within fp32 noise of an fp16 rounding boundary
+        if any(abs(float(np.float16(v)) - v) > 0.49 * abs(float(np.spacing(np.float16(v)))) for v in (ls, lo)):
+            continue
+        r = oracle.dq_encode_stream(x, t, C, F)
+        assert r["flags"] == 0
+        assert (r["s16"], r["o16"]) == (_f16_bits(ls), _f16_bits(lo))
+        m2, _, _ = oracle.dq_drift(x, _f16_val(r["s16"]), _f16_val(r["o16"]), t, C, F)
+        assert np.array_equal(r["m"], m2)
+        checked += 1
+    assert checked >= 15 and bound == 20
+
+
+# ---- whole-cache assembly ----------------------------------------------------
+
+def _hadamard(d):
+    scipy_linalg = pytest.importorskip("scipy.linalg")
+    return scipy_linalg.hadamard(d).astype(np.float64)
+
+
+def test_dquant_key_streams_are_head_major_rows_minus_the_window_mean():
+    """Stream assembly of the key cache (Sec. 4.2: one token's key over all KV
+    heads forms a stream; keys are rotated and lose a windowed channel mean).
+    Keys are built so that the rotated rows are known dyadic values y = z + c_w,
+    with z summing to zero over each 128-token window and c_w a window constant
+    exactly representable as INT8 times 2^-6.  The oracle's window means must
+    then be exactly c_w and its streams exactly the head-major concatenation of
+    z, which is checked by encoding those streams directly."""
+    H, d, ns, nq = 2, 64, 2, 300
+    S = ns + nq
+    n = H * d
+    rng = np.random.default_rng(31)
+    Hm = _hadamard(d)
+    nw = -(-nq // 128)
+    kq = rng.integers(-126, 127, size=(nw, n))
+    kq[:, 0] = 127                                      # max |mu| = 127 * 2^-6: the scale is exactly 2^-6
+    kq[:, 1] = -127
+    c = kq * 2.0 ** -6                                  # window constants [nw, n]
+    z = np.zeros((nq, n))
+    for w0 in range(0, nq, 128):                        # zero-sum pairs inside every window
+        cnt = min(128, nq - w0)
+        for t in range(w0, w0 + cnt - 1, 2):
+            v = rng.integers(-64, 65, size=n) * 2.0 ** -5
+            z[t], z[t + 1] = v, -v
+    y = z + c[np.arange(nq) // 128]                     # rotated, stream order [nq, H*d]
+    yh = y.reshape(nq, H, d).transpose(1, 0, 2)         # [H, nq, d]
+    # the raw key whose normalized Hadamard rotation (H/8 at d = 64) is y, exactly
+    kraw = np.zeros((1, H, S, d), dtype=np.float32)
+    kraw[0, :, ns:] = (yh @ Hm) / 8.0
+    kraw[0, :, :ns] = rng.standard_normal((H, ns, d)).astype(np.float32)   # sinks: outside every stream
+    w = __import__("workloads").DQUANT.with_(batch=1, n_kv_heads=H, n_q_heads=4 * H, head_dim=d, seq=S,
+                                             kv_dtype="f32", n_sink=ns, n_recent=0,
+                                             extra={**__import__("workloads").DQUANT.extra,
+                                                    "container_k": 64, "container_v": 48})
+    dt = oracle.quantize_dquant(w, kraw, True, S)
+    assert np.array_equal(dt.mean_q[0].astype(np.int64), kq)
+    assert np.all(dt.mean_sc[0] == _f16_bits(2.0 ** -6))
+    assert np.array_equal(dt.mu_hat[0].astype(np.float64), c)
+    tk, _ = oracle.cache.dq_tables(w)
+    cont, s16, o16, m, flags = oracle.dq_encode_streams(z.astype(np.float32), tk, 64)
+    assert np.array_equal(dt.container[0], cont) and np.array_equal(dt.m[0], m)
+    assert np.array_equal(dt.s16[0], s16) and np.array_equal(dt.o16[0], o16)
+    assert np.array_equal(dt.flags[0], flags)
+    # values: no rotation, no mean, the same head-major assembly of the raw rows
+    vraw = np.zeros((1, H, S, d), dtype=np.float32)
+    vraw[0, :, ns:] = yh
+    dv = oracle.quantize_dquant(w, vraw, False, S)
+    _, tv = oracle.cache.dq_tables(w)
+    cont, s16, o16, m, _ = oracle.dq_encode_streams(y.astype(np.float32), tv, 48)
+    assert dv.mean_q is None
+    assert np.array_equal(dv.container[0], cont) and np.array_equal(dv.m[0], m)
+
+
+def test_dquant_dequant_is_eq7_then_the_inverse_rotation():
+    """Dequantization (App. A Eq. (7)): k^ = s m + o + mu per stream value, then
+    the stream is split into heads and rotated back with the normalized Hadamard
+    matrix from scipy (its own inverse)."""
+    import workloads as W
+    H, d, ns, nq = 2, 64, 1, 260
+    S = ns + nq
+    w = W.DQUANT.with_(batch=2, n_kv_heads=H, n_q_heads=4 * H, head_dim=d, seq=S, kv_dtype="bf16", n_sink=ns,
+                       n_recent=0, extra={**W.DQUANT.extra, "container_k": 64, "container_v": 48})
+    k, v = W.make_kv(w)
+    Hn = _hadamard(d) / np.sqrt(d)
+    for is_key, x in ((True, k), (False, v)):
+        dt = oracle.quantize_dquant(w, x, is_key, S)
+        s = dt.s16.view(np.float16).astype(np.float64)
+        o = dt.o16.view(np.float16).astype(np.float64)
+        want = np.zeros((2, H, nq, d))
+        for b in range(2):
+            for t in range(nq):
+                vals = s[b, t] * dt.m[b, t].astype(np.float64) + o[b, t]
+                if is_key:
+                    vals = vals + dt.mu_hat[b, t // 128].astype(np.float64)
+                for h in range(H):
+                    row = vals[h * d:(h + 1) * d]
+                    want[b, h, t] = Hn @ row if is_key else row
+        got = oracle.dquant_dequant_f64(w, dt, is_key)
+        assert np.abs(got - want).max() < 1e-12
+        # and the result is close to the input it encodes (a 2-3 bit grid)
+        xin = W.bits_to_f32(x, w.kv_dtype)[:, :, ns:S].astype(np.float64)
+        assert np.sqrt(np.mean((got - xin) ** 2)) < 0.5
