@@ -53,6 +53,8 @@ def parse():
     p.add_argument("--no-dquant", action="store_true", help="skip the D-Quant cache measurement")
     p.add_argument("--qwen", default="32768,131072", help="Qwen3-8B-shaped long-context lengths measured")
     p.add_argument("--no-bf16", action="store_true", help="skip the unquantized 16-bit cache context entry")
+    p.add_argument("--profile-attn", action="store_true",
+                   help="profiler run: one Llama-shaped cache at --bits, warmup + steps attention calls, no timing")
     return p.parse_args()
 
 
@@ -852,8 +854,34 @@ def cpu_baseline(w, bits, S, budget_s, k, v, q):
                       f"full call"}
 
 
+def profile_attention(args):
+    """A short run for a profiler to capture: the Llama-shaped cache at
+    args.bits (prefilled once), then args.warmup + args.steps decode-attention
+    calls on one stream.  Nothing is timed here."""
+    import torch
+    import __graft_entry__
+    __graft_entry__.build()
+    w = W.LLAMA.with_(bits=args.bits)
+    S = w.seq
+    k, v = W.make_kv(w)
+    dev16 = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).cuda().view(torch.bfloat16)
+    k_dev, v_dev = dev16(k), dev16(v)
+    q_dev = torch.from_numpy(W.make_q(w)).cuda()
+    caches, _ = setup_caches(w, args.bits, S, k_dev, v_dev, 1)
+    out = torch.empty((w.batch, w.n_q_heads, w.head_dim), dtype=torch.bfloat16, device="cuda")
+    for _ in range(args.warmup + args.steps):
+        caches[0].attention(q_dev, out, S, w.head_dim ** -0.5)
+    torch.cuda.synchronize()
+    caches[0].check()
+    caches[0].close()
+    print(json.dumps({"profile_attn": w.name, "bits": args.bits, "calls": args.warmup + args.steps}))
+
+
 def main():
     args = parse()
+    if args.profile_attn:
+        profile_attention(args)
+        return
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     w = W.LLAMA.with_(bits=args.bits)

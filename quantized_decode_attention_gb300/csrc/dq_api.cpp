@@ -687,6 +687,11 @@ dq_status dq_decode_attention(dq_ctx **ctx, const dq_config *cfg, const dq_kv_bu
     a.partials = c->partials;
     a.counters = c->counters;
     a.status = c->status;
+    if (c->counters_dirty) {
+        if (cudaMemsetAsync(c->counters, 0, sizeof(int) * L.U, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+            return fail(DQ_ECUDA, "clearing the record counts failed");
+        c->counters_dirty = 0;
+    }
     dq::set_nuq_args(L, bufs, a);
     int e = dq::plan_attention(L, a, c->num_sms, static_cast<long long>(c->partials_cap));
     if (e != 0) return fail(DQ_ECUDA, "attention planning: %s", cudaGetErrorString(static_cast<cudaError_t>(e)));
@@ -731,7 +736,12 @@ dq_status dq_check(dq_ctx *ctx, void *stream) {
     if (cudaMemcpy(&st, ctx->status, sizeof st, cudaMemcpyDeviceToHost) != cudaSuccess)
         return fail(DQ_ECUDA, "status read failed");
     if (st && cudaMemset(ctx->status, 0, sizeof st) != cudaSuccess) return fail(DQ_ECUDA, "status clear failed");
-    if (st & dq::ST_TIMEOUT) return fail(DQ_ETIMEOUT, "a bounded device wait ran out");
+    if (st & dq::ST_TIMEOUT) {
+        // a wait that ran out may leave a unit's record count behind: the next
+        // attention call starts from cleared counts
+        ctx->counters_dirty = 1;
+        return fail(DQ_ETIMEOUT, "a bounded device wait ran out");
+    }
     if (st & dq::ST_INFEASIBLE) return fail(DQ_EINFEASIBLE, "a stream did not fit its container");
     if (st & dq::ST_SIDE_FULL)
         return fail(DQ_EINFEASIBLE, "the key outlier side channel is full: later decode-key outliers keep their level");

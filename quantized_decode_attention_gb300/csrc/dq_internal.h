@@ -190,6 +190,14 @@ struct AttnArgs {
     const uint16_t *ol_col_v, *ol_val_v;  // [U][Qcap][k_out_v]
     long long rp_stride, nnzk_cap;
     int k_out_v;                          // value outliers per token (0: none)
+    // affine 2/4-bit kernel schedule (set by plan_affine; affine = 1 routes the
+    // launch to it)
+    int affine;
+    long long n_pt;                       // 16-token packed tiles per unit
+    long long cpu;                        // packed chunks per unit
+    long long np_total, nr_total;         // packed chunks / 16-bit tiles of all units
+    int wp;                               // packed warps per CTA
+    int mps;                              // record slots per unit taken by packed CTAs
 };
 
 struct DequantArgs {
@@ -224,6 +232,14 @@ int launch_qcomp(const Layout &L, const float *q, const float *qc, float *qt, vo
 int plan_attention(const Layout &L, AttnArgs &a, int num_sms, long long cap_floats);
 long long attention_partial_floats(const Layout &L, const AttnArgs &a);
 size_t attention_smem_bytes(const Layout &L);
+// The affine kernel for 2- and 4-bit codes (attn_affine.cu); plan_attention
+// routes a call to it when it applies (a supported shape whose packed tokens
+// carry at least as many bytes as its 16-bit slots) and marks a.affine.
+bool affine_kernel_applies(const Layout &L, const AttnArgs &a);
+int plan_affine(const Layout &L, AttnArgs &a, int num_sms, long long cap_floats);
+long long affine_partial_floats(const Layout &L, const AttnArgs &a);
+int launch_affine(const Layout &L, const AttnArgs &a, void *stream);
+size_t affine_smem_bytes(const Layout &L);
 
 }  // namespace dq
 
@@ -236,6 +252,7 @@ struct dq_ctx {
     float *partials;     // split partials
     size_t partials_cap; // floats
     int *counters;       // [U]
+    int counters_dirty;  // set by dq_check after a timeout: clear the counts before the next call
     uint32_t *nuq_bits;  // non-uniform scheme: key outlier bitmap scratch [U][Qcap][d/32]
     dq::RansDevTables *rans;  // entropy-coded scheme: symbol models (device)
     uint8_t *rans_sym;   // entropy-coded scheme: symbol scratch of a prefill
