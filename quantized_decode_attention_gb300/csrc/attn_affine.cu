@@ -1,5 +1,5 @@
-// Split-K GQA decode attention over the packed affine cache with 2- or 4-bit
-// codes (sm_103a).
+// Split-K GQA decode attention over the packed affine cache with 2-, 3- or
+// 4-bit codes (sm_103a).
 //
 // Per sequence b and query head h reading KV head h / G it computes
 //   out_h = sum_t softmax_t(sm_scale * q_h . k^_t) v^_t,
@@ -80,7 +80,7 @@ struct ACfg {
     static constexpr int RING_P = AF_WPB * NS * SLOT;
     static constexpr int RING_R = (AF_WPB - 1) * NS * SLOT + AF_NSR * RSLOT;
     static constexpr int RING = RING_P > RING_R ? RING_P : RING_R;
-    static_assert(AF_WPB * 4 * PR * 4 <= RING, "final states overlay the rings");
+    static_assert(AF_WPB * 4 * PR * 4 <= RING, "the warps' final states overlay the rings");
 };
 
 template <int D, int BITS, bool M16>
@@ -91,8 +91,6 @@ struct ASmem {
     uint16_t rqh[AF_NUR][2][4][D + 8]; // 16-bit-tile warp: (hi, lo) halves of its units' raw q
     float uacc[AF_NUS][4][C::PR];      // per unit: states folded in by warps on their second move
     float save[AF_WPB][4][C::PR];      // a warp's first finished unit segment
-    float mw[AF_NUS][2 * AF_WPB + 1][4];  // final merge: weight of each source per (unit, head)
-    float mM[AF_NUS][4];
     int ulock[AF_NUS];
     int fin_u[AF_WPB];                 // unit of a warp's final state (-1: none)
     int save_u[AF_WPB];                // unit of a warp's saved state (-1: none)
@@ -355,7 +353,7 @@ __device__ __forceinline__ void fold_into_unit(ASmem<D, BITS, M16> &S, int i, Wa
         for (int rr = 0; rr < 2; rr++) {
             const int row = 16 * mi + 8 * rr + g;
             const float v = (st.acc[mi][2 * rr] + st.acc[mi][2 * rr + 1]) *
-                                exp2f(static_cast<float>(24 - field_exp(2 * mi + rr, BITS))) +
+                                pow2i(24 - field_exp(2 * mi + rr, BITS)) +
                             st.ao;
             ua[row] = ua[row] * as + v * aw;
         }
@@ -485,7 +483,6 @@ __global__ void __launch_bounds__(AF_WPB * 32, 1) attn_affine_kernel(AttnArgs a,
             for (int s = 0; s < AF_NSR; s++) mbar_init(&S.rfull[s], 1);
         }
         fence_mbar_init();
-        S.fin_u[warp] = -1;
         S.save_u[warp] = -1;
         if (warp < AF_NUS + AF_NUR) S.done_u[warp] = -1;
         if (warp < AF_NUS) S.ulock[warp] = 0;
@@ -671,95 +668,77 @@ __global__ void __launch_bounds__(AF_WPB * 32, 1) attn_affine_kernel(AttnArgs a,
     }
     if (timed_out && lane == 0) atomicOr(a.status, ST_TIMEOUT);
 
-    // ---- merge per unit: the shared accumulator and the warps' final states;
-    // one record per (unit, CTA)
-    __syncthreads();  // every ring is idle: the final states overlay them
+    // ---- merge per unit: each warp's final state (stored over the now idle
+    // rings), the warps' saved states and the unit's shared accumulator are
+    // summed, scaled to the unit's maximum, by one warp per (unit, head)
+    __syncthreads();
     float *fin = reinterpret_cast<float *>(S.ring);  // [AF_WPB][4][PR]
-    if (cu >= 0) {
-        store_state<D, BITS>(st, true, fin + warp * 4 * PR, PR);
-        if (lane == 0) S.fin_u[warp] = cu;
-    }
+    if (cu >= 0) store_state<D, BITS>(st, true, fin + warp * 4 * PR, PR);
+    if (lane == 0) S.fin_u[warp] = cu;
     __syncthreads();
-    // sources of a unit's record, per head: z < AF_WPB warp z's final state,
-    // AF_WPB <= z < 2 AF_WPB warp z - AF_WPB's saved state, z = 2 AF_WPB the
-    // unit's shared accumulator; each phase below runs one thread per item
-    constexpr int NSRC = 2 * AF_WPB + 1;
-    auto src_of = [&](int i, int z, int h) -> const float * {
-        if (z < AF_WPB) return fin + (z * 4 + h) * PR;
-        if (z < 2 * AF_WPB) return &S.save[z - AF_WPB][h][0];
-        return &S.uacc[i][h][0];
-    };
-    for (int t = threadIdx.x; t < n_units * NSRC * 4; t += blockDim.x) {  // each source's maximum, or -inf
-        const int i = t / (NSRC * 4), z = (t >> 2) % NSRC, h = t & 3, u = u_first + i;
-        const bool in = z < AF_WPB ? S.fin_u[z] == u : (z < 2 * AF_WPB ? S.save_u[z - AF_WPB] == u : true);
-        S.mw[i][z][h] = in ? src_of(i, z, h)[D] : -INFINITY;
-    }
-    __syncthreads();
-    if (threadIdx.x < 4 * n_units) {  // the unit's maximum per head
-        const int i = threadIdx.x >> 2, h = threadIdx.x & 3;
-        float M = -INFINITY;
+    constexpr int NSRC = 2 * AF_WPB + 1;  // warp z's final state, its saved state, the shared accumulator
+    static_assert(NSRC <= 64, "two sources per lane");
+    for (int ih = warp; ih < 4 * n_units; ih += AF_WPB) {
+        const int i = ih >> 2, h = ih & 3, u = u_first + i;
+        auto src = [&](int z) -> const float * {
+            if (z < AF_WPB) return S.fin_u[z] == u ? fin + (z * 4 + h) * PR : nullptr;
+            if (z < 2 * AF_WPB) return S.save_u[z - AF_WPB] == u ? &S.save[z - AF_WPB][h][0] : nullptr;
+            return z == 2 * AF_WPB ? &S.uacc[i][h][0] : nullptr;
+        };
+        // lane l holds sources l and l + 32: their maxima, then their weights
+        const float *s0 = src(lane), *s1 = src(lane + 32);
+        const float m0 = s0 ? s0[D] : -INFINITY, m1 = s1 ? s1[D] : -INFINITY;
+        const float M = warp_max(fmaxf(m0, m1));
+        const float w0 = m0 == -INFINITY ? 0.f : ex2(m0 - M), w1 = m1 == -INFINITY ? 0.f : ex2(m1 - M);
+        const float L = warp_sum((s0 ? w0 * s0[D + 1] : 0.f) + (s1 ? w1 * s1[D + 1] : 0.f));
+        constexpr int CPL = (D + 31) / 32;  // columns per lane
+        float acc[CPL];
 #pragma unroll
-        for (int z = 0; z < NSRC; z++) M = fmaxf(M, S.mw[i][z][h]);
-        S.mM[i][h] = M;
-    }
-    __syncthreads();
-    for (int t = threadIdx.x; t < n_units * NSRC * 4; t += blockDim.x) {  // weights
-        const int i = t / (NSRC * 4), z = (t >> 2) % NSRC, h = t & 3;
-        const float m = S.mw[i][z][h];
-        S.mw[i][z][h] = m == -INFINITY ? 0.f : ex2(m - S.mM[i][h]);
-    }
-    __syncthreads();
-    constexpr int P4 = PR / 4;
-    for (int idx = threadIdx.x; idx < n_units * 4 * P4; idx += blockDim.x) {
-        const int i = idx / (4 * P4), hc = idx - i * 4 * P4, h = hc / P4, c4 = hc - h * P4;
-        const int u = u_first + i;
-        float4 r = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (c4 < D / 4) {
-#pragma unroll 4
-            for (int z = 0; z < NSRC; z++) {
-                const float w = S.mw[i][z][h];
-                if (w == 0.f) continue;
-                const float4 v = reinterpret_cast<const float4 *>(src_of(i, z, h))[c4];
-                r.x += w * v.x;
-                r.y += w * v.y;
-                r.z += w * v.z;
-                r.w += w * v.w;
-            }
-        } else {
-            float L = 0.f;
-            for (int z = 0; z < NSRC; z++) {
-                const float w = S.mw[i][z][h];
-                if (w != 0.f) L += w * src_of(i, z, h)[D + 1];
-            }
-            r = make_float4(S.mM[i][h], L, 0.f, 0.f);
+        for (int j = 0; j < CPL; j++) acc[j] = 0.f;
+        for (int z = 0; z < NSRC; z++) {
+            const float w = __shfl_sync(FULL, z < 32 ? w0 : w1, z & 31);
+            if (w == 0.f) continue;  // warp-uniform
+            const float *sz = src(z);
+#pragma unroll
+            for (int j = 0; j < CPL; j++) acc[j] += w * sz[lane + 32 * j];
         }
         const int first = owner(static_cast<long long>(u) * cpu, NP, G);
-        float *rec = a.partials + (static_cast<long long>(u) * a.max_slots + (cta - first)) * 4 * PR;
-        reinterpret_cast<float4 *>(rec)[hc] = r;
+        float *rec = a.partials + (static_cast<long long>(u) * a.max_slots + (cta - first)) * 4 * PR + h * PR;
+#pragma unroll
+        for (int j = 0; j < CPL; j++) rec[lane + 32 * j] = acc[j];
+        if (lane == 0) {
+            rec[D] = M;
+            rec[D + 1] = L;
+        }
     }
-    // publish: the records are visible GPU-wide before the units' counts move;
-    // the CTA whose record completes a unit merges that unit's records
-    __threadfence();
+    // publish: the records are visible GPU-wide before the units' counts move
+    // (the barrier orders every thread's record stores before the fence of the
+    // threads that take the tickets); the CTA whose record completes a unit
+    // merges that unit's records
     __syncthreads();
     if (threadIdx.x < n_units + n_runits) {  // one ticket per record: packed units, then 16-bit ones
+        __threadfence();
         const int t = threadIdx.x;
         const int u = t < n_units ? u_first + t : ru0 + (t - n_units);
         int np, nr;
         unit_records(a, u, G, np, nr);
-        S.done_u[t] = atomicAdd(a.counters + u, 1) + 1 == np + nr ? u : -1;
+        const bool last = atomicAdd(a.counters + u, 1) + 1 == np + nr;
+        if (last) __threadfence();  // acquire: the unit's other records are visible (to the CTA after the barrier)
+        S.done_u[t] = last ? u : -1;
     }
     __syncthreads();
+    // the completed units, four warps (one per query head) per unit at a time
+    int k = 0;
     for (int i = 0; i < n_units + n_runits; i++) {
         const int u = S.done_u[i];
         if (u < 0) continue;
-        __threadfence();  // acquire: the other records of the unit are visible
-        if (warp < sh.G) {
+        if ((warp >> 2) == (k & 3) && (warp & 3) < sh.G) {
             int np, nr;
             unit_records(a, u, G, np, nr);
-            finish_head<D>(a, sh, u, warp, np, nr);
+            finish_head<D>(a, sh, u, warp & 3, np, nr);
+            if (lane == 0 && (warp & 3) == 0) a.counters[u] = 0;  // every record of this call has arrived
         }
-        __syncthreads();
-        if (threadIdx.x == 0) a.counters[u] = 0;  // every record of this call has arrived
+        ++k;
     }
 }
 
@@ -789,6 +768,7 @@ int dispatch_affine(const Layout &L, F &&f) {
     const bool m16 = L.meta_bytes == 2;
     if (L.d == 128) {
         if (L.bits_k == 2) return m16 ? f(AffineLauncher<128, 2, true>()) : f(AffineLauncher<128, 2, false>());
+        if (L.bits_k == 3) return m16 ? f(AffineLauncher<128, 3, true>()) : f(AffineLauncher<128, 3, false>());
         return m16 ? f(AffineLauncher<128, 4, true>()) : f(AffineLauncher<128, 4, false>());
     }
     if (L.bits_k == 2) return m16 ? f(AffineLauncher<64, 2, true>()) : f(AffineLauncher<64, 2, false>());
@@ -800,8 +780,8 @@ long long ceil_div(long long x, long long y) { return (x + y - 1) / y; }
 }  // namespace
 
 bool affine_kernel_applies(const Layout &L, const AttnArgs &a) {
-    if (!(L.scheme == DQ_AFFINE && L.bits_k == L.bits_v && (L.bits_k == 2 || L.bits_k == 4) &&
-          (L.d == 64 || L.d == 128) && L.G <= 4))
+    if (!(L.scheme == DQ_AFFINE && L.bits_k == L.bits_v && L.G <= 4 &&
+          ((L.d == 128 && L.bits_k >= 2 && L.bits_k <= 4) || (L.d == 64 && (L.bits_k == 2 || L.bits_k == 4)))))
         return false;
     // a cache read mostly as 16-bit slots streams better through the CTA-wide
     // ring of attn_kernel, whose every warp takes 16-bit tiles

@@ -277,7 +277,7 @@ __device__ __forceinline__ void store_state(WarpState<D / 16> &st, bool quant, f
         for (int rr = 0; rr < 2; rr++) {
             const int row = 16 * mi + 8 * rr + g;
             const float v = st.acc[mi][2 * rr] + st.acc[mi][2 * rr + 1];
-            if (quant) wp[row] = v * exp2f(static_cast<float>(24 - field_exp(2 * mi + rr, BV))) + st.ao;
+            if (quant) wp[row] = v * pow2i(24 - field_exp(2 * mi + rr, BV)) + st.ao;
             else wp[raw_v_channel<D>(row)] = v;
         }
     if (g == 0) {

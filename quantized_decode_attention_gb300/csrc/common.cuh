@@ -144,6 +144,15 @@ __device__ __forceinline__ uint32_t pack2(uint16_t lo, uint16_t hi) {
     return static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
 }
 
+// 2^e as an exact fp32 constant, e in [-126, 127].
+__host__ __device__ __forceinline__ float pow2i(int e) {
+#ifdef __CUDA_ARCH__
+    return __int_as_float((127 + e) << 23);
+#else
+    return e >= 0 ? static_cast<float>(1u << e) : 1.0f / static_cast<float>(1u << (-e));
+#endif
+}
+
 // ---- bulk async copy (TMA, non-tensor) + mbarrier --------------------------
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));

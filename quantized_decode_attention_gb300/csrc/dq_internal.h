@@ -190,7 +190,7 @@ struct AttnArgs {
     const uint16_t *ol_col_v, *ol_val_v;  // [U][Qcap][k_out_v]
     long long rp_stride, nnzk_cap;
     int k_out_v;                          // value outliers per token (0: none)
-    // affine 2/4-bit kernel schedule (set by plan_affine; affine = 1 routes the
+    // affine kernel schedule (set by plan_affine; affine = 1 routes the
     // launch to it)
     int affine;
     long long n_pt;                       // 16-token packed tiles per unit
@@ -232,7 +232,7 @@ int launch_qcomp(const Layout &L, const float *q, const float *qc, float *qt, vo
 int plan_attention(const Layout &L, AttnArgs &a, int num_sms, long long cap_floats);
 long long attention_partial_floats(const Layout &L, const AttnArgs &a);
 size_t attention_smem_bytes(const Layout &L);
-// The affine kernel for 2- and 4-bit codes (attn_affine.cu); plan_attention
+// The affine kernel (attn_affine.cu; 2-4 bit codes at d 128, 2 and 4 at d 64); plan_attention
 // routes a call to it when it applies (a supported shape whose packed tokens
 // carry at least as many bytes as its 16-bit slots) and marks a.affine.
 bool affine_kernel_applies(const Layout &L, const AttnArgs &a);
