@@ -265,9 +265,8 @@ def run_gpu(args, w, bits, S, k_dev, v_dev, q_dev, knew_dev, vnew_dev, rank):
     sm_scale = w.head_dim ** -0.5
     pos = S - 1
 
-    def step(c, s):
-        c.quantize(knew_dev, vnew_dev, pos0=pos, stream=s.cuda_stream)
-        c.attention(q_dev, out, S, sm_scale, stream=s.cuda_stream)
+    def step(c, s):  # append the new token and attend: one fused library call
+        c.decode_step(knew_dev, vnew_dev, q_dev, out, S, sm_scale, stream=s.cuda_stream)
 
     # CUDA graphs: one per cache copy holding [quantize new token, attention],
     # and one holding a step on every copy in turn (replayed for the bulk).
@@ -351,8 +350,7 @@ def run_gpu(args, w, bits, S, k_dev, v_dev, q_dev, knew_dev, vnew_dev, rank):
         for i in range(n_e2e):
             c = caches[i % nc]
             dev_in.copy_(host, non_blocking=True)
-            c.quantize(k_b, v_b, pos0=pos, stream=stream.cuda_stream)
-            c.attention(q_b, out, S, sm_scale, stream=stream.cuda_stream)
+            c.decode_step(k_b, v_b, q_b, out, S, sm_scale, stream=stream.cuda_stream)
             out_h.copy_(out, non_blocking=True)
         e_t1.record(stream)
         stream.synchronize()
@@ -963,12 +961,12 @@ def main():
                    "head_dim": w.head_dim, "seq_len": S, "bits": args.bits, "n_sink": w.n_sink,
                    "n_recent": w.n_recent, "parallelism": f"replicas{world}",
                    "l2": f"{res['copies']} cache copies rotated per step (> L2)",
-                   "step": "quantize 1 new token/seq + decode attention, CUDA graph per step"},
+                   "step": "dq_decode_step: append 1 new token/seq + decode attention (one launch), CUDA graph per step"},
         "roofline": roof(res, args.bits),
         "clocks": res["clocks"],
         "e2e": {"value": round(res["e2e_tok_s"], 1), "unit": "tokens/s", "h2d_bytes_per_step": res["h2d"],
                 "d2h_bytes_per_step": res["d2h"],
-                "how": "eager C-ABI calls per step: one pinned-host H2D copy of q and the new token, output D2H"},
+                "how": "eager dq_decode_step calls: one pinned-host H2D copy of q and the new token, output D2H"},
         "gpu_launches": 3 * args.steps,
         "quantize": {"token_us": round(res["token_ms"] * 1e3, 2), "prefill_us": round(res["prefill_ms"] * 1e3, 1),
                      "prefill_gbs": round(res["prefill_bytes"] / (res["prefill_ms"] / 1e3) / 1e9, 1),
@@ -998,7 +996,7 @@ def main():
             "config": {"batch": wq.batch, "q_heads": wq.n_q_heads, "kv_heads": wq.n_kv_heads,
                        "head_dim": wq.head_dim, "seq_len": wq.seq, "bits": wq.bits, "clip": wq.clip,
                        "key_transform": "dense", "l2": f"{r['copies']} cache copies rotated per step (> L2)",
-                       "step": "quantize 1 new token/seq + decode attention, CUDA graph per step"}}
+                       "step": "dq_decode_step: append 1 new token/seq + decode attention, CUDA graph per step"}}
     if bf16 is not None:
         line["variants"]["llama3-8b-decode-bf16-cache"] = {
             "value": round(w.batch / (bf16["total_ms"] / args.steps / 1e3), 1),

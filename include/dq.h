@@ -234,6 +234,28 @@ dq_status dq_decode_attention(dq_ctx **ctx, const dq_config *cfg, const dq_kv_bu
                               void *stream);
 
 /*
+ * One decode step: append token seq_len - 1 and attend over the first
+ * seq_len tokens -- the same results as dq_quantize_kv(pos0 = seq_len - 1,
+ * n_tok = 1) followed by dq_decode_attention(seq_len), cache bytes included
+ * ("D-Quant", Sec. 5.1: the newest tokens stay 16-bit in the recent window and
+ * enter the quantized region as they leave it; "KVQuant-NUQ", streaming
+ * decode).
+ *   k_new, v_new : device, [batch][n_kv_heads][1][head_dim] kv_dtype
+ *   q, out       : as for dq_decode_attention
+ * Requires 2 <= seq_len <= max_seq and a cache holding tokens [0, seq_len - 1).
+ * For affine caches with n_recent >= 1 that the affine attention kernel serves
+ * (head_dim 128 at 2-4 bits, head_dim 64 at 2 or 4 bits, at most 4 query
+ * heads per KV head), the step is one kernel launch: the new token's packed
+ * slot lies in the recent window, so nothing the attention reads depends on
+ * its quantization, and its 16-bit row is read from k_new / v_new directly.
+ * Otherwise the two calls run in order on the stream.
+ * Errors: as dq_quantize_kv and dq_decode_attention.
+ */
+dq_status dq_decode_step(dq_ctx **ctx, const dq_config *cfg, const dq_kv_buffers *bufs,
+                         const void *k_new, const void *v_new, const void *q, void *out,
+                         long long seq_len, float sm_scale, void *stream);
+
+/*
  * Test export: write the dequantized fp32 values of quantized slots
  * [slot0, slot0 + n) of K (which = 0) or V (which = 1) into
  *   out : device, [batch][n_kv_heads][n][head_dim] fp32

@@ -71,6 +71,8 @@ def load() -> C.CDLL:
                                  C.c_longlong, P]
     L.dq_decode_attention.argtypes = [C.POINTER(P), C.POINTER(Config), C.POINTER(Buffers), P, P,
                                       C.c_longlong, C.c_float, P]
+    L.dq_decode_step.argtypes = [C.POINTER(P), C.POINTER(Config), C.POINTER(Buffers), P, P, P, P,
+                                 C.c_longlong, C.c_float, P]
     L.dq_dequantize_kv.argtypes = [C.POINTER(P), C.POINTER(Config), C.POINTER(Buffers), C.c_int,
                                    C.c_longlong, C.c_longlong, P, P]
     L.dq_decode_attention_noalloc.argtypes = [C.POINTER(Config), C.POINTER(Buffers), P, P, C.c_longlong,
@@ -85,7 +87,7 @@ def load() -> C.CDLL:
     L.dq_rans_model.argtypes = [C.POINTER(Config), C.c_int, C.POINTER(C.c_int), C.POINTER(C.c_int),
                                 C.POINTER(C.c_int)]
     L.dq_symbol_probs.argtypes = [C.c_int, C.c_int, C.POINTER(C.c_double)]
-    for f in ("dq_kv_sizes", "dq_quantize_kv", "dq_decode_attention", "dq_dequantize_kv", "dq_check",
+    for f in ("dq_kv_sizes", "dq_quantize_kv", "dq_decode_attention", "dq_decode_step", "dq_dequantize_kv", "dq_check",
               "dq_rans_model", "dq_symbol_probs"):
         getattr(L, f).restype = C.c_int
     _lib = L
@@ -199,6 +201,15 @@ class KVCache:
         b = self.buffers()
         _raise(load().dq_decode_attention(C.byref(self.ctx), C.byref(self.cfg), C.byref(b), _ptr(q), _ptr(out),
                                           seq_len, sm_scale, _stream(stream)))
+
+    def decode_step(self, k_new, v_new, q, out, seq_len: int, sm_scale: float | None = None, stream=None):
+        """Append token seq_len - 1 (k_new, v_new: [B, Hkv, 1, d] in the kv dtype)
+        and attend over seq_len tokens (q fp32 [B, Hq, d], out [B, Hq, d])."""
+        if sm_scale is None:
+            sm_scale = self.cfg.head_dim ** -0.5
+        b = self.buffers()
+        _raise(load().dq_decode_step(C.byref(self.ctx), C.byref(self.cfg), C.byref(b), _ptr(k_new), _ptr(v_new),
+                                     _ptr(q), _ptr(out), seq_len, sm_scale, _stream(stream)))
 
     def attention_noalloc(self, q, out, seq_len: int, sm_scale: float | None = None, stream=None):
         """Same result as attention(), through the entry point that allocates nothing

@@ -51,6 +51,7 @@
 #include "attn_common.cuh"
 #include "common.cuh"
 #include "dq_internal.h"
+#include "quant_row.cuh"
 
 namespace dq {
 namespace {
@@ -447,6 +448,15 @@ __device__ void finish_head(const AttnArgs &a, const AttnShape &sh, int u, int h
     }
 }
 
+// The fused step's append of one unit's new token (keys, then values), kept
+// out of line: the attention's own loops keep the code layout they have
+// without it.
+template <int V, int BITS>
+__device__ __noinline__ void append_rows(QuantArgs qk, QuantArgs qv, RowGeom rg, int u, float *xs) {
+    quantize_row<V, BITS>(qk, rg, u, 0, xs);
+    quantize_row<V, BITS>(qv, rg, u, 0, xs);
+}
+
 // ---- the kernel ---------------------------------------------------------------
 // Chunks: chunk j of unit u holds its packed tiles [j TPC, min((j + 1) TPC,
 // n_pt)).  CTA c owns chunks [c N / G, (c + 1) N / G) of the list of all units'
@@ -539,6 +549,24 @@ __global__ void __launch_bounds__(AF_WPB * 32, 1) attn_affine_kernel(AttnArgs a,
                     S.rqh[j][1][h][c] = static_cast<uint16_t>(w >> 16);
                 }
             }
+        }
+    }
+    // fused decode step: the new token's 16-bit slot of unit u sits in tile
+    // e_new; the warp holding that tile quantizes the token into the cache (its
+    // packed slot lies in the recent window, so nothing in this call reads it)
+    // and, below, reads its 16-bit row from the input instead of the cache
+    int rs_new = -1, e_new = -1;
+    if (a.append) {
+        const long long tn = a.qa[0].pos0;
+        rs_new = tn < a.rg.n_sink ? static_cast<int>(tn) : a.rg.n_sink + static_cast<int>(tn % a.rg.n_recent);
+        e_new = rs_new / AF_RTILE;
+    }
+    if (raw_warp && a.append) {
+        for (int j = 0; j < n_runits; j++) {
+            const int u = ru0 + j;
+            const long long x = static_cast<long long>(u) * a.n_rt + e_new;
+            if (x < r0 || x >= r1) continue;
+            append_rows<D / 32, BITS>(a.qa[0], a.qa[1], a.rg, u, &S.save[warp][0][0]);
         }
     }
     // chunks in flight, oldest first: q0 in slot s, q1 in the next slot, ...
@@ -657,7 +685,21 @@ __global__ void __launch_bounds__(AF_WPB * 32, 1) attn_affine_kernel(AttnArgs a,
                     st.init();
                 }
                 if (!mbar_wait(&S.rfull[s], (k / AF_NSR) & 1, AF_WAIT_NS)) timed_out = true;
-                const uint8_t *tile = rring + s * C::RSLOT;
+                uint8_t *tile = rring + s * C::RSLOT;
+                if (e == e_new) {  // the new token's 16-bit row, from the input
+                    const int sl = rs_new - e * AF_RTILE;
+                    uint16_t *kr = reinterpret_cast<uint16_t *>(tile) + sl * D;
+                    uint16_t *vr = reinterpret_cast<uint16_t *>(tile + 32 * D) + (sl >> 1) * 2 * D + (sl & 1);
+                    constexpr int V = D / 32;
+                    const long long base = static_cast<long long>(u) * D;
+#pragma unroll
+                    for (int j = 0; j < V; j++) {
+                        const int c = lane * V + j;
+                        kr[c] = raw16_of(a.qa[0].x, base + c, a.qa[0].in_dtype);
+                        vr[2 * c] = raw16_of(a.qa[1].x, base + c, a.qa[1].in_dtype);
+                    }
+                    __syncwarp();
+                }
                 if (a.raw_bf16) process_raw<D, true>(a, tile, static_cast<long long>(e) * AF_RTILE, qb, st);
                 else process_raw<D, false>(a, tile, static_cast<long long>(e) * AF_RTILE, qb, st);
                 __syncwarp();

@@ -488,6 +488,95 @@ static dq_status quantize_rans(dq_ctx *c, const dq_config *cfg, const Layout &L,
     return ok();
 }
 
+// Arguments of the affine quantizer for tokens [pos0, pos0 + n_tok) of the
+// keys (which = 0) or values (which = 1); x is [B][Hkv][n_tok][d].
+static void fill_quant_args(const dq_config *cfg, const Layout &L, const dq_kv_buffers *bufs, int which, const void *x,
+                            long long pos0, long long n_tok, unsigned *status, dq::QuantArgs &a) {
+    const dq_tensor_cfg &t = which == 0 ? cfg->k : cfg->v;
+    a.x = x;
+    a.in_dtype = cfg->kv_dtype;
+    a.pos0 = pos0;
+    a.n_tok = n_tok;
+    a.seq_after = pos0 + n_tok;
+    a.is_key = which == 0;
+    a.bits = t.bits;
+    a.rot = t.rot;
+    a.use_mean = which == 0 && t.mean;
+    a.meta_f16 = cfg->meta_dtype == DQ_F16;
+    a.clip = t.clip;
+    if (t.clip > 0.0f) {
+        const double plo = (1.0 - static_cast<double>(t.clip)) * (L.d - 1);
+        const double phi = static_cast<double>(t.clip) * (L.d - 1);
+        a.clip_ilo = static_cast<int>(std::floor(plo));
+        a.clip_flo = static_cast<float>(plo - std::floor(plo));
+        a.clip_ihi = static_cast<int>(std::floor(phi));
+        a.clip_fhi = static_cast<float>(phi - std::floor(phi));
+    }
+    a.hscale = static_cast<float>(1.0 / std::sqrt(static_cast<double>(L.d)));
+    a.codes = static_cast<uint8_t *>(which == 0 ? bufs->codes_k : bufs->codes_v);
+    a.meta = which == 0 ? bufs->meta_k : bufs->meta_v;
+    a.mean = which == 0 && t.mean ? static_cast<float *>(bufs->mean_k) : nullptr;
+    a.T = which == 0 && t.rot == DQ_ROT_DENSE ? static_cast<const float *>(bufs->k_transform) : nullptr;
+    a.raw = static_cast<uint16_t *>(which == 0 ? bufs->raw_k : bufs->raw_v);
+    a.status = status;
+}
+
+// Arguments of an affine or non-uniform decode-attention call (the dense key
+// transform's compensated queries are computed here, on the stream).
+static dq_status fill_attn_args(const dq_config *cfg, const Layout &L, const dq_kv_buffers *bufs, dq_ctx *c,
+                                const void *q, void *out, long long seq_len, float sm_scale, void *stream,
+                                dq::AttnArgs &a) {
+    a.q = static_cast<const float *>(q);
+    a.out = out;
+    a.out_dtype = cfg->out_dtype;
+    a.codes_k = static_cast<const uint8_t *>(bufs->codes_k);
+    a.codes_v = static_cast<const uint8_t *>(bufs->codes_v);
+    a.meta_k = bufs->meta_k;
+    a.meta_v = bufs->meta_v;
+    a.mean_k = cfg->k.mean ? static_cast<const float *>(bufs->mean_k) : nullptr;
+    a.raw_k = static_cast<const uint16_t *>(bufs->raw_k);
+    a.raw_v = static_cast<const uint16_t *>(bufs->raw_v);
+    a.q_comp = cfg->k.rot == DQ_ROT_DENSE ? static_cast<const float *>(bufs->q_comp) : nullptr;
+    if (cfg->k.rot == DQ_ROT_DENSE) {
+        const int eq = dq::launch_qcomp(L, a.q, a.q_comp, c->q_tilde, stream);
+        if (eq != 0) return fail(DQ_ECUDA, "query compensation launch: %s", cudaGetErrorString(static_cast<cudaError_t>(eq)));
+        a.q_tilde = c->q_tilde;
+    }
+    a.rot_k = cfg->k.rot;
+    a.rot_v = cfg->v.rot;
+    a.raw_bf16 = cfg->kv_dtype == DQ_BF16;
+    a.seq_len = seq_len;
+    const long long n_s = seq_len < cfg->n_sink ? seq_len : cfg->n_sink;
+    long long q_hi = seq_len - cfg->n_recent;
+    if (q_hi < n_s) q_hi = n_s;
+    a.n_q = q_hi - n_s;
+    a.n_sink_eff = static_cast<int>(n_s);
+    a.n_sink_cfg = cfg->n_sink;
+    a.n_recent_cfg = cfg->n_recent;
+    a.n_raw_slots = cfg->n_sink + cfg->n_recent;
+    a.has_raw = a.n_raw_slots > 0 ? 1 : 0;
+    a.sm_log2 = sm_scale * 1.4426950408889634f;
+    a.hscale = static_cast<float>(1.0 / std::sqrt(static_cast<double>(L.d)));
+    a.partials = c->partials;
+    a.counters = c->counters;
+    a.status = c->status;
+    if (c->counters_dirty) {
+        if (cudaMemsetAsync(c->counters, 0, sizeof(int) * L.U, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+            return fail(DQ_ECUDA, "clearing the record counts failed");
+        c->counters_dirty = 0;
+    }
+    dq::set_nuq_args(L, bufs, a);
+    return DQ_OK;
+}
+
+static dq_status launch_attn(const Layout &L, dq_ctx *c, dq::AttnArgs &a, void *stream) {
+    int e = dq::plan_attention(L, a, c->num_sms, static_cast<long long>(c->partials_cap));
+    if (e != 0) return fail(DQ_ECUDA, "attention planning: %s", cudaGetErrorString(static_cast<cudaError_t>(e)));
+    e = dq::launch_attention(L, a, c->num_sms, stream);
+    if (e != 0) return fail(DQ_ECUDA, "attention launch: %s", cudaGetErrorString(static_cast<cudaError_t>(e)));
+    return ok();
+}
+
 extern "C" {
 
 const char *dq_last_error(void) { return g_err; }
@@ -560,34 +649,8 @@ dq_status dq_quantize_kv(dq_ctx **ctx, const dq_config *cfg, const dq_kv_buffers
     if (L.scheme == DQ_RANS) return quantize_rans(*ctx, cfg, L, bufs, k, v, pos0, n_tok, stream);
 
     for (int which = 0; which < 2; which++) {
-        const dq_tensor_cfg &t = which == 0 ? cfg->k : cfg->v;
         dq::QuantArgs a{};
-        a.x = which == 0 ? k : v;
-        a.in_dtype = cfg->kv_dtype;
-        a.pos0 = pos0;
-        a.n_tok = n_tok;
-        a.seq_after = pos0 + n_tok;
-        a.is_key = which == 0;
-        a.bits = t.bits;
-        a.rot = t.rot;
-        a.use_mean = which == 0 && t.mean;
-        a.meta_f16 = cfg->meta_dtype == DQ_F16;
-        a.clip = t.clip;
-        if (t.clip > 0.0f) {
-            const double plo = (1.0 - static_cast<double>(t.clip)) * (L.d - 1);
-            const double phi = static_cast<double>(t.clip) * (L.d - 1);
-            a.clip_ilo = static_cast<int>(std::floor(plo));
-            a.clip_flo = static_cast<float>(plo - std::floor(plo));
-            a.clip_ihi = static_cast<int>(std::floor(phi));
-            a.clip_fhi = static_cast<float>(phi - std::floor(phi));
-        }
-        a.hscale = static_cast<float>(1.0 / std::sqrt(static_cast<double>(L.d)));
-        a.codes = static_cast<uint8_t *>(which == 0 ? bufs->codes_k : bufs->codes_v);
-        a.meta = which == 0 ? bufs->meta_k : bufs->meta_v;
-        a.mean = which == 0 && t.mean ? static_cast<float *>(bufs->mean_k) : nullptr;
-        a.T = which == 0 && t.rot == DQ_ROT_DENSE ? static_cast<const float *>(bufs->k_transform) : nullptr;
-        a.raw = static_cast<uint16_t *>(which == 0 ? bufs->raw_k : bufs->raw_v);
-        a.status = (*ctx)->status;
+        fill_quant_args(cfg, L, bufs, which, which == 0 ? k : v, pos0, n_tok, (*ctx)->status, a);
         int e;
         if (a.use_mean && pos0 == 0) {
             if ((e = dq::launch_key_mean(L, a, stream)) != 0)
@@ -653,51 +716,40 @@ dq_status dq_decode_attention(dq_ctx **ctx, const dq_config *cfg, const dq_kv_bu
     }
 
     dq::AttnArgs a{};
-    a.q = static_cast<const float *>(q);
-    a.out = out;
-    a.out_dtype = cfg->out_dtype;
-    a.codes_k = static_cast<const uint8_t *>(bufs->codes_k);
-    a.codes_v = static_cast<const uint8_t *>(bufs->codes_v);
-    a.meta_k = bufs->meta_k;
-    a.meta_v = bufs->meta_v;
-    a.mean_k = cfg->k.mean ? static_cast<const float *>(bufs->mean_k) : nullptr;
-    a.raw_k = static_cast<const uint16_t *>(bufs->raw_k);
-    a.raw_v = static_cast<const uint16_t *>(bufs->raw_v);
-    a.q_comp = cfg->k.rot == DQ_ROT_DENSE ? static_cast<const float *>(bufs->q_comp) : nullptr;
-    if (cfg->k.rot == DQ_ROT_DENSE) {
-        const int eq = dq::launch_qcomp(L, a.q, a.q_comp, c->q_tilde, stream);
-        if (eq != 0) return fail(DQ_ECUDA, "query compensation launch: %s", cudaGetErrorString(static_cast<cudaError_t>(eq)));
-        a.q_tilde = c->q_tilde;
+    if ((s = fill_attn_args(cfg, L, bufs, c, q, out, seq_len, sm_scale, stream, a)) != DQ_OK) return s;
+    return launch_attn(L, c, a, stream);
+}
+
+dq_status dq_decode_step(dq_ctx **ctx, const dq_config *cfg, const dq_kv_buffers *bufs, const void *k_new,
+                         const void *v_new, const void *q, void *out, long long seq_len, float sm_scale, void *stream) {
+    if (!cfg || !bufs || !k_new || !v_new || !q || !out) return fail(DQ_EINVAL, "NULL argument");
+    Layout L;
+    dq_status s = dq::make_layout(cfg, &L);
+    if (s != DQ_OK) return s;
+    if (seq_len < 2 || seq_len > cfg->max_seq)
+        return fail(DQ_EINVAL, "seq_len %lld outside [2, max_seq]: a step appends to a prefilled cache", seq_len);
+    if (!std::isfinite(sm_scale)) return fail(DQ_EINVAL, "sm_scale is not finite");
+    if ((s = check_bufs(L, bufs)) != DQ_OK) return s;
+    if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(q) || !aligned16(out))
+        return fail(DQ_EALIGN, "k_new / v_new / q / out not 16-byte aligned");
+    if ((s = get_ctx(ctx, cfg, L)) != DQ_OK) return s;
+    dq_ctx *c = *ctx;
+    // one launch when the affine kernel serves the call and the new token lies
+    // in the recent window (so no packed slot this call reads is written by it)
+    if (L.scheme == DQ_AFFINE && cfg->n_recent >= 1) {
+        dq::AttnArgs a{};
+        if ((s = fill_attn_args(cfg, L, bufs, c, q, out, seq_len, sm_scale, stream, a)) != DQ_OK) return s;
+        if (dq::affine_kernel_applies(L, a)) {
+            a.append = 1;
+            for (int which = 0; which < 2; which++)
+                fill_quant_args(cfg, L, bufs, which, which == 0 ? k_new : v_new, seq_len - 1, 1, c->status,
+                                a.qa[which]);
+            a.rg = dq::row_geom(L);
+            return launch_attn(L, c, a, stream);
+        }
     }
-    a.rot_k = cfg->k.rot;
-    a.rot_v = cfg->v.rot;
-    a.raw_bf16 = cfg->kv_dtype == DQ_BF16;
-    a.seq_len = seq_len;
-    const long long n_s = seq_len < cfg->n_sink ? seq_len : cfg->n_sink;
-    long long q_hi = seq_len - cfg->n_recent;
-    if (q_hi < n_s) q_hi = n_s;
-    a.n_q = q_hi - n_s;
-    a.n_sink_eff = static_cast<int>(n_s);
-    a.n_sink_cfg = cfg->n_sink;
-    a.n_recent_cfg = cfg->n_recent;
-    a.n_raw_slots = cfg->n_sink + cfg->n_recent;
-    a.has_raw = a.n_raw_slots > 0 ? 1 : 0;
-    a.sm_log2 = sm_scale * 1.4426950408889634f;
-    a.hscale = static_cast<float>(1.0 / std::sqrt(static_cast<double>(L.d)));
-    a.partials = c->partials;
-    a.counters = c->counters;
-    a.status = c->status;
-    if (c->counters_dirty) {
-        if (cudaMemsetAsync(c->counters, 0, sizeof(int) * L.U, static_cast<cudaStream_t>(stream)) != cudaSuccess)
-            return fail(DQ_ECUDA, "clearing the record counts failed");
-        c->counters_dirty = 0;
-    }
-    dq::set_nuq_args(L, bufs, a);
-    int e = dq::plan_attention(L, a, c->num_sms, static_cast<long long>(c->partials_cap));
-    if (e != 0) return fail(DQ_ECUDA, "attention planning: %s", cudaGetErrorString(static_cast<cudaError_t>(e)));
-    e = dq::launch_attention(L, a, c->num_sms, stream);
-    if (e != 0) return fail(DQ_ECUDA, "attention launch: %s", cudaGetErrorString(static_cast<cudaError_t>(e)));
-    return ok();
+    if ((s = dq_quantize_kv(ctx, cfg, bufs, k_new, v_new, seq_len - 1, 1, stream)) != DQ_OK) return s;
+    return dq_decode_attention(ctx, cfg, bufs, q, out, seq_len, sm_scale, stream);
 }
 
 dq_status dq_dequantize_kv(dq_ctx **ctx, const dq_config *cfg, const dq_kv_buffers *bufs, int which,

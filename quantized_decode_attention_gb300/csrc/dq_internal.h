@@ -154,6 +154,15 @@ struct QuantArgs {
     int n_slots;            // quantized slots written by this call
 };
 
+// The geometry a token row's quantizer needs (a slice of Layout).
+struct RowGeom {
+    int U, Hkv, n_sink, n_recent, rcap, rowK, pairV;
+    long long qcap;
+};
+inline RowGeom row_geom(const Layout &L) {
+    return RowGeom{L.U, L.Hkv, L.n_sink, L.n_recent, L.rcap, L.rowK, L.pairV, L.qcap};
+}
+
 struct AttnArgs {
     const float *q;         // [B][Hq][d]
     void *out;              // [B][Hq][d]
@@ -198,6 +207,12 @@ struct AttnArgs {
     long long np_total, nr_total;         // packed chunks / 16-bit tiles of all units
     int wp;                               // packed warps per CTA
     int mps;                              // record slots per unit taken by packed CTAs
+    // fused decode step: the call first appends token seq_len - 1 (one row per
+    // unit of the keys qa[0] and values qa[1]; the 16-bit-tile warp holding its
+    // recent-window slot quantizes it and reads its 16-bit row from the input)
+    int append;
+    QuantArgs qa[2];
+    RowGeom rg;
 };
 
 struct DequantArgs {

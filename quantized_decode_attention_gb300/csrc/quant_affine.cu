@@ -19,39 +19,9 @@
 
 #include "common.cuh"
 #include "dq_internal.h"
+#include "quant_row.cuh"
 
 namespace dq {
-
-// ---------------------------------------------------------------------------
-// Rotation of one token row held V values per lane (lane l: l*V .. l*V+V-1).
-// Dense transform: y_i = sum_j T[i][j] x_j accumulated in j order from 0.
-// ---------------------------------------------------------------------------
-template <int V>
-__device__ __forceinline__ void rotate_row(float (&x)[V], int rot, float hscale, const float *T,
-                                          float *xs /* per-warp smem, d floats */) {
-    constexpr int D = 32 * V;
-    const int lane = threadIdx.x & 31;
-    if (rot == DQ_ROT_HADAMARD) {
-        fwht_warp<V>(x);
-#pragma unroll
-        for (int j = 0; j < V; j++) x[j] = __fmul_rn(x[j], hscale);
-    } else if (rot == DQ_ROT_DENSE) {
-#pragma unroll
-        for (int j = 0; j < V; j++) xs[lane * V + j] = x[j];
-        __syncwarp();
-        float y[V];
-#pragma unroll
-        for (int j = 0; j < V; j++) {
-            const float *Ti = T + static_cast<long long>(lane * V + j) * D;
-            float acc = 0.0f;
-            for (int k = 0; k < D; k++) acc = __fadd_rn(acc, __fmul_rn(__ldg(Ti + k), xs[k]));
-            y[j] = acc;
-        }
-        __syncwarp();
-#pragma unroll
-        for (int j = 0; j < V; j++) x[j] = y[j];
-    }
-}
 
 // ---------------------------------------------------------------------------
 // Key channel mean over tokens [t0, t1) of each unit (prefill).  One block per
@@ -88,165 +58,17 @@ __global__ void key_mean_kernel(QuantArgs a, int Hkv, long long t0, long long t1
 }
 
 // ---------------------------------------------------------------------------
-// Record packing helpers.
-// ---------------------------------------------------------------------------
-// ---------------------------------------------------------------------------
 // Quantize tokens [pos0, pos0 + n_tok): one warp per (unit, token).
 // ---------------------------------------------------------------------------
 template <int V, int BITS>
-__global__ void quantize_kernel(QuantArgs a, Layout L) {
+__global__ void quantize_kernel(QuantArgs a, RowGeom L) {
     constexpr int D = 32 * V;
     constexpr int WPB = 4;
     __shared__ float xs[WPB][D];
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
     const long long gw = static_cast<long long>(blockIdx.x) * WPB + warp;
     if (gw >= static_cast<long long>(L.U) * a.n_tok) return;
-    const int u = static_cast<int>(gw / a.n_tok);
-    const long long i = gw % a.n_tok;
-    const long long t = a.pos0 + i;
-    const int kvh = u % L.Hkv;
-    const long long base = (static_cast<long long>(u) * a.n_tok + i) * D;
-
-    float x[V];
-    bool finite = true;
-#pragma unroll
-    for (int j = 0; j < V; j++) {
-        x[j] = ld_in(a.x, base + lane * V + j, a.in_dtype);
-        finite = finite && isfinite(x[j]);
-    }
-    if (!__all_sync(FULL, finite) && lane == 0) atomicOr(a.status, ST_NONFINITE);
-
-    // 16-bit regions: sinks and the latest n_recent tokens, stored as given.
-    int raw_slot = -1;
-    if (t < L.n_sink) raw_slot = static_cast<int>(t);
-    else if (L.n_recent > 0 && t >= a.seq_after - L.n_recent) raw_slot = L.n_sink + static_cast<int>(t % L.n_recent);
-    if (raw_slot >= 0) {
-        const long long ub = static_cast<long long>(u) * L.rcap * D;
-#pragma unroll
-        for (int j = 0; j < V; j++) {
-            const int c = lane * V + j;
-            const uint16_t r = raw16_of(a.x, base + c, a.in_dtype);
-            long long off = a.is_key ? static_cast<long long>(raw_slot) * D + c
-                                     : (static_cast<long long>(raw_slot >> 1) * D + c) * 2 + (raw_slot & 1);
-            a.raw[ub + off] = r;
-        }
-    }
-    if (t < L.n_sink) return;
-    const long long slot = t - L.n_sink;
-
-    rotate_row<V>(x, a.rot, a.hscale, a.T ? a.T + static_cast<long long>(kvh) * D * D : nullptr, xs[warp]);
-    if (a.use_mean) {
-        const float *mu = a.mean + static_cast<long long>(u) * D;
-#pragma unroll
-        for (int j = 0; j < V; j++) x[j] = __fsub_rn(x[j], mu[lane * V + j]);
-    }
-
-    // grid
-    constexpr int LV = 1 << BITS;
-    float lo, hi;
-    if (a.clip > 0.0f) {
-        // order statistics by rank (ties broken by channel index)
-#pragma unroll
-        for (int j = 0; j < V; j++) xs[warp][lane * V + j] = x[j];
-        __syncwarp();
-        float vlo0 = 0.f, vlo1 = 0.f, vhi0 = 0.f, vhi1 = 0.f;
-        int have = 0;
-#pragma unroll
-        for (int j = 0; j < V; j++) {
-            const int c = lane * V + j;
-            const float xv = x[j];
-            int rank = 0;
-            for (int k = 0; k < D; k++) {
-                const float y = xs[warp][k];
-                rank += (y < xv) || (y == xv && k < c);
-            }
-            if (rank == a.clip_ilo) { vlo0 = xv; have |= 1; }
-            if (rank == a.clip_ilo + 1) { vlo1 = xv; have |= 2; }
-            if (rank == a.clip_ihi) { vhi0 = xv; have |= 4; }
-            if (rank == a.clip_ihi + 1) { vhi1 = xv; have |= 8; }
-        }
-        __syncwarp();
-        // gather the four order statistics (each held by exactly one lane)
-        const unsigned m1 = __ballot_sync(FULL, have & 1), m2 = __ballot_sync(FULL, have & 2);
-        const unsigned m4 = __ballot_sync(FULL, have & 4), m8 = __ballot_sync(FULL, have & 8);
-        vlo0 = __shfl_sync(FULL, vlo0, __ffs(m1) - 1);
-        vhi0 = __shfl_sync(FULL, vhi0, __ffs(m4) - 1);
-        vlo1 = m2 ? __shfl_sync(FULL, vlo1, __ffs(m2) - 1) : vlo0;
-        vhi1 = m8 ? __shfl_sync(FULL, vhi1, __ffs(m8) - 1) : vhi0;
-        lo = (a.clip_ilo + 1 >= D) ? vlo0 : __fadd_rn(vlo0, __fmul_rn(a.clip_flo, __fsub_rn(vlo1, vlo0)));
-        hi = (a.clip_ihi + 1 >= D) ? vhi0 : __fadd_rn(vhi0, __fmul_rn(a.clip_fhi, __fsub_rn(vhi1, vhi0)));
-    } else {
-        lo = x[0];
-        hi = x[0];
-#pragma unroll
-        for (int j = 1; j < V; j++) { lo = fminf(lo, x[j]); hi = fmaxf(hi, x[j]); }
-        lo = warp_min(lo);
-        hi = warp_max(hi);
-    }
-    float s = __fdiv_rn(__fsub_rn(hi, lo), static_cast<float>(LV - 1));
-    float o = lo;
-    if (a.meta_f16) {
-        s = __half2float(__float2half_rn(s));
-        o = __half2float(__float2half_rn(o));
-    }
-
-    uint32_t m[V];
-#pragma unroll
-    for (int j = 0; j < V; j++) {
-        float xv = x[j];
-        if (a.clip > 0.0f) xv = fminf(fmaxf(xv, lo), hi);
-        int q = 0;
-        if (s != 0.0f) {
-            const float tq = __fdiv_rn(__fsub_rn(xv, o), s);
-            if (tq == tq) q = min(max(__float2int_rn(tq), 0), LV - 1);
-        }
-        m[j] = static_cast<uint32_t>(q);
-    }
-
-    // meta
-    const long long ms = static_cast<long long>(u) * L.qcap + slot;
-    if (lane == 0) {
-        if (a.meta_f16) {
-            const uint32_t so = pack2(__half_as_ushort(__float2half_rn(s)), __half_as_ushort(__float2half_rn(o)));
-            reinterpret_cast<uint32_t *>(a.meta)[ms] = so;
-        } else {
-            reinterpret_cast<float2 *>(a.meta)[ms] = make_float2(s, o);
-        }
-    }
-
-    // pack
-    constexpr int WK = Rec<D, BITS>::K_WORDS, WV = Rec<D, BITS>::V_WORDS;
-    if (a.is_key) {
-        uint32_t *row = reinterpret_cast<uint32_t *>(a.codes + ms * L.rowK);
-        constexpr int WLO = D * 2 / 32;  // 2-bit plane words (BITS == 3)
-#pragma unroll
-        for (int w = 0; w < WK; w++) {
-            uint32_t v = 0;
-#pragma unroll
-            for (int j = 0; j < V; j++) {
-                const int c = lane * V + j;
-                v |= contrib<D, BITS>(w, k_idx(c, D), c & 1, m[j], WLO);
-            }
-            v = __reduce_or_sync(FULL, v);
-            if (lane == w) row[w] = v;
-        }
-    } else {
-        const int e = static_cast<int>(slot & 1);
-        uint16_t *rec = reinterpret_cast<uint16_t *>(
-            a.codes + (static_cast<long long>(u) * (L.qcap / 2) + slot / 2) * L.pairV);
-        constexpr int WLO = 2 * D * 2 / 32;
-#pragma unroll
-        for (int w = 0; w < WV; w++) {
-            uint32_t v = 0;
-#pragma unroll
-            for (int j = 0; j < V; j++) {
-                const int c = lane * V + j;
-                v |= contrib<D, BITS>(w, v_idx(c, D), e, m[j], WLO);
-            }
-            v = __reduce_or_sync(FULL, v);
-            if (lane == (w & 31)) rec[2 * w + e] = static_cast<uint16_t>(v >> (16 * e));
-        }
-    }
+    quantize_row<V, BITS>(a, L, static_cast<int>(gw / a.n_tok), gw % a.n_tok, xs[warp]);
 }
 
 // ---------------------------------------------------------------------------
@@ -318,10 +140,11 @@ template <int V>
 static void launch_q_bits(const Layout &L, const QuantArgs &a, cudaStream_t st) {
     const long long warps = static_cast<long long>(L.U) * a.n_tok;
     const unsigned grid = static_cast<unsigned>((warps + 3) / 4);
+    const RowGeom g = row_geom(L);
     switch (a.bits) {
-        case 2: quantize_kernel<V, 2><<<grid, 128, 0, st>>>(a, L); break;
-        case 3: quantize_kernel<V, 3><<<grid, 128, 0, st>>>(a, L); break;
-        default: quantize_kernel<V, 4><<<grid, 128, 0, st>>>(a, L); break;
+        case 2: quantize_kernel<V, 2><<<grid, 128, 0, st>>>(a, g); break;
+        case 3: quantize_kernel<V, 3><<<grid, 128, 0, st>>>(a, g); break;
+        default: quantize_kernel<V, 4><<<grid, 128, 0, st>>>(a, g); break;
     }
 }
 

@@ -84,6 +84,14 @@ def test_validation_errors_without_gpu(lib):
     assert lib.dq_quantize_kv(C.byref(ctx), C.byref(cfg), C.byref(b), 0x20000, 0x30000, 8190, 5, None) == 1
     assert lib.dq_decode_attention(C.byref(ctx), C.byref(cfg), C.byref(b), 0x20000, 0x30000, 0, 0.1, None) == 1
     assert lib.dq_decode_attention(C.byref(ctx), C.byref(cfg), C.byref(b), 0x20008, 0x30000, 10, 0.1, None) == 2
+    # the fused decode step: NULL inputs, a step without a prefilled token, a
+    # step past max_seq, a misaligned new token
+    step = lambda kn, vn, q, seq: lib.dq_decode_step(C.byref(ctx), C.byref(cfg), C.byref(b), kn, vn, q, 0x30000,
+                                                     seq, 0.1, None)
+    assert step(None, 0x40000, 0x20000, 10) == 1
+    assert step(0x50000, 0x40000, 0x20000, 1) == 1
+    assert step(0x50000, 0x40000, 0x20000, 8193) == 1
+    assert step(0x50008, 0x40000, 0x20000, 10) == 2
     assert not ctx  # no context was created by failing calls
     lib.dq_free(None)
     assert lib.dq_check(None, None) == 0
