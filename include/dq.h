@@ -301,10 +301,26 @@ dq_status dq_symbol_probs(int n, int levels, double p[16]);
  * that asked for more bytes than it holds), or
  * DQ_ECUDA if the stream reports an error.  ctx may be NULL (returns DQ_OK).
  * DQ_ETIMEOUT means a kernel stopped waiting after its time limit (2 s) so
- * that it could not hang: that call's output is not valid, and the context
- * may keep a stale per-unit count, so free it (dq_free) and start a new one.
+ * that it could not hang: that call's output is not valid.  A timed-out
+ * attention call may leave a per-unit record count behind; after dq_check has
+ * reported DQ_ETIMEOUT, the next attention call on the context clears those
+ * counts on its stream first, so the context stays usable.
  */
 dq_status dq_check(dq_ctx *ctx, void *stream);
+
+/*
+ * Test support for the timeout path.  Enqueues on `stream` one kernel whose
+ * bounded mbarrier wait (the same bounded wait the attention kernels use) is
+ * on a barrier nothing ever arrives at, so it gives up after limit_ns
+ * nanoseconds of wall time (clamped to [1000, 1e9]).  It then latches the
+ * same device status and leaves the same stale per-unit record count a
+ * timed-out attention call can leave, so that dq_check's DQ_ETIMEOUT report
+ * and the context's recovery can be exercised without a fault or a hang.
+ * `ctx` must come from an earlier call with a config (it owns the status word
+ * and the counts).  Errors: DQ_EINVAL (ctx NULL or without a workspace),
+ * DQ_ECUDA (launch).
+ */
+dq_status dq_test_expire_wait(dq_ctx *ctx, unsigned long long limit_ns, void *stream);
 
 /*
  * Allocation-free decode attention (this library's own addition; the pages
@@ -326,18 +342,25 @@ dq_status dq_check(dq_ctx *ctx, void *stream);
  *     call clears the part that must start at zero on `stream` first.  Calls
  *     whose work overlaps on the GPU (different streams, or different host
  *     threads without ordering) race on it and give wrong results: order them.
- *   - Limits: batch * n_kv_heads <= 16384, and the split partials (two
- *     records of 4 x (head_dim + 4) floats per KV head and CTA touching it)
- *     must fit the array; the grid is narrowed until they do, and a config
- *     that cannot fit even with one CTA is refused with DQ_EINVAL and a
- *     message naming the limit.
+ *   - Limits: batch * n_kv_heads <= 16384 (one ticket each), and the split
+ *     partials must fit the array: batch * n_kv_heads * r records of
+ *     4 x (head_dim + 4) floats, r being the record slots the plan gives a
+ *     unit (r = 2 to 7: one per CTA whose range touches the unit's packed
+ *     tokens and one per CTA that takes some of its 16-bit tiles).  Large
+ *     batches get r = 4 with 16-bit sink/recent slots and r = 2 without, so
+ *     the bound that comes first is the partials one: about 3,960 units at
+ *     head_dim 128 and 7,690 at head_dim 64 with 16-bit slots, twice that
+ *     without (then the 16384 ticket limit caps head_dim 64).  Where the
+ *     kernel can, the grid is narrowed until the partials fit; a config that
+ *     still does not fit is refused with DQ_EINVAL and a message naming the
+ *     bytes needed and held.
  *   - Device-side conditions (a bounded wait running out) are not reported by
  *     this entry point; use the context-based one with dq_check to see them.
  * DQ_RANS caches are refused (DQ_EUNSUPPORTED): their symbol model lives in a
  * context.
  * Errors: DQ_EINVAL, DQ_EALIGN, DQ_EUNSUPPORTED, DQ_ECUDA.
  */
-#define DQ_NOALLOC_SCRATCH_BYTES (4u << 20)
+#define DQ_NOALLOC_SCRATCH_BYTES (32u << 20)
 dq_status dq_decode_attention_noalloc(const dq_config *cfg, const dq_kv_buffers *bufs, const void *q,
                                       void *out, long long seq_len, float sm_scale, void *stream);
 

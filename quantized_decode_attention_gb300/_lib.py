@@ -79,6 +79,7 @@ def load() -> C.CDLL:
                                               C.c_float, P]
     L.dq_decode_attention_noalloc.restype = C.c_int
     L.dq_check.argtypes = [P, P]
+    L.dq_test_expire_wait.argtypes = [P, C.c_ulonglong, P]
     L.dq_free.argtypes = [P]
     L.dq_free.restype = None
     L.dq_last_error.restype = C.c_char_p
@@ -88,7 +89,7 @@ def load() -> C.CDLL:
                                 C.POINTER(C.c_int)]
     L.dq_symbol_probs.argtypes = [C.c_int, C.c_int, C.POINTER(C.c_double)]
     for f in ("dq_kv_sizes", "dq_quantize_kv", "dq_decode_attention", "dq_decode_step", "dq_dequantize_kv", "dq_check",
-              "dq_rans_model", "dq_symbol_probs"):
+              "dq_test_expire_wait", "dq_rans_model", "dq_symbol_probs"):
         getattr(L, f).restype = C.c_int
     _lib = L
     return L

@@ -34,8 +34,6 @@
 //    back and writes the output.
 #include <cuda_runtime.h>
 
-#include <cstdlib>
-
 #include "attn_common.cuh"
 #include "common.cuh"
 #include "dq_internal.h"
@@ -963,7 +961,6 @@ int plan_attention(const Layout &L, AttnArgs &a, int num_sms, long long cap_floa
     a.total_items = static_cast<long long>(L.U) * a.items_per_unit;
     if (a.total_items >= (1LL << 31)) return static_cast<int>(cudaErrorInvalidValue);  // entries are indexed in 32 bits
     long long G = static_cast<long long>(num_sms) * occ;
-    if (const char *env = std::getenv("DQ_ATTN_GRID")) G = std::atoll(env);
     if (G > a.total_items) G = a.total_items;
     if (G < 1) G = 1;
     for (;;) {
@@ -1027,6 +1024,37 @@ size_t attention_smem_bytes(const Layout &L) {
         return 0;
     });
     return s;
+}
+
+}  // namespace dq
+
+namespace dq {
+namespace {
+
+// One warp; lane 0 initialises an mbarrier that nothing arrives at and waits
+// on it with the bounded wait every pipeline here uses.  When the wait gives
+// up it latches ST_TIMEOUT and bumps unit 0's record count, as an attention
+// CTA that stopped waiting midway can, then completes the phase itself so the
+// barrier is quiet before it is invalidated.
+__global__ void __launch_bounds__(32) expire_wait_kernel(unsigned *status, int *counters, uint64_t limit_ns) {
+    __shared__ uint64_t bar;
+    if (threadIdx.x != 0) return;
+    const uint32_t b = smem_u32(&bar);
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;\n" ::"r"(b) : "memory");
+    asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+    if (!mbar_wait(&bar, 0, limit_ns)) {
+        atomicOr(status, ST_TIMEOUT);
+        atomicAdd(counters, 1);
+    }
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(b) : "memory");
+    asm volatile("mbarrier.inval.shared::cta.b64 [%0];\n" ::"r"(b) : "memory");
+}
+
+}  // namespace
+
+int launch_expire_wait(unsigned *status, int *counters, unsigned long long limit_ns, void *stream) {
+    expire_wait_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(status, counters, limit_ns);
+    return static_cast<int>(cudaGetLastError());
 }
 
 }  // namespace dq

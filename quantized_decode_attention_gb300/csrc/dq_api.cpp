@@ -802,6 +802,15 @@ dq_status dq_check(dq_ctx *ctx, void *stream) {
     return ok();
 }
 
+dq_status dq_test_expire_wait(dq_ctx *ctx, unsigned long long limit_ns, void *stream) {
+    if (!ctx || !ctx->status || !ctx->counters) return fail(DQ_EINVAL, "ctx has no workspace yet");
+    if (limit_ns < 1000ULL) limit_ns = 1000ULL;
+    if (limit_ns > 1000000000ULL) limit_ns = 1000000000ULL;
+    const int e = dq::launch_expire_wait(ctx->status, ctx->counters, limit_ns, stream);
+    if (e != 0) return fail(DQ_ECUDA, "expire-wait launch: %s", cudaGetErrorString(static_cast<cudaError_t>(e)));
+    return ok();
+}
+
 void dq_free(dq_ctx *ctx) {
     if (!ctx) return;
     cudaFree(ctx->status);

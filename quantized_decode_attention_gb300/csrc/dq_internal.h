@@ -242,6 +242,8 @@ int launch_dequant(const Layout &L, const DequantArgs &a, void *stream);
 int launch_attention(const Layout &L, const AttnArgs &a, int num_sms, void *stream);
 // q~ = T^{-T} q of every query head into qt [B][Hq][d] (dense key transforms)
 int launch_qcomp(const Layout &L, const float *q, const float *qc, float *qt, void *stream);
+// test support: a kernel whose bounded wait runs out (see dq_test_expire_wait)
+int launch_expire_wait(unsigned *status, int *counters, unsigned long long limit_ns, void *stream);
 // Fill the work schedule of `a` (items, grid, partial slots) for a launch on a
 // device with num_sms SMs whose partial workspace holds cap_floats floats.
 int plan_attention(const Layout &L, AttnArgs &a, int num_sms, long long cap_floats);

@@ -95,7 +95,9 @@ def test_validation_errors_without_gpu(lib):
     assert not ctx  # no context was created by failing calls
     lib.dq_free(None)
     assert lib.dq_check(None, None) == 0
+    assert lib.dq_test_expire_wait(None, 1000, None) == 1  # needs a context with a workspace
     assert lib.dq_status_name(7) == b"DQ_ENONFINITE"
+    assert lib.dq_status_name(8) == b"DQ_ETIMEOUT"
 
 
 def _dquant(**kw):

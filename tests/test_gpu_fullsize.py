@@ -3,8 +3,9 @@
 The caches and calls are the ones the benchmark times:
 - the Llama-3-8B-shaped decode layer (batch 16, 32 query / 8 KV heads, d128,
   8192 bf16 tokens, 4 sinks + 128 recent) at 2, 3 and 4 bits, prefilled, then
-  one token re-appended at position 8191 and attention over 8192 tokens, both
-  replayed from one CUDA graph;
+  the benchmark's step -- one token re-appended at position 8191 and attention
+  over 8192 tokens in one dq_decode_step -- replayed from a CUDA graph, with
+  bf16 outputs and, at 2 bits, fp32 outputs held to 2e-3 exactly;
 - the KVQuant NUQ cache (batch 8, 4096 fp16 Student-t tokens, 3 bits, 1 sink,
   1 % outliers), prefilled, attention over 4096 tokens from a CUDA graph.
 The oracle recomputes a few units one by one.  Their records, metadata, tables
@@ -55,21 +56,21 @@ def llama_inputs():
     return w, k, v, kn, vn, q
 
 
-@pytest.mark.parametrize("bits", [2, 3, 4])
-def test_llama_full_size_sampled_units(llama_inputs, bits):
+@pytest.mark.parametrize("bits,out_dtype", [(2, "bf16"), (3, "bf16"), (4, "bf16"), (2, "f32")])
+def test_llama_full_size_sampled_units(llama_inputs, bits, out_dtype):
     import torch
     from quantized_decode_attention_gb300 import KVCache
     w0, k, v, kn, vn, q = llama_inputs
-    w = w0.with_(bits=bits)
+    w = w0.with_(bits=bits, out_dtype=out_dtype)
     S = w.seq
     cache = KVCache.allocate(cfg_for(w), zero=False)
     cache.quantize(to_device(k, "bf16"), to_device(v, "bf16"), pos0=0)
     kn_d, vn_d, q_d = to_device(kn, "bf16"), to_device(vn, "bf16"), to_device(q, "f32")
-    out = torch.empty((w.batch, w.n_q_heads, w.head_dim), dtype=torch.bfloat16, device="cuda")
+    td = torch.float32 if out_dtype == "f32" else torch.bfloat16
+    out = torch.empty((w.batch, w.n_q_heads, w.head_dim), dtype=td, device="cuda")
 
     def step(s):
-        cache.quantize(kn_d, vn_d, pos0=S - 1, stream=s.cuda_stream)
-        cache.attention(q_d, out, S, stream=s.cuda_stream)
+        cache.decode_step(kn_d, vn_d, q_d, out, S, stream=s.cuda_stream)
 
     _graph_replay(step)
     cache.check()
