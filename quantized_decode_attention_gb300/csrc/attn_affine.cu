@@ -35,9 +35,7 @@
 //    they are widened to binary16 in registers, which costs more than the codes
 //    they would save.)
 //  * The sink and recent 16-bit tiles go to the CTA's last warp, which has a
-//    ring of its own and writes its records directly; packed warps never read
-//    16-bit slots, so only that warp waits for a preceding kernel in the stream
-//    (programmatic dependent launch).
+//    ring of its own.
 //  * Online softmax with a lagging maximum: accumulators are rescaled only when
 //    a logit exceeds the running maximum by more than 2^8, and the cross-lane
 //    reduction runs only then.
@@ -472,8 +470,6 @@ __global__ void __launch_bounds__(AF_WPB * 32, 1) attn_affine_kernel(AttnArgs a,
     ASmem<D, BITS, M16> &S = *reinterpret_cast<ASmem<D, BITS, M16> *>(smem_raw);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tig = lane & 3, g = lane >> 2;
     const int cta = blockIdx.x, G = gridDim.x;
-    // the combine grid may be scheduled now; it waits for the records it needs
-    asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
     const long long cpu = a.cpu, NP = a.np_total, NR = a.nr_total;
     const int WP = a.wp;
     const bool raw_warp = warp >= WP;
@@ -517,9 +513,7 @@ __global__ void __launch_bounds__(AF_WPB * 32, 1) attn_affine_kernel(AttnArgs a,
     const int x1i = static_cast<int>(x1);
     // each packed warp's first chunk, before the query preparation
     // the 16-bit tiles of this CTA's share of all units: the first AF_NSR
-    // copies go out now, with the packed warps' first chunks (the slots may be
-    // written by the kernel before this one in the stream, an append: wait for
-    // it first when launched as its programmatic dependent)
+    // copies go out now, with the packed warps' first chunks
     const long long r0 = static_cast<long long>(cta) * NR / G, r1 = static_cast<long long>(cta + 1) * NR / G;
     uint8_t *rring = S.ring + static_cast<size_t>(WP) * NS * C::SLOT;
     auto issue_raw_tile = [&](long long x, int s) {
@@ -530,7 +524,6 @@ __global__ void __launch_bounds__(AF_WPB * 32, 1) attn_affine_kernel(AttnArgs a,
     const int ru0 = r0 < r1 ? static_cast<int>(r0 / a.n_rt) : 0;
     const int n_runits = r0 < r1 ? static_cast<int>((r1 - 1) / a.n_rt) - ru0 + 1 : 0;  // <= AF_NUR (planner)
     if (raw_warp && r0 < r1) {
-        asm volatile("griddepcontrol.wait;\n" ::: "memory");
         for (int s = 0; s < AF_NSR && r0 + s < r1; s++) issue_raw_tile(r0 + s, s);
         // (hi, lo) 16-bit halves of the raw queries of the warp's units, loaded
         // now so that no load waits behind the cache stream later
@@ -720,29 +713,54 @@ __global__ void __launch_bounds__(AF_WPB * 32, 1) attn_affine_kernel(AttnArgs a,
     __syncthreads();
     constexpr int NSRC = 2 * AF_WPB + 1;  // warp z's final state, its saved state, the shared accumulator
     static_assert(NSRC <= 64, "two sources per lane");
+    const float *sbase = reinterpret_cast<const float *>(smem_raw);
     for (int ih = warp; ih < 4 * n_units; ih += AF_WPB) {
         const int i = ih >> 2, h = ih & 3, u = u_first + i;
-        auto src = [&](int z) -> const float * {
-            if (z < AF_WPB) return S.fin_u[z] == u ? fin + (z * 4 + h) * PR : nullptr;
-            if (z < 2 * AF_WPB) return S.save_u[z - AF_WPB] == u ? &S.save[z - AF_WPB][h][0] : nullptr;
-            return z == 2 * AF_WPB ? &S.uacc[i][h][0] : nullptr;
+        // source z as a float offset into shared memory (-1: no state of unit u)
+        auto src = [&](int z) -> int {
+            const float *p = nullptr;
+            if (z < AF_WPB) p = S.fin_u[z] == u ? fin + (z * 4 + h) * PR : nullptr;
+            else if (z < 2 * AF_WPB) p = S.save_u[z - AF_WPB] == u ? &S.save[z - AF_WPB][h][0] : nullptr;
+            else if (z == 2 * AF_WPB) p = &S.uacc[i][h][0];
+            return p ? static_cast<int>(p - sbase) : -1;
         };
         // lane l holds sources l and l + 32: their maxima, then their weights
-        const float *s0 = src(lane), *s1 = src(lane + 32);
-        const float m0 = s0 ? s0[D] : -INFINITY, m1 = s1 ? s1[D] : -INFINITY;
+        const int o0 = src(lane), o1 = src(lane + 32);
+        const float m0 = o0 >= 0 ? sbase[o0 + D] : -INFINITY, m1 = o1 >= 0 ? sbase[o1 + D] : -INFINITY;
         const float M = warp_max(fmaxf(m0, m1));
         const float w0 = m0 == -INFINITY ? 0.f : ex2(m0 - M), w1 = m1 == -INFINITY ? 0.f : ex2(m1 - M);
-        const float L = warp_sum((s0 ? w0 * s0[D + 1] : 0.f) + (s1 ? w1 * s1[D + 1] : 0.f));
+        const float L = warp_sum((o0 >= 0 ? w0 * sbase[o0 + D + 1] : 0.f) + (o1 >= 0 ? w1 * sbase[o1 + D + 1] : 0.f));
         constexpr int CPL = (D + 31) / 32;  // columns per lane
         float acc[CPL];
 #pragma unroll
         for (int j = 0; j < CPL; j++) acc[j] = 0.f;
-        for (int z = 0; z < NSRC; z++) {
-            const float w = __shfl_sync(FULL, z < 32 ? w0 : w1, z & 31);
-            if (w == 0.f) continue;  // warp-uniform
-            const float *sz = src(z);
+        // the live sources, eight at a time, their loads all in flight together
+        unsigned live0 = __ballot_sync(FULL, w0 != 0.f), live1 = __ballot_sync(FULL, w1 != 0.f);
+        while (live0 | live1) {
+            constexpr int NBAT = 8;
+            float wk[NBAT], v[NBAT][CPL];
 #pragma unroll
-            for (int j = 0; j < CPL; j++) acc[j] += w * sz[lane + 32 * j];
+            for (int k = 0; k < NBAT; k++) {
+                int off = 0;
+                wk[k] = 0.f;
+                if (live0) {
+                    const int z = __ffs(live0) - 1;
+                    live0 &= live0 - 1;
+                    wk[k] = __shfl_sync(FULL, w0, z);
+                    off = __shfl_sync(FULL, o0, z);
+                } else if (live1) {
+                    const int z = __ffs(live1) - 1;
+                    live1 &= live1 - 1;
+                    wk[k] = __shfl_sync(FULL, w1, z);
+                    off = __shfl_sync(FULL, o1, z);
+                }
+#pragma unroll
+                for (int j = 0; j < CPL; j++) v[k][j] = wk[k] != 0.f ? sbase[off + lane + 32 * j] : 0.f;
+            }
+#pragma unroll
+            for (int k = 0; k < NBAT; k++)
+#pragma unroll
+                for (int j = 0; j < CPL; j++) acc[j] = fmaf(wk[k], v[k][j], acc[j]);
         }
         const int first = owner(static_cast<long long>(u) * cpu, NP, G);
         float *rec = a.partials + (static_cast<long long>(u) * a.max_slots + (cta - first)) * 4 * PR + h * PR;

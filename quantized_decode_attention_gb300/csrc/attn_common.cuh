@@ -286,9 +286,16 @@ __device__ __forceinline__ void store_state(WarpState<D / 16> &st, bool quant, f
     }
 }
 
-// owner(x): the CTA whose item range [i*N/G, (i+1)*N/G) holds global item x.
+// owner(x): the CTA whose item range [i*N/G, (i+1)*N/G) holds global item x,
+// i.e. the largest c with c N < (x + 1) G.  Estimated in fp32 and settled with
+// exact 64-bit products, so no 64-bit division is needed (0 <= x < N).
 __device__ __forceinline__ int owner(long long x, long long N, int G) {
-    return static_cast<int>(((x + 1) * G + N - 1) / N) - 1;
+    const long long t = (x + 1) * G;
+    int c = static_cast<int>(__fdividef(static_cast<float>(t), static_cast<float>(N)));
+    c = c < 0 ? 0 : (c > G - 1 ? G - 1 : c);
+    while (c > 0 && static_cast<long long>(c) * N >= t) --c;
+    while (c + 1 < G && static_cast<long long>(c + 1) * N < t) ++c;
+    return c;
 }
 
 template <int V>
