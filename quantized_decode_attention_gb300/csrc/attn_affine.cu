@@ -446,13 +446,13 @@ __device__ void finish_head(const AttnArgs &a, const AttnShape &sh, int u, int h
     }
 }
 
-// The fused step's append of one unit's new token (keys, then values), kept
-// out of line: the attention's own loops keep the code layout they have
-// without it.
+// The fused step's append of one unit's new token (its keys or its values)
+// from inputs loaded earlier, kept out of line: the attention's own loops keep
+// the code layout they have without it.
 template <int V, int BITS>
-__device__ __noinline__ void append_rows(QuantArgs qk, QuantArgs qv, RowGeom rg, int u, float *xs) {
-    quantize_row<V, BITS>(qk, rg, u, 0, xs);
-    quantize_row<V, BITS>(qv, rg, u, 0, xs);
+__device__ __noinline__ void append_row(const QuantArgs &qa, const RowGeom &rg, int u, const RowIn<V> &in,
+                                        float *xs) {
+    quantize_loaded_row<V, BITS>(qa, rg, u, 0, in, xs);
 }
 
 // ---- the kernel ---------------------------------------------------------------
@@ -479,9 +479,30 @@ __global__ void __launch_bounds__(AF_WPB * 32, 1) attn_affine_kernel(AttnArgs a,
     const bool preps = (warp >> 2) < n_units;
     bool timed_out = false;
 
-    // the query loads go out first
+    // the query loads go out first, with the new token's rows in a fused step
+    // (loaded before any cache copy is issued, they do not queue behind them,
+    // and parked in shared memory until the append at the end)
     QLoad<D> qin;
     if (preps) load_unit_query<D>(a, sh, u_first + (warp >> 2), warp & 3, qin);
+    const bool appends = a.append && !raw_warp && warp >= WP - 2;
+    const int which = warp == WP - 1 ? 0 : 1;  // keys, values
+    // parking place: the save slot of the 16-bit-tile warp (a fused step has
+    // 16-bit slots, so that warp exists and never saves a state): keys and
+    // values as fp32 at [0, 2D), the key mean at [2D, 3D), the 16-bit bits
+    // from float 3D on
+    float *park = &S.save[AF_WPB - 1][0][0];
+    static_assert(4 * D <= 4 * PR, "the new token's rows fit a save slot");
+    if (appends && cta < sh.U) {
+        RowIn<D / 32> ain;
+        load_row<D / 32>(a.qa[which], cta, 0, ain);
+#pragma unroll
+        for (int j = 0; j < D / 32; j++) {
+            const int c = lane * (D / 32) + j;
+            park[which * D + c] = ain.x[j];
+            if (which == 0) park[2 * D + c] = ain.mu[j];
+            reinterpret_cast<uint16_t *>(park + 3 * D)[which * D + c] = ain.r[j];
+        }
+    }
     if (lane == 0) {
         if (!raw_warp) {
             for (int s = 0; s < NS; s++) mbar_init(&S.full[warp][s], 1);
@@ -545,22 +566,16 @@ __global__ void __launch_bounds__(AF_WPB * 32, 1) attn_affine_kernel(AttnArgs a,
         }
     }
     // fused decode step: the new token's 16-bit slot of unit u sits in tile
-    // e_new; the warp holding that tile quantizes the token into the cache (its
-    // packed slot lies in the recent window, so nothing in this call reads it)
-    // and, below, reads its 16-bit row from the input instead of the cache
+    // e_new, and the warp holding that tile reads the token's 16-bit row from
+    // the input instead of the cache.  The append itself is made by the
+    // packed warps below; nothing in this call reads what it writes (the
+    // token's packed slot lies in the recent window, its 16-bit row comes from
+    // the input).
     int rs_new = -1, e_new = -1;
     if (a.append) {
         const long long tn = a.qa[0].pos0;
         rs_new = tn < a.rg.n_sink ? static_cast<int>(tn) : a.rg.n_sink + static_cast<int>(tn % a.rg.n_recent);
         e_new = rs_new / AF_RTILE;
-    }
-    if (raw_warp && a.append) {
-        for (int j = 0; j < n_runits; j++) {
-            const int u = ru0 + j;
-            const long long x = static_cast<long long>(u) * a.n_rt + e_new;
-            if (x < r0 || x >= r1) continue;
-            append_rows<D / 32, BITS>(a.qa[0], a.qa[1], a.rg, u, &S.save[warp][0][0]);
-        }
     }
     // chunks in flight, oldest first: q0 in slot s, q1 in the next slot, ...
     int q0 = -1, q1 = -1, q2 = -1;
@@ -800,6 +815,27 @@ __global__ void __launch_bounds__(AF_WPB * 32, 1) attn_affine_kernel(AttnArgs a,
         }
         ++k;
     }
+    // fused decode step: CTA c appends the new token of units c, c + G, ...;
+    // its last two packed warps quantize the keys and the values here, at the
+    // end, where they overlap the warps finishing units instead of taking
+    // issue slots from the chunk loop
+    if (appends) {
+        for (int u = cta; u < sh.U; u += G) {
+            RowIn<D / 32> ain;
+            if (u == cta) {
+#pragma unroll
+                for (int j = 0; j < D / 32; j++) {
+                    const int c = lane * (D / 32) + j;
+                    ain.x[j] = park[which * D + c];
+                    ain.mu[j] = which == 0 ? park[2 * D + c] : 0.f;
+                    ain.r[j] = reinterpret_cast<const uint16_t *>(park + 3 * D)[which * D + c];
+                }
+            } else {
+                load_row<D / 32>(a.qa[which], u, 0, ain);
+            }
+            append_row<D / 32, BITS>(a.qa[which], a.rg, u, ain, &S.save[warp][0][0]);
+        }
+    }
 }
 
 template <int D, int BITS, bool M16>
@@ -807,6 +843,10 @@ struct AffineLauncher {
     using C = ACfg<D, BITS, M16>;
     static constexpr int TPC = C::TPC;
     static size_t smem() { return sizeof(ASmem<D, BITS, M16>); }
+    // a CTA's shared memory must fit the 227 KB an sm_103a block may use (2-bit
+    // head_dim 128 records with fp32 metadata do not: the older kernel serves them)
+    static constexpr bool FITS = sizeof(ASmem<D, BITS, M16>) <= 227 * 1024;
+
     static int prepare() {
         static bool done = false;
         if (done) return 0;
@@ -843,6 +883,7 @@ bool affine_kernel_applies(const Layout &L, const AttnArgs &a) {
     if (!(L.scheme == DQ_AFFINE && L.bits_k == L.bits_v && L.G <= 4 &&
           ((L.d == 128 && L.bits_k >= 2 && L.bits_k <= 4) || (L.d == 64 && (L.bits_k == 2 || L.bits_k == 4)))))
         return false;
+    if (!dispatch_affine(L, [](auto l) { return decltype(l)::FITS ? 1 : 0; })) return false;
     // a cache read mostly as 16-bit slots streams better through the CTA-wide
     // ring of attn_kernel, whose every warp takes 16-bit tiles
     const long long packed = a.n_q * (L.rowK + L.pairV / 2 + 4LL * L.meta_bytes);

@@ -40,24 +40,50 @@ __device__ __forceinline__ void rotate_row(float (&x)[V], int rot, float hscale,
 }
 
 // ---------------------------------------------------------------------------
-// Token pos0 + i of unit u: the 16-bit region copy (sinks and the latest
-// n_recent tokens, stored as given), then (past the sinks) rotation, mean
-// removal, the min/max or clipped grid, fp16 s and o, codes and the packed
-// record.  One warp; xs is D floats of the warp's shared memory.
+// The global inputs of token pos0 + i of unit u, lane l holding channels
+// l*V .. l*V+V-1: the values as fp32, the 16-bit bits a raw region keeps, and
+// the key channel mean (zeros when the row has none).  Split from the
+// arithmetic so that a caller can issue these loads early.
+// ---------------------------------------------------------------------------
+template <int V>
+struct RowIn {
+    float x[V], mu[V];
+    uint16_t r[V];
+};
+
+template <int V>
+__device__ __forceinline__ void load_row(const QuantArgs &a, int u, long long i, RowIn<V> &in) {
+    constexpr int D = 32 * V;
+    const int lane = threadIdx.x & 31;
+    const long long base = (static_cast<long long>(u) * a.n_tok + i) * D;
+#pragma unroll
+    for (int j = 0; j < V; j++) {
+        in.x[j] = ld_in(a.x, base + lane * V + j, a.in_dtype);
+        in.r[j] = raw16_of(a.x, base + lane * V + j, a.in_dtype);
+        in.mu[j] = a.use_mean ? a.mean[static_cast<long long>(u) * D + lane * V + j] : 0.f;
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Token pos0 + i of unit u from its loaded inputs: the 16-bit region copy
+// (sinks and the latest n_recent tokens, stored as given), then (past the
+// sinks) rotation, mean removal, the min/max or clipped grid, fp16 s and o,
+// codes and the packed record.  One warp; xs is D floats of the warp's shared
+// memory.
 // ---------------------------------------------------------------------------
 template <int V, int BITS>
-__device__ __forceinline__ void quantize_row(const QuantArgs &a, const RowGeom &L, int u, long long i, float *xs) {
+__device__ __forceinline__ void quantize_loaded_row(const QuantArgs &a, const RowGeom &L, int u, long long i,
+                                                    const RowIn<V> &in, float *xs) {
     constexpr int D = 32 * V;
     const int lane = threadIdx.x & 31;
     const long long t = a.pos0 + i;
     const int kvh = u % L.Hkv;
-    const long long base = (static_cast<long long>(u) * a.n_tok + i) * D;
 
     float x[V];
     bool finite = true;
 #pragma unroll
     for (int j = 0; j < V; j++) {
-        x[j] = ld_in(a.x, base + lane * V + j, a.in_dtype);
+        x[j] = in.x[j];
         finite = finite && isfinite(x[j]);
     }
     if (!__all_sync(FULL, finite) && lane == 0) atomicOr(a.status, ST_NONFINITE);
@@ -71,10 +97,9 @@ __device__ __forceinline__ void quantize_row(const QuantArgs &a, const RowGeom &
 #pragma unroll
         for (int j = 0; j < V; j++) {
             const int c = lane * V + j;
-            const uint16_t r = raw16_of(a.x, base + c, a.in_dtype);
             long long off = a.is_key ? static_cast<long long>(raw_slot) * D + c
                                      : (static_cast<long long>(raw_slot >> 1) * D + c) * 2 + (raw_slot & 1);
-            a.raw[ub + off] = r;
+            a.raw[ub + off] = in.r[j];
         }
     }
     if (t < L.n_sink) return;
@@ -82,9 +107,8 @@ __device__ __forceinline__ void quantize_row(const QuantArgs &a, const RowGeom &
 
     rotate_row<V>(x, a.rot, a.hscale, a.T ? a.T + static_cast<long long>(kvh) * D * D : nullptr, xs);
     if (a.use_mean) {
-        const float *mu = a.mean + static_cast<long long>(u) * D;
 #pragma unroll
-        for (int j = 0; j < V; j++) x[j] = __fsub_rn(x[j], mu[lane * V + j]);
+        for (int j = 0; j < V; j++) x[j] = __fsub_rn(x[j], in.mu[j]);
     }
 
     // grid
@@ -193,6 +217,14 @@ __device__ __forceinline__ void quantize_row(const QuantArgs &a, const RowGeom &
             if (lane == (w & 31)) rec[2 * w + e] = static_cast<uint16_t>(v >> (16 * e));
         }
     }
+}
+
+// Token pos0 + i of unit u: load_row, then quantize_loaded_row.
+template <int V, int BITS>
+__device__ __forceinline__ void quantize_row(const QuantArgs &a, const RowGeom &L, int u, long long i, float *xs) {
+    RowIn<V> in;
+    load_row<V>(a, u, i, in);
+    quantize_loaded_row<V, BITS>(a, L, u, i, in, xs);
 }
 
 }  // namespace dq

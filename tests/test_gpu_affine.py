@@ -34,6 +34,8 @@ CASES = {
     "llama3-ragged": (small(W.LLAMA, batch=2, n_kv_heads=2, n_q_heads=8, seq=409, bits=3), 409),
     "llama4-ragged": (small(W.LLAMA, batch=2, n_kv_heads=2, n_q_heads=8, seq=409, bits=4), 409),
     "llama2-short": (small(W.LLAMA, batch=1, n_kv_heads=2, n_q_heads=8, seq=100), 100),
+    "llama2-meta32": (small(W.LLAMA, batch=2, n_kv_heads=2, n_q_heads=8, seq=409, meta_dtype="f32"), 409),
+    "llama3-meta32": (small(W.LLAMA, batch=2, n_kv_heads=2, n_q_heads=8, seq=409, bits=3, meta_dtype="f32"), 409),
     "llama2-g2": (small(W.LLAMA, batch=2, n_kv_heads=4, n_q_heads=8, seq=257), 257),
     "qwen-dense-clip": (small(W.QWEN_LONG, batch=2, n_kv_heads=2, n_q_heads=8, seq=333), 333),
     "d64-bf16-2bit": (small(W.LLAMA, batch=2, n_kv_heads=2, n_q_heads=8, head_dim=64, seq=300, n_sink=2,
