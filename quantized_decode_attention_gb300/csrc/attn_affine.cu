@@ -729,6 +729,10 @@ __global__ void __launch_bounds__(AF_WPB * 32, 1) attn_affine_kernel(AttnArgs a,
     constexpr int NSRC = 2 * AF_WPB + 1;  // warp z's final state, its saved state, the shared accumulator
     static_assert(NSRC <= 64, "two sources per lane");
     const float *sbase = reinterpret_cast<const float *>(smem_raw);
+    // per warp, the live sources of the pair it merges (the query operands'
+    // space: they are dead once the chunks are done)
+    int2 *lists = reinterpret_cast<int2 *>(&S.qh[0][0][0][0]);
+    static_assert(sizeof(S.qh) >= AF_WPB * (NSRC + 1) * sizeof(int2), "merge lists fit the query operands' space");
     for (int ih = warp; ih < 4 * n_units; ih += AF_WPB) {
         const int i = ih >> 2, h = ih & 3, u = u_first + i;
         // source z as a float offset into shared memory (-1: no state of unit u)
@@ -749,34 +753,31 @@ __global__ void __launch_bounds__(AF_WPB * 32, 1) attn_affine_kernel(AttnArgs a,
         float acc[CPL];
 #pragma unroll
         for (int j = 0; j < CPL; j++) acc[j] = 0.f;
-        // the live sources, eight at a time, their loads all in flight together
-        unsigned live0 = __ballot_sync(FULL, w0 != 0.f), live1 = __ballot_sync(FULL, w1 != 0.f);
-        while (live0 | live1) {
-            constexpr int NBAT = 8;
-            float wk[NBAT], v[NBAT][CPL];
+        // the live sources, compacted into this warp's list as (offset, weight
+        // bits), then summed four at a time: every load address comes from a
+        // broadcast read, not from a chain of shuffles
+        int2 *lst = lists + warp * (NSRC + 1);
+        const unsigned b0 = __ballot_sync(FULL, w0 != 0.f), b1 = __ballot_sync(FULL, w1 != 0.f);
+        const unsigned below = (1u << lane) - 1u;
+        if (w0 != 0.f) lst[__popc(b0 & below)] = make_int2(o0, __float_as_int(w0));
+        if (w1 != 0.f) lst[__popc(b0) + __popc(b1 & below)] = make_int2(o1, __float_as_int(w1));
+        __syncwarp();
+        const int nlive = __popc(b0) + __popc(b1);
+        for (int k0 = 0; k0 < nlive; k0 += 4) {
+            int2 e[4];
+            float v[4][CPL];
 #pragma unroll
-            for (int k = 0; k < NBAT; k++) {
-                int off = 0;
-                wk[k] = 0.f;
-                if (live0) {
-                    const int z = __ffs(live0) - 1;
-                    live0 &= live0 - 1;
-                    wk[k] = __shfl_sync(FULL, w0, z);
-                    off = __shfl_sync(FULL, o0, z);
-                } else if (live1) {
-                    const int z = __ffs(live1) - 1;
-                    live1 &= live1 - 1;
-                    wk[k] = __shfl_sync(FULL, w1, z);
-                    off = __shfl_sync(FULL, o1, z);
-                }
+            for (int k = 0; k < 4; k++) e[k] = k0 + k < nlive ? lst[k0 + k] : make_int2(0, 0);
 #pragma unroll
-                for (int j = 0; j < CPL; j++) v[k][j] = wk[k] != 0.f ? sbase[off + lane + 32 * j] : 0.f;
-            }
+            for (int k = 0; k < 4; k++)
 #pragma unroll
-            for (int k = 0; k < NBAT; k++)
+                for (int j = 0; j < CPL; j++) v[k][j] = e[k].y != 0 ? sbase[e[k].x + lane + 32 * j] : 0.f;
 #pragma unroll
-                for (int j = 0; j < CPL; j++) acc[j] = fmaf(wk[k], v[k][j], acc[j]);
+            for (int k = 0; k < 4; k++)
+#pragma unroll
+                for (int j = 0; j < CPL; j++) acc[j] = fmaf(__int_as_float(e[k].y), v[k][j], acc[j]);
         }
+        __syncwarp();  // the list is rewritten for this warp's next pair
         const int first = owner(static_cast<long long>(u) * cpu, NP, G);
         float *rec = a.partials + (static_cast<long long>(u) * a.max_slots + (cta - first)) * 4 * PR + h * PR;
 #pragma unroll
@@ -787,18 +788,17 @@ __global__ void __launch_bounds__(AF_WPB * 32, 1) attn_affine_kernel(AttnArgs a,
         }
     }
     // publish: the records are visible GPU-wide before the units' counts move
-    // (the barrier orders every thread's record stores before the fence of the
-    // threads that take the tickets); the CTA whose record completes a unit
-    // merges that unit's records
+    // (the barrier orders every thread's record stores before the releasing
+    // add of the threads that take the tickets); the CTA whose record
+    // completes a unit merges that unit's records (the add also acquires: the
+    // unit's other records are visible to it, and to the CTA after the barrier)
     __syncthreads();
     if (threadIdx.x < n_units + n_runits) {  // one ticket per record: packed units, then 16-bit ones
-        __threadfence();
         const int t = threadIdx.x;
         const int u = t < n_units ? u_first + t : ru0 + (t - n_units);
         int np, nr;
         unit_records(a, u, G, np, nr);
-        const bool last = atomicAdd(a.counters + u, 1) + 1 == np + nr;
-        if (last) __threadfence();  // acquire: the unit's other records are visible (to the CTA after the barrier)
+        const bool last = atomic_add_acq_rel_gpu(a.counters + u, 1) + 1 == np + nr;
         S.done_u[t] = last ? u : -1;
     }
     __syncthreads();

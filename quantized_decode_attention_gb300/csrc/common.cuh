@@ -186,6 +186,16 @@ __device__ __forceinline__ float ex2(float x) {
     return y;
 }
 
+// Fetch-and-add with acquire-release semantics at GPU scope: writes made
+// before it (by the caller, or by its block before a barrier the caller
+// passed) are visible to whoever observes the new count, and writes released
+// by earlier adds to the same counter are visible to the caller.
+__device__ __forceinline__ int atomic_add_acq_rel_gpu(int *p, int v) {
+    int old;
+    asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;\n" : "=r"(old) : "l"(p), "r"(v) : "memory");
+    return old;
+}
+
 __device__ __forceinline__ uint64_t global_ns() {
     uint64_t t;
     asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
