@@ -62,12 +62,22 @@ def lib():
             L.or_rotate_hadamard.argtypes = [_f32, _f32, C.c_int]
             L.or_rotate_dense.argtypes = [_f32, _f32, _f32, C.c_int]
             L.or_quantile_pos.argtypes = [C.c_double, C.c_int, C.POINTER(C.c_int), C.POINTER(C.c_float)]
-            L.or_affine_quantize.argtypes = [_f32, C.c_int, C.c_int, C.c_int, C.c_double, _u8,
+            L.or_affine_quantize.argtypes = [_f32, C.c_int, C.c_int, C.c_int, C.c_double, C.c_float, _u8,
                                              C.POINTER(C.c_float), C.POINTER(C.c_float)]
+            L.or_quest_mse.restype = C.c_double
+            L.or_quest_mse.argtypes = [C.c_double, C.c_int]
+            L.or_quest_alpha_exact.restype = C.c_double
+            L.or_quest_alpha_exact.argtypes = [C.c_int]
+            L.or_quest_alpha.restype = C.c_double
+            L.or_quest_alpha.argtypes = [C.c_int]
+            L.or_quest_step_factor.restype = C.c_float
+            L.or_quest_step_factor.argtypes = [C.c_int]
+            L.or_quest_rms.restype = C.c_float
+            L.or_quest_rms.argtypes = [_f32, C.c_int]
             L.or_affine_dequant.argtypes = [_u8, C.c_int, C.c_float, C.c_float, C.c_void_p, _f32]
             L.or_quantize_unit.argtypes = [_f32, C.c_int, C.c_int, C.c_int, C.c_void_p, C.c_int,
                                            C.c_int, C.c_int, _f32, C.c_int, C.c_int, C.c_double,
-                                           C.c_int, _u8, _f32, _f32, C.c_void_p]
+                                           C.c_float, C.c_int, _u8, _f32, _f32, C.c_void_p]
             L.or_dequant_f64.argtypes = [_u8, _f32, _f32, C.c_void_p, C.c_int, C.c_int, C.c_int, _f64]
             L.or_attention_f64.argtypes = [_f64, _f64, _f64, C.c_int, C.c_int, C.c_int, C.c_double, _f64]
             L.or_k_row_bytes.restype = C.c_int
@@ -180,12 +190,35 @@ def quantile_pos(kappa: float, n: int):
     return i.value, f.value
 
 
-def affine_quantize(x: np.ndarray, bits: int, meta_f16: bool, clip: float = 0.0):
+def affine_quantize(x: np.ndarray, bits: int, meta_f16: bool, clip: float = 0.0, quest: bool = False):
+    """One token's codes and stored (s, o): min/max grid, quantile clip, or the
+    QuEST grid (quest=True)."""
     x = np.ascontiguousarray(x, dtype=np.float32)
     codes = np.zeros(x.shape[-1], dtype=np.uint8)
     s, o = C.c_float(), C.c_float()
-    lib().or_affine_quantize(x, x.shape[-1], bits, int(meta_f16), clip, codes, C.byref(s), C.byref(o))
+    qc = quest_step_factor(bits) if quest else 0.0
+    lib().or_affine_quantize(x, x.shape[-1], bits, int(meta_f16), clip, qc, codes, C.byref(s), C.byref(o))
     return codes, np.float32(s.value), np.float32(o.value)
+
+
+def quest_mse(alpha: float, levels: int) -> float:
+    """Mean squared error on N(0,1) of the symmetric grid clipped at +-alpha."""
+    return float(lib().or_quest_mse(alpha, levels))
+
+
+def quest_alpha(bits: int, exact: bool = False) -> float:
+    """The MSE-optimal Gaussian clip alpha_b (rounded to 4 decimals unless exact)."""
+    return float(lib().or_quest_alpha_exact(bits) if exact else lib().or_quest_alpha(bits))
+
+
+def quest_step_factor(bits: int) -> float:
+    """fp32 c_b = 2 alpha_b / 2^bits (s = c_b * RMS)."""
+    return float(lib().or_quest_step_factor(bits))
+
+
+def quest_rms(x: np.ndarray) -> float:
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    return float(lib().or_quest_rms(x, x.shape[-1]))
 
 
 def affine_dequant(codes, s, o, mu=None) -> np.ndarray:

@@ -19,7 +19,10 @@
  *    App. A Eq. (7)-(9): the affine terms fold into q.k and P.V.
  *  - "WUSH-KV: KV Cache Quantization with Data-Adaptive Transforms",
  *    Methodology: a dense d x d key transform after RoPE with query
- *    compensation, and an OSCAR-style percentile-clipped affine quantizer.
+ *    compensation, and an OSCAR-style percentile-clipped affine quantizer;
+ *    evaluation: the QuEST integer quantizer, per token, clipped from the
+ *    group RMS (symmetric), with the near-optimality result stated for
+ *    Gaussian tails.
  *  - "KVQuant-NUQ" (VeloxQuant-MLX docs), Attention Sink-Aware quantization:
  *    leading tokens kept exact in 16-bit and excluded from the fit.
  */
@@ -161,18 +164,122 @@ void or_quantile_pos(double kappa, int n, int *idx, float *frac) {
     *frac = (float)(pos - fl);
 }
 
+/* ------------------------------------------------------------------ */
+/* QuEST INT grid: symmetric, clipped at alpha_b times the token's RMS   */
+/* ------------------------------------------------------------------ */
+
+/* Standard normal cdf and density. */
+static double nrm_cdf(double x) { return 0.5 * erfc(-x / sqrt(2.0)); }
+static double nrm_pdf(double x) { return exp(-0.5 * x * x) / sqrt(2.0 * 3.14159265358979323846); }
+
+/* E[(X - c)^2 ; a < X < b] for X ~ N(0,1), from the closed forms
+ * int phi = Phi, int x phi = -phi, int x^2 phi = Phi - x phi; a = -inf or
+ * b = +inf allowed. */
+static double cell_mse(double a, double b, double c) {
+    double Pa = isinf(a) ? 0.0 : nrm_cdf(a), Pb = isinf(b) ? 1.0 : nrm_cdf(b);
+    double pa = isinf(a) ? 0.0 : nrm_pdf(a), pb = isinf(b) ? 0.0 : nrm_pdf(b);
+    double apa = isinf(a) ? 0.0 : a * pa, bpb = isinf(b) ? 0.0 : b * pb;
+    double m0 = Pb - Pa;
+    double m1 = -(pb - pa);
+    double m2 = (Pb - Pa) - (bpb - apa);
+    return m2 - 2.0 * c * m1 + c * c * m0;
+}
+
+/* Mean squared error on N(0,1) of the symmetric grid of L levels clipped at
+ * +-alpha: step D = 2 alpha / L, level k at -alpha + (k + 1/2) D, decision
+ * points halfway between levels, the outer cells open to +-infinity. */
+double or_quest_mse(double alpha, int L) {
+    double D = 2.0 * alpha / (double)L, sum = 0.0;
+    for (int k = 0; k < L; k++) {
+        double a = k == 0 ? -INFINITY : -alpha + (double)k * D;
+        double b = k == L - 1 ? INFINITY : -alpha + (double)(k + 1) * D;
+        sum += cell_mse(a, b, -alpha + ((double)k + 0.5) * D);
+    }
+    return sum;
+}
+
+/* The clip alpha that minimizes or_quest_mse for 2^bits levels
+ * (golden-section search on [0.05, 8]; the error is unimodal in alpha). */
+double or_quest_alpha_exact(int bits) {
+    int L = 1 << bits;
+    double lo = 0.05, hi = 8.0, g = (sqrt(5.0) - 1.0) / 2.0;
+    double x1 = hi - g * (hi - lo), x2 = lo + g * (hi - lo);
+    double f1 = or_quest_mse(x1, L), f2 = or_quest_mse(x2, L);
+    for (int it = 0; it < 200; it++) {
+        if (f1 < f2) { hi = x2; x2 = x1; f2 = f1; x1 = hi - g * (hi - lo); f1 = or_quest_mse(x1, L); }
+        else { lo = x1; x1 = x2; f1 = f2; x2 = lo + g * (hi - lo); f2 = or_quest_mse(x2, L); }
+    }
+    return 0.5 * (lo + hi);
+}
+
+/* alpha_b as the quantizer uses it: the minimizer rounded to 4 decimals. */
+double or_quest_alpha(int bits) { return floor(or_quest_alpha_exact(bits) * 1e4 + 0.5) / 1e4; }
+
+/* The fp32 step factor c_b = fp32(2 alpha_b / 2^bits): s = c_b * rms. */
+float or_quest_step_factor(int bits) { return (float)(2.0 * or_quest_alpha(bits) / (double)(1 << bits)); }
+
+/* fp32 RMS of x[0..d) in a fixed summation order: for l = 0..31, p_l sums
+ * the squares of channels l*V .. l*V+V-1 in channel order (V = d/32), then the
+ * 32 partial sums combine pairwise, p_l = p_l + p_(l xor k) for
+ * k = 16, 8, 4, 2, 1; rms = sqrt(p_0 / d).  Every step is one rounded fp32
+ * operation. */
+float or_quest_rms(const float *x, int d) {
+    int V = d / 32;
+    float p[32], q[32];
+    for (int l = 0; l < 32; l++) {
+        float a = x[l * V] * x[l * V];
+        for (int j = 1; j < V; j++) {
+            float t = x[l * V + j] * x[l * V + j];
+            a = a + t;
+        }
+        p[l] = a;
+    }
+    for (int k = 16; k >= 1; k >>= 1) {
+        for (int l = 0; l < 32; l++) q[l] = p[l] + p[l ^ k];
+        memcpy(p, q, sizeof p);
+    }
+    float ms = p[0] / (float)d;
+    return sqrtf(ms);
+}
+
 /*
  * Fit one token's grid and assign its codes.
  *   x[d]      : the (rotated, mean-removed) values
  *   clip      : 0 -> min/max grid (Eq. 4); else two-sided clip at the
  *               (1-clip) and clip quantiles of x, values clamped into it
+ *   quest_c   : > 0 -> the QuEST grid instead: s = quest_c * RMS(x),
+ *               o = -((L-1)/2) s (both rounded as meta_f16 says), a grid
+ *               symmetric about 0 whose outer levels sit half a step inside
+ *               +-alpha_b * RMS; values beyond fall to the outer codes
  *   meta_f16  : round s and o to binary16 before assigning codes (App. A)
  * Outputs codes[d] in 0..2^bits-1, and the stored scale/offset as floats.
  */
-void or_affine_quantize(const float *x, int d, int bits, int meta_f16, double clip,
+void or_affine_quantize(const float *x, int d, int bits, int meta_f16, double clip, float quest_c,
                         unsigned char *codes, float *s_out, float *o_out) {
     int L = 1 << bits;
     float lo, hi;
+    if (quest_c > 0.0f) {
+        float r = or_quest_rms(x, d);
+        float s = round_meta(quest_c * r, meta_f16);
+        float h = (float)(L - 1) * 0.5f;
+        float o = round_meta(-(h * s), meta_f16);
+        for (int j = 0; j < d; j++) {
+            int m = 0;
+            if (s != 0.0f) {
+                float t = (x[j] - o) / s;
+                if (t == t) {
+                    float rr = nearbyintf(t);
+                    if (rr < 0.0f) rr = 0.0f;
+                    if (rr > (float)(L - 1)) rr = (float)(L - 1);
+                    m = (int)rr;
+                }
+            }
+            codes[j] = (unsigned char)m;
+        }
+        *s_out = s;
+        *o_out = o;
+        return;
+    }
     if (clip > 0.0) {
         float *v = (float *)malloc(sizeof(float) * (size_t)d);
         memcpy(v, x, sizeof(float) * (size_t)d);
@@ -237,7 +344,7 @@ void or_affine_dequant(const unsigned char *codes, int d, float s, float o, cons
  */
 void or_quantize_unit(const float *x, int n, int d, int rot, const float *T, int mean,
                       int mean_t0, int mean_t1, float *mu_io, int bits, int meta_f16,
-                      double clip, int q_t0, unsigned char *codes, float *s, float *o,
+                      double clip, float quest_c, int q_t0, unsigned char *codes, float *s, float *o,
                       float *xhat) {
     float *y = (float *)malloc(sizeof(float) * (size_t)d);
     float *z = (float *)malloc(sizeof(float) * (size_t)d);
@@ -262,7 +369,7 @@ void or_quantize_unit(const float *x, int n, int d, int rot, const float *T, int
         if (mean) for (int j = 0; j < d; j++) z[j] = y[j] - mu_io[j];
         else memcpy(z, y, sizeof(float) * (size_t)d);
         long r = t - q_t0;
-        or_affine_quantize(z, d, bits, meta_f16, clip, codes + r * d, s + r, o + r);
+        or_affine_quantize(z, d, bits, meta_f16, clip, quest_c, codes + r * d, s + r, o + r);
         if (xhat) or_affine_dequant(codes + r * d, d, s[r], o[r], mean ? mu_io : NULL, xhat + r * d);
     }
     free(y);

@@ -76,6 +76,7 @@ def quantize_tensor(w: W.Workload, x_bits: np.ndarray, is_key: bool, S: int,
     rot = _ROT[w.rot_k if is_key else w.rot_v]
     mean = bool(w.mean_k) and is_key
     meta_f16 = 1 if w.meta_dtype == "f16" else 0
+    qc = float(L.or_quest_step_factor(bits)) if w.grid == "quest" else 0.0  # QuEST grid step factor
     q_t0 = max(0, w.n_sink - pos0)
     nq = n - q_t0
     codes = np.zeros((B, H, nq, d), dtype=np.uint8)
@@ -108,7 +109,7 @@ def quantize_tensor(w: W.Workload, x_bits: np.ndarray, is_key: bool, S: int,
             ou = np.zeros(nq, dtype=np.float32)
             xh = np.zeros((nq, d), dtype=np.float32)
             L.or_quantize_unit(xu, n, d, rot, Tp, mode, m_t0, m_t1, mu_u, bits, meta_f16,
-                               float(np.float32(w.clip)), q_t0, cu, su, ou, xh.ctypes.data_as(C.c_void_p))
+                               float(np.float32(w.clip)), qc, q_t0, cu, su, ou, xh.ctypes.data_as(C.c_void_p))
             codes[b, h], s[b, h], o[b, h], xhat[b, h], mu[b, h] = cu, su, ou, xh, mu_u
     return QuantTensor(codes, s, o, mu, xhat)
 

@@ -39,6 +39,7 @@ class Workload:
     rot_v: str = "hadamard"
     mean_k: bool = True
     clip: float = 0.0          # 0 = min/max; else two-sided quantile kappa
+    grid: str = "minmax"       # affine grid: "minmax" (or the kappa clip) | "quest"
     n_sink: int = 0
     n_recent: int = 0
     k_dist: str = "normal"     # "normal" | "llama" | "student4" | "cov"
