@@ -943,6 +943,51 @@ def preprocessing_effect(batch: int = 2, seq: int = 2048) -> dict:
             "model": [round(x, 6) for x in p.tolist()], "rows": rows}
 
 
+def grid_ablation(batch: int = 2, seq: int = 2048) -> dict:
+    """The grid comparison of "WUSH-KV" (evaluation: the quantizer held fixed,
+    relative squared Frobenius reconstruction error, keys and values quantized
+    separately, no full-precision windows), with the transform held fixed
+    instead: per token and head on the normalized Hadamard rotation, the
+    min/max grid, the percentile clip of the pages' serving setting (kappa 0.96
+    for keys, 0.92 for values) and the QuEST grid, at 2, 3 and 4 bits, through
+    the library (quantize, then dequantize in the rotated space).  Data: the
+    Llama-shaped synthetic keys and values, and the Qwen-shaped correlated keys."""
+    import torch
+    from quantized_decode_attention_gb300 import KVCache, make_config
+    out = []
+    dev16 = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).cuda().view(torch.bfloat16)
+    for w0 in (W.LLAMA, W.QWEN_LONG):
+        w = w0.with_(batch=batch, seq=seq)
+        B, H, d = w.batch, w.n_kv_heads, w.head_dim
+        k, v = W.make_kv(w)
+        k_dev, v_dev = dev16(k), dev16(v)
+        xr = {0: hadamard_rows(W.bf16_bits_to_f32(k).astype(np.float64)),
+              1: hadamard_rows(W.bf16_bits_to_f32(v).astype(np.float64))}
+        for bits in (2, 3, 4):
+            row = {"data": w0.name, "bits": bits}
+            for gname, kw in (("minmax", {}), ("clip", {"clip_k": 0.96, "clip_v": 0.92}),
+                              ("quest", {"grid_k": "quest"})):
+                cfg = make_config(batch=B, n_kv_heads=H, n_q_heads=w.n_q_heads, head_dim=d, max_seq=seq,
+                                  kv_dtype="bf16", meta_dtype="f16", out_dtype="f32", bits=bits, rot_k="hadamard",
+                                  rot_v="hadamard", mean_k=False, n_sink=0, n_recent=0, **kw)
+                cache = KVCache.allocate(cfg)
+                try:
+                    cache.quantize(k_dev, v_dev, pos0=0)
+                    xh = torch.empty((B, H, seq, d), dtype=torch.float32, device="cuda")
+                    for which, nm in ((0, "k"), (1, "v")):
+                        cache.dequantize(which, 0, seq, xh)
+                        torch.cuda.synchronize()
+                        e = xh.cpu().numpy().astype(np.float64) - xr[which]
+                        row[f"{nm}_{gname}"] = round(float(np.sum(e * e) / np.sum(xr[which] ** 2)), 5)
+                    cache.check()
+                finally:
+                    cache.close()
+            out.append(row)
+        del k_dev, v_dev
+        torch.cuda.empty_cache()
+    return {"rows": out, "workload": f"batch {batch}, {seq} tokens, 8 KV heads, d 128; fp16 s and o"}
+
+
 def cpu_baseline(w, bits, S, budget_s, k, v, q):
     """The oracle as it stands, timed on this host's cores, one worker process
     per core, a unit (sequence, KV head) per worker at a time: per unit the bulk
@@ -1170,6 +1215,13 @@ def main():
                        "3-bit quantizer: NMSE, entropy, Coding Gain = log2 M - H, Normal Gap = CE - H against "
                        "the analytic order-statistics model")
         line["diagnostics"]["preprocessing"] = pre
+        try:
+            gab = grid_ablation()
+        except Exception as e:  # a diagnostic never costs the measurement line
+            gab = {"error": f"{type(e).__name__}: {e}"}
+        gab["note"] = ("relative squared reconstruction error of K and V on the Hadamard rotation: min/max grid, "
+                       "percentile clip (kappa 0.96 keys / 0.92 values), QuEST grid (s = c_b RMS)")
+        line["diagnostics"]["grid_ablation"] = gab
     if rank == 0:
         print(json.dumps(line))
     if world > 1:

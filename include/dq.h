@@ -64,6 +64,8 @@ typedef enum {
 typedef enum { DQ_F32 = 0, DQ_F16 = 1, DQ_BF16 = 2 } dq_dtype;
 typedef enum { DQ_AFFINE = 0, DQ_NUQ = 1, DQ_RANS = 2 } dq_scheme;
 typedef enum { DQ_ROT_NONE = 0, DQ_ROT_HADAMARD = 1, DQ_ROT_DENSE = 2 } dq_rot;
+/* Affine grid of a token ("D-Quant", Sec. 4.2 Eq. (4); "WUSH-KV", evaluation). */
+typedef enum { DQ_GRID_MINMAX = 0, DQ_GRID_QUEST = 1 } dq_grid;
 
 /* Quantizer settings of one tensor (keys or values). */
 typedef struct {
@@ -75,6 +77,13 @@ typedef struct {
     int mean;            /* keys only: 1 = remove the channel mean frozen at prefill */
     float clip;          /* 0 = min/max grid; kappa in (0.5, 1) = clip to the
                             (1-kappa, kappa) linear-interpolated quantiles */
+    int grid;            /* DQ_AFFINE: DQ_GRID_MINMAX (min/max, or the clip above)
+                            or DQ_GRID_QUEST, the QuEST integer grid ("WUSH-KV",
+                            evaluation: per token, symmetric, clipped from the
+                            RMS): 2^bits levels o + s m with s = c_b RMS and
+                            o = -((2^bits - 1)/2) s, RMS over the token's
+                            rotated (mean-removed) values, c_b from
+                            dq_quest_step; needs clip = 0 */
     int lloyd_iters;     /* DQ_NUQ */
     float outlier_frac;  /* DQ_NUQ */
 } dq_tensor_cfg;
@@ -292,6 +301,16 @@ dq_status dq_rans_model(const dq_config *cfg, int which, int *levels, int f[16],
  * Errors: DQ_EINVAL (p NULL, n < 1, levels outside [2, 16]).
  */
 dq_status dq_symbol_probs(int n, int levels, double p[16]);
+
+/*
+ * The QuEST grid's step factor c_b = fp32(2 alpha_b / 2^bits) ("WUSH-KV",
+ * evaluation; the near-optimality result assumes Gaussian tails): alpha_b is
+ * the clip of the symmetric 2^bits-level grid that minimizes its mean squared
+ * error on a standard normal, rounded to 4 decimals (1.9914, 2.3441, 2.6816
+ * for 2, 3, 4 bits).  A token's scale is s = c_b * RMS.
+ * Host only.  Errors: DQ_EINVAL (c NULL, bits outside [1, 8]).
+ */
+dq_status dq_quest_step(int bits, float *c);
 
 /*
  * Synchronize `stream`, then return and clear the device-side status latched

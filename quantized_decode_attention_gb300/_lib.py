@@ -22,12 +22,13 @@ STATUS = ["DQ_OK", "DQ_EINVAL", "DQ_EALIGN", "DQ_EUNSUPPORTED", "DQ_EINFEASIBLE"
 DTYPES = {"f32": DQ_F32, "f16": DQ_F16, "bf16": DQ_BF16}
 ROTS = {"none": DQ_ROT_NONE, "hadamard": DQ_ROT_HADAMARD, "dense": DQ_ROT_DENSE}
 SCHEMES = {"affine": DQ_AFFINE, "nuq": DQ_NUQ, "rans": DQ_RANS}
+GRIDS = {"minmax": 0, "quest": 1}
 
 
 class TensorCfg(C.Structure):
     _fields_ = [("scheme", C.c_int), ("bits", C.c_int), ("levels", C.c_int), ("container_bytes", C.c_int),
-                ("rot", C.c_int), ("mean", C.c_int), ("clip", C.c_float), ("lloyd_iters", C.c_int),
-                ("outlier_frac", C.c_float)]
+                ("rot", C.c_int), ("mean", C.c_int), ("clip", C.c_float), ("grid", C.c_int),
+                ("lloyd_iters", C.c_int), ("outlier_frac", C.c_float)]
 
 
 class Config(C.Structure):
@@ -88,8 +89,9 @@ def load() -> C.CDLL:
     L.dq_rans_model.argtypes = [C.POINTER(Config), C.c_int, C.POINTER(C.c_int), C.POINTER(C.c_int),
                                 C.POINTER(C.c_int)]
     L.dq_symbol_probs.argtypes = [C.c_int, C.c_int, C.POINTER(C.c_double)]
+    L.dq_quest_step.argtypes = [C.c_int, C.POINTER(C.c_float)]
     for f in ("dq_kv_sizes", "dq_quantize_kv", "dq_decode_attention", "dq_decode_step", "dq_dequantize_kv", "dq_check",
-              "dq_test_expire_wait", "dq_rans_model", "dq_symbol_probs"):
+              "dq_test_expire_wait", "dq_rans_model", "dq_symbol_probs", "dq_quest_step"):
         getattr(L, f).restype = C.c_int
     _lib = L
     return L
@@ -112,6 +114,13 @@ def symbol_probs(n: int, levels: int):
     return list(p[:levels])
 
 
+def quest_step(bits: int) -> float:
+    """The QuEST grid's step factor c_b (a token's scale is c_b * RMS)."""
+    c = C.c_float()
+    _raise(load().dq_quest_step(bits, C.byref(c)))
+    return c.value
+
+
 def _raise(st: int):
     if st != 0:
         raise DQError(st, load().dq_last_error().decode())
@@ -119,7 +128,8 @@ def _raise(st: int):
 
 def make_config(*, batch, n_kv_heads, n_q_heads, head_dim, max_seq, kv_dtype="bf16", meta_dtype="f16",
                 out_dtype="bf16", bits=2, bits_v=None, rot_k="hadamard", rot_v="hadamard", mean_k=True,
-                clip_k=0.0, clip_v=None, n_sink=0, n_recent=0, scheme="affine", lloyd_iters=8,
+                clip_k=0.0, clip_v=None, grid_k="minmax", grid_v=None, n_sink=0, n_recent=0, scheme="affine",
+                lloyd_iters=8,
                 outlier_frac=0.01, levels_k=8, levels_v=6, container_k=331, container_v=231,
                 rans_alpha=1.4) -> Config:
     c = Config()
@@ -131,6 +141,8 @@ def make_config(*, batch, n_kv_heads, n_q_heads, head_dim, max_seq, kv_dtype="bf
     c.k.mean, c.v.mean = int(bool(mean_k)), 0
     c.k.clip = clip_k
     c.v.clip = clip_k if clip_v is None else clip_v
+    c.k.grid = GRIDS[grid_k]
+    c.v.grid = GRIDS[grid_k if grid_v is None else grid_v]
     c.n_sink, c.n_recent = n_sink, n_recent
     if scheme == "nuq":
         c.k.lloyd_iters = c.v.lloyd_iters = lloyd_iters

@@ -45,14 +45,15 @@ dq_status validate_tensor(const dq_tensor_cfg &t, int d, bool key, const char *n
             return fail(DQ_EINVAL, "%s: container_bytes must be in [8, 4096]", name);
         if (t.rot != DQ_ROT_NONE && t.rot != DQ_ROT_HADAMARD)
             return fail(DQ_EUNSUPPORTED, "%s: the entropy-coded scheme takes no rotation or a Hadamard one", name);
-        if (t.clip != 0.0f) return fail(DQ_EUNSUPPORTED, "%s: the entropy-coded scheme takes no clip", name);
+        if (t.clip != 0.0f || t.grid != DQ_GRID_MINMAX)
+            return fail(DQ_EUNSUPPORTED, "%s: the entropy-coded scheme takes no clip or grid choice", name);
         if (!key && t.mean) return fail(DQ_EINVAL, "%s: channel mean removal is for keys", name);
         return DQ_OK;
     }
     if (t.bits < 2 || t.bits > 4) return fail(DQ_EINVAL, "%s: bits must be 2, 3 or 4 (got %d)", name, t.bits);
     if (t.scheme == DQ_NUQ) {
-        if (t.rot != DQ_ROT_NONE || t.mean || t.clip != 0.0f)
-            return fail(DQ_EUNSUPPORTED, "%s: the non-uniform scheme takes no rotation, mean or clip", name);
+        if (t.rot != DQ_ROT_NONE || t.mean || t.clip != 0.0f || t.grid != DQ_GRID_MINMAX)
+            return fail(DQ_EUNSUPPORTED, "%s: the non-uniform scheme takes no rotation, mean, clip or grid", name);
         if (t.lloyd_iters < 0 || t.lloyd_iters > 64) return fail(DQ_EINVAL, "%s: lloyd_iters outside [0, 64]", name);
         if (!(t.outlier_frac >= 0.0f && t.outlier_frac < 0.5f))
             return fail(DQ_EINVAL, "%s: outlier_frac outside [0, 0.5)", name);
@@ -63,7 +64,51 @@ dq_status validate_tensor(const dq_tensor_cfg &t, int d, bool key, const char *n
     if (!key && t.mean) return fail(DQ_EINVAL, "%s: channel mean removal is for keys", name);
     if (!(t.clip == 0.0f || (t.clip > 0.5f && t.clip < 1.0f)))
         return fail(DQ_EINVAL, "%s: clip must be 0 or in (0.5, 1)", name);
+    if (t.grid != DQ_GRID_MINMAX && t.grid != DQ_GRID_QUEST) return fail(DQ_EINVAL, "%s: bad grid %d", name, t.grid);
+    if (t.grid == DQ_GRID_QUEST && t.clip != 0.0f)
+        return fail(DQ_EINVAL, "%s: the QuEST grid takes its clip from the RMS (clip must be 0)", name);
     return DQ_OK;
+}
+
+// ---- the QuEST grid's clip ---------------------------------------------------
+// The symmetric grid of L levels clipped at +-alpha has step D = 2 alpha / L and
+// level k at c_k = alpha (2k + 1 - L) / L, with decision points halfway between.
+// Its mean squared error e on N(0,1) has the derivative
+//   e'(alpha) = -2 sum_k (2k + 1 - L) / L * E[(X - c_k) ; X in cell k]
+// (moving alpha moves level k at rate (2k+1-L)/L; the cell edges move too,
+// but the error density is equal on both sides of a midpoint, so they add
+// nothing), with E[X - c ; a < X < b] = phi(a) - phi(b) - c (Phi(b) - Phi(a)).
+// e' is negative below the minimizing clip and positive above: bisection.
+double gauss_cdf(double x) { return 0.5 * std::erfc(-x * 0.70710678118654752440); }
+double gauss_pdf(double x) { return 0.39894228040143267794 * std::exp(-0.5 * x * x); }
+
+double quest_clip(int bits) {
+    const int L = 1 << bits;
+    auto g = [L](double alpha) {
+        const double D = 2.0 * alpha / L;
+        double acc = 0.0;
+        for (int k = 0; k < L; k++) {
+            const double c = alpha * (2.0 * k + 1.0 - L) / L;
+            const double pa = k == 0 ? 0.0 : gauss_pdf(-alpha + k * D);
+            const double pb = k == L - 1 ? 0.0 : gauss_pdf(-alpha + (k + 1) * D);
+            const double Pa = k == 0 ? 0.0 : gauss_cdf(-alpha + k * D);
+            const double Pb = k == L - 1 ? 1.0 : gauss_cdf(-alpha + (k + 1) * D);
+            acc += (2.0 * k + 1.0 - L) / L * ((pa - pb) - c * (Pb - Pa));
+        }
+        return -2.0 * acc;
+    };
+    double lo = 0.25, hi = 8.0;
+    for (int it = 0; it < 200 && hi - lo > 1e-15; it++) {
+        const double mid = 0.5 * (lo + hi);
+        (g(mid) < 0.0 ? lo : hi) = mid;
+    }
+    return std::floor(0.5 * (lo + hi) * 1e4 + 0.5) / 1e4;  // 4 decimals
+}
+
+float quest_step_factor(int bits) {
+    static float cache[9] = {};
+    if (cache[bits] == 0.0f) cache[bits] = static_cast<float>(2.0 * quest_clip(bits) / (1 << bits));
+    return cache[bits];
 }
 
 // Symbol models are a few milliseconds of host arithmetic; keep the last few.
@@ -504,6 +549,7 @@ static void fill_quant_args(const dq_config *cfg, const Layout &L, const dq_kv_b
     a.use_mean = which == 0 && t.mean;
     a.meta_f16 = cfg->meta_dtype == DQ_F16;
     a.clip = t.clip;
+    a.quest_c = t.grid == DQ_GRID_QUEST ? quest_step_factor(t.bits) : 0.0f;
     if (t.clip > 0.0f) {
         const double plo = (1.0 - static_cast<double>(t.clip)) * (L.d - 1);
         const double phi = static_cast<double>(t.clip) * (L.d - 1);
@@ -607,6 +653,13 @@ dq_status dq_symbol_probs(int n, int levels, double p[16]) {
     double q[dq::RANS_MAX_LEVELS];
     if (dq::rans_model_probs(n, levels, q) != 0) return fail(DQ_EINVAL, "no symbol model");
     for (int m = 0; m < 16; m++) p[m] = m < levels ? q[m] : 0.0;
+    return ok();
+}
+
+dq_status dq_quest_step(int bits, float *c) {
+    if (!c) return fail(DQ_EINVAL, "c is NULL");
+    if (bits < 1 || bits > 8) return fail(DQ_EINVAL, "bits must be in [1, 8] (got %d)", bits);
+    *c = quest_step_factor(bits);
     return ok();
 }
 

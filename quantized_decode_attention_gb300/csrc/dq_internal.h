@@ -132,6 +132,7 @@ struct QuantArgs {
     int is_key;
     int bits, rot, use_mean, meta_f16;
     float clip;             // 0 or kappa
+    float quest_c;          // > 0: the QuEST grid, s = quest_c * RMS (clip is 0)
     int clip_ilo, clip_ihi; // quantile order-statistic indices
     float clip_flo, clip_fhi;
     float hscale;           // fp32(1/sqrt(d))

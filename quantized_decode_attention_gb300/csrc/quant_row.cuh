@@ -113,8 +113,24 @@ __device__ __forceinline__ void quantize_loaded_row(const QuantArgs &a, const Ro
 
     // grid
     constexpr int LV = 1 << BITS;
-    float lo, hi;
-    if (a.clip > 0.0f) {
+    float lo = 0.f, hi = 0.f, s, o;
+    if (a.quest_c > 0.0f) {
+        // QuEST grid ("WUSH-KV", evaluation): symmetric about zero, step
+        // c_b * RMS.  The sum of squares runs over the lane's channels in
+        // order, then across lanes by xor butterfly (16, 8, 4, 2, 1), each
+        // step one rounded fp32 operation; the RMS divides by d (a power of
+        // two, exact) and takes the correctly rounded square root.
+        float ss = __fmul_rn(x[0], x[0]);
+#pragma unroll
+        for (int j = 1; j < V; j++) ss = __fadd_rn(ss, __fmul_rn(x[j], x[j]));
+#pragma unroll
+        for (int k = 16; k >= 1; k >>= 1) ss = __fadd_rn(ss, __shfl_xor_sync(FULL, ss, k));
+        const float rms = __fsqrt_rn(__fdiv_rn(ss, static_cast<float>(D)));
+        s = __fmul_rn(a.quest_c, rms);
+        if (a.meta_f16) s = __half2float(__float2half_rn(s));
+        o = -__fmul_rn(static_cast<float>(LV - 1) * 0.5f, s);
+        if (a.meta_f16) o = __half2float(__float2half_rn(o));
+    } else if (a.clip > 0.0f) {
         // order statistics by rank (ties broken by channel index)
 #pragma unroll
         for (int j = 0; j < V; j++) xs[lane * V + j] = x[j];
@@ -153,11 +169,13 @@ __device__ __forceinline__ void quantize_loaded_row(const QuantArgs &a, const Ro
         lo = warp_min(lo);
         hi = warp_max(hi);
     }
-    float s = __fdiv_rn(__fsub_rn(hi, lo), static_cast<float>(LV - 1));
-    float o = lo;
-    if (a.meta_f16) {
-        s = __half2float(__float2half_rn(s));
-        o = __half2float(__float2half_rn(o));
+    if (a.quest_c <= 0.0f) {
+        s = __fdiv_rn(__fsub_rn(hi, lo), static_cast<float>(LV - 1));
+        o = lo;
+        if (a.meta_f16) {
+            s = __half2float(__float2half_rn(s));
+            o = __half2float(__float2half_rn(o));
+        }
     }
 
     uint32_t m[V];

@@ -12,7 +12,8 @@ def cfg_for(w: W.Workload, max_seq: int | None = None, out_dtype: str | None = N
     return make_config(batch=w.batch, n_kv_heads=w.n_kv_heads, n_q_heads=w.n_q_heads, head_dim=w.head_dim,
                        max_seq=max_seq or w.seq, kv_dtype=w.kv_dtype, meta_dtype=w.meta_dtype,
                        out_dtype=out_dtype or w.out_dtype, bits=w.bits, rot_k=w.rot_k, rot_v=w.rot_v,
-                       mean_k=w.mean_k, clip_k=w.clip, clip_v=w.clip, n_sink=w.n_sink, n_recent=w.n_recent,
+                       mean_k=w.mean_k, clip_k=w.clip, clip_v=w.clip, grid_k=w.grid, n_sink=w.n_sink,
+                       n_recent=w.n_recent,
                        scheme=w.scheme, lloyd_iters=w.extra.get("lloyd_iters", 8),
                        outlier_frac=w.extra.get("outlier_frac", 0.01),
                        levels_k=w.extra.get("levels_k", 8), levels_v=w.extra.get("levels_v", 6),

@@ -240,3 +240,31 @@ def test_ablation_settings_feasibility(lib):
         assert fits(8, ck) and fits(6, cv), (ck, cv)
     for ck in bench.ABL_KEY_BYTES:
         assert fits(8, ck) and fits(6, bench.ABL_PAIR_BYTES - ck), ck
+
+
+def test_quest_step_factor_matches_the_oracle(lib):
+    # the library derives alpha_b on its own (bisection on the derivative of the
+    # Gaussian error); the oracle by golden-section search on the error itself
+    import oracle
+    from quantized_decode_attention_gb300 import _lib
+    for bits in range(1, 9):
+        assert _lib.quest_step(bits) == np.float32(oracle.quest_step_factor(bits)), bits
+    c = C.c_float()
+    assert lib.dq_quest_step(0, C.byref(c)) == 1 and lib.dq_quest_step(2, None) == 1
+
+
+def test_quest_grid_validation(lib):
+    from quantized_decode_attention_gb300 import _lib, make_config
+    arr = (C.c_size_t * _lib.NUM_BUFFERS)()
+    base = dict(batch=2, n_kv_heads=2, n_q_heads=8, head_dim=128, max_seq=512, n_sink=4, n_recent=16)
+    ref = (C.c_size_t * _lib.NUM_BUFFERS)()
+    assert lib.dq_kv_sizes(C.byref(make_config(**base)), ref) == 0
+    assert lib.dq_kv_sizes(C.byref(make_config(**base, grid_k="quest")), arr) == 0
+    assert list(arr) == list(ref)  # same layout: the grid only picks s and o
+    assert lib.dq_kv_sizes(C.byref(make_config(**base, grid_k="quest", clip_k=0.99)), arr) == 1
+    cfg = make_config(**base)
+    cfg.k.grid = 2
+    assert lib.dq_kv_sizes(C.byref(cfg), arr) == 1
+    nuq = make_config(**{**base, "n_recent": 0}, scheme="nuq", rot_k="none", rot_v="none", mean_k=False, bits=3)
+    nuq.k.grid = 1
+    assert lib.dq_kv_sizes(C.byref(nuq), arr) == 3

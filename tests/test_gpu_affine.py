@@ -35,6 +35,15 @@ CASES = {
     "llama4-ragged": (small(W.LLAMA, batch=2, n_kv_heads=2, n_q_heads=8, seq=409, bits=4), 409),
     "llama2-short": (small(W.LLAMA, batch=1, n_kv_heads=2, n_q_heads=8, seq=100), 100),
     "llama2-meta32": (small(W.LLAMA, batch=2, n_kv_heads=2, n_q_heads=8, seq=409, meta_dtype="f32"), 409),
+    # the QuEST grid ("WUSH-KV", evaluation) on the same caches
+    "llama2-quest": (small(W.LLAMA, batch=2, n_kv_heads=2, n_q_heads=8, seq=409, grid="quest"), 409),
+    "llama3-quest": (small(W.LLAMA, batch=2, n_kv_heads=2, n_q_heads=8, seq=409, bits=3, grid="quest"), 409),
+    "llama4-quest-meta32": (small(W.LLAMA, batch=2, n_kv_heads=2, n_q_heads=8, seq=409, bits=4, grid="quest",
+                                  meta_dtype="f32"), 409),
+    "d64-quest": (small(W.LLAMA, batch=2, n_kv_heads=2, n_q_heads=8, head_dim=64, seq=300, n_sink=2,
+                        n_recent=32, grid="quest"), 300),
+    "qwen-dense-quest": (small(W.QWEN_LONG, batch=2, n_kv_heads=2, n_q_heads=8, seq=333, clip=0.0,
+                               grid="quest"), 333),
     "llama3-meta32": (small(W.LLAMA, batch=2, n_kv_heads=2, n_q_heads=8, seq=409, bits=3, meta_dtype="f32"), 409),
     "llama2-g2": (small(W.LLAMA, batch=2, n_kv_heads=4, n_q_heads=8, seq=257), 257),
     "qwen-dense-clip": (small(W.QWEN_LONG, batch=2, n_kv_heads=2, n_q_heads=8, seq=333), 333),

@@ -28,6 +28,7 @@ CASES = {
     "d64-2bit": W.LLAMA.with_(batch=2, n_kv_heads=2, n_q_heads=8, head_dim=64, seq=400, n_sink=2, n_recent=32),
     "dense-clip": W.QWEN_LONG.with_(batch=2, n_kv_heads=2, n_q_heads=8, seq=400, n_sink=2, n_recent=16),
     "no-recent": W.LLAMA.with_(batch=1, n_kv_heads=2, n_q_heads=8, seq=400, bits=4, n_sink=1, n_recent=0),
+    "quest": W.LLAMA.with_(batch=2, n_kv_heads=2, n_q_heads=8, seq=400, grid="quest"),
 }
 
 
