@@ -342,6 +342,22 @@ dq_status dq_check(dq_ctx *ctx, void *stream);
 dq_status dq_test_expire_wait(dq_ctx *ctx, unsigned long long limit_ns, void *stream);
 
 /*
+ * Bounds-checked build.  Built with DQ_CHECKED defined (libdq_checked.so next
+ * to libdq.so), the library tests every global access of the affine path --
+ * the row quantizer and key mean, decode attention with the fused append, the
+ * allocation-free entry point, dequantization -- against the byte size of its
+ * buffer first; an access outside is skipped and latched, and dq_check then
+ * returns DQ_EINVAL ("an access fell outside its buffer").  A skipped bulk copy
+ * still completes its pipeline stage, so the call runs to its end.  The
+ * non-uniform and entropy-coded kernels are not checked.
+ * Test support: dq_test_checked_probe enqueues one range test that lies one
+ * byte past a buffer (nothing is accessed): the checked build latches it, the
+ * normal build does nothing.  Errors: DQ_EINVAL (ctx without a workspace),
+ * DQ_ECUDA.
+ */
+dq_status dq_test_checked_probe(dq_ctx *ctx, void *stream);
+
+/*
  * Allocation-free decode attention (this library's own addition; the pages
  * have no counterpart).  Computes exactly what dq_decode_attention computes,
  * with the same arguments minus the context, but never calls cudaMalloc,

@@ -56,6 +56,17 @@ class DQError(RuntimeError):
 
 
 _lib = None
+_lib_path = LIB_PATH
+
+
+def use_checked_build() -> None:
+    """Make this process load the bounds-checked build (libdq_checked.so, built
+    with quantized_decode_attention_gb300.build.build(checked=True)) instead of
+    libdq.so.  Call before the library is first loaded."""
+    global _lib_path
+    if _lib is not None:
+        raise RuntimeError("the library is already loaded in this process")
+    _lib_path = os.path.join(os.path.dirname(LIB_PATH), "libdq_checked.so")
 
 
 def load() -> C.CDLL:
@@ -63,9 +74,9 @@ def load() -> C.CDLL:
     global _lib
     if _lib is not None:
         return _lib
-    if not os.path.exists(LIB_PATH):
-        raise RuntimeError(f"{LIB_PATH} is not built; run quantized_decode_attention_gb300.build.build()")
-    L = C.CDLL(LIB_PATH)
+    if not os.path.exists(_lib_path):
+        raise RuntimeError(f"{_lib_path} is not built; run quantized_decode_attention_gb300.build.build()")
+    L = C.CDLL(_lib_path)
     P = C.c_void_p
     L.dq_kv_sizes.argtypes = [C.POINTER(Config), C.POINTER(C.c_size_t)]
     L.dq_quantize_kv.argtypes = [C.POINTER(P), C.POINTER(Config), C.POINTER(Buffers), P, P, C.c_longlong,
@@ -81,6 +92,7 @@ def load() -> C.CDLL:
     L.dq_decode_attention_noalloc.restype = C.c_int
     L.dq_check.argtypes = [P, P]
     L.dq_test_expire_wait.argtypes = [P, C.c_ulonglong, P]
+    L.dq_test_checked_probe.argtypes = [P, P]
     L.dq_free.argtypes = [P]
     L.dq_free.restype = None
     L.dq_last_error.restype = C.c_char_p
@@ -91,7 +103,8 @@ def load() -> C.CDLL:
     L.dq_symbol_probs.argtypes = [C.c_int, C.c_int, C.POINTER(C.c_double)]
     L.dq_quest_step.argtypes = [C.c_int, C.POINTER(C.c_float)]
     for f in ("dq_kv_sizes", "dq_quantize_kv", "dq_decode_attention", "dq_decode_step", "dq_dequantize_kv", "dq_check",
-              "dq_test_expire_wait", "dq_rans_model", "dq_symbol_probs", "dq_quest_step"):
+              "dq_test_expire_wait", "dq_test_checked_probe", "dq_rans_model", "dq_symbol_probs",
+              "dq_quest_step"):
         getattr(L, f).restype = C.c_int
     _lib = L
     return L

@@ -1050,7 +1050,18 @@ __global__ void __launch_bounds__(32) expire_wait_kernel(unsigned *status, int *
     asm volatile("mbarrier.inval.shared::cta.b64 [%0];\n" ::"r"(b) : "memory");
 }
 
+// One lane tests a byte range that ends one byte past a 4-byte buffer (the
+// status word itself): the checked build latches ST_OOB; nothing is accessed.
+__global__ void __launch_bounds__(32) checked_probe_kernel(unsigned *status) {
+    if (threadIdx.x == 0) (void)in_buf(reinterpret_cast<const char *>(status) + 1, 4, status, 4, status);
+}
+
 }  // namespace
+
+int launch_checked_probe(unsigned *status, void *stream) {
+    checked_probe_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(status);
+    return static_cast<int>(cudaGetLastError());
+}
 
 int launch_expire_wait(unsigned *status, int *counters, unsigned long long limit_ns, void *stream) {
     expire_wait_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(status, counters, limit_ns);

@@ -54,6 +54,8 @@
 namespace dq {
 namespace {
 
+static_assert(ST_OOB == 32u, "in_buf latches ST_OOB");
+
 constexpr int AF_WPB = 16;                       // warps per CTA
 constexpr int AF_NUS = 4;                        // units a CTA's packed range may touch
 constexpr int AF_NSR = 3;                        // ring slots of the 16-bit-tile warp
@@ -113,11 +115,14 @@ __device__ __forceinline__ void load_unit_query(const AttnArgs &a, const AttnSha
     const int lane = threadIdx.x & 31;
     const int b = u / sh.Hkv, kvh = u % sh.Hkv;
     const long long qo = (static_cast<long long>(b) * sh.Hkv * sh.G + kvh * sh.G + h) * D + lane * V;
+    const bool okq = h < sh.G && in_buf(a.q + qo - lane * V, D * 4, a.q, a.sz_q, a.status);
+    const bool okm = a.mean_k && in_buf(a.mean_k + static_cast<long long>(u) * D, D * 4, a.mean_k, a.sz_mean_k,
+                                        a.status);
 #pragma unroll
     for (int j = 0; j < V; j++) {
-        in.x[j] = h < sh.G ? __ldg(a.q + qo + j) : 0.f;
-        in.mu[j] = a.mean_k ? __ldg(a.mean_k + static_cast<long long>(u) * D + lane * V + j) : 0.f;
-        if (a.rot_k == DQ_ROT_DENSE && a.q_tilde) in.x[j] = h < sh.G ? __ldg(a.q_tilde + qo + j) : 0.f;
+        in.x[j] = okq ? __ldg(a.q + qo + j) : 0.f;
+        in.mu[j] = okm ? __ldg(a.mean_k + static_cast<long long>(u) * D + lane * V + j) : 0.f;
+        if (a.rot_k == DQ_ROT_DENSE && a.q_tilde) in.x[j] = okq ? __ldg(a.q_tilde + qo + j) : 0.f;
     }
 }
 
@@ -145,11 +150,13 @@ __device__ void prep_unit(const AttnArgs &a, const AttnShape &sh, ASmem<D, BITS,
         for (int j = 0; j < V; j++) scr[lane * V + j] = x[j];
         __syncwarp();
         const float *Qc = a.q_comp + static_cast<long long>(u % sh.Hkv) * D * D;
+        const bool okc = in_buf(Qc, static_cast<long long>(D) * D * 4, a.q_comp, a.sz_q_comp, a.status);
 #pragma unroll
         for (int j = 0; j < V; j++) {
             const float *row = Qc + static_cast<long long>(lane * V + j) * D;
             float acc = 0.f;
-            for (int k = 0; k < D; k++) acc += __ldg(row + k) * scr[k];
+            if (okc)
+                for (int k = 0; k < D; k++) acc += __ldg(row + k) * scr[k];
             x[j] = h < sh.G ? acc : 0.f;
         }
         __syncwarp();
@@ -189,6 +196,13 @@ __device__ __forceinline__ void issue_chunk(const AttnArgs &a, long long qcap, i
     const uint8_t *mv = static_cast<const uint8_t *>(a.meta_v) + g0 * 2 * C::MB;
     const uint32_t kb = nt * C::ROWK, vb = nt / 2 * C::PAIRV, mb = nt * 2 * C::MB;
     const uint32_t sb = smem_u32(slot), br = smem_u32(bar);
+    if (!(in_buf(ck, kb, a.codes_k, a.sz_codes_k, a.status) && in_buf(cv, vb, a.codes_v, a.sz_codes_v, a.status) &&
+          in_buf(mk, mb, a.meta_k, a.sz_meta_k, a.status) && in_buf(mv, mb, a.meta_v, a.sz_meta_v, a.status))) {
+        // checked build: the copies are skipped and the slot's phase completes empty
+        asm volatile("{\n .reg .pred p;\n elect.sync _|p, 0xffffffff;\n"
+                     "@p mbarrier.arrive.shared::cta.b64 _, [%0];\n}\n" ::"r"(br) : "memory");
+        return;
+    }
     asm volatile(
         "{\n .reg .pred p;\n elect.sync _|p, 0xffffffff;\n"
         "@p mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n"
@@ -206,6 +220,12 @@ template <int D>
 __device__ __forceinline__ void issue_raw(const AttnArgs &a, int rcap, int u, int e, uint8_t *slot, uint64_t *bar) {
     const long long r0 = static_cast<long long>(u) * rcap + static_cast<long long>(e) * AF_RTILE;
     const uint16_t *rk = a.raw_k + r0 * D, *rv = a.raw_v + r0 * D;
+    if (!(in_buf(rk, 32 * D, a.raw_k, a.sz_raw_k, a.status) && in_buf(rv, 32 * D, a.raw_v, a.sz_raw_v, a.status))) {
+        // checked build: the copies are skipped and the slot's phase completes empty
+        asm volatile("{\n .reg .pred p;\n elect.sync _|p, 0xffffffff;\n"
+                     "@p mbarrier.arrive.shared::cta.b64 _, [%0];\n}\n" ::"r"(smem_u32(bar)) : "memory");
+        return;
+    }
     asm volatile(
         "{\n .reg .pred p;\n elect.sync _|p, 0xffffffff;\n"
         "@p mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n"
@@ -404,9 +424,10 @@ __device__ void finish_head(const AttnArgs &a, const AttnShape &sh, int u, int h
             const bool in = r < n_rec;
             const int slot = r < np ? r : a.mps + (r - np);
             const float *p = pu + static_cast<long long>(in ? slot : 0) * 4 * PR;
-            mr[k] = in ? __ldcg(p + D) : -INFINITY;
-            lr[k] = in ? __ldcg(p + D + 1) : 0.f;
-            vv[k] = in ? __ldcg(reinterpret_cast<const VT *>(p) + lane) : VT{};
+            const bool ok = in && in_buf(p, PR * 4, a.partials, a.sz_partials, a.status);
+            mr[k] = ok ? __ldcg(p + D) : -INFINITY;
+            lr[k] = ok ? __ldcg(p + D + 1) : 0.f;
+            vv[k] = ok ? __ldcg(reinterpret_cast<const VT *>(p) + lane) : VT{};
         }
         float mb = M;
 #pragma unroll
@@ -436,6 +457,8 @@ __device__ void finish_head(const AttnArgs &a, const AttnShape &sh, int u, int h
     }
     const float inv = 1.f / Lsum;
     const long long ob = (static_cast<long long>(b) * sh.Hkv * sh.G + kvh * sh.G + h) * D;
+    const int osz = a.out_dtype == DQ_F32 ? 4 : 2;
+    if (!in_buf(static_cast<char *>(a.out) + ob * osz, D * osz, a.out, a.sz_out, a.status)) return;
 #pragma unroll
     for (int j = 0; j < V; j++) {
         const float y = (accq[j] + accr[j]) * inv;
@@ -554,10 +577,11 @@ __global__ void __launch_bounds__(AF_WPB * 32, 1) attn_affine_kernel(AttnArgs a,
 #pragma unroll
             for (int h = 0; h < 4; h++) {
                 const long long qo = (static_cast<long long>(b) * sh.Hkv * sh.G + kvh * sh.G + h) * D;
+                const bool okq = h < sh.G && in_buf(a.q + qo, D * 4, a.q, a.sz_q, a.status);
 #pragma unroll
                 for (int jj = 0; jj < V; jj++) {
                     const int c = lane * V + jj;
-                    const float xq = h < sh.G ? __ldg(a.q + qo + c) : 0.f;
+                    const float xq = okq ? __ldg(a.q + qo + c) : 0.f;
                     const uint32_t w = a.raw_bf16 ? hilo_bf16(xq) : hilo_f16(xq);
                     S.rqh[j][0][h][c] = static_cast<uint16_t>(w & 0xffffu);
                     S.rqh[j][1][h][c] = static_cast<uint16_t>(w >> 16);
@@ -676,7 +700,7 @@ __global__ void __launch_bounds__(AF_WPB * 32, 1) attn_affine_kernel(AttnArgs a,
                 const int first = owner(static_cast<long long>(ru) * n_rt, NR, G);
                 float *rec = a.partials +
                              (static_cast<long long>(ru) * a.max_slots + a.mps + (cta - first)) * 4 * PR;
-                store_state<D, BITS>(st, false, rec, PR);
+                if (in_buf(rec, 4 * PR * 4, a.partials, a.sz_partials, a.status)) store_state<D, BITS>(st, false, rec, PR);
             };
             for (long long x = r0; x < r1; x++) {
                 const int k = static_cast<int>(x - r0), s = k % AF_NSR;
@@ -700,11 +724,16 @@ __global__ void __launch_bounds__(AF_WPB * 32, 1) attn_affine_kernel(AttnArgs a,
                     uint16_t *vr = reinterpret_cast<uint16_t *>(tile + 32 * D) + (sl >> 1) * 2 * D + (sl & 1);
                     constexpr int V = D / 32;
                     const long long base = static_cast<long long>(u) * D;
+                    const long long esz = a.qa[0].in_dtype == 0 ? 4 : 2;
+                    const bool okk = in_buf(static_cast<const char *>(a.qa[0].x) + base * esz, D * esz, a.qa[0].x,
+                                            a.qa[0].sz_x, a.status);
+                    const bool okv = in_buf(static_cast<const char *>(a.qa[1].x) + base * esz, D * esz, a.qa[1].x,
+                                            a.qa[1].sz_x, a.status);
 #pragma unroll
                     for (int j = 0; j < V; j++) {
                         const int c = lane * V + j;
-                        kr[c] = raw16_of(a.qa[0].x, base + c, a.qa[0].in_dtype);
-                        vr[2 * c] = raw16_of(a.qa[1].x, base + c, a.qa[1].in_dtype);
+                        kr[c] = okk ? raw16_of(a.qa[0].x, base + c, a.qa[0].in_dtype) : 0;
+                        vr[2 * c] = okv ? raw16_of(a.qa[1].x, base + c, a.qa[1].in_dtype) : 0;
                     }
                     __syncwarp();
                 }
@@ -780,11 +809,13 @@ __global__ void __launch_bounds__(AF_WPB * 32, 1) attn_affine_kernel(AttnArgs a,
         __syncwarp();  // the list is rewritten for this warp's next pair
         const int first = owner(static_cast<long long>(u) * cpu, NP, G);
         float *rec = a.partials + (static_cast<long long>(u) * a.max_slots + (cta - first)) * 4 * PR + h * PR;
+        if (in_buf(rec, PR * 4, a.partials, a.sz_partials, a.status)) {
 #pragma unroll
-        for (int j = 0; j < CPL; j++) rec[lane + 32 * j] = acc[j];
-        if (lane == 0) {
-            rec[D] = M;
-            rec[D + 1] = L;
+            for (int j = 0; j < CPL; j++) rec[lane + 32 * j] = acc[j];
+            if (lane == 0) {
+                rec[D] = M;
+                rec[D + 1] = L;
+            }
         }
     }
     // publish: the records are visible GPU-wide before the units' counts move
@@ -798,7 +829,8 @@ __global__ void __launch_bounds__(AF_WPB * 32, 1) attn_affine_kernel(AttnArgs a,
         const int u = t < n_units ? u_first + t : ru0 + (t - n_units);
         int np, nr;
         unit_records(a, u, G, np, nr);
-        const bool last = atomic_add_acq_rel_gpu(a.counters + u, 1) + 1 == np + nr;
+        const bool last = in_buf(a.counters + u, 4, a.counters, a.sz_counters, a.status) &&
+                          atomic_add_acq_rel_gpu(a.counters + u, 1) + 1 == np + nr;
         S.done_u[t] = last ? u : -1;
     }
     __syncthreads();
@@ -811,7 +843,8 @@ __global__ void __launch_bounds__(AF_WPB * 32, 1) attn_affine_kernel(AttnArgs a,
             int np, nr;
             unit_records(a, u, G, np, nr);
             finish_head<D>(a, sh, u, warp & 3, np, nr);
-            if (lane == 0 && (warp & 3) == 0) a.counters[u] = 0;  // every record of this call has arrived
+            if (lane == 0 && (warp & 3) == 0 && in_buf(a.counters + u, 4, a.counters, a.sz_counters, a.status))
+                a.counters[u] = 0;  // every record of this call has arrived
         }
         ++k;
     }

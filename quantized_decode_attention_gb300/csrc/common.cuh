@@ -186,6 +186,26 @@ __device__ __forceinline__ float ex2(float x) {
     return y;
 }
 
+// ---- checked build -------------------------------------------------------------
+// With DQ_CHECKED defined (the library's bounds-checked build), an access on the
+// affine path first tests that its byte range [p, p + bytes) lies inside its
+// buffer [base, base + size); one that does not latches ST_OOB and is skipped
+// (no trap: the kernel runs on and the host reads the status).  Without it the
+// test is a constant true and compiles away.
+__device__ __forceinline__ bool in_buf(const void *p, long long bytes, const void *base, long long size,
+                                       unsigned *status) {
+#ifdef DQ_CHECKED
+    const char *a = static_cast<const char *>(p), *b = static_cast<const char *>(base);
+    if (b == nullptr || a < b || bytes < 0 || a + bytes > b + size) {
+        atomicOr(status, 32u);  // ST_OOB
+        return false;
+    }
+#else
+    (void)p; (void)bytes; (void)base; (void)size; (void)status;
+#endif
+    return true;
+}
+
 // Fetch-and-add with acquire-release semantics at GPU scope: writes made
 // before it (by the caller, or by its block before a barrier the caller
 // passed) are visible to whoever observes the new count, and writes released

@@ -565,6 +565,11 @@ static void fill_quant_args(const dq_config *cfg, const Layout &L, const dq_kv_b
     a.T = which == 0 && t.rot == DQ_ROT_DENSE ? static_cast<const float *>(bufs->k_transform) : nullptr;
     a.raw = static_cast<uint16_t *>(which == 0 ? bufs->raw_k : bufs->raw_v);
     a.status = status;
+    a.sz_x = static_cast<long long>(L.U) * n_tok * L.d * (cfg->kv_dtype == DQ_F32 ? 4 : 2);
+    a.sz_codes = static_cast<long long>(L.sz[which == 0 ? 0 : 1]);
+    a.sz_meta = static_cast<long long>(L.sz[which == 0 ? 2 : 3]);
+    a.sz_mean = which == 0 ? static_cast<long long>(L.sz[4]) : 0;
+    a.sz_raw = static_cast<long long>(L.sz[which == 0 ? 7 : 8]);
 }
 
 // Arguments of an affine or non-uniform decode-attention call (the dense key
@@ -606,6 +611,9 @@ static dq_status fill_attn_args(const dq_config *cfg, const Layout &L, const dq_
     a.partials = c->partials;
     a.counters = c->counters;
     a.status = c->status;
+    dq::attn_extents(L, cfg->out_dtype, a);
+    a.sz_partials = static_cast<long long>(c->partials_cap) * 4;
+    a.sz_counters = static_cast<long long>(L.U) * 4;
     if (c->counters_dirty) {
         if (cudaMemsetAsync(c->counters, 0, sizeof(int) * L.U, static_cast<cudaStream_t>(stream)) != cudaSuccess)
             return fail(DQ_ECUDA, "clearing the record counts failed");
@@ -828,6 +836,11 @@ dq_status dq_dequantize_kv(dq_ctx **ctx, const dq_config *cfg, const dq_kv_buffe
     a.slot0 = slot0;
     a.n = n;
     a.out = out;
+    a.sz_codes = static_cast<long long>(L.sz[which == 0 ? 0 : 1]);
+    a.sz_meta = static_cast<long long>(L.sz[which == 0 ? 2 : 3]);
+    a.sz_mean = which == 0 ? static_cast<long long>(L.sz[4]) : 0;
+    a.sz_out = static_cast<long long>(L.U) * n * L.d * 4;
+    a.status = (*ctx)->status;
     const int e = dq::launch_dequant(L, a, stream);
     if (e != 0) return fail(DQ_ECUDA, "dequantize launch: %s", cudaGetErrorString(static_cast<cudaError_t>(e)));
     return ok();
@@ -847,6 +860,7 @@ dq_status dq_check(dq_ctx *ctx, void *stream) {
         ctx->counters_dirty = 1;
         return fail(DQ_ETIMEOUT, "a bounded device wait ran out");
     }
+    if (st & dq::ST_OOB) return fail(DQ_EINVAL, "an access fell outside its buffer and was skipped (checked build)");
     if (st & dq::ST_INFEASIBLE) return fail(DQ_EINFEASIBLE, "a stream did not fit its container");
     if (st & dq::ST_SIDE_FULL)
         return fail(DQ_EINFEASIBLE, "the key outlier side channel is full: later decode-key outliers keep their level");
@@ -861,6 +875,13 @@ dq_status dq_test_expire_wait(dq_ctx *ctx, unsigned long long limit_ns, void *st
     if (limit_ns > 1000000000ULL) limit_ns = 1000000000ULL;
     const int e = dq::launch_expire_wait(ctx->status, ctx->counters, limit_ns, stream);
     if (e != 0) return fail(DQ_ECUDA, "expire-wait launch: %s", cudaGetErrorString(static_cast<cudaError_t>(e)));
+    return ok();
+}
+
+dq_status dq_test_checked_probe(dq_ctx *ctx, void *stream) {
+    if (!ctx || !ctx->status) return fail(DQ_EINVAL, "ctx has no workspace yet");
+    const int e = dq::launch_checked_probe(ctx->status, stream);
+    if (e != 0) return fail(DQ_ECUDA, "probe launch: %s", cudaGetErrorString(static_cast<cudaError_t>(e)));
     return ok();
 }
 

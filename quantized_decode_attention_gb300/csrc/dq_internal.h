@@ -9,7 +9,8 @@
 namespace dq {
 
 // Status bits latched on the device (ctx->status word).
-enum : unsigned { ST_NONFINITE = 1u, ST_TIMEOUT = 2u, ST_BOUNDS = 4u, ST_INFEASIBLE = 8u, ST_SIDE_FULL = 16u };
+enum : unsigned { ST_NONFINITE = 1u, ST_TIMEOUT = 2u, ST_BOUNDS = 4u, ST_INFEASIBLE = 8u, ST_SIDE_FULL = 16u,
+                  ST_OOB = 32u };  // ST_OOB: a checked build skipped an access outside its buffer
 
 // Sizes and strides derived from a config (all in bytes unless noted).
 struct Layout {
@@ -153,6 +154,8 @@ struct QuantArgs {
     float *thr;             // keys: [U][d] outlier thresholds frozen at prefill (fp32 magnitudes)
     long long slot_lo;      // first quantized slot written by this call
     int n_slots;            // quantized slots written by this call
+    // byte sizes of the buffers above (the checked build tests accesses against them)
+    long long sz_x, sz_codes, sz_meta, sz_mean, sz_raw;
 };
 
 // The geometry a token row's quantizer needs (a slice of Layout).
@@ -214,7 +217,26 @@ struct AttnArgs {
     int append;
     QuantArgs qa[2];
     RowGeom rg;
+    // byte sizes of the buffers above (the checked build tests accesses against them)
+    long long sz_q, sz_out, sz_codes_k, sz_codes_v, sz_meta_k, sz_meta_v, sz_mean_k, sz_raw_k, sz_raw_v, sz_q_comp;
+    long long sz_partials, sz_counters;
 };
+
+// Byte sizes of the attention call's buffers other than its workspace (the
+// checked build tests accesses against them).
+inline void attn_extents(const Layout &L, int out_dtype, AttnArgs &a) {
+    const long long qo = static_cast<long long>(L.B) * L.Hq * L.d;
+    a.sz_q = qo * 4;
+    a.sz_out = qo * (out_dtype == DQ_F32 ? 4 : 2);
+    a.sz_codes_k = static_cast<long long>(L.sz[0]);
+    a.sz_codes_v = static_cast<long long>(L.sz[1]);
+    a.sz_meta_k = static_cast<long long>(L.sz[2]);
+    a.sz_meta_v = static_cast<long long>(L.sz[3]);
+    a.sz_mean_k = static_cast<long long>(L.sz[4]);
+    a.sz_raw_k = static_cast<long long>(L.sz[7]);
+    a.sz_raw_v = static_cast<long long>(L.sz[8]);
+    a.sz_q_comp = static_cast<long long>(L.sz[16]);
+}
 
 struct DequantArgs {
     const uint8_t *codes;
@@ -223,6 +245,8 @@ struct DequantArgs {
     int is_key, bits, meta_f16;
     long long slot0, n;
     float *out;
+    long long sz_codes, sz_meta, sz_mean, sz_out;  // byte sizes (checked build)
+    unsigned *status;                               // checked build: ST_OOB
 };
 
 struct AttnArgs;
@@ -245,6 +269,8 @@ int launch_attention(const Layout &L, const AttnArgs &a, int num_sms, void *stre
 int launch_qcomp(const Layout &L, const float *q, const float *qc, float *qt, void *stream);
 // test support: a kernel whose bounded wait runs out (see dq_test_expire_wait)
 int launch_expire_wait(unsigned *status, int *counters, unsigned long long limit_ns, void *stream);
+// test support: one range test that fails in the checked build (see dq_test_checked_probe)
+int launch_checked_probe(unsigned *status, void *stream);
 // Fill the work schedule of `a` (items, grid, partial slots) for a launch on a
 // device with num_sms SMs whose partial workspace holds cap_floats floats.
 int plan_attention(const Layout &L, AttnArgs &a, int num_sms, long long cap_floats);

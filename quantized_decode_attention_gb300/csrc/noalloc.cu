@@ -123,6 +123,9 @@ extern "C" dq_status dq_decode_attention_noalloc(const dq_config *cfg, const dq_
     a.hscale = static_cast<float>(1.0 / std::sqrt(static_cast<double>(L.d)));
     a.counters = reinterpret_cast<int *>(scratch);
     a.status = reinterpret_cast<unsigned *>(scratch + kStatusOffset);
+    dq::attn_extents(L, cfg->out_dtype, a);
+    a.sz_partials = static_cast<long long>(kPartialsBytes);
+    a.sz_counters = static_cast<long long>(kCountersBytes);
     dq::set_nuq_args(L, bufs, a);
     a.partials = reinterpret_cast<float *>(scratch + kPartialsOffset);
     // the partials must fit the static scratch: the plan narrows the grid

@@ -42,9 +42,11 @@ __global__ void key_mean_kernel(QuantArgs a, int Hkv, long long t0, long long t1
         const int n = static_cast<int>(t1 - c0 < CH ? t1 - c0 : CH);
         for (int r = warp; r < n; r += nw) {
             const long long base = (static_cast<long long>(u) * a.n_tok + (c0 + r - a.pos0)) * D;
+            const long long esz = a.in_dtype == 0 ? 4 : 2;
+            const bool okx = in_buf(static_cast<const char *>(a.x) + base * esz, D * esz, a.x, a.sz_x, a.status);
             float x[V];
 #pragma unroll
-            for (int j = 0; j < V; j++) x[j] = ld_in(a.x, base + lane * V + j, a.in_dtype);
+            for (int j = 0; j < V; j++) x[j] = okx ? ld_in(a.x, base + lane * V + j, a.in_dtype) : 0.f;
             rotate_row<V>(x, a.rot, a.hscale, T, xs[warp]);
 #pragma unroll
             for (int j = 0; j < V; j++) ys[r][lane * V + j] = x[j];
@@ -54,7 +56,8 @@ __global__ void key_mean_kernel(QuantArgs a, int Hkv, long long t0, long long t1
         __syncthreads();
     }
     const long long cnt = t1 - t0;
-    a.mean[static_cast<long long>(u) * D + threadIdx.x] = cnt > 0 ? __fdiv_rn(acc, static_cast<float>(cnt)) : 0.0f;
+    float *mp = a.mean + static_cast<long long>(u) * D + threadIdx.x;
+    if (in_buf(mp, 4, a.mean, a.sz_mean, a.status)) *mp = cnt > 0 ? __fdiv_rn(acc, static_cast<float>(cnt)) : 0.0f;
 }
 
 // ---------------------------------------------------------------------------
@@ -94,6 +97,8 @@ __global__ void dequant_kernel(DequantArgs a, Layout L) {
     const int u = static_cast<int>(gw / a.n);
     const long long i = gw % a.n, slot = a.slot0 + i;
     const long long ms = static_cast<long long>(u) * L.qcap + slot;
+    const long long mbytes = a.meta_f16 ? 4 : 8;
+    if (!in_buf(static_cast<const char *>(a.meta) + ms * mbytes, mbytes, a.meta, a.sz_meta, a.status)) return;
     float s, o;
     if (a.meta_f16) {
         const uint32_t so = reinterpret_cast<const uint32_t *>(a.meta)[ms];
@@ -112,6 +117,9 @@ __global__ void dequant_kernel(DequantArgs a, Layout L) {
         rec = reinterpret_cast<const uint32_t *>(a.codes + (static_cast<long long>(u) * (L.qcap / 2) + slot / 2) * L.pairV);
         half = static_cast<int>(slot & 1);
     }
+    if (!in_buf(rec, a.is_key ? L.rowK : L.pairV, a.codes, a.sz_codes, a.status)) return;
+    if (a.mean && !in_buf(a.mean + static_cast<long long>(u) * D, D * 4, a.mean, a.sz_mean, a.status)) return;
+    if (!in_buf(a.out + (static_cast<long long>(u) * a.n + i) * D, D * 4, a.out, a.sz_out, a.status)) return;
 #pragma unroll
     for (int j = 0; j < V; j++) {
         const int c = lane * V + j;

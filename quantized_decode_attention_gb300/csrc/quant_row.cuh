@@ -56,11 +56,14 @@ __device__ __forceinline__ void load_row(const QuantArgs &a, int u, long long i,
     constexpr int D = 32 * V;
     const int lane = threadIdx.x & 31;
     const long long base = (static_cast<long long>(u) * a.n_tok + i) * D;
+    const long long esz = a.in_dtype == 0 ? 4 : 2;
+    const bool okx = in_buf(static_cast<const char *>(a.x) + base * esz, D * esz, a.x, a.sz_x, a.status);
+    const bool okm = a.use_mean && in_buf(a.mean + static_cast<long long>(u) * D, D * 4, a.mean, a.sz_mean, a.status);
 #pragma unroll
     for (int j = 0; j < V; j++) {
-        in.x[j] = ld_in(a.x, base + lane * V + j, a.in_dtype);
-        in.r[j] = raw16_of(a.x, base + lane * V + j, a.in_dtype);
-        in.mu[j] = a.use_mean ? a.mean[static_cast<long long>(u) * D + lane * V + j] : 0.f;
+        in.x[j] = okx ? ld_in(a.x, base + lane * V + j, a.in_dtype) : 0.f;
+        in.r[j] = okx ? raw16_of(a.x, base + lane * V + j, a.in_dtype) : 0;
+        in.mu[j] = okm ? a.mean[static_cast<long long>(u) * D + lane * V + j] : 0.f;
     }
 }
 
@@ -99,7 +102,7 @@ __device__ __forceinline__ void quantize_loaded_row(const QuantArgs &a, const Ro
             const int c = lane * V + j;
             long long off = a.is_key ? static_cast<long long>(raw_slot) * D + c
                                      : (static_cast<long long>(raw_slot >> 1) * D + c) * 2 + (raw_slot & 1);
-            a.raw[ub + off] = in.r[j];
+            if (in_buf(a.raw + ub + off, 2, a.raw, a.sz_raw, a.status)) a.raw[ub + off] = in.r[j];
         }
     }
     if (t < L.n_sink) return;
@@ -196,9 +199,11 @@ __device__ __forceinline__ void quantize_loaded_row(const QuantArgs &a, const Ro
     if (lane == 0) {
         if (a.meta_f16) {
             const uint32_t so = pack2(__half_as_ushort(__float2half_rn(s)), __half_as_ushort(__float2half_rn(o)));
-            reinterpret_cast<uint32_t *>(a.meta)[ms] = so;
+            uint32_t *mp = reinterpret_cast<uint32_t *>(a.meta) + ms;
+            if (in_buf(mp, 4, a.meta, a.sz_meta, a.status)) *mp = so;
         } else {
-            reinterpret_cast<float2 *>(a.meta)[ms] = make_float2(s, o);
+            float2 *mp = reinterpret_cast<float2 *>(a.meta) + ms;
+            if (in_buf(mp, 8, a.meta, a.sz_meta, a.status)) *mp = make_float2(s, o);
         }
     }
 
@@ -216,7 +221,7 @@ __device__ __forceinline__ void quantize_loaded_row(const QuantArgs &a, const Ro
                 v |= contrib<D, BITS>(w, k_idx(c, D), c & 1, m[j], WLO);
             }
             v = __reduce_or_sync(FULL, v);
-            if (lane == w) row[w] = v;
+            if (lane == w && in_buf(row + w, 4, a.codes, a.sz_codes, a.status)) row[w] = v;
         }
     } else {
         const int e = static_cast<int>(slot & 1);
@@ -232,7 +237,8 @@ __device__ __forceinline__ void quantize_loaded_row(const QuantArgs &a, const Ro
                 v |= contrib<D, BITS>(w, v_idx(c, D), e, m[j], WLO);
             }
             v = __reduce_or_sync(FULL, v);
-            if (lane == (w & 31)) rec[2 * w + e] = static_cast<uint16_t>(v >> (16 * e));
+            if (lane == (w & 31) && in_buf(rec + 2 * w + e, 2, a.codes, a.sz_codes, a.status))
+                rec[2 * w + e] = static_cast<uint16_t>(v >> (16 * e));
         }
     }
 }
