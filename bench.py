@@ -988,6 +988,40 @@ def grid_ablation(batch: int = 2, seq: int = 2048) -> dict:
     return {"rows": out, "workload": f"batch {batch}, {seq} tokens, 8 KV heads, d 128; fp16 s and o"}
 
 
+def drift_statistics(batch: int = 2, seq: int = 1024) -> dict:
+    """D-Quant App. C ("drift makes only sparse, local corrections"): the share
+    of coded symbols that drift moved off the nearest level of their stream's
+    final grid, and the largest move, counted by the library while it encodes
+    the D-Quant-shaped synthetic cache (8 / 6 levels in 331 / 231 bytes and at
+    1.96 bits per value)."""
+    import torch
+    from quantized_decode_attention_gb300 import KVCache, make_config
+    rows = []
+    for D in (W.DQUANT, W.DQUANT_196):
+        w = D.with_(batch=batch, seq=seq)
+        e = w.extra
+        k, v = W.make_kv(w)
+        dev16 = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).cuda().view(torch.bfloat16)
+        cfg = make_config(batch=w.batch, n_kv_heads=w.n_kv_heads, n_q_heads=w.n_q_heads, head_dim=w.head_dim,
+                          max_seq=seq, kv_dtype=w.kv_dtype, out_dtype=w.out_dtype, rot_k=w.rot_k, rot_v=w.rot_v,
+                          mean_k=w.mean_k, n_sink=w.n_sink, n_recent=w.n_recent, scheme="rans",
+                          levels_k=e["levels_k"], levels_v=e["levels_v"], container_k=e["container_k"],
+                          container_v=e["container_v"], rans_alpha=e["alpha"])
+        cache = KVCache.allocate(cfg)
+        try:
+            cache.quantize(dev16(k), dev16(v), pos0=0)
+            st = cache.drift_stats()
+            cache.check()
+        finally:
+            cache.close()
+        rows.append({"config": f"k{e['levels_k']}x{e['container_k']}-v{e['levels_v']}x{e['container_v']}",
+                     "k_changed_frac": round(st["k_changed"] / max(1, st["k_coded"]), 5),
+                     "k_max_move": st["k_max_move"],
+                     "v_changed_frac": round(st["v_changed"] / max(1, st["v_coded"]), 5),
+                     "v_max_move": st["v_max_move"], "symbols": st["k_coded"] + st["v_coded"]})
+    return {"rows": rows, "workload": f"batch {batch}, {seq} tokens, 8 KV heads, d 128 (synthetic)"}
+
+
 def cpu_baseline(w, bits, S, budget_s, k, v, q):
     """The oracle as it stands, timed on this host's cores, one worker process
     per core, a unit (sequence, KV head) per worker at a time: per unit the bulk
@@ -1222,6 +1256,14 @@ def main():
         gab["note"] = ("relative squared reconstruction error of K and V on the Hadamard rotation: min/max grid, "
                        "percentile clip (kappa 0.96 keys / 0.92 values), QuEST grid (s = c_b RMS)")
         line["diagnostics"]["grid_ablation"] = gab
+        if not args.no_dquant:
+            try:
+                dst = drift_statistics()
+            except Exception as e:  # a diagnostic never costs the measurement line
+                dst = {"error": f"{type(e).__name__}: {e}"}
+            dst["note"] = ("symbols moved by drift off the nearest level of their final grid, counted by the library "
+                           "while encoding (the page measures 0.75 % of keys and 5.00 % of values on real caches)")
+            line["diagnostics"]["drift"] = dst
     if rank == 0:
         print(json.dumps(line))
     if world > 1:

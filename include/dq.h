@@ -358,6 +358,19 @@ dq_status dq_test_expire_wait(dq_ctx *ctx, unsigned long long limit_ns, void *st
 dq_status dq_test_checked_probe(dq_ctx *ctx, void *stream);
 
 /*
+ * Drift statistics of the entropy-coded scheme ("D-Quant", App. C: drift makes
+ * only sparse, local corrections).  Accumulated by every prefill and flush on
+ * this context since it was created or last read, per tensor: the coded
+ * symbols that drift moved off the nearest level of their stream's final
+ * fp16 grid o + s m (nearest by |x - (o + s m)| in fp32, ties to the lower
+ * level), the symbols coded, and the largest such move in levels.
+ * Synchronizes `stream`, writes out[6] = {keys: changed, coded, largest move;
+ * values: the same} and clears the counts.
+ * Errors: DQ_EINVAL (NULL, or a context of another scheme), DQ_ECUDA.
+ */
+dq_status dq_drift_stats(dq_ctx *ctx, void *stream, unsigned long long out[6]);
+
+/*
  * Allocation-free decode attention (this library's own addition; the pages
  * have no counterpart).  Computes exactly what dq_decode_attention computes,
  * with the same arguments minus the context, but never calls cudaMalloc,

@@ -259,7 +259,8 @@ class DqTensor:
     symbols (n = Hkv * d, head-major); flags [B, Sq] (1 = over budget, 2 =
     container overflow); keys also carry the windowed mean: mean_q [B, Wn, n]
     int8, mean_sc [B, Wn] fp16 bits, mu_hat [B, Wn, n] fp32 (window = 128
-    quantized slots)."""
+    quantized slots); x [B, Sq, n] fp32 holds the coded stream values (rotated,
+    keys less their window mean)."""
     container: np.ndarray
     s16: np.ndarray
     o16: np.ndarray
@@ -268,6 +269,7 @@ class DqTensor:
     mean_q: np.ndarray | None = None
     mean_sc: np.ndarray | None = None
     mu_hat: np.ndarray | None = None
+    x: np.ndarray | None = None
 
 
 def dq_tables(w: W.Workload):
@@ -309,7 +311,7 @@ def quantize_dquant(w: W.Workload, x_bits: np.ndarray, is_key: bool, S: int) -> 
         streams = (streams - mu_hat[:, widx]).astype(np.float32)   # fp32 subtraction
     cont, s16, o16, m, flags = dq_encode_streams(streams.reshape(B * nq, n), tab, C_bytes)
     return DqTensor(cont.reshape(B, nq, C_bytes), s16.reshape(B, nq), o16.reshape(B, nq), m.reshape(B, nq, n),
-                    flags.reshape(B, nq), mean_q, mean_sc, mu_hat)
+                    flags.reshape(B, nq), mean_q, mean_sc, mu_hat, streams)
 
 
 def dquant_dequant_f64(w: W.Workload, dt: DqTensor, is_key: bool) -> np.ndarray:

@@ -93,6 +93,7 @@ def load() -> C.CDLL:
     L.dq_check.argtypes = [P, P]
     L.dq_test_expire_wait.argtypes = [P, C.c_ulonglong, P]
     L.dq_test_checked_probe.argtypes = [P, P]
+    L.dq_drift_stats.argtypes = [P, P, C.POINTER(C.c_ulonglong)]
     L.dq_free.argtypes = [P]
     L.dq_free.restype = None
     L.dq_last_error.restype = C.c_char_p
@@ -104,7 +105,7 @@ def load() -> C.CDLL:
     L.dq_quest_step.argtypes = [C.c_int, C.POINTER(C.c_float)]
     for f in ("dq_kv_sizes", "dq_quantize_kv", "dq_decode_attention", "dq_decode_step", "dq_dequantize_kv", "dq_check",
               "dq_test_expire_wait", "dq_test_checked_probe", "dq_rans_model", "dq_symbol_probs",
-              "dq_quest_step"):
+              "dq_quest_step", "dq_drift_stats"):
         getattr(L, f).restype = C.c_int
     _lib = L
     return L
@@ -262,6 +263,13 @@ class KVCache:
     def detach(self):
         """Forget a borrowed context without freeing it."""
         self.ctx = C.c_void_p()
+
+    def drift_stats(self, stream=None) -> dict:
+        """Entropy-coded caches: drift statistics since the last read (and clear)."""
+        out = (C.c_ulonglong * 6)()
+        _raise(load().dq_drift_stats(self.ctx, _stream(stream), out))
+        return {"k_changed": out[0], "k_coded": out[1], "k_max_move": out[2],
+                "v_changed": out[3], "v_coded": out[4], "v_max_move": out[5]}
 
     def check(self, stream=None):
         _raise(load().dq_check(self.ctx, _stream(stream)))

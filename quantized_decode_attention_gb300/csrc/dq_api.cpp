@@ -336,7 +336,9 @@ static dq_status get_ctx(dq_ctx **pctx, const dq_config *cfg, const Layout &L) {
     if (e4 == cudaSuccess && cfg->k.rot == DQ_ROT_DENSE)
         e4 = cudaMalloc(&c->q_tilde, sizeof(float) * static_cast<size_t>(L.B) * L.Hq * L.d);
     if (L.scheme == DQ_RANS) {
-        e4 = cudaMalloc(&c->rans, sizeof(dq::RansDevTables));
+        e4 = cudaMalloc(&c->drift_stats, 6 * sizeof(unsigned long long));
+        if (e4 == cudaSuccess) e4 = cudaMemset(c->drift_stats, 0, 6 * sizeof(unsigned long long));
+        if (e4 == cudaSuccess) e4 = cudaMalloc(&c->rans, sizeof(dq::RansDevTables));
         if (e4 == cudaSuccess)
             e4 = cudaMalloc(&c->rans_partials,
                             sizeof(float) * static_cast<size_t>(dq::rans_partial_floats(L.B, L.Hq, L.qcap)));
@@ -515,6 +517,7 @@ static dq_status quantize_rans(dq_ctx *c, const dq_config *cfg, const Layout &L,
         a.codes = static_cast<uint8_t *>(which == 0 ? bufs->codes_k : bufs->codes_v);
         a.meta = which == 0 ? bufs->meta_k : bufs->meta_v;
         a.mean = which == 0 && t.mean ? static_cast<uint8_t *>(bufs->mean_k) : nullptr;
+        a.drift_stats = c->drift_stats + 3 * which;
         const dq::RansTable *tb = which == 0 ? &c->rans->k : &c->rans->v;
         if (a.mean && (e = dq::launch_rans_mean(a, stream)) != 0)
             return fail(DQ_ECUDA, "window mean launch: %s", cudaGetErrorString(static_cast<cudaError_t>(e)));
@@ -878,6 +881,17 @@ dq_status dq_test_expire_wait(dq_ctx *ctx, unsigned long long limit_ns, void *st
     return ok();
 }
 
+dq_status dq_drift_stats(dq_ctx *ctx, void *stream, unsigned long long out[6]) {
+    if (!ctx || !out) return fail(DQ_EINVAL, "NULL argument");
+    if (!ctx->drift_stats) return fail(DQ_EINVAL, "drift statistics belong to the entropy-coded scheme");
+    cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return fail(DQ_ECUDA, "stream: %s", cudaGetErrorString(e));
+    if (cudaMemcpy(out, ctx->drift_stats, 6 * sizeof(unsigned long long), cudaMemcpyDeviceToHost) != cudaSuccess ||
+        cudaMemset(ctx->drift_stats, 0, 6 * sizeof(unsigned long long)) != cudaSuccess)
+        return fail(DQ_ECUDA, "drift statistics read failed");
+    return ok();
+}
+
 dq_status dq_test_checked_probe(dq_ctx *ctx, void *stream) {
     if (!ctx || !ctx->status) return fail(DQ_EINVAL, "ctx has no workspace yet");
     const int e = dq::launch_checked_probe(ctx->status, stream);
@@ -892,6 +906,7 @@ void dq_free(dq_ctx *ctx) {
     cudaFree(ctx->counters);
     cudaFree(ctx->nuq_bits);
     cudaFree(ctx->rans);
+    cudaFree(ctx->drift_stats);
     cudaFree(ctx->rans_sym);
     cudaFree(ctx->rans_partials);
     cudaFree(ctx->q_tilde);

@@ -88,6 +88,9 @@ struct RansQuantArgs {
     long long pos0, slot0;
     int raw_bf16;
     int raw_ns, raw_nr;     // this call's tokens copied as sinks / into the recent ring
+    // drift statistics, accumulated: symbols off the nearest level of their
+    // final grid, symbols coded, largest distance (or nullptr)
+    unsigned long long *drift_stats;
 };
 int launch_rans_mean(const RansQuantArgs &a, void *stream);
 int launch_rans_drift(const RansQuantArgs &a, const RansTable *tb, const float *F, int M, void *stream);
@@ -302,5 +305,6 @@ struct dq_ctx {
     uint8_t *rans_sym;   // entropy-coded scheme: symbol scratch of a prefill
     float *rans_partials;  // entropy-coded scheme: attention item records
     float *q_tilde;      // dense key transform: compensated queries [B][Hq][d]
+    unsigned long long *drift_stats;  // entropy-coded scheme: [keys, values][changed, coded, largest move]
     size_t rans_sym_cap; // bytes
 };

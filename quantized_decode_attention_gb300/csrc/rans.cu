@@ -211,6 +211,7 @@ enum { PASS_COST = 0, PASS_REFIT = 1, PASS_STORE = 2 };
 
 struct RefitSums {
     long long Sm, Smm;
+    int changed = 0, move = 0;  // PASS_STORE: symbols off the nearest level, the largest distance
 };
 
 // One assignment argmin_m fp32(D_im + fp32(lambda r_m)) (ties to the lower m)
@@ -253,6 +254,22 @@ __device__ __forceinline__ long long assign_at(const float *xs, const float (&g)
             }
             cost += tb.r[best];
             word |= static_cast<uint32_t>(best) << (8 * j);
+            if (PASS == PASS_STORE) {  // drift statistics: against the nearest level of the grid
+                float bn = fabsf(__fsub_rn(xv[j], g[0]));
+                int near = 0;
+#pragma unroll
+                for (int m = 1; m < MMAX; m++) {
+                    if (m < M) {
+                        const float dn = fabsf(__fsub_rn(xv[j], g[m]));
+                        if (dn < bn) {
+                            bn = dn;
+                            near = m;
+                        }
+                    }
+                }
+                rs.changed += best != near;
+                rs.move = max(rs.move, abs(best - near));
+            }
             if (PASS == PASS_REFIT) {
                 rs.Sm += best;
                 rs.Smm += best * best;
@@ -399,8 +416,22 @@ __global__ void __launch_bounds__(128) rans_drift_kernel(RansQuantArgs a, const 
     }
     const __half s16 = __float2half_rn(s), o16 = __float2half_rn(o);
     uint32_t *sym = reinterpret_cast<uint32_t *>(a.sym + gw * N);
+    rs.changed = rs.move = 0;
     const bool ok = drift<H, MMAX, PASS_STORE>(xs, __half2float(s16), __half2float(o16), tb, F, M, mx, rs, sym);
     if (!ok && lane == 0) atomicOr(a.status, ST_INFEASIBLE);
+    if (a.drift_stats) {  // symbols drift moved off the nearest level of the final grid, and how far
+        int ch = rs.changed, mv = rs.move;
+#pragma unroll
+        for (int o2 = 16; o2; o2 >>= 1) {
+            ch += __shfl_xor_sync(FULL, ch, o2);
+            mv = max(mv, __shfl_xor_sync(FULL, mv, o2));
+        }
+        if (lane == 0) {
+            atomicAdd(a.drift_stats, static_cast<unsigned long long>(ch));
+            atomicAdd(a.drift_stats + 1, static_cast<unsigned long long>(N));
+            atomicMax(a.drift_stats + 2, static_cast<unsigned long long>(mv));
+        }
+    }
     if (lane == 0) {
         __half2 *meta = reinterpret_cast<__half2 *>(a.meta);
         meta[static_cast<long long>(b) * a.qcap + slot] = __halves2half2(s16, o16);
