@@ -34,7 +34,14 @@ sys.path.insert(0, ROOT)
 import workloads as W  # noqa: E402
 
 METRIC = "quantized decode-attn tokens/s & achieved HBM GB/s (% of roofline), 2/3/4-bit"
-ATTN_SRC = os.path.join(ROOT, "quantized_decode_attention_gb300", "csrc", "attn.cu")
+CSRC = os.path.join(ROOT, "quantized_decode_attention_gb300", "csrc")
+# the sources each attention kernel is compiled from (the traffic record is
+# valid only for the exact sources it was captured with)
+KERNEL_SRCS = {
+    "affine": ["attn_affine.cu", "attn_common.cuh", "common.cuh", "quant_row.cuh"],
+    "generic": ["attn.cu", "attn_common.cuh", "common.cuh"],
+    "rans": ["attn_rans.cu", "common.cuh"],
+}
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "attn_traffic.json")
 
 
@@ -54,7 +61,10 @@ def parse():
     p.add_argument("--qwen", default="32768,131072", help="Qwen3-8B-shaped long-context lengths measured")
     p.add_argument("--no-bf16", action="store_true", help="skip the unquantized 16-bit cache context entry")
     p.add_argument("--profile-attn", action="store_true",
-                   help="profiler run: one Llama-shaped cache at --bits, warmup + steps attention calls, no timing")
+                   help="profiler run: one cache, warmup + steps attention calls, no timing")
+    p.add_argument("--profile-kind", default="affine", choices=["affine", "nuq", "dquant"],
+                   help="--profile-attn cache: the Llama-shaped affine cache at --bits, the KVQuant NUQ cache, or "
+                        "the D-Quant cache at a reduced batch")
     return p.parse_args()
 
 
@@ -268,19 +278,18 @@ class Clocks:
                 "reasons": reasons, "samples": len(smp), "window": how, "source": self.source}
 
 
-RANS_SRC = os.path.join(ROOT, "quantized_decode_attention_gb300", "csrc", "attn_rans.cu")
+def kernel_sha(kind: str) -> str:
+    h = hashlib.sha256()
+    for f in KERNEL_SRCS[kind]:
+        h.update(open(os.path.join(CSRC, f), "rb").read())
+    return h.hexdigest()[:16]
 
 
-def src_sha(path: str) -> str:
-    return hashlib.sha256(open(path, "rb").read()).hexdigest()[:16]
-
-
-def traffic_for(kernel_sha: str, bits):
+def traffic_for(kind: str, bits):
     """DRAM bytes per attention launch from the committed ncu capture, or None
-    when the kernel source differs from the one captured."""
+    when the kernel's sources differ from the ones captured."""
     key = bits if isinstance(bits, str) else f"{bits}bit"
-    if key.startswith("dquant"):
-        kernel_sha = src_sha(RANS_SRC)
+    kernel_sha = globals()["kernel_sha"](kind)
     try:
         with open(TRAFFIC_FILE) as f:
             d = json.load(f)
@@ -463,7 +472,7 @@ def run_gpu(args, w, bits, S, k_dev, v_dev, q_dev, knew_dev, vnew_dev, rank):
     res = {
         "total_ms": total_ms, "attn_ms": attn_graph_ms, "attn_ms_eager": statistics.mean(attn_ms),
         "attn_ms_eager_median": statistics.median(attn_ms), "attn_calls": reps * ng,
-        "clocks": step_clocks, "attn_clocks": attn_clocks, "copies": nc, "algo": ab,
+        "clocks": step_clocks, "attn_clocks": attn_clocks, "copies": nc, "algo": ab, "kernel": "affine",
         "attn_timing": "CUDA graph of back-to-back calls over the cache copies, events around the replays",
         "e2e_tok_s": w.batch * n_e2e / (e2e_ms / 1e3), "h2d": bytes_h2d, "d2h": bytes_d2h,
         "prefill_ms": prefill_ms, "token_ms": statistics.mean(token_ms),
@@ -576,6 +585,7 @@ def run_gpu_nuq(args, w):
     res = {"total_ms": total_ms, "steps": steps, "attn_ms": total_ms / steps, "attn_ms_eager": statistics.mean(attn_ms),
            "attn_ms_eager_median": statistics.median(attn_ms), "attn_calls": steps,
            "attn_timing": "CUDA graph of back-to-back calls over the cache copies", "algo": ab, "copies": nc,
+           "kernel": "generic",
            "prefill_ms": prefill_ms, "e2e_tok_s": w.batch * n_attn / (e2e_ms / 1e3)}
     for c in caches[1:]:
         c.detach()
@@ -658,6 +668,7 @@ def run_gpu_dquant(args, w):
     res = {"total_ms": total_ms, "steps": steps, "attn_ms": statistics.mean(attn_ms),
            "attn_ms_eager": statistics.mean(attn_ms), "attn_ms_eager_median": statistics.median(attn_ms),
            "attn_calls": steps, "attn_timing": "event pair around each call (calls of milliseconds)", "algo": ab,
+           "kernel": "rans",
            "copies": nc, "prefill_ms": prefill_ms, "e2e_tok_s": w.batch * n_e2e / (e2e_ms / 1e3)}
     for c in caches[1:]:
         c.detach()
@@ -1056,27 +1067,51 @@ def cpu_baseline(w, bits, S, budget_s, k, v, q):
                       f"attention over {S} tokens for {w.group} heads; decode time extrapolated to one full call"}
 
 
+def cfg_of(w: W.Workload, max_seq: int | None = None):
+    """The library config of a workload."""
+    from quantized_decode_attention_gb300 import make_config
+    e = w.extra
+    return make_config(batch=w.batch, n_kv_heads=w.n_kv_heads, n_q_heads=w.n_q_heads, head_dim=w.head_dim,
+                       max_seq=max_seq or w.seq, kv_dtype=w.kv_dtype, meta_dtype=w.meta_dtype, out_dtype=w.out_dtype,
+                       bits=w.bits, rot_k=w.rot_k, rot_v=w.rot_v, mean_k=w.mean_k, clip_k=w.clip, clip_v=w.clip,
+                       grid_k=w.grid, n_sink=w.n_sink, n_recent=w.n_recent, scheme=w.scheme,
+                       lloyd_iters=e.get("lloyd_iters", 8), outlier_frac=e.get("outlier_frac", 0.01),
+                       levels_k=e.get("levels_k", 8), levels_v=e.get("levels_v", 6),
+                       container_k=e.get("container_k", 331), container_v=e.get("container_v", 231),
+                       rans_alpha=e.get("alpha", 1.4))
+
+
 def profile_attention(args):
-    """A short run for a profiler to capture: the Llama-shaped cache at
-    args.bits (prefilled once), then args.warmup + args.steps decode-attention
-    calls on one stream.  Nothing is timed here."""
+    """A short run for a profiler to capture: one cache (the Llama-shaped affine
+    cache at args.bits, the KVQuant NUQ cache, or the D-Quant cache at batch 4),
+    prefilled once, then args.warmup + args.steps decode-attention calls on one
+    stream.  Nothing is timed here."""
     import torch
     import __graft_entry__
+    from quantized_decode_attention_gb300 import KVCache
     __graft_entry__.build()
-    w = W.LLAMA.with_(bits=args.bits)
+    if args.profile_kind == "affine":
+        w = W.LLAMA.with_(bits=args.bits)
+    elif args.profile_kind == "nuq":
+        w = W.NUQ
+    else:
+        w = W.DQUANT.with_(batch=4)
     S = w.seq
     k, v = W.make_kv(w)
-    dev16 = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).cuda().view(torch.bfloat16)
-    k_dev, v_dev = dev16(k), dev16(v)
+    dt = torch.float16 if w.kv_dtype == "f16" else torch.bfloat16
+    dev16 = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).cuda().view(dt)
     q_dev = torch.from_numpy(W.make_q(w)).cuda()
-    caches, _ = setup_caches(w, args.bits, S, k_dev, v_dev, 1)
-    out = torch.empty((w.batch, w.n_q_heads, w.head_dim), dtype=torch.bfloat16, device="cuda")
+    cache = KVCache.allocate(cfg_of(w), zero=False)
+    cache.quantize(dev16(k), dev16(v), pos0=0)
+    odt = {"bf16": torch.bfloat16, "f16": torch.float16, "f32": torch.float32}[w.out_dtype]
+    out = torch.empty((w.batch, w.n_q_heads, w.head_dim), dtype=odt, device="cuda")
     for _ in range(args.warmup + args.steps):
-        caches[0].attention(q_dev, out, S, w.head_dim ** -0.5)
+        cache.attention(q_dev, out, S, w.head_dim ** -0.5)
     torch.cuda.synchronize()
-    caches[0].check()
-    caches[0].close()
-    print(json.dumps({"profile_attn": w.name, "bits": args.bits, "calls": args.warmup + args.steps}))
+    cache.check()
+    cache.close()
+    print(json.dumps({"profile_attn": w.name, "kind": args.profile_kind, "bits": w.bits,
+                      "calls": args.warmup + args.steps}))
 
 
 def main():
@@ -1142,6 +1177,7 @@ def main():
     if not args.no_bf16:
         wb = W.LLAMA.with_(n_sink=S, n_recent=0, mean_k=False, rot_k="none", rot_v="none")
         bf16 = run_gpu(args, wb, wb.bits, S, k_dev, v_dev, q_dev, kn_dev, vn_dev, rank)
+        bf16["kernel"] = "generic"  # every token a 16-bit slot: the older kernel's CTA-wide ring serves it
         torch.cuda.empty_cache()
     del k_dev, v_dev
     nuq = None if args.no_nuq else run_gpu_nuq(args, W.NUQ)
@@ -1150,13 +1186,11 @@ def main():
 
     ms_step, value = aggregate(res["total_ms"], args.steps, w.batch, world)
     peak, peak_kind = peaks()
-    sha = hashlib.sha256(open(ATTN_SRC, "rb").read()).hexdigest()[:16]
-
     def roof(r, bits):
         achieved = r["algo"]["total"] / (r["attn_ms"] / 1e3) / 1e9
         d = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
              "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
-             "traffic": traffic_for(sha, bits), "algorithmic_bytes": r["algo"]["total"],
+             "traffic": traffic_for(r.get("kernel", "affine"), bits), "algorithmic_bytes": r["algo"]["total"],
              "attn_us": round(r["attn_ms"] * 1e3, 2), "calls_timed": r["attn_calls"], "timing": r["attn_timing"],
              "attn_us_eager": round(r["attn_ms_eager"] * 1e3, 2),
              "attn_us_eager_median": round(r["attn_ms_eager_median"] * 1e3, 2)}
