@@ -1,4 +1,7 @@
-// Split-K GQA decode attention over the packed affine cache (sm_103a).
+// Split-K GQA decode attention, the CTA-ring kernel (sm_103a): caches read
+// mostly as 16-bit slots, non-uniform (table) caches, and the affine shapes
+// the warp-ring kernel in attn_affine.cu does not take.  Also the planner that
+// routes each call, the query compensation kernel and test-support kernels.
 //
 // Computes, per sequence b and query head h reading KV head h / G,
 //   out_h = sum_t softmax_t(sm_scale * q_h . k^_t) v^_t
@@ -8,17 +11,19 @@
 //   sum_t a_t v^_t = sum_t (a_t s_t) m_t + sum_t a_t o_t               (Eq. 9)
 // Keys and values are rotated by the normalized Hadamard matrix Hn
 // (Sec. 4.2), so q is rotated once per call and the value accumulator is
-// rotated back with Hn (its own inverse) at the end.
+// rotated back with Hn (its own inverse) at the end.  Non-uniform caches
+// ("KVQuant-NUQ", How it works) take table values as operands instead and add
+// their outliers' corrections.
 //
 // Design for GB300:
-//  * Work items: per KV head ("unit"), its chunks of 64 packed tokens (32 at
-//    4 bits); the unit's 16-slot tiles of 16-bit sink/recent tokens ride along
-//    with its chunks.  A persistent grid of one wave splits the list of all
-//    chunks into equal contiguous ranges (stream-K); a CTA walks its range
-//    unit by unit, handing chunks to its warps one at a time.
-//  * Packed chunks and 16-bit tiles stream HBM -> shared memory with bulk
-//    asynchronous copies (cp.async.bulk, completion on an mbarrier), a 2-deep
-//    ring per warp.
+//  * Work items: per KV head ("unit"), its 16-slot tiles of 16-bit sink and
+//    recent tokens, then its packed entries of 128 tokens (the last ragged).
+//    A persistent grid of 3-4 CTAs per SM splits the list of all units'
+//    entries into equal contiguous ranges (stream-K).
+//  * Each CTA streams its range through one ring of 3-4 slots, one entry per
+//    slot (bulk asynchronous copies, completion on the slot's mbarrier); every
+//    warp takes 32 tokens of every entry, and the last warp to release a slot
+//    issues the copies of the entry the ring's depth later.
 //  * Codes become mma operands with one AND per code pair: a code m held in a
 //    binary16 bit pattern below 2048 is exactly m * 2^-24 (scaled by a
 //    per-field power of two, folded into q and into the output rows).
@@ -26,12 +31,12 @@
 //    columns are 4 query heads x (hi, lo) binary16 halves of an fp32 operand,
 //    adjacent, so each lane owns one head and adds its halves in registers.
 //    P' is transposed into the B operand with movmatrix (no shared memory).
-//  * Softmax bookkeeping once per 32 tokens; the running max may lag by 2^8,
-//    so the accumulators are rescaled only when it grows by more than that.
+//  * The running max may lag by 2^8, so the accumulators are rescaled only
+//    when it grows by more than that.
 //  * Each CTA merges its 4 warps and writes one partial per (unit, kind); a
-//    second grid, launched as a programmatic dependent of the first, waits for
-//    it to finish, merges each unit's partials, rotates the value accumulator
-//    back and writes the output.
+//    second grid (combine_kernel), launched as a programmatic dependent of the
+//    first, waits for each unit's partials, merges them, rotates the value
+//    accumulator back and writes the output.
 #include <cuda_runtime.h>
 
 #include "attn_common.cuh"
