@@ -25,36 +25,60 @@ namespace dq {
 
 // ---------------------------------------------------------------------------
 // Key channel mean over tokens [t0, t1) of each unit (prefill).  One block per
-// unit, D threads; thread j accumulates channel j over the tokens in order
-// (acc = acc + y_tj from 0.0f), then divides by the count.
+// unit; thread j < D accumulates channel j over the tokens in order (acc =
+// acc + y_tj from 0.0f), then divides by the count.  KM_WARPS warps rotate a
+// chunk's rows into shared memory while each holds its rows of the next chunk
+// in registers, loaded before the chunk is summed, so no row waits for HBM.
 // ---------------------------------------------------------------------------
+constexpr int KM_WARPS = 16;
+constexpr int KM_ROWS = 4;  // rows per warp per chunk
+
 template <int V>
-__global__ void key_mean_kernel(QuantArgs a, int Hkv, long long t0, long long t1) {
+__device__ __forceinline__ void key_mean_load(const QuantArgs &a, int u, long long c0, long long t1,
+                                              float (&xr)[KM_ROWS][V]) {
     constexpr int D = 32 * V;
-    constexpr int CH = 32;  // tokens per smem chunk
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const long long esz = a.in_dtype == 0 ? 4 : 2;
+#pragma unroll
+    for (int i = 0; i < KM_ROWS; i++) {
+        const long long t = c0 + warp + KM_WARPS * i;
+        const long long base = (static_cast<long long>(u) * a.n_tok + (t - a.pos0)) * D;
+        const bool ok = t < t1 && in_buf(static_cast<const char *>(a.x) + base * esz, D * esz, a.x, a.sz_x, a.status);
+#pragma unroll
+        for (int j = 0; j < V; j++) xr[i][j] = ok ? ld_in(a.x, base + lane * V + j, a.in_dtype) : 0.f;
+    }
+}
+
+template <int V>
+__global__ void __launch_bounds__(KM_WARPS * 32) key_mean_kernel(QuantArgs a, int Hkv, long long t0, long long t1) {
+    constexpr int D = 32 * V;
+    constexpr int CH = KM_WARPS * KM_ROWS;  // tokens per chunk
     __shared__ float ys[CH][D];
-    __shared__ float xs[D / 32][D];
+    __shared__ float xs[KM_WARPS][D];
     const int u = blockIdx.x, kvh = u % Hkv;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = D / 32;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const float *T = a.T ? a.T + static_cast<long long>(kvh) * D * D : nullptr;
     float acc = 0.0f;
+    float xr[KM_ROWS][V];
+    key_mean_load<V>(a, u, t0, t1, xr);
     for (long long c0 = t0; c0 < t1; c0 += CH) {
         const int n = static_cast<int>(t1 - c0 < CH ? t1 - c0 : CH);
-        for (int r = warp; r < n; r += nw) {
-            const long long base = (static_cast<long long>(u) * a.n_tok + (c0 + r - a.pos0)) * D;
-            const long long esz = a.in_dtype == 0 ? 4 : 2;
-            const bool okx = in_buf(static_cast<const char *>(a.x) + base * esz, D * esz, a.x, a.sz_x, a.status);
-            float x[V];
 #pragma unroll
-            for (int j = 0; j < V; j++) x[j] = okx ? ld_in(a.x, base + lane * V + j, a.in_dtype) : 0.f;
-            rotate_row<V>(x, a.rot, a.hscale, T, xs[warp]);
+        for (int i = 0; i < KM_ROWS; i++) {
+            const int r = warp + KM_WARPS * i;
+            if (r < n) {
+                rotate_row<V>(xr[i], a.rot, a.hscale, T, xs[warp]);
 #pragma unroll
-            for (int j = 0; j < V; j++) ys[r][lane * V + j] = x[j];
+                for (int j = 0; j < V; j++) ys[r][lane * V + j] = xr[i][j];
+            }
         }
+        if (c0 + CH < t1) key_mean_load<V>(a, u, c0 + CH, t1, xr);  // the next chunk's rows, in flight
         __syncthreads();
-        for (int r = 0; r < n; r++) acc = __fadd_rn(acc, ys[r][threadIdx.x]);
+        if (threadIdx.x < D)
+            for (int r = 0; r < n; r++) acc = __fadd_rn(acc, ys[r][threadIdx.x]);
         __syncthreads();
     }
+    if (threadIdx.x >= D) return;
     const long long cnt = t1 - t0;
     float *mp = a.mean + static_cast<long long>(u) * D + threadIdx.x;
     if (in_buf(mp, 4, a.mean, a.sz_mean, a.status)) *mp = cnt > 0 ? __fdiv_rn(acc, static_cast<float>(cnt)) : 0.0f;
@@ -139,8 +163,8 @@ int launch_key_mean(const Layout &L, const QuantArgs &a, void *stream) {
     long long t1 = a.seq_after - L.n_recent;
     if (t1 < t0) t1 = t0;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    if (L.d == 128) key_mean_kernel<4><<<L.U, 128, 0, st>>>(a, L.Hkv, t0, t1);
-    else key_mean_kernel<2><<<L.U, 64, 0, st>>>(a, L.Hkv, t0, t1);
+    if (L.d == 128) key_mean_kernel<4><<<L.U, KM_WARPS * 32, 0, st>>>(a, L.Hkv, t0, t1);
+    else key_mean_kernel<2><<<L.U, KM_WARPS * 32, 0, st>>>(a, L.Hkv, t0, t1);
     return static_cast<int>(cudaGetLastError());
 }
 

@@ -207,40 +207,41 @@ __device__ __forceinline__ void quantize_loaded_row(const QuantArgs &a, const Ro
         }
     }
 
-    // pack
+    // pack: each code ORs its bits into its record word in the warp's scratch
+    // (free again), then the record's words go out, one lane each (keys a
+    // whole row, values this token's 16-bit half of its pair record)
     constexpr int WK = Rec<D, BITS>::K_WORDS, WV = Rec<D, BITS>::V_WORDS;
-    if (a.is_key) {
-        uint32_t *row = reinterpret_cast<uint32_t *>(a.codes + ms * L.rowK);
-        constexpr int WLO = D * 2 / 32;  // 2-bit plane words (BITS == 3)
+    uint32_t *pw = reinterpret_cast<uint32_t *>(xs);
+    const int nwords = a.is_key ? WK : WV;
+    const int e = static_cast<int>(slot & 1);  // values: the token's half of its pair record
+    __syncwarp();
+    if (lane < nwords) pw[lane] = 0u;
+    __syncwarp();
 #pragma unroll
-        for (int w = 0; w < WK; w++) {
-            uint32_t v = 0;
-#pragma unroll
-            for (int j = 0; j < V; j++) {
-                const int c = lane * V + j;
-                v |= contrib<D, BITS>(w, k_idx(c, D), c & 1, m[j], WLO);
-            }
-            v = __reduce_or_sync(FULL, v);
-            if (lane == w && in_buf(row + w, 4, a.codes, a.sz_codes, a.status)) row[w] = v;
-        }
-    } else {
-        const int e = static_cast<int>(slot & 1);
-        uint16_t *rec = reinterpret_cast<uint16_t *>(
-            a.codes + (static_cast<long long>(u) * (L.qcap / 2) + slot / 2) * L.pairV);
-        constexpr int WLO = 2 * D * 2 / 32;
-#pragma unroll
-        for (int w = 0; w < WV; w++) {
-            uint32_t v = 0;
-#pragma unroll
-            for (int j = 0; j < V; j++) {
-                const int c = lane * V + j;
-                v |= contrib<D, BITS>(w, v_idx(c, D), e, m[j], WLO);
-            }
-            v = __reduce_or_sync(FULL, v);
-            if (lane == (w & 31) && in_buf(rec + 2 * w + e, 2, a.codes, a.sz_codes, a.status))
-                rec[2 * w + e] = static_cast<uint16_t>(v >> (16 * e));
+    for (int j = 0; j < V; j++) {
+        const int c = lane * V + j;
+        const int idx = a.is_key ? k_idx(c, D) : v_idx(c, D);
+        const int half = a.is_key ? (c & 1) : e;
+        if (BITS == 3) {
+            const int wlo = (a.is_key ? 1 : 2) * D * 2 / 32;  // 2-bit plane words come first
+            atomicOr(&pw[idx / 8], (m[j] & 3u) << (16 * half + 2 * (idx % 8)));
+            atomicOr(&pw[wlo + idx / 16], ((m[j] >> 2) & 1u) << (16 * half + idx % 16));
+        } else {
+            constexpr int F = 16 / BITS;
+            atomicOr(&pw[idx / F], m[j] << (16 * half + BITS * (idx % F)));
         }
     }
+    __syncwarp();
+    if (a.is_key) {
+        uint32_t *row = reinterpret_cast<uint32_t *>(a.codes + ms * L.rowK);
+        if (lane < WK && in_buf(row + lane, 4, a.codes, a.sz_codes, a.status)) row[lane] = pw[lane];
+    } else {
+        uint16_t *rec = reinterpret_cast<uint16_t *>(
+            a.codes + (static_cast<long long>(u) * (L.qcap / 2) + slot / 2) * L.pairV);
+        if (lane < WV && in_buf(rec + 2 * lane + e, 2, a.codes, a.sz_codes, a.status))
+            rec[2 * lane + e] = static_cast<uint16_t>(pw[lane] >> (16 * e));
+    }
+    __syncwarp();  // the scratch is the caller's again
 }
 
 // Token pos0 + i of unit u: load_row, then quantize_loaded_row.
