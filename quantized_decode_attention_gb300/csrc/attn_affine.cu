@@ -58,14 +58,14 @@ static_assert(ST_OOB == 32u, "in_buf latches ST_OOB");
 
 constexpr int AF_WPB = 16;                       // warps per CTA
 constexpr int AF_NUS = 4;                        // units a CTA's packed range may touch
-constexpr int AF_NSR = 3;                        // ring slots of the 16-bit-tile warp
+constexpr int AF_NSR = 2;                        // ring slots of the 16-bit-tile warp
 constexpr int AF_NUR = 3;                        // units the 16-bit-tile warp's range may touch
 constexpr int AF_RTILE = 16;                     // slots per 16-bit tile
 constexpr uint64_t AF_WAIT_NS = 2000000000ull;   // 2 s; a healthy copy lands in microseconds
 
 template <int D, int BITS, bool M16>
 struct ACfg {
-    static constexpr int TPC = BITS == 2 ? 4 : 2;  // 16-token tiles per chunk
+    static constexpr int TPC = BITS == 2 ? 4 : (BITS == 3 ? 3 : 2);  // 16-token tiles per chunk (what fits)
     static constexpr int NS = 2;                    // ring slots per packed warp
     static constexpr int ROWK = D * BITS / 8;       // bytes per key record
     static constexpr int PAIRV = 2 * D * BITS / 8;  // bytes per value pair record
