@@ -203,6 +203,20 @@ __device__ __forceinline__ void issue_chunk(const AttnArgs &a, long long qcap, i
                      "@p mbarrier.arrive.shared::cta.b64 _, [%0];\n}\n" ::"r"(br) : "memory");
         return;
     }
+    if (T == C::TPC) {  // a full chunk: the sizes are constants
+        constexpr uint32_t KB = 16 * C::TPC * C::ROWK, VB = 8 * C::TPC * C::PAIRV, MB2 = 32 * C::TPC * C::MB;
+        asm volatile(
+            "{\n .reg .pred p;\n elect.sync _|p, 0xffffffff;\n"
+            "@p mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n"
+            "@p cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%2], [%3], %4, [%0];\n"
+            "@p cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%5], [%6], %7, [%0];\n"
+            "@p cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%8], [%9], %10, [%0];\n"
+            "@p cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%11], [%12], %10, [%0];\n}\n" ::"r"(br),
+            "n"(KB + VB + 2 * MB2), "r"(sb), "l"(ck), "n"(KB), "r"(sb + C::VOFF), "l"(cv), "n"(VB),
+            "r"(sb + C::MKOFF), "l"(mk), "n"(MB2), "r"(sb + C::MVOFF), "l"(mv)
+            : "memory");
+        return;
+    }
     asm volatile(
         "{\n .reg .pred p;\n elect.sync _|p, 0xffffffff;\n"
         "@p mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n"
