@@ -103,6 +103,8 @@ def lib():
             L.or_nuq_assign.argtypes = [_f32, C.c_int, _u16, C.c_int, _u8]
             L.or_nuq_vector.restype = C.c_int
             L.or_nuq_vector.argtypes = [_f32, C.c_int, C.c_int, C.c_int, C.c_float, _u8, _u16, _u8]
+            L.or_nuq_vector_grouped.restype = C.c_int
+            L.or_nuq_vector_grouped.argtypes = [_f32, C.c_int, C.c_int, C.c_int, C.c_int, C.c_float, _u8, _u16, _u8]
             _i32 = _P(dtype=np.int32, flags="C_CONTIGUOUS")
             _i64 = _P(dtype=np.int64, flags="C_CONTIGUOUS")
             L.or_dq_expected_max.restype = C.c_double
@@ -309,6 +311,19 @@ def nuq_vector(x, bits: int, iters: int, frac: float):
     lut = np.zeros(1 << bits, dtype=np.uint16)
     codes = np.zeros(x.size, dtype=np.uint8)
     lib().or_nuq_vector(x, x.size, bits, iters, float(frac), flag, lut, codes)
+    return flag.astype(bool), lut, codes
+
+
+def nuq_vector_grouped(x, bits: int, iters: int, frac: float, group: int):
+    """One vector fitted per group of `group` elements: (outlier mask, fp16
+    tables [n / group, 2^bits], codes); outliers ranked over the whole vector."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    if group <= 0 or x.size % group:
+        raise ValueError("group must divide the vector")
+    flag = np.zeros(x.size, dtype=np.uint8)
+    lut = np.zeros((x.size // group, 1 << bits), dtype=np.uint16)
+    codes = np.zeros(x.size, dtype=np.uint8)
+    lib().or_nuq_vector_grouped(x, x.size, group, bits, iters, float(frac), flag, lut, codes)
     return flag.astype(bool), lut, codes
 
 

@@ -119,26 +119,37 @@ class NuqTensor:
     """Oracle result for one tensor under the non-uniform (Lloyd-Max) scheme.
 
     "KVQuant-NUQ" page, Quantization axes: keys get one table per channel over
-    the quantized tokens, values one table per token over its channels; the
+    the quantized tokens, values one table per token over its channels (per
+    group of channels with a group size, Configuration reference); the
     outliers of each vector (exactly k by rank) keep their fp16 value."""
     codes: np.ndarray     # [B, H, Sq, d] uint8 nearest-level codes (outliers included)
-    lut: np.ndarray       # keys [B, H, d, L], values [B, H, Sq, L]: fp16 bits
+    lut: np.ndarray       # keys [B, H, d, L]; values [B, H, Sq, G * L] (G tables per token): fp16 bits
     outlier: np.ndarray   # [B, H, Sq, d] bool
     val16: np.ndarray     # [B, H, Sq, d] uint16: fp16 bits of the input (outlier values)
-    xhat: np.ndarray      # [B, H, Sq, d] float32: table value, or the outlier's fp16 value
+    xhat: np.ndarray      # [B, H, Sq, d] float32: table value, or the outlier's fp16 value (NaN: not yet coded)
+    blk_lut: np.ndarray | None = None  # keys with a refit interval: [B, H, NB, d, L] tables per slot block
+    n_coded: int | None = None         # keys with a refit interval: slots [0, n_coded) are coded
 
 
-def quantize_nuq(w: W.Workload, x_bits: np.ndarray, is_key: bool, S: int) -> NuqTensor:
-    """Prefill of tokens [n_sink, S) of x_bits [B,H,S,d] under the NUQ scheme."""
-    from . import nuq_vector
+def _value_group(w: W.Workload) -> int:
+    g = w.extra.get("group_size", 0)
+    return w.head_dim if g in (0, None) else g
+
+
+def quantize_nuq(w: W.Workload, x_bits: np.ndarray, is_key: bool, S: int, t0: int | None = None) -> NuqTensor:
+    """Prefill of tokens [t0, S) of x_bits [B,H,S,d] under the NUQ scheme (t0
+    defaults to n_sink).  Values are fitted per token, per group of channels
+    when the workload sets a group size; keys per channel over all the tokens."""
+    from . import nuq_vector, nuq_vector_grouped
     B, H, n, d = x_bits.shape
-    x = _f32_input(x_bits, w.kv_dtype)[:, :, w.n_sink:S]
+    x = _f32_input(x_bits, w.kv_dtype)[:, :, (w.n_sink if t0 is None else t0):S]
     nq = x.shape[2]
     L = 1 << w.bits
     iters, frac = w.extra.get("lloyd_iters", 8), w.extra.get("outlier_frac", 0.01)
+    g = _value_group(w)
     codes = np.zeros((B, H, nq, d), dtype=np.uint8)
     out = np.zeros((B, H, nq, d), dtype=bool)
-    lut = np.zeros((B, H, d if is_key else nq, L), dtype=np.uint16)
+    lut = np.zeros((B, H, d, L) if is_key else (B, H, nq, (d // g) * L), dtype=np.uint16)
     for b in range(B):
         for h in range(H):
             if is_key:
@@ -147,8 +158,8 @@ def quantize_nuq(w: W.Workload, x_bits: np.ndarray, is_key: bool, S: int) -> Nuq
                     codes[b, h, :, c], out[b, h, :, c], lut[b, h, c] = co, fl, lu
             else:
                 for t in range(nq):
-                    fl, lu, co = nuq_vector(np.ascontiguousarray(x[b, h, t]), w.bits, iters, frac)
-                    codes[b, h, t], out[b, h, t], lut[b, h, t] = co, fl, lu
+                    fl, lu, co = nuq_vector_grouped(np.ascontiguousarray(x[b, h, t]), w.bits, iters, frac, g)
+                    codes[b, h, t], out[b, h, t], lut[b, h, t] = co, fl, lu.reshape(-1)
     # fp16 rounding (RNE) as a library primitive; the oracle's own binary16
     # conversion is pinned against the same numpy cast
     val16 = x.astype(np.float16).view(np.uint16)
@@ -156,7 +167,9 @@ def quantize_nuq(w: W.Workload, x_bits: np.ndarray, is_key: bool, S: int) -> Nuq
     if is_key:
         tab = np.take_along_axis(levels[:, :, None, :, :], codes[..., None].astype(np.int64), axis=-1)[..., 0]
     else:
-        tab = np.take_along_axis(levels[:, :, :, None, :], codes[..., None].astype(np.int64), axis=-1)[..., 0]
+        grp = np.repeat(np.arange(d // g), g)[None, None, None, :]        # table of each channel
+        idx = (grp * L + codes).astype(np.int64)
+        tab = np.take_along_axis(levels, idx.reshape(B, H, nq, d), axis=-1)
     xhat = np.where(out, val16.view(np.float16).astype(np.float32), tab).astype(np.float32)
     return NuqTensor(codes, lut, out, val16, xhat)
 
@@ -190,13 +203,26 @@ def quantize_nuq_stream(w: W.Workload, x_bits: np.ndarray, is_key: bool, P: int,
     takes the nearest level of its channel's table and is an outlier when
     |x| >= the channel's frozen threshold (nuq_key_thresholds).  The key side
     channel holds nnz_cap entries per (sequence, head), filled in token order and
-    channel order; an outlier that finds it full is not stored and keeps its level."""
+    channel order; an outlier that finds it full is not stored and keeps its level.
+
+    Configuration reference, kvquant_refit_interval N > 0 (keys): the key tables
+    belong to blocks of N quantized slots (slot = token - n_sink).  Every block
+    the prefill reaches keeps the prefill's tables, and its decode keys are
+    coded as above.  A block of decode keys only is refitted when its last slot
+    arrives: per channel, rank outliers and a Lloyd fit over the block's own N
+    keys, exactly as a prefill of those N tokens; until then its keys are not
+    coded (they are read from the 16-bit recent window)."""
     if not is_key:
         return quantize_nuq(w, x_bits, False, S)
+    N = w.extra.get("refit_interval", 0) or 0
     pre = quantize_nuq(w, x_bits, True, P)
     B, H, _, d = x_bits.shape
+    L = 1 << w.bits
+    ns = w.n_sink
+    pq, sq = P - ns, S - ns                      # prefill's and cache's quantized slot counts
+    imm = sq if N == 0 else min(sq, -(-pq // N) * N)   # slots coded with the prefill's tables
     thr = nuq_key_thresholds(w, x_bits, P)
-    x = _f32_input(x_bits, w.kv_dtype)[:, :, P:S]
+    x = _f32_input(x_bits, w.kv_dtype)[:, :, P:ns + imm]
     nd = x.shape[2]
     codes = np.zeros((B, H, nd, d), dtype=np.uint8)
     for b in range(B):
@@ -204,19 +230,53 @@ def quantize_nuq_stream(w: W.Workload, x_bits: np.ndarray, is_key: bool, P: int,
             for c in range(d):
                 codes[b, h, :, c] = nuq_assign(np.ascontiguousarray(x[b, h, :, c]), pre.lut[b, h, c])
     out = np.abs(x) >= thr[:, :, None, :]
-    if nnz_cap is not None:
-        for b in range(B):
-            for h in range(H):
-                room = nnz_cap - int(pre.outlier[b, h].sum())
-                flat = out[b, h].reshape(-1)             # token-major, channels ascending
-                idx = np.flatnonzero(flat)
-                flat[idx[max(room, 0):]] = False
     val16 = x.astype(np.float16).view(np.uint16)
     levels = pre.lut.view(np.float16).astype(np.float32)
     tab = np.take_along_axis(levels[:, :, None, :, :], codes[..., None].astype(np.int64), axis=-1)[..., 0]
     xhat = np.where(out, val16.view(np.float16).astype(np.float32), tab).astype(np.float32)
-    return NuqTensor(np.concatenate([pre.codes, codes], 2), pre.lut, np.concatenate([pre.outlier, out], 2),
-                     np.concatenate([pre.val16, val16], 2), np.concatenate([pre.xhat, xhat], 2))
+    parts = [(codes, out, val16, xhat)]
+    blk_lut, n_coded = None, None
+    if N > 0:
+        nb = -(-max(sq, 1) // N)
+        blk_lut = np.zeros((B, H, nb, d, L), dtype=np.uint16)
+        for blk in range(-(-pq // N)):
+            blk_lut[:, :, blk] = pre.lut
+        blk = -(-pq // N)
+        while (blk + 1) * N <= sq:               # complete blocks of decode keys
+            t0 = ns + blk * N
+            one = quantize_nuq(w, x_bits, True, t0 + N, t0=t0)
+            blk_lut[:, :, blk] = one.lut
+            parts.append((one.codes, one.outlier, one.val16, one.xhat))
+            blk += 1
+        n_coded = blk * N if blk > -(-pq // N) else imm
+        left = sq - n_coded                      # slots waiting for their block
+        if left > 0:
+            z = np.zeros((B, H, left, d), dtype=np.uint8)
+            parts.append((z, np.zeros(z.shape, bool), np.zeros(z.shape, np.uint16),
+                          np.full(z.shape, np.nan, np.float32)))
+    codes = np.concatenate([pre.codes] + [p[0] for p in parts], 2)
+    out = np.concatenate([pre.outlier] + [p[1] for p in parts], 2)
+    val16 = np.concatenate([pre.val16] + [p[2] for p in parts], 2)
+    xhat = np.concatenate([pre.xhat] + [p[3] for p in parts], 2)
+    if nnz_cap is not None:                      # decode entries in slot order while the channel has room
+        for b in range(B):
+            for h in range(H):
+                room = nnz_cap - int(pre.outlier[b, h].sum())
+                flat = out[b, h, pq:].reshape(-1)            # slot-major, channels ascending
+                idx = np.flatnonzero(flat)
+                cut = idx[max(room, 0):]
+                flat[cut] = False
+                out[b, h, pq:] = flat.reshape(out[b, h, pq:].shape)
+                # an entry that found no room keeps its level
+                tt, cc = np.unravel_index(cut, (sq - pq, d))
+                for t_, c_ in zip(tt, cc):
+                    xhat[b, h, pq + t_, c_] = _nuq_key_level(w, pre, blk_lut, b, h, pq + t_, c_, codes, N)
+    return NuqTensor(codes, pre.lut, out, val16, xhat, blk_lut, n_coded)
+
+
+def _nuq_key_level(w, pre, blk_lut, b, h, slot, c, codes, N):
+    lut = pre.lut[b, h, c] if N == 0 else blk_lut[b, h, slot // N, c]
+    return np.float32(lut.view(np.float16)[codes[b, h, slot, c]])
 
 
 def nuq_key_outliers_csr(nt: NuqTensor, qcap: int, nnz_cap: int):

@@ -19,6 +19,10 @@
  *    vector even when magnitudes tie.
  *  - Quantization axes: keys per channel (sample axis = tokens), values per
  *    token (sample axis = channels).
+ *  - Configuration reference, kvquant_group_size: the fit of a value token
+ *    runs per group of g consecutive channels, each group with its own table
+ *    (or_nuq_vector_grouped); the token's outliers are still chosen over the
+ *    whole token.
  * Readings where the page is silent (all stated with the tests):
  *  - k = floor(f * n + 0.5); ties in |x| go to the lower index.
  *  - Quantile init: level i = sorted[floor((2i+1) * n / (2L))] of the n fit values
@@ -167,5 +171,27 @@ int or_nuq_vector(const float *x, int n, int bits, int iters, float f, uint8_t *
     float lev[16];
     or_nuq_fit(x, flag, n, L, iters, lev, lut16);
     or_nuq_assign(x, n, lut16, L, codes);
+    return k;
+}
+
+/*
+ * A vector whose fit runs per group of g consecutive elements: the k =
+ * outlier_count(f, n) rank outliers are chosen over the whole vector first
+ * (Dense-and-Sparse isolation selects per channel / per token), then each
+ * group's remaining values get their own Lloyd fit (positions 0 .. g-1 of the
+ * group in the R32 order) and its elements are coded against the group's fp16
+ * table.  lut16 receives the n / g tables of L entries in group order.  g must
+ * divide n; with g == n this is or_nuq_vector.  Returns k.
+ */
+int or_nuq_vector_grouped(const float *x, int n, int g, int bits, int iters, float f, uint8_t *flag,
+                          uint16_t *lut16, uint8_t *codes) {
+    const int L = 1 << bits;
+    const int k = or_outlier_count(f, n);
+    or_topk_abs(x, n, k, flag);
+    float lev[16];
+    for (int s = 0; s + g <= n; s += g) {
+        or_nuq_fit(x + s, flag + s, g, L, iters, lev, lut16 + (s / g) * L);
+        or_nuq_assign(x + s, g, lut16 + (s / g) * L, L, codes + s);
+    }
     return k;
 }
