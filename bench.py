@@ -34,6 +34,11 @@ sys.path.insert(0, ROOT)
 import workloads as W  # noqa: E402
 
 METRIC = "quantized decode-attn tokens/s & achieved HBM GB/s (% of roofline), 2/3/4-bit"
+# the KVQuant-shaped cache with the page's configuration options on: value
+# tables per 32 channels, key tables per 128-slot block (a window of 128 recent
+# 16-bit tokens holds a block's keys until it is refitted)
+NUQ_GROUP_REFIT = W.NUQ.with_(n_recent=128, extra={"lloyd_iters": 8, "outlier_frac": 0.01, "group_size": 32,
+                                                   "refit_interval": 128})
 CSRC = os.path.join(ROOT, "quantized_decode_attention_gb300", "csrc")
 # the sources each attention kernel is compiled from (the traffic record is
 # valid only for the exact sources it was captured with)
@@ -122,17 +127,20 @@ def barrier():
 
 def nuq_algorithmic_bytes(w: W.Workload, S: int) -> dict:
     """Bytes one non-uniform decode-attention call must move: key and value
-    codes, per-token value tables, per-channel key tables, the outlier side
-    channels (key CSR by token with its row pointers, value entries per token),
-    the 16-bit sinks, q and out."""
+    codes, per-token value tables (one per channel group), per-channel key
+    tables (one set per refit block read), the outlier side channels (key CSR
+    by token with its row pointers, value entries per token), the 16-bit sinks
+    and recent window, q and out."""
     U, d, L = w.batch * w.n_kv_heads, w.head_dim, 1 << w.bits
-    n_raw = min(S, w.n_sink)
+    n_raw = min(S, w.n_sink) + min(max(S - w.n_sink, 0), w.n_recent)
     n_q = S - n_raw
     frac = w.extra.get("outlier_frac", 0.01)
     kk = int(np.floor(np.float64(np.float32(frac)) * n_q + 0.5))
     kv = int(np.floor(np.float64(np.float32(frac)) * d + 0.5))
+    gv = d // (w.extra.get("group_size", 0) or d)
+    N = w.extra.get("refit_interval", 0) or 0
     codes = U * n_q * d * w.bits // 8 * 2
-    lut = U * n_q * L * 2 + U * d * L * 2
+    lut = U * n_q * gv * L * 2 + U * (-(-n_q // N) if N else 1) * d * L * 2
     side = U * (d * kk * 4 + (n_q + 1) * 4) + U * n_q * kv * 4
     raw = U * n_raw * d * 2 * 2
     q = w.batch * w.n_q_heads * d * 4
@@ -516,7 +524,8 @@ def run_gpu_nuq(args, w):
     cfg = make_config(batch=w.batch, n_kv_heads=w.n_kv_heads, n_q_heads=w.n_q_heads, head_dim=w.head_dim,
                       max_seq=S, kv_dtype=w.kv_dtype, out_dtype=w.out_dtype, bits=w.bits, rot_k="none",
                       rot_v="none", mean_k=False, n_sink=w.n_sink, n_recent=w.n_recent, scheme="nuq",
-                      lloyd_iters=w.extra.get("lloyd_iters", 8), outlier_frac=w.extra.get("outlier_frac", 0.01))
+                      lloyd_iters=w.extra.get("lloyd_iters", 8), outlier_frac=w.extra.get("outlier_frac", 0.01),
+                      group_size_v=w.extra.get("group_size", 0), refit_k=w.extra.get("refit_interval", 0))
     L2 = torch.cuda.get_device_properties(0).L2_cache_size
     ab = nuq_algorithmic_bytes(w, S)
     copies = args.copies or max(3, int(np.ceil(3 * L2 / ab["total"])) + 1)
@@ -1181,6 +1190,7 @@ def main():
         torch.cuda.empty_cache()
     del k_dev, v_dev
     nuq = None if args.no_nuq else run_gpu_nuq(args, W.NUQ)
+    nuq_gr = None if args.no_nuq else run_gpu_nuq(args, NUQ_GROUP_REFIT)
     dqrs = [] if args.no_dquant else [(D, run_gpu_dquant(args, D)) for D in (W.DQUANT, W.DQUANT_196)]
     qwen = [run_qwen_long(args, int(x), rank) for x in args.qwen.split(",") if x.strip()]
 
@@ -1233,6 +1243,20 @@ def main():
                        "n_sink": W.NUQ.n_sink, "outlier_frac": 0.01, "lloyd_iters": 8,
                        "l2": f"{nuq['copies']} cache copies rotated per step (> L2)",
                        "step": "decode attention over a prefilled cache, CUDA graph over the copies"}}
+    if nuq_gr is not None:
+        wg = NUQ_GROUP_REFIT
+        line["variants"][f"{wg.name}-{wg.bits}bit-group32-refit128"] = {
+            "value": round(wg.batch / (nuq_gr["total_ms"] / nuq_gr["steps"] / 1e3), 1),
+            "ms_per_step": round(nuq_gr["total_ms"] / nuq_gr["steps"], 5),
+            "roofline": roof(nuq_gr, "nuq_g32_r128"), "e2e_tok_s": round(nuq_gr["e2e_tok_s"], 1),
+            "prefill_ms": round(nuq_gr["prefill_ms"], 3),
+            "config": {"batch": wg.batch, "q_heads": wg.n_q_heads, "kv_heads": wg.n_kv_heads,
+                       "head_dim": wg.head_dim, "seq_len": wg.seq, "bits": wg.bits, "n_sink": wg.n_sink,
+                       "n_recent": wg.n_recent, "outlier_frac": 0.01, "lloyd_iters": 8,
+                       "group_size_v": 32, "refit_interval_k": 128,
+                       "l2": f"{nuq_gr['copies']} cache copies rotated per step (> L2)",
+                       "step": "decode attention over a prefilled cache (value tables per 32 channels, key "
+                               "tables per 128-slot block), CUDA graph over the copies"}}
     for wq, r in qwen:
         line["variants"][f"{wq.name}-s{wq.seq}-{wq.bits}bit"] = {
             "value": round(wq.batch / (r["total_ms"] / args.steps / 1e3), 1),

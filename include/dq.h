@@ -86,6 +86,19 @@ typedef struct {
                             dq_quest_step; needs clip = 0 */
     int lloyd_iters;     /* DQ_NUQ */
     float outlier_frac;  /* DQ_NUQ */
+    int group_size;      /* DQ_NUQ values: channels per value table, 0 (the
+                            whole token) or 32 ("KVQuant-NUQ", Configuration
+                            reference, kvquant_group_size): a token's outliers
+                            are ranked over the token, then each group of 32
+                            consecutive channels is fitted alone.  32 needs
+                            head_dim 128.  Keys: 0 (a key table spans its
+                            channel's tokens) */
+    int refit_interval;  /* DQ_NUQ keys ("KVQuant-NUQ", Configuration reference,
+                            kvquant_refit_interval): 0 = the prefill's tables,
+                            frozen; N > 0, a multiple of 128, = key tables per
+                            block of N quantized slots, refitted on each block
+                            of decode keys when it completes (see
+                            dq_quantize_kv).  Values: 0 */
 } dq_tensor_cfg;
 
 typedef struct {
@@ -136,8 +149,14 @@ typedef struct {
  *                                 frozen at prefill (the magnitude of its kk-th
  *                                 rank outlier, +inf when kk = 0); present when
  *                                 kk > 0
- * lut_k       [U][head_dim][L]    fp16 levels of each key channel
- * lut_v       [U][Qcap][L]        fp16 levels of each value token (by slot)
+ * lut_k       [U][NBK][head_dim][L]  fp16 levels of each key channel for
+ *                                 each block of N = refit_interval quantized
+ *                                 slots (NBK = ceil(Qcap / N); NBK = 1 when N
+ *                                 = 0), then, when N > 0, [U] int32: the
+ *                                 prefill's quantized slot count
+ * lut_v       [U][Qcap][GV][L]    fp16 levels of each value token (by slot),
+ *                                 GV = head_dim / group_size tables, channel c
+ *                                 in table c / group_size (GV = 1 for 0)
  * ol_rowptr_k [U][Qcap+4]         int32: key outliers of slot p are entries
  *                                 [rowptr[p], rowptr[p+1]); rowptr[p] for p
  *                                 >= the quantized token count holds the total
@@ -207,7 +226,15 @@ dq_status dq_kv_sizes(const dq_config *cfg, size_t bytes[DQ_NUM_BUFFERS]);
  * tables, appends each element with |x| >= its channel's threshold to the key
  * side channel, and fits each value token as a prefill does.  Entries that
  * find the side channel full are not stored (the element keeps its level) and
- * dq_check reports DQ_EINFEASIBLE.  DQ_RANS (D-Quant Sec. 4.2, windowed key mean): a
+ * dq_check reports DQ_EINFEASIBLE.  With a key refit_interval N > 0 the key
+ * tables live per block of N quantized slots: the blocks a prefill reaches
+ * hold its tables and their appended keys are coded as above; an appended key
+ * of a later block stays in the 16-bit recent window only, and the append that
+ * completes such a block fits that block's tables on its N keys (rank
+ * outliers and Lloyd sweeps per channel, as a prefill of those tokens) and
+ * codes them, reading the block's older keys from the recent window.  That
+ * needs n_recent >= N, a 16-bit kv_dtype and head_dim 128, and appends that
+ * follow one another without gaps.  DQ_RANS (D-Quant Sec. 4.2, windowed key mean): a
  * prefill encodes every token t >= n_sink, its last 128-slot window's mean
  * taken over the tokens it has; an append (pos0 > 0) keeps its tokens in the
  * 16-bit recent window only and, for each 128-slot window that it completes,

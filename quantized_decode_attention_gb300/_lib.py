@@ -28,7 +28,8 @@ GRIDS = {"minmax": 0, "quest": 1}
 class TensorCfg(C.Structure):
     _fields_ = [("scheme", C.c_int), ("bits", C.c_int), ("levels", C.c_int), ("container_bytes", C.c_int),
                 ("rot", C.c_int), ("mean", C.c_int), ("clip", C.c_float), ("grid", C.c_int),
-                ("lloyd_iters", C.c_int), ("outlier_frac", C.c_float)]
+                ("lloyd_iters", C.c_int), ("outlier_frac", C.c_float), ("group_size", C.c_int),
+                ("refit_interval", C.c_int)]
 
 
 class Config(C.Structure):
@@ -144,7 +145,7 @@ def make_config(*, batch, n_kv_heads, n_q_heads, head_dim, max_seq, kv_dtype="bf
                 out_dtype="bf16", bits=2, bits_v=None, rot_k="hadamard", rot_v="hadamard", mean_k=True,
                 clip_k=0.0, clip_v=None, grid_k="minmax", grid_v=None, n_sink=0, n_recent=0, scheme="affine",
                 lloyd_iters=8,
-                outlier_frac=0.01, levels_k=8, levels_v=6, container_k=331, container_v=231,
+                outlier_frac=0.01, group_size_v=0, refit_k=0, levels_k=8, levels_v=6, container_k=331, container_v=231,
                 rans_alpha=1.4) -> Config:
     c = Config()
     c.batch, c.n_kv_heads, c.n_q_heads, c.head_dim, c.max_seq = batch, n_kv_heads, n_q_heads, head_dim, max_seq
@@ -161,6 +162,8 @@ def make_config(*, batch, n_kv_heads, n_q_heads, head_dim, max_seq, kv_dtype="bf
     if scheme == "nuq":
         c.k.lloyd_iters = c.v.lloyd_iters = lloyd_iters
         c.k.outlier_frac = c.v.outlier_frac = outlier_frac
+        c.v.group_size = group_size_v
+        c.k.refit_interval = refit_k
     c.rans_alpha, c.rans_prob_bits = rans_alpha, 8
     if scheme == "rans":
         c.k.levels, c.v.levels = levels_k, levels_v

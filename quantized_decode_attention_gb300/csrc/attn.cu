@@ -49,9 +49,11 @@ constexpr int RTILE = 16;                           // slots per 16-bit work ite
 constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;   // 2 s; a healthy copy takes microseconds
 
 
-// NUQ: the non-uniform scheme (per-channel key tables, per-token value tables,
-// fp16 outlier side channel) instead of the affine one.
-template <int D, int BK, int BV, bool M16, bool NUQ = false>
+// NUQ: 1 = the non-uniform scheme (per-channel key tables, per-token value
+// tables, fp16 outlier side channel) instead of the affine one; 2 = the same
+// with value tables per 32-channel group and/or key tables per refit block
+// (copied with each entry), head_dim 128.
+template <int D, int BK, int BV, bool M16, int NUQ = 0>
 struct Cfg {
     static constexpr int ST = 128;                // packed tokens per pipeline entry
     static constexpr int SUB = 32;                // tokens of an entry per warp (one softmax step)
@@ -65,8 +67,10 @@ struct Cfg {
     static constexpr int KBYTES = ST * ROWK;
     static constexpr int VBYTES = ST / 2 * PAIRV;
     static constexpr int MBYTES = NUQ ? 0 : ST * 2 * MB;
-    static constexpr int LUTV = NUQ ? ST * LV * 2 : 0;
-    static constexpr int ENTRY = KBYTES + VBYTES + 2 * MBYTES + LUTV;
+    static constexpr int GVMAX = NUQ == 2 ? D / 32 : 1;  // value tables per token, at most
+    static constexpr int LUTV = NUQ ? ST * GVMAX * LV * 2 : 0;
+    static constexpr int LUTK = NUQ == 2 ? D * (1 << BK) * 2 : 0;  // the entry's key tables (refit blocks)
+    static constexpr int ENTRY = KBYTES + VBYTES + 2 * MBYTES + LUTV + LUTK;
     static constexpr int RAWBYTES = 64 * D;       // one 16-slot tile of 16-bit keys + values
     static constexpr int SLOT = ((ENTRY > RAWBYTES ? ENTRY : RAWBYTES) + 127) / 128 * 128;
     // ring depth: four slots where four CTAs per SM still fit, else as many as
@@ -80,7 +84,7 @@ struct Cfg {
 
 
 // ---- shared memory -----------------------------------------------------------
-template <int D, int BK, int BV, bool M16, bool NUQ = false>
+template <int D, int BK, int BV, bool M16, int NUQ = 0>
 struct Smem {
     using C = Cfg<D, BK, BV, M16, NUQ>;
     // query operands of up to two units at a time: [unit slot][kind: 0 16-bit
@@ -128,7 +132,7 @@ __device__ __forceinline__ void mbar_arrive_elect(uint64_t *bar) {
 // packed tokens [p*ST, p*ST + ST): keys, value pairs, key meta, value meta,
 // each at its fixed offset in the slot.  A last entry that would run past the
 // unit's capacity copies the 64 tokens that exist (capacity is a multiple of 64).
-template <int D, int BK, int BV, bool M16, bool NUQ = false>
+template <int D, int BK, int BV, bool M16, int NUQ = 0>
 __device__ __forceinline__ void issue_entry(const AttnArgs &a, const AttnShape &sh, int u, int e, uint8_t *slot,
                                             uint64_t *bar) {
     using C = Cfg<D, BK, BV, M16, NUQ>;
@@ -151,8 +155,25 @@ __device__ __forceinline__ void issue_entry(const AttnArgs &a, const AttnShape &
     const uint8_t *ck = a.codes_k + g0 * C::ROWK;
     const uint8_t *cv = a.codes_v + g0 / 2 * C::PAIRV;
     if constexpr (NUQ) {
-        const uint8_t *lv = reinterpret_cast<const uint8_t *>(a.lut_v) + g0 * C::LV * 2;
-        const uint32_t kb = nt * C::ROWK, vb = nt / 2 * C::PAIRV, lb = nt * C::LV * 2;
+        const int gv = NUQ == 2 ? a.gv : 1;
+        const uint8_t *lv = reinterpret_cast<const uint8_t *>(a.lut_v) + g0 * gv * C::LV * 2;
+        const uint32_t kb = nt * C::ROWK, vb = nt / 2 * C::PAIRV, lb = nt * gv * C::LV * 2;
+        if constexpr (NUQ == 2) if (a.refit) {  // plus the key tables of the entry's block
+            const uint8_t *lk = reinterpret_cast<const uint8_t *>(a.lut_k) +
+                                (static_cast<long long>(u) * a.nbk + t0 / a.refit) * C::LUTK;
+            asm volatile(
+                "{\n .reg .pred p;\n elect.sync _|p, 0xffffffff;\n"
+                "@p mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n"
+                "@p cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%2], [%3], %4, [%0];\n"
+                "@p cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%5], [%6], %7, [%0];\n"
+                "@p cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%8], [%9], %10, [%0];\n"
+                "@p cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%11], [%12], %13, [%0];\n}\n" ::"r"(br),
+                "r"(kb + vb + lb + static_cast<uint32_t>(C::LUTK)), "r"(sb), "l"(ck), "r"(kb), "r"(sb + C::KBYTES), "l"(cv),
+                "r"(vb), "r"(sb + C::KBYTES + C::VBYTES), "l"(lv), "r"(lb), "r"(sb + C::KBYTES + C::VBYTES + C::LUTV),
+                "l"(lk), "n"(C::LUTK)
+                : "memory");
+            return;
+        }
         asm volatile(
             "{\n .reg .pred p;\n elect.sync _|p, 0xffffffff;\n"
             "@p mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n"
@@ -226,8 +247,8 @@ __device__ __forceinline__ float f16v(uint16_t h) { return __half2float(__ushort
 // loads issued before the key contraction; contributions meet in shared
 // memory (pb holds the logit corrections, then the probabilities).
 template <int D, int BK, int BV>
-__device__ __forceinline__ void process_block_nuq(const uint8_t *kp, const uint8_t *vp, const uint16_t *lvp, int valid,
-                                                  const uint32_t (&qb)[D / 16][2], const uint16_t *lutk,
+__device__ __forceinline__ void process_block_nuq(const uint8_t *kp, const uint8_t *vp, const uint16_t *lvp, int gv,
+                                                  int valid, const uint32_t (&qb)[D / 16][2], const uint16_t *lutk,
                                                   const float (*qf)[D], float sm_l2, WarpState<D / 16> &st,
                                                   float (*corr)[D], float (*pb)[32], const AttnArgs &a,
                                                   const AttnShape &sh, int u, long long s0) {
@@ -331,18 +352,22 @@ __device__ __forceinline__ void process_block_nuq(const uint8_t *kp, const uint8
         uint32_t v0[NWV], v1[NWV];
         load_v_slice<D, BV>(vp + (8 * t + tig) * PAIRV, g, v0);
         load_v_slice<D, BV>(vp + (8 * t + tig + 4) * PAIRV, g, v1);
-        const uint16_t *la = lvp + (16 * t + 2 * tig) * LV, *lb = la + 8 * LV;
+        // token 16t + 2tig (+1, +8, +9)'s tables; channels 16mi .. 16mi + 15 share one group's
+        const int TV = gv * LV;  // table entries per token
+        const uint16_t *la0 = lvp + (16 * t + 2 * tig) * TV, *lb0 = la0 + 8 * TV;
 #pragma unroll
         for (int mi = 0; mi < NMT; mi++) {
+            const int go = (16 * mi * gv) / D * LV;
+            const uint16_t *la = la0 + go, *lb = lb0 + go;
             uint32_t m0, m1, r[4];
             field_codes<BV>(v0, 2 * mi, m0, m1);
-            r[0] = pack2(la[m0], la[LV + m1]);
+            r[0] = pack2(la[m0], la[TV + m1]);
             field_codes<BV>(v0, 2 * mi + 1, m0, m1);
-            r[1] = pack2(la[m0], la[LV + m1]);
+            r[1] = pack2(la[m0], la[TV + m1]);
             field_codes<BV>(v1, 2 * mi, m0, m1);
-            r[2] = pack2(lb[m0], lb[LV + m1]);
+            r[2] = pack2(lb[m0], lb[TV + m1]);
             field_codes<BV>(v1, 2 * mi + 1, m0, m1);
-            r[3] = pack2(lb[m0], lb[LV + m1]);
+            r[3] = pack2(lb[m0], lb[TV + m1]);
             mma_f16(st.acc[mi], r[0], r[1], r[2], r[3], b0, b1);
         }
     }
@@ -355,7 +380,7 @@ __device__ __forceinline__ void process_block_nuq(const uint8_t *kp, const uint8
             }
             if (lane < valid && c != 0xffffu) {
                 const uint32_t m = code_in_rec<BV>(vp + (lane >> 1) * PAIRV, v_idx(static_cast<int>(c), D), lane & 1, D / 8);
-                const float dlt = f16v(static_cast<uint16_t>(xb)) - f16v(lvp[lane * LV + m]);
+                const float dlt = f16v(static_cast<uint16_t>(xb)) - f16v(lvp[(lane * gv + static_cast<int>(c) * gv / D) * LV + m]);
 #pragma unroll
                 for (int h = 0; h < 4; h++) atomicAdd(&corr[h][c], pb[h][lane] * dlt);
             }
@@ -544,7 +569,7 @@ __device__ __forceinline__ void load_query(const AttnArgs &a, const AttnShape &s
 }
 
 // The (hi, lo) 16-bit halves of v into S.qh[qs][kind][0 / 1][h][c].
-template <int D, int BK, int BV, bool M16, bool NUQ>
+template <int D, int BK, int BV, bool M16, int NUQ>
 __device__ __forceinline__ void put_hilo(Smem<D, BK, BV, M16, NUQ> &S, int qs, int kind, int h, int c, float v,
                                          bool bf16) {
     const uint32_t w = bf16 ? hilo_bf16(v) : hilo_f16(v);
@@ -557,7 +582,7 @@ __device__ __forceinline__ void put_hilo(Smem<D, BK, BV, M16, NUQ> &S, int qs, i
 // rotated (or compensated) and scaled by 2^-E for the code field E that
 // channel c meets in the key operand (register c>>3 of a lane's slice); also
 // sum q and q . mu for the fold of the affine code (Eq. 8).
-template <int D, int BK, int BV, bool M16, bool NUQ>
+template <int D, int BK, int BV, bool M16, int NUQ>
 __device__ __forceinline__ void prep_query(const AttnArgs &a, const AttnShape &sh, Smem<D, BK, BV, M16, NUQ> &S,
                                            int qs, int u, const QIn<D / 32> &in) {
     constexpr int V = D / 32;
@@ -611,7 +636,7 @@ __device__ __forceinline__ void prep_query(const AttnArgs &a, const AttnShape &s
     }
     if constexpr (NUQ) {  // the unit's key tables
         constexpr int LV = Cfg<D, BK, BV, M16, NUQ>::LV;
-        const uint32_t *src = reinterpret_cast<const uint32_t *>(a.lut_k + static_cast<long long>(u) * D * LV);
+        const uint32_t *src = reinterpret_cast<const uint32_t *>(a.lut_k + static_cast<long long>(u) * a.nbk * D * LV);
         uint32_t *dst = reinterpret_cast<uint32_t *>(S.lutk[qs]);
         for (int i = threadIdx.x; i < D * LV / 2; i += blockDim.x) dst[i] = src[i];
     }
@@ -620,7 +645,7 @@ __device__ __forceinline__ void prep_query(const AttnArgs &a, const AttnShape &s
 // This lane's mma B operand of q.K^T from the prepared halves: column g of the
 // operand is head g>>1, half g&1; lane slot (k-step i, sub, e) holds channel
 // perm(i, tig, sub, e), and e = 0, 1 are adjacent channels (one 32-bit load).
-template <int D, int BK, int BV, bool M16, bool NUQ, typename Perm>
+template <int D, int BK, int BV, bool M16, int NUQ, typename Perm>
 __device__ __forceinline__ void load_qb(const Smem<D, BK, BV, M16, NUQ> &S, int qs, int kind, Perm perm,
                                         uint32_t (&qb)[D / 16][2]) {
     const int lane = threadIdx.x & 31, g = lane >> 2, tig = lane & 3;
@@ -642,7 +667,7 @@ __device__ __forceinline__ void load_qb(const Smem<D, BK, BV, M16, NUQ> &S, int 
 // for every entry (also the 16-bit tiles it leaves to another warp): a warp is
 // then never more than one phase ahead of a slot, which the parity test of the
 // wait requires.
-template <int D, int BK, int BV, bool M16, bool NUQ = false>
+template <int D, int BK, int BV, bool M16, int NUQ = 0>
 __global__ void __launch_bounds__(128, Cfg<D, BK, BV, M16, NUQ>::MINB) attn_kernel(AttnArgs a, AttnShape sh) {
     using C = Cfg<D, BK, BV, M16, NUQ>;
     constexpr int PR = C::PR, NKS = C::NKS, NST = C::NST;
@@ -800,14 +825,18 @@ __global__ void __launch_bounds__(128, Cfg<D, BK, BV, M16, NUQ>::MINB) attn_kern
                 const int wv = static_cast<int>(a.n_q) - warp * C::SUB;
                 const int ok = warp * C::SUB * C::ROWK;
                 const int ov = C::KBYTES + warp * (C::SUB / 2) * C::PAIRV;
-                const int ol = C::KBYTES + C::VBYTES + warp * C::SUB * C::LV * 2;
+                const int gv = NUQ == 2 ? a.gv : 1;
+                const int ol = C::KBYTES + C::VBYTES + warp * C::SUB * gv * C::LV * 2;
+                const bool blk_tables = NUQ == 2 && a.refit;  // key tables of the entry's refit block
 #pragma unroll 1
                 for (int q = p0; q < p1; q++) {
                     const uint8_t *slot = acquire();
                     const int valid = wv - q * C::ST;
+                    const uint16_t *lutk = blk_tables ? reinterpret_cast<const uint16_t *>(slot + C::KBYTES + C::VBYTES + C::LUTV)
+                                                      : S.lutk[qs];
                     if (valid > 0)
                         process_block_nuq<D, BK, BV>(slot + ok, slot + ov, reinterpret_cast<const uint16_t *>(slot + ol),
-                                                     valid, qb, S.lutk[qs], S.qf[qs], a.sm_log2, st, S.corr[warp],
+                                                     gv, valid, qb, lutk, S.qf[qs], a.sm_log2, st, S.corr[warp],
                                                      S.pb[warp], a, sh, u,
                                                      static_cast<long long>(q) * C::ST + warp * C::SUB);
                     release();
@@ -880,7 +909,7 @@ __global__ void __launch_bounds__(128) combine_kernel(AttnArgs a, AttnShape sh) 
 }
 
 // ---- host side -------------------------------------------------------------
-template <int D, int BK, int BV, bool M16, bool NUQ = false>
+template <int D, int BK, int BV, bool M16, int NUQ = 0>
 struct Launcher {
     static constexpr int ST = Cfg<D, BK, BV, M16, NUQ>::ST;
     static int occupancy;  // resident CTAs per SM, set on first use
@@ -914,7 +943,7 @@ struct Launcher {
         return static_cast<int>(cudaLaunchKernelEx(&lc, combine_kernel<D>, a, sh));
     }
 };
-template <int D, int BK, int BV, bool M16, bool NUQ>
+template <int D, int BK, int BV, bool M16, int NUQ>
 int Launcher<D, BK, BV, M16, NUQ>::occupancy = 0;
 
 template <int D, bool M16, typename F>
@@ -927,14 +956,19 @@ static int dispatch_bits(const Layout &L, F &&f) {
 
 template <typename F>
 static int dispatch(const Layout &L, F &&f) {
-    if (L.scheme == DQ_NUQ) {  // no meta: one instantiation per (d, bits)
-        if (L.d == 128) {
-            if (L.bits_k == 2) return f(Launcher<128, 2, 2, true, true>());
-            if (L.bits_k == 3) return f(Launcher<128, 3, 3, true, true>());
-            return f(Launcher<128, 4, 4, true, true>());
+    if (L.scheme == DQ_NUQ) {  // no meta: one instantiation per (d, bits, table kind)
+        if (L.d == 128 && (L.gv > 1 || L.refit > 0)) {
+            if (L.bits_k == 2) return f(Launcher<128, 2, 2, true, 2>());
+            if (L.bits_k == 3) return f(Launcher<128, 3, 3, true, 2>());
+            return f(Launcher<128, 4, 4, true, 2>());
         }
-        if (L.bits_k == 2) return f(Launcher<64, 2, 2, true, true>());
-        return f(Launcher<64, 4, 4, true, true>());
+        if (L.d == 128) {
+            if (L.bits_k == 2) return f(Launcher<128, 2, 2, true, 1>());
+            if (L.bits_k == 3) return f(Launcher<128, 3, 3, true, 1>());
+            return f(Launcher<128, 4, 4, true, 1>());
+        }
+        if (L.bits_k == 2) return f(Launcher<64, 2, 2, true, 1>());
+        return f(Launcher<64, 4, 4, true, 1>());
     }
     const bool m16 = L.meta_bytes == 2;
     if (L.d == 128) return m16 ? dispatch_bits<128, true>(L, f) : dispatch_bits<128, false>(L, f);

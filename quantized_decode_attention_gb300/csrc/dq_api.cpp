@@ -57,6 +57,17 @@ dq_status validate_tensor(const dq_tensor_cfg &t, int d, bool key, const char *n
         if (t.lloyd_iters < 0 || t.lloyd_iters > 64) return fail(DQ_EINVAL, "%s: lloyd_iters outside [0, 64]", name);
         if (!(t.outlier_frac >= 0.0f && t.outlier_frac < 0.5f))
             return fail(DQ_EINVAL, "%s: outlier_frac outside [0, 0.5)", name);
+        if (key && t.group_size != 0)
+            return fail(DQ_EUNSUPPORTED, "%s: a key table spans its channel's tokens (group_size 0)", name);
+        if (!key && t.group_size != 0 && t.group_size != 32 && t.group_size != d)
+            return fail(DQ_EUNSUPPORTED, "%s: group_size must be 0, 32 or head_dim (got %d)", name, t.group_size);
+        if (!key && t.refit_interval != 0) return fail(DQ_EINVAL, "%s: refit_interval is for keys", name);
+        if (t.refit_interval < 0 || t.refit_interval % 128)
+            return fail(DQ_EINVAL, "%s: refit_interval must be 0 or a positive multiple of 128", name);
+        if (((t.group_size != 0 && t.group_size != d) || t.refit_interval > 0) && d != 128)
+            return fail(DQ_EUNSUPPORTED, "%s: value groups and key refit blocks need head_dim 128", name);
+    } else if (t.group_size != 0 || t.refit_interval != 0) {
+        return fail(DQ_EINVAL, "%s: group_size and refit_interval are for the non-uniform scheme", name);
     }
     if (t.bits == 3 && d != 128) return fail(DQ_EUNSUPPORTED, "%s: 3-bit records need head_dim 128", name);
     if (t.rot < DQ_ROT_NONE || t.rot > DQ_ROT_DENSE) return fail(DQ_EINVAL, "%s: bad rotation %d", name, t.rot);
@@ -164,6 +175,9 @@ void set_nuq_args(const Layout &L, const dq_kv_buffers *b, AttnArgs &a) {
     }
     a.rp_stride = L.rp_stride;
     a.nnzk_cap = L.nnzk_cap;
+    a.gv = L.gv;
+    a.refit = L.refit;
+    a.nbk = L.nbk;
 }
 
 dq_status set_last_error(dq_status s, const char *msg) {
@@ -203,6 +217,13 @@ dq_status make_layout(const dq_config *cfg, Layout *L) {
     if (c.k.scheme == DQ_NUQ && c.max_seq - c.n_sink > 8192)
         return fail(DQ_EUNSUPPORTED, "non-uniform key fit: at most 8192 quantized tokens (got %d)",
                     c.max_seq - c.n_sink);
+    if (c.k.scheme == DQ_NUQ && c.k.refit_interval > 0) {
+        if (c.n_recent < c.k.refit_interval)
+            return fail(DQ_EUNSUPPORTED, "key refit blocks: n_recent (%d) must hold a block (%d)", c.n_recent,
+                        c.k.refit_interval);
+        if (c.kv_dtype == DQ_F32)
+            return fail(DQ_EUNSUPPORTED, "key refit blocks read the recent window back: kv_dtype must be 16-bit");
+    }
 
     Layout &l = *L;
     std::memset(&l, 0, sizeof l);
@@ -230,6 +251,9 @@ dq_status make_layout(const dq_config *cfg, Layout *L) {
         l.nnzk_cap = round_up(2LL * static_cast<long long>(d) * l.k_out_cap, 8);  // room for decode keys
         l.k_out_v = dq::nuq_outlier_count(c.v.outlier_frac, c.head_dim);
         l.rp_stride = l.qcap + 4;
+        l.gv = c.v.group_size == 0 ? 1 : c.head_dim / c.v.group_size;
+        l.refit = c.k.refit_interval;
+        l.nbk = l.refit > 0 ? (l.qcap + l.refit - 1) / l.refit : 1;
     }
     l.sz[0] = U * l.qcap * l.rowK;                          // codes_k
     l.sz[1] = U * (l.qcap / 2) * l.pairV;                   // codes_v
@@ -237,8 +261,8 @@ dq_status make_layout(const dq_config *cfg, Layout *L) {
                   : U * l.qcap * 2 * l.meta_bytes;
     l.sz[3] = nuq ? 0 : U * l.qcap * 2 * l.meta_bytes;      // meta_v
     l.sz[4] = c.k.mean ? U * d * 4 : 0;                     // mean_k
-    l.sz[5] = nuq ? U * d * l.levels * 2 : 0;               // lut_k
-    l.sz[6] = nuq ? U * l.qcap * l.levels * 2 : 0;          // lut_v
+    l.sz[5] = nuq ? U * static_cast<size_t>(l.nbk) * d * l.levels * 2 + (l.refit > 0 ? U * 4 : 0) : 0;  // lut_k
+    l.sz[6] = nuq ? U * l.qcap * l.gv * l.levels * 2 : 0;   // lut_v
     l.sz[7] = U * l.rcap * d * 2;                           // raw_k
     l.sz[8] = U * l.rcap * d * 2;                           // raw_v
     for (int i = 9; i < 15; i++) l.sz[i] = 0;               // outlier side-channels
@@ -348,6 +372,7 @@ static dq_status get_ctx(dq_ctx **pctx, const dq_config *cfg, const Layout &L) {
         cudaFree(c->partials);
         cudaFree(c->counters);
         cudaFree(c->nuq_bits);
+        cudaFree(c->nuq_scr);
         cudaFree(c->rans);
         cudaFree(c->rans_partials);
         cudaFree(c->q_tilde);
@@ -427,6 +452,14 @@ static dq_status quantize_nuq(dq_ctx *c, const dq_config *cfg, const Layout &L, 
     a.thr = L.k_out_cap > 0 ? static_cast<float *>(bufs->meta_k) : nullptr;
     a.k_out = dq::nuq_outlier_count(cfg->k.outlier_frac, a.n_fit);
     a.iters = cfg->k.lloyd_iters;
+    const long long N = L.refit;
+    if (N > 0)  // the prefill's quantized slot count per unit follows the tables
+        a.pq = reinterpret_cast<int *>(static_cast<uint8_t *>(bufs->lut_k) +
+                                       static_cast<size_t>(L.U) * L.nbk * L.d * L.levels * 2);
+    a.fit_t0 = L.n_sink;
+    a.fit_slot0 = 0;
+    a.fit_blk = 0;
+    a.fit_nblk = N > 0 ? static_cast<int>((a.n_fit + N - 1) / N) : 1;  // every block the prefill reaches
     if (!append) {
         if (cudaMemsetAsync(c->nuq_bits, 0, static_cast<size_t>(L.U) * L.qcap * (L.d / 32) * sizeof(uint32_t), st) !=
             cudaSuccess)
@@ -434,8 +467,48 @@ static dq_status quantize_nuq(dq_ctx *c, const dq_config *cfg, const Layout &L, 
         if (a.n_fit > 0 && (e = dq::launch_nuq_key_fit(L, a, stream)) != 0)
             return fail(DQ_ECUDA, "key fit launch: %s", cudaGetErrorString(static_cast<cudaError_t>(e)));
     }
+    // refit blocks that this append completes: [fb_lo, fb_hi); their keys are
+    // gathered before this call's keys overwrite the recent window
+    const long long s_lo = pos0 - L.n_sink, s_hi = s_lo + n_tok;
+    const long long fb_lo = (append && N > 0) ? s_lo / N : 0, fb_hi = (append && N > 0) ? s_hi / N : 0;
+    if (fb_hi > fb_lo) {
+        a.scr_lo = fb_lo * N;
+        a.scr_n = static_cast<int>((fb_hi - fb_lo) * N);
+        const size_t need = static_cast<size_t>(L.U) * a.scr_n * L.d;
+        if (c->nuq_scr_cap < need) {
+            cudaFree(c->nuq_scr);
+            c->nuq_scr = nullptr;
+            c->nuq_scr_cap = 0;
+            if (cudaMalloc(&c->nuq_scr, need * sizeof(float)) != cudaSuccess)
+                return fail(DQ_ENOMEM, "key refit scratch (%zu bytes)", need * sizeof(float));
+            c->nuq_scr_cap = need;
+        }
+        a.scr = c->nuq_scr;
+        if ((e = dq::launch_nuq_gather(L, a, stream)) != 0)
+            return fail(DQ_ECUDA, "key refit gather launch: %s", cudaGetErrorString(static_cast<cudaError_t>(e)));
+    }
     if ((e = dq::launch_nuq_key_codes(L, a, stream)) != 0)
         return fail(DQ_ECUDA, "key quantize launch: %s", cudaGetErrorString(static_cast<cudaError_t>(e)));
+    if (fb_hi > fb_lo) {
+        for (long long b = fb_lo; b < fb_hi; b++) {  // per block: rank outliers, Lloyd fit, tables
+            dq::QuantArgs f = a;
+            f.x = a.scr;
+            f.in_dtype = DQ_F32;
+            f.n_tok = a.scr_n;
+            f.fit_t0 = (b - fb_lo) * N;
+            f.fit_slot0 = b * N;
+            f.n_fit = static_cast<int>(N);
+            f.k_out = dq::nuq_outlier_count(cfg->k.outlier_frac, static_cast<int>(N));
+            f.fit_blk = static_cast<int>(b);
+            f.fit_nblk = 1;
+            f.fit_flush = 1;
+            if ((e = dq::launch_nuq_key_fit(L, f, stream)) != 0)
+                return fail(DQ_ECUDA, "key refit launch: %s", cudaGetErrorString(static_cast<cudaError_t>(e)));
+        }
+        if ((e = dq::launch_nuq_block_codes(L, a, stream)) != 0)
+            return fail(DQ_ECUDA, "key refit codes launch: %s", cudaGetErrorString(static_cast<cudaError_t>(e)));
+        // the side-channel kernel extends its rows back to the first recoded slot
+    }
     if (L.k_out_cap > 0 && (e = dq::launch_nuq_key_csr(L, a, stream)) != 0)
         return fail(DQ_ECUDA, "key side-channel launch: %s", cudaGetErrorString(static_cast<cudaError_t>(e)));
     return ok();
@@ -905,6 +978,7 @@ void dq_free(dq_ctx *ctx) {
     cudaFree(ctx->partials);
     cudaFree(ctx->counters);
     cudaFree(ctx->nuq_bits);
+    cudaFree(ctx->nuq_scr);
     cudaFree(ctx->rans);
     cudaFree(ctx->drift_stats);
     cudaFree(ctx->rans_sym);

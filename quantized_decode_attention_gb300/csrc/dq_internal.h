@@ -30,6 +30,9 @@ struct Layout {
     long long nnzk_cap;  // key side-channel entries per unit (multiple of 8): twice the longest prefill's
     int k_out_v;         // value outliers per token
     long long rp_stride; // ints per unit of the key row pointers (qcap + 4)
+    int gv;              // value tables per token (head_dim / group_size)
+    int refit;           // key table block in quantized slots (0: one frozen block)
+    long long nbk;       // key table blocks per unit
     // entropy-coded scheme (scheme == DQ_RANS): one stream per token and tensor
     int n_stream;        // values per stream = Hkv * d
     int ck, cv;          // container bytes of a key / value stream
@@ -147,7 +150,7 @@ struct QuantArgs {
     uint16_t *raw;          // raw_k or raw_v
     unsigned *status;
     // non-uniform scheme
-    uint16_t *lut;          // keys [U][d][L], values [U][Qcap][L] fp16 tables
+    uint16_t *lut;          // keys [U][nbk][d][L], values [U][Qcap][gv][L] fp16 tables
     uint32_t *olbits;       // keys: [U][Qcap][d/32] outlier bitmap (scratch, zeroed first)
     int *ol_rowptr;         // keys: [U][rp_stride] row pointers by quantized slot
     uint16_t *ol_col, *ol_val;  // keys: [U][nnzk_cap]; values: [U][Qcap][k_out_v]
@@ -157,6 +160,19 @@ struct QuantArgs {
     float *thr;             // keys: [U][d] outlier thresholds frozen at prefill (fp32 magnitudes)
     long long slot_lo;      // first quantized slot written by this call
     int n_slots;            // quantized slots written by this call
+    // key refit blocks (Layout::refit > 0): the prefill's quantized slot count
+    // per unit (a block starting at or after it holds decode keys only)
+    int *pq;                // [U]
+    // key fit: input rows [fit_t0, fit_t0 + n_fit) of each unit are quantized
+    // slots [fit_slot0, ...); the table goes to blocks [fit_blk, fit_blk +
+    // fit_nblk); fit_flush: a refit block, skipped where the prefill reached it
+    long long fit_t0, fit_slot0;
+    int fit_blk, fit_nblk, fit_flush;
+    // block flush: fp32 keys of quantized slots [scr_lo, scr_lo + scr_n) per
+    // unit, [U][scr_n][d], gathered from the input and the recent window
+    float *scr;
+    long long scr_lo;
+    int scr_n;
     // byte sizes of the buffers above (the checked build tests accesses against them)
     long long sz_x, sz_codes, sz_meta, sz_mean, sz_raw;
 };
@@ -200,7 +216,10 @@ struct AttnArgs {
     int *counters;          // [U] CTAs done with the unit; zero between calls
     unsigned *status;
     // non-uniform scheme
-    const uint16_t *lut_k, *lut_v;        // [U][d][L] / [U][Qcap][L] fp16 tables
+    const uint16_t *lut_k, *lut_v;        // [U][nbk][d][L] / [U][Qcap][gv][L] fp16 tables
+    int gv;                               // value tables per token
+    int refit;                            // key table block in slots (0: one block)
+    long long nbk;                        // key table blocks per unit
     const int *ol_rowptr_k;               // [U][rp_stride] key side-channel rows by slot (or null)
     const uint16_t *ol_col_k, *ol_val_k;  // [U][nnzk_cap]
     const uint16_t *ol_col_v, *ol_val_v;  // [U][Qcap][k_out_v]
@@ -265,6 +284,9 @@ int launch_nuq_values(const Layout &L, const QuantArgs &a, void *stream);
 int launch_nuq_key_fit(const Layout &L, const QuantArgs &a, void *stream);
 int launch_nuq_key_codes(const Layout &L, const QuantArgs &a, void *stream);
 int launch_nuq_key_csr(const Layout &L, const QuantArgs &a, void *stream);
+// key refit blocks: gather the keys of a.scr's slots, code the gathered blocks
+int launch_nuq_gather(const Layout &L, const QuantArgs &a, void *stream);
+int launch_nuq_block_codes(const Layout &L, const QuantArgs &a, void *stream);
 int nuq_outlier_count(float f, int n);
 int launch_dequant(const Layout &L, const DequantArgs &a, void *stream);
 int launch_attention(const Layout &L, const AttnArgs &a, int num_sms, void *stream);
@@ -301,6 +323,8 @@ struct dq_ctx {
     int *counters;       // [U]
     int counters_dirty;  // set by dq_check after a timeout: clear the counts before the next call
     uint32_t *nuq_bits;  // non-uniform scheme: key outlier bitmap scratch [U][Qcap][d/32]
+    float *nuq_scr;      // non-uniform scheme, key refit blocks: gathered keys
+    size_t nuq_scr_cap;  // floats
     dq::RansDevTables *rans;  // entropy-coded scheme: symbol models (device)
     uint8_t *rans_sym;   // entropy-coded scheme: symbol scratch of a prefill
     float *rans_partials;  // entropy-coded scheme: attention item records

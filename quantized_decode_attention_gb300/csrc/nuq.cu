@@ -15,6 +15,11 @@
 //    channel's k-th rank outlier): |x| >= threshold goes to the side channel,
 //    appended in token order while it has room.  Decode values are fitted per
 //    token like prefill values.
+//  * Configuration reference: kvquant_group_size splits a value token's fit
+//    into groups of consecutive channels (outliers still ranked over the
+//    token); kvquant_refit_interval N gives the key tables blocks of N
+//    quantized slots, a block of decode keys fitted on its own keys, as a
+//    prefill of them, by the append that completes it.
 // The fit follows one fixed arithmetic order so that the tables are bit-exact:
 // level sums in the R32 order (lane l = position mod 32 adds its positions in
 // increasing order, then a xor butterfly), sum / count in fp32, fp16 table,
@@ -135,7 +140,10 @@ __global__ void __launch_bounds__(256) nuq_key_fit_kernel(QuantArgs a, Layout L,
     __shared__ float seed[LV];
     const int u = blockIdx.x / D, c = blockIdx.x % D;
     const int n = a.n_fit, k = a.k_out;
-    const long long base = (static_cast<long long>(u) * a.n_tok + L.n_sink) * D + c;
+    // a refit block the prefill reached keeps the prefill's tables
+    if (a.fit_flush && static_cast<long long>(a.fit_blk) * L.refit < a.pq[u]) return;
+    if (a.pq && !a.fit_flush && c == 0 && threadIdx.x == 0) a.pq[u] = n;
+    const long long base = (static_cast<long long>(u) * a.n_tok + a.fit_t0) * D + c;
     bool finite = true;
     for (int p = threadIdx.x; p < n2; p += blockDim.x) {
         if (p < n) {
@@ -155,10 +163,10 @@ __global__ void __launch_bounds__(256) nuq_key_fit_kernel(QuantArgs a, Layout L,
     for (int r = threadIdx.x; r < k; r += blockDim.x) {
         const int p = static_cast<int>(0xffffffffu - static_cast<uint32_t>(keys[r]));
         atomicOr(&outmask[p >> 5], 1u << (p & 31));
-        atomicOr(&a.olbits[(static_cast<long long>(u) * L.qcap + p) * (D / 32) + c / 32], 1u << (c & 31));
+        atomicOr(&a.olbits[(static_cast<long long>(u) * L.qcap + a.fit_slot0 + p) * (D / 32) + c / 32], 1u << (c & 31));
     }
     // the threshold decode keys are screened against: the k-th largest magnitude
-    if (threadIdx.x == 0 && a.thr)
+    if (threadIdx.x == 0 && a.thr && !a.fit_flush)
         a.thr[static_cast<long long>(u) * D + c] = k > 0 ? __uint_as_float(static_cast<uint32_t>(keys[k - 1] >> 32)) : INFINITY;
     __syncthreads();
     // quantile seeds: sort the fit values (outliers and padding sort last)
@@ -180,7 +188,9 @@ __global__ void __launch_bounds__(256) nuq_key_fit_kernel(QuantArgs a, Layout L,
 #pragma unroll
             for (int i = 1; i < LV; i++)
                 if (threadIdx.x == i) mine = lev[i];
-            a.lut[(static_cast<long long>(u) * D + c) * LV + threadIdx.x] = __half_as_ushort(__float2half_rn(mine));
+            const uint16_t h = __half_as_ushort(__float2half_rn(mine));
+            for (int b = a.fit_blk; b < a.fit_blk + a.fit_nblk; b++)
+                a.lut[((static_cast<long long>(u) * L.nbk + b) * D + c) * LV + threadIdx.x] = h;
         }
     }
 }
@@ -257,86 +267,101 @@ __global__ void __launch_bounds__(128) nuq_value_kernel(QuantArgs a, Layout L) {
         for (int j = 0; j < V; j++)
             if (lane + 32 * j == c) out[j] = true;
     }
-    // quantile seeds: rank of each fit value (equal keys ordered by channel)
-    const int nf = D - a.k_out;
+    // per group of g = D / gv consecutive channels (the whole token when gv = 1):
+    // quantile seeds from the ranks of the group's fit values (equal keys
+    // ordered by channel), Lloyd sweeps over the group's positions in the R32
+    // order (lane l holds positions l, l + 32, ... of the group in register
+    // order), its fp16 table, and the codes of its channels
 #pragma unroll
     for (int j = 0; j < V; j++) wk[warp][lane + 32 * j] = out[j] ? 0xffffffffu : ord_key(x[j]);
     __syncwarp();
-    float lev[LV];
-#pragma unroll
-    for (int i = 0; i < LV; i++) lev[i] = 0.f;
-    if (nf > 0) {
-        int rank[V];
+    const int gv = L.gv, g = D / gv;
+    const long long ts = static_cast<long long>(u) * L.qcap + slot;
+    uint32_t m[V];
+    for (int G = 0; G < gv; G++) {
+        bool in[V];
+        int nout = 0;
 #pragma unroll
         for (int j = 0; j < V; j++) {
-            const uint32_t kj = wk[warp][lane + 32 * j];
-            int r = 0;
-            for (int p = 0; p < D; p++) {
-                const uint32_t kp = wk[warp][p];
-                r += (kp < kj) || (kp == kj && p < lane + 32 * j);
-            }
-            rank[j] = out[j] ? -1 : r;
+            in[j] = (lane + 32 * j) / g == G;
+            nout += __popc(__ballot_sync(FULL, in[j] && out[j]));
         }
+        const int nf = g - nout;
+        float lev[LV];
 #pragma unroll
-        for (int i = 0; i < LV; i++) {
-            const int target = (2 * i + 1) * nf / (2 * LV);
-            float mine = 0.f;
-            bool have = false;
-#pragma unroll
-            for (int j = 0; j < V; j++)
-                if (rank[j] == target) {
-                    mine = ord_val(ord_key(x[j]));
-                    have = true;
-                }
-            const unsigned m = __ballot_sync(FULL, have);
-            lev[i] = __shfl_sync(FULL, mine, __ffs(m) - 1);
-        }
-        // Lloyd sweeps, R32 order
-        for (int it = 0; it < a.iters; it++) {
-            float sum[LV];
-            int cnt[LV];
-#pragma unroll
-            for (int i = 0; i < LV; i++) {
-                sum[i] = 0.f;
-                cnt[i] = 0;
-            }
+        for (int i = 0; i < LV; i++) lev[i] = 0.f;
+        if (nf > 0) {
+            int rank[V];
 #pragma unroll
             for (int j = 0; j < V; j++) {
-                if (out[j]) continue;
-                const int q = nearest<LV>(x[j], lev);
-#pragma unroll
-                for (int i = 0; i < LV; i++)
-                    if (q == i) {
-                        sum[i] = __fadd_rn(sum[i], x[j]);
-                        cnt[i]++;
-                    }
+                const uint32_t kj = wk[warp][lane + 32 * j];
+                int r = 0;
+                for (int p = G * g; p < G * g + g; p++) {
+                    const uint32_t kp = wk[warp][p];
+                    r += (kp < kj) || (kp == kj && p < lane + 32 * j);
+                }
+                rank[j] = (out[j] || !in[j]) ? -1 : r;
             }
 #pragma unroll
             for (int i = 0; i < LV; i++) {
+                const int target = (2 * i + 1) * nf / (2 * LV);
+                float mine = 0.f;
+                bool have = false;
 #pragma unroll
-                for (int off = 16; off; off >>= 1) {
-                    sum[i] = __fadd_rn(sum[i], __shfl_xor_sync(FULL, sum[i], off));
-                    cnt[i] += __shfl_xor_sync(FULL, cnt[i], off);
+                for (int j = 0; j < V; j++)
+                    if (rank[j] == target) {
+                        mine = ord_val(ord_key(x[j]));
+                        have = true;
+                    }
+                const unsigned mk = __ballot_sync(FULL, have);
+                lev[i] = __shfl_sync(FULL, mine, __ffs(mk) - 1);
+            }
+            // Lloyd sweeps, R32 order
+            for (int it = 0; it < a.iters; it++) {
+                float sum[LV];
+                int cnt[LV];
+#pragma unroll
+                for (int i = 0; i < LV; i++) {
+                    sum[i] = 0.f;
+                    cnt[i] = 0;
                 }
-                if (cnt[i] > 0) lev[i] = __fdiv_rn(sum[i], static_cast<float>(cnt[i]));
+#pragma unroll
+                for (int j = 0; j < V; j++) {
+                    if (out[j] || !in[j]) continue;
+                    const int q = nearest<LV>(x[j], lev);
+#pragma unroll
+                    for (int i = 0; i < LV; i++)
+                        if (q == i) {
+                            sum[i] = __fadd_rn(sum[i], x[j]);
+                            cnt[i]++;
+                        }
+                }
+#pragma unroll
+                for (int i = 0; i < LV; i++) {
+#pragma unroll
+                    for (int off = 16; off; off >>= 1) {
+                        sum[i] = __fadd_rn(sum[i], __shfl_xor_sync(FULL, sum[i], off));
+                        cnt[i] += __shfl_xor_sync(FULL, cnt[i], off);
+                    }
+                    if (cnt[i] > 0) lev[i] = __fdiv_rn(sum[i], static_cast<float>(cnt[i]));
+                }
             }
         }
+        // fp16 table; codes against it
+        float lev16[LV];
+#pragma unroll
+        for (int i = 0; i < LV; i++) lev16[i] = __half2float(__float2half_rn(lev[i]));
+        if (lane < LV) {
+            float mine = lev16[0];
+#pragma unroll
+            for (int i = 1; i < LV; i++)
+                if (lane == i) mine = lev16[i];
+            a.lut[(ts * gv + G) * LV + lane] = __half_as_ushort(__float2half_rn(mine));
+        }
+#pragma unroll
+        for (int j = 0; j < V; j++)
+            if (in[j]) m[j] = static_cast<uint32_t>(nearest<LV>(x[j], lev16));
     }
-    // fp16 table; codes against it
-    float lev16[LV];
-#pragma unroll
-    for (int i = 0; i < LV; i++) lev16[i] = __half2float(__float2half_rn(lev[i]));
-    const long long ts = static_cast<long long>(u) * L.qcap + slot;
-    if (lane < LV) {
-        float mine = lev16[0];
-#pragma unroll
-        for (int i = 1; i < LV; i++)
-            if (lane == i) mine = lev16[i];
-        a.lut[ts * LV + lane] = __half_as_ushort(__float2half_rn(mine));
-    }
-    uint32_t m[V];
-#pragma unroll
-    for (int j = 0; j < V; j++) m[j] = static_cast<uint32_t>(nearest<LV>(x[j], lev16));
     // pack this token's half of its value pair record
     constexpr int WV = Rec<D, BITS>::V_WORDS, WLO = 2 * D * 2 / 32;
     const int e = static_cast<int>(slot & 1);
@@ -366,8 +391,38 @@ __global__ void __launch_bounds__(128) nuq_value_kernel(QuantArgs a, Layout L) {
     }
 }
 
+// A key row's codes m[j] (channel lane + 32 j) packed into its record.
+template <int V, int BITS>
+__device__ __forceinline__ void store_key_row(const uint32_t (&m)[V], uint32_t *row) {
+    constexpr int D = 32 * V, WK = Rec<D, BITS>::K_WORDS, WLO = D * 2 / 32;
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int w = 0; w < WK; w++) {
+        uint32_t v = 0;
+#pragma unroll
+        for (int j = 0; j < V; j++) {
+            const int c = lane + 32 * j;
+            v |= contrib<D, BITS>(w, k_idx(c, D), c & 1, m[j], WLO);
+        }
+        v = __reduce_or_sync(FULL, v);
+        if (lane == w) row[w] = v;
+    }
+}
+
+// Nearest level of x in channel c's table of block `blk`.
+template <int D, int LV>
+__device__ __forceinline__ uint32_t key_code(const QuantArgs &a, const Layout &L, int u, long long blk, int c, float x) {
+    float lev[LV];
+    const uint16_t *t = a.lut + ((static_cast<long long>(u) * L.nbk + blk) * D + c) * LV;
+#pragma unroll
+    for (int i = 0; i < LV; i++) lev[i] = __half2float(__ushort_as_half(t[i]));
+    return static_cast<uint32_t>(nearest<LV>(x, lev));
+}
+
 // ---------------------------------------------------------------------------
-// Key codes against the per-channel tables: one warp per (unit, token).
+// Key codes against the per-channel tables: one warp per (unit, token).  With
+// refit blocks, a token of a block of decode keys only is not coded here: it
+// stays in the 16-bit recent window until its block completes.
 // ---------------------------------------------------------------------------
 template <int V, int BITS>
 __global__ void __launch_bounds__(128) nuq_key_code_kernel(QuantArgs a, Layout L) {
@@ -383,34 +438,73 @@ __global__ void __launch_bounds__(128) nuq_key_code_kernel(QuantArgs a, Layout L
     if (t < L.n_sink) return;
     const long long slot = t - L.n_sink;
     const bool screen = a.pos0 > 0 && a.thr != nullptr;  // decode keys: outliers by the frozen threshold
+    const long long blk = L.refit ? slot / L.refit : 0;
+    if (L.refit && blk * L.refit >= a.pq[u]) {          // coded when its block completes
+        if (screen && lane < V) a.olbits[(static_cast<long long>(u) * L.qcap + slot) * V + lane] = 0u;
+        return;
+    }
     uint32_t m[V];
 #pragma unroll
     for (int j = 0; j < V; j++) {
         const int c = lane + 32 * j;
         const float x = ld_in(a.x, base + c, a.in_dtype);
-        float lev[LV];
-#pragma unroll
-        for (int i = 0; i < LV; i++)
-            lev[i] = __half2float(__ushort_as_half(a.lut[(static_cast<long long>(u) * D + c) * LV + i]));
-        m[j] = static_cast<uint32_t>(nearest<LV>(x, lev));
+        m[j] = key_code<D, LV>(a, L, u, blk, c, x);
         if (screen) {
             const unsigned ob = __ballot_sync(FULL, fabsf(x) >= a.thr[static_cast<long long>(u) * D + c]);
             if (lane == 0) a.olbits[(static_cast<long long>(u) * L.qcap + slot) * V + j] = ob;
         }
     }
-    constexpr int WK = Rec<D, BITS>::K_WORDS, WLO = D * 2 / 32;
-    uint32_t *row = reinterpret_cast<uint32_t *>(a.codes + (static_cast<long long>(u) * L.qcap + slot) * L.rowK);
+    store_key_row<V, BITS>(m, reinterpret_cast<uint32_t *>(a.codes + (static_cast<long long>(u) * L.qcap + slot) * L.rowK));
+}
+
+// ---------------------------------------------------------------------------
+// Key refit blocks.  Gather: the fp32 keys of quantized slots [scr_lo, scr_lo
+// + scr_n) of every unit, one warp per (unit, slot), from this call's input or,
+// for a token older than the call, from its 16-bit recent-window slot (exact:
+// refit caches take 16-bit keys); their outlier bits are cleared for the fit.
+// ---------------------------------------------------------------------------
+template <int V>
+__global__ void __launch_bounds__(128) nuq_gather_kernel(QuantArgs a, Layout L) {
+    constexpr int D = 32 * V, WPB = 4;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const long long gw = static_cast<long long>(blockIdx.x) * WPB + warp;
+    if (gw >= static_cast<long long>(L.U) * a.scr_n) return;
+    const int u = static_cast<int>(gw / a.scr_n);
+    const long long j = gw % a.scr_n, slot = a.scr_lo + j, t = slot + L.n_sink;
+    float *dst = a.scr + (static_cast<long long>(u) * a.scr_n + j) * D;
 #pragma unroll
-    for (int w = 0; w < WK; w++) {
-        uint32_t v = 0;
-#pragma unroll
-        for (int j = 0; j < V; j++) {
-            const int c = lane + 32 * j;
-            v |= contrib<D, BITS>(w, k_idx(c, D), c & 1, m[j], WLO);
+    for (int i = 0; i < V; i++) {
+        const int c = lane + 32 * i;
+        float x;
+        if (t >= a.pos0) {
+            x = ld_in(a.x, (static_cast<long long>(u) * a.n_tok + (t - a.pos0)) * D + c, a.in_dtype);
+        } else {
+            const uint16_t r = a.raw[(static_cast<long long>(u) * L.rcap + L.n_sink + t % L.n_recent) * D + c];
+            x = a.in_dtype == DQ_BF16 ? __bfloat162float(__ushort_as_bfloat16(r)) : __half2float(__ushort_as_half(r));
         }
-        v = __reduce_or_sync(FULL, v);
-        if (lane == w) row[w] = v;
+        dst[c] = x;
     }
+    // a block of decode keys only gets its outliers from its fit; the bits of
+    // a block the prefill reached stay as they are
+    if (lane < V && slot / L.refit * L.refit >= a.pq[u]) a.olbits[(static_cast<long long>(u) * L.qcap + slot) * V + lane] = 0u;
+}
+
+// Codes of the gathered slots whose block holds decode keys only, against the
+// block's freshly fitted tables: one warp per (unit, slot).
+template <int V, int BITS>
+__global__ void __launch_bounds__(128) nuq_block_code_kernel(QuantArgs a, Layout L) {
+    constexpr int D = 32 * V, LV = 1 << BITS, WPB = 4;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const long long gw = static_cast<long long>(blockIdx.x) * WPB + warp;
+    if (gw >= static_cast<long long>(L.U) * a.scr_n) return;
+    const int u = static_cast<int>(gw / a.scr_n);
+    const long long j = gw % a.scr_n, slot = a.scr_lo + j, blk = slot / L.refit;
+    if (blk * L.refit < a.pq[u]) return;               // coded with the prefill's tables
+    const float *src = a.scr + (static_cast<long long>(u) * a.scr_n + j) * D;
+    uint32_t m[V];
+#pragma unroll
+    for (int i = 0; i < V; i++) m[i] = key_code<D, LV>(a, L, u, blk, lane + 32 * i, src[lane + 32 * i]);
+    store_key_row<V, BITS>(m, reinterpret_cast<uint32_t *>(a.codes + (static_cast<long long>(u) * L.qcap + slot) * L.rowK));
 }
 
 // ---------------------------------------------------------------------------
@@ -425,8 +519,17 @@ template <int D>
 __global__ void __launch_bounds__(256) nuq_key_csr_kernel(QuantArgs a, Layout L) {
     constexpr int W = D / 32;
     __shared__ int part[256];
-    const int u = blockIdx.x, n = a.n_slots;
-    const long long s0 = a.slot_lo, cap = L.nnzk_cap;
+    const int u = blockIdx.x;
+    long long s0 = a.slot_lo;
+    int n = a.n_slots;
+    if (a.scr) {  // refit blocks flushed by this call: rows rebuilt from the first slot they recoded
+        const long long f0 = max(a.scr_lo, (static_cast<long long>(a.pq[u]) + L.refit - 1) / L.refit * L.refit);
+        if (f0 < s0) {
+            n += static_cast<int>(s0 - f0);
+            s0 = f0;
+        }
+    }
+    const long long cap = L.nnzk_cap;
     const int chunk = (n + blockDim.x - 1) / blockDim.x;
     const int p0 = min(n, static_cast<int>(threadIdx.x) * chunk), p1 = min(n, p0 + chunk);
     const uint32_t *bits = a.olbits + (static_cast<long long>(u) * L.qcap + s0) * W;
@@ -458,9 +561,14 @@ __global__ void __launch_bounds__(256) nuq_key_csr_kernel(QuantArgs a, Layout L)
                 const int c = 32 * w + __ffs(b) - 1;
                 b &= b - 1;
                 if (run < cap) {
-                    const long long xi = (static_cast<long long>(u) * a.n_tok + (s0 + p + L.n_sink - a.pos0)) * D + c;
+                    const long long sl = s0 + p;
+                    float x;
+                    if (a.scr && sl >= a.scr_lo && sl < a.scr_lo + a.scr_n)
+                        x = a.scr[(static_cast<long long>(u) * a.scr_n + (sl - a.scr_lo)) * D + c];
+                    else
+                        x = ld_in(a.x, (static_cast<long long>(u) * a.n_tok + (sl + L.n_sink - a.pos0)) * D + c, a.in_dtype);
                     col[run] = static_cast<uint16_t>(c);
-                    val[run] = __half_as_ushort(__float2half_rn(ld_in(a.x, xi, a.in_dtype)));
+                    val[run] = __half_as_ushort(__float2half_rn(x));
                 }
                 run++;
             }
@@ -513,6 +621,23 @@ int launch_nuq_key_fit(const Layout &L, const QuantArgs &a, void *stream) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
         if (e != cudaSuccess) return static_cast<int>(e);
         kern<<<L.U * D, 256, smem, static_cast<cudaStream_t>(stream)>>>(a, L, n2);
+        return static_cast<int>(cudaGetLastError());
+    });
+}
+
+int launch_nuq_gather(const Layout &L, const QuantArgs &a, void *stream) {
+    const unsigned grid = static_cast<unsigned>((static_cast<long long>(L.U) * a.scr_n + 3) / 4);
+    return nuq_dispatch(L, [&](auto v, auto) {
+        nuq_gather_kernel<decltype(v)::value><<<grid, 128, 0, static_cast<cudaStream_t>(stream)>>>(a, L);
+        return static_cast<int>(cudaGetLastError());
+    });
+}
+
+int launch_nuq_block_codes(const Layout &L, const QuantArgs &a, void *stream) {
+    const unsigned grid = static_cast<unsigned>((static_cast<long long>(L.U) * a.scr_n + 3) / 4);
+    return nuq_dispatch(L, [&](auto v, auto b) {
+        nuq_block_code_kernel<decltype(v)::value, decltype(b)::value>
+            <<<grid, 128, 0, static_cast<cudaStream_t>(stream)>>>(a, L);
         return static_cast<int>(cudaGetLastError());
     });
 }

@@ -16,6 +16,7 @@ def cfg_for(w: W.Workload, max_seq: int | None = None, out_dtype: str | None = N
                        n_recent=w.n_recent,
                        scheme=w.scheme, lloyd_iters=w.extra.get("lloyd_iters", 8),
                        outlier_frac=w.extra.get("outlier_frac", 0.01),
+                       group_size_v=w.extra.get("group_size", 0), refit_k=w.extra.get("refit_interval", 0),
                        levels_k=w.extra.get("levels_k", 8), levels_v=w.extra.get("levels_v", 6),
                        container_k=w.extra.get("container_k", 331), container_v=w.extra.get("container_v", 231),
                        rans_alpha=w.extra.get("alpha", 1.4))
@@ -91,12 +92,20 @@ def nuq_views(w: W.Workload, cache, S: int):
     rowk = d * w.bits // 8
     t = {n: (x.cpu().numpy() if x is not None else None) for n, x in cache.tensors.items()}
     sizes = kv_sizes(cache.cfg)
+    gv = d // (w.extra.get("group_size", 0) or d)
+    N = w.extra.get("refit_interval", 0) or 0
     v = {
         "codes_k": t["codes_k"].reshape(B, H, qcap, rowk),
         "codes_v": t["codes_v"].reshape(B, H, qcap // 2, 2 * rowk),
-        "lut_k": t["lut_k"].view(np.uint16).reshape(B, H, d, L),
-        "lut_v": t["lut_v"].view(np.uint16).reshape(B, H, qcap, L),
+        "lut_v": t["lut_v"].view(np.uint16).reshape(B, H, qcap, gv * L),
     }
+    if N:  # key tables per refit block, then the prefill's quantized slot count per unit
+        nbk = -(-qcap // N)
+        tab = t["lut_k"][:B * H * nbk * d * L * 2]
+        v["lut_k_blk"] = tab.view(np.uint16).reshape(B, H, nbk, d, L)
+        v["pq"] = t["lut_k"][B * H * nbk * d * L * 2:].view(np.int32).reshape(B, H)
+    else:
+        v["lut_k"] = t["lut_k"].view(np.uint16).reshape(B, H, d, L)
     if t["ol_rowptr_k"] is not None:
         v["rowptr"] = t["ol_rowptr_k"].view(np.int32).reshape(B, H, -1)
         v["col_k"] = t["ol_col_k"].view(np.uint16).reshape(B, H, -1)

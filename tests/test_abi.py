@@ -268,3 +268,46 @@ def test_quest_grid_validation(lib):
     nuq = make_config(**{**base, "n_recent": 0}, scheme="nuq", rot_k="none", rot_v="none", mean_k=False, bits=3)
     nuq.k.grid = 1
     assert lib.dq_kv_sizes(C.byref(nuq), arr) == 3
+
+
+def test_nuq_group_and_refit_layout_and_validation(lib):
+    # KVQuant-NUQ, Configuration reference: value tables per group of 32
+    # channels, key tables per refit block of N quantized slots
+    from quantized_decode_attention_gb300 import _lib, make_config
+    arr = (C.c_size_t * _lib.NUM_BUFFERS)()
+    names = _lib.BUFFER_NAMES
+    base = dict(batch=2, n_kv_heads=2, n_q_heads=8, head_dim=128, max_seq=1025, kv_dtype="f16", n_sink=1,
+                scheme="nuq", rot_k="none", rot_v="none", mean_k=False, bits=3)
+    U, d, L, qcap = 4, 128, 8, 1024
+    assert lib.dq_kv_sizes(C.byref(make_config(**base)), arr) == 0
+    plain = dict(zip(names, list(arr)))
+    assert plain["lut_k"] == U * d * L * 2 and plain["lut_v"] == U * qcap * L * 2
+    assert lib.dq_kv_sizes(C.byref(make_config(**base, group_size_v=32)), arr) == 0
+    grp = dict(zip(names, list(arr)))
+    assert grp["lut_v"] == U * qcap * 4 * L * 2 and grp["lut_k"] == plain["lut_k"]
+    assert lib.dq_kv_sizes(C.byref(make_config(**base, group_size_v=128)), arr) == 0
+    assert dict(zip(names, list(arr)))["lut_v"] == plain["lut_v"]
+    assert lib.dq_kv_sizes(C.byref(make_config(**{**base, "n_recent": 256}, refit_k=256)), arr) == 0
+    ref = dict(zip(names, list(arr)))
+    assert ref["lut_k"] == U * 4 * d * L * 2 + U * 4        # 4 blocks of 256 slots, then the prefill counts
+    assert ref["codes_k"] == plain["codes_k"] and ref["lut_v"] == plain["lut_v"]
+    bad = [
+        (dict(group_size_v=16), 3), (dict(group_size_v=64), 3),              # only 0, 32 or head_dim
+        (dict(refit_k=100, n_recent=128), 1), (dict(refit_k=-128, n_recent=128), 1),
+        (dict(refit_k=128), 3),                                                # the window must hold a block
+        (dict(refit_k=128, n_recent=128, kv_dtype="f32"), 3),                  # 16-bit keys read back
+        (dict(refit_k=128, n_recent=128, head_dim=64, bits=2), 3),
+        (dict(group_size_v=32, head_dim=64, bits=2), 3),
+    ]
+    for kw, status in bad:
+        cfg = make_config(**{**base, **kw})
+        assert lib.dq_kv_sizes(C.byref(cfg), arr) == status, kw
+    cfg = make_config(**base)
+    cfg.k.group_size = 32                                                      # keys span their tokens
+    assert lib.dq_kv_sizes(C.byref(cfg), arr) == 3
+    cfg = make_config(**{**base, "n_recent": 128})
+    cfg.v.refit_interval = 128                                                 # refits are for keys
+    assert lib.dq_kv_sizes(C.byref(cfg), arr) == 1
+    aff = make_config(batch=2, n_kv_heads=2, n_q_heads=8, head_dim=128, max_seq=512)
+    aff.v.group_size = 32                                                      # non-uniform scheme only
+    assert lib.dq_kv_sizes(C.byref(aff), arr) == 1

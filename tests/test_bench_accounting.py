@@ -81,3 +81,28 @@ def test_nuq_bytes_from_buffer_sizes(lib):
     side = U * (d * kk * 4 + (n_q + 1) * 4) + U * n_q * kv * 4
     expect = U * n_q * per_slot + sz["lut_k"] + side + U * w.n_sink * d * 2 * 2 + _qo(w)
     assert bench.nuq_algorithmic_bytes(w, S)["total"] == expect
+
+
+def test_nuq_group_refit_bytes_from_buffer_sizes(lib):
+    """The grouped / refit variant: value tables per slot from the buffer sizes
+    (four per token), one key table set per refit block of the quantized
+    tokens read (the buffer holds one per block of the capacity, plus the
+    prefill counts), the 16-bit recent window besides the sink."""
+    import bench
+    from helpers import cfg_for
+    from quantized_decode_attention_gb300 import kv_sizes
+    w = bench.NUQ_GROUP_REFIT
+    S, U, d, L = w.seq, w.batch * w.n_kv_heads, w.head_dim, 1 << w.bits
+    sz = kv_sizes(cfg_for(w))
+    qcap = sz["codes_k"] // (U * d * w.bits // 8)
+    n_q = S - w.n_sink - w.n_recent
+    per_slot = (sz["codes_k"] + sz["codes_v"] + sz["lut_v"]) // (U * qcap)
+    assert sz["lut_v"] == U * qcap * 4 * L * 2
+    blocks = -(-qcap // 128)
+    assert sz["lut_k"] == U * blocks * d * L * 2 + U * 4
+    kk = int(0.01 * n_q + 0.5)
+    kv = int(0.01 * d + 0.5)
+    side = U * (d * kk * 4 + (n_q + 1) * 4) + U * n_q * kv * 4
+    tables_k = U * (-(-n_q // 128)) * d * L * 2
+    expect = U * n_q * per_slot + tables_k + side + U * (w.n_sink + w.n_recent) * d * 2 * 2 + _qo(w)
+    assert bench.nuq_algorithmic_bytes(w, S)["total"] == expect

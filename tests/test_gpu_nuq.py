@@ -26,15 +26,28 @@ CASES = {
                                      extra={"outlier_frac": 0.0, "lloyd_iters": 0}),
     # bf16 input: side-channel values are rounded to fp16
     "nuq3-bf16": W.NUQ.with_(batch=1, n_kv_heads=1, n_q_heads=4, seq=150, kv_dtype="bf16"),
+    # value tables per 32-channel group (Configuration reference, kvquant_group_size)
+    "nuq3-group32": W.NUQ.with_(batch=2, n_kv_heads=2, n_q_heads=8, seq=300,
+                                extra={"lloyd_iters": 8, "outlier_frac": 0.01, "group_size": 32}),
+    "nuq4-group32-bf16": W.NUQ.with_(batch=1, n_kv_heads=1, n_q_heads=4, seq=200, bits=4, kv_dtype="bf16",
+                                     extra={"lloyd_iters": 8, "outlier_frac": 0.02, "group_size": 32}),
+    "nuq2-group32": W.NUQ.with_(batch=1, n_kv_heads=2, n_q_heads=8, seq=170, bits=2,
+                                extra={"lloyd_iters": 8, "outlier_frac": 0.01, "group_size": 32}),
 }
 
 
 def _compare(w, got, qcap, k, v, nk, nv, S):
     """Tables, codes, side channels and 16-bit regions of a cache of length S."""
     nq = S - w.n_sink
-    assert np.array_equal(got["lut_k"], nk.lut)
+    if nk.blk_lut is not None:   # key refit blocks: the coded slots and the tables of their blocks
+        N = w.extra["refit_interval"]
+        nc = nk.n_coded
+        assert np.array_equal(got["lut_k_blk"][:, :, :-(-nc // N)], nk.blk_lut[:, :, :-(-nc // N)])
+        assert np.array_equal(got["codes_k"][:, :, :nc], OC.pack_k(nk.codes[:, :, :nc], w.bits))
+    else:
+        assert np.array_equal(got["lut_k"], nk.lut)
+        assert np.array_equal(got["codes_k"][:, :, :nq], OC.pack_k(nk.codes, w.bits))
     assert np.array_equal(got["lut_v"][:, :, :nq], nv.lut)
-    assert np.array_equal(got["codes_k"][:, :, :nq], OC.pack_k(nk.codes, w.bits))
     pv = OC.pack_v(nv.codes, w.bits)
     full = nq // 2
     assert np.array_equal(got["codes_v"][:, :, :full], pv[:, :, :full])
@@ -92,6 +105,19 @@ STREAM = {
                                     n_recent=16), [120, 1, 1, 1, 77]),
     "nuq4-bf16-nosink": (W.NUQ.with_(batch=1, n_kv_heads=1, n_q_heads=4, seq=180, bits=4, kv_dtype="bf16",
                                      n_sink=0), [100, 1, 79]),
+    # key refit blocks of 128 slots (Configuration reference, kvquant_refit_interval)
+    # with grouped values: the prefill reaches blocks 0-1; single tokens fill
+    # block 2 partway, a 300-token append completes blocks 2 and 3, single
+    # tokens then complete block 4
+    "nuq3-refit128-group32": (W.NUQ.with_(batch=1, n_kv_heads=2, n_q_heads=8, seq=650, n_recent=128,
+                                          extra={"lloyd_iters": 8, "outlier_frac": 0.01, "group_size": 32,
+                                                 "refit_interval": 128}),
+                              [200] + [1] * 60 + [300] + [1] * 90),
+    # refit alone (whole-token values), 4 bits, bf16, no sink; blocks of 256
+    "nuq4-refit256-bf16": (W.NUQ.with_(batch=2, n_kv_heads=1, n_q_heads=4, seq=700, bits=4, kv_dtype="bf16",
+                                       n_sink=0, n_recent=256,
+                                       extra={"lloyd_iters": 8, "outlier_frac": 0.02, "refit_interval": 256}),
+                           [100, 1, 1, 300, 298]),
 }
 
 
@@ -131,6 +157,8 @@ def test_nuq_appends_match_oracle(name):
             assert nk.outlier[:, :, P - w.n_sink:].any()  # decode keys did meet the threshold
         _compare(w, got, qcap, k, v, nk, nv, S)
         assert np.array_equal(got["thr_k"], OC.nuq_key_thresholds(w, k, P))
+        if "pq" in got:
+            assert np.all(got["pq"] == P - w.n_sink)
         cache.attention(qd, out, S)
         torch.cuda.synchronize()
         cache.check()
