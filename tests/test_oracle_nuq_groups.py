@@ -1,8 +1,8 @@
 """Pins of the oracle's grouped value fit and key refit blocks.
 
 Source: "KVQuant-NUQ" (VeloxQuant-MLX docs), Configuration reference:
-kvquant_group_size (group size for the per-token fits) and
-kvquant_refit_interval (refit the key levels every N decode steps), with How
+kvquant_group_size (how many elements share one fit) and
+kvquant_refit_interval (key levels fitted anew after N decode steps), with How
 it works (quantile-seeded Lloyd-Max, rank outliers per token) and Quantization
 axes (keys per channel, values per token).
 
