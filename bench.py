@@ -67,6 +67,7 @@ def parse():
     p.add_argument("--no-bf16", action="store_true", help="skip the unquantized 16-bit cache context entry")
     p.add_argument("--profile-attn", action="store_true",
                    help="profiler run: one cache, warmup + steps attention calls, no timing")
+    p.add_argument("--profile-batch", type=int, default=4, help="--profile-attn: batch of the D-Quant cache")
     p.add_argument("--profile-kind", default="affine", choices=["affine", "nuq", "dquant"],
                    help="--profile-attn cache: the Llama-shaped affine cache at --bits, the KVQuant NUQ cache, or "
                         "the D-Quant cache at a reduced batch")
@@ -1092,7 +1093,7 @@ def cfg_of(w: W.Workload, max_seq: int | None = None):
 
 def profile_attention(args):
     """A short run for a profiler to capture: one cache (the Llama-shaped affine
-    cache at args.bits, the KVQuant NUQ cache, or the D-Quant cache at batch 4),
+    cache at args.bits, the KVQuant NUQ cache, or the D-Quant cache at args.profile_batch),
     prefilled once, then args.warmup + args.steps decode-attention calls on one
     stream.  Nothing is timed here."""
     import torch
@@ -1104,7 +1105,7 @@ def profile_attention(args):
     elif args.profile_kind == "nuq":
         w = W.NUQ
     else:
-        w = W.DQUANT.with_(batch=4)
+        w = W.DQUANT.with_(batch=args.profile_batch)
     S = w.seq
     k, v = W.make_kv(w)
     dt = torch.float16 if w.kv_dtype == "f16" else torch.bfloat16
@@ -1112,6 +1113,9 @@ def profile_attention(args):
     q_dev = torch.from_numpy(W.make_q(w)).cuda()
     cache = KVCache.allocate(cfg_of(w), zero=False)
     cache.quantize(dev16(k), dev16(v), pos0=0)
+    torch.cuda.synchronize()
+    del k, v
+    torch.cuda.empty_cache()  # only the cache stays on the device
     odt = {"bf16": torch.bfloat16, "f16": torch.float16, "f32": torch.float32}[w.out_dtype]
     out = torch.empty((w.batch, w.n_q_heads, w.head_dim), dtype=odt, device="cuda")
     for _ in range(args.warmup + args.steps):

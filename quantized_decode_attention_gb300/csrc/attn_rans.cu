@@ -18,7 +18,8 @@
 // 32 tokens) or the 16-bit tokens (sinks + recent window) of one sequence.
 // Per KV head h a warp, for each of its chunks, decodes 128 key and 128 value
 // symbols per lane, takes the key dot products with the rotated query rows
-// (scalar FMAs, the query broadcast from shared memory), updates the online
+// (scalar FMAs, the rows of head h's query heads prepared in shared memory at
+// the start of the head and broadcast from there), updates the online
 // softmax of the G query heads, stages the value levels in shared memory and
 // runs P.V on the tensor cores (mma m16n8k16, 8 columns = 4 query heads x hi/lo
 // halves of P' = p s).  The decoder states of a lane's 4 tokens stay in
@@ -51,12 +52,14 @@ __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-// Predicated 32-bit read-only load into v: v = *p when pred, else v is kept.
-// Nothing reads v here, so the load's latency is only paid where v is next used.
-__device__ __forceinline__ void ldg_into_if(uint32_t &v, const uint32_t *p, bool pred) {
-    asm("{\n .reg .pred q;\n setp.ne.b32 q, %2, 0;\n @q ld.global.nc.u32 %0, [%1];\n}\n"
+// Predicated 32-bit read-only load into v: v = base[i] when pred, else v is
+// kept.  Nothing reads v here, so the load's latency is only paid where v is
+// next used.
+__device__ __forceinline__ void ldg_into_if(uint32_t &v, const uint32_t *base, uint32_t i, bool pred) {
+    asm("{\n .reg .pred q;\n .reg .u64 a;\n setp.ne.b32 q, %3, 0;\n mad.wide.u32 a, %2, 4, %1;\n"
+        " @q ld.global.nc.u32 %0, [a];\n}\n"
         : "+r"(v)
-        : "l"(p), "r"(static_cast<int>(pred)));
+        : "l"(base), "r"(i), "r"(static_cast<int>(pred)));
 }
 
 // One rANS stream being decoded by a lane.  The container bytes after the
@@ -65,45 +68,42 @@ __device__ __forceinline__ void ldg_into_if(uint32_t &v, const uint32_t *p, bool
 // prefetched at the previous refill in and fetches the next one (a predicated
 // load, so there is no branch and no wait), which keeps at least 4 unread bytes
 // in the pair - enough for 4 symbols, each taking at most one byte.  Loads stay
-// inside the aligned words that overlap the container (wl counts those not yet
-// loaded); an idle lane loads nothing.  A well-formed stream ends in the state
-// the encoder started from (2^23), which the caller checks.
+// inside the aligned words that overlap the container; an idle lane loads
+// nothing.  A well-formed stream ends in the state the encoder started from
+// (2^23), which the caller checks.  Six registers: kw holds k (bits 0-3) and
+// the words overlapping the container not yet loaded (bits 8 up); wi is the
+// next word's index from the tensor's base.
 struct Dec {
-    uint32_t x, lo, hi, nxt, k;
-    const uint32_t *wp;  // next word to load
-    int wl;              // words overlapping the container not yet loaded
-    __device__ __forceinline__ void open(const uint8_t *base, int C, bool valid) {
+    uint32_t x, lo, hi, nxt, kw, wi;
+    __device__ __forceinline__ void open(const uint8_t *codes, long long off0, int C, bool valid) {
         if (!valid) {  // an idle lane: decodes zeros, reads nothing
             x = RANS_L;
-            lo = hi = nxt = k = 0;
-            wp = nullptr;
-            wl = 0;
+            lo = hi = nxt = kw = wi = 0;
             return;
         }
+        const uint8_t *base = codes + off0;
         x = static_cast<uint32_t>(base[0]) | (static_cast<uint32_t>(base[1]) << 8) |
             (static_cast<uint32_t>(base[2]) << 16) | (static_cast<uint32_t>(base[3]) << 24);
-        const uintptr_t p0 = reinterpret_cast<uintptr_t>(base + 4);
-        const uintptr_t pe = reinterpret_cast<uintptr_t>(base + C - 1);  // C >= 8: pe >= p0
-        const int off = static_cast<int>(p0 & 3u);
-        const uint32_t *w0 = reinterpret_cast<const uint32_t *>(p0 - off);
-        const int words = static_cast<int>(((pe & ~uintptr_t(3)) - (p0 - off)) / 4) + 1;
-        lo = __ldg(w0);
-        hi = words > 1 ? __ldg(w0 + 1) : 0u;
-        nxt = words > 2 ? __ldg(w0 + 2) : 0u;
-        k = static_cast<uint32_t>(off);
-        wp = w0 + 3;
-        wl = words - 3;
+        const long long p0 = off0 + 4, pe = off0 + C - 1;  // C >= 8: pe >= p0; codes is 16-byte aligned
+        const int off = static_cast<int>(p0 & 3);
+        const long long w0 = (p0 - off) / 4;
+        const int words = static_cast<int>((pe & ~3LL) / 4 - w0) + 1;
+        const uint32_t *cw = reinterpret_cast<const uint32_t *>(codes);
+        lo = __ldg(cw + w0);
+        hi = words > 1 ? __ldg(cw + w0 + 1) : 0u;
+        nxt = words > 2 ? __ldg(cw + w0 + 2) : 0u;
+        kw = static_cast<uint32_t>(off) | (static_cast<uint32_t>(words - 3 > 0 ? words - 3 : 0) << 8);
+        wi = static_cast<uint32_t>(w0 + 3);
     }
     // Past the container's last word nxt keeps a stale word: a well-formed
     // stream never consumes those bytes (the final-state check catches one that does).
-    __device__ __forceinline__ void refill() {
-        const bool r = k >= 4u;
+    __device__ __forceinline__ void refill(const uint32_t *cw) {
+        const bool r = (kw & 0xffu) >= 4u;
         lo = r ? hi : lo;
         hi = r ? nxt : hi;
-        k = r ? k - 4u : k;
-        ldg_into_if(nxt, wp, r && wl > 0);
-        wp += r ? 1 : 0;
-        wl -= r ? 1 : 0;
+        ldg_into_if(nxt, cw, wi, r && kw >= 256u);
+        wi += (r && kw >= 256u) ? 1u : 0u;
+        kw -= r ? (kw >= 256u ? 260u : 4u) : 0u;
     }
 };
 
@@ -119,9 +119,9 @@ __device__ __forceinline__ void step_all(Dec (&d)[N], const uint2 *dec, uint2 (&
 #pragma unroll
     for (int ch = 0; ch < N; ch++) {
         const bool need = d[ch].x < RANS_L;
-        const uint32_t byte = __byte_perm(d[ch].lo, d[ch].hi, d[ch].k);  // byte k of (hi, lo) in byte 0
-        d[ch].x = need ? __byte_perm(byte, d[ch].x, 0x6540) : d[ch].x;   // (x << 8) | byte
-        d[ch].k += need ? 1u : 0u;
+        const uint32_t byte = __byte_perm(d[ch].lo, d[ch].hi, d[ch].kw);  // byte k of (hi, lo) in byte 0
+        d[ch].x = need ? __byte_perm(byte, d[ch].x, 0x6540) : d[ch].x;    // (x << 8) | byte
+        d[ch].kw += need ? 1u : 0u;
     }
 }
 
@@ -132,10 +132,10 @@ struct RecMerge {
 
 template <int H>
 struct RansSmem {
-    uint2 dec_k[256], dec_v[256];
-    float4 qk[H][128];               // rotated query rows of head h's 4 query heads, by channel
-    float qsum[4 * H];               // sum_c q_rot[qh][c]
-    float qmu[4][4 * H];             // sum_c q_rot[qh][c] mu^_w[c] for the item's 4 windows
+    uint2 dec_k[256], dec_v[256];   // (f | (z - c) << 16, level as fp32 bits / fp16 bits)
+    float4 qk[128];                  // rotated query rows of the current head's 4 query heads, by channel
+    float qsum[4];                   // sum_c q_rot[qh][c] of those heads
+    float qmu[4][4];                 // sum_c q_rot[qh][c] mu^_w[c] for the item's 4 windows
     uint16_t pst[RW][RCH][8][VST];   // staged P' (fp16 hi/lo), [chunk][column][token]
     union {                          // the merge follows the head's value pass
         uint16_t vst[RW][RCH][16][VST];  // staged value levels (fp16) of 16 channels, [chunk][channel][token]
@@ -150,8 +150,10 @@ template <int H>
 __device__ void rans_quant_item(RansSmem<H> &S, const RansAttnArgs &a, int b, long long s0) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, tig = lane & 3;
     constexpr int N = 128 * H, HQ = 4 * H;
-    // rotated queries of this sequence (normalized Hadamard per head when keys are rotated)
-    for (int qh = warp; qh < HQ; qh += RW) {
+    // rotated query rows of KV head h's query heads (warp gq takes head 4h +
+    // gq), their sums and their dot products with the item's window means
+    auto prep_queries = [&](int h) {
+        const int gq = warp, qh = 4 * h + gq;
         float q4[4];
         const float *qp = a.q + (static_cast<long long>(b) * HQ + qh) * 128 + 4 * lane;
 #pragma unroll
@@ -161,11 +163,10 @@ __device__ void rans_quant_item(RansSmem<H> &S, const RansAttnArgs &a, int b, lo
 #pragma unroll
             for (int j = 0; j < 4; j++) q4[j] = __fmul_rn(q4[j], a.hscale);
         }
-        const int h = qh >> 2, gq = qh & 3;
 #pragma unroll
-        for (int j = 0; j < 4; j++) reinterpret_cast<float *>(&S.qk[h][4 * lane + j])[gq] = q4[j];
+        for (int j = 0; j < 4; j++) reinterpret_cast<float *>(&S.qk[4 * lane + j])[gq] = q4[j];
         const float sum = warp_sum(q4[0] + q4[1] + q4[2] + q4[3]);
-        if (lane == 0) S.qsum[qh] = sum;
+        if (lane == 0) S.qsum[gq] = sum;
         // window means: INT8 q times the fp16 scale
         for (int w = 0; w < 4; w++) {
             const long long win = s0 / 128 + w;
@@ -179,23 +180,22 @@ __device__ void rans_quant_item(RansSmem<H> &S, const RansAttnArgs &a, int b, lo
                     dmu += q4[j] * (static_cast<float>(static_cast<int8_t>((qw >> (8 * j)) & 0xffu)) * sc);
             }
             dmu = warp_sum(dmu);
-            if (lane == 0) S.qmu[w][qh] = dmu;
+            if (lane == 0) S.qmu[w][gq] = dmu;
         }
-    }
-    __syncthreads();
-    // this lane's 4 tokens (one per chunk) and their decoders
+    };
     // this lane's 4 tokens (one per chunk), their decoders and metadata
     Dec dk[RCH], dv[RCH];
     bool bad = false, valid[RCH];
     float sk[RCH], ok[RCH], sv[RCH], ov[RCH];
-    int wi[RCH];
+    // the token's 128-slot mean window within the item: slot - s0 = 128 warp +
+    // 32 ch + lane, so it is window `warp` for every chunk of the lane
 #pragma unroll
     for (int ch = 0; ch < RCH; ch++) {
         const long long slot = s0 + 32 * (RCH * warp + ch) + lane;
         valid[ch] = slot < a.n_q;
         const long long rs = static_cast<long long>(b) * a.qcap + (valid[ch] ? slot : 0);
-        dk[ch].open(a.codes_k + rs * a.ck, a.ck, valid[ch]);
-        dv[ch].open(a.codes_v + rs * a.cv, a.cv, valid[ch]);
+        dk[ch].open(a.codes_k, rs * a.ck, a.ck, valid[ch]);
+        dv[ch].open(a.codes_v, rs * a.cv, a.cv, valid[ch]);
         sk[ch] = ok[ch] = sv[ch] = ov[ch] = 0.f;
         if (valid[ch]) {
             const __half2 mk = reinterpret_cast<const __half2 *>(a.meta_k)[rs];
@@ -205,12 +205,15 @@ __device__ void rans_quant_item(RansSmem<H> &S, const RansAttnArgs &a, int b, lo
             sv[ch] = __low2float(mv);
             ov[ch] = __high2float(mv);
         }
-        wi[ch] = static_cast<int>((slot - s0) >> 7);
     }
     uint16_t(*vst)[16][VST] = S.vst[warp];
     uint16_t(*pst)[8][VST] = S.pst[warp];
+    const uint32_t *ckw = reinterpret_cast<const uint32_t *>(a.codes_k);
+    const uint32_t *cvw = reinterpret_cast<const uint32_t *>(a.codes_v);
 #pragma unroll 1
     for (int h = 0; h < H; h++) {
+        prep_queries(h);
+        __syncthreads();
         // keys of head h: 128 symbols of each of the 4 streams, interleaved
         float dot[RCH][4];
 #pragma unroll
@@ -219,9 +222,9 @@ __device__ void rans_quant_item(RansSmem<H> &S, const RansAttnArgs &a, int b, lo
         for (int c = 0; c < 128; c++) {
             if ((c & 3) == 0) {
 #pragma unroll
-                for (int ch = 0; ch < RCH; ch++) dk[ch].refill();
+                for (int ch = 0; ch < RCH; ch++) dk[ch].refill(ckw);
             }
-            const float4 q4 = S.qk[h][c];
+            const float4 q4 = S.qk[c];
             uint2 ek[RCH];
             step_all<RCH>(dk, S.dec_k, ek);
 #pragma unroll
@@ -237,11 +240,10 @@ __device__ void rans_quant_item(RansSmem<H> &S, const RansAttnArgs &a, int b, lo
         float mrun[4], lsum[4], osum[4];
 #pragma unroll
         for (int gq = 0; gq < 4; gq++) {
-            const int qh = 4 * h + gq;
             float lg[RCH], mx = -INFINITY;
 #pragma unroll
             for (int ch = 0; ch < RCH; ch++) {
-                lg[ch] = valid[ch] ? a.sm_log2 * (sk[ch] * dot[ch][gq] + ok[ch] * S.qsum[qh] + S.qmu[wi[ch]][qh])
+                lg[ch] = valid[ch] ? a.sm_log2 * (sk[ch] * dot[ch][gq] + ok[ch] * S.qsum[gq] + S.qmu[warp][gq])
                                    : -INFINITY;
                 mx = fmaxf(mx, lg[ch]);
             }
@@ -280,7 +282,7 @@ __device__ void rans_quant_item(RansSmem<H> &S, const RansAttnArgs &a, int b, lo
             for (int cc = 0; cc < 16; cc++) {
                 if ((cc & 3) == 0) {
 #pragma unroll
-                    for (int ch = 0; ch < RCH; ch++) dv[ch].refill();
+                    for (int ch = 0; ch < RCH; ch++) dv[ch].refill(cvw);
                 }
                 uint2 ev[RCH];
                 step_all<RCH>(dv, S.dec_v, ev);
@@ -411,12 +413,11 @@ __global__ void __launch_bounds__(128, 4) attn_rans_kernel(RansAttnArgs a, const
     }
     // decoder tables: entry = (f | (z - c) << 16, level as fp32 bits) for keys,
     // (f | (z - c) << 16, level as fp16 bits) for values
-    for (int z = threadIdx.x; z < 256; z += blockDim.x) {
-        const uint32_t ek = tabs->k.dec[z], ev = tabs->v.dec[z];
-        const uint32_t mk = ek & 15u, mv = ev & 15u;
-        S.dec_k[z] = make_uint2(((ek >> 4) & 0x1ffu) | ((ek >> 16) << 16), __float_as_uint(static_cast<float>(mk)));
-        S.dec_v[z] = make_uint2(((ev >> 4) & 0x1ffu) | ((ev >> 16) << 16),
-                                static_cast<uint32_t>(__half_as_ushort(__uint2half_rn(mv))));
+    for (int i = threadIdx.x; i < 256; i += blockDim.x) {
+        const uint32_t ek = tabs->k.dec[i], ev = tabs->v.dec[i];
+        S.dec_k[i] = make_uint2(((ek >> 4) & 0x1ffu) | ((ek >> 16) << 16), __float_as_uint(static_cast<float>(ek & 15u)));
+        S.dec_v[i] = make_uint2(((ev >> 4) & 0x1ffu) | ((ev >> 16) << 16),
+                                static_cast<uint32_t>(__half_as_ushort(__uint2half_rn(ev & 15u))));
     }
     __syncthreads();
     rans_quant_item<H>(S, a, b, static_cast<long long>(it) * ITEM);
