@@ -866,7 +866,8 @@ def codes_of_records(rec: np.ndarray, bits: int) -> np.ndarray:
     fields.  At 3 bits, a 2-bit plane of R/16 words comes first (the 2-bit
     layout), then a 1-bit plane: field i of half h keeps its low two bits at
     bit 16h + 2(i mod 8) of plane word i/8, and its high bit at bit
-    16h + (i mod 16) of 1-bit-plane word i/16."""
+    16h + P(i mod 16) of 1-bit-plane word i/16, P(f) = 2f + 2 for f <= 6, 0 for
+    f = 7, 2f - 13 for 8 <= f <= 14, 1 for f = 15."""
     w = np.ascontiguousarray(rec, dtype=np.uint8)
     w = w.reshape(-1, w.shape[-1]).view("<u4").astype(np.int64)
     if bits in (2, 4):
@@ -877,7 +878,9 @@ def codes_of_records(rec: np.ndarray, bits: int) -> np.ndarray:
     out = []
     for h in (0, 1):
         lo = (w[:, i >> 3] >> (16 * h + 2 * (i & 7))) & 3
-        hi = (w[:, R // 16 + (i >> 4)] >> (16 * h + (i & 15))) & 1
+        f = i & 15
+        p1 = np.where(f <= 6, 2 * f + 2, np.where(f == 7, 0, np.where(f == 15, 1, 2 * f - 13)))
+        hi = (w[:, R // 16 + (i >> 4)] >> (16 * h + p1)) & 1
         out.append(lo | (hi << 2))
     return np.concatenate(out, axis=1).ravel()
 

@@ -135,7 +135,9 @@ typedef struct {
  * Bit layout of a record: little-endian 32-bit words; with b = 2 or 4 each
  * 16-bit half holds 16/b fields of b bits, field f at bits [b*f, b*f+b); with
  * b = 3 a 2-bit plane (low code bits, laid out as b = 2) is followed by a
- * 1-bit plane (16 fields per half).  Key channel c of a token goes to
+ * 1-bit plane (16 fields per half, field f at bit P(f) of its half: P(f) =
+ * 2f + 2 for f <= 6, 0 for f = 7, 2f - 13 for 8 <= f <= 14, 1 for f = 15).
+ * Key channel c of a token goes to
  *   idx = ((c>>1)&3)*(d/8) + 2*(c>>4) + ((c>>3)&1), half = c&1;
  * value channel c of token t goes to
  *   idx = (c&7)*(d/8) + 2*(c>>4) + ((c>>3)&1), half = t&1,

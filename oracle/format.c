@@ -14,7 +14,11 @@
  * bits per code, each 16-bit half of a word holds F = 16/b fields; field f
  * occupies bits [b*f, b*f + b) of its half.  With b = 3 the record is a
  * 2-bit plane (the low two bits of every code, laid out as b = 2) followed
- * by a 1-bit plane (bit 2 of every code, F = 16).
+ * by a 1-bit plane (bit 2 of every code, F = 16) whose field f sits at bit
+ * P(f) of its half, P(f) = 2f + 2 for f <= 6, 0 for f = 7, 2f - 13 for
+ * 8 <= f <= 14 and 1 for f = 15 (a permutation of 0..15: the bits of the
+ * fields that a reader turns into operands together then need few distinct
+ * shifts to meet their 2-bit fields).
  *
  * Key row of token t (d channels, one record per token):
  *   channel c -> e = c & 1, tig = (c >> 1) & 3, sub = (c >> 3) & 1, i = c >> 4
@@ -30,10 +34,17 @@
 
 static int fields_per_half(int b) { return 16 / b; }
 
-/* Bit position of (channel c, half e) in a record laid out for b in {1, 2, 4}. */
+/* Bit position of (channel c, half e) in a record laid out for b in {2, 4}. */
 static long bitpos(int idx, int e, int b) {
     int F = fields_per_half(b);
     return 32L * (idx / F) + 16L * e + (long)b * (idx % F);
+}
+
+/* Bit position of field idx, half e, in the 1-bit plane of a 3-bit record. */
+static long bitpos1(int idx, int e) {
+    int f = idx % 16;
+    int p = f <= 6 ? 2 * f + 2 : (f == 7 ? 0 : (f == 15 ? 1 : 2 * f - 13));
+    return 32L * (idx / 16) + 16L * e + p;
 }
 
 static int k_idx(int c, int d) {
@@ -74,7 +85,7 @@ void or_pack_k_row(const unsigned char *codes, int d, int b, uint8_t *row) {
         int idx = k_idx(c, d), e = c & 1;
         if (b == 3) {
             put_bits(row, bitpos(idx, e, 2), 2, codes[c] & 3u);
-            put_bits(row + d / 4, bitpos(idx, e, 1), 1, (codes[c] >> 2) & 1u);
+            put_bits(row + d / 4, bitpos1(idx, e), 1, (codes[c] >> 2) & 1u);
         } else {
             put_bits(row, bitpos(idx, e, b), b, codes[c]);
         }
@@ -86,7 +97,7 @@ void or_unpack_k_row(const uint8_t *row, int d, int b, unsigned char *codes) {
         int idx = k_idx(c, d), e = c & 1;
         if (b == 3)
             codes[c] = (unsigned char)(get_bits(row, bitpos(idx, e, 2), 2) |
-                                       (get_bits(row + d / 4, bitpos(idx, e, 1), 1) << 2));
+                                       (get_bits(row + d / 4, bitpos1(idx, e), 1) << 2));
         else
             codes[c] = (unsigned char)get_bits(row, bitpos(idx, e, b), b);
     }
@@ -99,7 +110,7 @@ void or_pack_v_token(const unsigned char *codes, int d, int b, int e, uint8_t *r
         int idx = v_idx(c, d);
         if (b == 3) {
             put_bits(rec, bitpos(idx, e, 2), 2, codes[c] & 3u);
-            put_bits(rec + d / 2, bitpos(idx, e, 1), 1, (codes[c] >> 2) & 1u);
+            put_bits(rec + d / 2, bitpos1(idx, e), 1, (codes[c] >> 2) & 1u);
         } else {
             put_bits(rec, bitpos(idx, e, b), b, codes[c]);
         }
@@ -111,7 +122,7 @@ void or_unpack_v_token(const uint8_t *rec, int d, int b, int e, unsigned char *c
         int idx = v_idx(c, d);
         if (b == 3)
             codes[c] = (unsigned char)(get_bits(rec, bitpos(idx, e, 2), 2) |
-                                       (get_bits(rec + d / 2, bitpos(idx, e, 1), 1) << 2));
+                                       (get_bits(rec + d / 2, bitpos1(idx, e), 1) << 2));
         else
             codes[c] = (unsigned char)get_bits(rec, bitpos(idx, e, b), b);
     }

@@ -215,9 +215,9 @@ __device__ __forceinline__ void field_codes(const uint32_t *w, int r, uint32_t &
     const uint32_t x = w[r >> 3], sh = 2 * (r & 7);
     m0 = (x >> sh) & 3u;
     m1 = (x >> (16 + sh)) & 3u;
-    if (BITS == 3) {  // the 1-bit plane word holds register r at bits r and 16 + r
-        m0 |= ((w[2] >> r) & 1u) << 2;
-        m1 |= ((w[2] >> (16 + r)) & 1u) << 2;
+    if (BITS == 3) {  // the 1-bit plane word holds register r at bits bit1_pos(r) and 16 + bit1_pos(r)
+        m0 |= ((w[2] >> bit1_pos(r)) & 1u) << 2;
+        m1 |= ((w[2] >> (16 + bit1_pos(r))) & 1u) << 2;
     }
 }
 
@@ -228,7 +228,7 @@ __device__ __forceinline__ uint32_t code_in_rec(const uint8_t *rec, int idx, int
     const uint32_t *w = reinterpret_cast<const uint32_t *>(rec);
     if (BITS == 3) {
         const uint32_t lo = (w[idx >> 3] >> (16 * half + 2 * (idx & 7))) & 3u;
-        const uint32_t hi = (w[words_lo + (idx >> 4)] >> (16 * half + (idx & 15))) & 1u;
+        const uint32_t hi = (w[words_lo + (idx >> 4)] >> (16 * half + bit1_pos(idx & 15))) & 1u;
         return lo | (hi << 2);
     }
     constexpr int F = 16 / BITS;

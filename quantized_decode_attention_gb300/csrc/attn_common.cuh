@@ -39,13 +39,16 @@ __device__ __forceinline__ uint32_t extract<4>(const uint32_t *w, int r) {
     return y & ((f & 1) ? 0x00F000F0u : 0x000F000Fu);
 }
 // 3-bit: w[0..1] = 2-bit plane words, w[2] = 1-bit plane word (register r at
-// bits r and 16 + r); bit 2 of the code lands two places above the 2-bit field.
+// bits bit1_pos(r) and 16 + bit1_pos(r)); bit 2 of the code lands two places
+// above the 2-bit field.  The plane's permutation gives the 16 registers of a
+// slice five distinct shifts (0, -1, -10, -11, +6, +5 with 0 free), which the
+// compiler computes once per slice.
 template <>
 __device__ __forceinline__ uint32_t extract<3>(const uint32_t *w, int r) {
     const uint32_t lo = extract<2>(w, r);
     const int f = r & 7;
     const int pos = (f <= 4 ? 2 * f : 2 * (f - 5)) + 2;
-    const int sh = pos - r;
+    const int sh = pos - bit1_pos(r);
     const uint32_t hb = sh >= 0 ? (w[2] << sh) : (w[2] >> (-sh));
     return lo | (hb & (0x00010001u << pos));
 }

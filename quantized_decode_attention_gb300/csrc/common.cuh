@@ -98,6 +98,13 @@ struct Rec {
     static constexpr int V_WORDS = 2 * D * BITS / 32;
 };
 
+// Bit of field f (0..15) within a half of a 3-bit record's 1-bit plane: a
+// permutation chosen so that the fields a lane turns into operands together
+// need few distinct shifts to meet their 2-bit fields.
+__host__ __device__ constexpr int bit1_pos(int f) {
+    return f <= 6 ? 2 * f + 2 : (f == 7 ? 0 : (f == 15 ? 1 : 2 * f - 13));
+}
+
 // OR-contribution of one code to word w of a key row (BITS 2/4: one plane;
 // BITS 3: 2-bit plane words first, then the 1-bit plane).
 template <int D, int BITS>
@@ -105,7 +112,7 @@ __device__ __forceinline__ uint32_t contrib(int w, int idx, int half, uint32_t m
     if (BITS == 3) {
         uint32_t v = 0;
         if (w == idx / 8) v |= (m & 3u) << (16 * half + 2 * (idx % 8));
-        if (w == words_lo + idx / 16) v |= ((m >> 2) & 1u) << (16 * half + (idx % 16));
+        if (w == words_lo + idx / 16) v |= ((m >> 2) & 1u) << (16 * half + bit1_pos(idx % 16));
         return v;
     }
     constexpr int F = 16 / BITS;

@@ -105,7 +105,7 @@ template <int D, int BITS>
 __device__ __forceinline__ uint32_t code_at(const uint32_t *rec, int idx, int half, int words_lo) {
     if (BITS == 3) {
         const uint32_t lo = (rec[idx / 8] >> (16 * half + 2 * (idx % 8))) & 3u;
-        const uint32_t hb = (rec[words_lo + idx / 16] >> (16 * half + idx % 16)) & 1u;
+        const uint32_t hb = (rec[words_lo + idx / 16] >> (16 * half + bit1_pos(idx % 16))) & 1u;
         return lo | (hb << 2);
     }
     constexpr int F = 16 / BITS;

@@ -225,7 +225,7 @@ __device__ __forceinline__ void quantize_loaded_row(const QuantArgs &a, const Ro
         if (BITS == 3) {
             const int wlo = (a.is_key ? 1 : 2) * D * 2 / 32;  // 2-bit plane words come first
             atomicOr(&pw[idx / 8], (m[j] & 3u) << (16 * half + 2 * (idx % 8)));
-            atomicOr(&pw[wlo + idx / 16], ((m[j] >> 2) & 1u) << (16 * half + idx % 16));
+            atomicOr(&pw[wlo + idx / 16], ((m[j] >> 2) & 1u) << (16 * half + bit1_pos(idx % 16)));
         } else {
             constexpr int F = 16 / BITS;
             atomicOr(&pw[idx / F], m[j] << (16 * half + BITS * (idx % F)));

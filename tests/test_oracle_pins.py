@@ -304,3 +304,25 @@ def test_raw_regions_sinks_exact_and_recent_ring():
     # n_sink = 0: no sink slots at all
     reg0 = oracle.raw_regions(w.with_(n_sink=0, n_recent=0), k, S)
     assert reg0 == {}
+
+
+def test_three_bit_key_row_hand_built_bytes():
+    # d = 128, 3 bits: a 32-byte 2-bit plane, then a 16-byte 1-bit plane whose
+    # field f sits at bit P(f) of its half: P = 2, 4, 6, 8, 10, 12, 14, 0, 3,
+    # 5, 7, 9, 11, 13, 15, 1.  Channel c -> field idx = tig*16 + 2i + sub
+    # (tig = (c >> 1) & 3, i = c >> 4, sub = (c >> 3) & 1), half c & 1.
+    codes = np.zeros(128, np.uint8)
+    # bit 2 only: channel -> (idx, half): 0 -> (0, 0) P 2; 1 -> (0, 1) P 2;
+    # 8 -> (1, 0) P 4; 56 -> (7, 0) P 0; 120 -> (15, 0) P 1; 64 -> (8, 0) P 3;
+    # 65 -> (8, 1) P 3; 2 -> (16, 0): second 1-bit word, P 2
+    for c in (0, 1, 8, 56, 120, 64, 65, 2):
+        codes[c] = 4
+    codes[3] = 3            # (16, 1): 2-bit plane word 2, field 0, half 1 -> byte 10 = 0b11
+    exp = np.zeros(48, np.uint8)
+    exp[32] = 0x04 | 0x10 | 0x01 | 0x02 | 0x08   # half 0 of 1-bit word 0: bits 2, 4, 0, 1, 3
+    exp[34] = 0x04 | 0x08                          # half 1 of 1-bit word 0: bits 2, 3
+    exp[36] = 0x04                                 # 1-bit word 1, bit 2
+    exp[10] = 0x03
+    row = oracle.pack_k_row(codes, 3)
+    assert np.array_equal(row, exp), np.flatnonzero(row != exp)
+    assert np.array_equal(oracle.unpack_k_row(row, 128, 3), codes)
