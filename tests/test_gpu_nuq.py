@@ -113,6 +113,11 @@ STREAM = {
                                           extra={"lloyd_iters": 8, "outlier_frac": 0.01, "group_size": 32,
                                                  "refit_interval": 128}),
                               [200] + [1] * 60 + [300] + [1] * 90),
+    # the prefill ends on a block boundary (256 quantized slots = blocks 0-1), so
+    # the first appended key already waits for block 2; 2 bits, one KV head
+    "nuq2-refit128-aligned": (W.NUQ.with_(batch=1, n_kv_heads=1, n_q_heads=4, seq=520, bits=2, n_recent=128,
+                                          extra={"lloyd_iters": 8, "outlier_frac": 0.02, "refit_interval": 128}),
+                              [257] + [1] * 5 + [250] + [8]),
     # refit alone (whole-token values), 4 bits, bf16, no sink; blocks of 256
     "nuq4-refit256-bf16": (W.NUQ.with_(batch=2, n_kv_heads=1, n_q_heads=4, seq=700, bits=4, kv_dtype="bf16",
                                        n_sink=0, n_recent=256,
