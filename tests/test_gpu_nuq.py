@@ -169,6 +169,10 @@ def test_nuq_appends_match_oracle(name):
         cache.check()
         ref = OC.attention(w, q, k[:, :, :S], v[:, :, :S], S, nk, nv)
         assert np.all(np.abs(out_to_np(out) - ref) <= _out_tol(w, ref)), (S, float(np.max(np.abs(out_to_np(out) - ref))))
+        out2 = torch.empty_like(out)  # the allocation-free entry point reads the same tables
+        cache.attention_noalloc(qd, out2, S)
+        torch.cuda.synchronize()
+        assert np.all(np.abs(out_to_np(out2) - ref) <= _out_tol(w, ref)), S
 
 
 def test_nuq_key_side_channel_overflow():
