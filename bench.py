@@ -68,9 +68,9 @@ def parse():
     p.add_argument("--profile-attn", action="store_true",
                    help="profiler run: one cache, warmup + steps attention calls, no timing")
     p.add_argument("--profile-batch", type=int, default=4, help="--profile-attn: batch of the D-Quant cache")
-    p.add_argument("--profile-kind", default="affine", choices=["affine", "nuq", "dquant"],
-                   help="--profile-attn cache: the Llama-shaped affine cache at --bits, the KVQuant NUQ cache, or "
-                        "the D-Quant cache at a reduced batch")
+    p.add_argument("--profile-kind", default="affine", choices=["affine", "nuq", "nuq_gr", "dquant"],
+                   help="--profile-attn cache: the Llama-shaped affine cache at --bits, the KVQuant NUQ cache "
+                        "(plain, or with value groups and key refit blocks), or the D-Quant cache")
     return p.parse_args()
 
 
@@ -1089,6 +1089,7 @@ def cfg_of(w: W.Workload, max_seq: int | None = None):
                        bits=w.bits, rot_k=w.rot_k, rot_v=w.rot_v, mean_k=w.mean_k, clip_k=w.clip, clip_v=w.clip,
                        grid_k=w.grid, n_sink=w.n_sink, n_recent=w.n_recent, scheme=w.scheme,
                        lloyd_iters=e.get("lloyd_iters", 8), outlier_frac=e.get("outlier_frac", 0.01),
+                       group_size_v=e.get("group_size", 0), refit_k=e.get("refit_interval", 0),
                        levels_k=e.get("levels_k", 8), levels_v=e.get("levels_v", 6),
                        container_k=e.get("container_k", 331), container_v=e.get("container_v", 231),
                        rans_alpha=e.get("alpha", 1.4))
@@ -1107,6 +1108,8 @@ def profile_attention(args):
         w = W.LLAMA.with_(bits=args.bits)
     elif args.profile_kind == "nuq":
         w = W.NUQ
+    elif args.profile_kind == "nuq_gr":
+        w = NUQ_GROUP_REFIT
     else:
         w = W.DQUANT.with_(batch=args.profile_batch)
     S = w.seq
