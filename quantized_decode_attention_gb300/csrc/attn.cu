@@ -101,10 +101,9 @@ struct Smem {
     uint64_t full[C::NST];         // slot filled (transaction count of its copies)
     unsigned rel[C::NST];          // releases of a slot so far (4 per entry)
     // non-uniform scheme only (one element otherwise): key tables [unit slot]
-    // [channel][level], fp32 queries, this block's probabilities per warp, and
-    // the value side channel's corrections per warp [warp][head][channel]
+    // [channel][level], this block's probabilities per warp, and the value
+    // side channel's corrections per warp [warp][head][channel]
     uint16_t lutk[NUQ ? 2 : 1][NUQ ? D * C::LV : 1];
-    float qf[NUQ ? 2 : 1][4][NUQ ? D : 1];
     float pb[NUQ ? 4 : 1][4][NUQ ? C::SUB : 1];
     float corr[NUQ ? 4 : 1][4][NUQ ? D : 1];
     alignas(128) uint8_t ring[C::NST][C::SLOT];
@@ -249,7 +248,7 @@ __device__ __forceinline__ float f16v(uint16_t h) { return __half2float(__ushort
 template <int D, int BK, int BV>
 __device__ __forceinline__ void process_block_nuq(const uint8_t *kp, const uint8_t *vp, const uint16_t *lvp, int gv,
                                                   int valid, const uint32_t (&qb)[D / 16][2], const uint16_t *lutk,
-                                                  const float (*qf)[D], float sm_l2, WarpState<D / 16> &st,
+                                                  const uint16_t (*qhl)[4][D + 8], float sm_l2, WarpState<D / 16> &st,
                                                   float (*corr)[D], float (*pb)[32], const AttnArgs &a,
                                                   const AttnShape &sh, int u, long long s0) {
     constexpr int NKS = D / 16, NMT = D / 16, T = 2, LV = 1 << BV, ROWK = D * BK / 8, PAIRV = 2 * D * BV / 8;
@@ -319,7 +318,8 @@ __device__ __forceinline__ void process_block_nuq(const uint8_t *kp, const uint8
                 const uint32_t m = code_in_rec<BK>(kp + r * ROWK, k_idx(c, D), c & 1, D / 16);
                 const float dlt = x - f16v(lutk[c * LV + m]);
 #pragma unroll
-                for (int h = 0; h < 4; h++) atomicAdd(&pb[h][r], qf[h][c] * dlt);
+                for (int h = 0; h < 4; h++)  // q = its fp16 hi + lo halves (about 22 significant bits)
+                    atomicAdd(&pb[h][r], (f16v(qhl[0][h][c]) + f16v(qhl[1][h][c])) * dlt);
             }
         }
         __syncwarp();
@@ -626,7 +626,6 @@ __device__ __forceinline__ void prep_query(const AttnArgs &a, const AttnShape &s
         // packed keys: 2^-E of the code field (affine), or 1 (table values)
         const float sc = NUQ ? 1.f : __int_as_float((127 - field_exp(c >> 3, BK)) << 23);
         put_hilo(S, qs, 1, h, c, xq[j] * sc, false);
-        if constexpr (NUQ) S.qf[qs][h][c] = xq[j];
     }
     qsum = warp_sum(qsum);
     qmu = warp_sum(qmu);
@@ -836,7 +835,7 @@ __global__ void __launch_bounds__(128, Cfg<D, BK, BV, M16, NUQ>::MINB) attn_kern
                                                       : S.lutk[qs];
                     if (valid > 0)
                         process_block_nuq<D, BK, BV>(slot + ok, slot + ov, reinterpret_cast<const uint16_t *>(slot + ol),
-                                                     gv, valid, qb, lutk, S.qf[qs], a.sm_log2, st, S.corr[warp],
+                                                     gv, valid, qb, lutk, S.qh[qs][1], a.sm_log2, st, S.corr[warp],
                                                      S.pb[warp], a, sh, u,
                                                      static_cast<long long>(q) * C::ST + warp * C::SUB);
                     release();
